@@ -1,0 +1,563 @@
+/*
+ * kvq_oracle.c — the CPU oracle of the quantized MLA KV-cache path.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by tests/, by the smoke check and by the benchmark's
+ * CPU-baseline leg; never by the product path.  Plain C, one thread, fp64 wherever the
+ * method leaves the precision open.  Compile with -ffp-contract=off: every fused
+ * multiply-add below is an explicit fmaf() because the method specifies it.
+ *
+ * Parity status per function (what pins it, in tests/test_oracle_*.py):
+ *   orc_e4m3_value / orc_e4m3_rne   exhaustive 256-code table, every midpoint, the
+ *                                    library float8_e4m3fn conversion
+ *   orc_f16_rne / orc_f16_value     numpy float16 conversion on all 65536 patterns and
+ *                                    random doubles
+ *   orc_encode_fp8                  brute-force nearest-code search on random rows
+ *   orc_tq4_codebook                centroid/threshold conditions in closed form
+ *   orc_fwht_*                      Sylvester Hadamard matrix (H·H = nI), scipy.linalg
+ *   orc_encode_tq4 / decode         nearest-centroid brute force, rel-L2 ~ 0.096,
+ *                                    radius invariance, rotated-domain identities
+ *   orc_q4_block / append / gather  all-zero group bits, tie blocks, dequant bound,
+ *                                    brute-force page placement
+ *   orc_mla_decode                  hand-expanded softmax, one-hot and uniform cases,
+ *                                    split invariance, a numpy float128-free re-derivation
+ */
+#include "kvq_oracle.h"
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ===================================================================================
+ * Number formats
+ * =================================================================================== */
+
+/* Round a non-negative double to the nearest integer, ties to the even integer. */
+static double rne_int(double t)
+{
+    double fl = floor(t);
+    double fr = t - fl;
+    if (fr > 0.5) return fl + 1.0;
+    if (fr < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* e4m3 (OCP FP8 E4M3, "fn" variant): 1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities.  Per the KV8 rebase note of colibri PR #399 (HIP
+ * portability item): normals are (1 + M/8) * 2^(E-7), denormals M * 2^-9, and the
+ * pattern S.1111.111 reads back as 0.  The encoder below never produces it. */
+double orc_e4m3_value(uint8_t code)
+{
+    int s = code >> 7, E = (code >> 3) & 15, M = code & 7;
+    double v;
+    if (E == 15 && M == 7)      v = 0.0;
+    else if (E == 0)            v = ldexp((double)M, -9);
+    else                        v = ldexp(1.0 + M / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* Nearest e4m3 code with ties to even mantissa; magnitudes at or above 448 (the
+ * largest finite code) saturate to 448; the sign bit is kept, also for values that
+ * round to zero.  Non-finite input is outside the contract. */
+uint8_t orc_e4m3_rne(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal spacing 2^-9; an integer n of 8 is exactly the smallest normal */
+        double n = rne_int(a * 512.0);
+        return sign | (uint8_t)n;
+    }
+    int e;
+    frexp(a, &e);                       /* a in [2^(e-1), 2^e)                  */
+    int E = (e - 1) + 7;                /* biased exponent field                */
+    double n = rne_int(ldexp(a, 3 - (e - 1)));   /* significand * 8, in [8, 16]  */
+    if (n == 16.0) { n = 8.0; E += 1; }
+    int code = (E << 3) | ((int)n - 8);
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+/* IEEE 754 binary16, round to nearest, ties to even; overflow to infinity. */
+uint16_t orc_f16_rne(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    if (isnan(v)) return sign | 0x7E00;
+    if (isinf(v)) return sign | 0x7C00;
+    double a = fabs(v);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal spacing 2^-24; n = 1024 is exactly the smallest normal */
+        double n = rne_int(ldexp(a, 24));
+        return sign | (uint16_t)n;
+    }
+    int e;
+    frexp(a, &e);
+    int E = (e - 1) + 15;
+    if (E >= 31) return sign | 0x7C00;
+    double n = rne_int(ldexp(a, 10 - (e - 1)));  /* in [1024, 2048] */
+    if (n == 2048.0) { n = 1024.0; E += 1; }
+    if (E >= 31) return sign | 0x7C00;
+    return sign | (uint16_t)(E << 10) | (uint16_t)((int)n - 1024);
+}
+
+double orc_f16_value(uint16_t h)
+{
+    int s = h >> 15, E = (h >> 10) & 31, M = h & 1023;
+    double v;
+    if (E == 31)      v = M ? NAN : INFINITY;
+    else if (E == 0)  v = ldexp((double)M, -24);
+    else              v = ldexp(1.0 + M / 1024.0, E - 15);
+    return s ? -v : v;
+}
+
+/* ===================================================================================
+ * fp8 (KV8) per-row encode — colibri PR #399, Summary ("fp8 e4m3 + per-row scale")
+ * and Commit 1 ("RNE, per-row amax/448 scale", encoder bit-exact with its consumers).
+ * Reading: the scale is amax/448 as an IEEE fp32 division, each element is divided
+ * by it (fp32 IEEE division) and rounded to e4m3 with ties to even; a row with
+ * amax = 0 stores scale 0 and all-zero codes.
+ * =================================================================================== */
+void orc_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
+                    uint8_t* codes, int64_t ldc, float* scales)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * ldx;
+        uint8_t* cr = codes + r * ldc;
+        float amax = 0.0f;
+        for (int i = 0; i < dim; ++i) {
+            float a = fabsf(xr[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 448.0f;
+        scales[r] = s;
+        for (int i = 0; i < dim; ++i)
+            cr[i] = (amax == 0.0f) ? 0x00 : orc_e4m3_rne(xr[i] / s);
+    }
+}
+
+void orc_decode_fp8(const uint8_t* codes, int64_t rows, int dim, int64_t ldc,
+                    const float* scales, double* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < dim; ++i)
+            out[r * dim + i] = orc_e4m3_value(codes[r * ldc + i]) * (double)scales[r];
+}
+
+/* ===================================================================================
+ * Rotated-int4 (TQ4) — colibri PR #399, "Why rotated-int4 for the 4-bit tier":
+ * a randomized-Hadamard rotation, then a fixed 16-level Lloyd-Max codebook that is
+ * optimal for N(0,1) and scaled by radius/sqrt(n); one fp32 radius per row survives
+ * the rotation.  The non-power-of-two refusal follows the rebase note ("KV_TQ now
+ * refuses non-power-of-two latent row widths").
+ * =================================================================================== */
+
+static double std_normal_pdf(double t) { return exp(-0.5 * t * t) / sqrt(2.0 * M_PI); }
+static double std_normal_cdf(double t) { return 0.5 * erfc(-t / sqrt(2.0)); }
+
+/* Lloyd-Max for N(0,1) with 16 levels: alternate "thresholds are midpoints of adjacent
+ * centroids" and "each centroid is the conditional mean of its cell",
+ *   c_k = (phi(t_{k-1}) - phi(t_k)) / (Phi(t_k) - Phi(t_{k-1})),
+ * from a uniform start until no centroid moves by 1e-15.  The stored codebook is each
+ * centroid rounded to the nearest binary16 value; the thresholds are the midpoints of
+ * the stored centroids (exact in fp32). */
+int orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters)
+{
+    double c[16], t[17];
+    for (int k = 0; k < 16; ++k) c[k] = -3.0 + 6.0 * k / 15.0;
+    int it;
+    for (it = 0; it < 1000000; ++it) {
+        t[0] = -INFINITY; t[16] = INFINITY;
+        for (int k = 1; k < 16; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
+        double move = 0.0;
+        for (int k = 0; k < 16; ++k) {
+            double pa = isinf(t[k]) ? 0.0 : std_normal_pdf(t[k]);
+            double pb = isinf(t[k + 1]) ? 0.0 : std_normal_pdf(t[k + 1]);
+            double mass = std_normal_cdf(t[k + 1]) - std_normal_cdf(t[k]);
+            double ck = (pa - pb) / mass;
+            if (fabs(ck - c[k]) > move) move = fabs(ck - c[k]);
+            c[k] = ck;
+        }
+        if (move < 1e-15) break;
+    }
+    for (int k = 0; k < 16; ++k) {
+        lloyd[k] = c[k];
+        cb[k] = (float)orc_f16_value(orc_f16_rne(c[k]));
+    }
+    for (int k = 0; k < 15; ++k) thr[k] = (cb[k] + cb[k + 1]) / 2.0f;
+    if (iters) *iters = it;
+    return 0;
+}
+
+static int is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+/* Unnormalised fast Walsh-Hadamard transform, radix 2, stages h = 1, 2, 4, ... n/2 in
+ * that order; each butterfly maps (a, b) to (a + b, a - b) in fp32. */
+void orc_fwht_f32(float* w, int n)
+{
+    for (int h = 1; h < n; h <<= 1)
+        for (int i = 0; i < n; ++i)
+            if ((i & h) == 0) {
+                float a = w[i], b = w[i + h];
+                w[i] = a + b;
+                w[i + h] = a - b;
+            }
+}
+
+void orc_fwht_f64(double* w, int n)
+{
+    for (int h = 1; h < n; h <<= 1)
+        for (int i = 0; i < n; ++i)
+            if ((i & h) == 0) {
+                double a = w[i], b = w[i + h];
+                w[i] = a + b;
+                w[i + h] = a - b;
+            }
+}
+
+static int sign_is_negative(const uint32_t* bits, int i)
+{
+    return (bits[i >> 5] >> (i & 31)) & 1u;
+}
+
+/* TQ4 encode of one row, step by step:
+ *   1. w = s (.) x with s_i = -1 where bit i of sign_bits is set;
+ *   2. w = FWHT_n(w) (unnormalised, stages ascending), y = w * c, c = fp32(1/sqrt(n));
+ *   3. ss = sum y_i^2 accumulated as 32 partial sums (partial l takes i = l, l+32, ...
+ *      ascending, each step one fmaf), then folded by the butterfly
+ *      p_l <- p_l + p_(l xor o) for o = 16, 8, 4, 2, 1;
+ *   4. radius r = sqrtf(ss) (IEEE), sigma = r * c; a zero radius marks an inert row
+ *      (all-zero bytes);
+ *   5. u_i = y_i / sigma, code_i = number of thresholds t_k with u_i >= t_k;
+ *   6. element 2j goes to the low nibble of byte j, element 2j+1 to the high nibble.
+ * Returns -2 (and writes nothing) for a dimension that is not a power of two. */
+int orc_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
+                   const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                   float* radius)
+{
+    if (!is_pow2(dim) || dim < 64) return -2;
+    double lloyd[16]; float cb[16], thr[15];
+    orc_tq4_codebook(lloyd, cb, thr, NULL);
+    const float c = (float)(1.0 / sqrt((double)dim));
+    float* y = (float*)malloc(sizeof(float) * (size_t)dim);
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * ldx;
+        for (int i = 0; i < dim; ++i)
+            y[i] = sign_is_negative(sign_bits, i) ? -xr[i] : xr[i];
+        orc_fwht_f32(y, dim);
+        for (int i = 0; i < dim; ++i) y[i] = y[i] * c;
+        float part[32];
+        for (int l = 0; l < 32; ++l) {
+            float acc = 0.0f;
+            for (int i = l; i < dim; i += 32) acc = fmaf(y[i], y[i], acc);
+            part[l] = acc;
+        }
+        for (int o = 16; o >= 1; o >>= 1) {
+            float nxt[32];
+            for (int l = 0; l < 32; ++l) nxt[l] = part[l] + part[l ^ o];
+            memcpy(part, nxt, sizeof part);
+        }
+        float rad = sqrtf(part[0]);
+        float sigma = rad * c;
+        uint8_t* pr = packed + r * ldp;
+        radius[r] = rad;
+        if (rad == 0.0f) {
+            memset(pr, 0, (size_t)dim / 2);
+            continue;
+        }
+        for (int j = 0; j < dim / 2; ++j) {
+            int code[2];
+            for (int h = 0; h < 2; ++h) {
+                float u = y[2 * j + h] / sigma;
+                int n = 0;
+                for (int k = 0; k < 15; ++k) n += (u >= thr[k]);
+                code[h] = n;
+            }
+            pr[j] = (uint8_t)(code[0] | (code[1] << 4));
+        }
+    }
+    free(y);
+    return 0;
+}
+
+/* TQ4 dequantisation in fp64: yhat_i = cb[code_i] * r / sqrt(n) (the rotated row) and
+ * xhat = (1/sqrt(n)) * s (.) FWHT_n(yhat) (the row in the original basis). */
+int orc_decode_tq4(const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
+                   const float* radius, const uint32_t* sign_bits,
+                   double* xhat, double* yhat)
+{
+    if (!is_pow2(dim) || dim < 64) return -2;
+    double lloyd[16]; float cb[16], thr[15];
+    orc_tq4_codebook(lloyd, cb, thr, NULL);
+    const double inv_sqrt_n = 1.0 / sqrt((double)dim);
+    double* w = (double*)malloc(sizeof(double) * (size_t)dim);
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t* pr = packed + r * ldp;
+        double sigma = (double)radius[r] * inv_sqrt_n;
+        for (int i = 0; i < dim; ++i) {
+            int code = (i & 1) ? (pr[i >> 1] >> 4) : (pr[i >> 1] & 15);
+            w[i] = (double)cb[code] * sigma;
+        }
+        if (yhat) memcpy(yhat + r * dim, w, sizeof(double) * (size_t)dim);
+        if (xhat) {
+            orc_fwht_f64(w, dim);
+            for (int i = 0; i < dim; ++i) {
+                double v = w[i] * inv_sqrt_n;
+                xhat[r * dim + i] = sign_is_negative(sign_bits, i) ? -v : v;
+            }
+        }
+    }
+    free(w);
+    return 0;
+}
+
+/* ===================================================================================
+ * q4_0 paged cache — Strata PR #2533, kv_q4.metal port commit: fwht256 with the
+ * orthonormal 1/16 scale; q4_group / q4_store with "a tie in |x| resolves to the
+ * larger value"; the fp16 scale rounded to nearest even in software; the codeword
+ * int(fma(x, id, 8.5f)) truncating toward zero.  Fixture commit: an all-zero group
+ * gives d = -0.0 (scale bits 0x8000), id = 0, code 8, every qs byte 0x88.
+ * =================================================================================== */
+
+/* z = FWHT_256(x) * (1/16); stages h = 1 .. 128 ascending, fp32. */
+void orc_fwht256_q4(const float* x, float* z)
+{
+    memcpy(z, x, sizeof(float) * 256);
+    orc_fwht_f32(z, 256);
+    for (int i = 0; i < 256; ++i) z[i] = z[i] * 0.0625f;
+}
+
+/* "a is preferred over b" in the tie rule: larger |.|, then larger value, then +0
+ * over -0. */
+static int q4_prefer(float a, float b)
+{
+    float fa = fabsf(a), fb = fabsf(b);
+    if (fa != fb) return fa > fb;
+    if (a != b) return a > b;
+    return !signbit(a) && signbit(b);
+}
+
+/* One 32-element block -> 18 bytes: fp16 d (little endian) and 16 bytes whose low
+ * nibble holds element j and high nibble element j + 16.
+ *   mval = the element of largest magnitude (tie rule above), d = mval / -8,
+ *   id = 1/d (0 when d is 0), q_j = trunc(fma(z_j, id, 8.5)) clamped to [0, 15]. */
+void orc_q4_block(const float* z, uint8_t out[18])
+{
+    float mval = z[0];
+    for (int j = 1; j < 32; ++j)
+        if (q4_prefer(z[j], mval)) mval = z[j];
+    float d = mval / -8.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    int q[32];
+    for (int j = 0; j < 32; ++j) {
+        float t = truncf(fmaf(z[j], id, 8.5f));
+        int v = (int)t;
+        if (v > 15) v = 15;
+        if (v < 0) v = 0;
+        q[j] = v;
+    }
+    uint16_t hb = orc_f16_rne((double)d);
+    out[0] = (uint8_t)(hb & 0xFF);
+    out[1] = (uint8_t)(hb >> 8);
+    for (int j = 0; j < 16; ++j) out[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+static int64_t q4_cell(const int32_t* page_table, int max_pages, int page_size,
+                       int seq, int pos, int64_t n_cells)
+{
+    int page = pos / page_size;
+    if (page < 0 || page >= max_pages) return -1;
+    int64_t pid = page_table[(int64_t)seq * max_pages + page];
+    int64_t cell = pid * page_size + pos % page_size;
+    if (pid < 0 || cell >= n_cells) return -1;
+    return cell;
+}
+
+/* Append n_tok tokens of K and V ([n_seq][n_tok][n_heads][head_dim] fp32) at positions
+ * pos0[s] .. pos0[s] + n_tok - 1 of each sequence; each (token, head) row is rotated
+ * by fwht256 and stored as 8 blocks (144 bytes) at pool offset
+ * (cell * n_heads + head) * 144, cell = page_table[s][pos / page_size] * page_size
+ * + pos % page_size.  Returns -1 when a position falls outside the table or pool. */
+int orc_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
+                  int n_tok, int n_heads, int head_dim, const int32_t* page_table,
+                  int max_pages, int page_size, int64_t n_cells,
+                  uint8_t* k_pool, uint8_t* v_pool)
+{
+    if (head_dim != 256) return -2;
+    float z[256];
+    for (int s = 0; s < n_seq; ++s)
+        for (int t = 0; t < n_tok; ++t) {
+            int64_t cell = q4_cell(page_table, max_pages, page_size, s, pos0[s] + t, n_cells);
+            if (cell < 0) return -1;
+            for (int kv = 0; kv < 2; ++kv) {
+                const float* src = kv ? v : k;
+                uint8_t* pool = kv ? v_pool : k_pool;
+                for (int h = 0; h < n_heads; ++h) {
+                    const float* row = src + (((int64_t)s * n_tok + t) * n_heads + h) * 256;
+                    orc_fwht256_q4(row, z);
+                    uint8_t* dst = pool + (cell * n_heads + h) * 144;
+                    for (int b = 0; b < 8; ++b) orc_q4_block(z + 32 * b, dst + 18 * b);
+                }
+            }
+        }
+    return 0;
+}
+
+/* Gather back to binary16 in the rotated domain: out = f16_rne((q - 8) * f32(d)),
+ * out laid out [n_seq][n_tok][n_heads][256]. */
+int orc_gather_q4(const uint8_t* pool, int n_seq, const int32_t* pos0, int n_tok,
+                  int n_heads, int head_dim, const int32_t* page_table,
+                  int max_pages, int page_size, int64_t n_cells, uint16_t* out)
+{
+    if (head_dim != 256) return -2;
+    for (int s = 0; s < n_seq; ++s)
+        for (int t = 0; t < n_tok; ++t) {
+            int64_t cell = q4_cell(page_table, max_pages, page_size, s, pos0[s] + t, n_cells);
+            if (cell < 0) return -1;
+            for (int h = 0; h < n_heads; ++h) {
+                const uint8_t* src = pool + (cell * n_heads + h) * 144;
+                uint16_t* dst = out + (((int64_t)s * n_tok + t) * n_heads + h) * 256;
+                for (int b = 0; b < 8; ++b) {
+                    const uint8_t* blk = src + 18 * b;
+                    uint16_t hb = (uint16_t)(blk[0] | (blk[1] << 8));
+                    float d = (float)orc_f16_value(hb);
+                    for (int j = 0; j < 32; ++j) {
+                        int q = (j < 16) ? (blk[2 + j] & 15) : (blk[2 + j - 16] >> 4);
+                        float val = (float)(q - 8) * d;
+                        dst[32 * b + j] = orc_f16_rne((double)val);
+                    }
+                }
+            }
+        }
+    return 0;
+}
+
+/* ===================================================================================
+ * Absorbed-MLA decode attention in fp64 — colibri PR #399: the MLA latent is both key
+ * and value; the decode kernels compute, per query and head,
+ *   s_t = tau * (q_lat . c_t + q_rope . k_rope_t)   over the admissible rows t,
+ *   out = sum_t softmax(s)_t c_t,     lse = log sum_t exp(s_t);
+ * "split-T kernels" merge per-chunk partial softmax states, and the "DSA-aware gather"
+ * restricts the rows to a top-k list of absolute row indices.  Rows are dequantised
+ * exactly (fp8: code value * scale; TQ4: the fp64 inverse rotation of cb[code] *
+ * r / sqrt(n)).  Causal multi-query (draft + verify): query j of a sequence holding L
+ * rows sees rows t <= L - n_q + j.
+ * =================================================================================== */
+
+static int64_t mla_pool_row(const orc_mla* p, int s, int64_t t)
+{
+    if (!p->block_table) return (int64_t)s * p->seq_stride_rows + t;
+    int64_t page = t / p->page_size;
+    if (page >= p->max_pages) return -1;
+    int32_t pid = p->block_table[(int64_t)s * p->max_pages + page];
+    if (pid < 0) return -1;
+    return (int64_t)pid * p->page_size + t % p->page_size;
+}
+
+/* dequantise pool row `row` of the tier `fmt` into c[d_lat] and kr[d_rope] (fp64) */
+static void mla_dequant(const orc_mla* p, int fmt, int64_t row, double* c, double* kr)
+{
+    const int DL = p->d_lat, DR = p->d_rope;
+    if (fmt == ORC_FMT_FP8) {
+        orc_decode_fp8(p->fp8_lat + row * DL, 1, DL, DL, p->fp8_lat_scale + row, c);
+        orc_decode_fp8(p->fp8_rope + row * DR, 1, DR, DR, p->fp8_rope_scale + row, kr);
+    } else {
+        orc_decode_tq4(p->tq4_lat + row * (DL / 2), 1, DL, DL / 2, p->tq4_radius + row,
+                       p->tq4_signs, c, NULL);
+        orc_decode_fp8(p->tq4_rope + row * DR, 1, DR, DR, p->tq4_rope_scale + row, kr);
+    }
+}
+
+int orc_mla_decode(const orc_mla* p, double* out, double* lse, uint32_t* bad_index)
+{
+    const int DL = p->d_lat, DR = p->d_rope, H = p->n_heads, NQ = p->n_q;
+    const int D = DL + DR;
+    int n_sel = p->seq_sel ? p->n_sel : p->n_seq;
+    for (int si = 0; si < n_sel; ++si) {
+        int s = p->seq_sel ? p->seq_sel[si] : si;
+        int L = p->seq_len[s];
+        int fmt = p->seq_fmt[s];
+        for (int qi = 0; qi < NQ; ++qi) {
+            /* the admissible rows of this query, in order */
+            int64_t lim = p->causal ? (int64_t)L - NQ + qi : (int64_t)L - 1;
+            int64_t n_cand = p->idx ? p->top_k : (int64_t)L;
+            int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_cand > 0 ? n_cand : 1));
+            int64_t n_rows = 0;
+            for (int64_t j = 0; j < n_cand; ++j) {
+                int64_t t = p->idx ? p->idx[((int64_t)s * NQ + qi) * p->top_k + j] : j;
+                if (t < 0 || t >= L) { if (bad_index) *bad_index = 1; continue; }
+                if (t > lim) continue;
+                rows[n_rows++] = t;
+            }
+            /* dequantise those rows once */
+            double* kv = (double*)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1) * D);
+            for (int64_t j = 0; j < n_rows; ++j) {
+                int64_t pr = mla_pool_row(p, s, rows[j]);
+                if (pr < 0) { if (bad_index) *bad_index = 1; pr = 0; }
+                mla_dequant(p, fmt, pr, kv + j * D, kv + j * D + DL);
+            }
+            double* sc = (double*)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
+            for (int h = p->head_lo; h < p->head_hi; ++h) {
+                const float* ql = p->q_lat + (((int64_t)s * NQ + qi) * H + h) * DL;
+                const float* qr = p->q_rope + (((int64_t)s * NQ + qi) * H + h) * DR;
+                double* o = out + (((int64_t)s * NQ + qi) * H + h) * DL;
+                double* ls = lse + ((int64_t)s * NQ + qi) * H + h;
+                for (int64_t j = 0; j < n_rows; ++j) {
+                    const double* row = kv + j * D;
+                    double dot = 0.0;
+                    for (int i = 0; i < DL; ++i) dot += (double)ql[i] * row[i];
+                    for (int i = 0; i < DR; ++i) dot += (double)qr[i] * row[DL + i];
+                    sc[j] = (double)p->sm_scale * dot;
+                }
+                for (int i = 0; i < DL; ++i) o[i] = 0.0;
+                if (n_rows == 0) { *ls = -INFINITY; continue; }
+                if (p->n_split <= 0) {
+                    /* direct: max-subtracted softmax over all admissible rows */
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < n_rows; ++j) if (sc[j] > m) m = sc[j];
+                    double l = 0.0;
+                    for (int64_t j = 0; j < n_rows; ++j) {
+                        double e = exp(sc[j] - m);
+                        l += e;
+                        for (int i = 0; i < DL; ++i) o[i] += e * kv[j * D + i];
+                    }
+                    for (int i = 0; i < DL; ++i) o[i] /= l;
+                    *ls = m + log(l);
+                } else {
+                    /* split-T: contiguous chunks of the admissible list, one partial
+                     * (m_S, l_S, o_S) each, merged by the log-sum-exp combine
+                     *   M = max m_S, L = sum l_S e^(m_S - M),
+                     *   out = sum o_S e^(m_S - M) / L, lse = M + log L. */
+                    int ns = p->n_split;
+                    double* pm = (double*)malloc(sizeof(double) * ns);
+                    double* pl = (double*)malloc(sizeof(double) * ns);
+                    double* po = (double*)calloc((size_t)ns * DL, sizeof(double));
+                    for (int S = 0; S < ns; ++S) {
+                        int64_t a = n_rows * S / ns, b = n_rows * (S + 1) / ns;
+                        double m = -INFINITY;
+                        for (int64_t j = a; j < b; ++j) if (sc[j] > m) m = sc[j];
+                        double l = 0.0;
+                        for (int64_t j = a; j < b; ++j) {
+                            double e = exp(sc[j] - m);
+                            l += e;
+                            for (int i = 0; i < DL; ++i) po[S * DL + i] += e * kv[j * D + i];
+                        }
+                        pm[S] = m; pl[S] = l;
+                    }
+                    double M = -INFINITY;
+                    for (int S = 0; S < ns; ++S) if (pm[S] > M) M = pm[S];
+                    double Ltot = 0.0;
+                    for (int S = 0; S < ns; ++S)
+                        if (pl[S] > 0.0) {
+                            double w = exp(pm[S] - M);
+                            Ltot += pl[S] * w;
+                            for (int i = 0; i < DL; ++i) o[i] += po[S * DL + i] * w;
+                        }
+                    for (int i = 0; i < DL; ++i) o[i] /= Ltot;
+                    *ls = M + log(Ltot);
+                    free(pm); free(pl); free(po);
+                }
+            }
+            free(sc); free(kv); free(rows);
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,180 @@
+"""Pins of the oracle's absorbed-MLA decode (colibri PR #399: the latent is both key
+and value; split-T partials merged by a log-sum-exp combine; the DSA-aware gather of
+absolute row indices; the native TQ4 consumer)."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+TAU = float(W.SM_SCALE)
+
+
+def _fp8_cache(orc, rows):
+    lat, ls = orc.encode_fp8(rows.c)
+    rope, rs = orc.encode_fp8(rows.k_rope)
+    return dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
+
+
+def _tq4_cache(orc, rows, signs):
+    lat, rad = orc.encode_tq4(rows.c, signs)
+    rope, rs = orc.encode_fp8(rows.k_rope)
+    return dict(lat=lat, lat_scale=rad, rope=rope, rope_scale=rs)
+
+
+def _dense_rows(orc, cache, fmt, signs=None):
+    """Dequantised rows (c, k_rope) in fp64 through the oracle's pinned decoders."""
+    if fmt == 1:
+        c = orc.decode_fp8(cache["lat"], cache["lat_scale"])
+    else:
+        c, _ = orc.decode_tq4(cache["lat"], cache["lat_scale"], signs, 512)
+    kr = orc.decode_fp8(cache["rope"], cache["rope_scale"])
+    return c, kr
+
+
+def _brute(c, kr, ql, qr, tau, rows):
+    """Hand-expanded softmax: p_t = exp(s_t) / sum exp(s) with s_t computed termwise."""
+    s = np.array([tau * (sum(float(ql[i]) * c[t, i] for i in range(c.shape[1]))
+                         + sum(float(qr[i]) * kr[t, i] for i in range(kr.shape[1])))
+                  for t in rows])
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    out = sum(p[j] * c[t] for j, t in enumerate(rows))
+    return out, s.max() + math.log(np.exp(s - s.max()).sum())
+
+
+@pytest.mark.parametrize("T", [1, 2, 17])
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_brute_force_tiny(orc, T, fmt):
+    rows = W.magnitude_rows(T, seed=T, lo=0.1, hi=3.0)
+    signs = W.sign_bits(T)
+    cache = _fp8_cache(orc, rows) if fmt == 1 else _tq4_cache(orc, rows, signs)
+    q = W.queries(1, 1, 3, seed=T)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    out, lse, bad = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                   sm_scale=TAU, **kw)
+    assert not bad
+    c, kr = _dense_rows(orc, cache, fmt, signs)
+    for h in range(3):
+        ref, ref_lse = _brute(c, kr, q.q_lat[0, 0, h], q.q_rope[0, 0, h], TAU, range(T))
+        assert np.allclose(out[0, 0, h], ref, rtol=0, atol=1e-12 * max(1, np.abs(ref).max()))
+        assert abs(lse[0, 0, h] - ref_lse) < 1e-12 * max(1, abs(ref_lse))
+
+
+def test_one_hot_and_uniform(orc):
+    T = 40
+    rows = W.unit_rows(T, seed=1)
+    cache = _fp8_cache(orc, rows)
+    c, kr = _dense_rows(orc, cache, 1)
+    # one huge score: q aligned with row 13, scaled up -> out == row 13
+    ql = np.zeros((1, 1, 2, 512), np.float32)
+    qr = np.zeros((1, 1, 2, 64), np.float32)
+    ql[0, 0, 0] = (c[13] * 200).astype(np.float32)
+    out, lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=ql, q_rope=qr, sm_scale=TAU,
+                                 fp8=cache)
+    assert np.allclose(out[0, 0, 0], c[13], atol=1e-9)
+    # zero query: equal scores -> the mean of the rows, lse = log T
+    assert np.allclose(out[0, 0, 1], c.mean(0), atol=1e-13)
+    assert abs(lse[0, 0, 1] - math.log(T)) < 1e-13
+
+
+@pytest.mark.parametrize("n_split", [1, 3, 7, 40])
+def test_split_invariance(orc, n_split):
+    T = 300
+    rows = W.fp8_tiny_rows(T, seed=2)
+    cache = _fp8_cache(orc, rows)
+    q = W.queries(1, 1, 4, seed=2)
+    kw = dict(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope, sm_scale=TAU, fp8=cache)
+    d_out, d_lse, _ = orc.mla_decode(**kw)
+    s_out, s_lse, _ = orc.mla_decode(n_split=n_split, **kw)
+    scale = np.abs(d_out).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(s_out - d_out) <= 1e-12 * scale)
+    assert np.allclose(s_lse, d_lse, rtol=0, atol=1e-12)
+
+
+def test_sparse_causal_paged_equivalences(orc):
+    T, NQ, H = 90, 3, 2
+    rows = W.unit_rows(T, seed=5)
+    cache = _fp8_cache(orc, rows)
+    q = W.queries(1, NQ, H, seed=5)
+    base = dict(seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope, sm_scale=TAU)
+    dense, _, _ = orc.mla_decode(seq_len=[T], fp8=cache, **base)
+    # a top-k list holding every row (shuffled) equals dense
+    idx = np.stack([np.random.default_rng(i).permutation(T) for i in range(NQ)])[None].astype(np.int32)
+    sp, _, bad = orc.mla_decode(seq_len=[T], fp8=cache, idx=idx, **base)
+    assert not bad and np.allclose(sp, dense, atol=1e-13)
+    # a strict subset equals dense attention over just those rows
+    sub = np.sort(np.random.default_rng(9).choice(T, 20, replace=False)).astype(np.int32)
+    sub_cache = {k: v[sub] for k, v in cache.items()}
+    sp, _, _ = orc.mla_decode(seq_len=[T], fp8=cache, idx=np.tile(sub, (1, NQ, 1)), **base)
+    ref, _, _ = orc.mla_decode(seq_len=[20], fp8=sub_cache, **base)
+    assert np.allclose(sp, ref, atol=1e-13)
+    # causal: query j sees rows t <= T - NQ + j, i.e. a dense decode over a prefix
+    ca, _, _ = orc.mla_decode(seq_len=[T], fp8=cache, causal=True, **base)
+    for j in range(NQ):
+        n = T - NQ + j + 1
+        pre, _, _ = orc.mla_decode(seq_len=[n], fp8={k: v[:n] for k, v in cache.items()}, **base)
+        assert np.allclose(ca[0, j], pre[0, j], atol=1e-13)
+    # paged under a permuted table equals the contiguous layout
+    ps = 8
+    n_pages = (T + ps - 1) // ps
+    perm = np.random.default_rng(3).permutation(n_pages + 2).astype(np.int32)[:n_pages]
+    pool = {k: np.zeros(((n_pages + 2) * ps,) + v.shape[1:], v.dtype) for k, v in cache.items()}
+    for t in range(T):
+        r = perm[t // ps] * ps + t % ps
+        for k in pool:
+            pool[k][r] = cache[k][t]
+    pg, _, _ = orc.mla_decode(seq_len=[T], fp8=pool, block_table=perm[None], page_size=ps, **base)
+    assert np.allclose(pg, dense, atol=1e-13)
+    # out-of-range indices are flagged and skipped
+    bad_idx = idx.copy()
+    bad_idx[0, 0, 0] = T + 5
+    _, _, bad = orc.mla_decode(seq_len=[T], fp8=cache, idx=bad_idx, **base)
+    assert bad
+
+
+def test_tq4_decode_matches_rotated_domain(orc):
+    """The TQ4 oracle attends over fully dequantised rows; restating it in the rotated
+    domain (rot(q) . yhat for the score, unrot of the weighted sum) gives the same."""
+    import scipy.linalg
+    T = 50
+    rows = W.unit_rows(T, seed=6)
+    signs = W.sign_bits(6)
+    cache = _tq4_cache(orc, rows, signs)
+    q = W.queries(1, 1, 2, seed=6)
+    out, _, _ = orc.mla_decode(seq_len=[T], seq_fmt=[2], q_lat=q.q_lat, q_rope=q.q_rope,
+                               sm_scale=TAU, tq4=cache, signs=signs)
+    _, yhat = orc.decode_tq4(cache["lat"], cache["lat_scale"], signs, 512)
+    kr = orc.decode_fp8(cache["rope"], cache["rope_scale"])
+    Hm = scipy.linalg.hadamard(512) / math.sqrt(512)
+    s = np.array([-1.0 if (signs[i // 32] >> (i % 32)) & 1 else 1.0 for i in range(512)])
+    for h in range(2):
+        rq = Hm @ (s * q.q_lat[0, 0, h])
+        sc = TAU * (yhat @ rq + kr @ q.q_rope[0, 0, h].astype(np.float64))
+        p = np.exp(sc - sc.max())
+        p /= p.sum()
+        ref = s * (Hm @ (p @ yhat))
+        assert np.allclose(out[0, 0, h], ref, atol=1e-12)
+
+
+def test_tolerance_discriminates(orc):
+    """The 1e-4 * max|out| parity bar has power: a wrong softmax scale or a dropped rope
+    term moves the output far beyond it (the page's counterfactual-check method).  On
+    the peaky fp8 workload some heads are dominated by one row whatever tau is, so the
+    check is on the output as a whole; on unit rows every head moves."""
+    for rows, every in ((W.fp8_tiny_rows(1024, seed=0), False), (W.unit_rows(1024, seed=1), True)):
+        cache = _fp8_cache(orc, rows)
+        q = W.queries(1, 1, 16, seed=0)
+        kw = dict(seq_len=[1024], seq_fmt=[1], fp8=cache)
+        ref, _, _ = orc.mla_decode(q_lat=q.q_lat, q_rope=q.q_rope, sm_scale=TAU, **kw)
+        bar = 1e-4 * np.abs(ref).max(axis=-1)
+        wrong_tau, _, _ = orc.mla_decode(q_lat=q.q_lat, q_rope=q.q_rope,
+                                         sm_scale=1 / math.sqrt(576), **kw)
+        no_rope, _, _ = orc.mla_decode(q_lat=q.q_lat, q_rope=np.zeros_like(q.q_rope),
+                                       sm_scale=TAU, **kw)
+        for bad in (wrong_tau, no_rope):
+            err = np.abs(bad - ref).max(axis=-1)
+            assert err.max() > 100 * bar.max()
+            if every:
+                assert np.all(err > 100 * bar)
