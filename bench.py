@@ -1,0 +1,372 @@
+"""Benchmark of the quantized MLA decode step on GB300.
+
+Workload (the 4-bit rotated-int4 tier): a decode step of a 32-layer MLA stack, each
+layer with its own cache of T = 32768 rows (512-wide latent as TQ4 codes + radius,
+64-wide rope key as fp8 + scale, 328 B/row; 343 MB in all, larger than L2), H = 64
+heads, one query.  Per layer and step: quantize-on-append of the new token's row
+(kvq_encode_tq4 + kvq_encode_fp8 into row T-1), then kvq_mla_decode over the T rows
+(query rotation, split-T partials, log-sum-exp combine + unrotation).
+
+metric  KV rows/s = layers x T / step time (higher is better); effective GB/s in the
+        roofline object.
+e2e     the same step through host buffers: new rows and queries copied host->device
+        from pinned memory, outputs copied back, every step.
+--impl reference  times the CPU oracle (test infrastructure) on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV MLA decode attention: KV rows/s (TQ4 tier)"
+UNIT = "rows/s"
+ROW_BYTES_TQ4 = 256 + 4 + 64 + 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--T", type=int, default=32768)
+    ap.add_argument("--H", type=int, default=64)
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------- helpers -----
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profile_traffic(kernel_file: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (its sha256 matches); else None."""
+    path = os.path.join(ROOT, "profiles", "mla_decode_tq4_T32768_H64.txt")
+    src = os.path.join(ROOT, "quantized_kv_cache_fp8_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = dict(l.split("=", 1) for l in text.splitlines() if "=" in l and not l.startswith("#"))
+    if fields.get("source_sha256", "").strip() != digest:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- oracle ----
+
+def oracle_sample(T_sample: int, H: int, seconds_target: float = 15.0):
+    """The oracle on a bounded sample of the workload: the new-row encode plus an fp64
+    decode over T_sample rows for all H heads; repeated until ~seconds_target.
+    Returns (rows/s scaled to the full step's unit, cores used, description)."""
+    import oracle
+    import workloads as W
+    oracle.build()
+    rows = W.unit_rows(T_sample, seed=0)
+    signs = W.sign_bits(0)
+    lat, rad = oracle.encode_tq4(rows.c, signs)
+    rope, rs = oracle.encode_fp8(rows.k_rope)
+    cache = dict(lat=lat, lat_scale=rad, rope=rope, rope_scale=rs)
+    q = W.queries(1, 1, H, seed=0)
+    new = W.unit_rows(1, seed=1)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.encode_tq4(new.c, signs)
+        oracle.encode_fp8(new.k_rope)
+        oracle.mla_decode(seq_len=[T_sample], seq_fmt=[2], q_lat=q.q_lat, q_rope=q.q_rope,
+                          sm_scale=W.SM_SCALE, tq4=cache, signs=signs)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target:
+            break
+    rate = n * T_sample / el
+    desc = (f"oracle (plain C, fp64, 1 thread): {n} x [encode 1 new row + decode over "
+            f"T={T_sample} rows, H={H}] in {el:.1f} s")
+    return rate, 1, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    rate, cores, desc = oracle_sample(4096, args.H, seconds_target=max(5.0, 2.0 * args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"tq4 MLA decode step, T={args.T}, H={args.H}, nq=1 (oracle "
+                               f"sampled at T=4096)"},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- ours ----
+
+def run_ours(args, world, rank, local):
+    import torch
+    import __graft_entry__
+    import quantized_kv_cache_fp8_gb300 as kvq
+    import workloads as W
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Lyr, T, H = args.layers, args.T, args.H
+    stream = torch.cuda.current_stream()
+
+    # ---- a cache of T rows encoded on the GPU, replicated into Lyr distinct layers
+    rows = W.unit_rows(T, seed=0)
+    signs = torch.from_numpy(W.sign_bits(0)).to(dev)
+    c = torch.from_numpy(rows.c).to(dev)
+    kr = torch.from_numpy(rows.k_rope).to(dev)
+    lat = torch.empty(Lyr, T, 256, dtype=torch.uint8, device=dev)
+    rad = torch.empty(Lyr, T, dtype=torch.float32, device=dev)
+    rope = torch.empty(Lyr, T, 64, dtype=torch.uint8, device=dev)
+    rsc = torch.empty(Lyr, T, dtype=torch.float32, device=dev)
+    kvq.kvq_encode_tq4(c, signs, lat[0], rad[0])
+    kvq.kvq_encode_fp8(kr, rope[0], rsc[0])
+    for l in range(1, Lyr):
+        lat[l].copy_(lat[0]); rad[l].copy_(rad[0]); rope[l].copy_(rope[0]); rsc[l].copy_(rsc[0])
+    del c, kr
+    q = W.queries(Lyr, 1, H, seed=0)
+    q_lat = torch.from_numpy(q.q_lat).to(dev)          # [L][1][H][512]
+    q_rope = torch.from_numpy(q.q_rope).to(dev)
+    new = W.unit_rows(Lyr, seed=1)
+    new_c = torch.from_numpy(new.c).to(dev)            # [L][512]
+    new_r = torch.from_numpy(new.k_rope).to(dev)       # [L][64]
+    out = torch.empty(Lyr, 1, 1, H, 512, dtype=torch.float32, device=dev)
+    lse = torch.empty(Lyr, 1, 1, H, dtype=torch.float32, device=dev)
+    seq_len = torch.tensor([T], dtype=torch.int32, device=dev)
+    probs = []
+    for l in range(Lyr):
+        planes = dict(lat=lat[l], lat_scale=rad[l], rope=rope[l], rope_scale=rsc[l])
+        probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat[l:l + 1], q_rope=q_rope[l:l + 1],
+                                      sm_scale=W.SM_SCALE, max_seq_len=T, fmt=kvq.FMT_TQ4,
+                                      tq4=planes, signs=signs))
+    ws = torch.empty(kvq.kvq_mla_decode_workspace(probs[0]), dtype=torch.uint8, device=dev)
+
+    def encode_step():
+        for l in range(Lyr):
+            kvq.kvq_encode_tq4(new_c[l:l + 1], signs, lat[l, T - 1:T], rad[l, T - 1:T])
+            kvq.kvq_encode_fp8(new_r[l:l + 1], rope[l, T - 1:T], rsc[l, T - 1:T])
+
+    def decode_step():
+        for l in range(Lyr):
+            kvq.kvq_mla_decode(probs[l], out[l, 0], lse[l, 0], ws)
+
+    # ---- capture the two halves of the step as CUDA graphs
+    encode_step(); decode_step(); torch.cuda.synchronize()
+    g_enc, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_enc):
+        encode_step()
+    with torch.cuda.graph(g_dec):
+        decode_step()
+    launches_per_step = Lyr * 2 + Lyr * 3          # encodes + (rotate, decode, combine)
+
+    for _ in range(max(3, args.warmup)):
+        g_enc.replay(); g_dec.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for k in range(K):
+            ev[k][0].record()
+            g_enc.replay()
+            ev[k][1].record()
+            g_dec.replay()
+            ev[k][2].record()
+        torch.cuda.synchronize()
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    rows_per_step = Lyr * T
+    value = rows_per_step * world / (ms_per_step / 1e3)
+
+    # ---- roofline of the dominant kernel (the decode call, per launch = one layer)
+    dec_launch_s = statistics.mean(dec_ms) / Lyr / 1e3
+    alg_bytes = T * ROW_BYTES_TQ4 + H * (512 + 64) * 4 + H * 512 * 4 + H * 4
+    peak, peak_kind = peaks()
+    achieved = alg_bytes / dec_launch_s / 1e9
+    traffic = profile_traffic("kvq_decode.cu")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_kind": peak_kind, "kernel": "kvq_mla_decode (TQ4, T=32768, H=64)",
+                "decode_us_per_layer": round(dec_launch_s * 1e6, 2),
+                "flops_per_launch": 2 * H * (512 + 64 + 512) * T}
+
+    # ---- e2e: host buffers in and out every step
+    e2e = None
+    if not args.no_e2e:
+        h_new_c = new_c.cpu().pin_memory()
+        h_new_r = new_r.cpu().pin_memory()
+        h_ql = q_lat.cpu().pin_memory()
+        h_qr = q_rope.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_new_c, h_new_r, h_ql, h_qr))
+        d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+        def e2e_step():
+            new_c.copy_(h_new_c, non_blocking=True)
+            new_r.copy_(h_new_r, non_blocking=True)
+            q_lat.copy_(h_ql, non_blocking=True)
+            q_rope.copy_(h_qr, non_blocking=True)
+            g_enc.replay()
+            g_dec.replay()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / K
+        assert np.isfinite(h_out.numpy()).all()
+        e2e = {"value": rows_per_step * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    if rank != 0:
+        return
+    cpu_rate, cores, desc = oracle_sample(4096, H, seconds_target=12.0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"tq4 MLA decode step: {Lyr} layers x T={T} rows (TQ4 latent + "
+                               f"fp8 rope, 328 B/row), H={H}, nq=1, append 1 row/layer + decode",
+                   "layers": Lyr, "T": T, "H": H, "n_q": 1, "split": "library default",
+                   "l2": f"inputs larger than L2 ({Lyr * T * ROW_BYTES_TQ4 / 1e6:.0f} MB of caches)",
+                   "graph": "CUDA graphs (encode half, decode half)"},
+        "effective_gbs": round(Lyr * T * ROW_BYTES_TQ4 / (ms_per_step / 1e3) / 1e9, 1),
+        "roofline": roofline,
+        "cpu_baseline": {"value": cpu_rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * kvq.h — C ABI of libkvq: a quantized KV cache for an MLA-style latent on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow two pages:
+ *   colibri PR #399 "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant (KV_TQ) on
+ *     CPU, CUDA, and Metal" — the fp8 tier (Summary; Commit 1), the rotated-int4 tier
+ *     ("Why rotated-int4 for the 4-bit tier"), split-T decode and the DSA-aware gather
+ *     (Commit 2), the native TQ4 consumer identities and the non-power-of-two refusal
+ *     (review-thread rebase notes);
+ *   Strata PR #2533 "metal: q4_0 KV cache on the Mac engine" — the q4_0 block codec
+ *     with the FWHT256 rotation, the paged append and the gather (kv_q4.metal port
+ *     commit; parity-fixture commit).
+ *
+ * Conventions for every entry point
+ *   - Pointers to tensors are DEVICE pointers owned by the caller.  libkvq allocates no
+ *     device memory, keeps no per-call state, and writes only the declared outputs,
+ *     the caller's workspace and *dev_status.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream) and
+ *     returns a host-side status.  Argument errors are detected on the host before any
+ *     launch: the call then launches nothing, writes nothing and returns the status;
+ *     kvq_last_error() holds a one-line reason (per calling thread).
+ *   - Data-dependent faults (a row index or page id out of range) never trap: the
+ *     offending row is skipped (or written as zeros where stated) and a bit is OR-ed
+ *     into *dev_status (if non-NULL), which the caller reads after synchronizing.
+ *   - Row-major layouts; leading dimensions are in elements; 16-byte-aligned bases and
+ *     leading dimensions are required where stated (KVQ_EALIGN otherwise).
+ *   - Non-finite inputs are outside the contract of every codec.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvq_stream_t;   /* a cudaStream_t */
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,          /* a size, count or pointer argument is invalid           */
+    KVQ_ENOTPOW2 = 2,        /* a rotated codec was given a non-power-of-two width      */
+    KVQ_EFORMAT = 3,         /* unknown or mismatched format enum                      */
+    KVQ_EALIGN = 4,          /* a base pointer or leading dimension is misaligned      */
+    KVQ_EWORKSPACE = 5,      /* the workspace is NULL or smaller than required         */
+    KVQ_ECUDA = 6,           /* a CUDA launch or attribute call failed                 */
+    KVQ_EFAULT_INJECTED = 7  /* host-side fault injection (kvq_set_fault) fired        */
+} kvq_status;
+
+/* bits of *dev_status */
+enum {
+    KVQ_DEV_BAD_INDEX = 1u,  /* a sparse / gather row index outside [0, rows)          */
+    KVQ_DEV_BAD_PAGE = 2u,   /* a position past the page table, or a page id outside
+                                the pool                                               */
+    KVQ_DEV_TIMEOUT = 4u,    /* a bounded device wait expired                          */
+    KVQ_DEV_BAD_FORMAT = 8u  /* a per-sequence format that is neither FP8 nor TQ4      */
+};
+
+typedef enum kvq_format {
+    KVQ_FMT_FP8 = 1,         /* e4m3 codes + one fp32 scale per row                    */
+    KVQ_FMT_TQ4 = 2,         /* rotated-int4: 4-bit Lloyd-Max codes + one fp32 radius  */
+    KVQ_FMT_Q4_0 = 3         /* FWHT256-rotated 18-byte q4_0 blocks                    */
+} kvq_format;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int kvq_version(void);
+
+/* Static text of a kvq_status value. */
+const char* kvq_status_string(int status);
+
+/* One-line reason for the last non-OK status returned to the calling thread. */
+const char* kvq_last_error(void);
+
+/*
+ * Host-side fault injection for tests of the error paths.  spec = "<entry>:<status>"
+ * makes the named entry point (e.g. "kvq_encode_fp8:6") return that status before any
+ * launch; NULL or "" clears it.  The environment variable KVQ_FAULT, read at the first
+ * call, sets the initial spec.  Returns KVQ_EINVAL for a malformed spec.
+ */
+int kvq_set_fault(const char* spec);
+
+/*
+ * The TQ4 codebook in use: the 16 centroids (the Lloyd-Max fixed point of N(0,1) with
+ * 16 levels, each rounded to the nearest binary16 value, ascending) and the 15
+ * thresholds (midpoints of adjacent centroids).  Host arrays, written by the call.
+ * colibri PR #399, "Why rotated-int4 for the 4-bit tier".
+ */
+int kvq_tq4_codebook(float centroids[16], float thresholds[15]);
+
+/*
+ * fp8 (KV8) per-row encode — colibri PR #399, Summary ("fp8 e4m3 + per-row scale") and
+ * Commit 1 ("RNE, per-row amax/448 scale").  For each row r:
+ *     amax = max_i |x[r][i]|,  scales[r] = amax / 448 (IEEE fp32 division),
+ *     codes[r][i] = e4m3 nearest-even of (x[r][i] / scales[r]), saturating at +-448;
+ * a row with amax = 0 stores scale 0 and all-zero codes.
+ *   x       device fp32 [rows][ldx]   (dim <= ldx)
+ *   codes   device u8   [rows][ldc]   (dim <= ldc)
+ *   scales  device fp32 [rows]
+ * 1 <= dim <= 16384.  The MLA cache encodes the 512-wide latent and the 64-wide rope
+ * key as separate calls (separate scales).  rows = 0 is a no-op.
+ */
+int kvq_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
+                   uint8_t* codes, int64_t ldc, float* scales, kvq_stream_t stream);
+
+/*
+ * Rotated-int4 (TQ4) encode — colibri PR #399, "Why rotated-int4 for the 4-bit tier":
+ * a randomized-Hadamard rotation, then a 16-level N(0,1) Lloyd-Max codebook scaled by
+ * radius/sqrt(n).  For each row, with n = dim and c = fp32(1/sqrt(n)):
+ *   1. w_i = s_i x_i, s_i = -1 where bit i of sign_bits is 1 (bit i%32 of word i/32);
+ *   2. w = FWHT_n(w), radix-2 stages h = 1, 2, ..., n/2 in that order, fp32; y = w * c;
+ *   3. ss = sum y_i^2 as 32 partial sums (partial l: i = l, l+32, ... ascending, one
+ *      fused multiply-add each) folded by p_l += p_(l xor o), o = 16, 8, 4, 2, 1;
+ *   4. radius = sqrt(ss) (IEEE); sigma = radius * c; radius 0 -> all-zero bytes;
+ *   5. code_i = #{k : y_i / sigma >= thresholds[k]} (IEEE division);
+ *   6. packed[r][j] = code_(2j) | code_(2j+1) << 4.
+ *   x        device fp32 [rows][ldx]
+ *   sign_bits device u32 [dim/32]
+ *   packed   device u8   [rows][ldp]  (dim/2 <= ldp)
+ *   radius   device fp32 [rows]
+ * dim must be a power of two (KVQ_ENOTPOW2 otherwise, per the page's refusal of
+ * non-power-of-two widths) in [64, 1024].  The 64-wide rope key of a TQ4 row is
+ * stored with kvq_encode_fp8.
+ */
+int kvq_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
+                   const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                   float* radius, kvq_stream_t stream);
+
+/*
+ * q4_0 paged append — Strata PR #2533, kv_q4.metal port commit (fwht256, q4_group /
+ * q4_store, the tie rule, the fp16 scale) and the page-table commit.  Token t of
+ * sequence s sits at position pos = pos0[s] + t and cell
+ *     page_table[s][pos / page_size] * page_size + pos % page_size;
+ * its row of head h (K and V alike) is rotated, z = FWHT_256(x) / 16 (stages
+ * h = 1..128 ascending, fp32), and stored as 8 blocks of 18 bytes at byte offset
+ * (cell * n_heads + h) * 144 of the pool.  Per 32-element block: mval = the element of
+ * largest |z| (a tie goes to the larger value, +0 over -0), d = mval / -8,
+ * id = (d != 0) ? 1/d : 0, q_j = clamp(trunc(fma(z_j, id, 8.5)), 0, 15); bytes 0-1 =
+ * binary16(d) nearest-even, little endian; byte 2+j = q_j | q_(j+16) << 4.
+ *   k, v       device fp32 [n_seq][n_tok][n_heads][256]
+ *   pos0       device i32  [n_seq]
+ *   page_table device i32  [n_seq][max_pages]
+ *   k_pool, v_pool device u8 [n_cells][n_heads][144]  (16-byte aligned)
+ * head_dim must be 256.  A position past the table or a page id outside the pool sets
+ * KVQ_DEV_BAD_PAGE and that token is skipped.
+ */
+int kvq_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
+                  int n_tok, int n_heads, int head_dim, const int32_t* page_table,
+                  int max_pages, int page_size, int64_t n_cells,
+                  uint8_t* k_pool, uint8_t* v_pool, uint32_t* dev_status,
+                  kvq_stream_t stream);
+
+/* Planes of one MLA cache tier (device pointers, pool-row indexed). */
+typedef struct kvq_mla_cache {
+    const uint8_t* lat;        /* FP8: [n_rows][512] e4m3; TQ4: [n_rows][256] nibbles   */
+    const float*   lat_scale;  /* FP8: [n_rows] scale;    TQ4: [n_rows] radius          */
+    const uint8_t* rope;       /* [n_rows][64] e4m3 codes of the rope key               */
+    const float*   rope_scale; /* [n_rows]                                              */
+    int64_t        n_rows;     /* rows in the pool                                      */
+} kvq_mla_cache;
+
+/*
+ * Gather — two modes selected by `format`.
+ *
+ * KVQ_FMT_Q4_0 (Strata PR #2533, kv_gather_q4 and the qsa decode commit's dequant
+ * "(nibble - 8) * f32_from_f16(d)"): for s < n_seq, t < n_tok, h < n_heads,
+ *     q4_out[s][t][h][32b + j] = binary16_rne((q_j - 8) * float(d_b))
+ * from the pool row of position pos0[s] + t (as in kvq_append_q4), i.e. in the ROTATED
+ * domain.  q4_out: device u16 (binary16 bits) [n_seq][n_tok][n_heads][256].  A bad
+ * position or page sets KVQ_DEV_BAD_PAGE and that token's rows are left untouched.
+ *
+ * KVQ_FMT_FP8 / KVQ_FMT_TQ4 (colibri PR #399, Commit 2, "DSA-aware gather"): copies the
+ * n_idx rows idx[j] of the cache `mla_src` (through page_table / page_size when
+ * page_table is non-NULL, one sequence) byte for byte into the compact cache dst_*
+ * (row j).  An index outside [0, mla_src_rows) sets KVQ_DEV_BAD_INDEX and row j is
+ * written as zeros.
+ */
+typedef struct kvq_gather_desc {
+    int32_t format;
+    /* q4_0 */
+    const uint8_t* q4_pool;
+    int32_t n_seq, n_tok, n_heads, head_dim;
+    const int32_t* pos0;
+    int64_t n_cells;
+    uint16_t* q4_out;
+    /* paging (both modes) */
+    const int32_t* page_table;
+    int32_t max_pages, page_size;
+    /* fp8 / TQ4 rows */
+    kvq_mla_cache mla_src;
+    int64_t mla_src_rows;           /* logical rows addressable by idx                 */
+    const int32_t* idx;             /* device [n_idx]                                  */
+    int64_t n_idx;
+    uint8_t* dst_lat; float* dst_lat_scale; uint8_t* dst_rope; float* dst_rope_scale;
+    uint32_t* dev_status;
+} kvq_gather_desc;
+
+int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
+
+/*
+ * Absorbed-MLA decode attention over a quantized cache — colibri PR #399: the MLA
+ * latent c_t is both key and value; per query and head
+ *     s_t = sm_scale * (q_lat . c_t + q_rope . k_rope_t),  out = sum_t softmax(s)_t c_t,
+ *     lse = log sum_t exp(s_t)
+ * over the admissible rows, computed as split-T partials (m, l, o) merged by a
+ * log-sum-exp combine (Commit 2, "split-T kernels").  Rows are dequantised inside the
+ * kernel: fp8 c_t = code * scale; TQ4 in the rotated domain (the page's identity
+ * q . xhat = rot(q) . yhat; the combine unrotates the output).  Admissible rows of
+ * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
+ * t <= L - n_q + j (draft + verify); with idx, only t in idx[i][j][:] (an index
+ * outside [0, L) sets KVQ_DEV_BAD_INDEX and is skipped).  A query with no admissible
+ * row gets out = 0 and lse = -inf.
+ */
+typedef struct kvq_mla_problem {
+    int32_t n_seq, n_q, n_heads;
+    int32_t d_lat, d_rope;          /* must be 512 and 64                               */
+    int32_t causal;
+    int32_t max_seq_len;            /* host: >= every seq_len[i] (sizes the grid)        */
+    const int32_t* seq_len;         /* device [n_seq]                                   */
+    const int32_t* seq_fmt;         /* device [n_seq] FP8 / TQ4, or NULL: all `fmt`      */
+    int32_t fmt;
+    const int32_t* block_table;     /* device [n_seq][max_pages] pool page ids, or NULL */
+    int32_t max_pages, page_size;
+    int64_t seq_stride_rows;        /* no block table: seq i row t = pool row i*stride+t */
+    kvq_mla_cache fp8, tq4;         /* the pools of each tier (unused tier: zeros)       */
+    const uint32_t* tq4_signs;      /* device [16]: the TQ4 rotation signs              */
+    const float* q_lat;             /* device [n_seq][n_q][n_heads][512]                */
+    const float* q_rope;            /* device [n_seq][n_q][n_heads][64]                 */
+    const int32_t* idx;             /* device [n_seq][n_q][top_k] or NULL               */
+    int32_t top_k;
+    float sm_scale;
+    int32_t split_rows;             /* rows per split (multiple of 64); 0: library's     */
+} kvq_mla_problem;
+
+/* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */
+size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
+
+/*
+ *   out        device fp32 [n_seq][n_q][n_heads][512]
+ *   lse        device fp32 [n_seq][n_q][n_heads] or NULL (natural log)
+ *   workspace  device, >= kvq_mla_decode_workspace(p) bytes, 256-byte aligned
+ *   dev_status device u32 or NULL
+ */
+int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
+                   size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,234 @@
+"""Quantized MLA KV cache on GB300 — Python binding of the C ABI ``libkvq``.
+
+Each function here has the name of the C entry point it wraps and only marshals its
+arguments (torch tensors -> device pointers, the current CUDA stream): every step of
+the path runs in the CUDA kernels of ``libkvq.so``.  There is no fallback: if the
+library is missing or fails to load, importing :func:`lib` raises.
+
+Layouts and semantics are documented once, in ``include/kvq.h``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+__all__ = [
+    "KvqError", "lib", "kvq_version", "kvq_tq4_codebook", "kvq_set_fault",
+    "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
+    "kvq_mla_decode", "kvq_mla_decode_workspace", "MlaCache", "MlaProblem",
+    "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
+    "DEV_BAD_FORMAT",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
+
+FMT_FP8, FMT_TQ4, FMT_Q4_0 = 1, 2, 3
+DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
+STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
+          5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED"}
+
+# every symbol include/kvq.h declares
+EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
+           "kvq_tq4_codebook", "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4",
+           "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode"]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+_p = C.c_void_p
+_i32, _i64, _f32 = C.c_int32, C.c_int64, C.c_float
+
+
+class MlaCache(C.Structure):
+    _fields_ = [("lat", _p), ("lat_scale", _p), ("rope", _p), ("rope_scale", _p),
+                ("n_rows", _i64)]
+
+
+class GatherDesc(C.Structure):
+    _fields_ = [("format", _i32),
+                ("q4_pool", _p), ("n_seq", _i32), ("n_tok", _i32), ("n_heads", _i32),
+                ("head_dim", _i32), ("pos0", _p), ("n_cells", _i64), ("q4_out", _p),
+                ("page_table", _p), ("max_pages", _i32), ("page_size", _i32),
+                ("mla_src", MlaCache), ("mla_src_rows", _i64), ("idx", _p), ("n_idx", _i64),
+                ("dst_lat", _p), ("dst_lat_scale", _p), ("dst_rope", _p),
+                ("dst_rope_scale", _p), ("dev_status", _p)]
+
+
+class MlaProblem(C.Structure):
+    _fields_ = [("n_seq", _i32), ("n_q", _i32), ("n_heads", _i32), ("d_lat", _i32),
+                ("d_rope", _i32), ("causal", _i32), ("max_seq_len", _i32),
+                ("seq_len", _p), ("seq_fmt", _p), ("fmt", _i32), ("block_table", _p),
+                ("max_pages", _i32), ("page_size", _i32), ("seq_stride_rows", _i64),
+                ("fp8", MlaCache), ("tq4", MlaCache), ("tq4_signs", _p),
+                ("q_lat", _p), ("q_rope", _p), ("idx", _p), ("top_k", _i32),
+                ("sm_scale", _f32), ("split_rows", _i32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load libkvq.so (built by ``__graft_entry__.build()``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"libkvq.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = C.CDLL(LIB_PATH)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L):
+    L.kvq_version.restype = C.c_int
+    L.kvq_status_string.restype = C.c_char_p
+    L.kvq_status_string.argtypes = [C.c_int]
+    L.kvq_last_error.restype = C.c_char_p
+    L.kvq_set_fault.restype = C.c_int
+    L.kvq_set_fault.argtypes = [C.c_char_p]
+    L.kvq_tq4_codebook.restype = C.c_int
+    L.kvq_tq4_codebook.argtypes = [_p, _p]
+    L.kvq_encode_fp8.restype = C.c_int
+    L.kvq_encode_fp8.argtypes = [_p, _i64, C.c_int, _i64, _p, _i64, _p, _p]
+    L.kvq_encode_tq4.restype = C.c_int
+    L.kvq_encode_tq4.argtypes = [_p, _i64, C.c_int, _i64, _p, _p, _i64, _p, _p]
+    L.kvq_append_q4.restype = C.c_int
+    L.kvq_append_q4.argtypes = [_p, _p, C.c_int, _p, C.c_int, C.c_int, C.c_int, _p, C.c_int,
+                                C.c_int, _i64, _p, _p, _p, _p]
+    L.kvq_gather.restype = C.c_int
+    L.kvq_gather.argtypes = [C.POINTER(GatherDesc), _p]
+    L.kvq_mla_decode_workspace.restype = C.c_size_t
+    L.kvq_mla_decode_workspace.argtypes = [C.POINTER(MlaProblem)]
+    L.kvq_mla_decode.restype = C.c_int
+    L.kvq_mla_decode.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, C.c_size_t, _p, _p]
+
+
+def _check(status: int):
+    if status != 0:
+        raise KvqError(status, lib().kvq_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+# ---------------------------------------------------------------------------------------
+
+def kvq_version() -> int:
+    return lib().kvq_version()
+
+
+def kvq_set_fault(spec: str | None) -> None:
+    _check(lib().kvq_set_fault(None if spec is None else spec.encode()))
+
+
+def kvq_tq4_codebook():
+    import numpy as np
+    cb = np.empty(16, np.float32)
+    thr = np.empty(15, np.float32)
+    _check(lib().kvq_tq4_codebook(cb.ctypes.data, thr.ctypes.data))
+    return cb, thr
+
+
+def kvq_encode_fp8(x, codes, scales, stream=None) -> None:
+    """x fp32 [rows][>=dim] -> codes u8 [rows][>=dim], scales fp32 [rows]; dim = codes
+    columns used = x.shape[1] unless x is a strided view."""
+    rows, dim = x.shape
+    _check(lib().kvq_encode_fp8(_ptr(x), rows, dim, x.stride(0), _ptr(codes), codes.stride(0),
+                                _ptr(scales), _stream(stream)))
+
+
+def kvq_encode_tq4(x, sign_bits, packed, radius, stream=None) -> None:
+    rows, dim = x.shape
+    _check(lib().kvq_encode_tq4(_ptr(x), rows, dim, x.stride(0), _ptr(sign_bits), _ptr(packed),
+                                packed.stride(0), _ptr(radius), _stream(stream)))
+
+
+def kvq_append_q4(k, v, pos0, page_table, page_size, n_cells, k_pool, v_pool,
+                  dev_status=None, stream=None) -> None:
+    n_seq, n_tok, n_heads, hd = k.shape
+    _check(lib().kvq_append_q4(_ptr(k), _ptr(v), n_seq, _ptr(pos0), n_tok, n_heads, hd,
+                               _ptr(page_table), page_table.shape[1], page_size, n_cells,
+                               _ptr(k_pool), _ptr(v_pool), _ptr(dev_status), _stream(stream)))
+
+
+def kvq_gather_q4(pool, pos0, n_tok, page_table, page_size, n_cells, out, dev_status=None,
+                  stream=None) -> None:
+    """q4_0 mode of kvq_gather: out u16/fp16 [n_seq][n_tok][n_heads][256]."""
+    d = GatherDesc()
+    d.format = FMT_Q4_0
+    d.q4_pool, d.n_seq, d.n_tok = _ptr(pool), pos0.shape[0], n_tok
+    d.n_heads, d.head_dim = out.shape[2], out.shape[3]
+    d.pos0, d.n_cells, d.q4_out = _ptr(pos0), n_cells, _ptr(out)
+    d.page_table, d.max_pages, d.page_size = _ptr(page_table), page_table.shape[-1], page_size
+    d.dev_status = _ptr(dev_status)
+    _check(lib().kvq_gather(C.byref(d), _stream(stream)))
+
+
+def kvq_gather_rows(fmt, src: dict, src_rows, idx, dst: dict, page_table=None, page_size=0,
+                    dev_status=None, stream=None) -> None:
+    """fp8 / TQ4 mode of kvq_gather: copy rows idx of `src` planes into `dst` planes."""
+    d = GatherDesc()
+    d.format = fmt
+    d.mla_src = MlaCache(_ptr(src["lat"]), _ptr(src["lat_scale"]), _ptr(src["rope"]),
+                         _ptr(src["rope_scale"]), src["lat"].shape[0])
+    d.mla_src_rows = src_rows
+    d.idx, d.n_idx = _ptr(idx), idx.numel()
+    if page_table is not None:
+        d.page_table, d.max_pages, d.page_size = _ptr(page_table), page_table.shape[-1], page_size
+    d.dst_lat, d.dst_lat_scale = _ptr(dst["lat"]), _ptr(dst["lat_scale"])
+    d.dst_rope, d.dst_rope_scale = _ptr(dst["rope"]), _ptr(dst["rope_scale"])
+    d.dev_status = _ptr(dev_status)
+    _check(lib().kvq_gather(C.byref(d), _stream(stream)))
+
+
+def _cache(planes):
+    if planes is None:
+        return MlaCache()
+    return MlaCache(_ptr(planes["lat"]), _ptr(planes["lat_scale"]), _ptr(planes["rope"]),
+                    _ptr(planes["rope_scale"]), planes["lat"].shape[0])
+
+
+def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, seq_fmt=None,
+                 causal=False, block_table=None, page_size=0, seq_stride_rows=0, fp8=None,
+                 tq4=None, signs=None, idx=None, split_rows=0) -> MlaProblem:
+    n_seq, n_q, H, DL = q_lat.shape
+    p = MlaProblem()
+    p.n_seq, p.n_q, p.n_heads, p.d_lat, p.d_rope = n_seq, n_q, H, DL, q_rope.shape[-1]
+    p.causal, p.max_seq_len = int(bool(causal)), int(max_seq_len)
+    p.seq_len, p.seq_fmt, p.fmt = _ptr(seq_len), _ptr(seq_fmt), fmt
+    if block_table is not None:
+        p.block_table, p.max_pages, p.page_size = _ptr(block_table), block_table.shape[-1], page_size
+    p.seq_stride_rows = seq_stride_rows
+    p.fp8, p.tq4, p.tq4_signs = _cache(fp8), _cache(tq4), _ptr(signs)
+    p.q_lat, p.q_rope = _ptr(q_lat), _ptr(q_rope)
+    if idx is not None:
+        p.idx, p.top_k = _ptr(idx), idx.shape[-1]
+    p.sm_scale, p.split_rows = float(sm_scale), int(split_rows)
+    return p
+
+
+def kvq_mla_decode_workspace(p: MlaProblem) -> int:
+    return lib().kvq_mla_decode_workspace(C.byref(p))
+
+
+def kvq_mla_decode(p: MlaProblem, out, lse=None, workspace=None, dev_status=None,
+                   stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kvq_mla_decode(C.byref(p), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                _ptr(dev_status), _stream(stream)))

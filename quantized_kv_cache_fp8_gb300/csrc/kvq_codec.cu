@@ -1,0 +1,457 @@
+// kvq_codec.cu — quantize-on-append encoders, the q4_0 paged append and the gathers.
+//
+// Built with --fmad=false: the byte-exact contract of each codec fixes every rounding,
+// so no multiply and add may be fused behind the source's back; each fused
+// multiply-add the methods specify is written as __fmaf_rn, each division as
+// __fdiv_rn (IEEE), each square root as __fsqrt_rn.
+//
+// All kernels are memory-streaming: one warp per row, coalesced loads of the fp32
+// input, shuffles for the Walsh-Hadamard butterflies and the row reductions, and
+// 16-byte stores of the packed output staged through shared memory.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kCodecThreads = 256;
+constexpr int kCodecWarps = kCodecThreads / 32;
+
+inline int grid_for(int64_t work_items, int per_block)
+{
+    int64_t g = (work_items + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)kNumSMs * 16;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+// ------------------------------------------------------------------------------------
+// fp8 (KV8) per-row encode — colibri PR #399, Summary and Commit 1: scale = amax/448,
+// codes = e4m3 nearest-even of x / scale, satfinite.
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    // cvt.rn.satfinite.e4m3x2.f32: nearest-even, saturating to +-448 (element .x -> low byte)
+    uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// LANES lanes per row (1 <= LANES <= 32, power of two), VPL float4 per lane:
+// dim = 4 * VPL * LANES.  Requires 16-byte aligned x rows and 4-byte aligned code rows.
+template <int LANES, int VPL>
+__global__ void __launch_bounds__(kCodecThreads)
+encode_fp8_vec_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                      uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales)
+{
+    constexpr int kRowsPerWarp = 32 / LANES;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LANES;
+    const int l = lane % LANES;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r0 = warp * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
+        const int64_t r = r0 + sub;
+        const bool valid = r < rows;
+        float4 v[VPL];
+        float amax = 0.0f;
+        if (valid) {
+            const float4* xr = reinterpret_cast<const float4*>(x + r * ldx);
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                v[k] = __ldcs(xr + k * LANES + l);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)),
+                                         fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+            }
+        }
+#pragma unroll
+        for (int o = LANES / 2; o >= 1; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        if (!valid) continue;
+        const float s = __fdiv_rn(amax, 448.0f);
+        uint32_t* cr = reinterpret_cast<uint32_t*>(codes + r * ldc);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            uint32_t w = 0;
+            if (amax != 0.0f)
+                w = e4m3x4(__fdiv_rn(v[k].x, s), __fdiv_rn(v[k].y, s),
+                           __fdiv_rn(v[k].z, s), __fdiv_rn(v[k].w, s));
+            cr[k * LANES + l] = w;
+        }
+        if (l == 0) scales[r] = s;
+    }
+}
+
+// Any dim / alignment: one warp per row, two passes over the row.
+__global__ void __launch_bounds__(kCodecThreads)
+encode_fp8_generic_kernel(const float* __restrict__ x, int64_t rows, int dim, int64_t ldx,
+                          uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += n_warps) {
+        const float* xr = x + r * ldx;
+        float amax = 0.0f;
+        for (int i = lane; i < dim; i += 32) amax = fmaxf(amax, fabsf(xr[i]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        const float s = __fdiv_rn(amax, 448.0f);
+        uint8_t* cr = codes + r * ldc;
+        for (int i = lane; i < dim; i += 32) {
+            uint8_t c = 0;
+            if (amax != 0.0f)
+                c = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(xr[i], s), __NV_SATFINITE, __NV_E4M3);
+            cr[i] = c;
+        }
+        if (lane == 0) scales[r] = s;
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Rotated-int4 (TQ4) encode — colibri PR #399, "Why rotated-int4 for the 4-bit tier".
+// ------------------------------------------------------------------------------------
+__constant__ float c_tq4_thr[15] = {
+    kTq4Thresholds[0], kTq4Thresholds[1], kTq4Thresholds[2], kTq4Thresholds[3],
+    kTq4Thresholds[4], kTq4Thresholds[5], kTq4Thresholds[6], kTq4Thresholds[7],
+    kTq4Thresholds[8], kTq4Thresholds[9], kTq4Thresholds[10], kTq4Thresholds[11],
+    kTq4Thresholds[12], kTq4Thresholds[13], kTq4Thresholds[14]};
+
+template <int VPL>   // dim = 32 * VPL
+__global__ void __launch_bounds__(kCodecThreads)
+encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                  const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
+                  int64_t ldp, float* __restrict__ radius, float c, bool vec_store)
+{
+    constexpr int kBytes = 16 * VPL;             // dim / 2
+    __shared__ float s_thr[16];
+    __shared__ __align__(16) uint8_t s_out[kCodecWarps][kBytes];
+    if (threadIdx.x < 15) s_thr[threadIdx.x] = c_tq4_thr[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    uint32_t neg = 0;                            // bit k: element k*32+lane has sign -1
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) neg |= ((__ldg(sign_bits + k) >> lane) & 1u) << k;
+
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += n_warps) {
+        const float* xr = x + r * ldx;
+        float y[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const float v = __ldcs(xr + k * 32 + lane);
+            y[k] = ((neg >> k) & 1u) ? -v : v;
+        }
+        fwht_warp<VPL>(y, lane);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) y[k] = __fmul_rn(y[k], c);
+        // pinned reduction order: per-lane fused accumulation, then the xor butterfly
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) acc = __fmaf_rn(y[k], y[k], acc);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, o));
+        const float rad = __fsqrt_rn(acc);
+        const float sigma = __fmul_rn(rad, c);
+        uint8_t* pr = packed + r * ldp;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            int code = 0;
+            if (rad != 0.0f) {
+                const float u = __fdiv_rn(y[k], sigma);
+                code = (u >= s_thr[7]) ? 8 : 0;           // count of thresholds <= u
+                code += (u >= s_thr[code + 3]) ? 4 : 0;
+                code += (u >= s_thr[code + 1]) ? 2 : 0;
+                code += (u >= s_thr[code]) ? 1 : 0;
+            }
+            const int hi = __shfl_down_sync(kFull, code, 1);
+            if ((lane & 1) == 0) {
+                const uint8_t b = (uint8_t)(code | (hi << 4));
+                if (vec_store) s_out[wib][k * 16 + (lane >> 1)] = b;
+                else pr[k * 16 + (lane >> 1)] = b;
+            }
+        }
+        if (vec_store) {
+            __syncwarp();
+            if (lane < kBytes / 16)
+                reinterpret_cast<uint4*>(pr)[lane] = reinterpret_cast<const uint4*>(s_out[wib])[lane];
+            __syncwarp();
+        }
+        if (lane == 0) radius[r] = rad;
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// q4_0 — Strata PR #2533, kv_q4.metal port commit: fwht256 (one warp a row, 8 values a
+// lane, orthonormal 1/16), q4_group / q4_store with the |x| tie rule, the fp16 scale,
+// int(fma(x, id, 8.5)) truncating toward zero.
+// ------------------------------------------------------------------------------------
+
+// "a is preferred over b": larger |.|, then larger value, then +0 over -0.  A total
+// order, so a butterfly reduction gives the same winner in every lane.
+__device__ __forceinline__ bool q4_prefer(float a, float b)
+{
+    const float fa = fabsf(a), fb = fabsf(b);
+    if (fa != fb) return fa > fb;
+    if (a != b) return a > b;
+    return !signbit(a) && signbit(b);
+}
+
+// cell of (sequence s, position pos), or -1 (and the status bit) when outside
+__device__ __forceinline__ int64_t q4_cell(const int32_t* __restrict__ page_table, int max_pages,
+                                           int page_size, int64_t n_cells, int s, int pos)
+{
+    if (pos < 0) return -1;
+    const int page = pos / page_size;
+    if (page >= max_pages) return -1;
+    const int64_t pid = page_table[(int64_t)s * max_pages + page];
+    const int64_t cell = pid * page_size + pos % page_size;
+    if (pid < 0 || cell >= n_cells) return -1;
+    return cell;
+}
+
+__global__ void __launch_bounds__(kCodecThreads)
+append_q4_kernel(const float* __restrict__ k, const float* __restrict__ v, int n_seq,
+                 const int32_t* __restrict__ pos0, int n_tok, int n_heads,
+                 const int32_t* __restrict__ page_table, int max_pages, int page_size,
+                 int64_t n_cells, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                 uint32_t* __restrict__ dev_status)
+{
+    __shared__ __align__(16) uint8_t s_row[kCodecWarps][144];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t n_rows = (int64_t)n_seq * n_tok * 2 * n_heads;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t id = warp; id < n_rows; id += n_warps) {
+        const int h = (int)(id % n_heads);
+        const int kv = (int)((id / n_heads) & 1);
+        const int64_t st = id / (2 * (int64_t)n_heads);
+        const int t = (int)(st % n_tok);
+        const int s = (int)(st / n_tok);
+        const int64_t cell = q4_cell(page_table, max_pages, page_size, n_cells, s, pos0[s] + t);
+        if (cell < 0) {
+            if (lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
+            continue;
+        }
+        const float* src = (kv ? v : k) + (((int64_t)s * n_tok + t) * n_heads + h) * 256;
+        float z[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[j] = __ldcs(src + j * 32 + lane);
+        fwht_warp<8>(z, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            float mval = z[b];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const float other = __shfl_xor_sync(kFull, mval, o);
+                if (q4_prefer(other, mval)) mval = other;
+            }
+            const float d = __fdiv_rn(mval, -8.0f);
+            const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+            int q = __float2int_rz(__fmaf_rn(z[b], idv, 8.5f));
+            q = min(max(q, 0), 15);
+            const int qhi = __shfl_down_sync(kFull, q, 16);
+            if (lane < 16) s_row[wib][b * 18 + 2 + lane] = (uint8_t)(q | (qhi << 4));
+            if (lane == 0) {
+                const unsigned short hb = __half_as_ushort(__float2half_rn(d));
+                s_row[wib][b * 18] = (uint8_t)(hb & 0xFF);
+                s_row[wib][b * 18 + 1] = (uint8_t)(hb >> 8);
+            }
+        }
+        __syncwarp();
+        uint8_t* dst = (kv ? v_pool : k_pool) + (cell * n_heads + h) * 144;
+        if (lane < 9)
+            reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(s_row[wib])[lane];
+        __syncwarp();
+    }
+}
+
+// gather: rows (s, t, h) -> binary16 [256], (q - 8) * d rounded to nearest even
+__global__ void __launch_bounds__(kCodecThreads)
+gather_q4_kernel(const uint8_t* __restrict__ pool, int n_seq, const int32_t* __restrict__ pos0,
+                 int n_tok, int n_heads, const int32_t* __restrict__ page_table, int max_pages,
+                 int page_size, int64_t n_cells, uint16_t* __restrict__ out,
+                 uint32_t* __restrict__ dev_status)
+{
+    __shared__ __align__(16) uint8_t s_row[kCodecWarps][144];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t n_rows = (int64_t)n_seq * n_tok * n_heads;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t id = warp; id < n_rows; id += n_warps) {
+        const int h = (int)(id % n_heads);
+        const int64_t st = id / n_heads;
+        const int t = (int)(st % n_tok);
+        const int s = (int)(st / n_tok);
+        const int64_t cell = q4_cell(page_table, max_pages, page_size, n_cells, s, pos0[s] + t);
+        if (cell < 0) {
+            if (lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
+            continue;
+        }
+        const uint8_t* src = pool + (cell * n_heads + h) * 144;
+        if (lane < 9)
+            reinterpret_cast<uint4*>(s_row[wib])[lane] = __ldcs(reinterpret_cast<const uint4*>(src) + lane);
+        __syncwarp();
+        const int b = lane >> 2, part = lane & 3;
+        const uint8_t* blk = s_row[wib] + b * 18;
+        const float d = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const int j0 = part * 8 + e, j1 = j0 + 1;
+            const int q0 = (j0 < 16) ? (blk[2 + j0] & 15) : (blk[2 + j0 - 16] >> 4);
+            const int q1 = (j1 < 16) ? (blk[2 + j1] & 15) : (blk[2 + j1 - 16] >> 4);
+            const unsigned short h0 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q0 - 8), d)));
+            const unsigned short h1 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q1 - 8), d)));
+            w[e >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        }
+        uint16_t* dst = out + (((int64_t)s * n_tok + t) * n_heads + h) * 256 + b * 32 + part * 8;
+        __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// MLA row gather (fp8 / TQ4 caches) — colibri PR #399, Commit 2 "DSA-aware gather".
+// One warp per gathered row; byte-for-byte copy of every plane.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCodecThreads)
+gather_mla_kernel(kvq_mla_cache src, int lat_bytes, int64_t src_rows,
+                  const int32_t* __restrict__ page_table, int max_pages, int page_size,
+                  const int32_t* __restrict__ idx, int64_t n_idx,
+                  uint8_t* __restrict__ dst_lat, float* __restrict__ dst_lat_scale,
+                  uint8_t* __restrict__ dst_rope, float* __restrict__ dst_rope_scale,
+                  uint32_t* __restrict__ dev_status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t j = warp; j < n_idx; j += n_warps) {
+        const int64_t t = idx[j];
+        int64_t row = -1;
+        if (t >= 0 && t < src_rows) {
+            if (page_table) {
+                const int64_t page = t / page_size;
+                const int64_t pid = page < max_pages ? page_table[page] : -1;
+                row = (pid < 0) ? -1 : pid * page_size + t % page_size;
+            } else {
+                row = t;
+            }
+            if (row >= src.n_rows) row = -1;
+        }
+        if (row < 0 && lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_INDEX);
+        const int n16 = lat_bytes / 16;
+        for (int i = lane; i < n16; i += 32) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row >= 0) w = reinterpret_cast<const uint4*>(src.lat + row * lat_bytes)[i];
+            reinterpret_cast<uint4*>(dst_lat + j * lat_bytes)[i] = w;
+        }
+        if (lane < 4) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row >= 0) w = reinterpret_cast<const uint4*>(src.rope + row * 64)[lane];
+            reinterpret_cast<uint4*>(dst_rope + j * 64)[lane] = w;
+        }
+        if (lane == 0) {
+            dst_lat_scale[j] = row >= 0 ? src.lat_scale[row] : 0.0f;
+            dst_rope_scale[j] = row >= 0 ? src.rope_scale[row] : 0.0f;
+        }
+    }
+}
+
+}  // namespace
+
+// ====================================================================================
+// launchers
+// ====================================================================================
+
+cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
+                              uint8_t* codes, int64_t ldc, float* scales, cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    const bool x16 = ((uintptr_t)x % 16 == 0) && (ldx % 4 == 0);
+    const bool c4 = ((uintptr_t)codes % 4 == 0) && (ldc % 4 == 0);
+    const int rows_per_block_warp = kCodecWarps;
+#define KVQ_FP8_CASE(D, LANES, VPL)                                                        \
+    if (dim == D && x16 && c4) {                                                           \
+        constexpr int kRpw = 32 / LANES;                                                   \
+        encode_fp8_vec_kernel<LANES, VPL><<<grid_for(rows, rows_per_block_warp * kRpw),   \
+                                            kCodecThreads, 0, s>>>(x, rows, ldx, codes, ldc, scales); \
+        return cudaGetLastError();                                                         \
+    }
+    KVQ_FP8_CASE(64, 16, 1)
+    KVQ_FP8_CASE(128, 32, 1)
+    KVQ_FP8_CASE(256, 32, 2)
+    KVQ_FP8_CASE(512, 32, 4)
+    KVQ_FP8_CASE(576, 16, 9)
+    KVQ_FP8_CASE(1024, 32, 8)
+#undef KVQ_FP8_CASE
+    encode_fp8_generic_kernel<<<grid_for(rows, rows_per_block_warp), kCodecThreads, 0, s>>>(
+        x, rows, dim, ldx, codes, ldc, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
+                              const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                              float* radius, cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    const float c = tq4_inv_sqrt(dim);
+    const bool vec = ((uintptr_t)packed % 16 == 0) && (ldp % 16 == 0);
+    const int g = grid_for(rows, kCodecWarps);
+    switch (dim) {
+        case 64:   encode_tq4_kernel<2><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        case 128:  encode_tq4_kernel<4><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        case 256:  encode_tq4_kernel<8><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        case 512:  encode_tq4_kernel<16><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        case 1024: encode_tq4_kernel<32><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
+                             int n_tok, int n_heads, const int32_t* page_table, int max_pages,
+                             int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,
+                             uint32_t* dev_status, cudaStream_t s)
+{
+    const int64_t n_rows = (int64_t)n_seq * n_tok * 2 * n_heads;
+    if (n_rows == 0) return cudaSuccess;
+    append_q4_kernel<<<grid_for(n_rows, kCodecWarps), kCodecThreads, 0, s>>>(
+        k, v, n_seq, pos0, n_tok, n_heads, page_table, max_pages, page_size, n_cells,
+        k_pool, v_pool, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s)
+{
+    const int64_t n_rows = (int64_t)d.n_seq * d.n_tok * d.n_heads;
+    if (n_rows == 0) return cudaSuccess;
+    gather_q4_kernel<<<grid_for(n_rows, kCodecWarps), kCodecThreads, 0, s>>>(
+        d.q4_pool, d.n_seq, d.pos0, d.n_tok, d.n_heads, d.page_table, d.max_pages,
+        d.page_size, d.n_cells, d.q4_out, d.dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s)
+{
+    if (d.n_idx == 0) return cudaSuccess;
+    const int lat_bytes = d.format == KVQ_FMT_FP8 ? kDLat : kDLat / 2;
+    gather_mla_kernel<<<grid_for(d.n_idx, kCodecWarps), kCodecThreads, 0, s>>>(
+        d.mla_src, lat_bytes, d.mla_src_rows, d.page_table, d.max_pages, d.page_size, d.idx,
+        d.n_idx, d.dst_lat, d.dst_lat_scale, d.dst_rope, d.dst_rope_scale, d.dev_status);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

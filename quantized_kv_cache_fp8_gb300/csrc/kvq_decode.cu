@@ -1,0 +1,421 @@
+// kvq_decode.cu — absorbed-MLA split-T decode over a quantized latent cache, the
+// log-sum-exp combine, and the TQ4 query rotation / output unrotation.
+//
+// colibri PR #399: the MLA latent c_t is both key and value, so per query and head
+//   s_t = tau (q_lat . c_t + q_rope . k_rope_t),  out = sum_t softmax(s)_t c_t;
+// long contexts are "split-T": each CTA reduces a chunk of rows to a partial softmax
+// state (m, l, o) and a combine merges the chunks; the "DSA-aware gather" restricts the
+// rows to a list of absolute indices; the native TQ4 consumer scores against
+// rot(q) and accumulates in the rotated domain, unrotating the output once.
+//
+// This file holds the CUDA-core (SIMT) kernel, the reference-grade path for every
+// shape.  Softmax runs in the log2 domain (scores pre-multiplied by log2 e).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRT = 32;              // rows per tile
+constexpr int kGH = 8;               // heads per CTA
+constexpr int kD = kDLat + kDRope;   // 576
+constexpr int kLDT = kD + 4;         // padded shared row, floats (16-byte multiple)
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned kDevBadFormat = KVQ_DEV_BAD_FORMAT;
+
+__constant__ float c_cb[16] = {
+    kTq4Centroids[0], kTq4Centroids[1], kTq4Centroids[2], kTq4Centroids[3],
+    kTq4Centroids[4], kTq4Centroids[5], kTq4Centroids[6], kTq4Centroids[7],
+    kTq4Centroids[8], kTq4Centroids[9], kTq4Centroids[10], kTq4Centroids[11],
+    kTq4Centroids[12], kTq4Centroids[13], kTq4Centroids[14], kTq4Centroids[15]};
+
+struct DecodeArgs {
+    kvq_mla_problem p;
+    int split_rows, n_splits, n_hblk;
+    float* q_rot;      // [n_seq][n_q][H][512]  (TQ4 sequences)
+    float* part_ml;    // [n_seq][n_q][H][n_splits][2]
+    float* part_o;     // [n_seq][n_q][H][n_splits][512]
+    float* out;
+    float* lse;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ int seq_format(const kvq_mla_problem& p, int s)
+{
+    return p.seq_fmt ? p.seq_fmt[s] : p.fmt;
+}
+
+// pool row of logical row t of sequence s, or -1
+__device__ __forceinline__ int64_t pool_row(const kvq_mla_problem& p, int s, int64_t t)
+{
+    if (!p.block_table) return (int64_t)s * p.seq_stride_rows + t;
+    const int64_t page = t / p.page_size;
+    if (page >= p.max_pages) return -1;
+    const int64_t pid = p.block_table[(int64_t)s * p.max_pages + page];
+    if (pid < 0) return -1;
+    return pid * p.page_size + t % p.page_size;
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte)
+{
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
+// ------------------------------------------------------------------------------------
+// TQ4 query rotation: q_rot = (1/sqrt(512)) FWHT_512(s (.) q_lat), one warp per row.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) rotate_queries_kernel(DecodeArgs a)
+{
+    const kvq_mla_problem& p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    uint32_t neg = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) neg |= ((p.tq4_signs[k] >> lane) & 1u) << k;
+    const float c = tq4_inv_sqrt(kDLat);
+    for (int64_t r = warp; r < n_rows; r += n_warps) {
+        const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));
+        if (seq_format(p, s) != KVQ_FMT_TQ4) continue;
+        const float* src = p.q_lat + r * kDLat;
+        float y[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float v = src[k * 32 + lane];
+            y[k] = ((neg >> k) & 1u) ? -v : v;
+        }
+        fwht_warp<16>(y, lane);
+        float* dst = a.q_rot + r * kDLat;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) dst[k * 32 + lane] = y[k] * c;
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Split-T decode, CUDA cores.  CTA = (split, sequence, query x head block of 8).
+// Per tile of 32 rows: dequantise into shared fp32 (fp8: code * scale; TQ4: the
+// rotated row cb[code] * radius / sqrt(512)); warp g scores head g against the 32 rows
+// (lane = row); online softmax within the warp; every thread then accumulates two
+// output columns for the 8 heads.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
+{
+    extern __shared__ __align__(16) float smem[];
+    float* s_q = smem;                      // [kGH][kLDT]
+    float* s_kv = s_q + kGH * kLDT;         // [kRT][kLDT]
+    float* s_p = s_kv + kRT * kLDT;         // [kRT][kGH]
+    float* s_alpha = s_p + kRT * kGH;       // [kGH]
+    int* s_valid = reinterpret_cast<int*>(s_alpha + kGH);   // [kRT]
+
+    const kvq_mla_problem& p = a.p;
+    const int split = blockIdx.x, s = blockIdx.y;
+    const int q = blockIdx.z / a.n_hblk;
+    const int h0 = (blockIdx.z % a.n_hblk) * kGH;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nh = min(kGH, p.n_heads - h0);
+    const int L = p.seq_len[s];
+    const int fmt = seq_format(p, s);
+    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
+    const int64_t r0 = (int64_t)split * a.split_rows;
+    const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
+    const int64_t lim = p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1;
+    const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;   // + h
+    auto slot = [&](int h) { return (qrow + h) * a.n_splits + split; };
+
+    const bool bad_fmt = (fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4);
+    if (r0 >= n_cand || bad_fmt) {
+        if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, kDevBadFormat);
+        if (tid < nh) {
+            a.part_ml[slot(h0 + tid) * 2] = -INFINITY;
+            a.part_ml[slot(h0 + tid) * 2 + 1] = 0.0f;
+        }
+        return;
+    }
+    const bool tq4 = fmt == KVQ_FMT_TQ4;
+    const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
+
+    for (int i = tid; i < kGH * kD; i += kThreads) {
+        const int g = i / kD, k = i % kD;
+        float v = 0.0f;
+        if (g < nh) {
+            const int64_t r = qrow + h0 + g;
+            if (k < kDLat) v = tq4 ? a.q_rot[r * kDLat + k] : p.q_lat[r * kDLat + k];
+            else v = p.q_rope[r * kDRope + (k - kDLat)];
+        }
+        s_q[g * kLDT + k] = v;
+    }
+
+    float m = -INFINITY, l = 0.0f;          // softmax state of head `warp` (log2 domain)
+    float o[kGH][2];
+#pragma unroll
+    for (int g = 0; g < kGH; ++g) o[g][0] = o[g][1] = 0.0f;
+    const float tau2 = p.sm_scale * kLog2e;
+    const float c512 = tq4_inv_sqrt(kDLat);
+
+    for (int64_t t0 = r0; t0 < r1; t0 += kRT) {
+        __syncthreads();
+        // ---- load + dequantise 32 rows (warp w: rows 4w .. 4w+3)
+        for (int rr = 0; rr < kRT / 8; ++rr) {
+            const int t = warp * (kRT / 8) + rr;
+            const int64_t j = t0 + t;
+            bool ok = false;
+            int64_t row = -1;
+            if (j < r1) {
+                const int64_t tl = p.idx ? (int64_t)p.idx[((int64_t)s * p.n_q + q) * p.top_k + j] : j;
+                if (tl < 0 || tl >= L) {
+                    if (lane == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_INDEX);
+                } else if (tl <= lim) {
+                    row = pool_row(p, s, tl);
+                    if (row < 0 || row >= C.n_rows) {
+                        if (lane == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_PAGE);
+                    } else {
+                        ok = true;
+                    }
+                }
+            }
+            float* dst = s_kv + t * kLDT;
+            if (lane == 0) s_valid[t] = ok ? 1 : 0;
+            if (!ok) {
+                for (int i = lane; i < kD; i += 32) dst[i] = 0.0f;
+                continue;
+            }
+            const float sr = C.rope_scale[row];
+            if (!tq4) {
+                const float sc = C.lat_scale[row];
+                const uint4 w = reinterpret_cast<const uint4*>(C.lat + row * kDLat)[lane];
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    dst[lane * 16 + e] = e4m3_to_float((ww[e >> 2] >> (8 * (e & 3))) & 0xFF) * sc;
+            } else {
+                const float sig = C.lat_scale[row] * c512;
+                const uint2 w = reinterpret_cast<const uint2*>(C.lat + row * (kDLat / 2))[lane];
+                const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const uint32_t byte = (ww[e >> 3] >> (8 * ((e >> 1) & 3))) & 0xFF;
+                    const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15);
+                    dst[lane * 16 + e] = c_cb[code] * sig;
+                }
+            }
+            const unsigned short rw = reinterpret_cast<const unsigned short*>(C.rope + row * kDRope)[lane];
+            dst[kDLat + 2 * lane] = e4m3_to_float(rw & 0xFF) * sr;
+            dst[kDLat + 2 * lane + 1] = e4m3_to_float(rw >> 8) * sr;
+        }
+        __syncthreads();
+        // ---- scores: warp = head g, lane = row t
+        {
+            const int g = warp, t = lane;
+            float sc = -INFINITY;
+            if (g < nh && t0 + t < r1 && s_valid[t]) {
+                const float4* qa = reinterpret_cast<const float4*>(s_q + g * kLDT);
+                const float4* ka = reinterpret_cast<const float4*>(s_kv + t * kLDT);
+                float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll 8
+                for (int k4 = 0; k4 < kD / 4; ++k4) {
+                    const float4 x = qa[k4], y = ka[k4];
+                    acc0 = fmaf(x.x, y.x, acc0);
+                    acc1 = fmaf(x.y, y.y, acc1);
+                    acc0 = fmaf(x.z, y.z, acc0);
+                    acc1 = fmaf(x.w, y.w, acc1);
+                }
+                sc = (acc0 + acc1) * tau2;
+            }
+            float tmax = sc;
+#pragma unroll
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, o2));
+            const float m_new = fmaxf(m, tmax);
+            const float pv = (sc == -INFINITY) ? 0.0f : exp2f(sc - m_new);
+            const float alpha = (m == -INFINITY) ? 0.0f : exp2f(m - m_new);
+            float psum = pv;
+#pragma unroll
+            for (int o2 = 16; o2 >= 1; o2 >>= 1) psum += __shfl_xor_sync(kFull, psum, o2);
+            l = l * alpha + psum;
+            m = m_new;
+            s_p[t * kGH + g] = pv;
+            if (lane == 0) s_alpha[g] = alpha;
+        }
+        __syncthreads();
+        // ---- context: columns tid and tid + 256, all heads
+#pragma unroll
+        for (int g = 0; g < kGH; ++g) {
+            const float al = s_alpha[g];
+            o[g][0] *= al;
+            o[g][1] *= al;
+        }
+        const int nt = (int)min((int64_t)kRT, r1 - t0);
+        for (int t = 0; t < nt; ++t) {
+            const float v0 = s_kv[t * kLDT + tid];
+            const float v1 = s_kv[t * kLDT + tid + 256];
+            const float4 pa = reinterpret_cast<const float4*>(s_p + t * kGH)[0];
+            const float4 pb = reinterpret_cast<const float4*>(s_p + t * kGH)[1];
+            const float pp[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+            for (int g = 0; g < kGH; ++g) {
+                o[g][0] = fmaf(pp[g], v0, o[g][0]);
+                o[g][1] = fmaf(pp[g], v1, o[g][1]);
+            }
+        }
+    }
+    if (lane == 0 && warp < nh) {
+        a.part_ml[slot(h0 + warp) * 2] = m;
+        a.part_ml[slot(h0 + warp) * 2 + 1] = l;
+    }
+    for (int g = 0; g < nh; ++g) {
+        float* dst = a.part_o + slot(h0 + g) * kDLat;
+        dst[tid] = o[g][0];
+        dst[tid + 256] = o[g][1];
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Log-sum-exp combine (+ TQ4 unrotation): one CTA of 128 threads per (seq, query, head).
+//   M = max_S m_S,  L = sum_S l_S 2^(m_S - M),  out = sum_S o_S 2^(m_S - M) / L,
+//   lse = (M + log2 L) ln 2;  TQ4: out <- (1/sqrt 512) s (.) FWHT_512(out).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) mla_combine_kernel(DecodeArgs a)
+{
+    __shared__ float s_o[kDLat];
+    const kvq_mla_problem& p = a.p;
+    const int64_t r = blockIdx.x;                 // (s * n_q + q) * H + h
+    const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));
+    const int tid = threadIdx.x;
+    const int L = p.seq_len[s];
+    const int fmt = seq_format(p, s);
+    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
+    const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
+    const float* ml = a.part_ml + r * a.n_splits * 2;
+    float M = -INFINITY;
+    for (int S = 0; S < ns; ++S)
+        if (ml[2 * S + 1] > 0.0f) M = fmaxf(M, ml[2 * S]);
+    float Lt = 0.0f;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int S = 0; S < ns; ++S) {
+        const float lS = ml[2 * S + 1];
+        if (!(lS > 0.0f)) continue;
+        const float w = exp2f(ml[2 * S] - M);
+        Lt += lS * w;
+        const float4 v = reinterpret_cast<const float4*>(a.part_o + (r * a.n_splits + S) * kDLat)[tid];
+        acc[0] = fmaf(v.x, w, acc[0]);
+        acc[1] = fmaf(v.y, w, acc[1]);
+        acc[2] = fmaf(v.z, w, acc[2]);
+        acc[3] = fmaf(v.w, w, acc[3]);
+    }
+    const bool empty = !(Lt > 0.0f);
+    const float inv = empty ? 0.0f : 1.0f / Lt;
+    float res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) res[e] = acc[e] * inv;
+    if (fmt == KVQ_FMT_TQ4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s_o[tid * 4 + e] = res[e];
+        __syncthreads();
+        for (int h = 1; h < kDLat; h <<= 1) {
+            for (int b = tid; b < kDLat / 2; b += 128) {
+                const int i = (b / h) * 2 * h + (b % h);
+                const float x = s_o[i], y = s_o[i + h];
+                s_o[i] = x + y;
+                s_o[i + h] = x - y;
+            }
+            __syncthreads();
+        }
+        const float c = tq4_inv_sqrt(kDLat);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = tid * 4 + e;
+            const bool ng = (p.tq4_signs[i >> 5] >> (i & 31)) & 1u;
+            res[e] = s_o[i] * c * (ng ? -1.0f : 1.0f);
+        }
+    }
+    reinterpret_cast<float4*>(a.out + r * kDLat)[tid] = make_float4(res[0], res[1], res[2], res[3]);
+    if (tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
+{
+    plan = DecodePlan();
+    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
+    plan.n_cand_max = (int)n_cand;
+    plan.head_block = kGH;
+    const int64_t n_hblk = (p.n_heads + kGH - 1) / kGH;
+    int64_t split_rows = p.split_rows;
+    if (split_rows <= 0) {
+        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * n_hblk);
+        int64_t splits = (2 * kNumSMs + units - 1) / units;
+        const int64_t max_splits = std::max<int64_t>(1, (n_cand + 63) / 64);
+        splits = std::min(std::max<int64_t>(splits, 1), max_splits);
+        split_rows = (n_cand + splits - 1) / splits;
+        split_rows = std::max<int64_t>(kRT, (split_rows + kRT - 1) / kRT * kRT);
+    }
+    plan.split_rows = (int)split_rows;
+    plan.n_splits = (int)std::max<int64_t>(1, (n_cand + split_rows - 1) / split_rows);
+    const size_t rows = (size_t)p.n_seq * p.n_q * p.n_heads;
+    const bool any_tq4 = p.seq_fmt != nullptr || p.fmt == KVQ_FMT_TQ4;
+    size_t off = 0;
+    plan.off_qrot = off;
+    off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
+    plan.off_ml = off;
+    off += align256(rows * plan.n_splits * 2 * sizeof(float));
+    plan.off_o = off;
+    off += align256(rows * plan.n_splits * kDLat * sizeof(float));
+    plan.bytes = off;
+    return true;
+}
+
+cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, float* out,
+                              float* lse, void* ws, uint32_t* dev_status, cudaStream_t s)
+{
+    if (p.n_seq == 0) return cudaSuccess;
+    DecodeArgs a;
+    a.p = p;
+    a.split_rows = plan.split_rows;
+    a.n_splits = plan.n_splits;
+    a.n_hblk = (p.n_heads + kGH - 1) / kGH;
+    char* base = static_cast<char*>(ws);
+    a.q_rot = reinterpret_cast<float*>(base + plan.off_qrot);
+    a.part_ml = reinterpret_cast<float*>(base + plan.off_ml);
+    a.part_o = reinterpret_cast<float*>(base + plan.off_o);
+    a.out = out;
+    a.lse = lse;
+    a.status = dev_status;
+    const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
+    const bool any_tq4 = p.seq_fmt != nullptr || p.fmt == KVQ_FMT_TQ4;
+    if (any_tq4) {
+        int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
+        rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
+    }
+    const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
+                        + kRT * sizeof(int);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> attr_set{0};       // one bit per device
+    const uint64_t bit = 1ull << (device & 63);
+    if (!(attr_set.load() & bit)) {
+        e = cudaFuncSetAttribute(mla_decode_simt_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
+    dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hblk);
+    mla_decode_simt_kernel<<<grid, kThreads, smem, s>>>(a);
+    mla_combine_kernel<<<(unsigned)rows, 128, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

