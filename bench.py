@@ -200,6 +200,7 @@ def run_ours(args, world, rank, local):
     import torch
     import __graft_entry__
     import quantized_kv_cache_fp8_gb300 as kvq
+    from quantized_kv_cache_fp8_gb300.sharding import max_over_ranks
     import workloads as W
 
     __graft_entry__.build()
@@ -277,11 +278,7 @@ def run_ours(args, world, rank, local):
     step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
     dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)
     ms_per_step = total_ms / K
     rows_per_step = Lyr * T
     value = rows_per_step * world / (ms_per_step / 1e3)

@@ -231,7 +231,9 @@ typedef struct kvq_mla_problem {
     const int32_t* idx;             /* device [n_seq][n_q][top_k] or NULL               */
     int32_t top_k;
     float sm_scale;
-    int32_t split_rows;             /* rows per split (multiple of 64); 0: library's     */
+    int32_t split_rows;             /* rows per split; 0: the library chooses            */
+    int32_t impl;                   /* 0: library chooses; 1: CUDA-core kernel;
+                                       2: tensor-core (tcgen05) kernel                   */
 } kvq_mla_problem;
 
 /* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */

@@ -25,6 +25,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 
 FMT_FP8, FMT_TQ4, FMT_Q4_0 = 1, 2, 3
+IMPL_AUTO, IMPL_SIMT, IMPL_TC = 0, 1, 2
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
           5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED"}
@@ -67,7 +68,7 @@ class MlaProblem(C.Structure):
                 ("max_pages", _i32), ("page_size", _i32), ("seq_stride_rows", _i64),
                 ("fp8", MlaCache), ("tq4", MlaCache), ("tq4_signs", _p),
                 ("q_lat", _p), ("q_rope", _p), ("idx", _p), ("top_k", _i32),
-                ("sm_scale", _f32), ("split_rows", _i32)]
+                ("sm_scale", _f32), ("split_rows", _i32), ("impl", _i32)]
 
 
 _lock = threading.Lock()
@@ -206,7 +207,7 @@ def _cache(planes):
 
 def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, seq_fmt=None,
                  causal=False, block_table=None, page_size=0, seq_stride_rows=0, fp8=None,
-                 tq4=None, signs=None, idx=None, split_rows=0) -> MlaProblem:
+                 tq4=None, signs=None, idx=None, split_rows=0, impl=0) -> MlaProblem:
     n_seq, n_q, H, DL = q_lat.shape
     p = MlaProblem()
     p.n_seq, p.n_q, p.n_heads, p.d_lat, p.d_rope = n_seq, n_q, H, DL, q_rope.shape[-1]
@@ -219,7 +220,7 @@ def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, 
     p.q_lat, p.q_rope = _ptr(q_lat), _ptr(q_rope)
     if idx is not None:
         p.idx, p.top_k = _ptr(idx), idx.shape[-1]
-    p.sm_scale, p.split_rows = float(sm_scale), int(split_rows)
+    p.sm_scale, p.split_rows, p.impl = float(sm_scale), int(split_rows), int(impl)
     return p
 
 

@@ -22,6 +22,7 @@ UNITS = {
     "kvq_api.cu": [],
     "kvq_codec.cu": ["--fmad=false"],
     "kvq_decode.cu": [],
+    "kvq_decode_tc.cu": [],
 }
 
 

@@ -351,16 +351,36 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan = DecodePlan();
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
-    plan.head_block = kGH;
-    const int64_t n_hblk = (p.n_heads + kGH - 1) / kGH;
+    // the tensor-core kernel unless the caller asks for CUDA cores; below 8 heads the
+    // 32-head MMA tile would be mostly padding
+    plan.tc = p.impl == 2 || (p.impl == 0 && p.n_heads >= 8);
     int64_t split_rows = p.split_rows;
-    if (split_rows <= 0) {
-        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * n_hblk);
-        int64_t splits = (2 * kNumSMs + units - 1) / units;
-        const int64_t max_splits = std::max<int64_t>(1, (n_cand + 63) / 64);
-        splits = std::min(std::max<int64_t>(splits, 1), max_splits);
-        split_rows = (n_cand + splits - 1) / splits;
-        split_rows = std::max<int64_t>(kRT, (split_rows + kRT - 1) / kRT * kRT);
+    if (plan.tc) {
+        constexpr int kTile = 128, kHeadsTc = 32;
+        plan.head_block = kHeadsTc;
+        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeadsTc - 1) / kHeadsTc));
+        if (split_rows <= 0) {
+            const int64_t tiles = std::max<int64_t>(1, (n_cand + kTile - 1) / kTile);
+            int64_t split_tiles;
+            if (units >= kNumSMs) {
+                split_tiles = std::max<int64_t>(1, (units * tiles + 4 * kNumSMs - 1) / (4 * kNumSMs));
+            } else {
+                const int64_t splits = std::min<int64_t>(tiles, kNumSMs / units);
+                split_tiles = (tiles + splits - 1) / splits;
+            }
+            split_rows = split_tiles * kTile;
+        }
+    } else {
+        plan.head_block = kGH;
+        const int64_t n_hblk = (p.n_heads + kGH - 1) / kGH;
+        if (split_rows <= 0) {
+            const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * n_hblk);
+            int64_t splits = (2 * kNumSMs + units - 1) / units;
+            const int64_t max_splits = std::max<int64_t>(1, (n_cand + 63) / 64);
+            splits = std::min(std::max<int64_t>(splits, 1), max_splits);
+            split_rows = (n_cand + splits - 1) / splits;
+            split_rows = std::max<int64_t>(kRT, (split_rows + kRT - 1) / kRT * kRT);
+        }
     }
     plan.split_rows = (int)split_rows;
     plan.n_splits = (int)std::max<int64_t>(1, (n_cand + split_rows - 1) / split_rows);
@@ -369,6 +389,8 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     size_t off = 0;
     plan.off_qrot = off;
     off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
+    plan.off_qimg = off;
+    off += plan.tc ? tc_q_image_bytes(p) : 0;
     plan.off_ml = off;
     off += align256(rows * plan.n_splits * 2 * sizeof(float));
     plan.off_o = off;
@@ -398,6 +420,13 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     if (any_tq4) {
         int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
+    }
+    if (plan.tc) {
+        cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,
+                                             a.part_o, dev_status, s);
+        if (e != cudaSuccess) return e;
+        mla_combine_kernel<<<(unsigned)rows, 128, 0, s>>>(a);
+        return cudaGetLastError();
     }
     const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
                         + kRT * sizeof(int);

@@ -1,0 +1,633 @@
+// kvq_decode_tc.cu — the tensor-core (tcgen05) split-T absorbed-MLA decode.
+//
+// Same operation as the CUDA-core kernel in kvq_decode.cu (colibri PR #399: score
+// s_t = tau (q_lat . c_t + q_rope . k_rope_t), context sum_t softmax(s)_t c_t, split-T
+// partials), restated as two dense contractions per tile of 128 rows:
+//
+//   S^T[rows x heads] = C_tile[rows x 576] . Q^T        (rows on M = 128, heads on N)
+//   O^T[dims x heads] += V_tile^T[dims x rows] . W^T     (dims on M, 4 M-tiles of 128)
+//
+// The codes are exact in fp16 (every e4m3 value; every TQ4 centroid is a binary16
+// value), and per-row scales are factored out: the latent and rope scores accumulate
+// separately and are scaled per row afterwards; the context weight of row t is
+// w = p_t * scale_t.  The fp32 operands q and w are split into fp16 hi + lo halves
+// that are stacked along N (N = 64 for 32 heads), so each A tile read serves both
+// halves; D accumulates in fp32 in tensor memory.
+//
+// Roles (288 threads): warps 0-3 dequantise code chunks [128 rows x 64] into a ring of
+// swizzled shared-memory slots (thread = row); warps 4-7 run the softmax (thread =
+// row) and the epilogue (thread = output dim); warp 8 allocates tensor memory and one
+// of its threads issues every MMA.  A schedule of 18 ring positions per tile step is
+// shared by producer and MMA issuer: 9 score chunks of tile i, one pad, 8 context
+// chunks of tile i-1 (pairs of context chunks land in adjacent slots).
+//
+// Every wait is bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT, raises a
+// CTA-wide abort flag, drains the MMAs in flight and frees tensor memory.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "kvq_internal.cuh"
+#include "kvq_sm100.cuh"
+
+namespace kvq {
+
+using namespace sm100;
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRT = 128;                 // rows per tile (MMA M)
+constexpr int kGQ = 32;                  // query-heads per CTA
+constexpr int kN = 2 * kGQ;              // MMA N: hi | lo stacked
+constexpr int kRing = 6;                 // dequantised chunk slots
+constexpr int kChunkBytes = kRT * 128;   // [128 rows x 64 fp16], 128B-swizzled
+constexpr int kQSlabBytes = kN * 128;    // [64 rows x 64 fp16]
+constexpr int kQBytes = 9 * kQSlabBytes; // 72 KB
+constexpr int kPBytes = kRT * 128;       // [128 rows x 64 fp16] MN-major
+constexpr int kPeriod = 18;              // ring positions per tile step
+constexpr int kThreads = 288;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.0f;            // rescale only when the max grows by > 2^8
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kOffQ + kQBytes;
+constexpr int kOffP = kOffRing + kRing * kChunkBytes;
+constexpr int kOffRed = kOffP + 2 * kPBytes;                 // [4][32] floats
+constexpr int kOffBar = kOffRed + 4 * 32 * 4;
+// barriers: full[kRing], empty[kRing], s_full[2], s_empty[2], p_full[2], p_empty[2],
+// o_done, drain
+constexpr int kNumBars = 2 * kRing + 10;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;             // + alignment slack
+
+// TMEM columns
+constexpr uint32_t kColS = 0;        // S buffer b: lat at 128b, rope at 128b + 64
+constexpr uint32_t kColO = 256;      // O^T M-tile m at 256 + 64m
+
+__constant__ float c_cb_tc[16] = {
+    kTq4Centroids[0], kTq4Centroids[1], kTq4Centroids[2], kTq4Centroids[3],
+    kTq4Centroids[4], kTq4Centroids[5], kTq4Centroids[6], kTq4Centroids[7],
+    kTq4Centroids[8], kTq4Centroids[9], kTq4Centroids[10], kTq4Centroids[11],
+    kTq4Centroids[12], kTq4Centroids[13], kTq4Centroids[14], kTq4Centroids[15]};
+
+struct TcArgs {
+    kvq_mla_problem p;
+    int split_rows, n_splits, n_hg;      // n_hg: head groups of 32
+    const float* q_rot;                  // [n_seq][n_q][H][512] (TQ4 sequences)
+    uint8_t* q_img;                      // [n_seq][n_q][n_hg][kQBytes]
+    float* part_ml;
+    float* part_o;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ int seq_fmt_of(const kvq_mla_problem& p, int s)
+{
+    return p.seq_fmt ? p.seq_fmt[s] : p.fmt;
+}
+
+__device__ __forceinline__ int64_t pool_row_of(const kvq_mla_problem& p, int s, int64_t t)
+{
+    if (!p.block_table) return (int64_t)s * p.seq_stride_rows + t;
+    const int64_t page = t / p.page_size;
+    if (page >= p.max_pages) return -1;
+    const int64_t pid = p.block_table[(int64_t)s * p.max_pages + page];
+    if (pid < 0) return -1;
+    return pid * p.page_size + t % p.page_size;
+}
+
+// byte offset of 16-byte chunk c (0..7) of row r in a 128B-swizzled [rows x 64] slab
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b)
+{
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// four e4m3 codes (one 32-bit word) -> two half2 words (exact)
+__device__ __forceinline__ void e4m3x4_to_half(uint32_t w, uint32_t& lo, uint32_t& hi)
+{
+    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
+    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+    hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
+}
+
+// ------------------------------------------------------------------------------------
+// Q image: per (seq, query, head group) the 9 swizzled K-major slabs [64 x 64] fp16 the
+// score MMA reads as B: rows 0..31 the hi halves of the group's 32 heads, rows 32..63
+// the lo halves; k < 512 from q_lat (rotated for TQ4), k >= 512 from q_rope.
+// One warp per (row of 64, slab).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
+{
+    const kvq_mla_problem& p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t it = warp; it < n_items; it += n_warps) {
+        const int n = (int)(it % kGQ);                       // head within group
+        const int64_t grp = it / kGQ;                        // (s, q, hg)
+        const int hg = (int)(grp % a.n_hg);
+        const int64_t sq = grp / a.n_hg;                     // s * n_q + q
+        const int s = (int)(sq / p.n_q);
+        const int h = hg * kGQ + n;
+        const bool tq4 = seq_fmt_of(p, s) == KVQ_FMT_TQ4;
+        uint8_t* img = a.q_img + grp * (int64_t)kQBytes;
+        // lane handles k = 2*lane, 2*lane+1 of every 64-wide slab: 18 values
+        for (int slab = 0; slab < 9; ++slab) {
+            float v[2] = {0.0f, 0.0f};
+            if (h < p.n_heads) {
+                const int64_t r = sq * p.n_heads + h;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = slab * 64 + 2 * lane + e;
+                    v[e] = k < kDLat ? (tq4 ? a.q_rot[r * kDLat + k] : p.q_lat[r * kDLat + k])
+                                     : p.q_rope[r * kDRope + (k - kDLat)];
+                }
+            }
+            const __half2 hi = __floats2half2_rn(v[0], v[1]);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(v[0] - hf.x, v[1] - hf.y);
+            // element k = 2*lane (+1) sits in 16B chunk lane/4, word lane%4
+            const int c = lane >> 2, wd = lane & 3;
+            uint8_t* slab_base = img + slab * kQSlabBytes;
+            *reinterpret_cast<__half2*>(slab_base + sw128(n, c) + 4 * wd) = hi;
+            *reinterpret_cast<__half2*>(slab_base + sw128(n + kGQ, c) + 4 * wd) = lo;
+        }
+    }
+}
+
+struct Shared {
+    uint8_t* base;
+    __device__ uint8_t* q() const { return base + kOffQ; }
+    __device__ uint8_t* slot(int i) const { return base + kOffRing + i * kChunkBytes; }
+    __device__ uint8_t* pbuf(int b) const { return base + kOffP + b * kPBytes; }
+    __device__ float* red() const { return reinterpret_cast<float*>(base + kOffRed); }
+    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
+    __device__ uint64_t* full(int i) const { return bar(i); }
+    __device__ uint64_t* empty(int i) const { return bar(kRing + i); }
+    __device__ uint64_t* s_full(int b) const { return bar(2 * kRing + b); }
+    __device__ uint64_t* s_empty(int b) const { return bar(2 * kRing + 2 + b); }
+    __device__ uint64_t* p_full(int b) const { return bar(2 * kRing + 4 + b); }
+    __device__ uint64_t* p_empty(int b) const { return bar(2 * kRing + 6 + b); }
+    __device__ uint64_t* o_done() const { return bar(2 * kRing + 8); }
+    __device__ uint64_t* drain() const { return bar(2 * kRing + 9); }
+    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + kOffMisc); }
+    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kOffMisc + 4); }
+};
+
+// bounded wait that also gives up once another role has aborted
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
+                                         uint32_t* status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*sh.abort_flag()) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *sh.abort_flag() = 1;
+            if (status) atomicOr(status, (unsigned)KVQ_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Row bookkeeping shared by producer and softmax threads: the pool row of candidate j
+// of this CTA's (sequence, query), or -1 when not admissible (flags bad data).
+struct RowCtx {
+    const kvq_mla_problem* p;
+    int s, q, L;
+    int64_t r1, lim;
+    const kvq_mla_cache* C;
+    uint32_t* status;
+    __device__ int64_t row(int64_t j, bool flag) const
+    {
+        if (j >= r1) return -1;
+        const int64_t tl = p->idx ? (int64_t)p->idx[((int64_t)s * p->n_q + q) * p->top_k + j] : j;
+        if (tl < 0 || tl >= L) {
+            if (flag && status) atomicOr(status, (unsigned)KVQ_DEV_BAD_INDEX);
+            return -1;
+        }
+        if (tl > lim) return -1;
+        const int64_t r = pool_row_of(*p, s, tl);
+        if (r < 0 || r >= C->n_rows) {
+            if (flag && status) atomicOr(status, (unsigned)KVQ_DEV_BAD_PAGE);
+            return -1;
+        }
+        return r;
+    }
+};
+
+// dequantise chunk `ch` (0..7 latent, 8 rope) of pool row `row` (or zeros) into row t of
+// a swizzled slot
+__device__ __forceinline__ void dequant_chunk(uint8_t* slot, int t, int64_t row, int ch, bool tq4,
+                                             const kvq_mla_cache& C)
+{
+    uint32_t h[32];
+    if (row < 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) h[i] = 0;
+    } else if (ch == 8 || !tq4) {
+        const uint8_t* src = ch == 8 ? C.rope + row * kDRope : C.lat + row * kDLat + ch * 64;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 w = __ldg(s4 + v);
+            e4m3x4_to_half(w.x, h[8 * v + 0], h[8 * v + 1]);
+            e4m3x4_to_half(w.y, h[8 * v + 2], h[8 * v + 3]);
+            e4m3x4_to_half(w.z, h[8 * v + 4], h[8 * v + 5]);
+            e4m3x4_to_half(w.w, h[8 * v + 6], h[8 * v + 7]);
+        }
+    } else {
+        // 64 nibbles = 32 bytes; element 2j low nibble, 2j+1 high nibble of byte j
+        const uint4* s4 = reinterpret_cast<const uint4*>(C.lat + row * (kDLat / 2) + ch * 32);
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const uint4 w = __ldg(s4 + v);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const uint32_t byte = (ww[b >> 2] >> (8 * (b & 3))) & 0xFF;
+                h[16 * v + b] = pack_half2(c_cb_tc[byte & 15], c_cb_tc[byte >> 4]);
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(slot + sw128(t, c)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
+{
+    extern __shared__ uint8_t dsm[];
+    Shared sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
+    const kvq_mla_problem& p = a.p;
+    const int split = blockIdx.x, s = blockIdx.y;
+    const int q = blockIdx.z / a.n_hg, hg = blockIdx.z % a.n_hg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = hg * kGQ;
+    const int nh = min(kGQ, p.n_heads - h0);
+    const int L = p.seq_len[s];
+    const int fmt = seq_fmt_of(p, s);
+    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
+    const int64_t r0 = (int64_t)split * a.split_rows;
+    const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
+    const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
+    const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
+
+    if (r0 >= n_cand || bad_fmt) {          // nothing to do: an empty partial
+        if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
+        if (tid < nh) {
+            const int64_t sl = (qrow + h0 + tid) * a.n_splits + split;
+            a.part_ml[sl * 2] = -INFINITY;
+            a.part_ml[sl * 2 + 1] = 0.0f;
+        }
+        return;
+    }
+    const bool tq4 = fmt == KVQ_FMT_TQ4;
+    const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
+    const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
+    RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
+
+    // ---- set-up: barriers, tensor memory, the Q image ---------------------------------
+    if (tid == 0) {
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(sh.full(i), 128);
+            mbar_init(sh.empty(i), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sh.s_full(b), 1);
+            mbar_init(sh.s_empty(b), 128);
+            mbar_init(sh.p_full(b), 128);
+            mbar_init(sh.p_empty(b), 1);
+        }
+        mbar_init(sh.o_done(), 1);
+        mbar_init(sh.drain(), 1);
+        *sh.abort_flag() = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(sh.tmem_base(), 512);
+        tmem_relinquish();
+    }
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes);
+        uint4* dst = reinterpret_cast<uint4*>(sh.q());
+        for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sh.tmem_base();
+    const int n_pos = kPeriod * (NT + 1);
+
+    if (warp < 4) {
+        // ================================ producer =======================================
+        const int t = tid;                            // row within the tile
+        int cur_tile = -1;
+        int64_t cur_row = -1;
+        for (int pos = 0; pos < n_pos; ++pos) {
+            const int slot = pos % kRing;
+            const uint32_t par = (uint32_t)(pos / kRing) & 1u;
+            if (!wait_bar(sh, sh.empty(slot), par ^ 1u, a.status)) break;
+            const int i = pos / kPeriod, j = pos % kPeriod;
+            int tile = -1, ch = -1;
+            if (j < 9 && i < NT) { tile = i; ch = j; }
+            else if (j >= 10 && i >= 1) { tile = i - 1; ch = j - 10; }
+            if (tile >= 0) {
+                if (tile != cur_tile) {
+                    cur_tile = tile;
+                    cur_row = rc.row(r0 + (int64_t)tile * kRT + t, false);
+                }
+                dequant_chunk(sh.slot(slot), t, cur_row, ch, tq4, C);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(sh.full(slot));
+        }
+    } else if (warp < 8) {
+        // ================================ softmax ========================================
+        // Control flow is identical in all 128 threads (the named barriers below need
+        // every one of them); `ok` only guards work and is kept warp-uniform for the
+        // .sync.aligned tensor-memory instructions.
+        const int t = tid - 128;                      // row within the tile
+        const int wq = warp - 4;                      // TMEM lane quarter
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const float tau2 = p.sm_scale * kLog2e;
+        const float c512 = tq4_inv_sqrt(kDLat);
+        float* red = sh.red();
+        float m_run[kGQ], l_part[kGQ];
+#pragma unroll
+        for (int g = 0; g < kGQ; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.0f; }
+        bool ok = true;
+        for (int i = 0; i < NT; ++i) {
+            const int b = i & 1;
+            const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
+            float sc_lat = 0.0f, sc_rope = 0.0f;
+            if (row >= 0) {
+                sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
+                sc_rope = C.rope_scale[row];
+            }
+            if (ok) ok = wait_bar(sh, sh.s_full(b), (uint32_t)(i >> 1) & 1u, a.status);
+            ok = __all_sync(kFull, ok);
+            float sv[kGQ];
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) sv[g] = 0.0f;
+            if (ok) {
+                tc_fence_after();
+                uint32_t x[16], y[16];
+#pragma unroll
+                for (int c = 0; c < kN; c += 16) {
+                    tmem_ld_x16(tmem + lane_base + kColS + 128 * b + c, x);
+                    tmem_ld_x16(tmem + lane_base + kColS + 128 * b + 64 + c, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        sv[(c + e) & (kGQ - 1)] += fmaf(sc_lat, __uint_as_float(x[e]),
+                                                        sc_rope * __uint_as_float(y[e]));
+                }
+                tc_fence_before();
+                mbar_arrive(sh.s_empty(b));
+            }
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) sv[g] = (row >= 0 && ok) ? sv[g] * tau2 : -INFINITY;
+            // per-head max over the 128 rows of the tile
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) {
+                float v = sv[g];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+                if (lane == 0) red[wq * 32 + g] = v;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            bool need_rescale = false;
+            float alpha[kGQ];
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) {
+                const float tm = fmaxf(fmaxf(red[g], red[32 + g]), fmaxf(red[64 + g], red[96 + g]));
+                alpha[g] = 1.0f;
+                if (tm > m_run[g] + kLazy || (m_run[g] == -INFINITY && tm > -INFINITY)) {
+                    alpha[g] = (m_run[g] == -INFINITY) ? 0.0f : exp2f(m_run[g] - tm);
+                    m_run[g] = tm;
+                    if (i > 0) need_rescale = true;
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");    // red[] is rewritten next tile
+            if (need_rescale && ok) {
+                // the context MMAs of tile i-1 must be complete before O is touched
+                ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+                ok = __all_sync(kFull, ok);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                        for (int c = 0; c < kN; c += 16) {
+                            uint32_t x[16];
+                            tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha[(c + e) & (kGQ - 1)]);
+                            tmem_st_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) l_part[g] *= alpha[g];
+            // weights: p = 2^(s - m), w = p * latent scale, split hi | lo
+            uint32_t wh[kGQ / 2], wl[kGQ / 2];
+#pragma unroll
+            for (int g = 0; g < kGQ; g += 2) {
+                const float p0 = sv[g] == -INFINITY ? 0.0f : exp2f(sv[g] - m_run[g]);
+                const float p1 = sv[g + 1] == -INFINITY ? 0.0f : exp2f(sv[g + 1] - m_run[g + 1]);
+                l_part[g] += p0;
+                l_part[g + 1] += p1;
+                const float w0 = p0 * sc_lat, w1 = p1 * sc_lat;
+                const __half2 hi = __floats2half2_rn(w0, w1);
+                const float2 hf = __half22float2(hi);
+                const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
+                wh[g / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                wl[g / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+            if (ok && i >= 2) ok = wait_bar(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
+            if (ok) {
+                uint8_t* pb = sh.pbuf(b);
+                // row t of W^T: 64 fp16, chunks 0..3 the hi halves, 4..7 the lo halves
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    *reinterpret_cast<uint4*>(pb + sw128(t, c)) =
+                        make_uint4(wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]);
+                    *reinterpret_cast<uint4*>(pb + sw128(t, c + 4)) =
+                        make_uint4(wl[4 * c], wl[4 * c + 1], wl[4 * c + 2], wl[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(sh.p_full(b));
+            }
+        }
+        // ---- epilogue: l over the 128 rows, O^T -> partials ------------------------------
+        if (ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
+        ok = __all_sync(kFull, ok);
+#pragma unroll
+        for (int g = 0; g < kGQ; ++g) {
+            float v = l_part[g];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+            if (lane == 0) red[wq * 32 + g] = v;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ok) {
+            tc_fence_after();
+            if (t < nh) {
+                const float lt = red[t] + red[32 + t] + red[64 + t] + red[96 + t];
+                const int64_t sl = (qrow + h0 + t) * a.n_splits + split;
+                float mt = m_run[0];
+#pragma unroll
+                for (int g = 1; g < kGQ; ++g) if (g == t) mt = m_run[g];
+                a.part_ml[sl * 2] = mt;
+                a.part_ml[sl * 2 + 1] = lt;
+            }
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+                const int d = 128 * m + 32 * wq + lane;
+                uint32_t x[16], y[16];
+#pragma unroll
+                for (int c = 0; c < kGQ; c += 16) {
+                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + kGQ + c, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int g = c + e;
+                        if (g < nh)
+                            a.part_o[((qrow + h0 + g) * a.n_splits + split) * kDLat + d] =
+                                __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================================ MMA issuer =====================================
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
+            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
+            const uint32_t q_base = smem_u32(sh.q());
+            bool ok = true;
+            for (int pos = 0; pos < n_pos && ok; ++pos) {
+                const int slot = pos % kRing;
+                const uint32_t par = (uint32_t)(pos / kRing) & 1u;
+                const int i = pos / kPeriod, j = pos % kPeriod;
+                if (!(ok = wait_bar(sh, sh.full(slot), par, a.status))) break;
+                tc_fence_after();
+                if (j < 9 && i < NT) {
+                    const int b = i & 1;
+                    if (j == 0 && i >= 2 && !(ok = wait_bar(sh, sh.s_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status))) break;
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sh.slot(slot));
+                    const uint32_t d = tmem + kColS + 128 * b + (j == 8 ? 64 : 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ss(d, desc_sw128(a_base + 32 * ks, 1024),
+                                   desc_sw128(q_base + j * kQSlabBytes + 32 * ks, 1024), idesc_s,
+                                   (j == 0 || j == 8) ? (ks > 0) : 1u);
+                    mma_commit(sh.empty(slot));
+                    if (j == 8) mma_commit(sh.s_full(b));
+                } else if (j >= 10 && i >= 1) {
+                    const int tile = i - 1, b = tile & 1, c = j - 10;
+                    if (c == 0 && !(ok = wait_bar(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
+                    tc_fence_after();
+                    if (c & 1) {
+                        // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
+                        const int m = c >> 1;
+                        const uint32_t a_base = smem_u32(sh.slot(slot - 1));
+                        const uint32_t p_base = smem_u32(sh.pbuf(b));
+#pragma unroll
+                        for (int ks = 0; ks < kRT / 16; ++ks) {
+                            // LBO: the slot holding the next 64 dims
+                            const uint64_t ad = desc_sw128_lbo(a_base + 2048 * ks, kChunkBytes, 1024);
+                            mma_f16_ss(tmem + kColO + 64 * m, ad, desc_sw128(p_base + 2048 * ks, 1024),
+                                       idesc_c, (tile == 0 && ks == 0) ? 0u : 1u);
+                        }
+                        mma_commit(sh.empty(slot - 1));
+                        mma_commit(sh.empty(slot));
+                        if (c == 7) {
+                            mma_commit(sh.p_empty(b));
+                            mma_commit(sh.o_done());
+                        }
+                    }
+                } else {
+                    mbar_arrive(sh.empty(slot));          // a pad position
+                }
+            }
+            // drain: every MMA issued so far completes before tensor memory is freed
+            mma_commit(sh.drain());
+            if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
+                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    }
+
+    // ---- tear-down -------------------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t tc_q_image_bytes(const kvq_mla_problem& p)
+{
+    const size_t n_hg = (size_t)(p.n_heads + kGQ - 1) / kGQ;
+    return align256((size_t)p.n_seq * p.n_q * n_hg * kQBytes);
+}
+
+cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
+                                 const float* q_rot, void* q_img, float* part_ml, float* part_o,
+                                 uint32_t* dev_status, cudaStream_t s)
+{
+    TcArgs a;
+    a.p = p;
+    a.split_rows = plan.split_rows;
+    a.n_splits = plan.n_splits;
+    a.n_hg = (p.n_heads + kGQ - 1) / kGQ;
+    a.q_rot = q_rot;
+    a.q_img = static_cast<uint8_t*>(q_img);
+    a.part_ml = part_ml;
+    a.part_o = part_o;
+    a.status = dev_status;
+    const int64_t items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
+    q_image_kernel<<<(int)std::min<int64_t>((items + 7) / 8, kNumSMs * 8), 256, 0, s>>>(a);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> attr_set{0};
+    const uint64_t bit = 1ull << (device & 63);
+    if (!(attr_set.load() & bit)) {
+        e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
+    dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
+    mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

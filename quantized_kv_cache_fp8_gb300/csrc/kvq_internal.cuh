@@ -87,14 +87,19 @@ cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
 
 struct DecodePlan {
+    bool tc = false;        // tensor-core kernel
     int split_rows = 0;     // candidate rows per split
     int n_splits = 0;       // splits per (seq, query) at most
     int n_cand_max = 0;     // candidate rows of the longest (seq, query)
-    int head_block = 0;     // heads per CTA (SIMT kernel)
-    size_t off_qrot = 0, off_ml = 0, off_o = 0, bytes = 0;
+    int head_block = 0;     // heads per CTA
+    size_t off_qrot = 0, off_qimg = 0, off_ml = 0, off_o = 0, bytes = 0;
 };
 bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan);
 cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, float* out,
                               float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
+size_t tc_q_image_bytes(const kvq_mla_problem& p);
+cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
+                                 const float* q_rot, void* q_img, float* part_ml, float* part_o,
+                                 uint32_t* dev_status, cudaStream_t s);
 
 }  // namespace kvq

@@ -12,6 +12,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
+IMPLS = pytest.mark.parametrize("impl", [1, 2], ids=["cudacore", "tcgen05"])
 
 
 @pytest.fixture(scope="module")
@@ -37,7 +38,7 @@ def encode(orc, rows, fmt, signs=None):
 
 def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=None,
             seq_fmt=None, idx=None, causal=False, block_table=None, page_size=0,
-            seq_stride_rows=0, split_rows=0, max_seq_len=None):
+            seq_stride_rows=0, split_rows=0, max_seq_len=None, impl=0):
     dcaches = {f: {k: dev(v) for k, v in c.items()} for f, c in caches.items()}
     n_seq, n_q, H, _ = q.q_lat.shape
     p = kvq.make_problem(
@@ -47,7 +48,7 @@ def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=No
         causal=causal, block_table=None if block_table is None else dev(block_table),
         page_size=page_size, seq_stride_rows=seq_stride_rows, fp8=dcaches.get(1),
         tq4=dcaches.get(2), signs=None if signs is None else dev(signs),
-        idx=None if idx is None else dev(idx), split_rows=split_rows)
+        idx=None if idx is None else dev(idx), split_rows=split_rows, impl=impl)
     keep = (dcaches, p)
     ws = torch.empty(max(1, kvq.kvq_mla_decode_workspace(p)), dtype=torch.uint8, device="cuda")
     out = torch.full((n_seq, n_q, H, 512), np.nan, dtype=torch.float32, device="cuda")
@@ -75,12 +76,13 @@ def check(out, lse, ref, ref_lse, sel=None):
 
 @pytest.mark.parametrize("fmt", [1, 2])
 @pytest.mark.parametrize("T,split", [(1, 0), (17, 0), (63, 32), (65, 32), (1024, 0), (1000, 96)])
-def test_decode_tiny_shapes(kvq, orc, fmt, T, split):
+@IMPLS
+def test_decode_tiny_shapes(kvq, orc, impl, fmt, T, split):
     rows = W.fp8_tiny_rows(T, seed=T) if fmt == 1 else W.unit_rows(T, seed=T)
     signs = W.sign_bits(T)
     cache = encode(orc, rows, fmt, signs)
     q = W.queries(1, 1, 16, seed=T)
-    out, lse, st = run_gpu(kvq, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
                            signs=signs, split_rows=split)
     kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
@@ -89,31 +91,34 @@ def test_decode_tiny_shapes(kvq, orc, fmt, T, split):
     check(out, lse, ref, ref_lse)
 
 
-def test_decode_fp8_tiny_workload(kvq, orc):
+@IMPLS
+def test_decode_fp8_tiny_workload(kvq, orc, impl):
     """T=1024 fp8 rows with magnitudes log-uniform in [1e-3, 40] and zero rows, H=16."""
     rows = W.fp8_tiny_rows(1024, seed=0)
     cache = encode(orc, rows, 1)
     q = W.queries(1, 1, 16, seed=0)
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[1024], q=q)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[1024], q=q)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[1024], seq_fmt=[1], q_lat=q.q_lat,
                                      q_rope=q.q_rope, sm_scale=W.SM_SCALE, fp8=cache)
     check(out, lse, ref, ref_lse)
 
 
-def test_decode_tq4_workload(kvq, orc):
+@IMPLS
+def test_decode_tq4_workload(kvq, orc, impl):
     """T=32768 N(0,1) rows of the 4-bit tier, H=64 (every head)."""
     T = 32768
     rows = W.unit_rows(T, seed=0)
     signs = W.sign_bits(0)
     cache = encode(orc, rows, 2, signs)
     q = W.queries(1, 1, 64, seed=0)
-    out, lse, st = run_gpu(kvq, cache_fmt=2, caches={2: cache}, seq_len=[T], q=q, signs=signs)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=2, caches={2: cache}, seq_len=[T], q=q, signs=signs)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[2], q_lat=q.q_lat, q_rope=q.q_rope,
                                      sm_scale=W.SM_SCALE, tq4=cache, signs=signs)
     check(out, lse, ref, ref_lse)
 
 
-def test_decode_sparse_workload(kvq, orc):
+@IMPLS
+def test_decode_sparse_workload(kvq, orc, impl):
     """T=131072 fp8 rows, H=128, 2048 unique indices per query; plus the dense variant
     on a sample of heads."""
     T = 131072
@@ -121,18 +126,19 @@ def test_decode_sparse_workload(kvq, orc):
     cache = encode(orc, rows, 1)
     q = W.queries(1, 1, 128, seed=0)
     idx = W.sparse_indices(T, 2048, 1, seed=0)[None]
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx)
     ref, ref_lse, bad = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
                                        sm_scale=W.SM_SCALE, fp8=cache, idx=idx)
     assert st == 0 and not bad
     check(out, lse, ref, ref_lse)
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
                                      sm_scale=W.SM_SCALE, fp8=cache, heads=(0, 8))
     check(out, lse, ref, ref_lse, sel=(slice(None), slice(None), slice(0, 8)))
 
 
-def test_decode_ragged_mixed_small(kvq, orc):
+@IMPLS
+def test_decode_ragged_mixed_small(kvq, orc, impl):
     """Ragged, paged, mixed tiers, 4 causal queries per sequence; lengths include 0,
     1 and a sequence shorter than n_q."""
     wl = W.ragged(n_seq=6, n_q=4, H=8, len_lo=1, len_hi=700, page_size=64, seed=3)
@@ -140,7 +146,7 @@ def test_decode_ragged_mixed_small(kvq, orc):
     wl.seq_len[1] = 1
     wl.seq_len[4] = 3
     caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
                            signs=wl.signs, seq_fmt=wl.seq_fmt, causal=True,
                            block_table=wl.block_table, page_size=wl.page_size, split_rows=64)
     ref, ref_lse, _ = orc.mla_decode(seq_len=wl.seq_len, seq_fmt=wl.seq_fmt, q_lat=wl.queries.q_lat,
@@ -152,13 +158,14 @@ def test_decode_ragged_mixed_small(kvq, orc):
 
 
 @pytest.mark.slow
-def test_decode_ragged_workload(kvq, orc):
+@IMPLS
+def test_decode_ragged_workload(kvq, orc, impl):
     """The full ragged batch (32 sequences, lengths U{1024..65536}, 4 causal queries,
     H=64, 16 fp8 + 16 TQ4 sequences, page size 64); the oracle checks 8 heads of 4
     sequences (two of each tier)."""
     wl = W.ragged(seed=0)
     caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries,
                            signs=wl.signs, seq_fmt=wl.seq_fmt, causal=True,
                            block_table=wl.block_table, page_size=wl.page_size)
     sel = np.array([0, 7, 16, 31], np.int32)
@@ -171,7 +178,8 @@ def test_decode_ragged_workload(kvq, orc):
     check(out[sel][:, :, :8], lse[sel][:, :, :8], ref[sel][:, :, :8], ref_lse[sel][:, :, :8])
 
 
-def test_decode_bad_index_and_sparse_causal(kvq, orc):
+@IMPLS
+def test_decode_bad_index_and_sparse_causal(kvq, orc, impl):
     T, NQ = 500, 3
     rows = W.unit_rows(T, seed=9)
     cache = encode(orc, rows, 1)
@@ -179,7 +187,7 @@ def test_decode_bad_index_and_sparse_causal(kvq, orc):
     idx = W.sparse_indices(T, 100, NQ, seed=9)[None]
     idx[0, 1, 5] = T + 10
     idx[0, 2, 0] = -3
-    out, lse, st = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx,
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q, idx=idx,
                            causal=True, split_rows=32)
     ref, ref_lse, bad = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
                                        sm_scale=W.SM_SCALE, fp8=cache, idx=idx, causal=True)
@@ -187,7 +195,8 @@ def test_decode_bad_index_and_sparse_causal(kvq, orc):
     check(out, lse, ref, ref_lse)
 
 
-def test_decode_split_invariance(kvq, orc):
+@IMPLS
+def test_decode_split_invariance(kvq, orc, impl):
     """Different split sizes give results within the same bar of the oracle."""
     T = 5000
     rows = W.magnitude_rows(T, seed=10, lo=1e-2, hi=10)
@@ -196,7 +205,7 @@ def test_decode_split_invariance(kvq, orc):
     ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
                                      sm_scale=W.SM_SCALE, fp8=cache)
     for split in (32, 64, 4992, 5000, 8192):
-        out, lse, _ = run_gpu(kvq, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q,
+        out, lse, _ = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q,
                               split_rows=split)
         check(out, lse, ref, ref_lse)
 
