@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--T", type=int, default=32768)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-impl", type=int, default=0,
+                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2/3 tensor cores")
     return ap.parse_args()
 
 
@@ -237,7 +239,7 @@ def run_ours(args, world, rank, local):
         planes = dict(lat=lat[l], lat_scale=rad[l], rope=rope[l], rope_scale=rsc[l])
         probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat[l:l + 1], q_rope=q_rope[l:l + 1],
                                       sm_scale=W.SM_SCALE, max_seq_len=T, fmt=kvq.FMT_TQ4,
-                                      tq4=planes, signs=signs))
+                                      tq4=planes, signs=signs, impl=args.decode_impl))
     ws = torch.empty(kvq.kvq_mla_decode_workspace(probs[0]), dtype=torch.uint8, device=dev)
 
     def encode_step():
@@ -339,6 +341,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": f"tq4 MLA decode step: {Lyr} layers x T={T} rows (TQ4 latent + "
                                f"fp8 rope, 328 B/row), H={H}, nq=1, append 1 row/layer + decode",
                    "layers": Lyr, "T": T, "H": H, "n_q": 1, "split": "library default",
+                   "decode_impl": args.decode_impl,
                    "l2": f"inputs larger than L2 ({Lyr * T * ROW_BYTES_TQ4 / 1e6:.0f} MB of caches)",
                    "graph": "CUDA graphs (encode half, decode half)"},
         "effective_gbs": round(Lyr * T * ROW_BYTES_TQ4 / (ms_per_step / 1e3) / 1e9, 1),

@@ -352,7 +352,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
     // impl 0 selects the CUDA-core kernel until the tensor-core one is validated
-    plan.tc = p.impl == 2;
+    plan.tc = p.impl == 2 || p.impl == 3;
     int64_t split_rows = p.split_rows;
     if (plan.tc) {
         constexpr int kTile = 128, kHeadsTc = 32;

@@ -588,6 +588,497 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
     }
 }
 
+
+// ====================================================================================
+// Variant 2: the score's A operand (the dequantised rows) is written by the producer
+// threads straight into tensor memory (thread = row = TMEM lane) and read from there
+// by the MMA; only the context's V^T chunks go through shared memory.  S is single
+// buffered (the softmax frees it as soon as it has loaded its row), and the producer
+// keeps 4 chunks of raw codes in flight in registers.
+// TMEM: S lat 0..63, S rope 64..127, score-A ring 4 x 32 columns at 128.., O^T 256..511.
+// ====================================================================================
+constexpr int kRingA = 4;                // TMEM score-A slots (32 columns each)
+constexpr int kRingC = 6;                // shared-memory context slots (pairs adjacent)
+constexpr int kPre = 4;                  // chunks of raw codes in flight per thread
+constexpr uint32_t kColA = 128;
+constexpr int k2OffQ = 0;
+constexpr int k2OffRing = k2OffQ + kQBytes;
+constexpr int k2OffP = k2OffRing + kRingC * kChunkBytes;
+constexpr int k2OffRed = k2OffP + 2 * kPBytes;
+constexpr int k2OffBar = k2OffRed + 4 * 32 * 4;
+// full_a[4], empty_a[4], full_c[6], empty_c[6], s_full, s_empty, p_full[2], p_empty[2],
+// o_done, drain
+constexpr int k2NumBars = 2 * kRingA + 2 * kRingC + 8;
+constexpr int k2OffMisc = k2OffBar + k2NumBars * 8;
+constexpr int k2SmemBytes = k2OffMisc + 16 + 1024;
+
+struct Shared2 {
+    uint8_t* base;
+    __device__ uint8_t* q() const { return base + k2OffQ; }
+    __device__ uint8_t* slot(int i) const { return base + k2OffRing + i * kChunkBytes; }
+    __device__ uint8_t* pbuf(int b) const { return base + k2OffP + b * kPBytes; }
+    __device__ float* red() const { return reinterpret_cast<float*>(base + k2OffRed); }
+    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + k2OffBar) + i; }
+    __device__ uint64_t* full_a(int i) const { return bar(i); }
+    __device__ uint64_t* empty_a(int i) const { return bar(kRingA + i); }
+    __device__ uint64_t* full_c(int i) const { return bar(2 * kRingA + i); }
+    __device__ uint64_t* empty_c(int i) const { return bar(2 * kRingA + kRingC + i); }
+    __device__ uint64_t* s_full() const { return bar(2 * kRingA + 2 * kRingC); }
+    __device__ uint64_t* s_empty() const { return bar(2 * kRingA + 2 * kRingC + 1); }
+    __device__ uint64_t* p_full(int b) const { return bar(2 * kRingA + 2 * kRingC + 2 + b); }
+    __device__ uint64_t* p_empty(int b) const { return bar(2 * kRingA + 2 * kRingC + 4 + b); }
+    __device__ uint64_t* o_done() const { return bar(2 * kRingA + 2 * kRingC + 6); }
+    __device__ uint64_t* drain() const { return bar(2 * kRingA + 2 * kRingC + 7); }
+    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k2OffMisc); }
+    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k2OffMisc + 4); }
+};
+
+__device__ __forceinline__ bool wait_bar2(const Shared2& sh, uint64_t* bar, uint32_t parity,
+                                          uint32_t* status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*sh.abort_flag()) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *sh.abort_flag() = 1;
+            if (status) atomicOr(status, (unsigned)KVQ_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// raw codes of one chunk of one row: fp8 (and every rope chunk) 64 bytes, TQ4 32 bytes
+struct RawChunk {
+    uint4 v[4];
+    bool valid;
+};
+
+__device__ __forceinline__ void load_raw(RawChunk& r, int64_t row, int ch, bool tq4,
+                                         const kvq_mla_cache& C)
+{
+    r.valid = row >= 0;
+    if (!r.valid) return;
+    if (ch == 8 || !tq4) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(ch == 8 ? C.rope + row * kDRope
+                                                                 : C.lat + row * kDLat + ch * 64);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) r.v[v] = __ldg(s4 + v);
+    } else {
+        const uint4* s4 = reinterpret_cast<const uint4*>(C.lat + row * (kDLat / 2) + ch * 32);
+        r.v[0] = __ldg(s4);
+        r.v[1] = __ldg(s4 + 1);
+    }
+}
+
+// 64 fp16 values (32 half2 words, element pairs in order) of a raw chunk
+__device__ __forceinline__ void raw_to_half(const RawChunk& r, int ch, bool tq4, uint32_t (&h)[32])
+{
+    if (!r.valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) h[i] = 0;
+        return;
+    }
+    if (ch == 8 || !tq4) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            e4m3x4_to_half(r.v[v].x, h[8 * v + 0], h[8 * v + 1]);
+            e4m3x4_to_half(r.v[v].y, h[8 * v + 2], h[8 * v + 3]);
+            e4m3x4_to_half(r.v[v].z, h[8 * v + 4], h[8 * v + 5]);
+            e4m3x4_to_half(r.v[v].w, h[8 * v + 6], h[8 * v + 7]);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const uint32_t ww[4] = {r.v[v].x, r.v[v].y, r.v[v].z, r.v[v].w};
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const uint32_t byte = (ww[b >> 2] >> (8 * (b & 3))) & 0xFF;
+                h[16 * v + b] = pack_half2(c_cb_tc[byte & 15], c_cb_tc[byte >> 4]);
+            }
+        }
+    }
+}
+
+// item n of the producer / MMA order: per step i, S(i) (9 chunks) if i < NT, then
+// C(i-1) (8 latent chunks) if i >= 1
+__device__ __forceinline__ void item_of(int n, int NT, int& tile, int& ch, bool& score)
+{
+    if (n < 9) { tile = 0; ch = n; score = true; return; }
+    const int m = n - 9;
+    const int i = 1 + m / 17, j = m % 17;
+    if (i < NT) {
+        if (j < 9) { tile = i; ch = j; score = true; }
+        else { tile = i - 1; ch = j - 9; score = false; }
+    } else {
+        tile = NT - 1; ch = j; score = false;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
+{
+    extern __shared__ uint8_t dsm[];
+    Shared2 sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
+    const kvq_mla_problem& p = a.p;
+    const int split = blockIdx.x, s = blockIdx.y;
+    const int q = blockIdx.z / a.n_hg, hg = blockIdx.z % a.n_hg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = hg * kGQ;
+    const int nh = min(kGQ, p.n_heads - h0);
+    const int L = p.seq_len[s];
+    const int fmt = seq_fmt_of(p, s);
+    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
+    const int64_t r0 = (int64_t)split * a.split_rows;
+    const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
+    const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
+    const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
+
+    if (r0 >= n_cand || bad_fmt) {
+        if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
+        if (tid < nh) {
+            const int64_t sl = (qrow + h0 + tid) * a.n_splits + split;
+            a.part_ml[sl * 2] = -INFINITY;
+            a.part_ml[sl * 2 + 1] = 0.0f;
+        }
+        return;
+    }
+    const bool tq4 = fmt == KVQ_FMT_TQ4;
+    const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
+    const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
+    RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
+
+    if (tid == 0) {
+        for (int i = 0; i < kRingA; ++i) {
+            mbar_init(sh.full_a(i), 128);
+            mbar_init(sh.empty_a(i), 1);
+        }
+        for (int i = 0; i < kRingC; ++i) {
+            mbar_init(sh.full_c(i), 128);
+            mbar_init(sh.empty_c(i), 1);
+        }
+        mbar_init(sh.s_full(), 1);
+        mbar_init(sh.s_empty(), 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sh.p_full(b), 128);
+            mbar_init(sh.p_empty(b), 1);
+        }
+        mbar_init(sh.o_done(), 1);
+        mbar_init(sh.drain(), 1);
+        *sh.abort_flag() = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(sh.tmem_base(), 512);
+        tmem_relinquish();
+    }
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes);
+        uint4* dst = reinterpret_cast<uint4*>(sh.q());
+        for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sh.tmem_base();
+    const int n_items = 17 * NT;
+
+    if (warp < 4) {
+        // ================================ producer =======================================
+        const int t = tid;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        int64_t row_cache[2] = {-1, -1};
+        int tile_cache[2] = {-1, -1};
+        auto row_of = [&](int tile) -> int64_t {
+            const int k = tile & 1;
+            if (tile_cache[k] != tile) {
+                tile_cache[k] = tile;
+                row_cache[k] = rc.row(r0 + (int64_t)tile * kRT + t, false);
+            }
+            return row_cache[k];
+        };
+        RawChunk R[kPre];
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            R[u].valid = false;
+            if (u < n_items) {
+                int tile, ch; bool sc;
+                item_of(u, NT, tile, ch, sc);
+                load_raw(R[u], row_of(tile), ch, tq4, C);
+            }
+        }
+        int a_cnt = 0, c_cnt = 0;
+        bool ok = true;
+        for (int n0 = 0; n0 < n_items && ok; n0 += kPre) {
+#pragma unroll
+            for (int u = 0; u < kPre; ++u) {
+                const int n = n0 + u;
+                if (n >= n_items || !ok) break;
+                int tile, ch; bool sc;
+                item_of(n, NT, tile, ch, sc);
+                uint32_t h[32];
+                raw_to_half(R[u], ch, tq4, h);
+                if (sc) {
+                    const int slot = a_cnt % kRingA;
+                    ok = wait_bar2(sh, sh.empty_a(slot), ((uint32_t)(a_cnt / kRingA) & 1u) ^ 1u, a.status);
+                    ok = __all_sync(kFull, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    tmem_st_x32(tmem + lane_base + kColA + 32 * slot, h);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(sh.full_a(slot));
+                    ++a_cnt;
+                } else {
+                    const int slot = c_cnt % kRingC;
+                    ok = wait_bar2(sh, sh.empty_c(slot), ((uint32_t)(c_cnt / kRingC) & 1u) ^ 1u, a.status);
+                    ok = __all_sync(kFull, ok);
+                    if (!ok) break;
+                    uint8_t* dst = sh.slot(slot);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(dst + sw128(t, c)) =
+                            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    mbar_arrive(sh.full_c(slot));
+                    ++c_cnt;
+                }
+                if (n + kPre < n_items) {
+                    int tile2, ch2; bool sc2;
+                    item_of(n + kPre, NT, tile2, ch2, sc2);
+                    load_raw(R[u], row_of(tile2), ch2, tq4, C);
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // ================================ softmax ========================================
+        const int t = tid - 128;
+        const int wq = warp - 4;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const float tau2 = p.sm_scale * kLog2e;
+        const float c512 = tq4_inv_sqrt(kDLat);
+        float* red = sh.red();
+        float m_run[kGQ], l_part[kGQ];
+#pragma unroll
+        for (int g = 0; g < kGQ; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.0f; }
+        bool ok = true;
+        for (int i = 0; i < NT; ++i) {
+            const int b = i & 1;
+            const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
+            float sc_lat = 0.0f, sc_rope = 0.0f;
+            if (row >= 0) {
+                sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
+                sc_rope = C.rope_scale[row];
+            }
+            if (ok) ok = wait_bar2(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
+            ok = __all_sync(kFull, ok);
+            float sv[kGQ];
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) sv[g] = 0.0f;
+            if (ok) {
+                tc_fence_after();
+                uint32_t x[16], y[16];
+#pragma unroll
+                for (int c = 0; c < kN; c += 16) {
+                    tmem_ld_x16(tmem + lane_base + c, x);
+                    tmem_ld_x16(tmem + lane_base + 64 + c, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        sv[(c + e) & (kGQ - 1)] += fmaf(sc_lat, __uint_as_float(x[e]),
+                                                        sc_rope * __uint_as_float(y[e]));
+                }
+                tc_fence_before();
+                mbar_arrive(sh.s_empty());
+            }
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) sv[g] = (row >= 0 && ok) ? sv[g] * tau2 : -INFINITY;
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) {
+                float v = sv[g];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+                if (lane == 0) red[wq * 32 + g] = v;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            bool need_rescale = false;
+            float alpha[kGQ];
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) {
+                const float tm = fmaxf(fmaxf(red[g], red[32 + g]), fmaxf(red[64 + g], red[96 + g]));
+                alpha[g] = 1.0f;
+                if (tm > m_run[g] + kLazy || (m_run[g] == -INFINITY && tm > -INFINITY)) {
+                    alpha[g] = (m_run[g] == -INFINITY) ? 0.0f : exp2f(m_run[g] - tm);
+                    m_run[g] = tm;
+                    if (i > 0) need_rescale = true;
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (need_rescale && ok) {
+                ok = wait_bar2(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+                ok = __all_sync(kFull, ok);
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                        for (int c = 0; c < kN; c += 16) {
+                            uint32_t x[16];
+                            tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha[(c + e) & (kGQ - 1)]);
+                            tmem_st_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kGQ; ++g) l_part[g] *= alpha[g];
+            uint32_t wh[kGQ / 2], wl[kGQ / 2];
+#pragma unroll
+            for (int g = 0; g < kGQ; g += 2) {
+                const float p0 = sv[g] == -INFINITY ? 0.0f : exp2f(sv[g] - m_run[g]);
+                const float p1 = sv[g + 1] == -INFINITY ? 0.0f : exp2f(sv[g + 1] - m_run[g + 1]);
+                l_part[g] += p0;
+                l_part[g + 1] += p1;
+                const float w0 = p0 * sc_lat, w1 = p1 * sc_lat;
+                const __half2 hi = __floats2half2_rn(w0, w1);
+                const float2 hf = __half22float2(hi);
+                const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
+                wh[g / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                wl[g / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+            if (ok && i >= 2) ok = wait_bar2(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
+            if (ok) {
+                uint8_t* pb = sh.pbuf(b);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    *reinterpret_cast<uint4*>(pb + sw128(t, c)) =
+                        make_uint4(wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]);
+                    *reinterpret_cast<uint4*>(pb + sw128(t, c + 4)) =
+                        make_uint4(wl[4 * c], wl[4 * c + 1], wl[4 * c + 2], wl[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(sh.p_full(b));
+            }
+        }
+        if (ok) ok = wait_bar2(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
+        ok = __all_sync(kFull, ok);
+#pragma unroll
+        for (int g = 0; g < kGQ; ++g) {
+            float v = l_part[g];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+            if (lane == 0) red[wq * 32 + g] = v;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ok) {
+            tc_fence_after();
+            if (t < nh) {
+                const float lt = red[t] + red[32 + t] + red[64 + t] + red[96 + t];
+                const int64_t sl = (qrow + h0 + t) * a.n_splits + split;
+                float mt = m_run[0];
+#pragma unroll
+                for (int g = 1; g < kGQ; ++g) if (g == t) mt = m_run[g];
+                a.part_ml[sl * 2] = mt;
+                a.part_ml[sl * 2 + 1] = lt;
+            }
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+                const int d = 128 * m + 32 * wq + lane;
+                uint32_t x[16], y[16];
+#pragma unroll
+                for (int c = 0; c < kGQ; c += 16) {
+                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
+                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + kGQ + c, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int g = c + e;
+                        if (g < nh)
+                            a.part_o[((qrow + h0 + g) * a.n_splits + split) * kDLat + d] =
+                                __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================================ MMA issuer =====================================
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);
+            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);
+            const uint32_t q_base = smem_u32(sh.q());
+            int a_cnt = 0, c_cnt = 0;
+            bool ok = true;
+            for (int i = 0; i <= NT && ok; ++i) {
+                if (i < NT) {
+                    if (i >= 1 && !(ok = wait_bar2(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status))) break;
+                    tc_fence_after();
+                    for (int ch = 0; ch < 9 && ok; ++ch) {
+                        const int slot = a_cnt % kRingA;
+                        if (!(ok = wait_bar2(sh, sh.full_a(slot), (uint32_t)(a_cnt / kRingA) & 1u, a.status))) break;
+                        tc_fence_after();
+                        const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16_ts(d, tmem + kColA + 32 * slot + 8 * ks,
+                                       desc_sw128(q_base + ch * kQSlabBytes + 32 * ks, 1024), idesc_s,
+                                       (ch == 0 || ch == 8) ? (ks > 0) : 1u);
+                        mma_commit(sh.empty_a(slot));
+                        ++a_cnt;
+                    }
+                    if (!ok) break;
+                    mma_commit(sh.s_full());
+                }
+                if (i >= 1) {
+                    const int tile = i - 1, b = tile & 1;
+                    if (!(ok = wait_bar2(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
+                    tc_fence_after();
+                    for (int c = 0; c < 8 && ok; ++c) {
+                        const int slot = c_cnt % kRingC;
+                        if (!(ok = wait_bar2(sh, sh.full_c(slot), (uint32_t)(c_cnt / kRingC) & 1u, a.status))) break;
+                        tc_fence_after();
+                        if (c & 1) {
+                            const int m = c >> 1;
+                            const uint32_t a_base = smem_u32(sh.slot(slot - 1));
+                            const uint32_t p_base = smem_u32(sh.pbuf(b));
+#pragma unroll
+                            for (int ks = 0; ks < kRT / 16; ++ks)
+                                mma_f16_ss(tmem + kColO + 64 * m,
+                                           desc_sw128_lbo(a_base + 2048 * ks, kChunkBytes, 1024),
+                                           desc_sw128(p_base + 2048 * ks, 1024), idesc_c,
+                                           (tile == 0 && ks == 0) ? 0u : 1u);
+                            mma_commit(sh.empty_c(slot - 1));
+                            mma_commit(sh.empty_c(slot));
+                        }
+                        ++c_cnt;
+                    }
+                    if (!ok) break;
+                    mma_commit(sh.p_empty(b));
+                    mma_commit(sh.o_done());
+                }
+            }
+            mma_commit(sh.drain());
+            if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
+                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -602,6 +1093,7 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s)
 {
+    const bool v2 = p.impl == 3;
     TcArgs a;
     a.p = p;
     a.split_rows = plan.split_rows;
@@ -623,10 +1115,14 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
         e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(mla_decode_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k2SmemBytes);
+        if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+    if (v2) mla_decode_tc2_kernel<<<grid, kThreads, k2SmemBytes, s>>>(a);
+    else mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -119,3 +119,42 @@ def test_fault_injection(kvq):
     finally:
         assert L.kvq_set_fault(None) == 0
     assert L.kvq_encode_fp8(FAKE, 4, 0, 512, FAKE, 512, FAKE, None) == 1
+
+
+def test_struct_layouts_match_headers(kvq, tmp_path):
+    """The ctypes mirrors have the sizes and field offsets the C headers give."""
+    import subprocess
+    import oracle
+    src = tmp_path / "sz.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "kvq.h"\n#include "kvq_oracle.h"\n'
+        'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(kvq_mla_cache),'
+        ' sizeof(kvq_gather_desc), sizeof(kvq_mla_problem), offsetof(kvq_mla_problem, impl),'
+        ' offsetof(kvq_gather_desc, dev_status), sizeof(orc_mla), offsetof(orc_mla, n_sel));'
+        'return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(ROOT, "oracle"),
+                    str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [C.sizeof(kvq.MlaCache), C.sizeof(kvq.GatherDesc), C.sizeof(kvq.MlaProblem),
+            kvq.MlaProblem.impl.offset, kvq.GatherDesc.dev_status.offset,
+            C.sizeof(oracle.OrcMla), oracle.OrcMla.n_sel.offset]
+    assert got == want
+
+
+def test_fault_injection_from_environment(tmp_path):
+    """KVQ_FAULT in the environment arms the injection at the first call (fresh process)."""
+    import subprocess
+    import sys
+    code = (
+        "import ctypes as C, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import quantized_kv_cache_fp8_gb300 as k\n"
+        "L = k.lib()\n"
+        f"print(L.kvq_encode_fp8({FAKE}, 4, 512, 512, {FAKE}, 512, {FAKE}, None),"
+        f" L.kvq_encode_tq4({FAKE}, 4, 384, 384, {FAKE}, {FAKE}, 192, {FAKE}, None))\n")
+    env = dict(os.environ, KVQ_FAULT="kvq_encode_fp8:6")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True).stdout.split()
+    assert out == ["6", "2"]
