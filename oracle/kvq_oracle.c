@@ -159,12 +159,21 @@ static double std_normal_cdf(double t) { return 0.5 * erfc(-t / sqrt(2.0)); }
  * from a uniform start until no centroid moves by 1e-15.  The stored codebook is each
  * centroid rounded to the nearest binary16 value; the thresholds are the midpoints of
  * the stored centroids (exact in fp32). */
-int orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters)
+/* The iteration converges linearly; it stops once no centroid moves by 1e-15, or, since
+ * the last bits of exp/erfc differ between C libraries and can leave the iterate
+ * oscillating at the rounding level, after 20000 steps (by then the moves are below
+ * 1e-14; the pins check the fixed-point condition to 1e-12).  Computed once per process. */
+static int    g_cb_ready = 0;
+static double g_cb_lloyd[16];
+static float  g_cb_f[16], g_cb_thr[15];
+static int    g_cb_iters = 0;
+
+static void tq4_codebook_compute(void)
 {
     double c[16], t[17];
     for (int k = 0; k < 16; ++k) c[k] = -3.0 + 6.0 * k / 15.0;
     int it;
-    for (it = 0; it < 1000000; ++it) {
+    for (it = 0; it < 20000; ++it) {
         t[0] = -INFINITY; t[16] = INFINITY;
         for (int k = 1; k < 16; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
         double move = 0.0;
@@ -179,11 +188,21 @@ int orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters)
         if (move < 1e-15) break;
     }
     for (int k = 0; k < 16; ++k) {
-        lloyd[k] = c[k];
-        cb[k] = (float)orc_f16_value(orc_f16_rne(c[k]));
+        g_cb_lloyd[k] = c[k];
+        g_cb_f[k] = (float)orc_f16_value(orc_f16_rne(c[k]));
     }
-    for (int k = 0; k < 15; ++k) thr[k] = (cb[k] + cb[k + 1]) / 2.0f;
-    if (iters) *iters = it;
+    for (int k = 0; k < 15; ++k) g_cb_thr[k] = (g_cb_f[k] + g_cb_f[k + 1]) / 2.0f;
+    g_cb_iters = it;
+    g_cb_ready = 1;
+}
+
+int orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters)
+{
+    if (!g_cb_ready) tq4_codebook_compute();
+    memcpy(lloyd, g_cb_lloyd, sizeof g_cb_lloyd);
+    memcpy(cb, g_cb_f, sizeof g_cb_f);
+    memcpy(thr, g_cb_thr, sizeof g_cb_thr);
+    if (iters) *iters = g_cb_iters;
     return 0;
 }
 

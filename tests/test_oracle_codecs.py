@@ -76,7 +76,7 @@ def test_fp8_zero_rows_and_scales(orc):
 
 def test_codebook_is_lloyd_max_fixed_point(orc):
     lloyd, cb, thr, iters = orc.tq4_codebook()
-    assert iters < 1000000
+    assert iters <= 20000
     # symmetric
     assert np.allclose(lloyd, -lloyd[::-1], atol=1e-13)
     # centroid condition E[X | cell] in closed form, with thresholds at midpoints

@@ -190,7 +190,7 @@ def test_q4_small_page_crossing(kvq, orc):
 
 
 def test_q4_tie_and_zero_blocks(kvq, orc):
-    wl = W.q4_paged(n_seq=1, n_tok=6, n_heads=2, page_size=4, seed=6)
+    wl = W.q4_paged(n_seq=1, n_tok=6, n_heads=2, page_size=4, pos0=2, seed=6, spare_pages=1)
     hd = 256
     # rows chosen so that the ROTATED blocks hit the tie rule: the Hadamard transform
     # of e_0 * v is v/16 everywhere (all-equal blocks); of zero is zero (all-zero)
