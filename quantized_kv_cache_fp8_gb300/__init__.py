@@ -208,6 +208,9 @@ def _cache(planes):
 def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, seq_fmt=None,
                  causal=False, block_table=None, page_size=0, seq_stride_rows=0, fp8=None,
                  tq4=None, signs=None, idx=None, split_rows=0, impl=0) -> MlaProblem:
+    """Fill a kvq_mla_problem from torch tensors.  The returned object holds a reference
+    to every tensor whose device pointer it carries, so the memory stays allocated (and
+    is not handed to a later allocation) for as long as the problem is alive."""
     n_seq, n_q, H, DL = q_lat.shape
     p = MlaProblem()
     p.n_seq, p.n_q, p.n_heads, p.d_lat, p.d_rope = n_seq, n_q, H, DL, q_rope.shape[-1]
@@ -221,6 +224,7 @@ def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, 
     if idx is not None:
         p.idx, p.top_k = _ptr(idx), idx.shape[-1]
     p.sm_scale, p.split_rows, p.impl = float(sm_scale), int(split_rows), int(impl)
+    p._keep = [seq_len, seq_fmt, block_table, fp8, tq4, signs, q_lat, q_rope, idx]
     return p
 
 

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
     float* s_p = s_kv + kRT * kLDT;         // [kRT][kGH]
     float* s_alpha = s_p + kRT * kGH;       // [kGH]
     int* s_valid = reinterpret_cast<int*>(s_alpha + kGH);   // [kRT]
+    float* s_cb = reinterpret_cast<float*>(s_valid + kRT);  // [16] TQ4 centroids
 
     const kvq_mla_problem& p = a.p;
     const int split = blockIdx.x, s = blockIdx.y;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
     }
     const bool tq4 = fmt == KVQ_FMT_TQ4;
     const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
+    if (tid < 16) s_cb[tid] = c_cb[tid];
 
     for (int i = tid; i < kGH * kD; i += kThreads) {
         const int g = i / kD, k = i % kD;
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
                 for (int e = 0; e < 16; ++e) {
                     const uint32_t byte = (ww[e >> 3] >> (8 * ((e >> 1) & 3))) & 0xFF;
                     const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15);
-                    dst[lane * 16 + e] = c_cb[code] * sig;
+                    dst[lane * 16 + e] = s_cb[code] * sig;
                 }
             }
             const unsigned short rw = reinterpret_cast<const unsigned short*>(C.rope + row * kDRope)[lane];
@@ -284,61 +286,73 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 //   M = max_S m_S,  L = sum_S l_S 2^(m_S - M),  out = sum_S o_S 2^(m_S - M) / L,
 //   lse = (M + log2 L) ln 2;  TQ4: out <- (1/sqrt 512) s (.) FWHT_512(out).
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) mla_combine_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 {
+    constexpr int kMaxW = 1024;                   // splits combined per pass of weights
     __shared__ float s_o[kDLat];
+    __shared__ float s_w[kMaxW];
+    __shared__ float s_red[2][16];
     const kvq_mla_problem& p = a.p;
     const int64_t r = blockIdx.x;                 // (s * n_q + q) * H + h
     const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = p.seq_len[s];
     const int fmt = seq_format(p, s);
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
     const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
     const float* ml = a.part_ml + r * a.n_splits * 2;
+    // M = max over splits holding rows
     float M = -INFINITY;
-    for (int S = 0; S < ns; ++S)
+    for (int S = tid; S < ns; S += 512)
         if (ml[2 * S + 1] > 0.0f) M = fmaxf(M, ml[2 * S]);
-    float Lt = 0.0f;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int S = 0; S < ns; ++S) {
-        const float lS = ml[2 * S + 1];
-        if (!(lS > 0.0f)) continue;
-        const float w = exp2f(ml[2 * S] - M);
-        Lt += lS * w;
-        const float4 v = reinterpret_cast<const float4*>(a.part_o + (r * a.n_splits + S) * kDLat)[tid];
-        acc[0] = fmaf(v.x, w, acc[0]);
-        acc[1] = fmaf(v.y, w, acc[1]);
-        acc[2] = fmaf(v.z, w, acc[2]);
-        acc[3] = fmaf(v.w, w, acc[3]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0) s_red[0][warp] = M;
+    __syncthreads();
+    M = s_red[0][0];
+    for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
+    float acc = 0.0f, Lpart = 0.0f;
+    for (int S0 = 0; S0 < ns; S0 += kMaxW) {
+        const int nw = min(kMaxW, ns - S0);
+        __syncthreads();
+        for (int S = tid; S < nw; S += 512) {
+            const float lS = ml[2 * (S0 + S) + 1];
+            const float w = lS > 0.0f ? exp2f(ml[2 * (S0 + S)] - M) : 0.0f;
+            s_w[S] = w;
+            Lpart += lS > 0.0f ? lS * w : 0.0f;
+        }
+        __syncthreads();
+        const float* po = a.part_o + (r * a.n_splits + S0) * kDLat + tid;
+#pragma unroll 8
+        for (int S = 0; S < nw; ++S) {
+            const float w = s_w[S];
+            if (w != 0.0f) acc = fmaf(po[(int64_t)S * kDLat], w, acc);
+        }
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) Lpart += __shfl_xor_sync(kFull, Lpart, o);
+    if (lane == 0) s_red[1][warp] = Lpart;
+    __syncthreads();
+    float Lt = 0.0f;
+    for (int w = 0; w < 16; ++w) Lt += s_red[1][w];
     const bool empty = !(Lt > 0.0f);
-    const float inv = empty ? 0.0f : 1.0f / Lt;
-    float res[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) res[e] = acc[e] * inv;
+    float res = empty ? 0.0f : acc / Lt;
     if (fmt == KVQ_FMT_TQ4) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s_o[tid * 4 + e] = res[e];
+        s_o[tid] = res;
         __syncthreads();
         for (int h = 1; h < kDLat; h <<= 1) {
-            for (int b = tid; b < kDLat / 2; b += 128) {
-                const int i = (b / h) * 2 * h + (b % h);
+            if (tid < kDLat / 2) {
+                const int i = (tid / h) * 2 * h + (tid % h);
                 const float x = s_o[i], y = s_o[i + h];
                 s_o[i] = x + y;
                 s_o[i + h] = x - y;
             }
             __syncthreads();
         }
-        const float c = tq4_inv_sqrt(kDLat);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = tid * 4 + e;
-            const bool ng = (p.tq4_signs[i >> 5] >> (i & 31)) & 1u;
-            res[e] = s_o[i] * c * (ng ? -1.0f : 1.0f);
-        }
+        const bool ng = (p.tq4_signs[tid >> 5] >> (tid & 31)) & 1u;
+        res = s_o[tid] * tq4_inv_sqrt(kDLat) * (ng ? -1.0f : 1.0f);
     }
-    reinterpret_cast<float4*>(a.out + r * kDLat)[tid] = make_float4(res[0], res[1], res[2], res[3]);
+    a.out[r * kDLat + tid] = res;
     if (tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
 }
 
@@ -424,11 +438,11 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
         cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,
                                              a.part_o, dev_status, s);
         if (e != cudaSuccess) return e;
-        mla_combine_kernel<<<(unsigned)rows, 128, 0, s>>>(a);
+        mla_combine_kernel<<<(unsigned)rows, 512, 0, s>>>(a);
         return cudaGetLastError();
     }
     const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
-                        + kRT * sizeof(int);
+                        + kRT * sizeof(int) + 16 * sizeof(float);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
@@ -442,7 +456,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hblk);
     mla_decode_simt_kernel<<<grid, kThreads, smem, s>>>(a);
-    mla_combine_kernel<<<(unsigned)rows, 128, 0, s>>>(a);
+    mla_combine_kernel<<<(unsigned)rows, 512, 0, s>>>(a);
     return cudaGetLastError();
 }
 

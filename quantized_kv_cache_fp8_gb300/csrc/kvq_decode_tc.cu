@@ -58,7 +58,8 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQBytes;
 constexpr int kOffP = kOffRing + kRing * kChunkBytes;
 constexpr int kOffRed = kOffP + 2 * kPBytes;                 // [4][32] floats
-constexpr int kOffBar = kOffRed + 4 * 32 * 4;
+constexpr int kOffLut = kOffRed + 4 * 32 * 4;                // [256] half2: byte -> 2 centroids
+constexpr int kOffBar = kOffLut + 256 * 4;
 // barriers: full[kRing], empty[kRing], s_full[2], s_empty[2], p_full[2], p_empty[2],
 // o_done, drain
 constexpr int kNumBars = 2 * kRing + 10;
@@ -170,6 +171,7 @@ struct Shared {
     __device__ uint8_t* slot(int i) const { return base + kOffRing + i * kChunkBytes; }
     __device__ uint8_t* pbuf(int b) const { return base + kOffP + b * kPBytes; }
     __device__ float* red() const { return reinterpret_cast<float*>(base + kOffRed); }
+    __device__ uint32_t* lut() const { return reinterpret_cast<uint32_t*>(base + kOffLut); }
     __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
     __device__ uint64_t* full(int i) const { return bar(i); }
     __device__ uint64_t* empty(int i) const { return bar(kRing + i); }
@@ -229,7 +231,7 @@ struct RowCtx {
 // dequantise chunk `ch` (0..7 latent, 8 rope) of pool row `row` (or zeros) into row t of
 // a swizzled slot
 __device__ __forceinline__ void dequant_chunk(uint8_t* slot, int t, int64_t row, int ch, bool tq4,
-                                             const kvq_mla_cache& C)
+                                             const kvq_mla_cache& C, const uint32_t* lut)
 {
     uint32_t h[32];
     if (row < 0) {
@@ -254,15 +256,18 @@ __device__ __forceinline__ void dequant_chunk(uint8_t* slot, int t, int64_t row,
             const uint4 w = __ldg(s4 + v);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int b = 0; b < 16; ++b) {
-                const uint32_t byte = (ww[b >> 2] >> (8 * (b & 3))) & 0xFF;
-                h[16 * v + b] = pack_half2(c_cb_tc[byte & 15], c_cb_tc[byte >> 4]);
-            }
+            for (int b = 0; b < 16; ++b) h[16 * v + b] = lut[(ww[b >> 2] >> (8 * (b & 3))) & 0xFF];
         }
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(slot + sw128(t, c)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+}
+
+// the code-byte -> (centroid of low nibble, centroid of high nibble) table, in fp16
+__device__ __forceinline__ void fill_lut(uint32_t* lut, int tid, int n_threads)
+{
+    for (int b = tid; b < 256; b += n_threads) lut[b] = pack_half2(c_cb_tc[b & 15], c_cb_tc[b >> 4]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
@@ -324,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
         uint4* dst = reinterpret_cast<uint4*>(sh.q());
         for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
     }
+    fill_lut(sh.lut(), tid, kThreads);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -349,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
                     cur_tile = tile;
                     cur_row = rc.row(r0 + (int64_t)tile * kRT + t, false);
                 }
-                dequant_chunk(sh.slot(slot), t, cur_row, ch, tq4, C);
+                dequant_chunk(sh.slot(slot), t, cur_row, ch, tq4, C, sh.lut());
             }
             fence_proxy_async_smem();
             mbar_arrive(sh.full(slot));
@@ -605,7 +611,8 @@ constexpr int k2OffQ = 0;
 constexpr int k2OffRing = k2OffQ + kQBytes;
 constexpr int k2OffP = k2OffRing + kRingC * kChunkBytes;
 constexpr int k2OffRed = k2OffP + 2 * kPBytes;
-constexpr int k2OffBar = k2OffRed + 4 * 32 * 4;
+constexpr int k2OffLut = k2OffRed + 4 * 32 * 4;
+constexpr int k2OffBar = k2OffLut + 256 * 4;
 // full_a[4], empty_a[4], full_c[6], empty_c[6], s_full, s_empty, p_full[2], p_empty[2],
 // o_done, drain
 constexpr int k2NumBars = 2 * kRingA + 2 * kRingC + 8;
@@ -618,6 +625,7 @@ struct Shared2 {
     __device__ uint8_t* slot(int i) const { return base + k2OffRing + i * kChunkBytes; }
     __device__ uint8_t* pbuf(int b) const { return base + k2OffP + b * kPBytes; }
     __device__ float* red() const { return reinterpret_cast<float*>(base + k2OffRed); }
+    __device__ uint32_t* lut() const { return reinterpret_cast<uint32_t*>(base + k2OffLut); }
     __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + k2OffBar) + i; }
     __device__ uint64_t* full_a(int i) const { return bar(i); }
     __device__ uint64_t* empty_a(int i) const { return bar(kRingA + i); }
@@ -673,7 +681,8 @@ __device__ __forceinline__ void load_raw(RawChunk& r, int64_t row, int ch, bool 
 }
 
 // 64 fp16 values (32 half2 words, element pairs in order) of a raw chunk
-__device__ __forceinline__ void raw_to_half(const RawChunk& r, int ch, bool tq4, uint32_t (&h)[32])
+__device__ __forceinline__ void raw_to_half(const RawChunk& r, int ch, bool tq4, const uint32_t* lut,
+                                            uint32_t (&h)[32])
 {
     if (!r.valid) {
 #pragma unroll
@@ -693,10 +702,7 @@ __device__ __forceinline__ void raw_to_half(const RawChunk& r, int ch, bool tq4,
         for (int v = 0; v < 2; ++v) {
             const uint32_t ww[4] = {r.v[v].x, r.v[v].y, r.v[v].z, r.v[v].w};
 #pragma unroll
-            for (int b = 0; b < 16; ++b) {
-                const uint32_t byte = (ww[b >> 2] >> (8 * (b & 3))) & 0xFF;
-                h[16 * v + b] = pack_half2(c_cb_tc[byte & 15], c_cb_tc[byte >> 4]);
-            }
+            for (int b = 0; b < 16; ++b) h[16 * v + b] = lut[(ww[b >> 2] >> (8 * (b & 3))) & 0xFF];
         }
     }
 }
@@ -778,6 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
         uint4* dst = reinterpret_cast<uint4*>(sh.q());
         for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
     }
+    fill_lut(sh.lut(), tid, kThreads);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -819,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                 int tile, ch; bool sc;
                 item_of(n, NT, tile, ch, sc);
                 uint32_t h[32];
-                raw_to_half(R[u], ch, tq4, h);
+                raw_to_half(R[u], ch, tq4, sh.lut(), h);
                 if (sc) {
                     const int slot = a_cnt % kRingA;
                     ok = wait_bar2(sh, sh.empty_a(slot), ((uint32_t)(a_cnt / kRingA) & 1u) ^ 1u, a.status);
