@@ -289,19 +289,19 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 {
     constexpr int kMaxW = 1024;                   // splits combined per pass of weights
-    __shared__ float s_o[kDLat];
     __shared__ float s_w[kMaxW];
+    __shared__ __align__(16) float s_part[4][kDLat];
     __shared__ float s_red[2][16];
     const kvq_mla_problem& p = a.p;
     const int64_t r = blockIdx.x;                 // (s * n_q + q) * H + h
     const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid >> 7, j = tid & 127;      // split group, float4 column
     const int L = p.seq_len[s];
     const int fmt = seq_format(p, s);
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
     const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
     const float* ml = a.part_ml + r * a.n_splits * 2;
-    // M = max over splits holding rows
     float M = -INFINITY;
     for (int S = tid; S < ns; S += 512)
         if (ml[2 * S + 1] > 0.0f) M = fmaxf(M, ml[2 * S]);
@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     __syncthreads();
     M = s_red[0][0];
     for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
-    float acc = 0.0f, Lpart = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float Lpart = 0.0f;
     for (int S0 = 0; S0 < ns; S0 += kMaxW) {
         const int nw = min(kMaxW, ns - S0);
         __syncthreads();
@@ -322,13 +323,20 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
             Lpart += lS > 0.0f ? lS * w : 0.0f;
         }
         __syncthreads();
-        const float* po = a.part_o + (r * a.n_splits + S0) * kDLat + tid;
+        const float4* po = reinterpret_cast<const float4*>(a.part_o + (r * a.n_splits + S0) * kDLat) + j;
 #pragma unroll 8
-        for (int S = 0; S < nw; ++S) {
+        for (int S = grp; S < nw; S += 4) {
             const float w = s_w[S];
-            if (w != 0.0f) acc = fmaf(po[(int64_t)S * kDLat], w, acc);
+            if (w != 0.0f) {
+                const float4 v = po[(int64_t)S * (kDLat / 4)];
+                acc.x = fmaf(v.x, w, acc.x);
+                acc.y = fmaf(v.y, w, acc.y);
+                acc.z = fmaf(v.z, w, acc.z);
+                acc.w = fmaf(v.w, w, acc.w);
+            }
         }
     }
+    reinterpret_cast<float4*>(s_part[grp])[j] = acc;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) Lpart += __shfl_xor_sync(kFull, Lpart, o);
     if (lane == 0) s_red[1][warp] = Lpart;
@@ -336,8 +344,12 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     float Lt = 0.0f;
     for (int w = 0; w < 16; ++w) Lt += s_red[1][w];
     const bool empty = !(Lt > 0.0f);
-    float res = empty ? 0.0f : acc / Lt;
+    // thread tid owns output dim tid from here on
+    float res = s_part[0][tid] + s_part[1][tid] + s_part[2][tid] + s_part[3][tid];
+    res = empty ? 0.0f : res / Lt;
     if (fmt == KVQ_FMT_TQ4) {
+        __syncthreads();
+        float* s_o = s_part[0];
         s_o[tid] = res;
         __syncthreads();
         for (int h = 1; h < kDLat; h <<= 1) {
@@ -430,7 +442,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.status = dev_status;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || p.fmt == KVQ_FMT_TQ4;
-    if (any_tq4) {
+    if (any_tq4 && !plan.tc) {
         int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
     }

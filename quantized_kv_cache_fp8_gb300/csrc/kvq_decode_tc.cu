@@ -132,6 +132,12 @@ __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
     const int64_t n_items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    uint32_t neg = 0;                                       // TQ4 signs of elements k*32+lane
+    if (p.tq4_signs) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) neg |= ((p.tq4_signs[k] >> lane) & 1u) << k;
+    }
+    const float c512 = tq4_inv_sqrt(kDLat);
     for (int64_t it = warp; it < n_items; it += n_warps) {
         const int n = (int)(it % kGQ);                       // head within group
         const int64_t grp = it / kGQ;                        // (s, q, hg)
@@ -141,24 +147,43 @@ __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
         const int h = hg * kGQ + n;
         const bool tq4 = seq_fmt_of(p, s) == KVQ_FMT_TQ4;
         uint8_t* img = a.q_img + grp * (int64_t)kQBytes;
-        // lane handles k = 2*lane, 2*lane+1 of every 64-wide slab: 18 values
-        for (int slab = 0; slab < 9; ++slab) {
-            float v[2] = {0.0f, 0.0f};
-            if (h < p.n_heads) {
-                const int64_t r = sq * p.n_heads + h;
+        // latent: element k = j*32 + lane in register j; TQ4 rotates it, (1/sqrt 512)
+        // FWHT_512(s (.) q), in fp32 first
+        float y[16];
+        float r2[2] = {0.0f, 0.0f};
+        if (h < p.n_heads) {
+            const int64_t r = sq * p.n_heads + h;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int k = slab * 64 + 2 * lane + e;
-                    v[e] = k < kDLat ? (tq4 ? a.q_rot[r * kDLat + k] : p.q_lat[r * kDLat + k])
-                                     : p.q_rope[r * kDRope + (k - kDLat)];
-                }
-            }
-            const __half2 hi = __floats2half2_rn(v[0], v[1]);
+            for (int j = 0; j < 16; ++j) y[j] = p.q_lat[r * kDLat + j * 32 + lane];
+            r2[0] = p.q_rope[r * kDRope + 2 * lane];
+            r2[1] = p.q_rope[r * kDRope + 2 * lane + 1];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = 0.0f;
+        }
+        if (tq4) {                                           // warp-uniform
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = ((neg >> j) & 1u) ? -y[j] : y[j];
+            fwht_warp<16>(y, lane);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] *= c512;
+        }
+        // hi | lo halves into the swizzled K-major slabs [64 rows x 64 k]
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int k = j * 32 + lane, slab = k >> 6, kk = k & 63;
+            const __half hi = __float2half_rn(y[j]);
+            const __half lo = __float2half_rn(y[j] - __half2float(hi));
+            uint8_t* base = img + slab * kQSlabBytes + (kk & 7) * 2;
+            *reinterpret_cast<__half*>(base + sw128(n, kk >> 3)) = hi;
+            *reinterpret_cast<__half*>(base + sw128(n + kGQ, kk >> 3)) = lo;
+        }
+        {
+            const __half2 hi = __floats2half2_rn(r2[0], r2[1]);
             const float2 hf = __half22float2(hi);
-            const __half2 lo = __floats2half2_rn(v[0] - hf.x, v[1] - hf.y);
-            // element k = 2*lane (+1) sits in 16B chunk lane/4, word lane%4
-            const int c = lane >> 2, wd = lane & 3;
-            uint8_t* slab_base = img + slab * kQSlabBytes;
+            const __half2 lo = __floats2half2_rn(r2[0] - hf.x, r2[1] - hf.y);
+            const int c = lane >> 2, wd = lane & 3;          // k = 512 + 2*lane (+1)
+            uint8_t* slab_base = img + 8 * kQSlabBytes;
             *reinterpret_cast<__half2*>(slab_base + sw128(n, c) + 4 * wd) = hi;
             *reinterpret_cast<__half2*>(slab_base + sw128(n + kGQ, c) + 4 * wd) = lo;
         }
@@ -428,11 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");    // red[] is rewritten next tile
+            // Consume o_done's phase i-1 (the context MMAs of tile i-1) at every tile,
+            // so that this wait and the epilogue's never trail the barrier by more than
+            // one phase (a parity wait cannot tell phase k from phase k+2); it also
+            // makes O safe to rescale.
+            if (i > 0 && ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+            ok = __all_sync(kFull, ok);
             if (need_rescale && ok) {
-                // the context MMAs of tile i-1 must be complete before O is touched
-                ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
-                ok = __all_sync(kFull, ok);
-                if (ok) {
+                {
                     tc_fence_after();
 #pragma unroll 1
                     for (int m = 0; m < 4; ++m) {
@@ -923,10 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
+            // Consume o_done's phase i-1 (the context MMAs of tile i-1) at every tile,
+            // so that this wait and the epilogue's never trail the barrier by more than
+            // one phase (a parity wait cannot tell phase k from phase k+2); it also
+            // makes O safe to rescale.
+            if (i > 0 && ok) ok = wait_bar2(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+            ok = __all_sync(kFull, ok);
             if (need_rescale && ok) {
-                ok = wait_bar2(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
-                ok = __all_sync(kFull, ok);
-                if (ok) {
+                {
                     tc_fence_after();
 #pragma unroll 1
                     for (int m = 0; m < 4; ++m) {

@@ -70,7 +70,9 @@ def check(out, lse, ref, ref_lse, sel=None):
     assert np.all(out[empty] == 0) and np.all(np.isneginf(lse[empty]))
     ok = empty | (err <= bar)
     assert ok.all(), f"worst err/max|out| = {np.max(err[~empty] / np.abs(ref[~empty]).max(-1)):.3e}"
-    assert np.allclose(lse[~empty], ref_lse[~empty], rtol=0, atol=1e-4)
+    # lse is a log of a sum of exponentials of scores as large as ~|lse|; fp32 score
+    # accumulation leaves a relative error of a few 1e-7 of that magnitude
+    assert np.allclose(lse[~empty], ref_lse[~empty], rtol=2e-6, atol=1e-4)
     return float(np.max(err[~empty] / np.abs(ref[~empty]).max(-1))) if (~empty).any() else 0.0
 
 
