@@ -248,6 +248,25 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
 int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
                    size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream);
 
+/*
+ * kvq_mla_decode without a workspace argument.  The paper has no counterpart: this is a
+ * convenience of the library for callers that cannot allocate device memory when they
+ * decode, such as code running inside a memory pool or custom allocator that owns the
+ * whole device, a latency-critical loop that must not enter the allocator, or an
+ * embedding that only receives pre-placed input and output buffers.
+ *
+ * Same problem, outputs, status word and errors as kvq_mla_decode; the scratch comes
+ * from one fixed 64 MiB device array inside the library, which every GPU that loads the
+ * library holds until the process exits.  A problem whose kvq_mla_decode_workspace()
+ * exceeds 64 MiB is rejected with KVQ_EWORKSPACE (nothing launched).  The call allocates
+ * nothing.  Its first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture.  All calls share the
+ * array: calls that overlap on the GPU (several streams or host threads) race, so
+ * serialise them.  No scratch byte needs to be zero beforehand.
+ */
+int kvq_mla_decode_noalloc(const kvq_mla_problem* p, float* out, float* lse,
+                           uint32_t* dev_status, kvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ import threading
 __all__ = [
     "KvqError", "lib", "kvq_version", "kvq_tq4_codebook", "kvq_set_fault",
     "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
-    "kvq_mla_decode", "kvq_mla_decode_workspace", "MlaCache", "MlaProblem",
+    "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "MlaCache",
+    "MlaProblem",
     "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
     "DEV_BAD_FORMAT",
 ]
@@ -33,7 +34,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 # every symbol include/kvq.h declares
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_tq4_codebook", "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4",
-           "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode"]
+           "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode",
+           "kvq_mla_decode_noalloc"]
 
 
 class KvqError(RuntimeError):
@@ -110,6 +112,8 @@ def _declare(L):
     L.kvq_mla_decode_workspace.argtypes = [C.POINTER(MlaProblem)]
     L.kvq_mla_decode.restype = C.c_int
     L.kvq_mla_decode.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, C.c_size_t, _p, _p]
+    L.kvq_mla_decode_noalloc.restype = C.c_int
+    L.kvq_mla_decode_noalloc.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, _p]
 
 
 def _check(status: int):
@@ -237,3 +241,10 @@ def kvq_mla_decode(p: MlaProblem, out, lse=None, workspace=None, dev_status=None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().kvq_mla_decode(C.byref(p), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                 _ptr(dev_status), _stream(stream)))
+
+
+def kvq_mla_decode_noalloc(p: MlaProblem, out, lse=None, dev_status=None, stream=None) -> None:
+    """kvq_mla_decode with the library's fixed scratch array instead of a workspace, for
+    callers that cannot allocate device memory (see include/kvq.h)."""
+    _check(lib().kvq_mla_decode_noalloc(C.byref(p), _ptr(out), _ptr(lse), _ptr(dev_status),
+                                        _stream(stream)))

@@ -70,6 +70,15 @@ int cuda_status(cudaError_t e, const char* entry)
 
 }  // namespace
 
+int kvq::set_last_error(int status, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
 extern "C" {
 
 int kvq_version(void) { return 100; }

@@ -73,6 +73,9 @@ __device__ __forceinline__ void fwht_warp(float (&y)[VPL], int lane)
     }
 }
 
+// Record a one-line reason for kvq_last_error() and return `status`.
+int set_last_error(int status, const char* fmt, ...);
+
 // ---- launchers (host), each enqueues on `s` and returns the launch error ----------
 cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
                               uint8_t* codes, int64_t ldc, float* scales, cudaStream_t s);

@@ -1,0 +1,90 @@
+"""kvq_mla_decode_noalloc: the decode for callers that cannot allocate device memory
+(an allocator or memory pool that owns the device, a loop that must not enter the
+allocator, an embedding handed only pre-placed buffers).  Its scratch is a fixed device
+array inside the library, so it takes no workspace.  Checked through the C ABI against
+kvq_mla_decode with a caller workspace, on two different problems called one after the
+other (the second call reuses the array the first one left behind).
+
+This file is named to be collected last; it must pass on its own in a fresh process as
+well as after every other test."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_kv_cache_fp8_gb300 as k
+    return k
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def problem(kvq, orc, fmt, T, H, n_q, seed):
+    rows = W.magnitude_rows(T, seed=seed, lo=1e-2, hi=10.0)
+    signs = W.sign_bits(seed)
+    if fmt == kvq.FMT_FP8:
+        lat, ls = orc.encode_fp8(rows.c)
+    else:
+        lat, ls = orc.encode_tq4(rows.c, signs)
+    rope, rs = orc.encode_fp8(rows.k_rope)
+    cache = {k: dev(v) for k, v in dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs).items()}
+    q = W.queries(1, n_q, H, seed=seed)
+    kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=dev(signs))
+    return kvq.make_problem(seq_len=dev(np.array([T], np.int32)), q_lat=dev(q.q_lat),
+                            q_rope=dev(q.q_rope), sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt,
+                            causal=n_q > 1, **kw)
+
+
+def decode_both(kvq, p):
+    shape = (p.n_seq, p.n_q, p.n_heads)
+    ws = torch.empty(kvq.kvq_mla_decode_workspace(p), dtype=torch.uint8, device="cuda")
+    out_ref = torch.full(shape + (512,), np.nan, device="cuda")
+    lse_ref = torch.full(shape, np.nan, device="cuda")
+    kvq.kvq_mla_decode(p, out_ref, lse_ref, ws)
+    out = torch.full(shape + (512,), np.nan, device="cuda")
+    lse = torch.full(shape, np.nan, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_mla_decode_noalloc(p, out, lse, st)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy(), lse.cpu().numpy(), out_ref.cpu().numpy(), lse_ref.cpu().numpy(),
+            int(st.item()))
+
+
+def test_noalloc_matches_workspace_decode_twice(kvq, orc):
+    # two calls in a row, different problems and scratch footprints
+    for fmt, T, H, n_q, seed in ((kvq.FMT_TQ4, 32768, 64, 1, 0), (kvq.FMT_FP8, 5000, 16, 3, 1)):
+        p = problem(kvq, orc, fmt, T, H, n_q, seed)
+        out, lse, out_ref, lse_ref, st = decode_both(kvq, p)
+        assert st == 0
+        assert not np.isnan(out).any() and not np.isnan(lse).any()
+        err = np.abs(out - out_ref).max(axis=-1)
+        assert np.all(err <= 1e-4 * np.abs(out_ref).max(axis=-1))
+        assert np.allclose(lse, lse_ref, rtol=2e-6, atol=1e-4)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(kvq):
+    """A problem needing more than the fixed 64 MiB is refused before any launch."""
+    H, n_q, n_seq, T = 128, 4, 64, 65536
+    z = lambda *s: torch.zeros(*s, device="cuda")
+    planes = dict(lat=torch.zeros(16, 512, dtype=torch.uint8, device="cuda"), lat_scale=z(16),
+                  rope=torch.zeros(16, 64, dtype=torch.uint8, device="cuda"), rope_scale=z(16))
+    p = kvq.make_problem(seq_len=torch.full((n_seq,), T, dtype=torch.int32, device="cuda"),
+                         q_lat=z(n_seq, n_q, H, 512), q_rope=z(n_seq, n_q, H, 64), sm_scale=0.1,
+                         max_seq_len=T, fmt=kvq.FMT_FP8, fp8=planes, seq_stride_rows=T)
+    assert kvq.kvq_mla_decode_workspace(p) > (64 << 20)
+    out = torch.full((n_seq, n_q, H, 512), 7.0, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_mla_decode_noalloc(p, out)
+    assert e.value.status == 5
+    assert "scratch" in str(e.value)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
