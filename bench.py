@@ -290,7 +290,7 @@ def run_ours(args, world, rank, local):
     alg_bytes = T * ROW_BYTES_TQ4 + H * (512 + 64) * 4 + H * 512 * 4 + H * 4
     peak, peak_kind = peaks()
     achieved = alg_bytes / dec_launch_s / 1e9
-    traffic = profile_traffic("kvq_decode.cu")
+    traffic = profile_traffic("kvq_decode_tc.cu")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": peak_kind, "kernel": "kvq_mla_decode (TQ4, T=32768, H=64)",
