@@ -65,8 +65,10 @@ __device__ __forceinline__ int64_t pool_row(const kvq_mla_problem& p, int s, int
     return pid * p.page_size + t % p.page_size;
 }
 
+// e4m3 code -> value; the pattern S.1111.111 (never written by the encoder) reads as 0
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte)
 {
+    if ((byte & 0x7Fu) == 0x7Fu) return 0.0f;
     const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
     return __half2float(__half(hr));
 }

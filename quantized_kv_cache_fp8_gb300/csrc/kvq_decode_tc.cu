@@ -110,9 +110,11 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b)
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// four e4m3 codes (one 32-bit word) -> two half2 words (exact)
+// four e4m3 codes (one 32-bit word) -> two half2 words (exact); the pattern S.1111.111,
+// which the encoder never writes, reads as 0
 __device__ __forceinline__ void e4m3x4_to_half(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
+    w &= ~__vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
     const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
     const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
     lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
@@ -624,37 +626,52 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
 
 
 // ====================================================================================
-// Variant 2: the score's A operand (the dequantised rows) is written by the producer
-// threads straight into tensor memory (thread = row = TMEM lane) and read from there
-// by the MMA; only the context's V^T chunks go through shared memory.  S is single
-// buffered (the softmax frees it as soon as it has loaded its row), and the producer
-// keeps 4 chunks of raw codes in flight in registers.
+// Variant 3: the contractions and tensor-memory map of variant 2 with reorganised
+// producer and softmax roles.
+//  * Eight producer warps in two sets of four that convert alternate chunks, so two
+//    chains of ring waits, stores and arrivals run at once and every warp scheduler
+//    holds one warp of each set.  Raw codes are prefetched kPre3 of a set's chunks
+//    ahead in registers, with loads that skip L1 and let L2 fetch the surrounding 256
+//    bytes.
+//  * TQ4 codes decode without a table in memory: the codebook is symmetric, so code k
+//    is +m[k - 8] (k >= 8) or -m[7 - k], and the bytes of the 8 binary16 magnitudes
+//    m[j] sit in four registers that byte permutes (prmt) index by j.
+//  * The per-head maximum over a tile's rows is a transposing butterfly (31 shuffles
+//    per warp instead of 160); the running maxima live in shared memory, and the row
+//    sums of p are reduced the same way into one register per lane.
+//  * The Q image arrives by one bulk asynchronous copy while the first codes load.
 // TMEM: S lat 0..63, S rope 64..127, score-A ring 4 x 32 columns at 128.., O^T 256..511.
 // ====================================================================================
 constexpr int kRingA = 4;                // TMEM score-A slots (32 columns each)
 constexpr int kRingC = 6;                // shared-memory context slots (pairs adjacent)
-constexpr int kPre = 4;                  // chunks of raw codes in flight per thread
+constexpr int kPre3 = 2;                 // chunks of raw codes in flight per thread
 constexpr uint32_t kColA = 128;
-constexpr int k2OffQ = 0;
-constexpr int k2OffRing = k2OffQ + kQBytes;
-constexpr int k2OffP = k2OffRing + kRingC * kChunkBytes;
-constexpr int k2OffRed = k2OffP + 2 * kPBytes;
-constexpr int k2OffLut = k2OffRed + 4 * 32 * 4;
-constexpr int k2OffBar = k2OffLut + 256 * 4;
+constexpr int kThreads3 = 416;           // 8 producer, 4 softmax and 1 MMA warps
+constexpr int k3OffQ = 0;
+constexpr int k3OffRing = k3OffQ + kQBytes;
+constexpr int k3OffP = k3OffRing + kRingC * kChunkBytes;
+constexpr int k3OffRed = k3OffP + 2 * kPBytes;            // [4][32] f32
+constexpr int k3OffM = k3OffRed + 4 * 32 * 4;             // [32] running maxima
+constexpr int k3OffAlpha = k3OffM + 32 * 4;               // [32] rescale factors
+constexpr int k3OffFlag = k3OffAlpha + 32 * 4;            // some head rescales O
+constexpr int k3OffBar = k3OffFlag + 16;
 // full_a[4], empty_a[4], full_c[6], empty_c[6], s_full, s_empty, p_full[2], p_empty[2],
-// o_done, drain
-constexpr int k2NumBars = 2 * kRingA + 2 * kRingC + 8;
-constexpr int k2OffMisc = k2OffBar + k2NumBars * 8;
-constexpr int k2SmemBytes = k2OffMisc + 16 + 1024;
+// o_done, drain, q_full
+constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 9;
+constexpr int k3OffMisc = k3OffBar + k3NumBars * 8;
+constexpr int k3SmemBytes = k3OffMisc + 16 + 1024;
+static_assert(k3SmemBytes <= 227 * 1024, "shared memory");
 
-struct Shared2 {
+struct Shared3 {
     uint8_t* base;
-    __device__ uint8_t* q() const { return base + k2OffQ; }
-    __device__ uint8_t* slot(int i) const { return base + k2OffRing + i * kChunkBytes; }
-    __device__ uint8_t* pbuf(int b) const { return base + k2OffP + b * kPBytes; }
-    __device__ float* red() const { return reinterpret_cast<float*>(base + k2OffRed); }
-    __device__ uint32_t* lut() const { return reinterpret_cast<uint32_t*>(base + k2OffLut); }
-    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + k2OffBar) + i; }
+    __device__ uint8_t* q() const { return base + k3OffQ; }
+    __device__ uint8_t* slot(int i) const { return base + k3OffRing + i * kChunkBytes; }
+    __device__ uint8_t* pbuf(int b) const { return base + k3OffP + b * kPBytes; }
+    __device__ float* red() const { return reinterpret_cast<float*>(base + k3OffRed); }
+    __device__ float* m_run() const { return reinterpret_cast<float*>(base + k3OffM); }
+    __device__ float* alpha() const { return reinterpret_cast<float*>(base + k3OffAlpha); }
+    __device__ volatile int* flag() const { return reinterpret_cast<volatile int*>(base + k3OffFlag); }
+    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + k3OffBar) + i; }
     __device__ uint64_t* full_a(int i) const { return bar(i); }
     __device__ uint64_t* empty_a(int i) const { return bar(kRingA + i); }
     __device__ uint64_t* full_c(int i) const { return bar(2 * kRingA + i); }
@@ -665,11 +682,12 @@ struct Shared2 {
     __device__ uint64_t* p_empty(int b) const { return bar(2 * kRingA + 2 * kRingC + 4 + b); }
     __device__ uint64_t* o_done() const { return bar(2 * kRingA + 2 * kRingC + 6); }
     __device__ uint64_t* drain() const { return bar(2 * kRingA + 2 * kRingC + 7); }
-    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k2OffMisc); }
-    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k2OffMisc + 4); }
+    __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 8); }
+    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k3OffMisc); }
+    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k3OffMisc + 4); }
 };
 
-__device__ __forceinline__ bool wait_bar2(const Shared2& sh, uint64_t* bar, uint32_t parity,
+__device__ __forceinline__ bool wait_bar3(const Shared3& sh, uint64_t* bar, uint32_t parity,
                                           uint32_t* status)
 {
     if (mbar_try_wait(bar, parity)) return true;
@@ -685,75 +703,141 @@ __device__ __forceinline__ bool wait_bar2(const Shared2& sh, uint64_t* bar, uint
     return true;
 }
 
-// raw codes of one chunk of one row: fp8 (and every rope chunk) 64 bytes, TQ4 32 bytes
-struct RawChunk {
-    uint4 v[4];
-    bool valid;
+__device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 16 bytes of codes that are read once: not kept in L1, and L2 fetches the aligned
+// 256 bytes around them (the rest of the row's codes are read shortly after).
+__device__ __forceinline__ uint4 ld_codes(const uint8_t* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// The codebook is symmetric (code 15 - k is code k with the sign flipped) and its upper
+// half is positive; the byte tables below rely on both.
+constexpr bool tq4_codebook_symmetric()
+{
+    for (int k = 0; k < 8; ++k) {
+        if (kTq4CentroidBits[15 - k] != (kTq4CentroidBits[k] ^ 0x8000u)) return false;
+        if (kTq4CentroidBits[8 + k] & 0x8000u) return false;
+    }
+    return true;
+}
+static_assert(tq4_codebook_symmetric(), "TQ4 codebook must be symmetric");
+
+// byte `hi` (0: low byte, 1: high byte) of the binary16 magnitudes m[4*part .. 4*part+3]
+constexpr uint32_t tq4_mag_bytes(int hi, int part)
+{
+    uint32_t r = 0;
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t h = kTq4CentroidBits[8 + 4 * part + b];
+        r |= (hi ? (h >> 8) : (h & 0xFFu)) << (8 * b);
+    }
+    return r;
+}
+
+// eight TQ4 codes (code i in nibble i of w) -> four half2 words of centroids
+__device__ __forceinline__ void tq4x8_to_half(uint32_t w, uint32_t* h)
+{
+    constexpr uint32_t kL0 = tq4_mag_bytes(0, 0), kL1 = tq4_mag_bytes(0, 1);
+    constexpr uint32_t kH0 = tq4_mag_bytes(1, 0), kH1 = tq4_mag_bytes(1, 1);
+    const uint32_t pos = (w >> 3) & 0x11111111u;                        // 1: code >= 8
+    const uint32_t j = (w & 0x77777777u) ^ ((pos ^ 0x11111111u) * 7u);  // magnitude index
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t js = j >> (16 * q), ps = pos >> (16 * q);
+        const uint32_t lo = prmt(kL0, kL1, js);
+        const uint32_t hi = prmt(kH0, kH1, js) | prmt(0x80u, 0u, ps);   // sign bit 0x80
+        h[2 * q] = prmt(lo, hi, 0x5140u);
+        h[2 * q + 1] = prmt(lo, hi, 0x7362u);
+    }
+}
+
+// Item j of a producer set that converts the chunks of parity `par` (NS = its score
+// chunks per tile: 5 for parity 0 of ch = 0..8, 4 for parity 1).  The common order is,
+// per step i: S(i) chunks 0..8 if i < NT, then C(i-1) latent chunks 0..7 if i >= 1.
+struct OwnItem {
+    int tile, ch;
+    bool score;
 };
 
-__device__ __forceinline__ void load_raw(RawChunk& r, int64_t row, int ch, bool tq4,
-                                         const kvq_mla_cache& C)
+template <int NS>
+__device__ __forceinline__ int own_count(int NT) { return NS + (NT - 1) * (NS + 4) + 4; }
+
+template <int NS>
+__device__ __forceinline__ OwnItem own_item(int j, int par, int NT)
 {
-    r.valid = row >= 0;
-    if (!r.valid) return;
-    if (ch == 8 || !tq4) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(ch == 8 ? C.rope + row * kDRope
-                                                                 : C.lat + row * kDLat + ch * 64);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) r.v[v] = __ldg(s4 + v);
-    } else {
-        const uint4* s4 = reinterpret_cast<const uint4*>(C.lat + row * (kDLat / 2) + ch * 32);
-        r.v[0] = __ldg(s4);
-        r.v[1] = __ldg(s4 + 1);
+    OwnItem o;
+    if (j < NS) {
+        o.tile = 0; o.ch = 2 * j + par; o.score = true;
+        return o;
     }
+    constexpr int B = NS + 4;
+    const int jj = j - NS, i = 1 + jj / B, r = jj - (jj / B) * B;
+    if (i < NT && r < NS) {
+        o.tile = i; o.ch = 2 * r + par; o.score = true;
+    } else {
+        o.tile = i - 1; o.ch = 2 * (i < NT ? r - NS : r) + par; o.score = false;
+    }
+    return o;
 }
 
-// 64 fp16 values (32 half2 words, element pairs in order) of a raw chunk
-__device__ __forceinline__ void raw_to_half(const RawChunk& r, int ch, bool tq4, const uint32_t* lut,
-                                            uint32_t (&h)[32])
+// codes -> 32 fp16 values (half hq of a 64-code chunk): fp8 chunks hold 64 bytes in
+// raw[0..3], TQ4 chunks 32 bytes in raw[0..1]
+__device__ __forceinline__ void codes_to_half(const uint4 (&raw)[4], int hq, bool fp8, uint32_t (&h)[16])
 {
-    if (!r.valid) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) h[i] = 0;
-        return;
-    }
-    if (ch == 8 || !tq4) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            e4m3x4_to_half(r.v[v].x, h[8 * v + 0], h[8 * v + 1]);
-            e4m3x4_to_half(r.v[v].y, h[8 * v + 2], h[8 * v + 3]);
-            e4m3x4_to_half(r.v[v].z, h[8 * v + 4], h[8 * v + 5]);
-            e4m3x4_to_half(r.v[v].w, h[8 * v + 6], h[8 * v + 7]);
-        }
-    } else {
+    if (fp8) {
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
-            const uint32_t ww[4] = {r.v[v].x, r.v[v].y, r.v[v].z, r.v[v].w};
+            const uint4 w = raw[2 * hq + v];
+            e4m3x4_to_half(w.x, h[8 * v + 0], h[8 * v + 1]);
+            e4m3x4_to_half(w.y, h[8 * v + 2], h[8 * v + 3]);
+            e4m3x4_to_half(w.z, h[8 * v + 4], h[8 * v + 5]);
+            e4m3x4_to_half(w.w, h[8 * v + 6], h[8 * v + 7]);
+        }
+    } else {
+        const uint4 w = raw[hq];
+        tq4x8_to_half(w.x, h + 0);
+        tq4x8_to_half(w.y, h + 4);
+        tq4x8_to_half(w.z, h + 8);
+        tq4x8_to_half(w.w, h + 12);
+    }
+}
+
+// max (or sum) over the warp's 32 lanes of each of 32 values, transposed: on return
+// v[0] of lane l holds the result for value index l.
+template <bool kMax>
+__device__ __forceinline__ void warp_reduce_transpose(float (&v)[32], int lane)
+{
 #pragma unroll
-            for (int b = 0; b < 16; ++b) h[16 * v + b] = lut[(ww[b >> 2] >> (8 * (b & 3))) & 0xFF];
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int j = 0; j < w; ++j) {
+            const float send = up ? v[j] : v[j + w];
+            const float keep = up ? v[j + w] : v[j];
+            const float got = __shfl_xor_sync(kFull, send, w);
+            v[j] = kMax ? fmaxf(keep, got) : keep + got;
         }
     }
 }
 
-// item n of the producer / MMA order: per step i, S(i) (9 chunks) if i < NT, then
-// C(i-1) (8 latent chunks) if i >= 1
-__device__ __forceinline__ void item_of(int n, int NT, int& tile, int& ch, bool& score)
-{
-    if (n < 9) { tile = 0; ch = n; score = true; return; }
-    const int m = n - 9;
-    const int i = 1 + m / 17, j = m % 17;
-    if (i < NT) {
-        if (j < 9) { tile = i; ch = j; score = true; }
-        else { tile = i - 1; ch = j - 9; score = false; }
-    } else {
-        tile = NT - 1; ch = j; score = false;
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
+// 13 warps: warp w runs on sub-partition w % 4, so sub-partition 0 holds four warps and
+// its 16K registers cap every thread at 128
+__global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ TcArgs a)
 {
     extern __shared__ uint8_t dsm[];
-    Shared2 sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
+    Shared3 sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
     const kvq_mla_problem& p = a.p;
     const int split = blockIdx.x, s = blockIdx.y;
     const int q = blockIdx.z / a.n_hg, hg = blockIdx.z % a.n_hg;
@@ -780,124 +864,146 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
     const bool tq4 = fmt == KVQ_FMT_TQ4;
     const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
     const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
-    RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
+    const RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
 
-    if (tid == 0) {
-        for (int i = 0; i < kRingA; ++i) {
-            mbar_init(sh.full_a(i), 128);
-            mbar_init(sh.empty_a(i), 1);
+    if (warp == 12) {
+        if (lane == 0) {
+            for (int i = 0; i < kRingA; ++i) {
+                mbar_init(sh.full_a(i), 4);          // one arrival per warp of the owning set
+                mbar_init(sh.empty_a(i), 1);
+            }
+            for (int i = 0; i < kRingC; ++i) {
+                mbar_init(sh.full_c(i), 4);
+                mbar_init(sh.empty_c(i), 1);
+            }
+            mbar_init(sh.s_full(), 1);
+            mbar_init(sh.s_empty(), 4);              // one arrival per softmax warp
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(sh.p_full(b), 4);
+                mbar_init(sh.p_empty(b), 1);
+            }
+            mbar_init(sh.o_done(), 1);
+            mbar_init(sh.drain(), 1);
+            mbar_init(sh.q_full(), 1);
+            *sh.abort_flag() = 0;
+            fence_mbar_init();
+            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
+            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
+                          kQBytes, sh.q_full());
         }
-        for (int i = 0; i < kRingC; ++i) {
-            mbar_init(sh.full_c(i), 128);
-            mbar_init(sh.empty_c(i), 1);
-        }
-        mbar_init(sh.s_full(), 1);
-        mbar_init(sh.s_empty(), 128);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sh.p_full(b), 128);
-            mbar_init(sh.p_empty(b), 1);
-        }
-        mbar_init(sh.o_done(), 1);
-        mbar_init(sh.drain(), 1);
-        *sh.abort_flag() = 0;
-        fence_mbar_init();
-    }
-    if (warp == 8) {
+        __syncwarp();
         tmem_alloc(sh.tmem_base(), 512);
         tmem_relinquish();
     }
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes);
-        uint4* dst = reinterpret_cast<uint4*>(sh.q());
-        for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
-    }
-    fill_lut(sh.lut(), tid, kThreads);
-    fence_proxy_async_smem();
+    if (tid < kGQ) sh.m_run()[tid] = -INFINITY;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *sh.tmem_base();
     const int n_items = 17 * NT;
 
-    if (warp < 4) {
-        // ================================ producer =======================================
-        const int t = tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        int64_t row_cache[2] = {-1, -1};
-        int tile_cache[2] = {-1, -1};
-        auto row_of = [&](int tile) -> int64_t {
-            const int k = tile & 1;
-            if (tile_cache[k] != tile) {
-                tile_cache[k] = tile;
-                row_cache[k] = rc.row(r0 + (int64_t)tile * kRT + t, false);
+    if (warp < 8) {
+        // ================================ producers ======================================
+        // Two sets of four warps (thread = row).  Set k converts the chunks of parity k
+        // (score chunks ch = k, k + 2, ..; context chunks c = k, k + 2, ..) in the common
+        // order into ring slots that only it writes: score-A slots k and k + 2, context
+        // slots k, k + 2, k + 4, so the two chunks of a context M-tile sit in adjacent
+        // slots.  The two sets' chains of waits, stores and arrivals overlap.
+        const int set = warp >> 2;
+        const int t = (warp & 3) * 32 + lane;             // row within the tile
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int n_own = set == 0 ? own_count<5>(NT) : own_count<4>(NT);
+        int64_t row_c0 = -1, row_c1 = -1;                 // rows of the last two tiles
+        int tile_c0 = -1, tile_c1 = -1;
+        uint4 R[kPre3][4];
+        auto load = [&](uint4 (&r)[4], int j) {
+            const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
+            int64_t row;
+            if (it.tile == tile_c0) row = row_c0;
+            else if (it.tile == tile_c1) row = row_c1;
+            else {
+                row = rc.row(r0 + (int64_t)it.tile * kRT + t, false);
+                if (it.tile & 1) { tile_c1 = it.tile; row_c1 = row; }
+                else { tile_c0 = it.tile; row_c0 = row; }
             }
-            return row_cache[k];
+            if (row < 0) {
+                r[0] = r[1] = r[2] = r[3] = make_uint4(0u, 0u, 0u, 0u);
+            } else if (it.ch == 8 || !tq4) {
+                const uint8_t* src = it.ch == 8 ? C.rope + row * kDRope : C.lat + row * kDLat + it.ch * 64;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) r[v] = ld_codes(src + 16 * v);
+            } else {
+                const uint8_t* src = C.lat + row * (kDLat / 2) + it.ch * 32;
+                r[0] = ld_codes(src);
+                r[1] = ld_codes(src + 16);
+            }
         };
-        RawChunk R[kPre];
 #pragma unroll
-        for (int u = 0; u < kPre; ++u) {
-            R[u].valid = false;
-            if (u < n_items) {
-                int tile, ch; bool sc;
-                item_of(u, NT, tile, ch, sc);
-                load_raw(R[u], row_of(tile), ch, tq4, C);
-            }
-        }
-        int a_cnt = 0, c_cnt = 0;
+        for (int u = 0; u < kPre3; ++u)
+            if (u < n_own) load(R[u], u);
+        int a_ord = 0, c_ord = 0;
         bool ok = true;
-        for (int n0 = 0; n0 < n_items && ok; n0 += kPre) {
+        for (int j0 = 0; j0 < n_own && ok; j0 += kPre3) {
 #pragma unroll
-            for (int u = 0; u < kPre; ++u) {
-                const int n = n0 + u;
-                if (n >= n_items || !ok) break;
-                int tile, ch; bool sc;
-                item_of(n, NT, tile, ch, sc);
-                uint32_t h[32];
-                raw_to_half(R[u], ch, tq4, sh.lut(), h);
-                if (sc) {
-                    const int slot = a_cnt % kRingA;
-                    ok = wait_bar2(sh, sh.empty_a(slot), ((uint32_t)(a_cnt / kRingA) & 1u) ^ 1u, a.status);
+            for (int u = 0; u < kPre3; ++u) {
+                const int j = j0 + u;
+                if (j >= n_own) break;
+                const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
+                const uint4 raw[4] = {R[u][0], R[u][1], R[u][2], R[u][3]};
+                if (j + kPre3 < n_own) load(R[u], j + kPre3);
+                const bool fp8 = it.ch == 8 || !tq4;
+                if (it.score) {
+                    const int slot = set + 2 * (a_ord & 1);
+                    ok = wait_bar3(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
                     ok = __all_sync(kFull, ok);
                     if (!ok) break;
                     tc_fence_after();
-                    tmem_st_x32(tmem + lane_base + kColA + 32 * slot, h);
+#pragma unroll
+                    for (int hq = 0; hq < 2; ++hq) {
+                        uint32_t h[16];
+                        codes_to_half(raw, hq, fp8, h);
+                        tmem_st_x16(tmem + lane_base + kColA + 32 * slot + 16 * hq, h);
+                    }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(sh.full_a(slot));
-                    ++a_cnt;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sh.full_a(slot));
+                    ++a_ord;
                 } else {
-                    const int slot = c_cnt % kRingC;
-                    ok = wait_bar2(sh, sh.empty_c(slot), ((uint32_t)(c_cnt / kRingC) & 1u) ^ 1u, a.status);
+                    const int slot = 2 * (c_ord % 3) + set;
+                    ok = wait_bar3(sh, sh.empty_c(slot), ((uint32_t)(c_ord / 3) & 1u) ^ 1u, a.status);
                     ok = __all_sync(kFull, ok);
                     if (!ok) break;
                     uint8_t* dst = sh.slot(slot);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(dst + sw128(t, c)) =
-                            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    for (int hq = 0; hq < 2; ++hq) {
+                        uint32_t h[16];
+                        codes_to_half(raw, hq, fp8, h);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(dst + sw128(t, 4 * hq + c)) =
+                                make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    }
                     fence_proxy_async_smem();
-                    mbar_arrive(sh.full_c(slot));
-                    ++c_cnt;
-                }
-                if (n + kPre < n_items) {
-                    int tile2, ch2; bool sc2;
-                    item_of(n + kPre, NT, tile2, ch2, sc2);
-                    load_raw(R[u], row_of(tile2), ch2, tq4, C);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sh.full_c(slot));
+                    ++c_ord;
                 }
             }
         }
-    } else if (warp < 8) {
+    } else if (warp < 12) {
         // ================================ softmax ========================================
-        const int t = tid - 128;
-        const int wq = warp - 4;
+        // Control flow is identical in all 128 threads (the named barriers need every one
+        // of them); `ok` only guards work and is kept warp-uniform.
+        const int t = tid - 256;                      // row within the tile
+        const int wq = warp - 8;                      // TMEM lane quarter
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const float tau2 = p.sm_scale * kLog2e;
         const float c512 = tq4_inv_sqrt(kDLat);
         float* red = sh.red();
-        float m_run[kGQ], l_part[kGQ];
-#pragma unroll
-        for (int g = 0; g < kGQ; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.0f; }
+        float* m_s = sh.m_run();
+        float* alpha_s = sh.alpha();
+        float l_lane = 0.0f;                          // sum of p over this warp's rows, head `lane`
         bool ok = true;
         for (int i = 0; i < NT; ++i) {
             const int b = i & 1;
@@ -907,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                 sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
                 sc_rope = C.rope_scale[row];
             }
-            if (ok) ok = wait_bar2(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
+            if (ok) ok = wait_bar3(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
             ok = __all_sync(kFull, ok);
             float sv[kGQ];
 #pragma unroll
@@ -926,75 +1032,90 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                                                         sc_rope * __uint_as_float(y[e]));
                 }
                 tc_fence_before();
-                mbar_arrive(sh.s_empty());
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sh.s_empty());
             }
 #pragma unroll
             for (int g = 0; g < kGQ; ++g) sv[g] = (row >= 0 && ok) ? sv[g] * tau2 : -INFINITY;
+            {
+                float mx[kGQ];
 #pragma unroll
-            for (int g = 0; g < kGQ; ++g) {
-                float v = sv[g];
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-                if (lane == 0) red[wq * 32 + g] = v;
+                for (int g = 0; g < kGQ; ++g) mx[g] = sv[g];
+                warp_reduce_transpose<true>(mx, lane);
+                red[wq * 32 + lane] = mx[0];
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            bool need_rescale = false;
-            float alpha[kGQ];
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) {
-                const float tm = fmaxf(fmaxf(red[g], red[32 + g]), fmaxf(red[64 + g], red[96 + g]));
-                alpha[g] = 1.0f;
-                if (tm > m_run[g] + kLazy || (m_run[g] == -INFINITY && tm > -INFINITY)) {
-                    alpha[g] = (m_run[g] == -INFINITY) ? 0.0f : exp2f(m_run[g] - tm);
-                    m_run[g] = tm;
-                    if (i > 0) need_rescale = true;
+            named_bar_softmax();
+            if (wq == 0) {
+                const float tm = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
+                const float mo = m_s[lane];
+                float al = 1.0f;
+                bool resc = false;
+                if (tm > mo + kLazy || (mo == -INFINITY && tm > -INFINITY)) {
+                    al = (mo == -INFINITY) ? 0.0f : exp2f(mo - tm);
+                    m_s[lane] = tm;
+                    resc = i > 0;
                 }
+                alpha_s[lane] = al;
+                const bool any = __any_sync(kFull, resc);
+                if (lane == 0) *sh.flag() = any ? 1 : 0;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_softmax();
+            const bool need_rescale = *sh.flag() != 0;
             // Consume o_done's phase i-1 (the context MMAs of tile i-1) at every tile,
             // so that this wait and the epilogue's never trail the barrier by more than
             // one phase (a parity wait cannot tell phase k from phase k+2); it also
             // makes O safe to rescale.
-            if (i > 0 && ok) ok = wait_bar2(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+            if (i > 0 && ok) ok = wait_bar3(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
             ok = __all_sync(kFull, ok);
-            if (need_rescale && ok) {
-                {
+            if (need_rescale) {
+                l_lane *= alpha_s[lane];
+                if (ok) {
                     tc_fence_after();
 #pragma unroll 1
                     for (int m = 0; m < 4; ++m) {
-#pragma unroll
+#pragma unroll 1
                         for (int c = 0; c < kN; c += 16) {
                             uint32_t x[16];
                             tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha[(c + e) & (kGQ - 1)]);
+                            for (int e = 0; e < 16; e += 4) {
+                                const float4 al = *reinterpret_cast<const float4*>(alpha_s + ((c + e) & (kGQ - 1)));
+                                x[e] = __float_as_uint(__uint_as_float(x[e]) * al.x);
+                                x[e + 1] = __float_as_uint(__uint_as_float(x[e + 1]) * al.y);
+                                x[e + 2] = __float_as_uint(__uint_as_float(x[e + 2]) * al.z);
+                                x[e + 3] = __float_as_uint(__uint_as_float(x[e + 3]) * al.w);
+                            }
                             tmem_st_x16(tmem + lane_base + kColO + 64 * m + c, x);
                         }
                     }
                     tmem_st_wait();
                 }
             }
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) l_part[g] *= alpha[g];
+            // weights: p = 2^(s - m), w = p * latent scale, split hi | lo
             uint32_t wh[kGQ / 2], wl[kGQ / 2];
 #pragma unroll
-            for (int g = 0; g < kGQ; g += 2) {
-                const float p0 = sv[g] == -INFINITY ? 0.0f : exp2f(sv[g] - m_run[g]);
-                const float p1 = sv[g + 1] == -INFINITY ? 0.0f : exp2f(sv[g + 1] - m_run[g + 1]);
-                l_part[g] += p0;
-                l_part[g + 1] += p1;
-                const float w0 = p0 * sc_lat, w1 = p1 * sc_lat;
-                const __half2 hi = __floats2half2_rn(w0, w1);
-                const float2 hf = __half22float2(hi);
-                const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
-                wh[g / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-                wl[g / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            for (int g = 0; g < kGQ; g += 4) {
+                const float4 mv = *reinterpret_cast<const float4*>(m_s + g);
+                const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float p0 = sv[g + e] == -INFINITY ? 0.0f : exp2f(sv[g + e] - mm[e]);
+                    const float p1 = sv[g + e + 1] == -INFINITY ? 0.0f : exp2f(sv[g + e + 1] - mm[e + 1]);
+                    sv[g + e] = p0;
+                    sv[g + e + 1] = p1;
+                    const float w0 = p0 * sc_lat, w1 = p1 * sc_lat;
+                    const __half2 hi = __floats2half2_rn(w0, w1);
+                    const float2 hf = __half22float2(hi);
+                    const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
+                    wh[(g + e) / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                    wl[(g + e) / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
             }
-            if (ok && i >= 2) ok = wait_bar2(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
+            if (ok && i >= 2) ok = wait_bar3(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
             if (ok) {
                 uint8_t* pb = sh.pbuf(b);
+                // row t of W^T: 64 fp16, chunks 0..3 the hi halves, 4..7 the lo halves
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     *reinterpret_cast<uint4*>(pb + sw128(t, c)) =
@@ -1003,29 +1124,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                         make_uint4(wl[4 * c], wl[4 * c + 1], wl[4 * c + 2], wl[4 * c + 3]);
                 }
                 fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(sh.p_full(b));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sh.p_full(b));
             }
+            warp_reduce_transpose<false>(sv, lane);
+            l_lane += sv[0];
         }
-        if (ok) ok = wait_bar2(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
+        // ---- epilogue: l over the 128 rows, O^T -> partials ------------------------------
+        if (ok) ok = wait_bar3(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
         ok = __all_sync(kFull, ok);
-#pragma unroll
-        for (int g = 0; g < kGQ; ++g) {
-            float v = l_part[g];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-            if (lane == 0) red[wq * 32 + g] = v;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        red[wq * 32 + lane] = l_lane;
+        named_bar_softmax();
         if (ok) {
             tc_fence_after();
             if (t < nh) {
                 const float lt = red[t] + red[32 + t] + red[64 + t] + red[96 + t];
                 const int64_t sl = (qrow + h0 + t) * a.n_splits + split;
-                float mt = m_run[0];
-#pragma unroll
-                for (int g = 1; g < kGQ; ++g) if (g == t) mt = m_run[g];
-                a.part_ml[sl * 2] = mt;
+                a.part_ml[sl * 2] = m_s[t];
                 a.part_ml[sl * 2 + 1] = lt;
             }
 #pragma unroll 1
@@ -1050,18 +1165,20 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
     } else {
         // ================================ MMA issuer =====================================
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);
-            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);
+            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
+            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
             const uint32_t q_base = smem_u32(sh.q());
-            int a_cnt = 0, c_cnt = 0;
-            bool ok = true;
+            bool ok = wait_bar3(sh, sh.q_full(), 0u, a.status);
+            tc_fence_after();
             for (int i = 0; i <= NT && ok; ++i) {
                 if (i < NT) {
-                    if (i >= 1 && !(ok = wait_bar2(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status))) break;
+                    if (i >= 1 && !(ok = wait_bar3(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status))) break;
                     tc_fence_after();
                     for (int ch = 0; ch < 9 && ok; ++ch) {
-                        const int slot = a_cnt % kRingA;
-                        if (!(ok = wait_bar2(sh, sh.full_a(slot), (uint32_t)(a_cnt / kRingA) & 1u, a.status))) break;
+                        // chunk ch comes from producer set ch & 1: its ord-th score chunk
+                        const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
+                        const int slot = (ch & 1) + 2 * (ord & 1);
+                        if (!(ok = wait_bar3(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status))) break;
                         tc_fence_after();
                         const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
 #pragma unroll
@@ -1070,20 +1187,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                                        desc_sw128(q_base + ch * kQSlabBytes + 32 * ks, 1024), idesc_s,
                                        (ch == 0 || ch == 8) ? (ks > 0) : 1u);
                         mma_commit(sh.empty_a(slot));
-                        ++a_cnt;
                     }
                     if (!ok) break;
                     mma_commit(sh.s_full());
                 }
                 if (i >= 1) {
                     const int tile = i - 1, b = tile & 1;
-                    if (!(ok = wait_bar2(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
+                    if (!(ok = wait_bar3(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
                     tc_fence_after();
                     for (int c = 0; c < 8 && ok; ++c) {
-                        const int slot = c_cnt % kRingC;
-                        if (!(ok = wait_bar2(sh, sh.full_c(slot), (uint32_t)(c_cnt / kRingC) & 1u, a.status))) break;
+                        // chunk c comes from set c & 1: its ord-th context chunk, in slot
+                        // 2 (ord % 3) + (c & 1), next to its M-tile partner
+                        const int ord = 4 * tile + (c >> 1);
+                        const int slot = 2 * (ord % 3) + (c & 1);
+                        if (!(ok = wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord / 3) & 1u, a.status))) break;
                         tc_fence_after();
                         if (c & 1) {
+                            // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
                             const int m = c >> 1;
                             const uint32_t a_base = smem_u32(sh.slot(slot - 1));
                             const uint32_t p_base = smem_u32(sh.pbuf(b));
@@ -1096,15 +1216,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
                             mma_commit(sh.empty_c(slot - 1));
                             mma_commit(sh.empty_c(slot));
                         }
-                        ++c_cnt;
                     }
                     if (!ok) break;
                     mma_commit(sh.p_empty(b));
                     mma_commit(sh.o_done());
                 }
             }
+            // drain: every MMA issued so far completes before tensor memory is freed, and
+            // the Q copy has landed before the CTA's shared memory is released
             mma_commit(sh.drain());
             if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
+                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+            if (!mbar_wait(sh.q_full(), 0, kTimeoutNs) && a.status)
                 atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
         }
         __syncwarp();
@@ -1112,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc2_kernel(TcArgs a)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == 12) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1132,7 +1255,7 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s)
 {
-    const bool v2 = p.impl == 3;
+    const bool v3 = p.impl == 3;
     TcArgs a;
     a.p = p;
     a.split_rows = plan.split_rows;
@@ -1154,13 +1277,13 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
         e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mla_decode_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 k2SmemBytes);
+        e = cudaFuncSetAttribute(mla_decode_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k3SmemBytes);
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    if (v2) mla_decode_tc2_kernel<<<grid, kThreads, k2SmemBytes, s>>>(a);
+    if (v3) mla_decode_tc3_kernel<<<grid, kThreads3, k3SmemBytes, s>>>(a);
     else mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }

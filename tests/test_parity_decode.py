@@ -12,7 +12,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-IMPLS = pytest.mark.parametrize("impl", [1, 2], ids=["cudacore", "tcgen05"])
+IMPLS = pytest.mark.parametrize("impl", [1, 2, 3], ids=["cudacore", "tcgen05", "tcgen05v3"])
 
 
 @pytest.fixture(scope="module")
@@ -102,6 +102,24 @@ def test_decode_fp8_tiny_workload(kvq, orc, impl):
     out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[1024], q=q)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[1024], seq_fmt=[1], q_lat=q.q_lat,
                                      q_rope=q.q_rope, sm_scale=W.SM_SCALE, fp8=cache)
+    check(out, lse, ref, ref_lse)
+
+
+@IMPLS
+def test_decode_fp8_unwritten_pattern_reads_zero(kvq, orc, impl):
+    """The e4m3 pattern S.1111.111, which the encoder never writes, reads back as 0 in
+    the latent and the rope parts alike (planted into about 5% of the codes)."""
+    T = 700
+    rows = W.unit_rows(T, seed=5)
+    cache = encode(orc, rows, 1)
+    for i, key in enumerate(("lat", "rope")):
+        mask, val = W.planted_codes(cache[key].shape, 0.05, seed=5 + i)
+        cache[key] = np.where(mask, val, cache[key])
+    q = W.queries(1, 1, 16, seed=5)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=[T], q=q)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, fp8=cache)
+    assert st == 0
     check(out, lse, ref, ref_lse)
 
 

@@ -106,6 +106,15 @@ def sparse_indices(T: int, k: int, n: int, seed: int) -> np.ndarray:
     return np.stack([g.choice(T, size=k, replace=False) for _ in range(n)]).astype(np.int32)
 
 
+def planted_codes(shape, frac: float, seed: int):
+    """A mask of about `frac` of the entries of `shape` and, for each entry, one of the
+    two e4m3 bytes S.1111.111 (0x7F, 0xFF) that no encoder writes, for planting into
+    an encoded cache."""
+    g = rng(seed + 15485863)
+    mask = g.random(shape) < frac
+    return mask, np.where(g.random(shape) < 0.5, 0x7F, 0xFF).astype(np.uint8)
+
+
 @dataclass
 class Q4Workload:
     k: np.ndarray            # [n_seq][n_tok][n_heads][256] fp32
