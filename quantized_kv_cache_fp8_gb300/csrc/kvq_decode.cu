@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 {
-    constexpr int kMaxW = 1024;                   // splits combined per pass of weights
-    __shared__ float s_w[kMaxW];
+    constexpr int kBatch = 64;                    // splits whose partials load at once
+    __shared__ float s_w[kBatch];
     __shared__ __align__(16) float s_part[4][kDLat];
     __shared__ float s_red[2][16];
     const kvq_mla_problem& p = a.p;
@@ -304,37 +304,60 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
     const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
     const float* ml = a.part_ml + r * a.n_splits * 2;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o + r * a.n_splits * kDLat) + j;
+    // the partials come from the decode kernel launched just before this one
+    grid_dependency_wait();
+    // the first batch of partials is requested before the maxima are known; splits
+    // with l = 0 (no admissible row) may hold stale values and get weight 0 below
+    float4 v[kBatch / 4];
+#pragma unroll
+    for (int i = 0; i < kBatch / 4; ++i) {
+        const int S = grp + 4 * i;
+        v[i] = S < ns ? po[(int64_t)S * (kDLat / 4)] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     float M = -INFINITY;
-    for (int S = tid; S < ns; S += 512)
-        if (ml[2 * S + 1] > 0.0f) M = fmaxf(M, ml[2 * S]);
+    float2 mine = make_float2(-INFINITY, 0.0f);   // (m, l) of split tid
+    for (int S = tid; S < ns; S += 512) {
+        const float2 x = reinterpret_cast<const float2*>(ml)[S];
+        if (S == tid) mine = x;
+        if (x.y > 0.0f) M = fmaxf(M, x.x);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     if (lane == 0) s_red[0][warp] = M;
     __syncthreads();
     M = s_red[0][0];
+#pragma unroll
     for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float Lpart = 0.0f;
-    for (int S0 = 0; S0 < ns; S0 += kMaxW) {
-        const int nw = min(kMaxW, ns - S0);
-        __syncthreads();
-        for (int S = tid; S < nw; S += 512) {
-            const float lS = ml[2 * (S0 + S) + 1];
-            const float w = lS > 0.0f ? exp2f(ml[2 * (S0 + S)] - M) : 0.0f;
-            s_w[S] = w;
-            Lpart += lS > 0.0f ? lS * w : 0.0f;
+    for (int S0 = 0; S0 < ns; S0 += kBatch) {
+        const int nb = min(kBatch, ns - S0);
+        if (S0 > 0) {
+            __syncthreads();                      // s_w of the previous batch is consumed
+#pragma unroll
+            for (int i = 0; i < kBatch / 4; ++i) {
+                const int S = grp + 4 * i;
+                v[i] = S < nb ? po[(int64_t)(S0 + S) * (kDLat / 4)] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+        if (tid < nb) {
+            const float2 x = (S0 + tid < 512) && S0 == 0 ? mine
+                                                          : reinterpret_cast<const float2*>(ml)[S0 + tid];
+            const float w = x.y > 0.0f ? exp2f(x.x - M) : 0.0f;
+            s_w[tid] = w;
+            Lpart += w > 0.0f ? x.y * w : 0.0f;
         }
         __syncthreads();
-        const float4* po = reinterpret_cast<const float4*>(a.part_o + (r * a.n_splits + S0) * kDLat) + j;
-#pragma unroll 8
-        for (int S = grp; S < nw; S += 4) {
-            const float w = s_w[S];
+#pragma unroll
+        for (int i = 0; i < kBatch / 4; ++i) {
+            const int S = grp + 4 * i;
+            const float w = S < nb ? s_w[S] : 0.0f;
             if (w != 0.0f) {
-                const float4 v = po[(int64_t)S * (kDLat / 4)];
-                acc.x = fmaf(v.x, w, acc.x);
-                acc.y = fmaf(v.y, w, acc.y);
-                acc.z = fmaf(v.z, w, acc.z);
-                acc.w = fmaf(v.w, w, acc.w);
+                acc.x = fmaf(v[i].x, w, acc.x);
+                acc.y = fmaf(v[i].y, w, acc.y);
+                acc.z = fmaf(v[i].z, w, acc.z);
+                acc.w = fmaf(v[i].w, w, acc.w);
             }
         }
     }
@@ -344,27 +367,29 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     if (lane == 0) s_red[1][warp] = Lpart;
     __syncthreads();
     float Lt = 0.0f;
+#pragma unroll
     for (int w = 0; w < 16; ++w) Lt += s_red[1][w];
     const bool empty = !(Lt > 0.0f);
     // thread tid owns output dim tid from here on
     float res = s_part[0][tid] + s_part[1][tid] + s_part[2][tid] + s_part[3][tid];
     res = empty ? 0.0f : res / Lt;
     if (fmt == KVQ_FMT_TQ4) {
-        __syncthreads();
+        // unrotate: (1/sqrt 512) s (.) FWHT_512(out); stages h < 32 within the warp,
+        // h >= 32 through shared memory
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+            const float o = __shfl_xor_sync(kFull, res, h);
+            res = (tid & h) ? o - res : res + o;
+        }
         float* s_o = s_part[0];
-        s_o[tid] = res;
-        __syncthreads();
-        for (int h = 1; h < kDLat; h <<= 1) {
-            if (tid < kDLat / 2) {
-                const int i = (tid / h) * 2 * h + (tid % h);
-                const float x = s_o[i], y = s_o[i + h];
-                s_o[i] = x + y;
-                s_o[i + h] = x - y;
-            }
+        for (int h = 32; h < kDLat; h <<= 1) {
             __syncthreads();
+            s_o[tid] = res;
+            __syncthreads();
+            res = (tid & h) ? s_o[tid - h] - res : res + s_o[tid + h];
         }
         const bool ng = (p.tq4_signs[tid >> 5] >> (tid & 31)) & 1u;
-        res = s_o[tid] * tq4_inv_sqrt(kDLat) * (ng ? -1.0f : 1.0f);
+        res = res * tq4_inv_sqrt(kDLat) * (ng ? -1.0f : 1.0f);
     }
     a.out[r * kDLat + tid] = res;
     if (tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
@@ -453,8 +478,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
         cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,
                                              a.part_o, dev_status, s);
         if (e != cudaSuccess) return e;
-        mla_combine_kernel<<<(unsigned)rows, 512, 0, s>>>(a);
-        return cudaGetLastError();
+        return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
     }
     const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
                         + kRT * sizeof(int) + 16 * sizeof(float);
@@ -471,8 +495,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hblk);
     mla_decode_simt_kernel<<<grid, kThreads, smem, s>>>(a);
-    mla_combine_kernel<<<(unsigned)rows, 512, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
 }
 
 }  // namespace kvq

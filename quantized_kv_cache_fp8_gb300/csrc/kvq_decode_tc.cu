@@ -129,6 +129,7 @@ __device__ __forceinline__ void e4m3x4_to_half(uint32_t w, uint32_t& lo, uint32_
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
 {
+    grid_dependents_launch();                    // the decode may start loading codes
     const kvq_mla_problem& p = a.p;
     const int lane = threadIdx.x & 31;
     const int64_t n_items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
@@ -851,6 +852,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
     const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
     const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
     const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
+    grid_dependents_launch();                    // the combine may start launching
 
     if (r0 >= n_cand || bad_fmt) {
         if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
@@ -887,9 +889,6 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             mbar_init(sh.q_full(), 1);
             *sh.abort_flag() = 0;
             fence_mbar_init();
-            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
-            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
-                          kQBytes, sh.q_full());
         }
         __syncwarp();
         tmem_alloc(sh.tmem_base(), 512);
@@ -1168,6 +1167,11 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
             const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
             const uint32_t q_base = smem_u32(sh.q());
+            // the Q image is written by the kernel launched just before this one
+            grid_dependency_wait();
+            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
+            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
+                          kQBytes, sh.q_full());
             bool ok = wait_bar3(sh, sh.q_full(), 0u, a.status);
             tc_fence_after();
             for (int i = 0; i <= NT && ok; ++i) {
@@ -1283,7 +1287,7 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
         attr_set.fetch_or(bit);
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    if (v3) mla_decode_tc3_kernel<<<grid, kThreads3, k3SmemBytes, s>>>(a);
+    if (v3) return launch_dependent(mla_decode_tc3_kernel, grid, dim3(kThreads3), k3SmemBytes, s, a);
     else mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 
 #include "kvq.h"
 
@@ -71,6 +72,32 @@ __device__ __forceinline__ void fwht_warp(float (&y)[VPL], int lane)
             }
         }
     }
+}
+
+// ---- dependent launches ----------------------------------------------------------------
+// A kernel launched by launch_dependent() may start while the kernel before it in the
+// stream is still running; before it touches that kernel's output it calls
+// grid_dependency_wait(), which returns once the earlier kernel has completed and its
+// writes are visible.  A kernel calls grid_dependents_launch() to let the next kernel
+// start early.  Both are no-ops when no such launch is involved.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Record a one-line reason for kvq_last_error() and return `status`.
