@@ -631,9 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
 // producer and softmax roles.
 //  * Eight producer warps in two sets of four that convert alternate chunks, so two
 //    chains of ring waits, stores and arrivals run at once and every warp scheduler
-//    holds one warp of each set.  Raw codes are prefetched kPre3 of a set's chunks
-//    ahead in registers, with loads that skip L1 and let L2 fetch the surrounding 256
-//    bytes.
+//    holds one warp of each set.  Raw codes of a set's next kStages chunks are in
+//    flight at any time as asynchronous global -> shared copies (cp.async, no
+//    registers held), with an L2 hint that fetches the surrounding 256 bytes.
+//  * W (the context operand) is single-buffered: the softmax writes W(i) only after
+//    the context MMAs of tile i-1, which read W(i-1), have completed.
 //  * TQ4 codes decode without a table in memory: the codebook is symmetric, so code k
 //    is +m[k - 8] (k >= 8) or -m[7 - k], and the bytes of the 8 binary16 magnitudes
 //    m[j] sit in four registers that byte permutes (prmt) index by j.
@@ -644,21 +646,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
 // TMEM: S lat 0..63, S rope 64..127, score-A ring 4 x 32 columns at 128.., O^T 256..511.
 // ====================================================================================
 constexpr int kRingA = 4;                // TMEM score-A slots (32 columns each)
-constexpr int kRingC = 6;                // shared-memory context slots (pairs adjacent)
-constexpr int kPre3 = 2;                 // chunks of raw codes in flight per thread
+constexpr int kRingC = 4;                // shared-memory context slots (pairs adjacent)
+constexpr int kStages = 4;               // raw-code stages in flight per producer set
+constexpr int kStageBytes = kRT * 64;    // one chunk of raw codes, [4 pieces][128 rows][16 B]
 constexpr uint32_t kColA = 128;
 constexpr int kThreads3 = 416;           // 8 producer, 4 softmax and 1 MMA warps
 constexpr int k3OffQ = 0;
 constexpr int k3OffRing = k3OffQ + kQBytes;
 constexpr int k3OffP = k3OffRing + kRingC * kChunkBytes;
-constexpr int k3OffRed = k3OffP + 2 * kPBytes;            // [4][32] f32
+constexpr int k3OffStage = k3OffP + kPBytes;
+constexpr int k3OffRed = k3OffStage + 2 * kStages * kStageBytes;   // [4][32] f32
 constexpr int k3OffM = k3OffRed + 4 * 32 * 4;             // [32] running maxima
 constexpr int k3OffAlpha = k3OffM + 32 * 4;               // [32] rescale factors
 constexpr int k3OffFlag = k3OffAlpha + 32 * 4;            // some head rescales O
 constexpr int k3OffBar = k3OffFlag + 16;
-// full_a[4], empty_a[4], full_c[6], empty_c[6], s_full, s_empty, p_full[2], p_empty[2],
-// o_done, drain, q_full
-constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 9;
+// full_a[4], empty_a[4], full_c[4], empty_c[4], s_full, s_empty, p_full, o_done, drain,
+// q_full
+constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 6;
 constexpr int k3OffMisc = k3OffBar + k3NumBars * 8;
 constexpr int k3SmemBytes = k3OffMisc + 16 + 1024;
 static_assert(k3SmemBytes <= 227 * 1024, "shared memory");
@@ -667,7 +671,8 @@ struct Shared3 {
     uint8_t* base;
     __device__ uint8_t* q() const { return base + k3OffQ; }
     __device__ uint8_t* slot(int i) const { return base + k3OffRing + i * kChunkBytes; }
-    __device__ uint8_t* pbuf(int b) const { return base + k3OffP + b * kPBytes; }
+    __device__ uint8_t* pbuf() const { return base + k3OffP; }
+    __device__ uint8_t* stage(int set, int d) const { return base + k3OffStage + (set * kStages + d) * kStageBytes; }
     __device__ float* red() const { return reinterpret_cast<float*>(base + k3OffRed); }
     __device__ float* m_run() const { return reinterpret_cast<float*>(base + k3OffM); }
     __device__ float* alpha() const { return reinterpret_cast<float*>(base + k3OffAlpha); }
@@ -679,11 +684,10 @@ struct Shared3 {
     __device__ uint64_t* empty_c(int i) const { return bar(2 * kRingA + kRingC + i); }
     __device__ uint64_t* s_full() const { return bar(2 * kRingA + 2 * kRingC); }
     __device__ uint64_t* s_empty() const { return bar(2 * kRingA + 2 * kRingC + 1); }
-    __device__ uint64_t* p_full(int b) const { return bar(2 * kRingA + 2 * kRingC + 2 + b); }
-    __device__ uint64_t* p_empty(int b) const { return bar(2 * kRingA + 2 * kRingC + 4 + b); }
-    __device__ uint64_t* o_done() const { return bar(2 * kRingA + 2 * kRingC + 6); }
-    __device__ uint64_t* drain() const { return bar(2 * kRingA + 2 * kRingC + 7); }
-    __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 8); }
+    __device__ uint64_t* p_full() const { return bar(2 * kRingA + 2 * kRingC + 2); }
+    __device__ uint64_t* o_done() const { return bar(2 * kRingA + 2 * kRingC + 3); }
+    __device__ uint64_t* drain() const { return bar(2 * kRingA + 2 * kRingC + 4); }
+    __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 5); }
     __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k3OffMisc); }
     __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k3OffMisc + 4); }
 };
@@ -716,6 +720,19 @@ __device__ __forceinline__ uint4 ld_codes(const uint8_t* p)
                  : "l"(p));
     return v;
 }
+
+// 16 bytes global -> shared without registers (zero-filled when `bytes` is 0), with the
+// same L2 hint as ld_codes; completion is tracked per thread in commit groups
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
@@ -880,10 +897,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             }
             mbar_init(sh.s_full(), 1);
             mbar_init(sh.s_empty(), 4);              // one arrival per softmax warp
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(sh.p_full(b), 4);
-                mbar_init(sh.p_empty(b), 1);
-            }
+            mbar_init(sh.p_full(), 4);
             mbar_init(sh.o_done(), 1);
             mbar_init(sh.drain(), 1);
             mbar_init(sh.q_full(), 1);
@@ -914,82 +928,83 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
         const int n_own = set == 0 ? own_count<5>(NT) : own_count<4>(NT);
         int64_t row_c0 = -1, row_c1 = -1;                 // rows of the last two tiles
         int tile_c0 = -1, tile_c1 = -1;
-        uint4 R[kPre3][4];
-        auto load = [&](uint4 (&r)[4], int j) {
-            const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
-            int64_t row;
-            if (it.tile == tile_c0) row = row_c0;
-            else if (it.tile == tile_c1) row = row_c1;
-            else {
-                row = rc.row(r0 + (int64_t)it.tile * kRT + t, false);
-                if (it.tile & 1) { tile_c1 = it.tile; row_c1 = row; }
-                else { tile_c0 = it.tile; row_c0 = row; }
-            }
-            if (row < 0) {
-                r[0] = r[1] = r[2] = r[3] = make_uint4(0u, 0u, 0u, 0u);
-            } else if (it.ch == 8 || !tq4) {
-                const uint8_t* src = it.ch == 8 ? C.rope + row * kDRope : C.lat + row * kDLat + it.ch * 64;
-#pragma unroll
-                for (int v = 0; v < 4; ++v) r[v] = ld_codes(src + 16 * v);
-            } else {
-                const uint8_t* src = C.lat + row * (kDLat / 2) + it.ch * 32;
-                r[0] = ld_codes(src);
-                r[1] = ld_codes(src + 16);
-            }
-        };
-#pragma unroll
-        for (int u = 0; u < kPre3; ++u)
-            if (u < n_own) load(R[u], u);
-        int a_ord = 0, c_ord = 0;
-        bool ok = true;
-        for (int j0 = 0; j0 < n_own && ok; j0 += kPre3) {
-#pragma unroll
-            for (int u = 0; u < kPre3; ++u) {
-                const int j = j0 + u;
-                if (j >= n_own) break;
+        // stage d holds piece p of row t at (p * 128 + t) * 16: conflict-free reads
+        auto issue = [&](int j) {
+            if (j < n_own) {
                 const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
-                const uint4 raw[4] = {R[u][0], R[u][1], R[u][2], R[u][3]};
-                if (j + kPre3 < n_own) load(R[u], j + kPre3);
+                int64_t row;
+                if (it.tile == tile_c0) row = row_c0;
+                else if (it.tile == tile_c1) row = row_c1;
+                else {
+                    row = rc.row(r0 + (int64_t)it.tile * kRT + t, false);
+                    if (it.tile & 1) { tile_c1 = it.tile; row_c1 = row; }
+                    else { tile_c0 = it.tile; row_c0 = row; }
+                }
                 const bool fp8 = it.ch == 8 || !tq4;
-                if (it.score) {
-                    const int slot = set + 2 * (a_ord & 1);
-                    ok = wait_bar3(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
-                    ok = __all_sync(kFull, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int hq = 0; hq < 2; ++hq) {
-                        uint32_t h[16];
-                        codes_to_half(raw, hq, fp8, h);
-                        tmem_st_x16(tmem + lane_base + kColA + 32 * slot + 16 * hq, h);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sh.full_a(slot));
-                    ++a_ord;
-                } else {
-                    const int slot = 2 * (c_ord % 3) + set;
-                    ok = wait_bar3(sh, sh.empty_c(slot), ((uint32_t)(c_ord / 3) & 1u) ^ 1u, a.status);
-                    ok = __all_sync(kFull, ok);
-                    if (!ok) break;
-                    uint8_t* dst = sh.slot(slot);
-#pragma unroll
-                    for (int hq = 0; hq < 2; ++hq) {
-                        uint32_t h[16];
-                        codes_to_half(raw, hq, fp8, h);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            *reinterpret_cast<uint4*>(dst + sw128(t, 4 * hq + c)) =
-                                make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sh.full_c(slot));
-                    ++c_ord;
+                const uint8_t* src = row < 0 ? C.rope
+                                   : it.ch == 8 ? C.rope + row * kDRope
+                                   : tq4 ? C.lat + row * (kDLat / 2) + it.ch * 32
+                                         : C.lat + row * kDLat + it.ch * 64;
+                const uint32_t nb = row < 0 ? 0u : 16u;      // invalid rows read as zeros
+                uint8_t* st = sh.stage(set, j % kStages) + t * 16;
+                cp_async16(st, src, nb);
+                cp_async16(st + kRT * 16, src + 16, nb);
+                if (fp8) {
+                    cp_async16(st + 2 * kRT * 16, src + 32, nb);
+                    cp_async16(st + 3 * kRT * 16, src + 48, nb);
                 }
             }
+            cp_async_commit();                            // one group per item, maybe empty
+        };
+#pragma unroll
+        for (int d = 0; d < kStages; ++d) issue(d);
+        int a_ord = 0, c_ord = 0;
+        bool ok = true;
+        for (int j = 0; j < n_own && ok; ++j) {
+            const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
+            const bool fp8 = it.ch == 8 || !tq4;
+            cp_async_wait<kStages - 1>();                 // item j's group has landed
+            uint4 raw[4];
+            {
+                const uint8_t* st = sh.stage(set, j % kStages) + t * 16;
+                raw[0] = *reinterpret_cast<const uint4*>(st);
+                raw[1] = *reinterpret_cast<const uint4*>(st + kRT * 16);
+                raw[2] = fp8 ? *reinterpret_cast<const uint4*>(st + 2 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
+                raw[3] = fp8 ? *reinterpret_cast<const uint4*>(st + 3 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            issue(j + kStages);                           // refills the stage just read
+            uint32_t h[32];
+            codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
+            codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+            if (it.score) {
+                const int slot = set + 2 * (a_ord & 1);
+                ok = wait_bar3(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = __all_sync(kFull, ok);
+                if (!ok) break;
+                tc_fence_after();
+                tmem_st_x32(tmem + lane_base + kColA + 32 * slot, h);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sh.full_a(slot));
+                ++a_ord;
+            } else {
+                const int slot = 2 * (c_ord & 1) + set;
+                ok = wait_bar3(sh, sh.empty_c(slot), ((uint32_t)(c_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = __all_sync(kFull, ok);
+                if (!ok) break;
+                uint8_t* dst = sh.slot(slot);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(dst + sw128(t, c)) =
+                        make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sh.full_c(slot));
+                ++c_ord;
+            }
         }
+        cp_async_wait_all();                              // nothing lands after the CTA ends
     } else if (warp < 12) {
         // ================================ softmax ========================================
         // Control flow is identical in all 128 threads (the named barriers need every one
@@ -1111,9 +1126,9 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                     wl[(g + e) / 2] = *reinterpret_cast<const uint32_t*>(&lo);
                 }
             }
-            if (ok && i >= 2) ok = wait_bar3(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
+            // W of tile i-1 was consumed by the context MMAs that o_done(i-1) covers
             if (ok) {
-                uint8_t* pb = sh.pbuf(b);
+                uint8_t* pb = sh.pbuf();
                 // row t of W^T: 64 fp16, chunks 0..3 the hi halves, 4..7 the lo halves
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -1124,7 +1139,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sh.p_full(b));
+                if (lane == 0) mbar_arrive(sh.p_full());
             }
             warp_reduce_transpose<false>(sv, lane);
             l_lane += sv[0];
@@ -1196,21 +1211,21 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                     mma_commit(sh.s_full());
                 }
                 if (i >= 1) {
-                    const int tile = i - 1, b = tile & 1;
-                    if (!(ok = wait_bar3(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
+                    const int tile = i - 1;
+                    if (!(ok = wait_bar3(sh, sh.p_full(), (uint32_t)tile & 1u, a.status))) break;
                     tc_fence_after();
                     for (int c = 0; c < 8 && ok; ++c) {
                         // chunk c comes from set c & 1: its ord-th context chunk, in slot
-                        // 2 (ord % 3) + (c & 1), next to its M-tile partner
+                        // 2 (ord % 2) + (c & 1), next to its M-tile partner
                         const int ord = 4 * tile + (c >> 1);
-                        const int slot = 2 * (ord % 3) + (c & 1);
-                        if (!(ok = wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord / 3) & 1u, a.status))) break;
+                        const int slot = 2 * (ord & 1) + (c & 1);
+                        if (!(ok = wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status))) break;
                         tc_fence_after();
                         if (c & 1) {
                             // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
                             const int m = c >> 1;
                             const uint32_t a_base = smem_u32(sh.slot(slot - 1));
-                            const uint32_t p_base = smem_u32(sh.pbuf(b));
+                            const uint32_t p_base = smem_u32(sh.pbuf());
 #pragma unroll
                             for (int ks = 0; ks < kRT / 16; ++ks)
                                 mma_f16_ss(tmem + kColO + 64 * m,
@@ -1222,7 +1237,6 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                         }
                     }
                     if (!ok) break;
-                    mma_commit(sh.p_empty(b));
                     mma_commit(sh.o_done());
                 }
             }
