@@ -710,6 +710,16 @@ __device__ __forceinline__ bool wait_bar3(const Shared3& sh, uint64_t* bar, uint
 
 __device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// true in exactly one lane of the (converged) warp
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // 16 bytes of codes that are read once: not kept in L1, and L2 fetches the aligned
 // 256 bytes around them (the rest of the row's codes are read shortly after).
 __device__ __forceinline__ uint4 ld_codes(const uint8_t* p)
@@ -1178,70 +1188,89 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
         }
     } else {
         // ================================ MMA issuer =====================================
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
-            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
-            const uint32_t q_base = smem_u32(sh.q());
-            // the Q image is written by the kernel launched just before this one
-            grid_dependency_wait();
+        // The whole warp runs the loop (operands are computed warp-uniformly); one elected
+        // lane issues the MMAs and commits.
+        const bool leader = elect_one();
+        const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
+        const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
+        const uint64_t q_desc = desc_sw128(smem_u32(sh.q()), 1024);
+        const uint64_t p_desc = desc_sw128(smem_u32(sh.pbuf()), 1024);
+        const uint64_t v_desc = desc_sw128_lbo(smem_u32(sh.slot(0)), kChunkBytes, 1024);
+        // the Q image is written by the kernel launched just before this one
+        grid_dependency_wait();
+        if (leader) {
             mbar_arrive_expect_tx(sh.q_full(), kQBytes);
             bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
                           kQBytes, sh.q_full());
-            bool ok = wait_bar3(sh, sh.q_full(), 0u, a.status);
-            tc_fence_after();
-            for (int i = 0; i <= NT && ok; ++i) {
-                if (i < NT) {
-                    if (i >= 1 && !(ok = wait_bar3(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status))) break;
+        }
+        __syncwarp();
+        bool ok = __all_sync(kFull, wait_bar3(sh, sh.q_full(), 0u, a.status));
+        tc_fence_after();
+        for (int i = 0; i <= NT && ok; ++i) {
+            if (i < NT) {
+                if (i >= 1) ok = __all_sync(kFull, wait_bar3(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                for (int ch = 0; ch < 9; ++ch) {
+                    // chunk ch comes from producer set ch & 1: its ord-th score chunk
+                    const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
+                    const int slot = (ch & 1) + 2 * (ord & 1);
+                    ok = __all_sync(kFull, wait_bar3(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    if (!ok) break;
                     tc_fence_after();
-                    for (int ch = 0; ch < 9 && ok; ++ch) {
-                        // chunk ch comes from producer set ch & 1: its ord-th score chunk
-                        const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
-                        const int slot = (ch & 1) + 2 * (ord & 1);
-                        if (!(ok = wait_bar3(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status))) break;
-                        tc_fence_after();
-                        const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
+                    const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
+                    const uint32_t a_tm = tmem + kColA + 32 * slot;
+                    const uint64_t b_desc = q_desc + (uint64_t)((ch * kQSlabBytes) >> 4);
+                    if (leader) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_f16_ts(d, tmem + kColA + 32 * slot + 8 * ks,
-                                       desc_sw128(q_base + ch * kQSlabBytes + 32 * ks, 1024), idesc_s,
+                            mma_f16_ts(d, a_tm + 8 * ks, b_desc + 2 * ks, idesc_s,
                                        (ch == 0 || ch == 8) ? (ks > 0) : 1u);
                         mma_commit(sh.empty_a(slot));
                     }
-                    if (!ok) break;
-                    mma_commit(sh.s_full());
+                    __syncwarp();
                 }
-                if (i >= 1) {
-                    const int tile = i - 1;
-                    if (!(ok = wait_bar3(sh, sh.p_full(), (uint32_t)tile & 1u, a.status))) break;
+                if (!ok) break;
+                if (leader) mma_commit(sh.s_full());
+                __syncwarp();
+            }
+            if (i >= 1) {
+                const int tile = i - 1;
+                ok = __all_sync(kFull, wait_bar3(sh, sh.p_full(), (uint32_t)tile & 1u, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                for (int c = 0; c < 8; ++c) {
+                    // chunk c comes from set c & 1: its ord-th context chunk, in slot
+                    // 2 (ord % 2) + (c & 1), next to its M-tile partner
+                    const int ord = 4 * tile + (c >> 1);
+                    const int slot = 2 * (ord & 1) + (c & 1);
+                    ok = __all_sync(kFull, wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    if (!ok) break;
                     tc_fence_after();
-                    for (int c = 0; c < 8 && ok; ++c) {
-                        // chunk c comes from set c & 1: its ord-th context chunk, in slot
-                        // 2 (ord % 2) + (c & 1), next to its M-tile partner
-                        const int ord = 4 * tile + (c >> 1);
-                        const int slot = 2 * (ord & 1) + (c & 1);
-                        if (!(ok = wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status))) break;
-                        tc_fence_after();
-                        if (c & 1) {
-                            // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
-                            const int m = c >> 1;
-                            const uint32_t a_base = smem_u32(sh.slot(slot - 1));
-                            const uint32_t p_base = smem_u32(sh.pbuf());
+                    if (c & 1) {
+                        // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
+                        const int m = c >> 1;
+                        const uint64_t a_desc = v_desc + (uint64_t)(((slot - 1) * kChunkBytes) >> 4);
+                        const uint32_t d = tmem + kColO + 64 * m;
+                        if (leader) {
 #pragma unroll
                             for (int ks = 0; ks < kRT / 16; ++ks)
-                                mma_f16_ss(tmem + kColO + 64 * m,
-                                           desc_sw128_lbo(a_base + 2048 * ks, kChunkBytes, 1024),
-                                           desc_sw128(p_base + 2048 * ks, 1024), idesc_c,
-                                           (tile == 0 && ks == 0) ? 0u : 1u);
+                                mma_f16_ss(d, a_desc + (uint64_t)((2048 * ks) >> 4), p_desc + (uint64_t)((2048 * ks) >> 4),
+                                           idesc_c, (tile == 0 && ks == 0) ? 0u : 1u);
                             mma_commit(sh.empty_c(slot - 1));
                             mma_commit(sh.empty_c(slot));
                         }
+                        __syncwarp();
                     }
-                    if (!ok) break;
-                    mma_commit(sh.o_done());
                 }
+                if (!ok) break;
+                if (leader) mma_commit(sh.o_done());
+                __syncwarp();
             }
-            // drain: every MMA issued so far completes before tensor memory is freed, and
-            // the Q copy has landed before the CTA's shared memory is released
+        }
+        // drain: every MMA issued so far completes before tensor memory is freed, and
+        // the Q copy has landed before the CTA's shared memory is released
+        if (leader) {
             mma_commit(sh.drain());
             if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
                 atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
