@@ -23,10 +23,14 @@
 //
 // Every wait is bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT, raises a
 // CTA-wide abort flag, drains the MMAs in flight and frees tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <climits>
+#include <cstring>
 #include <atomic>
 
 #include "kvq_internal.cuh"
@@ -77,6 +81,9 @@ __constant__ float c_cb_tc[16] = {
     kTq4Centroids[12], kTq4Centroids[13], kTq4Centroids[14], kTq4Centroids[15]};
 
 struct TcArgs {
+    // tensor maps of the code planes ([0] fp8 tier, [1] TQ4 tier), used when use_tma
+    CUtensorMap tm_lat[2], tm_rope[2];
+    int use_tma;                         // contiguous rows: chunks arrive by TMA
     kvq_mla_problem p;
     int split_rows, n_splits, n_hg;      // n_hg: head groups of 32
     const float* q_rot;                  // [n_seq][n_q][H][512] (TQ4 sequences)
@@ -650,7 +657,7 @@ constexpr int kRingC = 4;                // shared-memory context slots (pairs a
 constexpr int kStages = 4;               // raw-code stages in flight per producer set
 constexpr int kStageBytes = kRT * 64;    // one chunk of raw codes, [4 pieces][128 rows][16 B]
 constexpr uint32_t kColA = 128;
-constexpr int kThreads3 = 416;           // 8 producer, 4 softmax and 1 MMA warps
+constexpr int kThreads3 = 448;           // 8 producer, 4 softmax, 1 MMA and 1 loader warps
 constexpr int k3OffQ = 0;
 constexpr int k3OffRing = k3OffQ + kQBytes;
 constexpr int k3OffP = k3OffRing + kRingC * kChunkBytes;
@@ -661,8 +668,8 @@ constexpr int k3OffAlpha = k3OffM + 32 * 4;               // [32] rescale factor
 constexpr int k3OffFlag = k3OffAlpha + 32 * 4;            // some head rescales O
 constexpr int k3OffBar = k3OffFlag + 16;
 // full_a[4], empty_a[4], full_c[4], empty_c[4], s_full, s_empty, p_full, o_done, drain,
-// q_full
-constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 6;
+// q_full, raw_full[2][kStages], raw_empty[2][kStages]
+constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 6 + 4 * kStages;
 constexpr int k3OffMisc = k3OffBar + k3NumBars * 8;
 constexpr int k3SmemBytes = k3OffMisc + 16 + 1024;
 static_assert(k3SmemBytes <= 227 * 1024, "shared memory");
@@ -688,6 +695,8 @@ struct Shared3 {
     __device__ uint64_t* o_done() const { return bar(2 * kRingA + 2 * kRingC + 3); }
     __device__ uint64_t* drain() const { return bar(2 * kRingA + 2 * kRingC + 4); }
     __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 5); }
+    __device__ uint64_t* raw_full(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + set * kStages + d); }
+    __device__ uint64_t* raw_empty(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + 2 * kStages + set * kStages + d); }
     __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k3OffMisc); }
     __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k3OffMisc + 4); }
 };
@@ -743,6 +752,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// 2-D tiled TMA load of the box at (x, y) of `map` into shared memory; its bytes count
+// against the transaction count of `bar`
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
@@ -801,6 +821,23 @@ struct OwnItem {
 
 template <int NS>
 __device__ __forceinline__ int own_count(int NT) { return NS + (NT - 1) * (NS + 4) + 4; }
+
+// position n of the common order
+__device__ __forceinline__ OwnItem common_item(int n, int NT)
+{
+    OwnItem o;
+    if (n < 9) {
+        o.tile = 0; o.ch = n; o.score = true;
+        return o;
+    }
+    const int m = n - 9, i = 1 + m / 17, j = m - (m / 17) * 17;
+    if (i < NT && j < 9) {
+        o.tile = i; o.ch = j; o.score = true;
+    } else {
+        o.tile = i - 1; o.ch = i < NT ? j - 9 : j; o.score = false;
+    }
+    return o;
+}
 
 template <int NS>
 __device__ __forceinline__ OwnItem own_item(int j, int par, int NT)
@@ -911,6 +948,10 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             mbar_init(sh.o_done(), 1);
             mbar_init(sh.drain(), 1);
             mbar_init(sh.q_full(), 1);
+            for (int i = 0; i < 2 * kStages; ++i) {
+                mbar_init(sh.raw_full(i / kStages, i % kStages), 1);
+                mbar_init(sh.raw_empty(i / kStages, i % kStages), 4);   // one per warp of the set
+            }
             *sh.abort_flag() = 0;
             fence_mbar_init();
         }
@@ -966,26 +1007,44 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             }
             cp_async_commit();                            // one group per item, maybe empty
         };
+        const bool tma = a.use_tma != 0;
+        if (!tma) {
 #pragma unroll
-        for (int d = 0; d < kStages; ++d) issue(d);
+            for (int d = 0; d < kStages; ++d) issue(d);
+        }
         int a_ord = 0, c_ord = 0;
         bool ok = true;
         for (int j = 0; j < n_own && ok; ++j) {
             const OwnItem it = set == 0 ? own_item<5>(j, 0, NT) : own_item<4>(j, 1, NT);
             const bool fp8 = it.ch == 8 || !tq4;
-            cp_async_wait<kStages - 1>();                 // item j's group has landed
             uint4 raw[4];
-            {
+            if (tma) {
+                // the loader's box: row t at t * (bytes per row of the chunk)
+                const int d = j % kStages;
+                ok = __all_sync(kFull, wait_bar3(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status));
+                if (!ok) break;
+                const uint8_t* st = sh.stage(set, d) + t * (fp8 ? 64 : 32);
+                raw[0] = *reinterpret_cast<const uint4*>(st);
+                raw[1] = *reinterpret_cast<const uint4*>(st + 16);
+                raw[2] = fp8 ? *reinterpret_cast<const uint4*>(st + 32) : make_uint4(0u, 0u, 0u, 0u);
+                raw[3] = fp8 ? *reinterpret_cast<const uint4*>(st + 48) : make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                cp_async_wait<kStages - 1>();             // item j's group has landed
                 const uint8_t* st = sh.stage(set, j % kStages) + t * 16;
                 raw[0] = *reinterpret_cast<const uint4*>(st);
                 raw[1] = *reinterpret_cast<const uint4*>(st + kRT * 16);
                 raw[2] = fp8 ? *reinterpret_cast<const uint4*>(st + 2 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
                 raw[3] = fp8 ? *reinterpret_cast<const uint4*>(st + 3 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
+                issue(j + kStages);                       // refills the stage just read
             }
-            issue(j + kStages);                           // refills the stage just read
             uint32_t h[32];
             codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
             codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+            if (tma) {
+                // the stage is released once every lane's reads of it have been consumed
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sh.raw_empty(set, j % kStages));
+            }
             if (it.score) {
                 const int slot = set + 2 * (a_ord & 1);
                 ok = wait_bar3(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
@@ -1186,6 +1245,46 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                 }
             }
         }
+    } else if (warp == 13) {
+        // ================================ loader =========================================
+        // Contiguous rows: one TMA box per chunk ([128 rows x 32 or 64 bytes]) into the
+        // owning producer set's next stage, in the common order.
+        if (a.use_tma) {
+            const bool leader = elect_one();
+            const CUtensorMap* m_lat = &a.tm_lat[tq4 ? 1 : 0];
+            const CUtensorMap* m_rope = &a.tm_rope[tq4 ? 1 : 0];
+            const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;   // pool row of candidate r0
+            int o0 = 0, o1 = 0;
+            bool ok = true;
+            for (int n = 0; n < n_items && ok; ++n) {
+                const OwnItem it = common_item(n, NT);
+                const int set = it.ch & 1;
+                const int j = set ? o1++ : o0++;
+                const int d = j % kStages;
+                ok = __all_sync(kFull, wait_bar3(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status));
+                if (!ok) break;
+                if (leader) {
+                    const bool rope = it.ch == 8;
+                    const int inner = (rope || !tq4) ? 64 : 32;
+                    mbar_arrive_expect_tx(sh.raw_full(set, d), (uint32_t)(inner * kRT));
+                    tma_load_2d(sh.stage(set, d), rope ? m_rope : m_lat, rope ? 0 : it.ch * inner,
+                                (int)(row0 + (int64_t)it.tile * kRT), sh.raw_full(set, d));
+                }
+                __syncwarp();
+            }
+            // every box issued has landed before the CTA's shared memory is released
+            if (leader) {
+                for (int set = 0; set < 2; ++set) {
+                    const int o = set ? o1 : o0;
+                    for (int d = 0; d < kStages && d < o; ++d) {
+                        const int jl = d + kStages * ((o - 1 - d) / kStages);
+                        if (!mbar_wait(sh.raw_full(set, d), (uint32_t)(jl / kStages) & 1u, kTimeoutNs) && a.status)
+                            atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+                    }
+                }
+            }
+            __syncwarp();
+        }
     } else {
         // ================================ MMA issuer =====================================
         // The whole warp runs the loop (operands are computed warp-uniformly); one elected
@@ -1298,12 +1397,56 @@ size_t tc_q_image_bytes(const kvq_mla_problem& p)
     return align256((size_t)p.n_seq * p.n_q * n_hg * kQBytes);
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+// [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes]; rows past n_rows read as 0
+bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || !plane || n_rows < 1 || n_rows > INT32_MAX) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)n_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kRT};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s)
 {
     const bool v3 = p.impl == 3;
     TcArgs a;
+    memset(&a, 0, sizeof(a));
+    if (v3 && !p.block_table && !p.idx) {
+        bool ok = true;
+        for (int k = 0; k < 2 && ok; ++k) {
+            const bool used = p.seq_fmt || p.fmt == (k ? KVQ_FMT_TQ4 : KVQ_FMT_FP8);
+            if (!used) continue;
+            const kvq_mla_cache& c = k ? p.tq4 : p.fp8;
+            ok = make_code_map(&a.tm_lat[k], c.lat, c.n_rows, k ? kDLat / 2 : kDLat, k ? 32 : 64) &&
+                 make_code_map(&a.tm_rope[k], c.rope, c.n_rows, kDRope, 64);
+        }
+        a.use_tma = ok ? 1 : 0;
+    }
     a.p = p;
     a.split_rows = plan.split_rows;
     a.n_splits = plan.n_splits;
