@@ -47,8 +47,10 @@ def parse():
     ap.add_argument("--T", type=int, default=32768)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--suite", default="decode", choices=["decode", "codecs"],
+                    help="decode: the decode step (one JSON line); codecs: one line per codec kernel")
     ap.add_argument("--decode-impl", type=int, default=0,
-                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2/3 tensor cores")
+                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores")
     return ap.parse_args()
 
 
@@ -108,12 +110,13 @@ class ClockSampler:
 
 
 def peaks():
+    """(hbm GB/s, sustained bf16 TFLOP/s, kind): the measured figures when present."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             m = json.load(f)
-        return float(m["hbm_gbs"]), "measured"
+        return float(m["hbm_gbs"]), float(m["bf16_tflops_sustained"]), "measured"
     except (OSError, KeyError, ValueError):
-        return 6800.0, "fallback"
+        return 6800.0, 1700.0, "fallback"
 
 
 def profile_traffic(kernel_file: str):
@@ -285,17 +288,25 @@ def run_ours(args, world, rank, local):
     rows_per_step = Lyr * T
     value = rows_per_step * world / (ms_per_step / 1e3)
 
-    # ---- roofline of the dominant kernel (the decode call, per launch = one layer)
+    # ---- roofline of the dominant kernel (the decode call, per launch = one layer).
+    # At H = 64 the decode is a dense contraction of 2 H (512 + 64 + 512) flops per row,
+    # which the tensor cores run as split fp16 (hi + lo halves of q and w: twice the
+    # algorithmic flops); that roofline binds before HBM (328 B per row).
     dec_launch_s = statistics.mean(dec_ms) / Lyr / 1e3
     alg_bytes = T * ROW_BYTES_TQ4 + H * (512 + 64) * 4 + H * 512 * 4 + H * 4
-    peak, peak_kind = peaks()
-    achieved = alg_bytes / dec_launch_s / 1e9
-    traffic = profile_traffic("kvq_decode_tc.cu")
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_kind": peak_kind, "kernel": "kvq_mla_decode (TQ4, T=32768, H=64)",
+    alg_flops = 2 * H * (512 + 64 + 512) * T
+    hbm_peak, tc_peak, peak_kind = peaks()
+    achieved_tf = alg_flops / dec_launch_s / 1e12
+    achieved_gbs = alg_bytes / dec_launch_s / 1e9
+    roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / tc_peak, 4), "traffic": profile_traffic("kvq_decode_tc.cu"),
+                "peak_kind": f"{peak_kind} bf16 sustained (fp16 runs at the same rate)",
+                "kernel": f"kvq_mla_decode (TQ4, T={T}, H={H}): query image, decode, combine",
                 "decode_us_per_layer": round(dec_launch_s * 1e6, 2),
-                "flops_per_launch": 2 * H * (512 + 64 + 512) * T}
+                "flops_per_launch": alg_flops, "tensor_flops_executed_per_launch": 2 * alg_flops,
+                "tensor_pipe_frac": round(2 * achieved_tf / tc_peak, 4),
+                "bytes_per_launch": alg_bytes, "hbm_achieved_gbs": round(achieved_gbs, 1),
+                "hbm_peak_gbs": hbm_peak, "hbm_frac": round(achieved_gbs / hbm_peak, 4)}
 
     # ---- e2e: host buffers in and out every step
     e2e = None
@@ -355,11 +366,113 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_codecs(args, local):
+    """One JSON line per codec / gather kernel on its workload's sizes: median of K
+    launches, each timed with CUDA events after writing a buffer larger than L2 (so the
+    inputs come from HBM), against the algorithmic bytes the kernel must move."""
+    import torch
+    import __graft_entry__
+    import quantized_kv_cache_fp8_gb300 as kvq
+    import workloads as W
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, _, peak_kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    K = max(5, args.steps)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        ts = []
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        return statistics.median(ts)
+
+    def report(kernel, workload, alg_bytes, seconds, units, unit_name):
+        gbs = alg_bytes / seconds / 1e9
+        print(json.dumps({"suite": "codecs", "kernel": kernel, "workload": workload,
+                          "us": round(seconds * 1e6, 2), f"{unit_name}_per_s": units / seconds,
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                                       "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                                       "bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
+                          "l2": "flushed before each timed launch", "steps": K}), flush=True)
+
+    # a1: fp8 encode of the latent and rope planes, T = 131072 rows (the long-context cache)
+    T = 131072
+    x = torch.randn(T, 512, generator=gen, device=dev)
+    xr = torch.randn(T, 64, generator=gen, device=dev)
+    codes = torch.empty(T, 512, dtype=torch.uint8, device=dev)
+    rcodes = torch.empty(T, 64, dtype=torch.uint8, device=dev)
+    sc = torch.empty(T, device=dev)
+    rsc = torch.empty(T, device=dev)
+    s = timed(lambda: (kvq.kvq_encode_fp8(x, codes, sc), kvq.kvq_encode_fp8(xr, rcodes, rsc)))
+    report("kvq_encode_fp8", f"T={T} rows of 512 + 64 (two launches)", T * (576 * 4 + 576 + 8), s, T, "rows")
+    del x, xr, codes, rcodes, sc, rsc
+
+    # a2: TQ4 encode of the latent, T = 32768 rows (the 4-bit tier's cache)
+    T = 32768
+    x = torch.randn(T, 512, generator=gen, device=dev)
+    signs = torch.from_numpy(W.sign_bits(0)).to(dev)
+    packed = torch.empty(T, 256, dtype=torch.uint8, device=dev)
+    rad = torch.empty(T, device=dev)
+    s = timed(lambda: kvq.kvq_encode_tq4(x, signs, packed, rad))
+    report("kvq_encode_tq4", f"T={T} rows of 512", T * (512 * 4 + 256 + 4) + 64, s, T, "rows")
+    del x, packed, rad
+
+    # a3 / a4: q4_0 paged append and gather, 16 sequences x 8192 tokens x 8 heads x 256
+    n_seq, n_tok, n_heads, ps = 16, 8192, 8, 64
+    pos0, table, n_cells = W.paged_table(n_seq, n_tok, ps, ps - 8, seed=0)
+    amp = torch.tensor([1e-3, 1.0, 40.0], device=dev)
+
+    def rows_kv():
+        r = torch.randn(n_seq, n_tok, n_heads, 256, generator=gen, device=dev)
+        return r * amp[torch.randint(0, 3, (n_seq, n_tok, n_heads, 1), generator=gen, device=dev)]
+
+    k, v = rows_kv(), rows_kv()
+    pos0_d = torch.from_numpy(pos0).to(dev)
+    table_d = torch.from_numpy(table).to(dev)
+    k_pool = torch.zeros(n_cells, n_heads, 144, dtype=torch.uint8, device=dev)
+    v_pool = torch.zeros(n_cells, n_heads, 144, dtype=torch.uint8, device=dev)
+    toks = n_seq * n_tok
+    s = timed(lambda: kvq.kvq_append_q4(k, v, pos0_d, table_d, ps, n_cells, k_pool, v_pool))
+    report("kvq_append_q4", f"{n_seq} seqs x {n_tok} tokens x K,V x {n_heads} heads x 256, pages of {ps}",
+           toks * (2 * n_heads * 256 * 4 + 2 * n_heads * 144) + table.size * 4, s, toks, "tokens")
+    del k, v
+    out = torch.empty(n_seq, n_tok, n_heads, 256, dtype=torch.float16, device=dev)
+    s = timed(lambda: kvq.kvq_gather_q4(k_pool, pos0_d, n_tok, table_d, ps, n_cells, out))
+    report("kvq_gather (q4_0)", f"one pool: {n_seq} seqs x {n_tok} tokens x {n_heads} heads -> fp16",
+           toks * n_heads * (144 + 256 * 2) + table.size * 4, s, toks, "tokens")
+    del out, k_pool, v_pool
+
+    # a7: sparse row gather of the fp8 MLA cache, top-k = 2048 of T = 131072
+    T, k_sel = 131072, 2048
+    src = dict(lat=torch.zeros(T, 512, dtype=torch.uint8, device=dev), lat_scale=torch.ones(T, device=dev),
+               rope=torch.zeros(T, 64, dtype=torch.uint8, device=dev), rope_scale=torch.ones(T, device=dev))
+    idx = torch.from_numpy(W.sparse_indices(T, k_sel, 1, seed=0)[0]).to(dev)
+    dst = dict(lat=torch.empty(k_sel, 512, dtype=torch.uint8, device=dev), lat_scale=torch.empty(k_sel, device=dev),
+               rope=torch.empty(k_sel, 64, dtype=torch.uint8, device=dev), rope_scale=torch.empty(k_sel, device=dev))
+    s = timed(lambda: kvq.kvq_gather_rows(kvq.FMT_FP8, src, T, idx, dst))
+    report("kvq_gather (fp8 rows by index)", f"top-k {k_sel} of T={T} rows", k_sel * (584 * 2 + 4), s, k_sel, "rows")
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.suite == "codecs":
+        if rank == 0:
+            run_codecs(args, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -213,7 +213,7 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if (p->n_q < 1 || p->n_heads < 1 || p->max_seq_len < 0 || p->split_rows < 0)
         return fail(KVQ_EINVAL, "%s: bad sizes", E);
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
-    if (p->impl < 0 || p->impl > 3) return fail(KVQ_EINVAL, "%s: impl must be 0..3", E);
+    if (p->impl < 0 || p->impl > 2) return fail(KVQ_EINVAL, "%s: impl must be 0..2", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && p->fmt != KVQ_FMT_TQ4)
         return fail(KVQ_EFORMAT, "%s: fmt %d is neither FP8 nor TQ4", E, p->fmt);

@@ -406,7 +406,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.n_cand_max = (int)n_cand;
     // the tensor-core kernel unless the caller asks for CUDA cores; below 8 heads the
     // 32-head MMA tile would be mostly padding
-    plan.tc = p.impl == 2 || p.impl == 3 || (p.impl == 0 && p.n_heads >= 8);
+    plan.tc = p.impl == 2 || (p.impl == 0 && p.n_heads >= 8);
     int64_t split_rows = p.split_rows;
     if (plan.tc) {
         constexpr int kTile = 128, kHeadsTc = 32;

@@ -14,13 +14,6 @@
 // that are stacked along N (N = 64 for 32 heads), so each A tile read serves both
 // halves; D accumulates in fp32 in tensor memory.
 //
-// Roles (288 threads): warps 0-3 dequantise code chunks [128 rows x 64] into a ring of
-// swizzled shared-memory slots (thread = row); warps 4-7 run the softmax (thread =
-// row) and the epilogue (thread = output dim); warp 8 allocates tensor memory and one
-// of its threads issues every MMA.  A schedule of 18 ring positions per tile step is
-// shared by producer and MMA issuer: 9 score chunks of tile i, one pad, 8 context
-// chunks of tile i-1 (pairs of context chunks land in adjacent slots).
-//
 // Every wait is bounded (%globaltimer); a timeout sets KVQ_DEV_TIMEOUT, raises a
 // CTA-wide abort flag, drains the MMAs in flight and frees tensor memory.
 #include <cuda.h>
@@ -46,39 +39,16 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRT = 128;                 // rows per tile (MMA M)
 constexpr int kGQ = 32;                  // query-heads per CTA
 constexpr int kN = 2 * kGQ;              // MMA N: hi | lo stacked
-constexpr int kRing = 6;                 // dequantised chunk slots
 constexpr int kChunkBytes = kRT * 128;   // [128 rows x 64 fp16], 128B-swizzled
 constexpr int kQSlabBytes = kN * 128;    // [64 rows x 64 fp16]
 constexpr int kQBytes = 9 * kQSlabBytes; // 72 KB
 constexpr int kPBytes = kRT * 128;       // [128 rows x 64 fp16] MN-major
-constexpr int kPeriod = 18;              // ring positions per tile step
-constexpr int kThreads = 288;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // rescale only when the max grows by > 2^8
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-// shared-memory map (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kQBytes;
-constexpr int kOffP = kOffRing + kRing * kChunkBytes;
-constexpr int kOffRed = kOffP + 2 * kPBytes;                 // [4][32] floats
-constexpr int kOffLut = kOffRed + 4 * 32 * 4;                // [256] half2: byte -> 2 centroids
-constexpr int kOffBar = kOffLut + 256 * 4;
-// barriers: full[kRing], empty[kRing], s_full[2], s_empty[2], p_full[2], p_empty[2],
-// o_done, drain
-constexpr int kNumBars = 2 * kRing + 10;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;             // tmem base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;             // + alignment slack
-
 // TMEM columns
-constexpr uint32_t kColS = 0;        // S buffer b: lat at 128b, rope at 128b + 64
 constexpr uint32_t kColO = 256;      // O^T M-tile m at 256 + 64m
-
-__constant__ float c_cb_tc[16] = {
-    kTq4Centroids[0], kTq4Centroids[1], kTq4Centroids[2], kTq4Centroids[3],
-    kTq4Centroids[4], kTq4Centroids[5], kTq4Centroids[6], kTq4Centroids[7],
-    kTq4Centroids[8], kTq4Centroids[9], kTq4Centroids[10], kTq4Centroids[11],
-    kTq4Centroids[12], kTq4Centroids[13], kTq4Centroids[14], kTq4Centroids[15]};
 
 struct TcArgs {
     // tensor maps of the code planes ([0] fp8 tier, [1] TQ4 tier), used when use_tma
@@ -110,12 +80,6 @@ __device__ __forceinline__ int64_t pool_row_of(const kvq_mla_problem& p, int s, 
 
 // byte offset of 16-byte chunk c (0..7) of row r in a 128B-swizzled [rows x 64] slab
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b)
-{
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // four e4m3 codes (one 32-bit word) -> two half2 words (exact); the pattern S.1111.111,
 // which the encoder never writes, reads as 0
@@ -200,43 +164,6 @@ __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
     }
 }
 
-struct Shared {
-    uint8_t* base;
-    __device__ uint8_t* q() const { return base + kOffQ; }
-    __device__ uint8_t* slot(int i) const { return base + kOffRing + i * kChunkBytes; }
-    __device__ uint8_t* pbuf(int b) const { return base + kOffP + b * kPBytes; }
-    __device__ float* red() const { return reinterpret_cast<float*>(base + kOffRed); }
-    __device__ uint32_t* lut() const { return reinterpret_cast<uint32_t*>(base + kOffLut); }
-    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
-    __device__ uint64_t* full(int i) const { return bar(i); }
-    __device__ uint64_t* empty(int i) const { return bar(kRing + i); }
-    __device__ uint64_t* s_full(int b) const { return bar(2 * kRing + b); }
-    __device__ uint64_t* s_empty(int b) const { return bar(2 * kRing + 2 + b); }
-    __device__ uint64_t* p_full(int b) const { return bar(2 * kRing + 4 + b); }
-    __device__ uint64_t* p_empty(int b) const { return bar(2 * kRing + 6 + b); }
-    __device__ uint64_t* o_done() const { return bar(2 * kRing + 8); }
-    __device__ uint64_t* drain() const { return bar(2 * kRing + 9); }
-    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + kOffMisc); }
-    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kOffMisc + 4); }
-};
-
-// bounded wait that also gives up once another role has aborted
-__device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
-                                         uint32_t* status)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*sh.abort_flag()) return false;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
-            *sh.abort_flag() = 1;
-            if (status) atomicOr(status, (unsigned)KVQ_DEV_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
 // Row bookkeeping shared by producer and softmax threads: the pool row of candidate j
 // of this CTA's (sequence, query), or -1 when not admissible (flags bad data).
 struct RowCtx {
@@ -263,392 +190,30 @@ struct RowCtx {
     }
 };
 
-// dequantise chunk `ch` (0..7 latent, 8 rope) of pool row `row` (or zeros) into row t of
-// a swizzled slot
-__device__ __forceinline__ void dequant_chunk(uint8_t* slot, int t, int64_t row, int ch, bool tq4,
-                                             const kvq_mla_cache& C, const uint32_t* lut)
-{
-    uint32_t h[32];
-    if (row < 0) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) h[i] = 0;
-    } else if (ch == 8 || !tq4) {
-        const uint8_t* src = ch == 8 ? C.rope + row * kDRope : C.lat + row * kDLat + ch * 64;
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const uint4 w = __ldg(s4 + v);
-            e4m3x4_to_half(w.x, h[8 * v + 0], h[8 * v + 1]);
-            e4m3x4_to_half(w.y, h[8 * v + 2], h[8 * v + 3]);
-            e4m3x4_to_half(w.z, h[8 * v + 4], h[8 * v + 5]);
-            e4m3x4_to_half(w.w, h[8 * v + 6], h[8 * v + 7]);
-        }
-    } else {
-        // 64 nibbles = 32 bytes; element 2j low nibble, 2j+1 high nibble of byte j
-        const uint4* s4 = reinterpret_cast<const uint4*>(C.lat + row * (kDLat / 2) + ch * 32);
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const uint4 w = __ldg(s4 + v);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int b = 0; b < 16; ++b) h[16 * v + b] = lut[(ww[b >> 2] >> (8 * (b & 3))) & 0xFF];
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(slot + sw128(t, c)) = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-}
-
-// the code-byte -> (centroid of low nibble, centroid of high nibble) table, in fp16
-__device__ __forceinline__ void fill_lut(uint32_t* lut, int tid, int n_threads)
-{
-    for (int b = tid; b < 256; b += n_threads) lut[b] = pack_half2(c_cb_tc[b & 15], c_cb_tc[b >> 4]);
-}
-
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(TcArgs a)
-{
-    extern __shared__ uint8_t dsm[];
-    Shared sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
-    const kvq_mla_problem& p = a.p;
-    const int split = blockIdx.x, s = blockIdx.y;
-    const int q = blockIdx.z / a.n_hg, hg = blockIdx.z % a.n_hg;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h0 = hg * kGQ;
-    const int nh = min(kGQ, p.n_heads - h0);
-    const int L = p.seq_len[s];
-    const int fmt = seq_fmt_of(p, s);
-    const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
-    const int64_t r0 = (int64_t)split * a.split_rows;
-    const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
-    const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
-    const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
-
-    if (r0 >= n_cand || bad_fmt) {          // nothing to do: an empty partial
-        if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
-        if (tid < nh) {
-            const int64_t sl = (qrow + h0 + tid) * a.n_splits + split;
-            a.part_ml[sl * 2] = -INFINITY;
-            a.part_ml[sl * 2 + 1] = 0.0f;
-        }
-        return;
-    }
-    const bool tq4 = fmt == KVQ_FMT_TQ4;
-    const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
-    const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
-    RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
-
-    // ---- set-up: barriers, tensor memory, the Q image ---------------------------------
-    if (tid == 0) {
-        for (int i = 0; i < kRing; ++i) {
-            mbar_init(sh.full(i), 128);
-            mbar_init(sh.empty(i), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sh.s_full(b), 1);
-            mbar_init(sh.s_empty(b), 128);
-            mbar_init(sh.p_full(b), 128);
-            mbar_init(sh.p_empty(b), 1);
-        }
-        mbar_init(sh.o_done(), 1);
-        mbar_init(sh.drain(), 1);
-        *sh.abort_flag() = 0;
-        fence_mbar_init();
-    }
-    if (warp == 8) {
-        tmem_alloc(sh.tmem_base(), 512);
-        tmem_relinquish();
-    }
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes);
-        uint4* dst = reinterpret_cast<uint4*>(sh.q());
-        for (int i = tid; i < kQBytes / 16; i += kThreads) dst[i] = __ldg(src + i);
-    }
-    fill_lut(sh.lut(), tid, kThreads);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *sh.tmem_base();
-    const int n_pos = kPeriod * (NT + 1);
-
-    if (warp < 4) {
-        // ================================ producer =======================================
-        const int t = tid;                            // row within the tile
-        int cur_tile = -1;
-        int64_t cur_row = -1;
-        for (int pos = 0; pos < n_pos; ++pos) {
-            const int slot = pos % kRing;
-            const uint32_t par = (uint32_t)(pos / kRing) & 1u;
-            if (!wait_bar(sh, sh.empty(slot), par ^ 1u, a.status)) break;
-            const int i = pos / kPeriod, j = pos % kPeriod;
-            int tile = -1, ch = -1;
-            if (j < 9 && i < NT) { tile = i; ch = j; }
-            else if (j >= 10 && i >= 1) { tile = i - 1; ch = j - 10; }
-            if (tile >= 0) {
-                if (tile != cur_tile) {
-                    cur_tile = tile;
-                    cur_row = rc.row(r0 + (int64_t)tile * kRT + t, false);
-                }
-                dequant_chunk(sh.slot(slot), t, cur_row, ch, tq4, C, sh.lut());
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(sh.full(slot));
-        }
-    } else if (warp < 8) {
-        // ================================ softmax ========================================
-        // Control flow is identical in all 128 threads (the named barriers below need
-        // every one of them); `ok` only guards work and is kept warp-uniform for the
-        // .sync.aligned tensor-memory instructions.
-        const int t = tid - 128;                      // row within the tile
-        const int wq = warp - 4;                      // TMEM lane quarter
-        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const float tau2 = p.sm_scale * kLog2e;
-        const float c512 = tq4_inv_sqrt(kDLat);
-        float* red = sh.red();
-        float m_run[kGQ], l_part[kGQ];
-#pragma unroll
-        for (int g = 0; g < kGQ; ++g) { m_run[g] = -INFINITY; l_part[g] = 0.0f; }
-        bool ok = true;
-        for (int i = 0; i < NT; ++i) {
-            const int b = i & 1;
-            const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
-            float sc_lat = 0.0f, sc_rope = 0.0f;
-            if (row >= 0) {
-                sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
-                sc_rope = C.rope_scale[row];
-            }
-            if (ok) ok = wait_bar(sh, sh.s_full(b), (uint32_t)(i >> 1) & 1u, a.status);
-            ok = __all_sync(kFull, ok);
-            float sv[kGQ];
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) sv[g] = 0.0f;
-            if (ok) {
-                tc_fence_after();
-                uint32_t x[16], y[16];
-#pragma unroll
-                for (int c = 0; c < kN; c += 16) {
-                    tmem_ld_x16(tmem + lane_base + kColS + 128 * b + c, x);
-                    tmem_ld_x16(tmem + lane_base + kColS + 128 * b + 64 + c, y);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        sv[(c + e) & (kGQ - 1)] += fmaf(sc_lat, __uint_as_float(x[e]),
-                                                        sc_rope * __uint_as_float(y[e]));
-                }
-                tc_fence_before();
-                mbar_arrive(sh.s_empty(b));
-            }
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) sv[g] = (row >= 0 && ok) ? sv[g] * tau2 : -INFINITY;
-            // per-head max over the 128 rows of the tile
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) {
-                float v = sv[g];
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-                if (lane == 0) red[wq * 32 + g] = v;
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            bool need_rescale = false;
-            float alpha[kGQ];
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) {
-                const float tm = fmaxf(fmaxf(red[g], red[32 + g]), fmaxf(red[64 + g], red[96 + g]));
-                alpha[g] = 1.0f;
-                if (tm > m_run[g] + kLazy || (m_run[g] == -INFINITY && tm > -INFINITY)) {
-                    alpha[g] = (m_run[g] == -INFINITY) ? 0.0f : exp2f(m_run[g] - tm);
-                    m_run[g] = tm;
-                    if (i > 0) need_rescale = true;
-                }
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");    // red[] is rewritten next tile
-            // Consume o_done's phase i-1 (the context MMAs of tile i-1) at every tile,
-            // so that this wait and the epilogue's never trail the barrier by more than
-            // one phase (a parity wait cannot tell phase k from phase k+2); it also
-            // makes O safe to rescale.
-            if (i > 0 && ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
-            ok = __all_sync(kFull, ok);
-            if (need_rescale && ok) {
-                {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                        for (int c = 0; c < kN; c += 16) {
-                            uint32_t x[16];
-                            tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha[(c + e) & (kGQ - 1)]);
-                            tmem_st_x16(tmem + lane_base + kColO + 64 * m + c, x);
-                        }
-                    }
-                    tmem_st_wait();
-                }
-            }
-#pragma unroll
-            for (int g = 0; g < kGQ; ++g) l_part[g] *= alpha[g];
-            // weights: p = 2^(s - m), w = p * latent scale, split hi | lo
-            uint32_t wh[kGQ / 2], wl[kGQ / 2];
-#pragma unroll
-            for (int g = 0; g < kGQ; g += 2) {
-                const float p0 = sv[g] == -INFINITY ? 0.0f : exp2f(sv[g] - m_run[g]);
-                const float p1 = sv[g + 1] == -INFINITY ? 0.0f : exp2f(sv[g + 1] - m_run[g + 1]);
-                l_part[g] += p0;
-                l_part[g + 1] += p1;
-                const float w0 = p0 * sc_lat, w1 = p1 * sc_lat;
-                const __half2 hi = __floats2half2_rn(w0, w1);
-                const float2 hf = __half22float2(hi);
-                const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
-                wh[g / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-                wl[g / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-            }
-            if (ok && i >= 2) ok = wait_bar(sh, sh.p_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status);
-            if (ok) {
-                uint8_t* pb = sh.pbuf(b);
-                // row t of W^T: 64 fp16, chunks 0..3 the hi halves, 4..7 the lo halves
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    *reinterpret_cast<uint4*>(pb + sw128(t, c)) =
-                        make_uint4(wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]);
-                    *reinterpret_cast<uint4*>(pb + sw128(t, c + 4)) =
-                        make_uint4(wl[4 * c], wl[4 * c + 1], wl[4 * c + 2], wl[4 * c + 3]);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(sh.p_full(b));
-            }
-        }
-        // ---- epilogue: l over the 128 rows, O^T -> partials ------------------------------
-        if (ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
-        ok = __all_sync(kFull, ok);
-#pragma unroll
-        for (int g = 0; g < kGQ; ++g) {
-            float v = l_part[g];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-            if (lane == 0) red[wq * 32 + g] = v;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ok) {
-            tc_fence_after();
-            if (t < nh) {
-                const float lt = red[t] + red[32 + t] + red[64 + t] + red[96 + t];
-                const int64_t sl = (qrow + h0 + t) * a.n_splits + split;
-                float mt = m_run[0];
-#pragma unroll
-                for (int g = 1; g < kGQ; ++g) if (g == t) mt = m_run[g];
-                a.part_ml[sl * 2] = mt;
-                a.part_ml[sl * 2 + 1] = lt;
-            }
-#pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-                const int d = 128 * m + 32 * wq + lane;
-                uint32_t x[16], y[16];
-#pragma unroll
-                for (int c = 0; c < kGQ; c += 16) {
-                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + c, x);
-                    tmem_ld_x16(tmem + lane_base + kColO + 64 * m + kGQ + c, y);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int g = c + e;
-                        if (g < nh)
-                            a.part_o[((qrow + h0 + g) * a.n_splits + split) * kDLat + d] =
-                                __uint_as_float(x[e]) + __uint_as_float(y[e]);
-                    }
-                }
-            }
-        }
-    } else {
-        // ================================ MMA issuer =====================================
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
-            const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
-            const uint32_t q_base = smem_u32(sh.q());
-            bool ok = true;
-            for (int pos = 0; pos < n_pos && ok; ++pos) {
-                const int slot = pos % kRing;
-                const uint32_t par = (uint32_t)(pos / kRing) & 1u;
-                const int i = pos / kPeriod, j = pos % kPeriod;
-                if (!(ok = wait_bar(sh, sh.full(slot), par, a.status))) break;
-                tc_fence_after();
-                if (j < 9 && i < NT) {
-                    const int b = i & 1;
-                    if (j == 0 && i >= 2 && !(ok = wait_bar(sh, sh.s_empty(b), (uint32_t)((i - 2) >> 1) & 1u, a.status))) break;
-                    tc_fence_after();
-                    const uint32_t a_base = smem_u32(sh.slot(slot));
-                    const uint32_t d = tmem + kColS + 128 * b + (j == 8 ? 64 : 0);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_f16_ss(d, desc_sw128(a_base + 32 * ks, 1024),
-                                   desc_sw128(q_base + j * kQSlabBytes + 32 * ks, 1024), idesc_s,
-                                   (j == 0 || j == 8) ? (ks > 0) : 1u);
-                    mma_commit(sh.empty(slot));
-                    if (j == 8) mma_commit(sh.s_full(b));
-                } else if (j >= 10 && i >= 1) {
-                    const int tile = i - 1, b = tile & 1, c = j - 10;
-                    if (c == 0 && !(ok = wait_bar(sh, sh.p_full(b), (uint32_t)(tile >> 1) & 1u, a.status))) break;
-                    tc_fence_after();
-                    if (c & 1) {
-                        // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
-                        const int m = c >> 1;
-                        const uint32_t a_base = smem_u32(sh.slot(slot - 1));
-                        const uint32_t p_base = smem_u32(sh.pbuf(b));
-#pragma unroll
-                        for (int ks = 0; ks < kRT / 16; ++ks) {
-                            // LBO: the slot holding the next 64 dims
-                            const uint64_t ad = desc_sw128_lbo(a_base + 2048 * ks, kChunkBytes, 1024);
-                            mma_f16_ss(tmem + kColO + 64 * m, ad, desc_sw128(p_base + 2048 * ks, 1024),
-                                       idesc_c, (tile == 0 && ks == 0) ? 0u : 1u);
-                        }
-                        mma_commit(sh.empty(slot - 1));
-                        mma_commit(sh.empty(slot));
-                        if (c == 7) {
-                            mma_commit(sh.p_empty(b));
-                            mma_commit(sh.o_done());
-                        }
-                    }
-                } else {
-                    mbar_arrive(sh.empty(slot));          // a pad position
-                }
-            }
-            // drain: every MMA issued so far completes before tensor memory is freed
-            mma_commit(sh.drain());
-            if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
-                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
-        }
-        __syncwarp();
-    }
-
-    // ---- tear-down -------------------------------------------------------------------
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 8) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
-}
-
-
 // ====================================================================================
-// Variant 3: the contractions and tensor-memory map of variant 2 with reorganised
-// producer and softmax roles.
-//  * Eight producer warps in two sets of four that convert alternate chunks, so two
-//    chains of ring waits, stores and arrivals run at once and every warp scheduler
-//    holds one warp of each set.  Raw codes of a set's next kStages chunks are in
-//    flight at any time as asynchronous global -> shared copies (cp.async, no
-//    registers held), with an L2 hint that fetches the surrounding 256 bytes.
-//  * W (the context operand) is single-buffered: the softmax writes W(i) only after
-//    the context MMAs of tile i-1, which read W(i-1), have completed.
+// The decode kernel.
+//  * Roles (448 threads): warps 0-7 are two producer sets of four warps (thread = row)
+//    that convert alternate chunks of codes to fp16, so two chains of ring waits,
+//    stores and arrivals run at once and every warp scheduler holds one warp of each
+//    set; warps 8-11 run the softmax (thread = row) and the epilogue (thread = output
+//    dim); warp 12 allocates tensor memory and issues every MMA from one elected lane;
+//    warp 13 loads code chunks by TMA (contiguous caches).
+//  * Order of work, common to producers, loader and MMA issuer: per step i, the 9
+//    score chunks of tile i (8 latent, 1 rope) if i < NT, then the 8 latent context
+//    chunks of tile i-1.  Score chunks go to tensor memory (thread = row = TMEM lane)
+//    and are read from there by the MMA; context chunks go to a shared-memory ring,
+//    the two chunks of an M-tile in adjacent slots.
+//  * Raw codes: contiguous caches stream [128 rows x 32 or 64 bytes] boxes by TMA
+//    into the owning set's stages; paged and sparse caches copy each row's 16-byte
+//    pieces with cp.async.  Either way a set's next kStages chunks are in flight.
 //  * TQ4 codes decode without a table in memory: the codebook is symmetric, so code k
 //    is +m[k - 8] (k >= 8) or -m[7 - k], and the bytes of the 8 binary16 magnitudes
 //    m[j] sit in four registers that byte permutes (prmt) index by j.
 //  * The per-head maximum over a tile's rows is a transposing butterfly (31 shuffles
-//    per warp instead of 160); the running maxima live in shared memory, and the row
-//    sums of p are reduced the same way into one register per lane.
+//    per warp); the running maxima live in shared memory, and the row sums of p are
+//    reduced the same way into one register per lane.
+//  * W (the context operand) is single-buffered: the softmax writes W(i) only after
+//    the context MMAs of tile i-1, which read W(i-1), have completed.
 //  * The Q image arrives by one bulk asynchronous copy while the first codes load.
 // TMEM: S lat 0..63, S rope 64..127, score-A ring 4 x 32 columns at 128.., O^T 256..511.
 // ====================================================================================
@@ -657,34 +222,34 @@ constexpr int kRingC = 4;                // shared-memory context slots (pairs a
 constexpr int kStages = 4;               // raw-code stages in flight per producer set
 constexpr int kStageBytes = kRT * 64;    // one chunk of raw codes, [4 pieces][128 rows][16 B]
 constexpr uint32_t kColA = 128;
-constexpr int kThreads3 = 448;           // 8 producer, 4 softmax, 1 MMA and 1 loader warps
-constexpr int k3OffQ = 0;
-constexpr int k3OffRing = k3OffQ + kQBytes;
-constexpr int k3OffP = k3OffRing + kRingC * kChunkBytes;
-constexpr int k3OffStage = k3OffP + kPBytes;
-constexpr int k3OffRed = k3OffStage + 2 * kStages * kStageBytes;   // [4][32] f32
-constexpr int k3OffM = k3OffRed + 4 * 32 * 4;             // [32] running maxima
-constexpr int k3OffAlpha = k3OffM + 32 * 4;               // [32] rescale factors
-constexpr int k3OffFlag = k3OffAlpha + 32 * 4;            // some head rescales O
-constexpr int k3OffBar = k3OffFlag + 16;
+constexpr int kThreads = 448;           // 8 producer, 4 softmax, 1 MMA and 1 loader warps
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kOffQ + kQBytes;
+constexpr int kOffP = kOffRing + kRingC * kChunkBytes;
+constexpr int kOffStage = kOffP + kPBytes;
+constexpr int kOffRed = kOffStage + 2 * kStages * kStageBytes;   // [4][32] f32
+constexpr int kOffM = kOffRed + 4 * 32 * 4;             // [32] running maxima
+constexpr int kOffAlpha = kOffM + 32 * 4;               // [32] rescale factors
+constexpr int kOffFlag = kOffAlpha + 32 * 4;            // some head rescales O
+constexpr int kOffBar = kOffFlag + 16;
 // full_a[4], empty_a[4], full_c[4], empty_c[4], s_full, s_empty, p_full, o_done, drain,
 // q_full, raw_full[2][kStages], raw_empty[2][kStages]
-constexpr int k3NumBars = 2 * kRingA + 2 * kRingC + 6 + 4 * kStages;
-constexpr int k3OffMisc = k3OffBar + k3NumBars * 8;
-constexpr int k3SmemBytes = k3OffMisc + 16 + 1024;
-static_assert(k3SmemBytes <= 227 * 1024, "shared memory");
+constexpr int kNumBars = 2 * kRingA + 2 * kRingC + 6 + 4 * kStages;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-struct Shared3 {
+struct Shared {
     uint8_t* base;
-    __device__ uint8_t* q() const { return base + k3OffQ; }
-    __device__ uint8_t* slot(int i) const { return base + k3OffRing + i * kChunkBytes; }
-    __device__ uint8_t* pbuf() const { return base + k3OffP; }
-    __device__ uint8_t* stage(int set, int d) const { return base + k3OffStage + (set * kStages + d) * kStageBytes; }
-    __device__ float* red() const { return reinterpret_cast<float*>(base + k3OffRed); }
-    __device__ float* m_run() const { return reinterpret_cast<float*>(base + k3OffM); }
-    __device__ float* alpha() const { return reinterpret_cast<float*>(base + k3OffAlpha); }
-    __device__ volatile int* flag() const { return reinterpret_cast<volatile int*>(base + k3OffFlag); }
-    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + k3OffBar) + i; }
+    __device__ uint8_t* q() const { return base + kOffQ; }
+    __device__ uint8_t* slot(int i) const { return base + kOffRing + i * kChunkBytes; }
+    __device__ uint8_t* pbuf() const { return base + kOffP; }
+    __device__ uint8_t* stage(int set, int d) const { return base + kOffStage + (set * kStages + d) * kStageBytes; }
+    __device__ float* red() const { return reinterpret_cast<float*>(base + kOffRed); }
+    __device__ float* m_run() const { return reinterpret_cast<float*>(base + kOffM); }
+    __device__ float* alpha() const { return reinterpret_cast<float*>(base + kOffAlpha); }
+    __device__ volatile int* flag() const { return reinterpret_cast<volatile int*>(base + kOffFlag); }
+    __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
     __device__ uint64_t* full_a(int i) const { return bar(i); }
     __device__ uint64_t* empty_a(int i) const { return bar(kRingA + i); }
     __device__ uint64_t* full_c(int i) const { return bar(2 * kRingA + i); }
@@ -697,11 +262,11 @@ struct Shared3 {
     __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 5); }
     __device__ uint64_t* raw_full(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + set * kStages + d); }
     __device__ uint64_t* raw_empty(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + 2 * kStages + set * kStages + d); }
-    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + k3OffMisc); }
-    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + k3OffMisc + 4); }
+    __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + kOffMisc); }
+    __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kOffMisc + 4); }
 };
 
-__device__ __forceinline__ bool wait_bar3(const Shared3& sh, uint64_t* bar, uint32_t parity,
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
                                           uint32_t* status)
 {
     if (mbar_try_wait(bar, parity)) return true;
@@ -729,19 +294,9 @@ __device__ __forceinline__ bool elect_one()
     return pred != 0;
 }
 
-// 16 bytes of codes that are read once: not kept in L1, and L2 fetches the aligned
-// 256 bytes around them (the rest of the row's codes are read shortly after).
-__device__ __forceinline__ uint4 ld_codes(const uint8_t* p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// 16 bytes global -> shared without registers (zero-filled when `bytes` is 0), with the
-// same L2 hint as ld_codes; completion is tracked per thread in commit groups
+// 16 bytes global -> shared without registers (zero-filled when `bytes` is 0); L2
+// fetches the aligned 256 bytes around them (the rest of the row's codes follow soon);
+// completion is tracked per thread in commit groups
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes)
 {
     asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
@@ -899,10 +454,10 @@ __device__ __forceinline__ void warp_reduce_transpose(float (&v)[32], int lane)
 
 // 13 warps: warp w runs on sub-partition w % 4, so sub-partition 0 holds four warps and
 // its 16K registers cap every thread at 128
-__global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ TcArgs a)
+__global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ TcArgs a)
 {
     extern __shared__ uint8_t dsm[];
-    Shared3 sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
+    Shared sh{reinterpret_cast<uint8_t*>(((uintptr_t)dsm + 1023) & ~(uintptr_t)1023)};
     const kvq_mla_problem& p = a.p;
     const int split = blockIdx.x, s = blockIdx.y;
     const int q = blockIdx.z / a.n_hg, hg = blockIdx.z % a.n_hg;
@@ -1021,7 +576,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             if (tma) {
                 // the loader's box: row t at t * (bytes per row of the chunk)
                 const int d = j % kStages;
-                ok = __all_sync(kFull, wait_bar3(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status));
                 if (!ok) break;
                 const uint8_t* st = sh.stage(set, d) + t * (fp8 ? 64 : 32);
                 raw[0] = *reinterpret_cast<const uint4*>(st);
@@ -1047,7 +602,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             }
             if (it.score) {
                 const int slot = set + 2 * (a_ord & 1);
-                ok = wait_bar3(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = wait_bar(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -1059,7 +614,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                 ++a_ord;
             } else {
                 const int slot = 2 * (c_ord & 1) + set;
-                ok = wait_bar3(sh, sh.empty_c(slot), ((uint32_t)(c_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = wait_bar(sh, sh.empty_c(slot), ((uint32_t)(c_ord >> 1) & 1u) ^ 1u, a.status);
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 uint8_t* dst = sh.slot(slot);
@@ -1089,14 +644,13 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
         float l_lane = 0.0f;                          // sum of p over this warp's rows, head `lane`
         bool ok = true;
         for (int i = 0; i < NT; ++i) {
-            const int b = i & 1;
             const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
             float sc_lat = 0.0f, sc_rope = 0.0f;
             if (row >= 0) {
                 sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
                 sc_rope = C.rope_scale[row];
             }
-            if (ok) ok = wait_bar3(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
+            if (ok) ok = wait_bar(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
             ok = __all_sync(kFull, ok);
             float sv[kGQ];
 #pragma unroll
@@ -1148,7 +702,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             // so that this wait and the epilogue's never trail the barrier by more than
             // one phase (a parity wait cannot tell phase k from phase k+2); it also
             // makes O safe to rescale.
-            if (i > 0 && ok) ok = wait_bar3(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+            if (i > 0 && ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
             ok = __all_sync(kFull, ok);
             if (need_rescale) {
                 l_lane *= alpha_s[lane];
@@ -1214,7 +768,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             l_lane += sv[0];
         }
         // ---- epilogue: l over the 128 rows, O^T -> partials ------------------------------
-        if (ok) ok = wait_bar3(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
+        if (ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
         ok = __all_sync(kFull, ok);
         red[wq * 32 + lane] = l_lane;
         named_bar_softmax();
@@ -1261,7 +815,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                 const int set = it.ch & 1;
                 const int j = set ? o1++ : o0++;
                 const int d = j % kStages;
-                ok = __all_sync(kFull, wait_bar3(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status));
                 if (!ok) break;
                 if (leader) {
                     const bool rope = it.ch == 8;
@@ -1303,18 +857,18 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                           kQBytes, sh.q_full());
         }
         __syncwarp();
-        bool ok = __all_sync(kFull, wait_bar3(sh, sh.q_full(), 0u, a.status));
+        bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status));
         tc_fence_after();
         for (int i = 0; i <= NT && ok; ++i) {
             if (i < NT) {
-                if (i >= 1) ok = __all_sync(kFull, wait_bar3(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status));
+                if (i >= 1) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status));
                 if (!ok) break;
                 tc_fence_after();
                 for (int ch = 0; ch < 9; ++ch) {
                     // chunk ch comes from producer set ch & 1: its ord-th score chunk
                     const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
                     const int slot = (ch & 1) + 2 * (ord & 1);
-                    ok = __all_sync(kFull, wait_bar3(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    ok = __all_sync(kFull, wait_bar(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
@@ -1335,7 +889,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
             }
             if (i >= 1) {
                 const int tile = i - 1;
-                ok = __all_sync(kFull, wait_bar3(sh, sh.p_full(), (uint32_t)tile & 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)tile & 1u, a.status));
                 if (!ok) break;
                 tc_fence_after();
                 for (int c = 0; c < 8; ++c) {
@@ -1343,7 +897,7 @@ __global__ void __maxnreg__(128) mla_decode_tc3_kernel(const __grid_constant__ T
                     // 2 (ord % 2) + (c & 1), next to its M-tile partner
                     const int ord = 4 * tile + (c >> 1);
                     const int slot = 2 * (ord & 1) + (c & 1);
-                    ok = __all_sync(kFull, wait_bar3(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    ok = __all_sync(kFull, wait_bar(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status));
                     if (!ok) break;
                     tc_fence_after();
                     if (c & 1) {
@@ -1433,10 +987,9 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s)
 {
-    const bool v3 = p.impl == 3;
     TcArgs a;
     memset(&a, 0, sizeof(a));
-    if (v3 && !p.block_table && !p.idx) {
+    if (!p.block_table && !p.idx) {
         bool ok = true;
         for (int k = 0; k < 2 && ok; ++k) {
             const bool used = p.seq_fmt || p.fmt == (k ? KVQ_FMT_TQ4 : KVQ_FMT_FP8);
@@ -1467,15 +1020,10 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
         e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(mla_decode_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 k3SmemBytes);
-        if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    if (v3) return launch_dependent(mla_decode_tc3_kernel, grid, dim3(kThreads3), k3SmemBytes, s, a);
-    else mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(mla_decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, a);
 }
 
 }  // namespace kvq

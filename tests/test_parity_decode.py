@@ -12,7 +12,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-IMPLS = pytest.mark.parametrize("impl", [1, 2, 3], ids=["cudacore", "tcgen05", "tcgen05v3"])
+IMPLS = pytest.mark.parametrize("impl", [1, 2], ids=["cudacore", "tcgen05"])
 
 
 @pytest.fixture(scope="module")

@@ -144,6 +144,15 @@ def q4_paged(n_seq: int = 16, n_tok: int = 8192, n_heads: int = 8, page_size: in
     return Q4Workload(k, v, np.full(n_seq, pos0, np.int32), table, page_size, n_pages * page_size)
 
 
+def paged_table(n_seq: int, n_tok: int, page_size: int, pos0: int, seed: int):
+    """(pos0 [n_seq], page table [n_seq][max_pages], n_cells) for appending n_tok tokens
+    per sequence from position pos0: the table is a seeded permutation of all page ids."""
+    g = rng(seed + 7)
+    max_pages = (pos0 + n_tok + page_size - 1) // page_size
+    perm = g.permutation(n_seq * max_pages).astype(np.int32)
+    return np.full(n_seq, pos0, np.int32), perm.reshape(n_seq, max_pages), n_seq * max_pages * page_size
+
+
 @dataclass
 class RaggedWorkload:
     seq_len: np.ndarray       # [n_seq] int32
