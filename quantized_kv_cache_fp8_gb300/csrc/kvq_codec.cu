@@ -218,6 +218,49 @@ __device__ __forceinline__ int64_t q4_cell(const int32_t* __restrict__ page_tabl
     return cell;
 }
 
+// FWHT256 of a row held as 8 consecutive elements per lane (element 8 * lane + k in
+// z[k]): stages h = 1, 2, 4 inside the lane, h = 8 .. 128 across lanes (xor h / 8), in
+// the order h = 1, 2, ..., 128; each butterfly (a, b) -> (a + b, a - b) in fp32.  Every
+// butterfly of a stage is independent, so this layout gives the same bits as any other.
+__device__ __forceinline__ void fwht256_lane8(float (&z)[8], int lane)
+{
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if ((k & h) == 0) {
+                const float a = z[k], b = z[k + h];
+                z[k] = __fadd_rn(a, b);
+                z[k + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float p = __shfl_xor_sync(kFull, z[k], m);
+            z[k] = (lane & m) ? __fsub_rn(p, z[k]) : __fadd_rn(z[k], p);
+        }
+    }
+}
+
+// One warp per (sequence, token, K/V, head) row of 256, 8 elements per lane; block b of
+// 32 elements is lanes 4b .. 4b + 3.  The next row's loads are issued before this row's
+// arithmetic (16-byte loads when k and v allow them).
+template <bool kVec>
+__device__ __forceinline__ void load8(const float* p, float4& a, float4& b)
+{
+    if (kVec) {
+        a = __ldcs(reinterpret_cast<const float4*>(p));
+        b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    } else {
+        a = make_float4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
+        b = make_float4(__ldcs(p + 4), __ldcs(p + 5), __ldcs(p + 6), __ldcs(p + 7));
+    }
+}
+
+template <bool kVec>
 __global__ void __launch_bounds__(kCodecThreads)
 append_q4_kernel(const float* __restrict__ k, const float* __restrict__ v, int n_seq,
                  const int32_t* __restrict__ pos0, int n_tok, int n_heads,
@@ -228,52 +271,68 @@ append_q4_kernel(const float* __restrict__ k, const float* __restrict__ v, int n
     __shared__ __align__(16) uint8_t s_row[kCodecWarps][144];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int64_t n_rows = (int64_t)n_seq * n_tok * 2 * n_heads;
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
+    const int rows = 2 * n_heads;                     // K heads, then V heads
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t id = warp; id < n_rows; id += n_warps) {
-        const int h = (int)(id % n_heads);
-        const int kv = (int)((id / n_heads) & 1);
-        const int64_t st = id / (2 * (int64_t)n_heads);
-        const int t = (int)(st % n_tok);
-        const int s = (int)(st / n_tok);
+    // row r of token tok: (r < n_heads ? k : v) [tok][r % n_heads][256]; lane's 8 values
+    auto src_of = [&](int64_t tok, int r) {
+        const int kv = r >= n_heads;
+        return (kv ? v : k) + (tok * n_heads + (r - kv * n_heads)) * 256 + 8 * lane;
+    };
+    float4 nx0 = make_float4(0.f, 0.f, 0.f, 0.f), nx1 = nx0;
+    if (warp < n_tokens) load8<kVec>(src_of(warp, 0), nx0, nx1);
+    for (int64_t tok = warp; tok < n_tokens; tok += n_warps) {
+        const int s = (int)(tok / n_tok), t = (int)(tok - (int64_t)s * n_tok);
         const int64_t cell = q4_cell(page_table, max_pages, page_size, n_cells, s, pos0[s] + t);
-        if (cell < 0) {
-            if (lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
-            continue;
-        }
-        const float* src = (kv ? v : k) + (((int64_t)s * n_tok + t) * n_heads + h) * 256;
-        float z[8];
+        if (cell < 0 && lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
+        for (int r = 0; r < rows; ++r) {
+            float z[8] = {nx0.x, nx0.y, nx0.z, nx0.w, nx1.x, nx1.y, nx1.z, nx1.w};
+            // the next row's loads (of this token, or the next token's first row)
+            if (r + 1 < rows) load8<kVec>(src_of(tok, r + 1), nx0, nx1);
+            else if (tok + n_warps < n_tokens) load8<kVec>(src_of(tok + n_warps, 0), nx0, nx1);
+            if (cell < 0) continue;
+            fwht256_lane8(z, lane);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) z[j] = __ldcs(src + j * 32 + lane);
-        fwht_warp<8>(z, lane);
+            for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
+            // the block's preferred element (a total order: every lane of the block agrees)
+            float mval = z[0];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
+            for (int j = 1; j < 8; ++j)
+                if (q4_prefer(z[j], mval)) mval = z[j];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            float mval = z[b];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
+            for (int o = 1; o <= 2; o <<= 1) {
                 const float other = __shfl_xor_sync(kFull, mval, o);
                 if (q4_prefer(other, mval)) mval = other;
             }
-            const float d = __fdiv_rn(mval, -8.0f);
+            const float d = __fmul_rn(mval, -0.125f);          // mval / -8, exact
             const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-            int q = __float2int_rz(__fmaf_rn(z[b], idv, 8.5f));
-            q = min(max(q, 0), 15);
-            const int qhi = __shfl_down_sync(kFull, q, 16);
-            if (lane < 16) s_row[wib][b * 18 + 2 + lane] = (uint8_t)(q | (qhi << 4));
-            if (lane == 0) {
-                const unsigned short hb = __half_as_ushort(__float2half_rn(d));
-                s_row[wib][b * 18] = (uint8_t)(hb & 0xFF);
-                s_row[wib][b * 18 + 1] = (uint8_t)(hb >> 8);
+            uint32_t q[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                q[j] = (uint32_t)min(max(__float2int_rz(__fmaf_rn(z[j], idv, 8.5f)), 0), 15);
+            // lanes 4b + p (p = 0, 1) hold codes j = 8p .. 8p + 7 of block b, lanes
+            // 4b + p + 2 the codes j + 16 that share their bytes (high nibble)
+            uint32_t w0 = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+            uint32_t w1 = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+            const uint32_t u0 = __shfl_down_sync(kFull, w0, 2), u1 = __shfl_down_sync(kFull, w1, 2);
+            const int b = lane >> 2, p = lane & 3;
+            if (p < 2) {
+                w0 |= u0 << 4;
+                w1 |= u1 << 4;
+                uint8_t* blk = s_row[wib] + b * 18;
+                uint16_t* dst = reinterpret_cast<uint16_t*>(blk + 2 + 8 * p);   // bytes 2 + 8p ..
+                dst[0] = (uint16_t)w0; dst[1] = (uint16_t)(w0 >> 16);
+                dst[2] = (uint16_t)w1; dst[3] = (uint16_t)(w1 >> 16);
+                if (p == 0) *reinterpret_cast<uint16_t*>(blk) = __half_as_ushort(__float2half_rn(d));
             }
+            __syncwarp();
+            const int kv = r >= n_heads;
+            uint8_t* dst = (kv ? v_pool : k_pool) + (cell * n_heads + (r - kv * n_heads)) * 144;
+            if (lane < 9)
+                reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(s_row[wib])[lane];
+            __syncwarp();
         }
-        __syncwarp();
-        uint8_t* dst = (kv ? v_pool : k_pool) + (cell * n_heads + h) * 144;
-        if (lane < 9)
-            reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(s_row[wib])[lane];
-        __syncwarp();
     }
 }
 
@@ -284,42 +343,57 @@ gather_q4_kernel(const uint8_t* __restrict__ pool, int n_seq, const int32_t* __r
                  int page_size, int64_t n_cells, uint16_t* __restrict__ out,
                  uint32_t* __restrict__ dev_status)
 {
-    __shared__ __align__(16) uint8_t s_row[kCodecWarps][144];
+    constexpr int kHeadsPerPass = 8;                  // 8 x 144 B = 72 pieces of 16 B
+    __shared__ __align__(16) uint8_t s_cell[kCodecWarps][kHeadsPerPass * 144];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int64_t n_rows = (int64_t)n_seq * n_tok * n_heads;
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t id = warp; id < n_rows; id += n_warps) {
-        const int h = (int)(id % n_heads);
-        const int64_t st = id / n_heads;
-        const int t = (int)(st % n_tok);
-        const int s = (int)(st / n_tok);
+    const int b = lane >> 2, part = lane & 3;
+    for (int64_t tok = warp; tok < n_tokens; tok += n_warps) {
+        const int s = (int)(tok / n_tok), t = (int)(tok - (int64_t)s * n_tok);
         const int64_t cell = q4_cell(page_table, max_pages, page_size, n_cells, s, pos0[s] + t);
         if (cell < 0) {
             if (lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
             continue;
         }
-        const uint8_t* src = pool + (cell * n_heads + h) * 144;
-        if (lane < 9)
-            reinterpret_cast<uint4*>(s_row[wib])[lane] = __ldcs(reinterpret_cast<const uint4*>(src) + lane);
-        __syncwarp();
-        const int b = lane >> 2, part = lane & 3;
-        const uint8_t* blk = s_row[wib] + b * 18;
-        const float d = __half2float(__ushort_as_half((unsigned short)(blk[0] | (blk[1] << 8))));
-        uint32_t w[4];
+        // the token's heads are contiguous in the pool: h0 .. h0 + nh - 1 in one pass
+        for (int h0 = 0; h0 < n_heads; h0 += kHeadsPerPass) {
+            const int nh = min(kHeadsPerPass, n_heads - h0);
+            const uint4* src = reinterpret_cast<const uint4*>(pool + (cell * n_heads + h0) * 144);
+            uint4 pc[3];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const int j0 = part * 8 + e, j1 = j0 + 1;
-            const int q0 = (j0 < 16) ? (blk[2 + j0] & 15) : (blk[2 + j0 - 16] >> 4);
-            const int q1 = (j1 < 16) ? (blk[2 + j1] & 15) : (blk[2 + j1 - 16] >> 4);
-            const unsigned short h0 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q0 - 8), d)));
-            const unsigned short h1 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q1 - 8), d)));
-            w[e >> 1] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            for (int i = 0; i < 3; ++i)
+                if (lane + 32 * i < 9 * nh) pc[i] = __ldcs(src + lane + 32 * i);
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (lane + 32 * i < 9 * nh) reinterpret_cast<uint4*>(s_cell[wib])[lane + 32 * i] = pc[i];
+            __syncwarp();
+            for (int hh = 0; hh < nh; ++hh) {
+                const uint8_t* blk = s_cell[wib] + hh * 144 + b * 18;
+                const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk)));
+                // codes j = 8 part .. 8 part + 7: low nibbles of bytes 2 + j (j < 16), else
+                // high nibbles of bytes 2 + j - 16
+                const uint16_t* bytes = reinterpret_cast<const uint16_t*>(blk + 2 + 8 * (part & 1));
+                const uint32_t lo4 = (uint32_t)bytes[0] | ((uint32_t)bytes[1] << 16);
+                const uint32_t hi4 = (uint32_t)bytes[2] | ((uint32_t)bytes[3] << 16);
+                const int sh = part >= 2 ? 4 : 0;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const uint32_t src4 = e < 4 ? lo4 : hi4;
+                    const int q0 = (int)((src4 >> (8 * (e & 3) + sh)) & 15);
+                    const int q1 = (int)((src4 >> (8 * ((e + 1) & 3) + sh)) & 15);
+                    const unsigned short x0 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q0 - 8), d)));
+                    const unsigned short x1 = __half_as_ushort(__float2half_rn(__fmul_rn((float)(q1 - 8), d)));
+                    w[e >> 1] = (uint32_t)x0 | ((uint32_t)x1 << 16);
+                }
+                uint16_t* dst = out + (tok * n_heads + h0 + hh) * 256 + b * 32 + part * 8;
+                __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
+            }
+            __syncwarp();
         }
-        uint16_t* dst = out + (((int64_t)s * n_tok + t) * n_heads + h) * 256 + b * 32 + part * 8;
-        __stcs(reinterpret_cast<uint4*>(dst), make_uint4(w[0], w[1], w[2], w[3]));
-        __syncwarp();
     }
 }
 
@@ -426,19 +500,25 @@ cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const in
                              int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,
                              uint32_t* dev_status, cudaStream_t s)
 {
-    const int64_t n_rows = (int64_t)n_seq * n_tok * 2 * n_heads;
-    if (n_rows == 0) return cudaSuccess;
-    append_q4_kernel<<<grid_for(n_rows, kCodecWarps), kCodecThreads, 0, s>>>(
-        k, v, n_seq, pos0, n_tok, n_heads, page_table, max_pages, page_size, n_cells,
-        k_pool, v_pool, dev_status);
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
+    if (n_tokens == 0 || n_heads == 0) return cudaSuccess;
+    const bool vec = (uintptr_t)k % 16 == 0 && (uintptr_t)v % 16 == 0;
+    if (vec)
+        append_q4_kernel<true><<<grid_for(n_tokens, kCodecWarps), kCodecThreads, 0, s>>>(
+            k, v, n_seq, pos0, n_tok, n_heads, page_table, max_pages, page_size, n_cells,
+            k_pool, v_pool, dev_status);
+    else
+        append_q4_kernel<false><<<grid_for(n_tokens, kCodecWarps), kCodecThreads, 0, s>>>(
+            k, v, n_seq, pos0, n_tok, n_heads, page_table, max_pages, page_size, n_cells,
+            k_pool, v_pool, dev_status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s)
 {
-    const int64_t n_rows = (int64_t)d.n_seq * d.n_tok * d.n_heads;
-    if (n_rows == 0) return cudaSuccess;
-    gather_q4_kernel<<<grid_for(n_rows, kCodecWarps), kCodecThreads, 0, s>>>(
+    const int64_t n_tokens = (int64_t)d.n_seq * d.n_tok;
+    if (n_tokens == 0 || d.n_heads == 0) return cudaSuccess;
+    gather_q4_kernel<<<grid_for(n_tokens, kCodecWarps), kCodecThreads, 0, s>>>(
         d.q4_pool, d.n_seq, d.pos0, d.n_tok, d.n_heads, d.page_table, d.max_pages,
         d.page_size, d.n_cells, d.q4_out, d.dev_status);
     return cudaGetLastError();
