@@ -47,8 +47,9 @@ def parse():
     ap.add_argument("--T", type=int, default=32768)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--suite", default="decode", choices=["decode", "codecs"],
-                    help="decode: the decode step (one JSON line); codecs: one line per codec kernel")
+    ap.add_argument("--suite", default="decode", choices=["decode", "codecs", "decode-configs"],
+                    help="decode: the decode step (one JSON line); codecs: one line per codec "
+                         "kernel; decode-configs: one line per decode configuration")
     ap.add_argument("--decode-impl", type=int, default=0,
                     help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores")
     return ap.parse_args()
@@ -465,6 +466,118 @@ def run_codecs(args, local):
     report("kvq_gather (fp8 rows by index)", f"top-k {k_sel} of T={T} rows", k_sel * (584 * 2 + 4), s, k_sel, "rows")
 
 
+def run_decode_configs(args, local):
+    """One JSON line per decode configuration: one kvq_mla_decode call (query image,
+    decode, combine), median of K calls, L2 flushed before each, against both rooflines:
+    the measured HBM copy rate for the cache bytes and the measured bf16 rate for the
+    algorithmic flops (2 H n_q (512 + 64 + 512) per admissible row)."""
+    import torch
+    import __graft_entry__
+    import quantized_kv_cache_fp8_gb300 as kvq
+    import workloads as W
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, tc_peak, peak_kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    K = max(5, args.steps)
+    signs = torch.from_numpy(W.sign_bits(0)).to(dev)
+
+    def encode_pool(n_rows, fmt, mag=None):
+        """A pool of n_rows quantized rows (N(0,1), optionally times per-row magnitudes)."""
+        c = torch.randn(n_rows, 512, generator=gen, device=dev)
+        r = torch.randn(n_rows, 64, generator=gen, device=dev)
+        if mag is not None:
+            m = torch.exp(torch.empty(n_rows, 1, device=dev).uniform_(
+                float(np.log(mag[0])), float(np.log(mag[1])), generator=gen))
+            c *= m
+            r *= m
+        lat = torch.empty(n_rows, 512 if fmt == kvq.FMT_FP8 else 256, dtype=torch.uint8, device=dev)
+        ls = torch.empty(n_rows, device=dev)
+        rope = torch.empty(n_rows, 64, dtype=torch.uint8, device=dev)
+        rs = torch.empty(n_rows, device=dev)
+        if fmt == kvq.FMT_FP8:
+            kvq.kvq_encode_fp8(c, lat, ls)
+        else:
+            kvq.kvq_encode_tq4(c, signs, lat, ls)
+        kvq.kvq_encode_fp8(r, rope, rs)
+        return dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
+
+    def measure(name, p, out_shape, rows_read, row_bytes, flops):
+        ws = torch.empty(max(1, kvq.kvq_mla_decode_workspace(p)), dtype=torch.uint8, device=dev)
+        out = torch.empty(out_shape, device=dev)
+        lse = torch.empty(out_shape[:-1], device=dev)
+        for _ in range(3):
+            kvq.kvq_mla_decode(p, out, lse, ws)
+        ts = []
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kvq_mla_decode(p, out, lse, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3)
+        sec = statistics.median(ts)
+        assert torch.isfinite(out).all()
+        gbs = rows_read * row_bytes / sec / 1e9
+        tf = flops / sec / 1e12
+        print(json.dumps({"suite": "decode-configs", "config": name, "decode_impl": args.decode_impl,
+                          "us": round(sec * 1e6, 2),
+                          "kv_rows_per_s": rows_read / sec,
+                          "hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm_peak,
+                                  "frac": round(gbs / hbm_peak, 4), "bytes": rows_read * row_bytes},
+                          "tensor": {"achieved_tflops": round(tf, 2), "peak": tc_peak,
+                                     "frac": round(tf / tc_peak, 4), "flops": flops},
+                          "peak_kind": peak_kind, "l2": "flushed before each call", "steps": K}),
+              flush=True)
+
+    def one_seq(name, fmt, T, H, idx_k=0, mag=None):
+        cache = encode_pool(T, fmt, mag)
+        q = W.queries(1, 1, H, seed=0)
+        idx = None
+        if idx_k:
+            idx = torch.from_numpy(W.sparse_indices(T, idx_k, 1, seed=0)).to(dev).reshape(1, 1, idx_k)
+        kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
+        p = kvq.make_problem(seq_len=torch.tensor([T], dtype=torch.int32, device=dev),
+                             q_lat=torch.from_numpy(q.q_lat).to(dev), q_rope=torch.from_numpy(q.q_rope).to(dev),
+                             sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx, impl=args.decode_impl, **kw)
+        n = idx_k or T
+        rb = 584 if fmt == kvq.FMT_FP8 else 328
+        measure(name, p, (1, 1, H, 512), n, rb, 2 * H * 1088 * n)
+
+    F8, T4 = kvq.FMT_FP8, kvq.FMT_TQ4
+    one_seq("fp8 tiny: T=1024, H=16, magnitudes log-uniform [1e-3, 40]", F8, 1024, 16, mag=(1e-3, 40.0))
+    one_seq("TQ4: T=32768, H=64", T4, 32768, 64)
+    one_seq("fp8 long context dense: T=131072, H=128", F8, 131072, 128)
+    one_seq("fp8 long context sparse: top-k 2048 of T=131072, H=128", F8, 131072, 128, idx_k=2048)
+    for fmt, tag in ((F8, "fp8"), (T4, "TQ4")):
+        for T in (32768, 131072):
+            one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
+
+    # ragged mixed-tier batch: 32 sequences, L ~ U[1024, 65536], 4 causal queries, H=64
+    n_seq, n_q, H, ps = 32, 4, 64, 64
+    L, fmt, table, pool_pages = W.ragged_layout(n_seq, 1024, 65536, ps, seed=0)
+    pools = {f: encode_pool(pool_pages[f] * ps, f, mag=(1e-2, 10.0)) for f in (F8, T4)}
+    q = W.queries(n_seq, n_q, H, seed=0)
+    p = kvq.make_problem(seq_len=torch.from_numpy(L).to(dev), q_lat=torch.from_numpy(q.q_lat).to(dev),
+                         q_rope=torch.from_numpy(q.q_rope).to(dev), sm_scale=W.SM_SCALE,
+                         max_seq_len=int(L.max()), seq_fmt=torch.from_numpy(fmt).to(dev),
+                         block_table=torch.from_numpy(table).to(dev), page_size=ps, causal=True,
+                         fp8=pools[F8], tq4=pools[T4], signs=signs, impl=args.decode_impl)
+    rows_fp8 = int(L[fmt == 1].sum())
+    rows_tq4 = int(L[fmt == 2].sum())
+    # bytes: every sequence's rows are read once per head group and query by the kernel,
+    # but the algorithmic minimum is once per sequence
+    measure(f"ragged: 32 seqs, L ~ U[1024, 65536] ({rows_fp8 + rows_tq4} rows), 4 causal queries, "
+            f"H=64, fp8 + TQ4, pages of 64", p, (n_seq, n_q, H, 512), rows_fp8 + rows_tq4,
+            (rows_fp8 * 584 + rows_tq4 * 328) / (rows_fp8 + rows_tq4),
+            2 * H * n_q * 1088 * (rows_fp8 + rows_tq4))
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -473,6 +586,9 @@ def main():
     elif args.suite == "codecs":
         if rank == 0:
             run_codecs(args, local)
+    elif args.suite == "decode-configs":
+        if rank == 0:
+            run_decode_configs(args, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -167,6 +167,28 @@ class RaggedWorkload:
     H: int
 
 
+def ragged_layout(n_seq: int = 32, len_lo: int = 1024, len_hi: int = 65536, page_size: int = 64,
+                  seed: int = 0):
+    """The shape of the ragged batch without its rows, for timing runs that generate the
+    rows on the device: (L [n_seq], fmt [n_seq], block table, pages per tier)."""
+    g = rng(seed + 11)
+    L = g.integers(len_lo, len_hi + 1, n_seq).astype(np.int32)
+    fmt = np.where(np.arange(n_seq) < n_seq // 2, 1, 2).astype(np.int32)
+    pages = (L + page_size - 1) // page_size
+    table = np.full((n_seq, int(pages.max())), -1, np.int32)
+    pool_pages = {}
+    for f in (1, 2):
+        seqs = np.nonzero(fmt == f)[0]
+        total = int(pages[seqs].sum())
+        pool_pages[f] = total
+        perm = g.permutation(total).astype(np.int32)
+        o = 0
+        for s in seqs:
+            table[s, : pages[s]] = perm[o: o + pages[s]]
+            o += pages[s]
+    return L, fmt, table, pool_pages
+
+
 def ragged(n_seq: int = 32, n_q: int = 4, H: int = 64, len_lo: int = 1024,
            len_hi: int = 65536, page_size: int = 64, seed: int = 0,
            mag: tuple = (1e-2, 10.0)) -> RaggedWorkload:
