@@ -237,10 +237,11 @@ __device__ __forceinline__ void fwht256_lane8(float (&z)[8], int lane)
     }
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
+        const float sgn = (lane & m) ? -1.0f : 1.0f;   // a + b or a - b as fma(s, own, partner)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float p = __shfl_xor_sync(kFull, z[k], m);
-            z[k] = (lane & m) ? __fsub_rn(p, z[k]) : __fadd_rn(z[k], p);
+            z[k] = __fmaf_rn(sgn, z[k], p);
         }
     }
 }
