@@ -95,6 +95,8 @@ def test_decode_argument_errors(kvq):
     assert dec(_problem(kvq, tq4_signs=None)) == 1
     assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
     assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1
+    assert dec(_problem(kvq, impl=3)) == 1                                       # 0, 1 or 2 only
+    assert dec(_problem(kvq, impl=-1)) == 1
     p = _problem(kvq)
     need = L.kvq_mla_decode_workspace(C.byref(p))
     assert need > 0
