@@ -108,6 +108,9 @@ def _declare(L: C.CDLL) -> None:
                                 C.c_int, _i64, _p]
     L.orc_mla_decode.restype = C.c_int
     L.orc_mla_decode.argtypes = [C.POINTER(OrcMla), _p, _p, _p]
+    L.orc_q4_decode.argtypes = [C.c_int, C.c_int, C.c_int, _p, _p, C.c_int, C.c_int, _i64, _p, _p,
+                                _p, _p, C.c_double, _p, C.c_int, _p, _p, _p]
+    L.orc_q4_decode.restype = C.c_int
 
 
 def _ptr(a):
@@ -251,6 +254,33 @@ def gather_q4(pool, pos0, n_tok, page_table, page_size, n_cells, n_heads) -> np.
     if rc != 0:
         raise ValueError(f"oracle q4 gather refused (rc={rc})")
     return out
+
+
+def q4_decode(*, seq_len, page_table, page_size, n_cells, k_pool, v_pool, q, n_kv, sm_scale,
+              gate=None, seq_sel=None):
+    """q4_0 paged GQA decode attention in fp64: q [n_seq][n_qh][256] fp32 (unrotated),
+    pools [n_cells][n_kv][144] u8, optional gate [n_seq][n_qh][256] fp32.
+    -> (out [n_seq][n_qh][256] f64, lse [n_seq][n_qh] f64, bad_page flag)."""
+    seq_len = _c(seq_len, np.int32)
+    pt = _c(page_table, np.int32)
+    q = _c(q, np.float32)
+    n_seq, n_qh, hd = q.shape
+    assert hd == 256
+    k_pool = _c(k_pool, np.uint8)
+    v_pool = _c(v_pool, np.uint8)
+    g = None if gate is None else _c(gate, np.float32)
+    sel = None if seq_sel is None else _c(seq_sel, np.int32)
+    out = np.zeros((n_seq, n_qh, 256), np.float64)
+    lse = np.full((n_seq, n_qh), np.nan, np.float64)
+    bad = np.zeros(1, np.uint32)
+    rc = lib().orc_q4_decode(n_seq, n_qh, n_kv, _ptr(seq_len), _ptr(pt), pt.shape[1], page_size,
+                             n_cells, _ptr(k_pool), _ptr(v_pool), _ptr(q),
+                             None if g is None else _ptr(g), float(sm_scale),
+                             None if sel is None else _ptr(sel), 0 if sel is None else len(sel),
+                             _ptr(out), _ptr(lse), _ptr(bad))
+    if rc != 0:
+        raise ValueError(f"oracle q4 decode refused (rc={rc})")
+    return out, lse, int(bad[0])
 
 
 # --- MLA decode -----------------------------------------------------------------------

@@ -580,3 +580,98 @@ int orc_mla_decode(const orc_mla* p, double* out, double* lse, uint32_t* bad_ind
     }
     return 0;
 }
+
+/* ===================================================================================
+ * q4_0 paged decode attention in fp64 — Strata PR #2533, the qsa decode commit: the q
+ * attention rows pass through the orthonormal 256-point FWHT (as the K and V rows did
+ * when they were appended); attention reads the q4 pools with every block dequantised
+ * as (nibble - 8) * f32(d); the merged output row o = (sum_t p_t v_t) / L is rotated back
+ * (the orthonormal FWHT is its own inverse) BEFORE the optional sigmoid(gate) multiply.
+ * Grouped-query attention: query head h reads KV head h / (n_qh / n_kv).  Sequence s
+ * holds tokens at positions 0 .. seq_len[s] - 1; a position whose page is missing or
+ * outside the pool is skipped and flagged.
+ *   q_rot = (1/16) FWHT256(q);  s_t = sm_scale * q_rot . k_t;  p = softmax(s)
+ *   out = (1/16) FWHT256(sum_t p_t v_t) [* sigmoid(gate)];  lse = log sum_t exp(s_t)
+ * out [n_seq][n_qh][256], lse [n_seq][n_qh] (NULL allowed).  An empty sequence gives
+ * out = 0 and lse = -inf.  seq_sel (optional) restricts the sequences computed.
+ * =================================================================================== */
+
+/* the 256 values of one dequantised row (exact in fp32, returned in fp64) */
+static void q4_row_values(const uint8_t* row, double* x)
+{
+    for (int b = 0; b < 8; ++b) {
+        const uint8_t* blk = row + 18 * b;
+        const float d = (float)orc_f16_value((uint16_t)(blk[0] | (blk[1] << 8)));
+        for (int j = 0; j < 32; ++j) {
+            const int q = (j < 16) ? (blk[2 + j] & 15) : (blk[2 + j - 16] >> 4);
+            x[32 * b + j] = (double)((float)(q - 8) * d);
+        }
+    }
+}
+
+int orc_q4_decode(int n_seq, int n_qh, int n_kv, const int32_t* seq_len,
+                  const int32_t* page_table, int max_pages, int page_size, int64_t n_cells,
+                  const uint8_t* k_pool, const uint8_t* v_pool, const float* q,
+                  const float* gate, double sm_scale, const int32_t* seq_sel, int n_sel,
+                  double* out, double* lse, uint32_t* bad_page)
+{
+    if (n_kv <= 0 || n_qh % n_kv != 0) return -1;
+    const int grp = n_qh / n_kv;
+    double qr[256], kv[256], acc[256];
+    const int n_run = seq_sel ? n_sel : n_seq;
+    for (int si = 0; si < n_run; ++si) {
+        const int s = seq_sel ? seq_sel[si] : si;
+        const int L = seq_len[s];
+        for (int h = 0; h < n_qh; ++h) {
+            const int kvh = h / grp;
+            const float* qh = q + ((int64_t)s * n_qh + h) * 256;
+            for (int i = 0; i < 256; ++i) qr[i] = qh[i];
+            orc_fwht_f64(qr, 256);
+            for (int i = 0; i < 256; ++i) qr[i] /= 16.0;
+            /* pass 1: the maximum score */
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                const int64_t cell = q4_cell(page_table, max_pages, page_size, s, t, n_cells);
+                if (cell < 0) { if (bad_page) *bad_page = 1; continue; }
+                q4_row_values(k_pool + (cell * n_kv + kvh) * 144, kv);
+                double dot = 0.0;
+                for (int i = 0; i < 256; ++i) dot += qr[i] * kv[i];
+                const double sc = sm_scale * dot;
+                if (sc > m) m = sc;
+            }
+            /* pass 2: weights and the weighted sum of the V rows */
+            double l = 0.0;
+            for (int i = 0; i < 256; ++i) acc[i] = 0.0;
+            if (m > -INFINITY) {
+                for (int t = 0; t < L; ++t) {
+                    const int64_t cell = q4_cell(page_table, max_pages, page_size, s, t, n_cells);
+                    if (cell < 0) continue;
+                    q4_row_values(k_pool + (cell * n_kv + kvh) * 144, kv);
+                    double dot = 0.0;
+                    for (int i = 0; i < 256; ++i) dot += qr[i] * kv[i];
+                    const double pw = exp(sm_scale * dot - m);
+                    l += pw;
+                    q4_row_values(v_pool + (cell * n_kv + kvh) * 144, kv);
+                    for (int i = 0; i < 256; ++i) acc[i] += pw * kv[i];
+                }
+            }
+            double* oh = out + ((int64_t)s * n_qh + h) * 256;
+            if (l > 0.0) {
+                for (int i = 0; i < 256; ++i) acc[i] /= l;
+                orc_fwht_f64(acc, 256);                       /* rotate back ... */
+                for (int i = 0; i < 256; ++i) {
+                    double o = acc[i] / 16.0;
+                    if (gate) {                                /* ... then gate */
+                        const double g = gate[((int64_t)s * n_qh + h) * 256 + i];
+                        o *= 1.0 / (1.0 + exp(-g));
+                    }
+                    oh[i] = o;
+                }
+            } else {
+                for (int i = 0; i < 256; ++i) oh[i] = 0.0;
+            }
+            if (lse) lse[(int64_t)s * n_qh + h] = (l > 0.0) ? m + log(l) : -INFINITY;
+        }
+    }
+    return 0;
+}

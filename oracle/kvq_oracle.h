@@ -88,4 +88,11 @@ typedef struct orc_mla {
 
 int orc_mla_decode(const orc_mla* p, double* out, double* lse, uint32_t* bad_index);
 
+/* ---- q4_0 paged decode attention (GQA, head_dim 256), fp64 ------------------------ */
+int orc_q4_decode(int n_seq, int n_qh, int n_kv, const int32_t* seq_len,
+                  const int32_t* page_table, int max_pages, int page_size, int64_t n_cells,
+                  const uint8_t* k_pool, const uint8_t* v_pool, const float* q,
+                  const float* gate, double sm_scale, const int32_t* seq_sel, int n_sel,
+                  double* out, double* lse, uint32_t* bad_page);
+
 #endif
