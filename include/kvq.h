@@ -10,7 +10,8 @@
  *     (review-thread rebase notes);
  *   Strata PR #2533 "metal: q4_0 KV cache on the Mac engine" — the q4_0 block codec
  *     with the FWHT256 rotation, the paged append and the gather (kv_q4.metal port
- *     commit; parity-fixture commit).
+ *     commit; parity-fixture commit), and the decode attention over the q4_0 pools
+ *     (qsa decode commit).
  *
  * Conventions for every entry point
  *   - Pointers to tensors are DEVICE pointers owned by the caller.  libkvq allocates no
@@ -266,6 +267,55 @@ int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* works
  */
 int kvq_mla_decode_noalloc(const kvq_mla_problem* p, float* out, float* lse,
                            uint32_t* dev_status, kvq_stream_t stream);
+
+/*
+ * q4_0 paged decode attention, grouped-query, head_dim 256 — Strata PR #2533, the qsa
+ * decode commit: the query rows pass through the orthonormal 256-point FWHT (the
+ * rotation the K and V rows received when kvq_append_q4 stored them), attention reads
+ * the q4_0 pools with every block dequantised as (nibble - 8) * f32(d), and the merged
+ * output row is rotated back (the orthonormal FWHT is its own inverse) BEFORE the
+ * optional sigmoid(gate) multiply.  For sequence s and query head h, with KV head
+ * g = h / (n_qh / n_kv) and the tokens at positions 0 .. seq_len[s] - 1:
+ *   q_rot = FWHT256(q[s][h]) / 16,  score_t = sm_scale * q_rot . k_t,
+ *   out[s][h] = FWHT256(sum_t softmax(score)_t v_t) / 16  [* sigmoid(gate[s][h])],
+ *   lse[s][h] = log sum_t exp(score_t).
+ * Positions map to pool cells as in kvq_append_q4: page_table[s][t / page_size] *
+ * page_size + t % page_size.  A page index past max_pages, a missing page id (< 0) or a
+ * cell outside the pool skips that position and sets KVQ_DEV_BAD_PAGE; a sequence with no
+ * position gives out = 0, lse = -inf.  seq_len[s] is clamped to [0, max_seq_len].
+ * Computed as split-T partials (one warp per split, sequence and KV head) merged by a
+ * log-sum-exp combine.  Errors: KVQ_EINVAL (sizes, group ratio, NULL pointers),
+ * KVQ_EALIGN, KVQ_EWORKSPACE (workspace below kvq_q4_decode_workspace(p)), KVQ_ECUDA.
+ */
+typedef struct kvq_q4_problem {
+    int32_t n_seq;
+    int32_t n_qh;                   /* query heads                                      */
+    int32_t n_kv;                   /* KV heads; n_qh / n_kv is 1, 2, 4 or 8            */
+    int32_t head_dim;               /* 256                                              */
+    const int32_t* seq_len;         /* device [n_seq] tokens held                       */
+    int32_t max_seq_len;            /* host bound on every seq_len (sizes the splits)   */
+    const int32_t* page_table;      /* device [n_seq][max_pages]                        */
+    int32_t max_pages, page_size;
+    int64_t n_cells;                /* cells in each pool                               */
+    const uint8_t* k_pool;          /* device [n_cells][n_kv][144], 16-byte aligned      */
+    const uint8_t* v_pool;          /* device [n_cells][n_kv][144], 16-byte aligned      */
+    const float* q;                 /* device [n_seq][n_qh][256], not rotated, 16 B al. */
+    const float* gate;              /* device [n_seq][n_qh][256] or NULL                */
+    float sm_scale;
+    int32_t split_rows;             /* positions per split; 0: the library chooses      */
+} kvq_q4_problem;
+
+/* Bytes of workspace kvq_q4_decode needs for this problem (0 if invalid). */
+size_t kvq_q4_decode_workspace(const kvq_q4_problem* p);
+
+/*
+ *   out        device fp32 [n_seq][n_qh][256]
+ *   lse        device fp32 [n_seq][n_qh] or NULL (natural log)
+ *   workspace  device, >= kvq_q4_decode_workspace(p) bytes, 256-byte aligned
+ *   dev_status device u32 or NULL
+ */
+int kvq_q4_decode(const kvq_q4_problem* p, float* out, float* lse, void* workspace,
+                  size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,7 @@ __all__ = [
     "KvqError", "lib", "kvq_version", "kvq_tq4_codebook", "kvq_set_fault",
     "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
     "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "MlaCache",
-    "MlaProblem",
+    "MlaProblem", "Q4Problem", "make_q4_problem", "kvq_q4_decode", "kvq_q4_decode_workspace",
     "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
     "DEV_BAD_FORMAT",
 ]
@@ -35,7 +35,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_tq4_codebook", "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4",
            "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode",
-           "kvq_mla_decode_noalloc"]
+           "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode"]
 
 
 class KvqError(RuntimeError):
@@ -71,6 +71,14 @@ class MlaProblem(C.Structure):
                 ("fp8", MlaCache), ("tq4", MlaCache), ("tq4_signs", _p),
                 ("q_lat", _p), ("q_rope", _p), ("idx", _p), ("top_k", _i32),
                 ("sm_scale", _f32), ("split_rows", _i32), ("impl", _i32)]
+
+
+class Q4Problem(C.Structure):
+    _fields_ = [("n_seq", _i32), ("n_qh", _i32), ("n_kv", _i32), ("head_dim", _i32),
+                ("seq_len", _p), ("max_seq_len", _i32), ("page_table", _p),
+                ("max_pages", _i32), ("page_size", _i32), ("n_cells", _i64),
+                ("k_pool", _p), ("v_pool", _p), ("q", _p), ("gate", _p),
+                ("sm_scale", _f32), ("split_rows", _i32)]
 
 
 _lock = threading.Lock()
@@ -114,6 +122,10 @@ def _declare(L):
     L.kvq_mla_decode.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, C.c_size_t, _p, _p]
     L.kvq_mla_decode_noalloc.restype = C.c_int
     L.kvq_mla_decode_noalloc.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, _p]
+    L.kvq_q4_decode_workspace.restype = C.c_size_t
+    L.kvq_q4_decode_workspace.argtypes = [C.POINTER(Q4Problem)]
+    L.kvq_q4_decode.restype = C.c_int
+    L.kvq_q4_decode.argtypes = [C.POINTER(Q4Problem), _p, _p, _p, C.c_size_t, _p, _p]
 
 
 def _check(status: int):
@@ -248,3 +260,31 @@ def kvq_mla_decode_noalloc(p: MlaProblem, out, lse=None, dev_status=None, stream
     callers that cannot allocate device memory (see include/kvq.h)."""
     _check(lib().kvq_mla_decode_noalloc(C.byref(p), _ptr(out), _ptr(lse), _ptr(dev_status),
                                         _stream(stream)))
+
+
+def make_q4_problem(*, seq_len, page_table, page_size, k_pool, v_pool, q, sm_scale,
+                    max_seq_len, gate=None, split_rows=0) -> Q4Problem:
+    """Fill a kvq_q4_problem from torch tensors: pools [n_cells, n_kv, 144] uint8, q (and
+    gate) [n_seq, n_qh, 256] fp32, page_table [n_seq, max_pages] int32.  The returned
+    object keeps a reference to every tensor whose pointer it carries."""
+    n_seq, n_qh, hd = q.shape
+    p = Q4Problem()
+    p.n_seq, p.n_qh, p.n_kv, p.head_dim = n_seq, n_qh, k_pool.shape[1], hd
+    p.seq_len, p.max_seq_len = _ptr(seq_len), int(max_seq_len)
+    p.page_table, p.max_pages, p.page_size = _ptr(page_table), page_table.shape[-1], int(page_size)
+    p.n_cells = k_pool.shape[0]
+    p.k_pool, p.v_pool, p.q, p.gate = _ptr(k_pool), _ptr(v_pool), _ptr(q), _ptr(gate)
+    p.sm_scale, p.split_rows = float(sm_scale), int(split_rows)
+    p._keep = [seq_len, page_table, k_pool, v_pool, q, gate]
+    return p
+
+
+def kvq_q4_decode_workspace(p: Q4Problem) -> int:
+    return lib().kvq_q4_decode_workspace(C.byref(p))
+
+
+def kvq_q4_decode(p: Q4Problem, out, lse=None, workspace=None, dev_status=None,
+                  stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kvq_q4_decode(C.byref(p), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                               _ptr(dev_status), _stream(stream)))

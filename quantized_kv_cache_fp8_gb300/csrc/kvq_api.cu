@@ -267,4 +267,53 @@ int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* works
                                               (cudaStream_t)stream), E);
 }
 
+static int validate_q4_decode(const kvq_q4_problem* p, const char* E)
+{
+    if (!p) return fail(KVQ_EINVAL, "%s: NULL problem", E);
+    if (p->head_dim != 256) return fail(KVQ_EINVAL, "%s: head_dim must be 256", E);
+    if (p->n_seq < 0 || p->n_seq > 65535) return fail(KVQ_EINVAL, "%s: n_seq outside [0, 65535]", E);
+    if (p->n_kv < 1 || p->n_kv > 65535 || p->n_qh < 1 || p->n_qh % p->n_kv != 0)
+        return fail(KVQ_EINVAL, "%s: n_qh must be a positive multiple of n_kv", E);
+    const int grp = p->n_qh / p->n_kv;
+    if (grp != 1 && grp != 2 && grp != 4 && grp != 8)
+        return fail(KVQ_EINVAL, "%s: n_qh / n_kv must be 1, 2, 4 or 8", E);
+    if (p->max_seq_len < 0 || p->split_rows < 0) return fail(KVQ_EINVAL, "%s: bad sizes", E);
+    if (p->max_pages < 1 || p->page_size < 1 || p->n_cells < 0)
+        return fail(KVQ_EINVAL, "%s: bad paging sizes", E);
+    if (!(p->sm_scale == p->sm_scale)) return fail(KVQ_EINVAL, "%s: sm_scale is NaN", E);
+    if (p->n_seq == 0) return KVQ_OK;
+    if (!p->seq_len || !p->page_table || !p->k_pool || !p->v_pool || !p->q)
+        return fail(KVQ_EINVAL, "%s: NULL pointer", E);
+    if (!aligned(p->k_pool, 16) || !aligned(p->v_pool, 16) || !aligned(p->q, 16) ||
+        (p->gate && !aligned(p->gate, 16)))
+        return fail(KVQ_EALIGN, "%s: pools, q and gate must be 16-byte aligned", E);
+    return KVQ_OK;
+}
+
+size_t kvq_q4_decode_workspace(const kvq_q4_problem* p)
+{
+    if (validate_q4_decode(p, "kvq_q4_decode_workspace") != KVQ_OK) return 0;
+    kvq::Q4Plan plan;
+    kvq::plan_q4_decode(*p, plan);
+    return plan.bytes;
+}
+
+int kvq_q4_decode(const kvq_q4_problem* p, float* out, float* lse, void* workspace,
+                  size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream)
+{
+    const char* E = "kvq_q4_decode";
+    if (int st = injected(E)) return st;
+    if (int st = validate_q4_decode(p, E)) return st;
+    if (p->n_seq == 0) return KVQ_OK;
+    if (!out) return fail(KVQ_EINVAL, "%s: NULL out", E);
+    if (!aligned(out, 16) || (lse && !aligned(lse, 4))) return fail(KVQ_EALIGN, "%s: out/lse misaligned", E);
+    kvq::Q4Plan plan;
+    kvq::plan_q4_decode(*p, plan);
+    if (!workspace || ws_bytes < plan.bytes)
+        return fail(KVQ_EWORKSPACE, "%s: workspace %zu bytes, need %zu", E, ws_bytes, plan.bytes);
+    if (!aligned(workspace, 256)) return fail(KVQ_EALIGN, "%s: workspace not 256-byte aligned", E);
+    return cuda_status(kvq::launch_q4_decode(*p, plan, out, lse, workspace, dev_status,
+                                             (cudaStream_t)stream), E);
+}
+
 }  // extern "C"

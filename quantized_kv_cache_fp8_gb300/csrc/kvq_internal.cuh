@@ -132,4 +132,13 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s);
 
+struct Q4Plan {
+    int split_rows = 0;     // positions per split
+    int n_splits = 0;       // splits per (seq, KV head)
+    size_t off_ml = 0, off_o = 0, bytes = 0;
+};
+bool plan_q4_decode(const kvq_q4_problem& p, Q4Plan& plan);
+cudaError_t launch_q4_decode(const kvq_q4_problem& p, const Q4Plan& plan, float* out, float* lse,
+                             void* ws, uint32_t* dev_status, cudaStream_t s);
+
 }  // namespace kvq

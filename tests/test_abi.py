@@ -109,6 +109,45 @@ def test_decode_argument_errors(kvq):
     assert L.kvq_mla_decode_workspace(C.byref(_problem(kvq, d_lat=7))) == 0
 
 
+def _q4_problem(kvq, **kw):
+    p = kvq.Q4Problem()
+    base = dict(n_seq=2, n_qh=16, n_kv=8, head_dim=256, seq_len=FAKE, max_seq_len=4096,
+                page_table=FAKE, max_pages=64, page_size=64, n_cells=8192, k_pool=FAKE,
+                v_pool=FAKE, q=FAKE, gate=None, sm_scale=0.0625, split_rows=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_q4_decode_argument_errors(kvq):
+    L = kvq.lib()
+    dec = lambda p, ws=None, n=0: L.kvq_q4_decode(C.byref(p), FAKE, None, ws, n, None, None)
+    assert dec(_q4_problem(kvq, head_dim=128)) == 1
+    assert dec(_q4_problem(kvq, n_qh=12)) == 1                        # not a multiple of n_kv
+    assert dec(_q4_problem(kvq, n_qh=48, n_kv=8)) == 1                # ratio 6
+    assert dec(_q4_problem(kvq, n_qh=128, n_kv=8)) == 1               # ratio 16
+    assert dec(_q4_problem(kvq, page_size=0)) == 1
+    assert dec(_q4_problem(kvq, v_pool=None)) == 1
+    assert dec(_q4_problem(kvq, k_pool=FAKE + 8)) == 4
+    assert dec(_q4_problem(kvq, gate=FAKE + 4)) == 4
+    assert dec(_q4_problem(kvq, sm_scale=float("nan"))) == 1
+    assert L.kvq_q4_decode(C.byref(_q4_problem(kvq)), FAKE + 4, None, None, 0, None, None) == 4
+    p = _q4_problem(kvq)
+    need = L.kvq_q4_decode_workspace(C.byref(p))
+    assert need > 0
+    assert dec(p) == 5
+    assert dec(p, FAKE, need - 1) == 5
+    assert dec(p, FAKE + 64, need) == 4
+    assert L.kvq_q4_decode_workspace(C.byref(_q4_problem(kvq, n_kv=3))) == 0
+    # n_seq == 0 is a valid empty call that touches nothing
+    assert dec(_q4_problem(kvq, n_seq=0, seq_len=None, q=None)) == 0
+    # the workspace holds (m, l) and a 256-float partial per (sequence, head, split)
+    p1 = _q4_problem(kvq, split_rows=1024)
+    rows, splits = 2 * 16, 4
+    assert L.kvq_q4_decode_workspace(C.byref(p1)) >= rows * splits * (2 + 256) * 4
+
+
 def test_fault_injection(kvq):
     L = kvq.lib()
     assert L.kvq_set_fault(b"nonsense") == 1
@@ -133,6 +172,8 @@ def test_struct_layouts_match_headers(kvq, tmp_path):
         'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(kvq_mla_cache),'
         ' sizeof(kvq_gather_desc), sizeof(kvq_mla_problem), offsetof(kvq_mla_problem, impl),'
         ' offsetof(kvq_gather_desc, dev_status), sizeof(orc_mla), offsetof(orc_mla, n_sel));'
+        'printf("%zu %zu %zu\\n", sizeof(kvq_q4_problem), offsetof(kvq_q4_problem, gate),'
+        ' offsetof(kvq_q4_problem, split_rows));'
         'return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(ROOT, "oracle"),
@@ -141,7 +182,8 @@ def test_struct_layouts_match_headers(kvq, tmp_path):
                                           check=True).stdout.split()]
     want = [C.sizeof(kvq.MlaCache), C.sizeof(kvq.GatherDesc), C.sizeof(kvq.MlaProblem),
             kvq.MlaProblem.impl.offset, kvq.GatherDesc.dev_status.offset,
-            C.sizeof(oracle.OrcMla), oracle.OrcMla.n_sel.offset]
+            C.sizeof(oracle.OrcMla), oracle.OrcMla.n_sel.offset,
+            C.sizeof(kvq.Q4Problem), kvq.Q4Problem.gate.offset, kvq.Q4Problem.split_rows.offset]
     assert got == want
 
 
