@@ -443,9 +443,9 @@ def run_codecs(args, local):
     pos0, table, n_cells = W.paged_table(n_seq, n_tok, ps, ps - 8, seed=0)
     amp = torch.tensor([1e-3, 1.0, 40.0], device=dev)
 
-    def rows_kv():
-        r = torch.randn(n_seq, n_tok, n_heads, 256, generator=gen, device=dev)
-        return r * amp[torch.randint(0, 3, (n_seq, n_tok, n_heads, 1), generator=gen, device=dev)]
+    def rows_kv(n=n_seq):
+        r = torch.randn(n, n_tok, n_heads, 256, generator=gen, device=dev)
+        return r * amp[torch.randint(0, 3, (n, n_tok, n_heads, 1), generator=gen, device=dev)]
 
     k, v = rows_kv(), rows_kv()
     pos0_d = torch.from_numpy(pos0).to(dev)
@@ -461,7 +461,32 @@ def run_codecs(args, local):
     s = timed(lambda: kvq.kvq_gather_q4(k_pool, pos0_d, n_tok, table_d, ps, n_cells, out))
     report("kvq_gather (q4_0)", f"one pool: {n_seq} seqs x {n_tok} tokens x {n_heads} heads -> fp16",
            toks * n_heads * (144 + 256 * 2) + table.size * 4, s, toks, "tokens")
-    del out, k_pool, v_pool
+    del out
+
+    # q4_0 decode attention over the same pools' layout: 16 sequences x 8192 positions
+    # (appended from position 0), 8 KV heads, 16 query heads (two per KV head), gated
+    pos0z, table_z, _ = W.paged_table(n_seq, n_tok, ps, 0, seed=1)
+    pos0z_d, table_zd = torch.from_numpy(pos0z).to(dev), torch.from_numpy(table_z).to(dev)
+    for s0 in range(0, n_seq, 4):                   # 4 sequences of K, V rows at a time
+        kk, vv = rows_kv(4), rows_kv(4)
+        kvq.kvq_append_q4(kk, vv, pos0z_d[s0:s0 + 4], table_zd[s0:s0 + 4], ps, n_cells, k_pool, v_pool)
+        del kk, vv
+    n_qh = 16
+    qd = torch.randn(n_seq, n_qh, 256, generator=gen, device=dev)
+    gate = torch.randn(n_seq, n_qh, 256, generator=gen, device=dev)
+    seq_len = torch.full((n_seq,), n_tok, dtype=torch.int32, device=dev)
+    prob = kvq.make_q4_problem(seq_len=seq_len, page_table=table_zd, page_size=ps, k_pool=k_pool,
+                               v_pool=v_pool, q=qd, gate=gate, sm_scale=1.0 / 16, max_seq_len=n_tok)
+    ws = torch.empty(kvq.kvq_q4_decode_workspace(prob), dtype=torch.uint8, device=dev)
+    out = torch.empty(n_seq, n_qh, 256, device=dev)
+    lse = torch.empty(n_seq, n_qh, device=dev)
+    s = timed(lambda: kvq.kvq_q4_decode(prob, out, lse, ws))
+    assert torch.isfinite(out).all()
+    report("kvq_q4_decode", f"{n_seq} seqs x {n_tok} positions, {n_heads} KV heads x 2 query heads, "
+           f"head_dim 256, pages of {ps}, gated",
+           toks * n_heads * 288 + 3 * n_seq * n_qh * 1024 + n_seq * n_qh * 4 + table_z.size * 4,
+           s, toks, "tokens")
+    del out, k_pool, v_pool, ws
 
     # a7: sparse row gather of the fp8 MLA cache, top-k = 2048 of T = 131072
     T, k_sel = 131072, 2048

@@ -4,20 +4,26 @@
 // dequantised as (nibble - 8) * f32(d), and the merged output is rotated back before
 // the optional sigmoid gate.
 //
-// A few query heads share each KV head (G = n_qh / n_kv <= 8), so a row carries
-// 2 G (256 + 256) flops for 288 bytes: CUDA-core work, bound by streaming the pools.
-// One warp per (split, sequence, KV head); lane l owns dims 8l .. 8l + 7 of the
-// 256-wide rows, which are elements 8p .. 8p + 7 of block b = l / 4 (p = l % 4): the
-// low nibbles of bytes 2 + 8p .. 9 + 8p for p < 2, the high nibbles of bytes
-// 2 + 8(p - 2) .. for p >= 2.  Rows go in groups of R = 32 / G, so the R x G partial
-// scores of a group are 32 values and one transposing butterfly hands each lane one
-// full score.  Each row's bytes are staged through shared memory with 16-byte loads,
-// the next group's loads in flight while the current group is reduced.  Split-T
-// partials (m, l, o in the rotated domain, log2 units) are merged by a combine kernel
-// that also rotates back and gates.
+// One warp per (split, sequence, KV head) [and half of the 8 query heads when a KV head
+// serves 8]; four such warps per CTA, each with its own 2-stage cp.async ring of 16-row
+// tiles (the K and V rows of 16 positions, 4.5 KB); 128 registers, four CTAs per SM.
+// Both contractions of a tile run on the tensor cores with register operands
+// (mma.sync m16n8k16, fp16 in, fp32 out; the operands are built in registers, so
+// there is no shared-memory or tensor-memory operand image to stage):
+//   score    S[row][n]  = sum_k (code - 8)[row][k] * Q[k][n]      per 32-element block,
+//                         then sum over blocks of d_K[row][block] * S_block
+//   context  O[dim][n] += sum_row (code - 8)[row][dim] * P[row][n][block(dim)]
+// The codes are exact in fp16: one lop3 puts two nibbles into the mantissas of 1024 + c
+// and one packed subtract (or fma, for high nibbles) leaves c - 8.  The fp32 operands
+// (the rotated query; P = p * d_V) are split into fp16 value + fp16 residual columns
+// (n = 2 * head + part), so the products keep ~22 bits; a power-of-two scale keeps
+// them inside the fp16 range (fixed per split for Q, per tile for P with the running
+// output rescaled when it changes).  Split-T partials (m, l, o in the rotated domain,
+// log2 units) are merged by a combine kernel that also rotates back and gates.
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "kvq_internal.cuh"
@@ -30,10 +36,13 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRowBytes = 144;           // 8 blocks of 18 bytes
+constexpr int kMaxDevices = 64;
 
 struct Q4Args {
     kvq_q4_problem p;
     int split_rows, n_splits;
+    int n_hg;                            // warps per (split, sequence, KV head): 2 when 8 heads share it
+    int64_t n_units;                     // n_splits * n_seq * n_kv * n_hg
     float* part_ml;                      // [n_seq][n_qh][n_splits][2]
     float* part_o;                       // [n_seq][n_qh][n_splits][256]
     float* out;
@@ -67,215 +76,383 @@ __device__ __forceinline__ void fwht256_lane8(float (&z)[8], int lane)
     }
 }
 
-// the 8 codes of this lane in a staged row, as (code - 8) floats, and the block scale
-__device__ __forceinline__ float lane_codes(const uint8_t* row, int lane, float (&x)[8])
+__device__ __forceinline__ float exp2i(int k)             // 2^k, k in [-126, 127]
 {
-    const int b = lane >> 2, p = lane & 3;
-    const uint8_t* blk = row + 18 * b;
-    const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk)));
-    const uint16_t* w = reinterpret_cast<const uint16_t*>(blk + 2 + 8 * (p & 1));
-    const uint32_t lo = (uint32_t)w[0] | ((uint32_t)w[1] << 16);
-    const uint32_t hi = (uint32_t)w[2] | ((uint32_t)w[3] << 16);
-    const int sh = p >= 2 ? 4 : 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t word = k < 4 ? lo : hi;
-        const uint32_t code = (word >> (8 * (k & 3) + sh)) & 15u;
-        // 2^23 + code, minus 2^23 + 8: exact
-        x[k] = __uint_as_float(0x4B000000u | code) - 8388616.0f;
-    }
-    return d;
+    return __int_as_float((k + 127) << 23);
 }
 
-// sum over the warp's lanes of each of 32 values, transposed: lane l ends with value l
-__device__ __forceinline__ float reduce_transpose32(float (&v)[32], int lane)
+__device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
+
+__device__ __forceinline__ uint16_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+
+// {lo, hi} -> f16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
-#pragma unroll
-        for (int j = 0; j < w; ++j) {
-            const float send = up ? v[j] : v[j + w];
-            const float keep = up ? v[j + w] : v[j];
-            v[j] = keep + __shfl_xor_sync(kFull, send, w);
-        }
-    }
-    return v[0];
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
-template <int G>
-__global__ void __launch_bounds__(32) q4_decode_kernel(const __grid_constant__ Q4Args a)
+__device__ __forceinline__ void unpack_h2(uint32_t h, float& lo, float& hi)
 {
-    constexpr int R = 32 / G;                        // rows per group
-    constexpr int kPieces = 2 * R * (kRowBytes / 16);    // K and V rows, 16-byte pieces
-    constexpr int kPerLane = (kPieces + 31) / 32;
-    __shared__ __align__(16) uint8_t s_rows[2 * R * kRowBytes];
+    asm("{.reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h;}"
+        : "=f"(lo), "=f"(hi) : "r"(h));
+}
+
+// The fp16 values (part 0) or the fp16 residuals x - f16(x) (part 1) of a pair.
+__device__ __forceinline__ uint32_t split_pair(float x, float y, float part)
+{
+    float hx, hy;
+    unpack_h2(pack_h2(x, y), hx, hy);
+    return pack_h2(fmaf(-part, hx, x), fmaf(-part, hy, y));
+}
+
+// Nibbles at bits 0-3 and 16-19 of x as f16x2 {c - 8, c' - 8}: 0x6400 | c is 1024 + c.
+__device__ __forceinline__ uint32_t nib_lo(uint32_t x)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(0x000F000Fu), "r"(0x64006400u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x64086408u));        // - 1032
+    return r;
+}
+
+// Nibbles at bits 4-7 and 20-23: 0x6400 | 16c is 1024 + 16c; (1024 + 16c) / 16 - 72 = c - 8.
+__device__ __forceinline__ uint32_t nib_hi(uint32_t x)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(0x00F000F0u), "r"(0x64006400u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(r), "r"(0x2C002C00u), "r"(0xD480D480u));
+    return r;
+}
+
+// D += A (16 x 16, row-major) * B (16 x 8, column-major), fp16 in, fp32 accumulate
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Code bytes 4t .. 4t + 3 of a block (they start 2 bytes into the block, so the word is
+// 4-byte aligned in odd blocks only).
+template <bool kOdd>
+__device__ __forceinline__ uint32_t code_word(const uint8_t* p)
+{
+    if constexpr (kOdd) return *reinterpret_cast<const uint32_t*>(p);
+    else return __byte_perm(lds16(p), lds16(p + 2), 0x5410);
+}
+
+constexpr int kTileRows = 16;
+constexpr int kStages = 2;
+constexpr int kWarps = 4;
+constexpr int kStageBytes = 2 * kTileRows * kRowBytes;    // K rows 0..15, then V rows 0..15
+
+// dynamic shared memory: per warp kStages tiles, then per warp the score's B fragments
+// (8 blocks x 32 lanes x 16 B), then per warp kStages row-validity masks.  The rotated
+// query rows (fp32, at most 4 KB) are built in the last stage, which the prologue leaves
+// free.
+constexpr int kFragBytes = 8 * 32 * 16;
+constexpr size_t kQ4SmemBytes = (size_t)kWarps * (kStages * kStageBytes + kFragBytes + kStages * 4);
+static_assert(4 * 256 * 4 <= kStageBytes, "query scratch must fit in one stage");
+
+template <int GH>   // query heads per warp: 1, 2 or 4
+__global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_constant__ Q4Args a)
+{
+    extern __shared__ __align__(16) uint8_t q4_smem[];
     grid_dependents_launch();                        // the combine may start launching
     const kvq_q4_problem& p = a.p;
-    const int split = blockIdx.x, s = blockIdx.y, kvh = blockIdx.z;
-    const int lane = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t u = (int64_t)blockIdx.x * kWarps + warp;
+    if (u >= a.n_units) return;
+    const int hh = (int)(u % a.n_hg);
+    int64_t rest = u / a.n_hg;
+    const int kvh = (int)(rest % p.n_kv);
+    rest /= p.n_kv;
+    const int s = (int)(rest % p.n_seq);
+    const int split = (int)(rest / p.n_seq);
+    const int64_t head0 = (int64_t)s * p.n_qh + (int64_t)kvh * (p.n_qh / p.n_kv) + hh * GH;
     const int L = min(max(p.seq_len[s], 0), p.max_seq_len);
     const int64_t r0 = (int64_t)split * a.split_rows;
     const int64_t r1 = min(r0 + (int64_t)a.split_rows, (int64_t)L);
-    const int64_t head0 = (int64_t)s * p.n_qh + (int64_t)kvh * G;
     if (r0 >= r1) {
-        if (lane < G) {
+        if (lane < GH) {
             const int64_t sl = (head0 + lane) * a.n_splits + split;
             a.part_ml[sl * 2] = -INFINITY;
             a.part_ml[sl * 2 + 1] = 0.0f;
         }
         return;
     }
-    // rotated queries of the G heads, pre-scaled into log2 units: 8 dims per lane
-    float qr[G][8];
-    const float qs = p.sm_scale * kLog2e * (1.0f / 16.0f);
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t (*tiles)[kStageBytes] = reinterpret_cast<uint8_t (*)[kStageBytes]>(q4_smem + warp * kStages * kStageBytes);
+    uint4* frag = reinterpret_cast<uint4*>(q4_smem + kWarps * kStages * kStageBytes + warp * kFragBytes);
+    unsigned* valid_of = reinterpret_cast<unsigned*>(q4_smem + kWarps * (kStages * kStageBytes + kFragBytes)) + warp * kStages;
+    float* qs = reinterpret_cast<float*>(tiles[kStages - 1]);
+
+    // ---- tile loads: lane l copies row l & 15 of K (l < 16) or V (l >= 16), 9 x 16 B
+    const int n_tiles = (int)((r1 - r0 + kTileRows - 1) / kTileRows);
+    const int64_t cell_stride = (int64_t)p.n_kv * kRowBytes;
+    const uint8_t* pool = (lane < 16 ? p.k_pool : p.v_pool) + (int64_t)kvh * kRowBytes;
+    const int32_t* table = p.page_table + (int64_t)s * p.max_pages;
+    // positions are below 2^31 (seq_len is int32): 32-bit page arithmetic
+    auto page_id = [&](int tile) -> int {
+        const int pos = (int)r0 + tile * kTileRows + (lane & 15);
+        if (pos >= (int)r1) return -1;
+        const int page = pos / p.page_size;
+        return page < p.max_pages ? __ldg(table + page) : -1;
+    };
+    auto issue = [&](int tile, int pid) {
+        const int pos = (int)r0 + tile * kTileRows + (lane & 15);
+        int64_t cell = -1;
+        if (pos < (int)r1) {
+            cell = (int64_t)pid * p.page_size + (pos - (pos / p.page_size) * p.page_size);
+            if (pid < 0 || cell >= p.n_cells) {
+                if (a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_PAGE);
+                cell = -1;
+            }
+        }
+        const int st = tile % kStages;
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(tiles[st] + lane * kRowBytes);
+        const uint8_t* src = pool + (cell < 0 ? 0 : cell) * cell_stride;
+        const uint32_t nb = cell < 0 ? 0u : 16u;     // 0: zero-fill, read nothing
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
+        for (int i = 0; i < kRowBytes / 16; ++i) cp_async16(dst + 16 * i, src + 16 * i, nb);
+        const unsigned m = __ballot_sync(kFull, cell >= 0) & 0xFFFFu;
+        if (lane == 0) valid_of[st] = m;
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+        if (i < n_tiles) issue(i, page_id(i));
+        cp_async_commit();
+    }
+    int pid_next = (kStages - 1 < n_tiles) ? page_id(kStages - 1) : -1;
+
+    // ---- query: rotate, scale into log2 units, choose a power of two for the fp16 split
+    const float qmul = p.sm_scale * kLog2e * (1.0f / 16.0f);
+    float qmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < GH; ++j) {
         const float4* qp = reinterpret_cast<const float4*>(p.q + (head0 + j) * 256 + 8 * lane);
         const float4 x0 = qp[0], x1 = qp[1];
         float z[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         fwht256_lane8(z, lane);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) qr[j][k] = z[k] * qs;
+        for (int k = 0; k < 8; ++k) {
+            z[k] *= qmul;
+            qmax = fmaxf(qmax, fabsf(z[k]));
+        }
+        float4* qd = reinterpret_cast<float4*>(qs + j * 256 + 8 * lane);
+        qd[0] = make_float4(z[0], z[1], z[2], z[3]);
+        qd[1] = make_float4(z[4], z[5], z[6], z[7]);
     }
-    float o[G][8];
 #pragma unroll
-    for (int j = 0; j < G; ++j)
+    for (int w = 16; w >= 1; w >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(kFull, qmax, w));
+    const int qexp = qmax > 0.0f ? (int)((__float_as_uint(qmax) >> 23) & 0xFF) - 127 : 0;
+    const int sigma = min(max(13 - qexp, -100), 100);   // max |Q| * 2^sigma in [2^13, 2^14)
+    const float qscale = exp2i(sigma), sinv = exp2i(-sigma);
+    __syncwarp();
+    // B operand of the score: column n = g is head g >> 1, part g & 1; rows k = 2t, 2t+1
+    // are code bytes 4t, 4t+2 and rows 2t+8, 2t+9 bytes 4t+1, 4t+3 of the block
+    const int jq = g >> 1;
+    const float part = (g & 1) ? 1.0f : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) o[j][k] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f;           // of head (lane % G)
+    for (int b = 0; b < 8; ++b) {
+        uint32_t w[4];
+#pragma unroll
+        for (int hn = 0; hn < 2; ++hn) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (jq < GH) v = *reinterpret_cast<const float4*>(qs + jq * 256 + 32 * b + 16 * hn + 4 * t);
+            w[2 * hn] = split_pair(v.x * qscale, v.z * qscale, part);
+            w[2 * hn + 1] = split_pair(v.y * qscale, v.w * qscale, part);
+        }
+        frag[b * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();                                    // the query scratch becomes a stage again
 
-    // pool cell of position t, or -1 (flagged)
-    auto cell_of = [&](int64_t t) -> int64_t {
-        if (t >= r1) return -1;
-        const int64_t page = t / p.page_size;
-        const int64_t pid = page < p.max_pages ? p.page_table[(int64_t)s * p.max_pages + page] : -1;
-        const int64_t cell = pid * p.page_size + t % p.page_size;
-        if (pid < 0 || cell >= p.n_cells) {
-            if (a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_PAGE);
-            return -1;
-        }
-        return cell;
-    };
-    // this lane's pieces of a group's rows (K rows 0..R-1, then V rows), zero for
-    // masked rows
-    auto load_group = [&](int64_t t0, uint4 (&pc)[kPerLane], int64_t& my_cell) {
-        my_cell = lane < R ? cell_of(t0 + lane) : -1;
+    float o[8][2][4];
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int idx = lane + 32 * i;
-            const int row = idx / 9, piece = idx - row * 9;
-            const int r = row % R;
-            const int64_t cell = __shfl_sync(kFull, my_cell, r);
-            pc[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (idx < kPieces && cell >= 0) {
-                const uint8_t* pool = row < R ? p.k_pool : p.v_pool;
-                pc[i] = __ldcs(reinterpret_cast<const uint4*>(pool + (cell * p.n_kv + kvh) * kRowBytes) + piece);
-            }
-        }
-    };
-    uint4 nxt[kPerLane];
-    int64_t ncell;
-    load_group(r0, nxt, ncell);
-    for (int64_t t0 = r0; t0 < r1; t0 += R) {
-        const int64_t cur_cell = ncell;
+    for (int b = 0; b < 8; ++b)
 #pragma unroll
-        for (int i = 0; i < kPerLane; ++i)
-            if (lane + 32 * i < kPieces) reinterpret_cast<uint4*>(s_rows)[lane + 32 * i] = nxt[i];
-        if (t0 + R < r1) load_group(t0 + R, nxt, ncell);
+        for (int k = 0; k < 4; ++k) o[b][0][k] = o[b][1][k] = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f;           // head t (t < GH)
+    int tau = 40;                                    // P carries 2^tau
+
+    for (int i = 0; i < n_tiles; ++i) {
+        const int ti = i + kStages - 1;
+        if (ti < n_tiles) {
+            issue(ti, pid_next);
+            if (ti + 1 < n_tiles) pid_next = page_id(ti + 1);
+        }
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
         __syncwarp();
-        // scores: partial dot products of this lane's 8 dims, one per (row, head)
-        float part[32];
-        float dk[R];
+        const uint8_t* sK = tiles[i % kStages];
+        const uint8_t* sV = sK + kTileRows * kRowBytes;
+        const unsigned valid = valid_of[i % kStages];
+
+        // ---- scores of rows g and g + 8 for head t
+        float sg = 0.0f, sg8 = 0.0f;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float x[8];
-            dk[r] = lane_codes(s_rows + r * kRowBytes, lane, x);
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) acc = fmaf(qr[j][k], x[k], acc);
-                part[r * G + j] = acc * dk[r];
+        for (int b = 0; b < 8; ++b) {
+            const uint8_t* rg = sK + g * kRowBytes + 18 * b;
+            const uint8_t* rg8 = rg + 8 * kRowBytes;
+            uint32_t xg, xg8;
+            if (b & 1) {
+                xg = code_word<true>(rg + 2 + 4 * t);
+                xg8 = code_word<true>(rg8 + 2 + 4 * t);
+            } else {
+                xg = code_word<false>(rg + 2 + 4 * t);
+                xg8 = code_word<false>(rg8 + 2 + 4 * t);
             }
+            const uint4 bq = frag[b * 32 + lane];
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma16816(c, nib_lo(xg), nib_lo(xg8), nib_lo(xg >> 8), nib_lo(xg8 >> 8), bq.x, bq.y);
+            mma16816(c, nib_hi(xg), nib_hi(xg8), nib_hi(xg >> 8), nib_hi(xg8 >> 8), bq.z, bq.w);
+            sg = fmaf(h2f(lds16(rg)), c[0] + c[1], sg);
+            sg8 = fmaf(h2f(lds16(rg8)), c[2] + c[3], sg8);
         }
-        float sc = reduce_transpose32(part, lane);   // row lane / G, head lane % G
-        const bool valid = __shfl_sync(kFull, cur_cell, lane / G) >= 0;
-        sc = valid ? sc : -INFINITY;
-        // online softmax per head over the R rows (lanes of equal lane % G)
-        float mx = sc;
-#pragma unroll
-        for (int w = G; w < 32; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, w));
+        const bool head_ok = t < GH;
+        const bool vg = head_ok && ((valid >> g) & 1u), vg8 = head_ok && ((valid >> (g + 8)) & 1u);
+        const float s0 = vg ? sg * sinv : -INFINITY;
+        const float s1 = vg8 ? sg8 * sinv : -INFINITY;
+        // ---- online softmax of head t over the 16 rows (lanes of equal t)
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
         const float m_new = fmaxf(m_run, mx);
-        const float pw = (sc == -INFINITY) ? 0.0f : exp2f(sc - m_new);
-        const float alpha = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new);
-        float ps = pw;
-#pragma unroll
-        for (int w = G; w < 32; w <<= 1) ps += __shfl_xor_sync(kFull, ps, w);
+        const float alpha = (m_new == m_run) ? 1.0f : exp2f(m_run - m_new);
+        const float p0 = vg ? exp2f(s0 - m_new) : 0.0f;
+        const float p1 = vg8 ? exp2f(s1 - m_new) : 0.0f;
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(kFull, ps, 4);
+        ps += __shfl_xor_sync(kFull, ps, 8);
+        ps += __shfl_xor_sync(kFull, ps, 16);
         l_run = l_run * alpha + ps;
         m_run = m_new;
-        // context: o[j] = alpha_j o[j] + sum_r p[r][j] d_v[r] (code - 8)
+        // ---- the tile's largest V block scale bounds P = p * d (p <= 1): P * 2^tau < 2^15
+        const uint8_t* rv = sV + (lane & 15) * kRowBytes + 72 * (lane >> 4);
+        uint32_t dm = max(max(lds16(rv) & 0x7FFFu, lds16(rv + 18) & 0x7FFFu),
+                          max(lds16(rv + 36) & 0x7FFFu, lds16(rv + 54) & 0x7FFFu));
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            const float al = __shfl_sync(kFull, alpha, j);
+        for (int w = 16; w >= 1; w >>= 1) dm = max(dm, __shfl_xor_sync(kFull, dm, w));
+        int tau_new = tau;
+        if (dm != 0) tau_new = min(tau, 14 - (dm >= 0x400u ? (int)(dm >> 10) - 15 : -15));
+        const float f = alpha * exp2i(tau_new - tau);
+        if (__any_sync(kFull, f != 1.0f)) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) o[j][k] *= al;
+            for (int b = 0; b < 8; ++b)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[b][0][k] *= f;
+                    o[b][1][k] *= f;
+                }
         }
+        tau = tau_new;
+        // ---- B operand of the context: column n = g (head g >> 1, part g & 1), rows
+        // k = 2t, 2t+1, 2t+8, 2t+9 of the tile; softmax weights from the score lanes
+        const int src = 8 * t + (g >> 1);
+        const float pscale = ((g >> 1) < GH) ? exp2i(tau) : 0.0f;
+        const float pa = __shfl_sync(kFull, p0, src) * pscale;
+        const float pb = __shfl_sync(kFull, p0, src + 4) * pscale;
+        const float pc = __shfl_sync(kFull, p1, src) * pscale;
+        const float pd = __shfl_sync(kFull, p1, src + 4) * pscale;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float x[8];
-            const float dv = lane_codes(s_rows + (R + r) * kRowBytes, lane, x);
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float pj = __shfl_sync(kFull, pw, r * G + j) * dv;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) o[j][k] = fmaf(pj, x[k], o[j][k]);
-            }
+        for (int b = 0; b < 8; ++b) {
+            const uint8_t* v0 = sV + 2 * t * kRowBytes + 18 * b;
+            const uint8_t* v1 = v0 + kRowBytes;
+            const uint8_t* v2 = v0 + 8 * kRowBytes;
+            const uint8_t* v3 = v2 + kRowBytes;
+            const uint32_t b0 = split_pair(pa * h2f(lds16(v0)), pb * h2f(lds16(v1)), part);
+            const uint32_t b1 = split_pair(pc * h2f(lds16(v2)), pd * h2f(lds16(v3)), part);
+            // A = V^T: m = g is code byte 2g, m = g + 8 byte 2g + 1; k = rows
+            const uint32_t X = __byte_perm(lds16(v0 + 2 + 2 * g), lds16(v1 + 2 + 2 * g), 0x5410);
+            const uint32_t Y = __byte_perm(lds16(v2 + 2 + 2 * g), lds16(v3 + 2 + 2 * g), 0x5410);
+            mma16816(o[b][0], nib_lo(X), nib_lo(X >> 8), nib_lo(Y), nib_lo(Y >> 8), b0, b1);
+            mma16816(o[b][1], nib_hi(X), nib_hi(X >> 8), nib_hi(Y), nib_hi(Y >> 8), b0, b1);
         }
-        __syncwarp();
+        __syncwarp();                                // the stage is refilled next iteration
     }
-    // partials: (m, l) of head j from lane j, o of all heads from every lane
-    if (lane < G) {
-        const int64_t sl = (head0 + lane) * a.n_splits + split;
-        a.part_ml[sl * 2] = m_run;
-        a.part_ml[sl * 2 + 1] = l_run;
-    }
+    // ---- partials: (m, l) of head t from lane t, o of head t: dims 32b + 16mt + 2g (+1)
+    if (t < GH) {
+        const int64_t sl = (head0 + t) * a.n_splits + split;
+        if (g == 0) {
+            a.part_ml[sl * 2] = m_run;
+            a.part_ml[sl * 2 + 1] = l_run;
+        }
+        const float inv = exp2i(-tau);
+        float* dst = a.part_o + sl * 256 + 2 * g;
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + ((head0 + j) * a.n_splits + split) * 256 + 8 * lane);
-        dst[0] = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
-        dst[1] = make_float4(o[j][4], o[j][5], o[j][6], o[j][7]);
+        for (int b = 0; b < 8; ++b)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                *reinterpret_cast<float2*>(dst + 32 * b + 16 * mt) =
+                    make_float2((o[b][mt][0] + o[b][mt][1]) * inv, (o[b][mt][2] + o[b][mt][3]) * inv);
     }
 }
 
-// one warp per (sequence, query head): merge the splits, rotate back, gate
-__global__ void __launch_bounds__(256) q4_combine_kernel(const __grid_constant__ Q4Args a)
+// One CTA of 8 warps per (sequence, query head): warp w folds splits w, w + 8, ... into
+// its partial row (independent loads, lane = 8 dims); the 8 partial rows are summed in
+// shared memory, and warp 0 rotates back and gates.
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCombineWarps) q4_combine_kernel(const __grid_constant__ Q4Args a)
 {
+    __shared__ __align__(16) float s_z[kCombineWarps][256];
+    __shared__ float s_l[kCombineWarps];
     const kvq_q4_problem& p = a.p;
-    const int lane = threadIdx.x & 31;
-    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (row >= (int64_t)p.n_seq * p.n_qh) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = blockIdx.x;
     const int s = (int)(row / p.n_qh);
     const int L = min(max(p.seq_len[s], 0), p.max_seq_len);
     const int ns = (int)min((int64_t)a.n_splits, ((int64_t)L + a.split_rows - 1) / a.split_rows);
     grid_dependency_wait();                          // the partials of the decode kernel
     const float* ml = a.part_ml + row * a.n_splits * 2;
     float M = -INFINITY;
-    for (int S = 0; S < ns; ++S)
+    for (int S = lane; S < ns; S += 32)
         if (ml[2 * S + 1] > 0.0f) M = fmaxf(M, ml[2 * S]);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, w));
     float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float Lt = 0.0f;
-    for (int S = 0; S < ns; ++S) {
+    const float* po = a.part_o + row * a.n_splits * 256 + 8 * lane;
+#pragma unroll 4
+    for (int S = warp; S < ns; S += kCombineWarps) {  // every split below ns wrote its row
         const float lS = ml[2 * S + 1];
-        if (!(lS > 0.0f)) continue;
-        const float w = exp2f(ml[2 * S] - M);
-        Lt += w * lS;
-        const float4* src = reinterpret_cast<const float4*>(a.part_o + (row * a.n_splits + S) * 256 + 8 * lane);
+        const float w = lS > 0.0f ? exp2f(ml[2 * S] - M) : 0.0f;
+        Lt = fmaf(w, lS, Lt);
+        const float4* src = reinterpret_cast<const float4*>(po + (int64_t)S * 256);
         const float4 x0 = src[0], x1 = src[1];
         z[0] = fmaf(w, x0.x, z[0]); z[1] = fmaf(w, x0.y, z[1]);
         z[2] = fmaf(w, x0.z, z[2]); z[3] = fmaf(w, x0.w, z[3]);
         z[4] = fmaf(w, x1.x, z[4]); z[5] = fmaf(w, x1.y, z[5]);
         z[6] = fmaf(w, x1.z, z[6]); z[7] = fmaf(w, x1.w, z[7]);
+    }
+    float4* zs = reinterpret_cast<float4*>(&s_z[warp][8 * lane]);
+    zs[0] = make_float4(z[0], z[1], z[2], z[3]);
+    zs[1] = make_float4(z[4], z[5], z[6], z[7]);
+    if (lane == 0) s_l[warp] = Lt;
+    __syncthreads();
+    if (warp != 0) return;
+    Lt = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) Lt += s_l[w];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) {
+        const float4* zw = reinterpret_cast<const float4*>(&s_z[w][8 * lane]);
+        const float4 y0 = zw[0], y1 = zw[1];
+        z[0] += y0.x; z[1] += y0.y; z[2] += y0.z; z[3] += y0.w;
+        z[4] += y1.x; z[5] += y1.y; z[6] += y1.z; z[7] += y1.w;
     }
     const bool empty = !(Lt > 0.0f);
     const float inv = empty ? 0.0f : 1.0f / (16.0f * Lt);
@@ -305,14 +482,16 @@ bool plan_q4_decode(const kvq_q4_problem& p, Q4Plan& plan)
     plan = Q4Plan();
     int64_t split_rows = p.split_rows;
     if (split_rows <= 0) {
-        // about 32 warps per SM over all (sequence, KV head) units
-        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_kv);
-        const int64_t target = (int64_t)kNumSMs * 32;
-        int64_t splits = std::max<int64_t>(1, (target + units - 1) / units);
+        // about 24 warps per SM over all (sequence, KV head) units: 1.5 waves of the 16
+        // resident warps, enough splits to hide the ragged end of each
+        const int64_t hg = (p.n_kv > 0 && p.n_qh / p.n_kv == 8) ? 2 : 1;
+        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_kv * hg);
+        const int64_t target = (int64_t)kNumSMs * 12 * 2;
+        const int64_t splits = std::max<int64_t>(1, (target + units - 1) / units);
         split_rows = std::max<int64_t>(64, ((int64_t)p.max_seq_len + splits - 1) / splits);
-        split_rows = (split_rows + 31) / 32 * 32;
+        split_rows = (split_rows + 15) / 16 * 16;
     }
-    plan.split_rows = (int)split_rows;
+    plan.split_rows = (int)std::min<int64_t>(split_rows, INT32_MAX);
     plan.n_splits = (int)std::max<int64_t>(1, ((int64_t)p.max_seq_len + split_rows - 1) / split_rows);
     const size_t rows = (size_t)p.n_seq * p.n_qh;
     plan.off_ml = 0;
@@ -335,18 +514,34 @@ cudaError_t launch_q4_decode(const kvq_q4_problem& p, const Q4Plan& plan, float*
     a.out = out;
     a.lse = lse;
     a.status = dev_status;
-    const dim3 grid(plan.n_splits, p.n_seq, p.n_kv);
-    switch (p.n_qh / p.n_kv) {
-        case 1: q4_decode_kernel<1><<<grid, 32, 0, s>>>(a); break;
-        case 2: q4_decode_kernel<2><<<grid, 32, 0, s>>>(a); break;
-        case 4: q4_decode_kernel<4><<<grid, 32, 0, s>>>(a); break;
-        case 8: q4_decode_kernel<8><<<grid, 32, 0, s>>>(a); break;
+    const int G = p.n_qh / p.n_kv;
+    a.n_hg = G == 8 ? 2 : 1;
+    a.n_units = (int64_t)plan.n_splits * p.n_seq * p.n_kv * a.n_hg;
+    const dim3 grid((unsigned)((a.n_units + kWarps - 1) / kWarps));
+    void (*kern)(Q4Args) = nullptr;
+    switch (G) {
+        case 1: kern = q4_decode_kernel<1>; break;
+        case 2: kern = q4_decode_kernel<2>; break;
+        case 4:
+        case 8: kern = q4_decode_kernel<4>; break;
         default: return cudaErrorInvalidValue;
     }
+    // the shared-memory opt-in is set once per (device, kernel)
+    static std::atomic<uint32_t> opted[kMaxDevices];
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    const uint32_t bit = 1u << (G == 1 ? 0 : G == 2 ? 1 : 2);
+    if (dev >= kMaxDevices || !(opted[dev].load(std::memory_order_acquire) & bit)) {
+        e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQ4SmemBytes);
+        if (e0 != cudaSuccess) return e0;
+        if (dev < kMaxDevices) opted[dev].fetch_or(bit, std::memory_order_release);
+    }
+    kern<<<grid, 32 * kWarps, kQ4SmemBytes, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.n_seq * p.n_qh;
-    return launch_dependent(q4_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, a);
+    return launch_dependent(q4_combine_kernel, dim3((unsigned)rows), dim3(32 * kCombineWarps), 0, s, a);
 }
 
 }  // namespace kvq

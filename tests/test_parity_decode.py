@@ -73,7 +73,8 @@ def check(out, lse, ref, ref_lse, sel=None):
     # lse is a log of a sum of exponentials of scores as large as ~|lse|; fp32 score
     # accumulation leaves a relative error of a few 1e-7 of that magnitude
     assert np.allclose(lse[~empty], ref_lse[~empty], rtol=2e-6, atol=1e-4)
-    return float(np.max(err[~empty] / np.abs(ref[~empty]).max(-1))) if (~empty).any() else 0.0
+    scale = np.maximum(np.abs(ref[~empty]).max(-1), np.finfo(np.float64).tiny)
+    return float(np.max(err[~empty] / scale)) if (~empty).any() else 0.0
 
 
 @pytest.mark.parametrize("fmt", [1, 2])

@@ -74,7 +74,8 @@ def check(out, lse, ref, ref_lse, sel=None):
     err = np.abs(out - ref).max(axis=-1)
     bar = TOL * np.abs(ref).max(axis=-1)
     ok = empty | (err <= bar)
-    worst = float(np.max(err[~empty] / np.abs(ref[~empty]).max(-1))) if (~empty).any() else 0.0
+    scale = np.maximum(np.abs(ref[~empty]).max(-1), np.finfo(np.float64).tiny)
+    worst = float(np.max(err[~empty] / scale)) if (~empty).any() else 0.0
     assert ok.all(), f"worst err/max|out| = {worst:.3e}"
     if lse is not None:
         assert np.all(np.isneginf(lse[empty]))
@@ -85,8 +86,9 @@ def check(out, lse, ref, ref_lse, sel=None):
 @pytest.mark.parametrize("n_qh,n_kv", [(2, 2), (4, 2), (8, 2), (16, 2), (16, 8)])
 @pytest.mark.parametrize("split", [0, 32])
 def test_ratios_ragged_lengths(kvq, orc, n_qh, n_kv, split):
-    """Group ratios 1, 2, 4, 8; lengths 0 (empty), 1, a group's worth of rows and one
-    more, page-crossing, several splits with a ragged tail."""
+    """Group ratios 1, 2, 4, 8 (8: two warps per KV head); lengths 0 (empty), 1, one
+    short of and one past two 16-position tiles, page-crossing, several splits with a
+    ragged tail."""
     lengths = [0, 1, 31, 33, 70, 200]
     case, gate = make_case(orc, len(lengths), n_qh, n_kv, lengths, seed=n_qh * 10 + n_kv)
     for gt in (None, gate):
@@ -96,10 +98,10 @@ def test_ratios_ragged_lengths(kvq, orc, n_qh, n_kv, split):
         check(out, lse, ref, ref_lse)
 
 
-@pytest.mark.parametrize("split", [16, 48, 64, 1000])
+@pytest.mark.parametrize("split", [16, 40, 64, 1000])
 def test_split_sizes(kvq, orc, split):
-    """The LSE combine over 1 to 20 splits, split sizes that are and are not multiples of
-    the rows a warp takes per step."""
+    """The LSE combine over 1 to 19 splits, split sizes that are and are not multiples of
+    the 16-position tile a warp takes per step."""
     lengths = [300, 129, 5]
     case, gate = make_case(orc, 3, 8, 2, lengths, seed=77, page_size=32)
     ref, ref_lse, _ = orc.q4_decode(sm_scale=SCALE, gate=gate, **case)
