@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--suite", default="decode", choices=["decode", "codecs", "decode-configs"],
                     help="decode: the decode step (one JSON line); codecs: one line per codec "
                          "kernel; decode-configs: one line per decode configuration")
+    ap.add_argument("--only", default="",
+                    help="decode-configs: run only the configurations whose name contains this text")
     ap.add_argument("--decode-impl", type=int, default=0,
                     help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores")
     return ap.parse_args()
@@ -568,7 +570,12 @@ def run_decode_configs(args, local):
                           "peak_kind": peak_kind, "l2": "flushed before each call", "steps": K}),
               flush=True)
 
+    def wanted(name):
+        return args.only in name
+
     def one_seq(name, fmt, T, H, idx_k=0, mag=None):
+        if not wanted(name):
+            return
         cache = encode_pool(T, fmt, mag)
         q = W.queries(1, 1, H, seed=0)
         idx = None
@@ -592,6 +599,8 @@ def run_decode_configs(args, local):
             one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
 
     # ragged mixed-tier batch: 32 sequences, L ~ U[1024, 65536], 4 causal queries, H=64
+    if not wanted("ragged: 32 seqs"):
+        return
     n_seq, n_q, H, ps = 32, 4, 64, 64
     L, fmt, table, pool_pages = W.ragged_layout(n_seq, 1024, 65536, ps, seed=0)
     pools = {f: encode_pool(pool_pages[f] * ps, f, mag=(1e-2, 10.0)) for f in (F8, T4)}

@@ -5,8 +5,9 @@
 // the optional sigmoid gate.
 //
 // One warp per (split, sequence, KV head) [and half of the 8 query heads when a KV head
-// serves 8]; four such warps per CTA, each with its own 2-stage cp.async ring of 16-row
-// tiles (the K and V rows of 16 positions, 4.5 KB); 128 registers, four CTAs per SM.
+// serves 8]; four such warps per CTA, each with its own 3-stage cp.async ring of 16-row
+// tiles (the K and V rows of 16 positions, 4.5 KB); three CTAs per SM.  A warp computes
+// tile i + 1's scores and tile i's context in one straight-line body.
 // Both contractions of a tile run on the tensor cores with register operands
 // (mma.sync m16n8k16, fp16 in, fp32 out; the operands are built in registers, so
 // there is no shared-memory or tensor-memory operand image to stage):
@@ -154,7 +155,7 @@ __device__ __forceinline__ uint32_t code_word(const uint8_t* p)
 }
 
 constexpr int kTileRows = 16;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kWarps = 4;
 constexpr int kStageBytes = 2 * kTileRows * kRowBytes;    // K rows 0..15, then V rows 0..15
 
@@ -167,7 +168,7 @@ constexpr size_t kQ4SmemBytes = (size_t)kWarps * (kStages * kStageBytes + kFragB
 static_assert(4 * 256 * 4 <= kStageBytes, "query scratch must fit in one stage");
 
 template <int GH>   // query heads per warp: 1, 2 or 4
-__global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_constant__ Q4Args a)
+__global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_constant__ Q4Args a)
 {
     extern __shared__ __align__(16) uint8_t q4_smem[];
     grid_dependents_launch();                        // the combine may start launching
@@ -286,22 +287,12 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
         for (int k = 0; k < 4; ++k) o[b][0][k] = o[b][1][k] = 0.0f;
     float m_run = -INFINITY, l_run = 0.0f;           // head t (t < GH)
     int tau = 40;                                    // P carries 2^tau
+    const bool head_ok = t < GH;
 
-    for (int i = 0; i < n_tiles; ++i) {
-        const int ti = i + kStages - 1;
-        if (ti < n_tiles) {
-            issue(ti, pid_next);
-            if (ti + 1 < n_tiles) pid_next = page_id(ti + 1);
-        }
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint8_t* sK = tiles[i % kStages];
-        const uint8_t* sV = sK + kTileRows * kRowBytes;
-        const unsigned valid = valid_of[i % kStages];
-
-        // ---- scores of rows g and g + 8 for head t
-        float sg = 0.0f, sg8 = 0.0f;
+    // scores of rows g and g + 8 of a staged tile for head t (unscaled)
+    auto scores = [&](const uint8_t* sK, float& sg, float& sg8) {
+        sg = 0.0f;
+        sg8 = 0.0f;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             const uint8_t* rg = sK + g * kRowBytes + 18 * b;
@@ -321,11 +312,15 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
             sg = fmaf(h2f(lds16(rg)), c[0] + c[1], sg);
             sg8 = fmaf(h2f(lds16(rg8)), c[2] + c[3], sg8);
         }
-        const bool head_ok = t < GH;
+    };
+    // online softmax of head t over a tile's 16 rows (lanes of equal t); returns the
+    // factor the running output takes before this tile's context, and this tile's
+    // weights of head g >> 1 for rows 2t, 2t+1, 2t+8, 2t+9 times 2^tau
+    float f = 1.0f, pa = 0.0f, pb = 0.0f, pc = 0.0f, pd = 0.0f;
+    auto softmax = [&](float sg, float sg8, unsigned valid, const uint8_t* sV) {
         const bool vg = head_ok && ((valid >> g) & 1u), vg8 = head_ok && ((valid >> (g + 8)) & 1u);
         const float s0 = vg ? sg * sinv : -INFINITY;
         const float s1 = vg8 ? sg8 * sinv : -INFINITY;
-        // ---- online softmax of head t over the 16 rows (lanes of equal t)
         float mx = fmaxf(s0, s1);
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
@@ -340,7 +335,7 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
         ps += __shfl_xor_sync(kFull, ps, 16);
         l_run = l_run * alpha + ps;
         m_run = m_new;
-        // ---- the tile's largest V block scale bounds P = p * d (p <= 1): P * 2^tau < 2^15
+        // the tile's largest V block scale bounds P = p * d (p <= 1): P * 2^tau < 2^15
         const uint8_t* rv = sV + (lane & 15) * kRowBytes + 72 * (lane >> 4);
         uint32_t dm = max(max(lds16(rv) & 0x7FFFu, lds16(rv + 18) & 0x7FFFu),
                           max(lds16(rv + 36) & 0x7FFFu, lds16(rv + 54) & 0x7FFFu));
@@ -348,7 +343,19 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
         for (int w = 16; w >= 1; w >>= 1) dm = max(dm, __shfl_xor_sync(kFull, dm, w));
         int tau_new = tau;
         if (dm != 0) tau_new = min(tau, 14 - (dm >= 0x400u ? (int)(dm >> 10) - 15 : -15));
-        const float f = alpha * exp2i(tau_new - tau);
+        f = alpha * exp2i(tau_new - tau);
+        tau = tau_new;
+        // B operand of the context: column n = g (head g >> 1, part g & 1), rows
+        // k = 2t, 2t+1, 2t+8, 2t+9 of the tile, taken from the score lanes
+        const int src = 8 * t + (g >> 1);
+        const float pscale = ((g >> 1) < GH) ? exp2i(tau) : 0.0f;
+        pa = __shfl_sync(kFull, p0, src) * pscale;
+        pb = __shfl_sync(kFull, p0, src + 4) * pscale;
+        pc = __shfl_sync(kFull, p1, src) * pscale;
+        pd = __shfl_sync(kFull, p1, src + 4) * pscale;
+    };
+    // context of a staged tile with the current weights
+    auto context = [&](const uint8_t* sV) {
         if (__any_sync(kFull, f != 1.0f)) {
 #pragma unroll
             for (int b = 0; b < 8; ++b)
@@ -358,15 +365,6 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
                     o[b][1][k] *= f;
                 }
         }
-        tau = tau_new;
-        // ---- B operand of the context: column n = g (head g >> 1, part g & 1), rows
-        // k = 2t, 2t+1, 2t+8, 2t+9 of the tile; softmax weights from the score lanes
-        const int src = 8 * t + (g >> 1);
-        const float pscale = ((g >> 1) < GH) ? exp2i(tau) : 0.0f;
-        const float pa = __shfl_sync(kFull, p0, src) * pscale;
-        const float pb = __shfl_sync(kFull, p0, src + 4) * pscale;
-        const float pc = __shfl_sync(kFull, p1, src) * pscale;
-        const float pd = __shfl_sync(kFull, p1, src + 4) * pscale;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             const uint8_t* v0 = sV + 2 * t * kRowBytes + 18 * b;
@@ -381,7 +379,34 @@ __global__ void __launch_bounds__(32 * kWarps, 4) q4_decode_kernel(const __grid_
             mma16816(o[b][0], nib_lo(X), nib_lo(X >> 8), nib_lo(Y), nib_lo(Y >> 8), b0, b1);
             mma16816(o[b][1], nib_hi(X), nib_hi(X >> 8), nib_hi(Y), nib_hi(Y >> 8), b0, b1);
         }
-        __syncwarp();                                // the stage is refilled next iteration
+    };
+
+    // Software pipeline: iteration i computes the scores of tile i + 1 and the context of
+    // tile i in one straight-line body (two independent chains for the scheduler), then
+    // the softmax of tile i + 1.  The last iteration's scores read a stale stage and are
+    // discarded.
+    cp_async_wait<kStages - 2>();                    // tile 0 has landed
+    __syncwarp();
+    {
+        float sg, sg8;
+        scores(tiles[0], sg, sg8);
+        softmax(sg, sg8, valid_of[0], tiles[0] + kTileRows * kRowBytes);
+    }
+    for (int i = 0; i < n_tiles; ++i) {
+        const int ti = i + kStages - 1;
+        if (ti < n_tiles) {
+            issue(ti, pid_next);
+            if (ti + 1 < n_tiles) pid_next = page_id(ti + 1);
+        }
+        cp_async_commit();
+        cp_async_wait<kStages - 2>();                // tile i + 1 has landed
+        __syncwarp();
+        const int sn = (i + 1) % kStages;
+        float sg, sg8;
+        scores(tiles[sn], sg, sg8);
+        context(tiles[i % kStages] + kTileRows * kRowBytes);
+        __syncwarp();                                // tile i's stage is refilled next iteration
+        if (i + 1 < n_tiles) softmax(sg, sg8, valid_of[sn], tiles[sn] + kTileRows * kRowBytes);
     }
     // ---- partials: (m, l) of head t from lane t, o of head t: dims 32b + 16mt + 2g (+1)
     if (t < GH) {
