@@ -85,11 +85,15 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^
 // which the encoder never writes, reads as 0
 __device__ __forceinline__ void e4m3x4_to_half(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    w &= ~__vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
-    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-    lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
-    hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
+    // (b & 0x7F) + 1 has bit 7 set exactly when the low seven bits of b are all set;
+    // prmt's sign mode (selector 8 + i) spreads that bit over byte i, which then clears it
+    const uint32_t t = (w & 0x7F7F7F7Fu) + 0x01010101u;
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(t));
+    w &= ~m;
+    // low byte -> low half, as the two halves of one register
+    asm("{.reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h;}"
+        : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
 // ------------------------------------------------------------------------------------
