@@ -196,12 +196,13 @@ struct RowCtx {
 
 // ====================================================================================
 // The decode kernel.
-//  * Roles (448 threads): warps 0-7 are two producer sets of four warps (thread = row)
+//  * Roles (480 threads): warps 0-7 are two producer sets of four warps (thread = row)
 //    that convert alternate chunks of codes to fp16, so two chains of ring waits,
 //    stores and arrivals run at once and every warp scheduler holds one warp of each
 //    set; warps 8-11 run the softmax (thread = row) and the epilogue (thread = output
 //    dim); warp 12 allocates tensor memory and issues every MMA from one elected lane;
-//    warp 13 loads code chunks by TMA (contiguous caches).
+//    warps 13 and 14 load code chunks by TMA for producer sets 0 and 1 (contiguous
+//    caches).
 //  * Order of work, common to producers, loader and MMA issuer: per step i, the 9
 //    score chunks of tile i (8 latent, 1 rope) if i < NT, then the 8 latent context
 //    chunks of tile i-1.  Score chunks go to tensor memory (thread = row = TMEM lane)
@@ -226,7 +227,7 @@ constexpr int kRingC = 4;                // shared-memory context slots (pairs a
 constexpr int kStages = 4;               // raw-code stages in flight per producer set
 constexpr int kStageBytes = kRT * 64;    // one chunk of raw codes, [4 pieces][128 rows][16 B]
 constexpr uint32_t kColA = 128;
-constexpr int kThreads = 448;           // 8 producer, 4 softmax, 1 MMA and 1 loader warps
+constexpr int kThreads = 480;           // 8 producer, 4 softmax, 1 MMA and 2 loader warps
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQBytes;
 constexpr int kOffP = kOffRing + kRingC * kChunkBytes;
@@ -456,8 +457,8 @@ __device__ __forceinline__ void warp_reduce_transpose(float (&v)[32], int lane)
     }
 }
 
-// 13 warps: warp w runs on sub-partition w % 4, so sub-partition 0 holds four warps and
-// its 16K registers cap every thread at 128
+// 15 warps: warp w runs on sub-partition w % 4, so sub-partitions 0-2 hold four warps
+// each and their 16K registers cap every thread at 128
 __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ TcArgs a)
 {
     extern __shared__ uint8_t dsm[];
@@ -803,10 +804,13 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 }
             }
         }
-    } else if (warp == 13) {
-        // ================================ loader =========================================
+    } else if (warp >= 13) {
+        // ================================ loaders ========================================
         // Contiguous rows: one TMA box per chunk ([128 rows x 32 or 64 bytes]) into the
-        // owning producer set's next stage, in the common order.
+        // owning producer set's next stage, in the common order.  Warp 13 loads set 0's
+        // chunks and warp 14 set 1's, so a set that falls behind does not hold back the
+        // other set's refills.
+        const int my_set = warp - 13;
         if (a.use_tma) {
             const bool leader = elect_one();
             const CUtensorMap* m_lat = &a.tm_lat[tq4 ? 1 : 0];
@@ -817,6 +821,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             for (int n = 0; n < n_items && ok; ++n) {
                 const OwnItem it = common_item(n, NT);
                 const int set = it.ch & 1;
+                if (set != my_set) continue;
                 const int j = set ? o1++ : o0++;
                 const int d = j % kStages;
                 ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status));
@@ -832,7 +837,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             }
             // every box issued has landed before the CTA's shared memory is released
             if (leader) {
-                for (int set = 0; set < 2; ++set) {
+                for (int set = my_set; set == my_set; ++set) {
                     const int o = set ? o1 : o0;
                     for (int d = 0; d < kStages && d < o; ++d) {
                         const int jl = d + kStages * ((o - 1 - d) / kStages);
