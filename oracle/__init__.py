@@ -96,6 +96,12 @@ def _declare(L: C.CDLL) -> None:
     L.orc_encode_tq4.argtypes = [_p, _i64, C.c_int, _i64, _p, _p, _i64, _p]
     L.orc_decode_tq4.restype = C.c_int
     L.orc_decode_tq4.argtypes = [_p, _i64, C.c_int, _i64, _p, _p, _p, _p]
+    L.orc_tq_codebook.restype = C.c_int
+    L.orc_tq_codebook.argtypes = [C.c_int, _p, _p, _p, _p]
+    L.orc_encode_tq.restype = C.c_int
+    L.orc_encode_tq.argtypes = [C.c_int, _p, _i64, C.c_int, _i64, _p, _p, _i64, _p]
+    L.orc_decode_tq.restype = C.c_int
+    L.orc_decode_tq.argtypes = [C.c_int, _p, _i64, C.c_int, _i64, _p, _p, _p, _p]
     L.orc_fwht256_q4.restype = None
     L.orc_fwht256_q4.argtypes = [_p, _p]
     L.orc_q4_block.restype = None
@@ -209,6 +215,53 @@ def decode_tq4(packed: np.ndarray, radius: np.ndarray, sign_bits: np.ndarray, di
                               _ptr(xhat), _ptr(yhat))
     if rc != 0:
         raise ValueError(f"oracle TQ4 decode refused dim={dim}")
+    return xhat, yhat
+
+
+# --- TQ-b (b = 3, 4, 6) ---------------------------------------------------------------
+
+TQ_FMT = {3: 5, 4: 2, 6: 4}        # library / oracle format code of each width
+
+
+def tq_codebook(bits: int):
+    """(lloyd fp64 [2^b], centroids f32 [2^b] (binary16 values), thresholds f32 [2^b - 1],
+    iterations)."""
+    L = 1 << bits
+    lloyd = np.empty(L, np.float64)
+    cb = np.empty(L, np.float32)
+    thr = np.empty(L - 1, np.float32)
+    it = C.c_int(0)
+    if lib().orc_tq_codebook(bits, _ptr(lloyd), _ptr(cb), _ptr(thr), C.addressof(it)) != 0:
+        raise ValueError(f"oracle TQ codebook refused bits={bits}")
+    return lloyd, cb, thr, it.value
+
+
+def encode_tq(x: np.ndarray, sign_bits: np.ndarray, bits: int):
+    """rows [R][n] fp32 -> (packed u8 [R][n*b/8], radius f32 [R])."""
+    x = _c(x, np.float32)
+    sb = _c(sign_bits, np.uint32)
+    R, D = x.shape
+    rb = D * bits // 8
+    packed = np.empty((R, rb), np.uint8)
+    radius = np.empty(R, np.float32)
+    rc = lib().orc_encode_tq(bits, _ptr(x), R, D, D, _ptr(sb), _ptr(packed), rb, _ptr(radius))
+    if rc != 0:
+        raise ValueError(f"oracle TQ encode refused dim={D} bits={bits} (rc={rc})")
+    return packed, radius
+
+
+def decode_tq(packed: np.ndarray, radius: np.ndarray, sign_bits: np.ndarray, dim: int, bits: int):
+    """-> (xhat fp64 [R][dim] in the original basis, yhat fp64 [R][dim] rotated)."""
+    packed = _c(packed, np.uint8)
+    radius = _c(radius, np.float32)
+    sb = _c(sign_bits, np.uint32)
+    R = packed.shape[0]
+    xhat = np.empty((R, dim), np.float64)
+    yhat = np.empty((R, dim), np.float64)
+    rc = lib().orc_decode_tq(bits, _ptr(packed), R, dim, dim * bits // 8, _ptr(radius), _ptr(sb),
+                             _ptr(xhat), _ptr(yhat))
+    if rc != 0:
+        raise ValueError(f"oracle TQ decode refused dim={dim} bits={bits}")
     return xhat, yhat
 
 

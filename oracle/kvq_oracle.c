@@ -153,57 +153,144 @@ void orc_decode_fp8(const uint8_t* codes, int64_t rows, int dim, int64_t ldc,
 static double std_normal_pdf(double t) { return exp(-0.5 * t * t) / sqrt(2.0 * M_PI); }
 static double std_normal_cdf(double t) { return 0.5 * erfc(-t / sqrt(2.0)); }
 
-/* Lloyd-Max for N(0,1) with 16 levels: alternate "thresholds are midpoints of adjacent
- * centroids" and "each centroid is the conditional mean of its cell",
- *   c_k = (phi(t_{k-1}) - phi(t_k)) / (Phi(t_k) - Phi(t_{k-1})),
- * from a uniform start until no centroid moves by 1e-15.  The stored codebook is each
- * centroid rounded to the nearest binary16 value; the thresholds are the midpoints of
- * the stored centroids (exact in fp32). */
-/* The iteration converges linearly; it stops once no centroid moves by 1e-15, or, since
- * the last bits of exp/erfc differ between C libraries and can leave the iterate
- * oscillating at the rounding level, after 20000 steps (by then the moves are below
- * 1e-14; the pins check the fixed-point condition to 1e-12).  Computed once per process. */
-static int    g_cb_ready = 0;
-static double g_cb_lloyd[16];
-static float  g_cb_f[16], g_cb_thr[15];
-static int    g_cb_iters = 0;
+/* Lloyd-Max for N(0,1) with L = 2^bits levels: the fixed point of "thresholds are the
+ * midpoints of adjacent centroids" and "each centroid is the conditional mean of its
+ * cell",
+ *   c_k = (phi(t_k) - phi(t_{k+1})) / (Phi(t_{k+1}) - Phi(t_k)),  t_k = (c_{k-1} + c_k) / 2,
+ * with t_0 = -inf and t_L = +inf.  The stored codebook is each centroid rounded to the
+ * nearest binary16 value; the thresholds are the midpoints of the stored centroids
+ * (exact in fp32).
+ *
+ * 16 levels (the 4-bit tier): the plain alternation from a uniform start on [-3, 3]
+ * until no centroid moves by 1e-15, or, since the last bits of exp/erfc differ between
+ * C libraries and can leave the iterate oscillating at the rounding level, after 20000
+ * steps (by then the moves are below 1e-14).
+ * 8 and 64 levels: the alternation converges too slowly at 64 levels (its contraction
+ * factor is close to 1), so after 500 warm-up steps the same fixed point is solved by
+ * Newton's method on c - T(c) = 0.  T_k depends on c_{k-1}, c_k, c_{k+1} only, through
+ *   dT_k/dt_k     = phi(t_k) (T_k - t_k) / mass_k,
+ *   dT_k/dt_{k+1} = phi(t_{k+1}) (t_{k+1} - T_k) / mass_k,
+ * and dt_k/dc_{k-1} = dt_k/dc_k = 1/2, so each step is one tridiagonal solve.  It stops
+ * when no centroid moves by 1e-15 (at most 60 steps).
+ * The pins check the fixed-point condition to 1e-12 in closed form.  Computed once per
+ * process and width. */
+#define ORC_TQ_MAXL 64
+typedef struct {
+    int ready, iters;
+    double lloyd[ORC_TQ_MAXL];
+    float cb[ORC_TQ_MAXL], thr[ORC_TQ_MAXL];
+} tq_codebook_t;
+static tq_codebook_t g_tq_cb[7];     /* indexed by bits */
 
-static void tq4_codebook_compute(void)
+/* Phi(b) - Phi(a) without cancellation in either tail: from the upper tail
+ * Q(x) = erfc(x / sqrt 2) / 2 when the cell lies above 0, the lower tail when below. */
+static double cell_mass(double a, double b)
 {
-    double c[16], t[17];
-    for (int k = 0; k < 16; ++k) c[k] = -3.0 + 6.0 * k / 15.0;
-    int it;
-    for (it = 0; it < 20000; ++it) {
-        t[0] = -INFINITY; t[16] = INFINITY;
-        for (int k = 1; k < 16; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
-        double move = 0.0;
-        for (int k = 0; k < 16; ++k) {
-            double pa = isinf(t[k]) ? 0.0 : std_normal_pdf(t[k]);
-            double pb = isinf(t[k + 1]) ? 0.0 : std_normal_pdf(t[k + 1]);
-            double mass = std_normal_cdf(t[k + 1]) - std_normal_cdf(t[k]);
-            double ck = (pa - pb) / mass;
-            if (fabs(ck - c[k]) > move) move = fabs(ck - c[k]);
-            c[k] = ck;
+    const double r = 0.70710678118654752440;
+    if (a >= 0.0) return 0.5 * (erfc(a * r) - erfc(b * r));
+    if (b <= 0.0) return 0.5 * (erfc(-b * r) - erfc(-a * r));
+    return 1.0 - 0.5 * erfc(b * r) - 0.5 * erfc(-a * r);
+}
+
+/* one Lloyd step: T(c) into cn; optional tridiagonal Jacobian of T (sub, diag, sup);
+ * returns the largest |T_k - c_k|.  `tails`: cell masses from cell_mass (the 4-bit
+ * codebook keeps the plain difference of the two CDF values it was computed with) */
+static double lloyd_map(const double* c, int L, double* cn, double* sub, double* dia, double* sup,
+                        int tails)
+{
+    double t[ORC_TQ_MAXL + 1];
+    t[0] = -INFINITY; t[L] = INFINITY;
+    for (int k = 1; k < L; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
+    double move = 0.0;
+    for (int k = 0; k < L; ++k) {
+        double pa = isinf(t[k]) ? 0.0 : std_normal_pdf(t[k]);
+        double pb = isinf(t[k + 1]) ? 0.0 : std_normal_pdf(t[k + 1]);
+        double mass = tails ? cell_mass(t[k], t[k + 1]) : std_normal_cdf(t[k + 1]) - std_normal_cdf(t[k]);
+        double ck = (pa - pb) / mass;
+        if (fabs(ck - c[k]) > move) move = fabs(ck - c[k]);
+        cn[k] = ck;
+        if (dia) {
+            double a = isinf(t[k]) ? 0.0 : pa * (ck - t[k]) / mass;          /* dT_k/dt_k     */
+            double b = isinf(t[k + 1]) ? 0.0 : pb * (t[k + 1] - ck) / mass;  /* dT_k/dt_{k+1} */
+            sub[k] = 0.5 * a;
+            dia[k] = 0.5 * (a + b);
+            sup[k] = 0.5 * b;
         }
-        if (move < 1e-15) break;
     }
-    for (int k = 0; k < 16; ++k) {
-        g_cb_lloyd[k] = c[k];
-        g_cb_f[k] = (float)orc_f16_value(orc_f16_rne(c[k]));
+    return move;
+}
+
+static void tq_codebook_compute(int bits)
+{
+    const int L = 1 << bits;
+    tq_codebook_t* cbk = &g_tq_cb[bits];
+    double c[ORC_TQ_MAXL], cn[ORC_TQ_MAXL];
+    int it = 0;
+    if (bits == 4) {
+        for (int k = 0; k < L; ++k) c[k] = -3.0 + 6.0 * k / (L - 1);
+        for (it = 0; it < 20000; ++it) {
+            double move = lloyd_map(c, L, cn, NULL, NULL, NULL, 0);
+            memcpy(c, cn, sizeof(double) * L);
+            if (move < 1e-15) break;
+        }
+    } else {
+        for (int k = 0; k < L; ++k) c[k] = -3.0 + 6.0 * k / (L - 1);
+        for (it = 0; it < 500; ++it) {
+            lloyd_map(c, L, cn, NULL, NULL, NULL, 1);
+            memcpy(c, cn, sizeof(double) * L);
+        }
+        double sub[ORC_TQ_MAXL], dia[ORC_TQ_MAXL], sup[ORC_TQ_MAXL];
+        for (int n = 0; n < 60; ++n, ++it) {
+            /* F(c) = T(c) - c = 0:  (J - I) delta = -F, J tridiagonal */
+            lloyd_map(c, L, cn, sub, dia, sup, 1);
+            double a[ORC_TQ_MAXL], b[ORC_TQ_MAXL], cc[ORC_TQ_MAXL], d[ORC_TQ_MAXL];
+            for (int k = 0; k < L; ++k) {
+                a[k] = sub[k];                /* coefficient of delta_{k-1} */
+                b[k] = dia[k] - 1.0;          /* of delta_k                 */
+                cc[k] = sup[k];               /* of delta_{k+1}             */
+                d[k] = -(cn[k] - c[k]);
+            }
+            for (int k = 1; k < L; ++k) {     /* Thomas algorithm */
+                double w = a[k] / b[k - 1];
+                b[k] -= w * cc[k - 1];
+                d[k] -= w * d[k - 1];
+            }
+            double delta[ORC_TQ_MAXL], move = 0.0;
+            delta[L - 1] = d[L - 1] / b[L - 1];
+            for (int k = L - 2; k >= 0; --k) delta[k] = (d[k] - cc[k] * delta[k + 1]) / b[k];
+            for (int k = 0; k < L; ++k) {
+                c[k] += delta[k];
+                if (fabs(delta[k]) > move) move = fabs(delta[k]);
+            }
+            if (move < 1e-15) break;
+        }
     }
-    for (int k = 0; k < 15; ++k) g_cb_thr[k] = (g_cb_f[k] + g_cb_f[k + 1]) / 2.0f;
-    g_cb_iters = it;
-    g_cb_ready = 1;
+    for (int k = 0; k < L; ++k) {
+        cbk->lloyd[k] = c[k];
+        cbk->cb[k] = (float)orc_f16_value(orc_f16_rne(c[k]));
+    }
+    for (int k = 0; k < L - 1; ++k) cbk->thr[k] = (cbk->cb[k] + cbk->cb[k + 1]) / 2.0f;
+    cbk->iters = it;
+    cbk->ready = 1;
+}
+
+static int tq_bits_ok(int bits) { return bits == 3 || bits == 4 || bits == 6; }
+
+int orc_tq_codebook(int bits, double* lloyd, float* cb, float* thr, int* iters)
+{
+    if (!tq_bits_ok(bits)) return -1;
+    const int L = 1 << bits;
+    if (!g_tq_cb[bits].ready) tq_codebook_compute(bits);
+    if (lloyd) memcpy(lloyd, g_tq_cb[bits].lloyd, sizeof(double) * L);
+    if (cb) memcpy(cb, g_tq_cb[bits].cb, sizeof(float) * L);
+    if (thr) memcpy(thr, g_tq_cb[bits].thr, sizeof(float) * (L - 1));
+    if (iters) *iters = g_tq_cb[bits].iters;
+    return 0;
 }
 
 int orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters)
 {
-    if (!g_cb_ready) tq4_codebook_compute();
-    memcpy(lloyd, g_cb_lloyd, sizeof g_cb_lloyd);
-    memcpy(cb, g_cb_f, sizeof g_cb_f);
-    memcpy(thr, g_cb_thr, sizeof g_cb_thr);
-    if (iters) *iters = g_cb_iters;
-    return 0;
+    return orc_tq_codebook(4, lloyd, cb, thr, iters);
 }
 
 static int is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
@@ -237,7 +324,7 @@ static int sign_is_negative(const uint32_t* bits, int i)
     return (bits[i >> 5] >> (i & 31)) & 1u;
 }
 
-/* TQ4 encode of one row, step by step:
+/* TQ-b encode of one row (b = 3, 4, 6 bits), step by step:
  *   1. w = s (.) x with s_i = -1 where bit i of sign_bits is set;
  *   2. w = FWHT_n(w) (unnormalised, stages ascending), y = w * c, c = fp32(1/sqrt(n));
  *   3. ss = sum y_i^2 accumulated as 32 partial sums (partial l takes i = l, l+32, ...
@@ -246,16 +333,21 @@ static int sign_is_negative(const uint32_t* bits, int i)
  *   4. radius r = sqrtf(ss) (IEEE), sigma = r * c; a zero radius marks an inert row
  *      (all-zero bytes);
  *   5. u_i = y_i / sigma, code_i = number of thresholds t_k with u_i >= t_k;
- *   6. element 2j goes to the low nibble of byte j, element 2j+1 to the high nibble.
- * Returns -2 (and writes nothing) for a dimension that is not a power of two. */
-int orc_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
-                   const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
-                   float* radius)
+ *   6. the codes form a little-endian bit stream: code i occupies bits b*i .. b*i + b - 1
+ *      of the row's n*b/8 bytes (bit 0 is the low bit of byte 0).  For b = 4, element 2j
+ *      is the low nibble of byte j and element 2j+1 the high nibble.
+ * Returns -2 (and writes nothing) for a dimension that is not a power of two, -1 for an
+ * unsupported width. */
+int orc_encode_tq(int bits, const float* x, int64_t rows, int dim, int64_t ldx,
+                  const uint32_t* sign_bits, uint8_t* packed, int64_t ldp, float* radius)
 {
+    if (!tq_bits_ok(bits)) return -1;
     if (!is_pow2(dim) || dim < 64) return -2;
-    double lloyd[16]; float cb[16], thr[15];
-    orc_tq4_codebook(lloyd, cb, thr, NULL);
+    const int L = 1 << bits;
+    float cb[ORC_TQ_MAXL], thr[ORC_TQ_MAXL];
+    orc_tq_codebook(bits, NULL, cb, thr, NULL);
     const float c = (float)(1.0 / sqrt((double)dim));
+    const int row_bytes = dim * bits / 8;
     float* y = (float*)malloc(sizeof(float) * (size_t)dim);
     for (int64_t r = 0; r < rows; ++r) {
         const float* xr = x + r * ldx;
@@ -278,43 +370,56 @@ int orc_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
         float sigma = rad * c;
         uint8_t* pr = packed + r * ldp;
         radius[r] = rad;
-        if (rad == 0.0f) {
-            memset(pr, 0, (size_t)dim / 2);
-            continue;
-        }
-        for (int j = 0; j < dim / 2; ++j) {
-            int code[2];
-            for (int h = 0; h < 2; ++h) {
-                float u = y[2 * j + h] / sigma;
-                int n = 0;
-                for (int k = 0; k < 15; ++k) n += (u >= thr[k]);
-                code[h] = n;
-            }
-            pr[j] = (uint8_t)(code[0] | (code[1] << 4));
+        memset(pr, 0, (size_t)row_bytes);
+        if (rad == 0.0f) continue;
+        for (int i = 0; i < dim; ++i) {
+            float u = y[i] / sigma;
+            int n = 0;
+            for (int k = 0; k < L - 1; ++k) n += (u >= thr[k]);
+            for (int bit = 0; bit < bits; ++bit)
+                if ((n >> bit) & 1) {
+                    const int pos = bits * i + bit;
+                    pr[pos >> 3] |= (uint8_t)(1u << (pos & 7));
+                }
         }
     }
     free(y);
     return 0;
 }
 
-/* TQ4 dequantisation in fp64: yhat_i = cb[code_i] * r / sqrt(n) (the rotated row) and
- * xhat = (1/sqrt(n)) * s (.) FWHT_n(yhat) (the row in the original basis). */
-int orc_decode_tq4(const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
-                   const float* radius, const uint32_t* sign_bits,
-                   double* xhat, double* yhat)
+int orc_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
+                   const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                   float* radius)
 {
+    return orc_encode_tq(4, x, rows, dim, ldx, sign_bits, packed, ldp, radius);
+}
+
+/* code i of a TQ-b row (the bit stream above) */
+static int tq_code(const uint8_t* pr, int bits, int i)
+{
+    int code = 0;
+    for (int bit = 0; bit < bits; ++bit) {
+        const int pos = bits * i + bit;
+        code |= ((pr[pos >> 3] >> (pos & 7)) & 1) << bit;
+    }
+    return code;
+}
+
+/* TQ-b dequantisation in fp64: yhat_i = cb[code_i] * r / sqrt(n) (the rotated row) and
+ * xhat = (1/sqrt(n)) * s (.) FWHT_n(yhat) (the row in the original basis). */
+int orc_decode_tq(int bits, const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
+                  const float* radius, const uint32_t* sign_bits, double* xhat, double* yhat)
+{
+    if (!tq_bits_ok(bits)) return -1;
     if (!is_pow2(dim) || dim < 64) return -2;
-    double lloyd[16]; float cb[16], thr[15];
-    orc_tq4_codebook(lloyd, cb, thr, NULL);
+    float cb[ORC_TQ_MAXL];
+    orc_tq_codebook(bits, NULL, cb, NULL, NULL);
     const double inv_sqrt_n = 1.0 / sqrt((double)dim);
     double* w = (double*)malloc(sizeof(double) * (size_t)dim);
     for (int64_t r = 0; r < rows; ++r) {
         const uint8_t* pr = packed + r * ldp;
         double sigma = (double)radius[r] * inv_sqrt_n;
-        for (int i = 0; i < dim; ++i) {
-            int code = (i & 1) ? (pr[i >> 1] >> 4) : (pr[i >> 1] & 15);
-            w[i] = (double)cb[code] * sigma;
-        }
+        for (int i = 0; i < dim; ++i) w[i] = (double)cb[tq_code(pr, bits, i)] * sigma;
         if (yhat) memcpy(yhat + r * dim, w, sizeof(double) * (size_t)dim);
         if (xhat) {
             orc_fwht_f64(w, dim);
@@ -326,6 +431,13 @@ int orc_decode_tq4(const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
     }
     free(w);
     return 0;
+}
+
+int orc_decode_tq4(const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
+                   const float* radius, const uint32_t* sign_bits,
+                   double* xhat, double* yhat)
+{
+    return orc_decode_tq(4, packed, rows, dim, ldp, radius, sign_bits, xhat, yhat);
 }
 
 /* ===================================================================================
@@ -479,8 +591,11 @@ static void mla_dequant(const orc_mla* p, int fmt, int64_t row, double* c, doubl
         orc_decode_fp8(p->fp8_lat + row * DL, 1, DL, DL, p->fp8_lat_scale + row, c);
         orc_decode_fp8(p->fp8_rope + row * DR, 1, DR, DR, p->fp8_rope_scale + row, kr);
     } else {
-        orc_decode_tq4(p->tq4_lat + row * (DL / 2), 1, DL, DL / 2, p->tq4_radius + row,
-                       p->tq4_signs, c, NULL);
+        /* the rotated tiers share one set of planes; the format gives the code width */
+        const int bits = fmt == ORC_FMT_TQ3 ? 3 : fmt == ORC_FMT_TQ6 ? 6 : 4;
+        const int rb = DL * bits / 8;
+        orc_decode_tq(bits, p->tq4_lat + row * rb, 1, DL, rb, p->tq4_radius + row,
+                      p->tq4_signs, c, NULL);
         orc_decode_fp8(p->tq4_rope + row * DR, 1, DR, DR, p->tq4_rope_scale + row, kr);
     }
 }

@@ -27,6 +27,8 @@
 
 #define ORC_FMT_FP8 1
 #define ORC_FMT_TQ4 2
+#define ORC_FMT_TQ6 4
+#define ORC_FMT_TQ3 5
 
 /* ---- number formats ---------------------------------------------------------- */
 double   orc_e4m3_value(uint8_t code);     /* value of an e4m3 code (S.1111.111 reads 0) */
@@ -40,7 +42,12 @@ void orc_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
 void orc_decode_fp8(const uint8_t* codes, int64_t rows, int dim, int64_t ldc,
                     const float* scales, double* out);
 
-/* ---- rotated-int4 (TQ4) -------------------------------------------------------- */
+/* ---- rotated tiers: TQ-b, b = 3, 4, 6 (TQ4 = rotated-int4) --------------------- */
+int  orc_tq_codebook(int bits, double* lloyd, float* cb, float* thr, int* iters);
+int  orc_encode_tq(int bits, const float* x, int64_t rows, int dim, int64_t ldx,
+                   const uint32_t* sign_bits, uint8_t* packed, int64_t ldp, float* radius);
+int  orc_decode_tq(int bits, const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
+                   const float* radius, const uint32_t* sign_bits, double* xhat, double* yhat);
 int  orc_tq4_codebook(double lloyd[16], float cb[16], float thr[15], int* iters);
 void orc_fwht_f32(float* w, int n);
 void orc_fwht_f64(double* w, int n);
@@ -66,7 +73,8 @@ int  orc_gather_q4(const uint8_t* pool, int n_seq, const int32_t* pos0, int n_to
 typedef struct orc_mla {
     int32_t n_seq, n_q, n_heads, d_lat, d_rope, causal;
     const int32_t* seq_len;       /* [n_seq] rows held by each sequence                  */
-    const int32_t* seq_fmt;       /* [n_seq] ORC_FMT_FP8 or ORC_FMT_TQ4                   */
+    const int32_t* seq_fmt;       /* [n_seq] ORC_FMT_FP8, _TQ4, _TQ6 or _TQ3 (the rotated
+                                     tiers share the tq4_* planes, n*b/8 bytes a row)     */
     const int32_t* block_table;   /* [n_seq][max_pages] pool page ids, or NULL            */
     int32_t max_pages, page_size;
     int64_t seq_stride_rows;      /* without a block table: seq i row t = i*stride + t    */
