@@ -57,13 +57,15 @@ enum {
     KVQ_DEV_BAD_PAGE = 2u,   /* a position past the page table, or a page id outside
                                 the pool                                               */
     KVQ_DEV_TIMEOUT = 4u,    /* a bounded device wait expired                          */
-    KVQ_DEV_BAD_FORMAT = 8u  /* a per-sequence format that is neither FP8 nor TQ4      */
+    KVQ_DEV_BAD_FORMAT = 8u  /* a per-sequence format the kernel in use cannot read    */
 };
 
 typedef enum kvq_format {
     KVQ_FMT_FP8 = 1,         /* e4m3 codes + one fp32 scale per row                    */
     KVQ_FMT_TQ4 = 2,         /* rotated-int4: 4-bit Lloyd-Max codes + one fp32 radius  */
-    KVQ_FMT_Q4_0 = 3         /* FWHT256-rotated 18-byte q4_0 blocks                    */
+    KVQ_FMT_Q4_0 = 3,        /* FWHT256-rotated 18-byte q4_0 blocks                    */
+    KVQ_FMT_TQ6 = 4,         /* rotated tier, 6-bit codes (64 levels) + fp32 radius     */
+    KVQ_FMT_TQ3 = 5          /* rotated tier, 3-bit codes (8 levels) + fp32 radius      */
 } kvq_format;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -90,6 +92,15 @@ int kvq_set_fault(const char* spec);
  * colibri PR #399, "Why rotated-int4 for the 4-bit tier".
  */
 int kvq_tq4_codebook(float centroids[16], float thresholds[15]);
+
+/*
+ * The codebook of the rotated tier of width bits = 3, 4 or 6 (colibri PR #399: the
+ * TurboQuant tier's bit widths, KV_TQ=6 and a 3-bit setting besides the 4-bit one): the
+ * 2^bits centroids (Lloyd-Max outputs of N(0,1), each rounded to the nearest binary16
+ * value, ascending) and the 2^bits - 1 thresholds (midpoints).  Host arrays of at least
+ * 2^bits and 2^bits - 1 floats.  KVQ_EINVAL for another width or a NULL output.
+ */
+int kvq_tq_codebook(int bits, float* centroids, float* thresholds);
 
 /*
  * fp8 (KV8) per-row encode — colibri PR #399, Summary ("fp8 e4m3 + per-row scale") and
@@ -128,6 +139,19 @@ int kvq_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
 int kvq_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
                    const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
                    float* radius, kvq_stream_t stream);
+
+/*
+ * Rotated-tier encode at bits = 3, 4 or 6: steps 1-5 of kvq_encode_tq4 with the codebook
+ * of that width (kvq_tq_codebook), then
+ *   6'. the codes form a little-endian bit stream: code i occupies bits
+ *       bits*i .. bits*i + bits - 1 of the row's dim*bits/8 bytes (bit 0 = low bit of
+ *       byte 0).  For bits = 4 this is step 6 of kvq_encode_tq4, which it calls.
+ *   packed   device u8 [rows][ldp], ldp >= dim*bits/8
+ * Same dims, alignment and errors as kvq_encode_tq4, plus KVQ_EINVAL for another width.
+ */
+int kvq_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
+                  const uint32_t* sign_bits, uint8_t* packed, int64_t ldp, float* radius,
+                  kvq_stream_t stream);
 
 /*
  * q4_0 paged append — Strata PR #2533, kv_q4.metal port commit (fwht256, q4_group /
@@ -172,7 +196,8 @@ typedef struct kvq_mla_cache {
  * domain.  q4_out: device u16 (binary16 bits) [n_seq][n_tok][n_heads][256].  A bad
  * position or page sets KVQ_DEV_BAD_PAGE and that token's rows are left untouched.
  *
- * KVQ_FMT_FP8 / KVQ_FMT_TQ4 (colibri PR #399, Commit 2, "DSA-aware gather"): copies the
+ * KVQ_FMT_FP8 / KVQ_FMT_TQ4 / KVQ_FMT_TQ6 / KVQ_FMT_TQ3 (colibri PR #399, Commit 2,
+ * "DSA-aware gather"; rows of 512, 256, 384 or 192 code bytes): copies the
  * n_idx rows idx[j] of the cache `mla_src` (through page_table / page_size when
  * page_table is non-NULL, one sequence) byte for byte into the compact cache dst_*
  * (row j).  An index outside [0, mla_src_rows) sets KVQ_DEV_BAD_INDEX and row j is
@@ -207,8 +232,12 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  *     lse = log sum_t exp(s_t)
  * over the admissible rows, computed as split-T partials (m, l, o) merged by a
  * log-sum-exp combine (Commit 2, "split-T kernels").  Rows are dequantised inside the
- * kernel: fp8 c_t = code * scale; TQ4 in the rotated domain (the page's identity
- * q . xhat = rot(q) . yhat; the combine unrotates the output).  Admissible rows of
+ * kernel: fp8 c_t = code * scale; the rotated tiers (TQ4, and TQ3 / TQ6 from
+ * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
+ * the combine unrotates the output).  The tensor-core kernel reads FP8 and TQ4 rows; a
+ * uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2 with such a `fmt` is
+ * refused with KVQ_EFORMAT), and in a seq_fmt batch on the tensor-core kernel their
+ * sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
  * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
  * t <= L - n_q + j (draft + verify); with idx, only t in idx[i][j][:] (an index
  * outside [0, L) sets KVQ_DEV_BAD_INDEX and is skipped).  A query with no admissible
@@ -220,13 +249,16 @@ typedef struct kvq_mla_problem {
     int32_t causal;
     int32_t max_seq_len;            /* host: >= every seq_len[i] (sizes the grid)        */
     const int32_t* seq_len;         /* device [n_seq]                                   */
-    const int32_t* seq_fmt;         /* device [n_seq] FP8 / TQ4, or NULL: all `fmt`      */
+    const int32_t* seq_fmt;         /* device [n_seq] FP8 / TQ3 / TQ4 / TQ6, or NULL:
+                                       all `fmt`                                          */
     int32_t fmt;
     const int32_t* block_table;     /* device [n_seq][max_pages] pool page ids, or NULL */
     int32_t max_pages, page_size;
     int64_t seq_stride_rows;        /* no block table: seq i row t = pool row i*stride+t */
-    kvq_mla_cache fp8, tq4;         /* the pools of each tier (unused tier: zeros)       */
-    const uint32_t* tq4_signs;      /* device [16]: the TQ4 rotation signs              */
+    kvq_mla_cache fp8, tq4;         /* the pools of each tier (unused tier: zeros); `tq4`
+                                       holds the rotated tier's rows, 512 * b / 8 bytes
+                                       of codes each for the b-bit format in use          */
+    const uint32_t* tq4_signs;      /* device [16]: the rotation signs of the rotated tier */
     const float* q_lat;             /* device [n_seq][n_q][n_heads][512]                */
     const float* q_rope;            /* device [n_seq][n_q][n_heads][64]                 */
     const int32_t* idx;             /* device [n_seq][n_q][top_k] or NULL               */

@@ -18,14 +18,16 @@ __all__ = [
     "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
     "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "MlaCache",
     "MlaProblem", "Q4Problem", "make_q4_problem", "kvq_q4_decode", "kvq_q4_decode_workspace",
-    "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
+    "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "FMT_TQ6", "FMT_TQ3", "TQ_FMT", "kvq_encode_tq",
+    "kvq_tq_codebook", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
     "DEV_BAD_FORMAT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 
-FMT_FP8, FMT_TQ4, FMT_Q4_0 = 1, 2, 3
+FMT_FP8, FMT_TQ4, FMT_Q4_0, FMT_TQ6, FMT_TQ3 = 1, 2, 3, 4, 5
+TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code width
 IMPL_AUTO, IMPL_SIMT, IMPL_TC = 0, 1, 2
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
@@ -33,7 +35,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 
 # every symbol include/kvq.h declares
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
-           "kvq_tq4_codebook", "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4",
+           "kvq_tq4_codebook", "kvq_tq_codebook", "kvq_encode_fp8", "kvq_encode_tq4",
+           "kvq_encode_tq", "kvq_append_q4",
            "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode",
            "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode"]
 
@@ -109,6 +112,10 @@ def _declare(L):
     L.kvq_tq4_codebook.argtypes = [_p, _p]
     L.kvq_encode_fp8.restype = C.c_int
     L.kvq_encode_fp8.argtypes = [_p, _i64, C.c_int, _i64, _p, _i64, _p, _p]
+    L.kvq_tq_codebook.restype = C.c_int
+    L.kvq_tq_codebook.argtypes = [C.c_int, _p, _p]
+    L.kvq_encode_tq.restype = C.c_int
+    L.kvq_encode_tq.argtypes = [_p, _i64, C.c_int, _i64, C.c_int, _p, _p, _i64, _p, _p]
     L.kvq_encode_tq4.restype = C.c_int
     L.kvq_encode_tq4.argtypes = [_p, _i64, C.c_int, _i64, _p, _p, _i64, _p, _p]
     L.kvq_append_q4.restype = C.c_int
@@ -162,6 +169,15 @@ def kvq_tq4_codebook():
     return cb, thr
 
 
+def kvq_tq_codebook(bits: int):
+    import numpy as np
+    L = 1 << bits
+    cb = np.empty(L, np.float32)
+    thr = np.empty(L - 1, np.float32)
+    _check(lib().kvq_tq_codebook(bits, cb.ctypes.data, thr.ctypes.data))
+    return cb, thr
+
+
 def kvq_encode_fp8(x, codes, scales, stream=None) -> None:
     """x fp32 [rows][>=dim] -> codes u8 [rows][>=dim], scales fp32 [rows]; dim = codes
     columns used = x.shape[1] unless x is a strided view."""
@@ -174,6 +190,13 @@ def kvq_encode_tq4(x, sign_bits, packed, radius, stream=None) -> None:
     rows, dim = x.shape
     _check(lib().kvq_encode_tq4(_ptr(x), rows, dim, x.stride(0), _ptr(sign_bits), _ptr(packed),
                                 packed.stride(0), _ptr(radius), _stream(stream)))
+
+
+def kvq_encode_tq(x, sign_bits, bits, packed, radius, stream=None) -> None:
+    """Rotated-tier encode at 3, 4 or 6 bits: packed u8 [rows][>= dim*bits/8]."""
+    rows, dim = x.shape
+    _check(lib().kvq_encode_tq(_ptr(x), rows, dim, x.stride(0), int(bits), _ptr(sign_bits),
+                               _ptr(packed), packed.stride(0), _ptr(radius), _stream(stream)))
 
 
 def kvq_append_q4(k, v, pos0, page_table, page_size, n_cells, k_pool, v_pool,

@@ -117,6 +117,14 @@ int kvq_tq4_codebook(float centroids[16], float thresholds[15])
     return KVQ_OK;
 }
 
+int kvq_tq_codebook(int bits, float* centroids, float* thresholds)
+{
+    if (bits != 3 && bits != 4 && bits != 6) return fail(KVQ_EINVAL, "kvq_tq_codebook: bits %d not 3, 4 or 6", bits);
+    if (!centroids || !thresholds) return fail(KVQ_EINVAL, "kvq_tq_codebook: NULL output");
+    kvq::tq_codebook_values(bits, centroids, thresholds);
+    return KVQ_OK;
+}
+
 int kvq_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx, uint8_t* codes,
                    int64_t ldc, float* scales, kvq_stream_t stream)
 {
@@ -148,6 +156,25 @@ int kvq_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
         return fail(KVQ_EALIGN, "%s: x/radius/sign_bits not 4-byte aligned", E);
     return cuda_status(kvq::launch_encode_tq4(x, rows, dim, ldx, sign_bits, packed, ldp, radius,
                                               (cudaStream_t)stream), E);
+}
+
+int kvq_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
+                  const uint32_t* sign_bits, uint8_t* packed, int64_t ldp, float* radius,
+                  kvq_stream_t stream)
+{
+    const char* E = "kvq_encode_tq";
+    if (int st = injected(E)) return st;
+    if (bits != 3 && bits != 4 && bits != 6) return fail(KVQ_EINVAL, "%s: bits %d not 3, 4 or 6", E, bits);
+    if (!is_pow2(dim)) return fail(KVQ_ENOTPOW2, "%s: dim %d is not a power of two", E, dim);
+    if (dim < 64 || dim > 1024) return fail(KVQ_EINVAL, "%s: dim %d outside [64, 1024]", E, dim);
+    if (rows < 0) return fail(KVQ_EINVAL, "%s: rows < 0", E);
+    if (ldx < dim || ldp < (int64_t)dim * bits / 8) return fail(KVQ_EINVAL, "%s: ldx/ldp too small", E);
+    if (rows == 0) return KVQ_OK;
+    if (!x || !sign_bits || !packed || !radius) return fail(KVQ_EINVAL, "%s: NULL pointer", E);
+    if (!aligned(x, 4) || !aligned(radius, 4) || !aligned(sign_bits, 4))
+        return fail(KVQ_EALIGN, "%s: x/radius/sign_bits not 4-byte aligned", E);
+    return cuda_status(kvq::launch_encode_tq(x, rows, dim, ldx, bits, sign_bits, packed, ldp, radius,
+                                             (cudaStream_t)stream), E);
 }
 
 int kvq_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0, int n_tok,
@@ -188,7 +215,7 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream)
             return fail(KVQ_EALIGN, "%s: pool/out not 16-byte aligned", E);
         return cuda_status(kvq::launch_gather_q4(*d, (cudaStream_t)stream), E);
     }
-    if (d->format == KVQ_FMT_FP8 || d->format == KVQ_FMT_TQ4) {
+    if (d->format == KVQ_FMT_FP8 || kvq::rotated_format(d->format)) {
         if (d->n_idx < 0 || d->mla_src_rows < 0) return fail(KVQ_EINVAL, "%s: bad sizes", E);
         if (d->n_idx == 0) return KVQ_OK;
         const kvq_mla_cache& c = d->mla_src;
@@ -215,12 +242,14 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
     if (p->impl < 0 || p->impl > 2) return fail(KVQ_EINVAL, "%s: impl must be 0..2", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
-    if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && p->fmt != KVQ_FMT_TQ4)
-        return fail(KVQ_EFORMAT, "%s: fmt %d is neither FP8 nor TQ4", E, p->fmt);
+    if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
+        return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);
+    if (p->impl == 2 && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
+        return fail(KVQ_EFORMAT, "%s: the tensor-core kernel reads FP8 and TQ4 rows only", E);
     if (p->n_seq == 0) return KVQ_OK;
     if (!p->seq_len || !p->q_lat || !p->q_rope) return fail(KVQ_EINVAL, "%s: NULL pointer", E);
     const bool need_fp8 = p->seq_fmt || p->fmt == KVQ_FMT_FP8;
-    const bool need_tq4 = p->seq_fmt || p->fmt == KVQ_FMT_TQ4;
+    const bool need_tq4 = p->seq_fmt || kvq::rotated_format(p->fmt);
     const kvq_mla_cache* tiers[2] = {need_fp8 ? &p->fp8 : nullptr, need_tq4 ? &p->tq4 : nullptr};
     for (const kvq_mla_cache* c : tiers) {
         if (!c) continue;

@@ -123,6 +123,29 @@ __constant__ float c_tq4_thr[15] = {
     kTq4Thresholds[8], kTq4Thresholds[9], kTq4Thresholds[10], kTq4Thresholds[11],
     kTq4Thresholds[12], kTq4Thresholds[13], kTq4Thresholds[14]};
 
+// The rotated row of the TQ tiers (every width): y = c * FWHT(s (.) x) with element
+// k * 32 + lane in y[k], and its radius: per-lane fused sums of squares, then the xor
+// butterfly, then the IEEE square root (the pinned reduction order).
+template <int VPL>
+__device__ __forceinline__ float tq_rotate_row(const float* __restrict__ xr, uint32_t neg, int lane,
+                                               float c, float (&y)[VPL])
+{
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) {
+        const float v = __ldcs(xr + k * 32 + lane);
+        y[k] = ((neg >> k) & 1u) ? -v : v;
+    }
+    fwht_warp<VPL>(y, lane);
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) y[k] = __fmul_rn(y[k], c);
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) acc = __fmaf_rn(y[k], y[k], acc);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, o));
+    return __fsqrt_rn(acc);
+}
+
 template <int VPL>   // dim = 32 * VPL
 __global__ void __launch_bounds__(kCodecThreads)
 encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
@@ -143,23 +166,8 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t r = warp; r < rows; r += n_warps) {
-        const float* xr = x + r * ldx;
         float y[VPL];
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const float v = __ldcs(xr + k * 32 + lane);
-            y[k] = ((neg >> k) & 1u) ? -v : v;
-        }
-        fwht_warp<VPL>(y, lane);
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) y[k] = __fmul_rn(y[k], c);
-        // pinned reduction order: per-lane fused accumulation, then the xor butterfly
-        float acc = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) acc = __fmaf_rn(y[k], y[k], acc);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, o));
-        const float rad = __fsqrt_rn(acc);
+        const float rad = tq_rotate_row<VPL>(x + r * ldx, neg, lane, c, y);
         const float sigma = __fmul_rn(rad, c);
         uint8_t* pr = packed + r * ldp;
 #pragma unroll
@@ -183,6 +191,83 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
             __syncwarp();
             if (lane < kBytes / 16)
                 reinterpret_cast<uint4*>(pr)[lane] = reinterpret_cast<const uint4*>(s_out[wib])[lane];
+            __syncwarp();
+        }
+        if (lane == 0) radius[r] = rad;
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// The rotated tiers at 3 and 6 bits (colibri PR #399: KV_TQ=6, and 3 bits): the same row
+// transform and radius as TQ4, a 2^b-level codebook, and codes packed as a little-endian
+// bit stream (code i at bits b*i .. b*i + b - 1 of the row).  24 / b consecutive codes fill
+// 3 bytes: lanes combine them with a shuffle tree and the first lane of each group writes
+// the 3 bytes into shared memory, which the warp copies out with 16-byte stores.
+// ------------------------------------------------------------------------------------
+
+__constant__ TqCodebook<8> c_tq3 = kTq3;
+__constant__ TqCodebook<64> c_tq6 = kTq6;
+
+template <int BITS>
+__device__ __forceinline__ const float* tq_thresholds()
+{
+    if constexpr (BITS == 3) return c_tq3.thr;
+    else return c_tq6.thr;
+}
+
+template <int VPL, int BITS>   // dim = 32 * VPL
+__global__ void __launch_bounds__(kCodecThreads)
+encode_tqb_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                  const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
+                  int64_t ldp, float* __restrict__ radius, float c, bool vec_store)
+{
+    constexpr int kL = 1 << BITS;
+    constexpr int kBytes = 4 * VPL * BITS;       // dim * BITS / 8
+    constexpr int kG = 24 / BITS;                // codes per 3 bytes
+    constexpr bool kVecOk = kBytes % 16 == 0;
+    __shared__ float s_thr[kL];
+    __shared__ __align__(16) uint8_t s_out[kCodecWarps][kBytes];
+    for (int i = threadIdx.x; i < kL - 1; i += blockDim.x) s_thr[i] = tq_thresholds<BITS>()[i];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    uint32_t neg = 0;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) neg |= ((__ldg(sign_bits + k) >> lane) & 1u) << k;
+    const bool vec = kVecOk && vec_store;
+
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = warp; r < rows; r += n_warps) {
+        float y[VPL];
+        const float rad = tq_rotate_row<VPL>(x + r * ldx, neg, lane, c, y);
+        const float sigma = __fmul_rn(rad, c);
+        uint8_t* pr = packed + r * ldp;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            uint32_t code = 0;
+            if (rad != 0.0f) {
+                const float u = __fdiv_rn(y[k], sigma);
+                // count of thresholds <= u, by bisection over the sorted thresholds
+#pragma unroll
+                for (int step = kL / 2; step >= 1; step >>= 1)
+                    code += (u >= s_thr[code + step - 1]) ? step : 0;
+            }
+            uint32_t v = code;
+#pragma unroll
+            for (int w = 1; w < kG; w <<= 1) v |= __shfl_down_sync(kFull, v, w) << (BITS * w);
+            if (lane % kG == 0) {
+                const int off = (k * 32 + lane) * BITS / 8;
+                uint8_t* dst = vec ? s_out[wib] + off : pr + off;
+                dst[0] = (uint8_t)v;
+                dst[1] = (uint8_t)(v >> 8);
+                dst[2] = (uint8_t)(v >> 16);
+            }
+        }
+        if (vec) {
+            __syncwarp();
+            for (int i = lane; i < kBytes / 16; i += 32)
+                reinterpret_cast<uint4*>(pr)[i] = reinterpret_cast<const uint4*>(s_out[wib])[i];
             __syncwarp();
         }
         if (lane == 0) radius[r] = rad;
@@ -496,6 +581,47 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
     return cudaGetLastError();
 }
 
+void tq_codebook_values(int bits, float* centroids, float* thresholds)
+{
+    const int L = 1 << bits;
+    for (int k = 0; k < L; ++k) {
+        centroids[k] = bits == 4 ? kTq4Centroids[k] : bits == 3 ? kTq3.cb[k] : kTq6.cb[k];
+    }
+    for (int k = 0; k + 1 < L; ++k)
+        thresholds[k] = bits == 4 ? kTq4Thresholds[k] : bits == 3 ? kTq3.thr[k] : kTq6.thr[k];
+}
+
+cudaError_t launch_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
+                             const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                             float* radius, cudaStream_t s)
+{
+    if (bits == 4) return launch_encode_tq4(x, rows, dim, ldx, sign_bits, packed, ldp, radius, s);
+    if (rows == 0) return cudaSuccess;
+    const float c = tq4_inv_sqrt(dim);
+    const bool vec = ((uintptr_t)packed % 16 == 0) && (ldp % 16 == 0);
+    const int g = grid_for(rows, kCodecWarps);
+#define KVQ_TQB(VPL, B) encode_tqb_kernel<VPL, B><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec)
+#define KVQ_TQB_DIMS(B)                                   \
+    switch (dim) {                                        \
+        case 64:   KVQ_TQB(2, B); break;                  \
+        case 128:  KVQ_TQB(4, B); break;                  \
+        case 256:  KVQ_TQB(8, B); break;                  \
+        case 512:  KVQ_TQB(16, B); break;                 \
+        case 1024: KVQ_TQB(32, B); break;                 \
+        default: return cudaErrorInvalidValue;            \
+    }
+    if (bits == 3) {
+        KVQ_TQB_DIMS(3)
+    } else if (bits == 6) {
+        KVQ_TQB_DIMS(6)
+    } else {
+        return cudaErrorInvalidValue;
+    }
+#undef KVQ_TQB_DIMS
+#undef KVQ_TQB
+    return cudaGetLastError();
+}
+
 cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
                              int n_tok, int n_heads, const int32_t* page_table, int max_pages,
                              int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,
@@ -528,7 +654,7 @@ cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s)
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s)
 {
     if (d.n_idx == 0) return cudaSuccess;
-    const int lat_bytes = d.format == KVQ_FMT_FP8 ? kDLat : kDLat / 2;
+    const int lat_bytes = d.format == KVQ_FMT_FP8 ? kDLat : kDLat * rotated_bits(d.format) / 8;
     gather_mla_kernel<<<grid_for(d.n_idx, kCodecWarps), kCodecThreads, 0, s>>>(
         d.mla_src, lat_bytes, d.mla_src_rows, d.page_table, d.max_pages, d.page_size, d.idx,
         d.n_idx, d.dst_lat, d.dst_lat_scale, d.dst_rope, d.dst_rope_scale, d.dev_status);

@@ -37,6 +37,8 @@ __constant__ float c_cb[16] = {
     kTq4Centroids[4], kTq4Centroids[5], kTq4Centroids[6], kTq4Centroids[7],
     kTq4Centroids[8], kTq4Centroids[9], kTq4Centroids[10], kTq4Centroids[11],
     kTq4Centroids[12], kTq4Centroids[13], kTq4Centroids[14], kTq4Centroids[15]};
+__constant__ TqCodebook<8> c_cb3 = kTq3;
+__constant__ TqCodebook<64> c_cb6 = kTq6;
 
 struct DecodeArgs {
     kvq_mla_problem p;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) rotate_queries_kernel(DecodeArgs a)
     const float c = tq4_inv_sqrt(kDLat);
     for (int64_t r = warp; r < n_rows; r += n_warps) {
         const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));
-        if (seq_format(p, s) != KVQ_FMT_TQ4) continue;
+        if (!rotated_format(seq_format(p, s))) continue;
         const float* src = p.q_lat + r * kDLat;
         float y[16];
 #pragma unroll
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
     float* s_p = s_kv + kRT * kLDT;         // [kRT][kGH]
     float* s_alpha = s_p + kRT * kGH;       // [kGH]
     int* s_valid = reinterpret_cast<int*>(s_alpha + kGH);   // [kRT]
-    float* s_cb = reinterpret_cast<float*>(s_valid + kRT);  // [16] TQ4 centroids
+    float* s_cb = reinterpret_cast<float*>(s_valid + kRT);  // [64] rotated-tier centroids
 
     const kvq_mla_problem& p = a.p;
     const int split = blockIdx.x, s = blockIdx.y;
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
     const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;   // + h
     auto slot = [&](int h) { return (qrow + h) * a.n_splits + split; };
 
-    const bool bad_fmt = (fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4);
+    const bool bad_fmt = (fmt != KVQ_FMT_FP8 && !rotated_format(fmt));
     if (r0 >= n_cand || bad_fmt) {
         if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, kDevBadFormat);
         if (tid < nh) {
@@ -145,9 +147,11 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
         }
         return;
     }
-    const bool tq4 = fmt == KVQ_FMT_TQ4;
+    const bool tq4 = rotated_format(fmt);               // rows in the rotated domain
+    const int bits = rotated_bits(fmt);
     const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
-    if (tid < 16) s_cb[tid] = c_cb[tid];
+    if (tid < 64) s_cb[tid] = bits == 3 ? (tid < 8 ? c_cb3.cb[tid] : 0.0f)
+                            : bits == 6 ? c_cb6.cb[tid] : (tid < 16 ? c_cb[tid] : 0.0f);
 
     for (int i = tid; i < kGH * kD; i += kThreads) {
         const int g = i / kD, k = i % kD;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     dst[lane * 16 + e] = e4m3_to_float((ww[e >> 2] >> (8 * (e & 3))) & 0xFF) * sc;
-            } else {
+            } else if (bits == 4) {
                 const float sig = C.lat_scale[row] * c512;
                 const uint2 w = reinterpret_cast<const uint2*>(C.lat + row * (kDLat / 2))[lane];
                 const uint32_t ww[2] = {w.x, w.y};
@@ -212,6 +216,28 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
                     const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15);
                     dst[lane * 16 + e] = s_cb[code] * sig;
                 }
+            } else if (bits == 6) {
+                // elements 16 lane .. 16 lane + 15: bits 96 lane .. +95 of the bit stream
+                const float sig = C.lat_scale[row] * c512;
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(C.lat + row * (kDLat * 6 / 8) + lane * 12);
+                const uint64_t lo = (uint64_t)w[0] | ((uint64_t)w[1] << 32);
+                const uint32_t hi = w[2];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int b0 = 6 * e;          // 0 .. 90
+                    uint32_t code;
+                    if (b0 + 6 <= 64) code = (uint32_t)(lo >> b0) & 63u;
+                    else if (b0 >= 64) code = (hi >> (b0 - 64)) & 63u;
+                    else code = ((uint32_t)(lo >> b0) | (hi << (64 - b0))) & 63u;
+                    dst[lane * 16 + e] = s_cb[code] * sig;
+                }
+            } else {
+                // 3 bits: elements 16 lane .. +15 are bits 48 lane .. +47, six bytes
+                const float sig = C.lat_scale[row] * c512;
+                const uint16_t* w = reinterpret_cast<const uint16_t*>(C.lat + row * (kDLat * 3 / 8) + lane * 6);
+                const uint64_t v = (uint64_t)w[0] | ((uint64_t)w[1] << 16) | ((uint64_t)w[2] << 32);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dst[lane * 16 + e] = s_cb[(uint32_t)(v >> (3 * e)) & 7u] * sig;
             }
             const unsigned short rw = reinterpret_cast<const unsigned short*>(C.rope + row * kDRope)[lane];
             dst[kDLat + 2 * lane] = e4m3_to_float(rw & 0xFF) * sr;
@@ -373,7 +399,7 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     // thread tid owns output dim tid from here on
     float res = s_part[0][tid] + s_part[1][tid] + s_part[2][tid] + s_part[3][tid];
     res = empty ? 0.0f : res / Lt;
-    if (fmt == KVQ_FMT_TQ4) {
+    if (rotated_format(fmt)) {
         // unrotate: (1/sqrt 512) s (.) FWHT_512(out); stages h < 32 within the warp,
         // h >= 32 through shared memory
 #pragma unroll
@@ -406,7 +432,8 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.n_cand_max = (int)n_cand;
     // the tensor-core kernel unless the caller asks for CUDA cores; below 8 heads the
     // 32-head MMA tile would be mostly padding
-    plan.tc = p.impl == 2 || (p.impl == 0 && p.n_heads >= 8);
+    // (uniform 3- and 6-bit problems: the CUDA-core kernel, the only one that reads them)
+    plan.tc = p.impl == 2 || (p.impl == 0 && p.n_heads >= 8 && !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
     int64_t split_rows = p.split_rows;
     if (plan.tc) {
         constexpr int kTile = 128, kHeadsTc = 32;
@@ -438,7 +465,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.split_rows = (int)split_rows;
     plan.n_splits = (int)std::max<int64_t>(1, (n_cand + split_rows - 1) / split_rows);
     const size_t rows = (size_t)p.n_seq * p.n_q * p.n_heads;
-    const bool any_tq4 = p.seq_fmt != nullptr || p.fmt == KVQ_FMT_TQ4;
+    const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
     size_t off = 0;
     plan.off_qrot = off;
     off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
@@ -469,7 +496,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.lse = lse;
     a.status = dev_status;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
-    const bool any_tq4 = p.seq_fmt != nullptr || p.fmt == KVQ_FMT_TQ4;
+    const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
     if (any_tq4 && !plan.tc) {
         int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
@@ -481,7 +508,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
         return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
     }
     const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
-                        + kRT * sizeof(int) + 16 * sizeof(float);
+                        + kRT * sizeof(int) + 64 * sizeof(float);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;

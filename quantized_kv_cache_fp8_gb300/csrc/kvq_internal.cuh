@@ -7,6 +7,7 @@
 #include <utility>
 
 #include "kvq.h"
+#include "kvq_tq_codebooks.cuh"
 
 namespace kvq {
 
@@ -43,6 +44,44 @@ constexpr float kTq4Thresholds[15] = {
     -0x1.334p+1f, -0x1.d7ep+0f, -0x1.6fep+0f, -0x1.196p+0f, -0x1.996p-1f, -0x1.0b7p-1f,
     -0x1.086p-2f, 0.0f, 0x1.086p-2f, 0x1.0b7p-1f, 0x1.996p-1f, 0x1.196p+0f, 0x1.6fep+0f,
     0x1.d7ep+0f, 0x1.334p+1f};
+
+// The rotated tiers at 3 and 6 bits: the generated binary16 centroids (see
+// gen_tq_codebooks.py), their exact fp32 values and the midpoints, at compile time.
+constexpr float f16_bits_value(uint16_t h)
+{
+    const int e = (h >> 10) & 31, m = h & 1023;
+    float v = e == 0 ? (float)m / 1024.0f * (1.0f / 16384.0f) : (1.0f + (float)m / 1024.0f);
+    for (int i = 15; i < e; ++i) v *= 2.0f;
+    for (int i = e; i < 15 && e != 0; ++i) v *= 0.5f;
+    return (h & 0x8000) ? -v : v;
+}
+
+template <int N>
+struct TqCodebook {
+    float cb[N];
+    float thr[N - 1];
+};
+
+template <int N>
+constexpr TqCodebook<N> tq_codebook_of(const uint16_t (&bits)[N])
+{
+    TqCodebook<N> r{};
+    for (int k = 0; k < N; ++k) r.cb[k] = f16_bits_value(bits[k]);
+    for (int k = 0; k + 1 < N; ++k) r.thr[k] = (r.cb[k] + r.cb[k + 1]) * 0.5f;
+    return r;
+}
+
+constexpr TqCodebook<8> kTq3 = tq_codebook_of(kTq3CentroidBits);
+constexpr TqCodebook<64> kTq6 = tq_codebook_of(kTq6CentroidBits);
+
+__host__ __device__ constexpr bool rotated_format(int fmt)
+{
+    return fmt == KVQ_FMT_TQ4 || fmt == KVQ_FMT_TQ6 || fmt == KVQ_FMT_TQ3;
+}
+__host__ __device__ constexpr int rotated_bits(int fmt)
+{
+    return fmt == KVQ_FMT_TQ3 ? 3 : fmt == KVQ_FMT_TQ6 ? 6 : 4;
+}
 
 // ------------------------------------------------------------------------------------
 // Walsh-Hadamard butterflies over a warp-distributed row: element i = k * 32 + lane,
@@ -109,6 +148,12 @@ cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx
 cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
                               const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
                               float* radius, cudaStream_t s);
+// rotated tiers at b = 3, 4, 6 bits: b = 4 is launch_encode_tq4
+cudaError_t launch_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
+                             const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
+                             float* radius, cudaStream_t s);
+// the stored codebook of width b (2^b centroids, 2^b - 1 thresholds), host side
+void tq_codebook_values(int bits, float* centroids, float* thresholds);
 cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,
                              int n_tok, int n_heads, const int32_t* page_table, int max_pages,
                              int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,

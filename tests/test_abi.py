@@ -91,7 +91,11 @@ def test_decode_argument_errors(kvq):
     L = kvq.lib()
     dec = lambda p, ws=None, n=0: L.kvq_mla_decode(C.byref(p), FAKE, None, ws, n, None, None)
     assert dec(_problem(kvq, d_lat=256)) == 1
-    assert dec(_problem(kvq, fmt=5)) == 3
+    assert dec(_problem(kvq, fmt=7)) == 3
+    # 3- and 6-bit rotated rows: the CUDA-core kernel; the tensor-core one refuses them
+    for fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6):
+        assert dec(_problem(kvq, fmt=fmt)) == 5                                  # workspace next
+        assert dec(_problem(kvq, fmt=fmt, impl=2)) == 3
     assert dec(_problem(kvq, tq4_signs=None)) == 1
     assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
     assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1
@@ -146,6 +150,33 @@ def test_q4_decode_argument_errors(kvq):
     p1 = _q4_problem(kvq, split_rows=1024)
     rows, splits = 2 * 16, 4
     assert L.kvq_q4_decode_workspace(C.byref(p1)) >= rows * splits * (2 + 256) * 4
+
+
+def test_tq_codebooks_equal_the_oracle(kvq, orc):
+    """The library's binary16 codebooks (written by gen_tq_codebooks.py, its own Lloyd-Max
+    solve) equal the oracle's, centroids and thresholds, at every width."""
+    import numpy as np
+    for bits in (3, 4, 6):
+        cb, thr = kvq.kvq_tq_codebook(bits)
+        _, ocb, othr, _ = orc.tq_codebook(bits)
+        assert np.array_equal(cb, ocb) and np.array_equal(thr, othr)
+    L = kvq.lib()
+    buf = (C.c_float * 64)()
+    assert L.kvq_tq_codebook(5, buf, buf) == 1
+    assert L.kvq_tq_codebook(6, None, buf) == 1
+
+
+def test_encode_tq_argument_errors(kvq):
+    L = kvq.lib()
+    enc = lambda rows, dim, ldx, bits, ldp: L.kvq_encode_tq(FAKE, rows, dim, ldx, bits, FAKE, FAKE,
+                                                            ldp, FAKE, None)
+    assert enc(4, 512, 512, 5, 512) == 1                      # width
+    assert enc(4, 384, 384, 6, 384) == 2                      # not a power of two
+    assert enc(4, 2048, 2048, 6, 2048) == 1                   # above 1024
+    assert enc(4, 512, 512, 6, 383) == 1                      # ldp < 512 * 6 / 8
+    assert enc(4, 512, 512, 3, 191) == 1
+    assert enc(0, 512, 512, 6, 384) == 0                      # nothing to do
+    assert L.kvq_encode_tq(FAKE + 2, 4, 512, 512, 6, FAKE, FAKE, 384, FAKE, None) == 4
 
 
 def test_fault_injection(kvq):
