@@ -438,6 +438,13 @@ def run_codecs(args, local):
     rad = torch.empty(T, device=dev)
     s = timed(lambda: kvq.kvq_encode_tq4(x, signs, packed, rad))
     report("kvq_encode_tq4", f"T={T} rows of 512", T * (512 * 4 + 256 + 4) + 64, s, T, "rows")
+    # the rotated tier at 6 and 3 bits on the same rows
+    for bits in (6, 3):
+        pk = torch.empty(T, 512 * bits // 8, dtype=torch.uint8, device=dev)
+        s = timed(lambda: kvq.kvq_encode_tq(x, signs, bits, pk, rad))
+        report(f"kvq_encode_tq ({bits} bits)", f"T={T} rows of 512",
+               T * (512 * 4 + 512 * bits // 8 + 4) + 64, s, T, "rows")
+        del pk
     del x, packed, rad
 
     # a3 / a4: q4_0 paged append and gather, 16 sequences x 8192 tokens x 8 heads x 256
@@ -530,14 +537,15 @@ def run_decode_configs(args, local):
                 float(np.log(mag[0])), float(np.log(mag[1])), generator=gen))
             c *= m
             r *= m
-        lat = torch.empty(n_rows, 512 if fmt == kvq.FMT_FP8 else 256, dtype=torch.uint8, device=dev)
+        bits = {kvq.FMT_TQ3: 3, kvq.FMT_TQ4: 4, kvq.FMT_TQ6: 6}.get(fmt, 8)
+        lat = torch.empty(n_rows, 512 * bits // 8, dtype=torch.uint8, device=dev)
         ls = torch.empty(n_rows, device=dev)
         rope = torch.empty(n_rows, 64, dtype=torch.uint8, device=dev)
         rs = torch.empty(n_rows, device=dev)
         if fmt == kvq.FMT_FP8:
             kvq.kvq_encode_fp8(c, lat, ls)
         else:
-            kvq.kvq_encode_tq4(c, signs, lat, ls)
+            kvq.kvq_encode_tq(c, signs, bits, lat, ls)
         kvq.kvq_encode_fp8(r, rope, rs)
         return dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
 
@@ -582,11 +590,13 @@ def run_decode_configs(args, local):
         if idx_k:
             idx = torch.from_numpy(W.sparse_indices(T, idx_k, 1, seed=0)).to(dev).reshape(1, 1, idx_k)
         kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
+        # 3- and 6-bit rows are read by the CUDA-core kernel only
+        impl = 1 if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and args.decode_impl == 2 else args.decode_impl
         p = kvq.make_problem(seq_len=torch.tensor([T], dtype=torch.int32, device=dev),
                              q_lat=torch.from_numpy(q.q_lat).to(dev), q_rope=torch.from_numpy(q.q_rope).to(dev),
-                             sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx, impl=args.decode_impl, **kw)
+                             sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx, impl=impl, **kw)
         n = idx_k or T
-        rb = 584 if fmt == kvq.FMT_FP8 else 328
+        rb = {kvq.FMT_FP8: 584, kvq.FMT_TQ4: 328, kvq.FMT_TQ6: 456, kvq.FMT_TQ3: 264}[fmt]
         measure(name, p, (1, 1, H, 512), n, rb, 2 * H * 1088 * n)
 
     F8, T4 = kvq.FMT_FP8, kvq.FMT_TQ4
@@ -597,6 +607,9 @@ def run_decode_configs(args, local):
     for fmt, tag in ((F8, "fp8"), (T4, "TQ4")):
         for T in (32768, 131072):
             one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
+    # the rotated tier at 6 and 3 bits (CUDA-core kernel, the one that reads them)
+    for fmt, tag in ((kvq.FMT_TQ6, "TQ6"), (kvq.FMT_TQ3, "TQ3")):
+        one_seq(f"{tag}: T=32768, H=16 (CUDA-core kernel)", fmt, 32768, 16)
 
     # ragged mixed-tier batch: 32 sequences, L ~ U[1024, 65536], 4 causal queries, H=64
     if not wanted("ragged: 32 seqs"):
