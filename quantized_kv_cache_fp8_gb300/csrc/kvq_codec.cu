@@ -208,6 +208,45 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
 __constant__ TqCodebook<8> c_tq3 = kTq3;
 __constant__ TqCodebook<64> c_tq6 = kTq6;
 
+// 64 levels: instead of a six-step bisection, u is placed in one of 257 buckets
+// b = round-to-even(32 u + 128) (one fma against 1.5 * 2^23, exact), clamped to [0, 256];
+// kTq6Base[b] counts the thresholds below the bucket's lowest possible u (32 u + 128 =
+// b - 1/2), and no bucket, edges included, holds more than one threshold (checked below),
+// so the code is kTq6Base[b] + (u >= thr[kTq6Base[b]]).  thr[63] is +inf padding.
+struct Tq6Buckets {
+    uint8_t base[257];
+};
+
+constexpr Tq6Buckets tq6_buckets()
+{
+    Tq6Buckets r{};
+    for (int b = 0; b <= 256; ++b) {
+        int n = 0;
+        for (int k = 0; k < 63; ++k)
+            if (kTq6.thr[k] * 32.0f + 128.0f < (float)b - 0.5f) ++n;
+        r.base[b] = (uint8_t)n;
+    }
+    return r;
+}
+
+constexpr bool tq6_buckets_hold_one_threshold()
+{
+    for (int b = 0; b <= 256; ++b) {
+        int n = 0;
+        for (int k = 0; k < 63; ++k) {
+            const float v = kTq6.thr[k] * 32.0f + 128.0f;
+            if (v >= (float)b - 0.5f && v <= (float)b + 0.5f) ++n;
+        }
+        if (n > 1) return false;
+    }
+    // the clamped end buckets hold no threshold beyond their range
+    return kTq6.thr[0] * 32.0f + 128.0f > 0.5f && kTq6.thr[62] * 32.0f + 128.0f < 255.5f;
+}
+static_assert(tq6_buckets_hold_one_threshold(), "6-bit bucket table needs a finer grid");
+
+constexpr Tq6Buckets kTq6Buckets = tq6_buckets();
+__constant__ Tq6Buckets c_tq6_buckets = kTq6Buckets;
+
 template <int BITS>
 __device__ __forceinline__ const float* tq_thresholds()
 {
@@ -216,7 +255,7 @@ __device__ __forceinline__ const float* tq_thresholds()
 }
 
 template <int VPL, int BITS>   // dim = 32 * VPL
-__global__ void __launch_bounds__(kCodecThreads)
+__global__ void __launch_bounds__(kCodecThreads, 4)
 encode_tqb_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
                   const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
                   int64_t ldp, float* __restrict__ radius, float c, bool vec_store)
@@ -226,8 +265,12 @@ encode_tqb_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
     constexpr int kG = 24 / BITS;                // codes per 3 bytes
     constexpr bool kVecOk = kBytes % 16 == 0;
     __shared__ float s_thr[kL];
+    __shared__ uint8_t s_base[BITS == 6 ? 257 : 1];
     __shared__ __align__(16) uint8_t s_out[kCodecWarps][kBytes];
-    for (int i = threadIdx.x; i < kL - 1; i += blockDim.x) s_thr[i] = tq_thresholds<BITS>()[i];
+    for (int i = threadIdx.x; i < kL; i += blockDim.x)
+        s_thr[i] = i < kL - 1 ? tq_thresholds<BITS>()[i] : INFINITY;
+    if constexpr (BITS == 6)
+        for (int i = threadIdx.x; i < 257; i += blockDim.x) s_base[i] = c_tq6_buckets.base[i];
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
@@ -248,10 +291,16 @@ encode_tqb_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
             uint32_t code = 0;
             if (rad != 0.0f) {
                 const float u = __fdiv_rn(y[k], sigma);
-                // count of thresholds <= u, by bisection over the sorted thresholds
+                if constexpr (BITS == 6) {
+                    const int b = __float_as_int(fmaf(u, 32.0f, 128.0f + 12582912.0f)) - 0x4B400000;
+                    code = s_base[min(max(b, 0), 256)];
+                    code += (u >= s_thr[code]) ? 1u : 0u;
+                } else {
+                    // count of thresholds <= u, by bisection over the sorted thresholds
 #pragma unroll
-                for (int step = kL / 2; step >= 1; step >>= 1)
-                    code += (u >= s_thr[code + step - 1]) ? step : 0;
+                    for (int step = kL / 2; step >= 1; step >>= 1)
+                        code += (u >= s_thr[code + step - 1]) ? step : 0;
+                }
             }
             uint32_t v = code;
 #pragma unroll
