@@ -579,15 +579,24 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             const bool fp8 = it.ch == 8 || !tq4;
             uint4 raw[4];
             if (tma) {
-                // the loader's box: row t at t * (bytes per row of the chunk)
+                // the loader's box: row t at t * (bytes per row of the chunk), its 16-byte
+                // pieces swizzled (64-byte rows: piece i at i ^ ((t >> 1) & 3); 32-byte rows:
+                // i ^ ((t >> 2) & 1)) so that the rows a quarter-warp reads share no bank
                 const int d = j % kStages;
                 ok = __all_sync(kFull, wait_bar(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status));
                 if (!ok) break;
                 const uint8_t* st = sh.stage(set, d) + t * (fp8 ? 64 : 32);
-                raw[0] = *reinterpret_cast<const uint4*>(st);
-                raw[1] = *reinterpret_cast<const uint4*>(st + 16);
-                raw[2] = fp8 ? *reinterpret_cast<const uint4*>(st + 32) : make_uint4(0u, 0u, 0u, 0u);
-                raw[3] = fp8 ? *reinterpret_cast<const uint4*>(st + 48) : make_uint4(0u, 0u, 0u, 0u);
+                if (fp8) {
+                    const int x = (t >> 1) & 3;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) raw[i] = *reinterpret_cast<const uint4*>(st + 16 * (i ^ x));
+                } else {
+                    const int x = (t >> 2) & 1;
+                    raw[0] = *reinterpret_cast<const uint4*>(st + 16 * x);
+                    raw[1] = *reinterpret_cast<const uint4*>(st + 16 * (1 ^ x));
+                    raw[2] = make_uint4(0u, 0u, 0u, 0u);
+                    raw[3] = make_uint4(0u, 0u, 0u, 0u);
+                }
             } else {
                 cp_async_wait<kStages - 1>();             // item j's group has landed
                 const uint8_t* st = sh.stage(set, j % kStages) + t * 16;
@@ -986,7 +995,9 @@ bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row
     const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kRT};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
