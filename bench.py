@@ -497,6 +497,43 @@ def run_codecs(args, local):
            s, toks, "tokens")
     del out, k_pool, v_pool, ws
 
+    # cache files: save and load of the 4-bit tier's cache (T=32768 rows), and the
+    # quantize-on-load of an fp32 file into the fp8 tier; host I/O through the page cache,
+    # so file bytes per second, not an HBM fraction
+    import tempfile
+    T = 32768
+    c = torch.randn(T, 512, generator=gen, device=dev)
+    r = torch.randn(T, 64, generator=gen, device=dev)
+    planes = dict(lat=torch.empty(T, 256, dtype=torch.uint8, device=dev), lat_scale=torch.empty(T, device=dev),
+                  rope=torch.empty(T, 64, dtype=torch.uint8, device=dev), rope_scale=torch.empty(T, device=dev))
+    kvq.kvq_encode_tq4(c, signs, planes["lat"], planes["lat_scale"])
+    kvq.kvq_encode_fp8(r, planes["rope"], planes["rope_scale"])
+    p8 = dict(lat=torch.empty(T, 512, dtype=torch.uint8, device=dev), lat_scale=torch.empty(T, device=dev),
+              rope=torch.empty(T, 64, dtype=torch.uint8, device=dev), rope_scale=torch.empty(T, device=dev))
+    ws_up = torch.empty(kvq.kvq_cache_load_workspace(), dtype=torch.uint8, device=dev)
+    with tempfile.TemporaryDirectory() as td:
+        f4, f32 = os.path.join(td, "tq4.kvq"), os.path.join(td, "f32.kvq")
+        kvq.kvq_cache_save_f32(f32, c, r)
+        for name, fn, path in (("kvq_cache_save (TQ4)", lambda: kvq.kvq_cache_save(f4, kvq.FMT_TQ4, planes, T, signs=signs), f4),
+                               ("kvq_cache_load (TQ4)", lambda: kvq.kvq_cache_load(f4, kvq.FMT_TQ4, planes, signs=signs), f4),
+                               ("kvq_cache_load (fp32 file -> fp8 tier)",
+                                lambda: kvq.kvq_cache_load(f32, kvq.FMT_FP8, p8, workspace=ws_up), f32)):
+            fn()
+            ts = []
+            for _ in range(max(3, min(K, 10))):
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            sec = statistics.median(ts)
+            nb = os.path.getsize(path)
+            print(json.dumps({"suite": "codecs", "kernel": name, "workload": f"T={T} rows, file {nb} B",
+                              "us": round(sec * 1e6, 1), "rows_per_s": T / sec,
+                              "file_gbs": round(nb / sec / 1e9, 3),
+                              "note": "host file I/O through the page cache (wall clock)",
+                              "steps": len(ts)}), flush=True)
+    del c, r, planes, p8, ws_up
+
     # a7: sparse row gather of the fp8 MLA cache, top-k = 2048 of T = 131072
     T, k_sel = 131072, 2048
     src = dict(lat=torch.zeros(T, 512, dtype=torch.uint8, device=dev), lat_scale=torch.ones(T, device=dev),

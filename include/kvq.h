@@ -48,7 +48,10 @@ typedef enum kvq_status {
     KVQ_EALIGN = 4,          /* a base pointer or leading dimension is misaligned      */
     KVQ_EWORKSPACE = 5,      /* the workspace is NULL or smaller than required         */
     KVQ_ECUDA = 6,           /* a CUDA launch or attribute call failed                 */
-    KVQ_EFAULT_INJECTED = 7  /* host-side fault injection (kvq_set_fault) fired        */
+    KVQ_EFAULT_INJECTED = 7, /* host-side fault injection (kvq_set_fault) fired        */
+    KVQ_EMISMATCH = 8,       /* a cache file written under another mode: refused       */
+    KVQ_EIO = 9              /* a cache file cannot be opened, read or written, or its
+                                byte counts do not add up                              */
 } kvq_status;
 
 /* bits of *dev_status */
@@ -348,6 +351,87 @@ size_t kvq_q4_decode_workspace(const kvq_q4_problem* p);
  */
 int kvq_q4_decode(const kvq_q4_problem* p, float* out, float* lse, void* workspace,
                   size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream);
+
+/*
+ * Cache persistence — colibri PR #399, Commit 1 (".coli_kv v2: quantize-on-upgrade from
+ * v1, reject-on-mismatch, self-heal"), Commit 6 (v3: the magic encodes the tier and a
+ * header word carries codec << 8 | bits) and the review thread (a cache written under
+ * one mode and read under another must be refused, never misread; containers whose
+ * byte counts do not add up are refused).  The layout is this library's own:
+ *
+ *   header  16 little-endian u32 words
+ *     w0  magic: 0x3151564B "KVQ1" fp32 rows, 0x3251564B "KVQ2" fp8 tier,
+ *                0x3351564B "KVQ3" rotated tier
+ *     w1  layout version = 1
+ *     w2  d_lat = 512      w3  d_rope = 64
+ *     w4  n_rows (low)     w5  n_rows (high)      complete records
+ *     w6  format: 0 (fp32 rows), KVQ_FMT_FP8, KVQ_FMT_TQ3, KVQ_FMT_TQ4, KVQ_FMT_TQ6
+ *     w7  codec << 8 | bits: (0, 32) fp32, (0, 8) fp8, (1, b) rotated b-bit
+ *     w8  record bytes      w9 .. w15  zero
+ *   rotated tier: the 16 u32 rotation-sign words
+ *   n_rows records, row after row:
+ *     fp32     lat f32[512], rope f32[64]                                  (2304 B)
+ *     fp8      lat u8[512], lat_scale f32, rope u8[64], rope_scale f32     (584 B)
+ *     rotated  lat u8[512 b / 8], radius f32, rope u8[64], rope_scale f32  (264/328/456 B)
+ *
+ * These calls are synchronous: they synchronize `stream`, move the planes through host
+ * memory (they allocate host buffers, never device memory) and return when done.
+ */
+typedef struct kvq_cache_info {
+    int32_t format;           /* w6                                                      */
+    int32_t codec, bits;      /* w7                                                      */
+    int32_t d_lat, d_rope;
+    int64_t n_rows;           /* complete records the header counts                      */
+    int64_t record_bytes;
+    int64_t trailing_bytes;   /* bytes after those records (an interrupted append)      */
+} kvq_cache_info;
+
+/* Read and check a cache file's header (host only).  KVQ_EIO if it cannot be read, is
+ * not a cache file, or holds fewer bytes than its header counts. */
+int kvq_cache_probe(const char* path, kvq_cache_info* info);
+
+/*
+ * Write rows [0, rows) of a quantized cache (format KVQ_FMT_FP8 / TQ3 / TQ4 / TQ6) to
+ * `path`, replacing it.  planes: device planes of that format (lat rows of 512 or
+ * 512 b / 8 bytes); signs: device u32[16] rotation signs (rotated tiers; else NULL).
+ */
+int kvq_cache_save(const char* path, int32_t format, const kvq_mla_cache* planes,
+                   const uint32_t* signs, int64_t rows, kvq_stream_t stream);
+
+/* Write an fp32 (layout "KVQ1") file of rows: lat device f32 [rows][512], rope device f32
+ * [rows][64] — the unquantized cache an upgrade starts from. */
+int kvq_cache_save_f32(const char* path, const float* lat, const float* rope, int64_t rows,
+                       kvq_stream_t stream);
+
+/*
+ * Append rows [row0, row0 + rows) of the planes to a quantized cache file in place.
+ * Self-heal: bytes after the header's n_rows records (a record an interrupted append
+ * left behind) are cut first; the records are written, then n_rows.  KVQ_EMISMATCH if
+ * the file holds another format; KVQ_EIO as for kvq_cache_probe.
+ */
+int kvq_cache_append(const char* path, int32_t format, const kvq_mla_cache* planes,
+                     int64_t row0, int64_t rows, kvq_stream_t stream);
+
+/* Device workspace bytes kvq_cache_load needs to upgrade an fp32 file (0 otherwise
+ * suffices for same-format loads). */
+size_t kvq_cache_load_workspace(void);
+
+/*
+ * Load a cache file under `format` into device planes with room for `capacity` rows
+ * (*n_loaded = the file's n_rows):
+ *   - the file holds `format` (rotated: the same width and the same signs as `signs`):
+ *     its records are copied into the planes;
+ *   - the file holds fp32 rows ("KVQ1") and `format` is quantized: quantize on load —
+ *     the rows are encoded by kvq_encode_fp8 / kvq_encode_tq (and the rope by
+ *     kvq_encode_fp8) through `workspace`; the file is left as it is;
+ *   - any other pairing: KVQ_EMISMATCH, nothing written.
+ * KVQ_EINVAL if n_rows > capacity; KVQ_EWORKSPACE for an upgrade without
+ * kvq_cache_load_workspace() bytes.  Trailing bytes after the n_rows records are
+ * ignored (kvq_cache_append cuts them).
+ */
+int kvq_cache_load(const char* path, int32_t format, const uint32_t* signs,
+                   const kvq_mla_cache* planes, int64_t capacity, int64_t* n_loaded,
+                   void* workspace, size_t ws_bytes, kvq_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -31,14 +31,17 @@ TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code wi
 IMPL_AUTO, IMPL_SIMT, IMPL_TC = 0, 1, 2
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
-          5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED"}
+          5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED", 8: "KVQ_EMISMATCH",
+          9: "KVQ_EIO"}
 
 # every symbol include/kvq.h declares
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_tq4_codebook", "kvq_tq_codebook", "kvq_encode_fp8", "kvq_encode_tq4",
            "kvq_encode_tq", "kvq_append_q4",
            "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode",
-           "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode"]
+           "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode",
+           "kvq_cache_probe", "kvq_cache_save", "kvq_cache_save_f32", "kvq_cache_append",
+           "kvq_cache_load_workspace", "kvq_cache_load"]
 
 
 class KvqError(RuntimeError):
@@ -82,6 +85,12 @@ class Q4Problem(C.Structure):
                 ("max_pages", _i32), ("page_size", _i32), ("n_cells", _i64),
                 ("k_pool", _p), ("v_pool", _p), ("q", _p), ("gate", _p),
                 ("sm_scale", _f32), ("split_rows", _i32)]
+
+
+class CacheInfo(C.Structure):
+    _fields_ = [("format", _i32), ("codec", _i32), ("bits", _i32), ("d_lat", _i32),
+                ("d_rope", _i32), ("n_rows", _i64), ("record_bytes", _i64),
+                ("trailing_bytes", _i64)]
 
 
 _lock = threading.Lock()
@@ -129,6 +138,19 @@ def _declare(L):
     L.kvq_mla_decode.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, C.c_size_t, _p, _p]
     L.kvq_mla_decode_noalloc.restype = C.c_int
     L.kvq_mla_decode_noalloc.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, _p]
+    L.kvq_cache_probe.restype = C.c_int
+    L.kvq_cache_probe.argtypes = [C.c_char_p, C.POINTER(CacheInfo)]
+    L.kvq_cache_save.restype = C.c_int
+    L.kvq_cache_save.argtypes = [C.c_char_p, C.c_int32, C.POINTER(MlaCache), _p, _i64, _p]
+    L.kvq_cache_save_f32.restype = C.c_int
+    L.kvq_cache_save_f32.argtypes = [C.c_char_p, _p, _p, _i64, _p]
+    L.kvq_cache_append.restype = C.c_int
+    L.kvq_cache_append.argtypes = [C.c_char_p, C.c_int32, C.POINTER(MlaCache), _i64, _i64, _p]
+    L.kvq_cache_load_workspace.restype = C.c_size_t
+    L.kvq_cache_load_workspace.argtypes = []
+    L.kvq_cache_load.restype = C.c_int
+    L.kvq_cache_load.argtypes = [C.c_char_p, C.c_int32, _p, C.POINTER(MlaCache), _i64,
+                                 C.POINTER(_i64), _p, C.c_size_t, _p]
     L.kvq_q4_decode_workspace.restype = C.c_size_t
     L.kvq_q4_decode_workspace.argtypes = [C.POINTER(Q4Problem)]
     L.kvq_q4_decode.restype = C.c_int
@@ -311,3 +333,44 @@ def kvq_q4_decode(p: Q4Problem, out, lse=None, workspace=None, dev_status=None,
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().kvq_q4_decode(C.byref(p), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                _ptr(dev_status), _stream(stream)))
+
+
+# --- cache files ------------------------------------------------------------------------
+
+def kvq_cache_probe(path) -> CacheInfo:
+    info = CacheInfo()
+    _check(lib().kvq_cache_probe(os.fsencode(path), C.byref(info)))
+    return info
+
+
+def kvq_cache_save(path, fmt, planes: dict, rows, signs=None, stream=None) -> None:
+    """planes: dict of device tensors lat, lat_scale, rope, rope_scale (a quantized tier)."""
+    c = _cache(planes)
+    _check(lib().kvq_cache_save(os.fsencode(path), int(fmt), C.byref(c), _ptr(signs), int(rows),
+                                _stream(stream)))
+
+
+def kvq_cache_save_f32(path, lat, rope, stream=None) -> None:
+    _check(lib().kvq_cache_save_f32(os.fsencode(path), _ptr(lat), _ptr(rope), lat.shape[0],
+                                    _stream(stream)))
+
+
+def kvq_cache_append(path, fmt, planes: dict, row0, rows, stream=None) -> None:
+    c = _cache(planes)
+    _check(lib().kvq_cache_append(os.fsencode(path), int(fmt), C.byref(c), int(row0), int(rows),
+                                  _stream(stream)))
+
+
+def kvq_cache_load_workspace() -> int:
+    return lib().kvq_cache_load_workspace()
+
+
+def kvq_cache_load(path, fmt, planes: dict, signs=None, workspace=None, stream=None) -> int:
+    """Load `path` under `fmt` into the device planes (their row count is the capacity);
+    returns the rows loaded."""
+    c = _cache(planes)
+    n = _i64(0)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kvq_cache_load(os.fsencode(path), int(fmt), _ptr(signs), C.byref(c), c.n_rows,
+                                C.byref(n), _ptr(workspace), ws_bytes, _stream(stream)))
+    return n.value

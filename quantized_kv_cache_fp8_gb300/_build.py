@@ -25,6 +25,7 @@ UNITS = {
     "kvq_decode_tc.cu": [],
     "kvq_noalloc.cu": [],
     "kvq_q4_decode.cu": [],
+    "kvq_persist.cu": [],
 }
 
 
