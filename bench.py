@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--only", default="",
                     help="decode-configs: run only the configurations whose name contains this text")
     ap.add_argument("--decode-impl", type=int, default=0,
-                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores")
+                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores "
+                         "(tcgen05), 3 tensor cores (warp-level MMA)")
     return ap.parse_args()
 
 
@@ -628,7 +629,7 @@ def run_decode_configs(args, local):
             idx = torch.from_numpy(W.sparse_indices(T, idx_k, 1, seed=0)).to(dev).reshape(1, 1, idx_k)
         kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
         # 3- and 6-bit rows are read by the CUDA-core kernel only
-        impl = 1 if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and args.decode_impl == 2 else args.decode_impl
+        impl = 1 if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and args.decode_impl >= 2 else args.decode_impl
         p = kvq.make_problem(seq_len=torch.tensor([T], dtype=torch.int32, device=dev),
                              q_lat=torch.from_numpy(q.q_lat).to(dev), q_rope=torch.from_numpy(q.q_rope).to(dev),
                              sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx, impl=impl, **kw)

@@ -237,10 +237,10 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  * log-sum-exp combine (Commit 2, "split-T kernels").  Rows are dequantised inside the
  * kernel: fp8 c_t = code * scale; the rotated tiers (TQ4, and TQ3 / TQ6 from
  * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
- * the combine unrotates the output).  The tensor-core kernel reads FP8 and TQ4 rows; a
- * uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2 with such a `fmt` is
- * refused with KVQ_EFORMAT), and in a seq_fmt batch on the tensor-core kernel their
- * sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
+ * the combine unrotates the output).  The two tensor-core kernels read FP8 and TQ4 rows;
+ * a uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2 or 3 with such a
+ * `fmt` is refused with KVQ_EFORMAT), and in a seq_fmt batch on a tensor-core kernel
+ * their sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
  * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
  * t <= L - n_q + j (draft + verify); with idx, only t in idx[i][j][:] (an index
  * outside [0, L) sets KVQ_DEV_BAD_INDEX and is skipped).  A query with no admissible
@@ -269,7 +269,8 @@ typedef struct kvq_mla_problem {
     float sm_scale;
     int32_t split_rows;             /* rows per split; 0: the library chooses            */
     int32_t impl;                   /* 0: library chooses; 1: CUDA-core kernel;
-                                       2: tensor-core (tcgen05) kernel                   */
+                                       2: tensor-core (tcgen05) kernel, 32 heads a CTA;
+                                       3: warp-level MMA kernel, 16 heads a CTA          */
 } kvq_mla_problem;
 
 /* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */

@@ -240,12 +240,12 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if (p->n_q < 1 || p->n_heads < 1 || p->max_seq_len < 0 || p->split_rows < 0)
         return fail(KVQ_EINVAL, "%s: bad sizes", E);
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
-    if (p->impl < 0 || p->impl > 2) return fail(KVQ_EINVAL, "%s: impl must be 0..2", E);
+    if (p->impl < 0 || p->impl > 3) return fail(KVQ_EINVAL, "%s: impl must be 0..3", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
         return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);
-    if (p->impl == 2 && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
-        return fail(KVQ_EFORMAT, "%s: the tensor-core kernel reads FP8 and TQ4 rows only", E);
+    if (p->impl >= 2 && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
+        return fail(KVQ_EFORMAT, "%s: the tensor-core kernels read FP8 and TQ4 rows only", E);
     if (p->n_seq == 0) return KVQ_OK;
     if (!p->seq_len || !p->q_lat || !p->q_rope) return fail(KVQ_EINVAL, "%s: NULL pointer", E);
     const bool need_fp8 = p->seq_fmt || p->fmt == KVQ_FMT_FP8;

@@ -430,12 +430,20 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan = DecodePlan();
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
-    // the tensor-core kernel unless the caller asks for CUDA cores; below 8 heads the
-    // 32-head MMA tile would be mostly padding
-    // (uniform 3- and 6-bit problems: the CUDA-core kernel, the only one that reads them)
-    plan.tc = p.impl == 2 || (p.impl == 0 && p.n_heads >= 8 && !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
+    // The library's choice (impl 0), by measurement on GB300: fp8 problems of at most 16
+    // heads, or with a top-k index list, run on the warp-level MMA kernel (16 heads a CTA,
+    // each code converted once); other problems of 8 or more heads on the tcgen05 kernel
+    // (32 heads a CTA), below that the CUDA-core kernel; uniform 3- and 6-bit problems on
+    // the CUDA-core kernel, the only one that reads them.
+    const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
+    plan.mma = p.impl == 3 || (p.impl == 0 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
+    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.mma && p.n_heads >= 8 &&
+                              !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
     int64_t split_rows = p.split_rows;
-    if (plan.tc) {
+    if (plan.mma) {
+        plan.head_block = mma_head_block();
+        if (split_rows <= 0) plan_mma_splits(p, n_cand, split_rows);
+    } else if (plan.tc) {
         constexpr int kTile = 128, kHeadsTc = 32;
         plan.head_block = kHeadsTc;
         const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeadsTc - 1) / kHeadsTc));
@@ -497,9 +505,14 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.status = dev_status;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
-    if (any_tq4 && !plan.tc) {
+    if (any_tq4 && !plan.tc && !plan.mma) {
         int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
+    }
+    if (plan.mma) {
+        cudaError_t e = launch_mla_decode_mma(p, plan, a.part_ml, a.part_o, dev_status, s);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
     }
     if (plan.tc) {
         cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,

@@ -162,7 +162,8 @@ cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
 
 struct DecodePlan {
-    bool tc = false;        // tensor-core kernel
+    bool tc = false;        // tensor-core (tcgen05) kernel
+    bool mma = false;       // warp-level MMA kernel (blocks of 16 heads)
     int split_rows = 0;     // candidate rows per split
     int n_splits = 0;       // splits per (seq, query) at most
     int n_cand_max = 0;     // candidate rows of the longest (seq, query)
@@ -176,6 +177,12 @@ size_t tc_q_image_bytes(const kvq_mla_problem& p);
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s);
+
+// the warp-level MMA decode (kvq_decode_mma.cu)
+int mma_head_block();
+void plan_mma_splits(const kvq_mla_problem& p, int64_t n_cand, int64_t& split_rows);
+cudaError_t launch_mla_decode_mma(const kvq_mla_problem& p, const DecodePlan& plan, float* part_ml,
+                                  float* part_o, uint32_t* dev_status, cudaStream_t s);
 
 struct Q4Plan {
     int split_rows = 0;     // positions per split

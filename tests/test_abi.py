@@ -92,14 +92,15 @@ def test_decode_argument_errors(kvq):
     dec = lambda p, ws=None, n=0: L.kvq_mla_decode(C.byref(p), FAKE, None, ws, n, None, None)
     assert dec(_problem(kvq, d_lat=256)) == 1
     assert dec(_problem(kvq, fmt=7)) == 3
-    # 3- and 6-bit rotated rows: the CUDA-core kernel; the tensor-core one refuses them
+    # 3- and 6-bit rotated rows: the CUDA-core kernel; the tensor-core ones refuse them
     for fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6):
         assert dec(_problem(kvq, fmt=fmt)) == 5                                  # workspace next
         assert dec(_problem(kvq, fmt=fmt, impl=2)) == 3
+        assert dec(_problem(kvq, fmt=fmt, impl=3)) == 3
     assert dec(_problem(kvq, tq4_signs=None)) == 1
     assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
     assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1
-    assert dec(_problem(kvq, impl=3)) == 1                                       # 0, 1 or 2 only
+    assert dec(_problem(kvq, impl=4)) == 1                                       # 0 .. 3 only
     assert dec(_problem(kvq, impl=-1)) == 1
     p = _problem(kvq)
     need = L.kvq_mla_decode_workspace(C.byref(p))

@@ -12,7 +12,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-IMPLS = pytest.mark.parametrize("impl", [1, 2], ids=["cudacore", "tcgen05"])
+IMPLS = pytest.mark.parametrize("impl", [1, 2, 3], ids=["cudacore", "tcgen05", "mma"])
 
 
 @pytest.fixture(scope="module")
@@ -197,6 +197,63 @@ def test_decode_ragged_workload(kvq, orc, impl):
                                      heads=(0, 8))
     assert st == 0
     check(out[sel][:, :, :8], lse[sel][:, :, :8], ref[sel][:, :, :8], ref_lse[sel][:, :, :8])
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@IMPLS
+def test_decode_partial_head_block_multi_tile(kvq, orc, impl, fmt):
+    """H=20 (one full block of 16 heads and one of 4), 2 causal queries, splits of 640
+    rows (5 tiles of 128, so the staging ring wraps) over T=2900 (a ragged last tile)."""
+    T = 2900
+    rows = W.magnitude_rows(T, seed=40 + fmt, lo=1e-2, hi=10.0)
+    signs = W.sign_bits(40)
+    cache = encode(orc, rows, fmt, signs)
+    q = W.queries(1, 2, 20, seed=40)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
+                           signs=signs, causal=True, split_rows=640)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, causal=True, **kw)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@IMPLS
+def test_decode_sixteen_heads_long(kvq, orc, impl, fmt):
+    """T=131072 rows, H=16, one query: the HBM-bound decode points, library splits."""
+    T = 131072
+    rows = W.unit_rows(T, seed=50)
+    signs = W.sign_bits(50)
+    cache = encode(orc, rows, fmt, signs)
+    q = W.queries(1, 1, 16, seed=50)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
+                           signs=signs)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, **kw)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+@IMPLS
+def test_decode_rows_past_the_pool(kvq, orc, impl, fmt):
+    """A contiguous cache whose pool ends inside the sequence (300 rows, seq_len 500): the
+    rows past the pool are skipped and flagged as bad pages, so the result is the
+    attention over the 300 rows that exist."""
+    T, L = 300, 500
+    rows = W.unit_rows(T, seed=45 + fmt)
+    signs = W.sign_bits(45)
+    cache = encode(orc, rows, fmt, signs)
+    q = W.queries(1, 1, 16, seed=45)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=fmt, caches={fmt: cache}, seq_len=[L], q=q,
+                           signs=signs)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, **kw)
+    assert st & kvq.DEV_BAD_PAGE
+    check(out, lse, ref, ref_lse)
 
 
 @IMPLS

@@ -121,7 +121,7 @@ def test_decode_paged_causal_multi_query(kvq, orc, bits):
 
 def test_mixed_batch_tensor_core_flags_six_bit_sequences(kvq, orc):
     """A seq_fmt batch of an fp8 and a 6-bit sequence: the CUDA-core kernel reads both;
-    the tensor-core kernel reads the fp8 one and flags the other (out 0, lse -inf)."""
+    the two tensor-core kernels read the fp8 one and flag the other (out 0, lse -inf)."""
     T = 300
     rows = W.unit_rows(2 * T, seed=70)                     # sequence i: pool rows i*T ..
     signs = W.sign_bits(70)
@@ -137,10 +137,11 @@ def test_mixed_batch_tensor_core_flags_six_bit_sequences(kvq, orc):
     out, lse, st = run_gpu(kvq, impl=1, **kw)
     assert st == 0
     check(out, lse, ref, ref_lse)
-    out2, lse2, st2 = run_gpu(kvq, impl=2, **kw)
-    assert st2 & kvq.DEV_BAD_FORMAT
-    check(out2[:1], lse2[:1], ref[:1], ref_lse[:1])
-    assert np.all(out2[1] == 0) and np.all(np.isneginf(lse2[1]))
+    for impl in (2, 3):
+        out2, lse2, st2 = run_gpu(kvq, impl=impl, **kw)
+        assert st2 & kvq.DEV_BAD_FORMAT
+        check(out2[:1], lse2[:1], ref[:1], ref_lse[:1])
+        assert np.all(out2[1] == 0) and np.all(np.isneginf(lse2[1]))
 
 
 @pytest.mark.parametrize("bits", [3, 6])
