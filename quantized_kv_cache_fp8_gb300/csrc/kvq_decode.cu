@@ -310,10 +310,104 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 }
 
 // ------------------------------------------------------------------------------------
-// Log-sum-exp combine (+ TQ4 unrotation): one CTA of 128 threads per (seq, query, head).
+// Log-sum-exp combine (+ TQ4 unrotation), grid (row, quarter) of 512-thread CTAs, row =
+// (seq, query, head):
 //   M = max_S m_S,  L = sum_S l_S 2^(m_S - M),  out = sum_S o_S 2^(m_S - M) / L,
 //   lse = (M + log2 L) ln 2;  TQ4: out <- (1/sqrt 512) s (.) FWHT_512(out).
+// With more than 64 splits a row (one CTA, 64 splits in flight) takes several dependent
+// batches; then the grid has four quarters per row, and a row not in a rotated tier is
+// split into four CTAs of 128 dims whose 16 split groups keep up to 192 splits' partials
+// in flight at once.  A row of a rotated tier needs all 512 dims for the unrotation:
+// quarter 0 does the whole row.
 // ------------------------------------------------------------------------------------
+__device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, int quarter, int ns)
+{
+    constexpr int kGroups = 16, kPer = 12, kBatch = kGroups * kPer;
+    __shared__ float s_w[kBatch];
+    __shared__ __align__(16) float4 s_acc[kGroups][32];
+    __shared__ float s_red[2][16];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid >> 5, j = tid & 31;       // split group, float4 column of the quarter
+    const float* ml = a.part_ml + r * a.n_splits * 2;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o + r * a.n_splits * kDLat + quarter * 128) + j;
+    // the partials come from the decode kernel launched just before this one
+    grid_dependency_wait();
+    // the first batch is requested before the maxima are known; splits with l = 0 (no
+    // admissible row) may hold stale values and get weight 0 below
+    float4 v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int S = grp + kGroups * i;
+        v[i] = S < ns ? po[(int64_t)S * (kDLat / 4)] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    float M = -INFINITY;
+    for (int S = tid; S < ns; S += 512) {
+        const float2 x = reinterpret_cast<const float2*>(ml)[S];
+        if (x.y > 0.0f) M = fmaxf(M, x.x);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0) s_red[0][warp] = M;
+    __syncthreads();
+    M = s_red[0][0];
+#pragma unroll
+    for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float Lpart = 0.0f;
+    for (int S0 = 0; S0 < ns; S0 += kBatch) {
+        const int nb = min(kBatch, ns - S0);
+        if (S0 > 0) {
+            __syncthreads();                      // s_w of the previous batch is consumed
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int S = grp + kGroups * i;
+                v[i] = S < nb ? po[(int64_t)(S0 + S) * (kDLat / 4)] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+        }
+        if (tid < nb) {
+            const float2 x = reinterpret_cast<const float2*>(ml)[S0 + tid];
+            const float w = x.y > 0.0f ? exp2f(x.x - M) : 0.0f;
+            s_w[tid] = w;
+            Lpart += w > 0.0f ? x.y * w : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int S = grp + kGroups * i;
+            const float w = S < nb ? s_w[S] : 0.0f;
+            if (w != 0.0f) {
+                acc.x = fmaf(v[i].x, w, acc.x);
+                acc.y = fmaf(v[i].y, w, acc.y);
+                acc.z = fmaf(v[i].z, w, acc.z);
+                acc.w = fmaf(v[i].w, w, acc.w);
+            }
+        }
+    }
+    s_acc[grp][j] = acc;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) Lpart += __shfl_xor_sync(kFull, Lpart, o);
+    if (lane == 0) s_red[1][warp] = Lpart;
+    __syncthreads();
+    if (tid >= 32) return;
+    float Lt = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) Lt += s_red[1][w];
+    const bool empty = !(Lt > 0.0f);
+    float4 res = s_acc[0][j];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) {
+        const float4 x = s_acc[g][j];
+        res.x += x.x;
+        res.y += x.y;
+        res.z += x.z;
+        res.w += x.w;
+    }
+    res = empty ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                : make_float4(res.x / Lt, res.y / Lt, res.z / Lt, res.w / Lt);
+    reinterpret_cast<float4*>(a.out + r * kDLat + quarter * 128)[j] = res;
+    if (quarter == 0 && tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+}
+
 __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 {
     constexpr int kBatch = 64;                    // splits whose partials load at once
@@ -329,6 +423,11 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     const int fmt = seq_format(p, s);
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
     const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
+    if (gridDim.y == 4 && !rotated_format(fmt)) {
+        combine_quarter(a, r, blockIdx.y, ns);
+        return;
+    }
+    if (blockIdx.y != 0) return;                  // a rotated row: quarter 0 does it all
     const float* ml = a.part_ml + r * a.n_splits * 2;
     const float4* po = reinterpret_cast<const float4*>(a.part_o + r * a.n_splits * kDLat) + j;
     // the partials come from the decode kernel launched just before this one
@@ -423,6 +522,11 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+dim3 combine_grid(int64_t rows, const DecodePlan& plan)
+{
+    return dim3((unsigned)rows, plan.n_splits > 64 ? 4 : 1);
+}
+
 }  // namespace
 
 bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
@@ -512,13 +616,13 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     if (plan.mma) {
         cudaError_t e = launch_mla_decode_mma(p, plan, a.part_ml, a.part_o, dev_status, s);
         if (e != cudaSuccess) return e;
-        return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
+        return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }
     if (plan.tc) {
         cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,
                                              a.part_o, dev_status, s);
         if (e != cudaSuccess) return e;
-        return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
+        return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }
     const size_t smem = (size_t)(kGH * kLDT + kRT * kLDT + kRT * kGH + kGH) * sizeof(float)
                         + kRT * sizeof(int) + 64 * sizeof(float);
@@ -535,7 +639,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hblk);
     mla_decode_simt_kernel<<<grid, kThreads, smem, s>>>(a);
-    return launch_dependent(mla_combine_kernel, dim3((unsigned)rows), dim3(512), 0, s, a);
+    return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
 }
 
 }  // namespace kvq
