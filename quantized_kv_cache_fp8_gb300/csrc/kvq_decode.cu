@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 // (seq, query, head):
 //   M = max_S m_S,  L = sum_S l_S 2^(m_S - M),  out = sum_S o_S 2^(m_S - M) / L,
 //   lse = (M + log2 L) ln 2;  TQ4: out <- (1/sqrt 512) s (.) FWHT_512(out).
-// With more than 64 splits a row (one CTA, 64 splits in flight) takes several dependent
+// With more than 80 splits a row (one CTA, 80 splits in flight) takes several dependent
 // batches; then the grid has four quarters per row, and a row not in a rotated tier is
 // split into four CTAs of 128 dims whose 16 split groups keep up to 192 splits' partials
 // in flight at once.  A row of a rotated tier needs all 512 dims for the unrotation:
@@ -410,7 +410,7 @@ __device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, 
 
 __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 {
-    constexpr int kBatch = 64;                    // splits whose partials load at once
+    constexpr int kBatch = 80;                    // splits whose partials load at once
     __shared__ float s_w[kBatch];
     __shared__ __align__(16) float s_part[4][kDLat];
     __shared__ float s_red[2][16];
@@ -524,7 +524,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 dim3 combine_grid(int64_t rows, const DecodePlan& plan)
 {
-    return dim3((unsigned)rows, plan.n_splits > 64 ? 4 : 1);
+    return dim3((unsigned)rows, plan.n_splits > 80 ? 4 : 1);
 }
 
 }  // namespace

@@ -90,6 +90,7 @@ constexpr int kSmemBytes = kOffGroups + 2 * kGroupBytes;
 static_assert(kGOffStage % 16 == 0 && kGroupBytes % 16 == 0 && stage_bytes<Fp8Rows>() % 16 == 0 &&
               stage_bytes<Tq4Rows>() % 16 == 0, "16-byte alignment of the staged rows");
 static_assert(kH * kDLat * 4 <= kStageArea, "a group's output fits in its staging ring");
+static_assert(kH * (kDLat + kDRope + 4) * 4 <= kGOffStage, "the staged query fits before group 0's ring");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // Row of column n inside an 8-row n-tile.  With this order the four rows that one
@@ -267,43 +268,52 @@ __device__ __forceinline__ int64_t candidate_row(const kvq_mla_problem& p, const
 // column kap of block ks holds dim 64 kk + 16 (kap % 8 / 2) + 4 e + kap % 2 + 2 (kap / 8),
 // the order in which a thread's 4-byte code word feeds its B fragment.  Head h's 32-byte
 // row stores its two 16-byte halves swapped when bit 2 of h is set.
-__device__ __forceinline__ int q_image_offset(int h, int d)
-{
-    const int kk = d < kDLat ? d >> 6 : 8;
-    const int rr = d & 63;
-    const int lo2 = rr & 3;
-    const int kap = 2 * (rr >> 4) + (lo2 & 1) + 8 * (lo2 >> 1);
-    const int ks = 4 * kk + ((rr >> 2) & 3);
-    return ks * 1024 + h * 32 + (((kap >> 3) ^ ((h >> 2) & 1)) << 4) + (kap & 7) * 2;
-}
-
+//
 // The query image of (sequence, query) row sq, heads h0 .. h0 + nh - 1, built into
-// shared memory by the CTA: warp w builds heads w and w + 8.  Rotated sequences use
-// rot(q) = (1/sqrt 512) FWHT_512(s (.) q), computed here in fp32.
-__device__ __forceinline__ void build_q_image(uint8_t* s_q, const kvq_mla_problem& p, int64_t sq, int h0,
-                                              int nh, bool rotated)
+// shared memory by the CTA in two steps.  (1) Warp w stages heads w and w + 8 (rotated
+// sequences: rot(q) = (1/sqrt 512) FWHT_512(s (.) q), in fp32 registers) into an fp32
+// copy [16 heads][kQStageLd].  (2) Thread i of item list (k-step, head, column
+// pair) writes one 4-byte hi pair and one lo pair of the image: a warp covers 128
+// contiguous bytes of one k-step block, free of bank conflicts.
+constexpr int kQStageLd = kDLat + kDRope + 4;            // floats per staged head
+
+// This warp's two heads of the query (w and w + 8; zeros past nh) and the rotation signs
+// of its lanes, requested at the start of the kernel so that their latency overlaps the
+// first tile loads.
+struct QRegs {
+    float y[2][16];
+    float2 r2[2];
+    uint32_t signs[16];
+};
+
+__device__ __forceinline__ void load_q(QRegs& q, const kvq_mla_problem& p, int64_t sq, int h0, int nh,
+                                       bool rotated)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t neg = 0;                                // rotation signs of elements j * 32 + lane
-    if (rotated) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) neg |= ((p.tq4_signs[j] >> lane) & 1u) << j;
+    for (int j = 0; j < 16; ++j) q.signs[j] = rotated ? p.tq4_signs[j] : 0u;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int h = warp + 8 * hh;
+        const bool ok = h < nh;
+        const int64_t r = sq * p.n_heads + h0 + (ok ? h : 0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q.y[hh][j] = ok ? p.q_lat[r * kDLat + j * 32 + lane] : 0.0f;
+        q.r2[hh] = ok ? reinterpret_cast<const float2*>(p.q_rope + r * kDRope)[lane] : make_float2(0.0f, 0.0f);
     }
+}
+
+__device__ __forceinline__ void build_q_image(uint8_t* s_q, float* s_stage_q, QRegs& q, bool rotated)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t neg = 0;                                // rotation signs of elements j * 32 + lane
+#pragma unroll
+    for (int j = 0; j < 16; ++j) neg |= ((q.signs[j] >> lane) & 1u) << j;
     const float c512 = tq4_inv_sqrt(kDLat);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int h = warp + 8 * hh;
-        float y[16], r2[2] = {0.0f, 0.0f};
-        if (h < nh) {
-            const int64_t r = sq * p.n_heads + h0 + h;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = p.q_lat[r * kDLat + j * 32 + lane];
-            r2[0] = p.q_rope[r * kDRope + 2 * lane];
-            r2[1] = p.q_rope[r * kDRope + 2 * lane + 1];
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = 0.0f;
-        }
+        float (&y)[16] = q.y[hh];
         if (rotated) {                               // CTA-uniform
 #pragma unroll
             for (int j = 0; j < 16; ++j) y[j] = ((neg >> j) & 1u) ? -y[j] : y[j];
@@ -311,16 +321,27 @@ __device__ __forceinline__ void build_q_image(uint8_t* s_q, const kvq_mla_proble
 #pragma unroll
             for (int j = 0; j < 16; ++j) y[j] *= c512;
         }
+        float* row = s_stage_q + h * kQStageLd;
 #pragma unroll
-        for (int j = 0; j < 18; ++j) {
-            const float v = j < 16 ? y[j] : r2[j - 16];
-            const int d = j < 16 ? j * 32 + lane : kDLat + 2 * lane + (j - 16);
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
-            const int off = q_image_offset(h, d);
-            *reinterpret_cast<__half*>(s_q + off) = hi;
-            *reinterpret_cast<__half*>(s_q + off + 512) = lo;
-        }
+        for (int j = 0; j < 16; ++j) row[j * 32 + lane] = y[j];
+        reinterpret_cast<float2*>(row + kDLat)[lane] = q.r2[hh];
+    }
+    __syncthreads();
+    // item i: column pair m = i % 8 (columns 2m, 2m + 1), head (i / 8) % 16, k-step i / 128
+    constexpr int kItems = kKSteps * kH * 8;
+    static_assert(kItems % kThreads == 0, "image items per thread");
+#pragma unroll 2
+    for (int i = tid; i < kItems; i += kThreads) {
+        const int m = i & 7, h = (i >> 3) & 15, ks = i >> 7;
+        // column 2m of k-step ks = 4 kk + e is dim 64 kk + 16 (m % 4) + 4 e + 2 (m / 4)
+        const int d0 = 64 * (ks >> 2) + 16 * (m & 3) + 4 * (ks & 3) + 2 * (m >> 2);
+        const float2 v = *reinterpret_cast<const float2*>(s_stage_q + h * kQStageLd + d0);
+        const __half2 hi = __floats2half2_rn(v.x, v.y);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(v.x - hf.x, v.y - hf.y);
+        const int off = ks * 1024 + h * 32 + (((m >> 2) ^ ((h >> 2) & 1)) << 4) + 4 * (m & 3);
+        *reinterpret_cast<__half2*>(s_q + off) = hi;
+        *reinterpret_cast<__half2*>(s_q + off + 512) = lo;
     }
 }
 
@@ -411,14 +432,17 @@ __device__ __forceinline__ void decode_split(const MmaArgs& a, uint8_t* smem, co
         }
     };
 
-    // ---- the first tiles, then (while they load) the query image
+    // ---- the query's loads, the first tiles, then (while they land) the query image
+    QRegs qr;
+    load_q(qr, p, (int64_t)sp.s * p.n_q + sp.q, sp.h0, sp.nh, !R::kFp8);
 #pragma unroll
     for (int k = 0; k < kS - 1; ++k) {
         if (k < my_tiles) issue(k);
         cp_async_commit();
     }
     grid_dependents_launch();                      // the combine may launch; it waits for us
-    build_q_image(s_q, p, (int64_t)sp.s * p.n_q + sp.q, sp.h0, sp.nh, !R::kFp8);
+    // staging: group 0's fp16 tile and swap area, unused until its first score
+    build_q_image(s_q, reinterpret_cast<float*>(smem + kOffGroups), qr, !R::kFp8);
     __syncthreads();                               // the query image is complete
 
     // this lane's ldmatrix row: matrix lane / 8 = (heads 0-7 | 8-15) x (columns 0-7 | 8-15)
