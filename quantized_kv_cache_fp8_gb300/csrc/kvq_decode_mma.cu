@@ -34,6 +34,9 @@
 //    w = p * scale(row) goes to shared memory as fp16 hi | lo;
 //  * context O[16 x 512] += W[16 x 32] C: warp q owns output dims 128 q .. 128 q + 127;
 //    B comes from the fp16 tile by transposing matrix loads, A = W hi, then W lo.
+// The CTA requests its query before its first tiles and builds the query image (fp16 hi
+// | lo, rotated in fp32 for TQ4) while they land; it lets the combine launch early
+// (programmatic dependent launch; the combine waits for this grid).
 // The split-fp16 operands keep the products exact to ~2^-22 relative, which the 1e-4
 // tolerance needs; the codes themselves are exact in fp16.
 //
