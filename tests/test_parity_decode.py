@@ -257,6 +257,25 @@ def test_decode_rows_past_the_pool(kvq, orc, impl, fmt):
 
 
 @IMPLS
+def test_decode_mixed_tiers_many_splits(kvq, orc, impl):
+    """A seq_fmt batch of an fp8 and a TQ4 sequence (T=3000 each) in splits of 32 rows:
+    94 splits, so the combine runs in its four-quarter grid, the fp8 rows summed by
+    four 128-dim CTAs and the TQ4 rows (unrotated over all 512 dims) by one."""
+    T = 3000
+    rows = W.magnitude_rows(2 * T, seed=48, lo=1e-2, hi=10.0)    # sequence i: pool rows i*T ..
+    signs = W.sign_bits(48)
+    caches = {1: encode(orc, rows, 1), 2: encode(orc, rows, 2, signs)}
+    q = W.queries(2, 1, 8, seed=48)
+    kw = dict(seq_len=[T, T], q=q, signs=signs, seq_fmt=[1, 2], seq_stride_rows=T, split_rows=32)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches=caches, **kw)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T, T], seq_fmt=[1, 2], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, seq_stride_rows=T, fp8=caches[1],
+                                     tq4=caches[2], signs=signs)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@IMPLS
 def test_decode_bad_index_and_sparse_causal(kvq, orc, impl):
     T, NQ = 500, 3
     rows = W.unit_rows(T, seed=9)
