@@ -338,6 +338,22 @@ def q4_decode(*, seq_len, page_table, page_size, n_cells, k_pool, v_pool, q, n_k
 
 # --- MLA decode -----------------------------------------------------------------------
 
+def mla_abs_terms(*, lat_rows, rope_rows, q_lat, q_rope, sm_scale):
+    """The sum of the absolute values of the terms of each output element of one
+    sequence's decode (colibri PR #399: out = sum_t softmax(s)_t c_t), the denominator of
+    the Σ|terms|-relative error: A[q][h][d] = sum_t p_t |c_{t,d}|, with p the softmax of
+    s_t = sm_scale (q_lat . c_t + q_rope . k_rope_t), in fp64 over the dequantized rows
+    lat_rows [T][512] and rope_rows [T][64] (every row admissible).  |out_d| <= A_d,
+    with equality when every c_{t,d} >= 0."""
+    lat = np.asarray(lat_rows, np.float64)
+    rope = np.asarray(rope_rows, np.float64)
+    tau = float(np.float32(sm_scale))
+    s = tau * (np.asarray(q_lat, np.float64) @ lat.T + np.asarray(q_rope, np.float64) @ rope.T)
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    return p @ np.abs(lat)
+
+
 def mla_decode(*, seq_len, seq_fmt, q_lat, q_rope, sm_scale, causal=False,
                block_table=None, page_size=0, seq_stride_rows=0,
                fp8=None, tq4=None, signs=None, idx=None, n_split=0,

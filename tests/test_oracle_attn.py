@@ -178,3 +178,49 @@ def test_tolerance_discriminates(orc):
             assert err.max() > 100 * bar.max()
             if every:
                 assert np.all(err > 100 * bar)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_abs_terms_bounds_and_equality(orc, fmt):
+    """The Σ|terms| denominator: it bounds |out| element-wise, equals out exactly when
+    every latent value is non-negative, and is |c_0| for one row."""
+    T = 300
+    rows = W.magnitude_rows(T, seed=31 + fmt, lo=0.1, hi=5.0)
+    signs = W.sign_bits(31)
+    q = W.queries(1, 2, 4, seed=31)
+    for positive in (False, True):
+        if positive:
+            rows.c = np.abs(rows.c)
+            if fmt == 2:                       # a rotated row's decode has mixed signs:
+                continue                       # the equality case is the fp8 one
+        cache = _fp8_cache(orc, rows) if fmt == 1 else _tq4_cache(orc, rows, signs)
+        kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+        out, _, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                                   sm_scale=TAU, **kw)
+        c, kr = _dense_rows(orc, cache, fmt, signs)
+        A = orc.mla_abs_terms(lat_rows=c, rope_rows=kr, q_lat=q.q_lat[0], q_rope=q.q_rope[0],
+                              sm_scale=TAU)
+        assert np.all(np.abs(out[0]) <= A * (1 + 1e-12) + 1e-300)
+        if positive:
+            assert np.allclose(A, out[0], rtol=1e-12, atol=0)
+    c1 = c[:1]
+    A1 = orc.mla_abs_terms(lat_rows=c1, rope_rows=kr[:1], q_lat=q.q_lat[0], q_rope=q.q_rope[0],
+                           sm_scale=TAU)
+    assert np.array_equal(A1, np.broadcast_to(np.abs(c1[0]), A1.shape))
+
+
+def test_abs_terms_brute_force(orc):
+    """Against a termwise expansion of sum_t p_t |c_t| on a tiny case."""
+    T = 5
+    rows = W.magnitude_rows(T, seed=33, lo=0.5, hi=2.0)
+    cache = _fp8_cache(orc, rows)
+    c, kr = _dense_rows(orc, cache, 1)
+    q = W.queries(1, 1, 2, seed=33)
+    A = orc.mla_abs_terms(lat_rows=c, rope_rows=kr, q_lat=q.q_lat[0], q_rope=q.q_rope[0], sm_scale=TAU)
+    for h in range(2):
+        s = [TAU * (sum(float(q.q_lat[0, 0, h, i]) * c[t, i] for i in range(512))
+                    + sum(float(q.q_rope[0, 0, h, i]) * kr[t, i] for i in range(64))) for t in range(T)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        ref = sum(e[t] * np.abs(c[t]) for t in range(T)) / sum(e)
+        assert np.allclose(A[0, h], ref, rtol=1e-12, atol=0)

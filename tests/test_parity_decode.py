@@ -275,6 +275,40 @@ def test_decode_mixed_tiers_many_splits(kvq, orc, impl):
     check(out, lse, ref, ref_lse)
 
 
+@pytest.mark.parametrize("fmt", [1, 2])
+@IMPLS
+def test_decode_sum_abs_terms_error(kvq, orc, impl, fmt):
+    """The error of every output element relative to the sum of the absolute values of
+    its terms, sum_t p_t |c_t,d| (the dot-product tolerance form), on the fp8 tiny
+    workload (magnitudes 1e-3..40, zero rows) and on T=4096 N(0,1) rows of the 4-bit
+    tier, H=16.  Measured on GB300: 1.7e-5 to 3.5e-5 (fp8; the fp32 CUDA-core kernel
+    included, so it is the fp32 rounding of logits of magnitude ~10^2, which moves each
+    p_t by ~|s|·2^-23) and 5e-7 to 1.2e-6 (TQ4); the bound is 1e-4."""
+    T = 1024 if fmt == 1 else 4096
+    rows = W.fp8_tiny_rows(T, seed=0) if fmt == 1 else W.unit_rows(T, seed=0)
+    signs = W.sign_bits(0)
+    cache = encode(orc, rows, fmt, signs)
+    q = W.queries(1, 1, 16, seed=0)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=fmt, caches={fmt: cache}, seq_len=[T], q=q,
+                           signs=signs)
+    kw = dict(fp8=cache) if fmt == 1 else dict(tq4=cache, signs=signs)
+    ref, _, _ = orc.mla_decode(seq_len=[T], seq_fmt=[fmt], q_lat=q.q_lat, q_rope=q.q_rope,
+                               sm_scale=W.SM_SCALE, **kw)
+    if fmt == 1:
+        c = orc.decode_fp8(cache["lat"], cache["lat_scale"])
+    else:
+        c, _ = orc.decode_tq4(cache["lat"], cache["lat_scale"], signs, 512)
+    kr = orc.decode_fp8(cache["rope"], cache["rope_scale"])
+    A = orc.mla_abs_terms(lat_rows=c, rope_rows=kr, q_lat=q.q_lat[0], q_rope=q.q_rope[0],
+                          sm_scale=W.SM_SCALE)
+    err = np.abs(out[0] - ref[0])
+    nz = A > 0
+    assert st == 0 and np.all(err[~nz] == 0)
+    worst = float((err[nz] / A[nz]).max())
+    print(f"sum|terms|-relative error, fmt {fmt}, impl {impl}: {worst:.3e}")
+    assert worst <= 1e-4
+
+
 @IMPLS
 def test_decode_bad_index_and_sparse_causal(kvq, orc, impl):
     T, NQ = 500, 3
