@@ -87,17 +87,21 @@ __host__ __device__ constexpr int rotated_bits(int fmt)
 // Walsh-Hadamard butterflies over a warp-distributed row: element i = k * 32 + lane,
 // VPL registers per lane.  Stages run in the order h = 1, 2, ..., 32 * VPL / 2: the
 // five lane stages (shuffles) first, then the register stages.  Each butterfly is
-// (a, b) -> (a + b, a - b) in fp32.
+// (a, b) -> (a + b, a - b) in fp32.  A lane stage computes its half as one fused
+// multiply-add with a +-1 multiplier, fma(s, own, partner): the product is exact, so the
+// single rounding gives the same bits as the add or subtract, with no lane-dependent
+// branch.
 // ------------------------------------------------------------------------------------
 template <int VPL>
 __device__ __forceinline__ void fwht_warp(float (&y)[VPL], int lane)
 {
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
+        const float sgn = (lane & m) ? -1.0f : 1.0f;   // upper lane: partner - own
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const float p = __shfl_xor_sync(0xffffffffu, y[k], m);
-            y[k] = (lane & m) ? __fsub_rn(p, y[k]) : __fadd_rn(y[k], p);
+            y[k] = __fmaf_rn(sgn, y[k], p);
         }
     }
 #pragma unroll
