@@ -286,7 +286,7 @@ int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* works
                    size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream);
 
 /*
- * kvq_mla_decode without a workspace argument.  The paper has no counterpart: this is a
+ * kvq_mla_decode without a workspace argument.  The pages have no counterpart: this is a
  * convenience of the library for callers that cannot allocate device memory when they
  * decode, such as code running inside a memory pool or custom allocator that owns the
  * whole device, a latency-critical loop that must not enter the allocator, or an
