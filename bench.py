@@ -606,8 +606,9 @@ def run_decode_configs(args, local):
         assert torch.isfinite(out).all()
         gbs = rows_read * row_bytes / sec / 1e9
         tf = flops / sec / 1e12
+        kernel = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma"}[kvq.kvq_mla_decode_kernel(p)]
         print(json.dumps({"suite": "decode-configs", "config": name, "decode_impl": args.decode_impl,
-                          "us": round(sec * 1e6, 2),
+                          "kernel": kernel, "us": round(sec * 1e6, 2),
                           "kv_rows_per_s": rows_read / sec,
                           "hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm_peak,
                                   "frac": round(gbs / hbm_peak, 4), "bytes": rows_read * row_bytes},

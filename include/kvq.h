@@ -277,6 +277,16 @@ typedef struct kvq_mla_problem {
 size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
 
 /*
+ * The decode kernel kvq_mla_decode runs for this problem: 1 the CUDA-core kernel, 2 the
+ * tcgen05 kernel, 3 the warp-level MMA kernel; `impl` when it is non-zero, else the
+ * library's choice (fp8 problems of at most 16 heads or with a top-k list: 3; other
+ * problems of 8 or more heads: 2, except the 3- and 6-bit tiers; the rest: 1).  Host
+ * only, nothing enqueued.  An invalid problem returns the negated status
+ * kvq_mla_decode would return (-KVQ_EINVAL, -KVQ_EFORMAT, -KVQ_EALIGN).
+ */
+int kvq_mla_decode_kernel(const kvq_mla_problem* p);
+
+/*
  *   out        device fp32 [n_seq][n_q][n_heads][512]
  *   lse        device fp32 [n_seq][n_q][n_heads] or NULL (natural log)
  *   workspace  device, >= kvq_mla_decode_workspace(p) bytes, 256-byte aligned

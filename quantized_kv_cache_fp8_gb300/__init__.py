@@ -16,7 +16,8 @@ import threading
 __all__ = [
     "KvqError", "lib", "kvq_version", "kvq_tq4_codebook", "kvq_set_fault",
     "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
-    "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "MlaCache",
+    "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "kvq_mla_decode_kernel",
+    "MlaCache",
     "MlaProblem", "Q4Problem", "make_q4_problem", "kvq_q4_decode", "kvq_q4_decode_workspace",
     "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "FMT_TQ6", "FMT_TQ3", "TQ_FMT", "kvq_encode_tq",
     "kvq_tq_codebook", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
@@ -28,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 
 FMT_FP8, FMT_TQ4, FMT_Q4_0, FMT_TQ6, FMT_TQ3 = 1, 2, 3, 4, 5
 TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code width
-IMPL_AUTO, IMPL_SIMT, IMPL_TC = 0, 1, 2
+IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_MMA = 0, 1, 2, 3
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
           5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED", 8: "KVQ_EMISMATCH",
@@ -38,7 +39,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_tq4_codebook", "kvq_tq_codebook", "kvq_encode_fp8", "kvq_encode_tq4",
            "kvq_encode_tq", "kvq_append_q4",
-           "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode",
+           "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode_kernel", "kvq_mla_decode",
            "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode",
            "kvq_cache_probe", "kvq_cache_save", "kvq_cache_save_f32", "kvq_cache_append",
            "kvq_cache_load_workspace", "kvq_cache_load"]
@@ -134,6 +135,8 @@ def _declare(L):
     L.kvq_gather.argtypes = [C.POINTER(GatherDesc), _p]
     L.kvq_mla_decode_workspace.restype = C.c_size_t
     L.kvq_mla_decode_workspace.argtypes = [C.POINTER(MlaProblem)]
+    L.kvq_mla_decode_kernel.restype = C.c_int
+    L.kvq_mla_decode_kernel.argtypes = [C.POINTER(MlaProblem)]
     L.kvq_mla_decode.restype = C.c_int
     L.kvq_mla_decode.argtypes = [C.POINTER(MlaProblem), _p, _p, _p, C.c_size_t, _p, _p]
     L.kvq_mla_decode_noalloc.restype = C.c_int
@@ -291,6 +294,14 @@ def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, 
 
 def kvq_mla_decode_workspace(p: MlaProblem) -> int:
     return lib().kvq_mla_decode_workspace(C.byref(p))
+
+
+def kvq_mla_decode_kernel(p: MlaProblem) -> int:
+    """The kernel kvq_mla_decode runs for p: IMPL_SIMT, IMPL_TC or IMPL_MMA."""
+    r = lib().kvq_mla_decode_kernel(C.byref(p))
+    if r < 0:
+        _check(-r)
+    return r
 
 
 def kvq_mla_decode(p: MlaProblem, out, lse=None, workspace=None, dev_status=None,

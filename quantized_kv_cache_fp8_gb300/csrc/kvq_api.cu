@@ -278,6 +278,14 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p)
     return plan.bytes;
 }
 
+int kvq_mla_decode_kernel(const kvq_mla_problem* p)
+{
+    if (int st = validate_decode(p, "kvq_mla_decode_kernel")) return -st;
+    kvq::DecodePlan plan;
+    kvq::plan_decode(*p, plan);
+    return plan.mma ? 3 : plan.tc ? 2 : 1;
+}
+
 int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
                    size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream)
 {

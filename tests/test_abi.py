@@ -87,6 +87,29 @@ def _problem(kvq, **kw):
     return p
 
 
+def test_decode_kernel_choice(kvq):
+    """Which kernel kvq_mla_decode runs (host only): fp8 with at most 16 heads or a top-k
+    list on the warp-level MMA kernel, other problems of 8+ heads on tcgen05, the rest
+    (and the 3- and 6-bit tiers) on CUDA cores; an explicit impl wins."""
+    fp8 = dict(fmt=kvq.FMT_FP8, fp8=kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768))
+    k = lambda **kw: kvq.kvq_mla_decode_kernel(_problem(kvq, **kw))
+    assert k(n_heads=16, **fp8) == kvq.IMPL_MMA
+    assert k(n_heads=4, **fp8) == kvq.IMPL_MMA
+    assert k(n_heads=64, **fp8) == kvq.IMPL_TC
+    assert k(n_heads=128, idx=FAKE, top_k=2048, **fp8) == kvq.IMPL_MMA
+    assert k(n_heads=64) == kvq.IMPL_TC                                   # TQ4
+    assert k(n_heads=16) == kvq.IMPL_TC
+    assert k(n_heads=4) == kvq.IMPL_SIMT
+    assert k(n_heads=16, fmt=kvq.FMT_TQ6) == kvq.IMPL_SIMT
+    assert k(n_heads=16, fmt=kvq.FMT_TQ3) == kvq.IMPL_SIMT
+    for impl in (1, 2, 3):
+        assert k(n_heads=16, impl=impl) == impl
+    with pytest.raises(kvq.KvqError) as e:
+        k(fmt=kvq.FMT_TQ6, impl=3)
+    assert e.value.status == 3
+    assert kvq.lib().kvq_mla_decode_kernel(C.byref(_problem(kvq, d_lat=256))) == -1
+
+
 def test_decode_argument_errors(kvq):
     L = kvq.lib()
     dec = lambda p, ws=None, n=0: L.kvq_mla_decode(C.byref(p), FAKE, None, ws, n, None, None)
