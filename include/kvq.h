@@ -106,8 +106,9 @@ int kvq_tq4_codebook(float centroids[16], float thresholds[15]);
 int kvq_tq_codebook(int bits, float* centroids, float* thresholds);
 
 /*
- * fp8 (KV8) per-row encode — colibri PR #399, Summary ("fp8 e4m3 + per-row scale") and
- * Commit 1 ("RNE, per-row amax/448 scale").  For each row r:
+ * fp8 (KV8) per-row encode — colibri PR #399, Summary and Commit 1 (e4m3 codes with one
+ * scale per row, the row's largest magnitude over 448, rounding to nearest even).  For each
+ * row r:
  *     amax = max_i |x[r][i]|,  scales[r] = amax / 448 (IEEE fp32 division),
  *     codes[r][i] = e4m3 nearest-even of (x[r][i] / scales[r]), saturating at +-448;
  * a row with amax = 0 stores scale 0 and all-zero codes.
@@ -192,15 +193,17 @@ typedef struct kvq_mla_cache {
 /*
  * Gather — two modes selected by `format`.
  *
- * KVQ_FMT_Q4_0 (Strata PR #2533, kv_gather_q4 and the qsa decode commit's dequant
- * "(nibble - 8) * f32_from_f16(d)"): for s < n_seq, t < n_tok, h < n_heads,
+ * KVQ_FMT_Q4_0 (Strata PR #2533, kv_gather_q4 and the qsa decode commit, where a block
+ * value is its nibble minus 8 times the fp32 value of the binary16 scale): for s < n_seq,
+ * t < n_tok, h < n_heads,
  *     q4_out[s][t][h][32b + j] = binary16_rne((q_j - 8) * float(d_b))
  * from the pool row of position pos0[s] + t (as in kvq_append_q4), i.e. in the ROTATED
  * domain.  q4_out: device u16 (binary16 bits) [n_seq][n_tok][n_heads][256].  A bad
  * position or page sets KVQ_DEV_BAD_PAGE and that token's rows are left untouched.
  *
- * KVQ_FMT_FP8 / KVQ_FMT_TQ4 / KVQ_FMT_TQ6 / KVQ_FMT_TQ3 (colibri PR #399, Commit 2,
- * "DSA-aware gather"; rows of 512, 256, 384 or 192 code bytes): copies the
+ * KVQ_FMT_FP8 / KVQ_FMT_TQ4 / KVQ_FMT_TQ6 / KVQ_FMT_TQ3 (colibri PR #399, Commit 2: the
+ * gather by absolute row index for DSA-style sparse attention; rows of 512, 256, 384 or
+ * 192 code bytes): copies the
  * n_idx rows idx[j] of the cache `mla_src` (through page_table / page_size when
  * page_table is non-NULL, one sequence) byte for byte into the compact cache dst_*
  * (row j).  An index outside [0, mla_src_rows) sets KVQ_DEV_BAD_INDEX and row j is
@@ -234,7 +237,7 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  *     s_t = sm_scale * (q_lat . c_t + q_rope . k_rope_t),  out = sum_t softmax(s)_t c_t,
  *     lse = log sum_t exp(s_t)
  * over the admissible rows, computed as split-T partials (m, l, o) merged by a
- * log-sum-exp combine (Commit 2, "split-T kernels").  Rows are dequantised inside the
+ * log-sum-exp combine (Commit 2: the kernels that split T).  Rows are dequantised inside the
  * kernel: fp8 c_t = code * scale; the rotated tiers (TQ4, and TQ3 / TQ6 from
  * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
  * the combine unrotates the output).  The two tensor-core kernels read FP8 and TQ4 rows;

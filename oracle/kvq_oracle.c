@@ -110,8 +110,9 @@ double orc_f16_value(uint16_t h)
 }
 
 /* ===================================================================================
- * fp8 (KV8) per-row encode — colibri PR #399, Summary ("fp8 e4m3 + per-row scale")
- * and Commit 1 ("RNE, per-row amax/448 scale", encoder bit-exact with its consumers).
+ * fp8 (KV8) per-row encode — colibri PR #399, Summary and Commit 1: e4m3 codes with
+ * one scale per row (amax / 448), nearest-even rounding, and an encoder whose bytes
+ * every consumer reads identically.
  * Reading: the scale is amax/448 as an IEEE fp32 division, each element is divided
  * by it (fp32 IEEE division) and rounded to e4m3 with ties to even; a row with
  * amax = 0 stores scale 0 and all-zero codes.
@@ -442,8 +443,8 @@ int orc_decode_tq4(const uint8_t* packed, int64_t rows, int dim, int64_t ldp,
 
 /* ===================================================================================
  * q4_0 paged cache — Strata PR #2533, kv_q4.metal port commit: fwht256 with the
- * orthonormal 1/16 scale; q4_group / q4_store with "a tie in |x| resolves to the
- * larger value"; the fp16 scale rounded to nearest even in software; the codeword
+ * orthonormal 1/16 scale; q4_group / q4_store, where of two elements with equal |x|
+ * the larger value wins; the fp16 scale rounded to nearest even in software; the codeword
  * int(fma(x, id, 8.5f)) truncating toward zero.  Fixture commit: an all-zero group
  * gives d = -0.0 (scale bits 0x8000), id = 0, code 8, every qs byte 0x88.
  * =================================================================================== */
@@ -566,8 +567,8 @@ int orc_gather_q4(const uint8_t* pool, int n_seq, const int32_t* pos0, int n_tok
  * and value; the decode kernels compute, per query and head,
  *   s_t = tau * (q_lat . c_t + q_rope . k_rope_t)   over the admissible rows t,
  *   out = sum_t softmax(s)_t c_t,     lse = log sum_t exp(s_t);
- * "split-T kernels" merge per-chunk partial softmax states, and the "DSA-aware gather"
- * restricts the rows to a top-k list of absolute row indices.  Rows are dequantised
+ * kernels that split T merge per-chunk partial softmax states, and the sparse
+ * (DSA-style) gather restricts the rows to a top-k list of absolute row indices.  Rows are dequantised
  * exactly (fp8: code value * scale; TQ4: the fp64 inverse rotation of cb[code] *
  * r / sqrt(n)).  Causal multi-query (draft + verify): query j of a sequence holding L
  * rows sees rows t <= L - n_q + j.

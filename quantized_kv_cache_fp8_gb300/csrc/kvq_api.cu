@@ -286,22 +286,42 @@ int kvq_mla_decode_kernel(const kvq_mla_problem* p)
     return plan.mma ? 3 : plan.tc ? 2 : 1;
 }
 
-int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
-                   size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream)
+}  // extern "C"
+
+int kvq::fault_injected(const char* entry) { return injected(entry); }
+
+int kvq::validate_mla_decode_call(const kvq_mla_problem* p, const float* out, const float* lse,
+                                  const char* E)
 {
-    const char* E = "kvq_mla_decode";
-    if (int st = injected(E)) return st;
     if (int st = validate_decode(p, E)) return st;
     if (p->n_seq == 0) return KVQ_OK;
     if (!out) return fail(KVQ_EINVAL, "%s: NULL out", E);
     if (!aligned(out, 16) || (lse && !aligned(lse, 4))) return fail(KVQ_EALIGN, "%s: out/lse misaligned", E);
+    return KVQ_OK;
+}
+
+int kvq::mla_decode_checked(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
+                            size_t ws_bytes, uint32_t* dev_status, cudaStream_t stream, const char* E)
+{
+    if (int st = validate_mla_decode_call(p, out, lse, E)) return st;
+    if (p->n_seq == 0) return KVQ_OK;
     kvq::DecodePlan plan;
     kvq::plan_decode(*p, plan);
     if (plan.bytes > 0 && (!workspace || ws_bytes < plan.bytes))
         return fail(KVQ_EWORKSPACE, "%s: workspace %zu bytes, need %zu", E, ws_bytes, plan.bytes);
     if (!aligned(workspace, 256)) return fail(KVQ_EALIGN, "%s: workspace not 256-byte aligned", E);
-    return cuda_status(kvq::launch_mla_decode(*p, plan, out, lse, workspace, dev_status,
-                                              (cudaStream_t)stream), E);
+    return cuda_status(kvq::launch_mla_decode(*p, plan, out, lse, workspace, dev_status, stream), E);
+}
+
+extern "C" {
+
+int kvq_mla_decode(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
+                   size_t ws_bytes, uint32_t* dev_status, kvq_stream_t stream)
+{
+    const char* E = "kvq_mla_decode";
+    if (int st = injected(E)) return st;
+    return kvq::mla_decode_checked(p, out, lse, workspace, ws_bytes, dev_status,
+                                   (cudaStream_t)stream, E);
 }
 
 static int validate_q4_decode(const kvq_q4_problem* p, const char* E)

@@ -533,7 +533,8 @@ gather_q4_kernel(const uint8_t* __restrict__ pool, int n_seq, const int32_t* __r
 }
 
 // ------------------------------------------------------------------------------------
-// MLA row gather (fp8 / TQ4 caches) — colibri PR #399, Commit 2 "DSA-aware gather".
+// MLA row gather (fp8 / TQ4 caches) — colibri PR #399, Commit 2: rows gathered by
+// absolute index for DSA-style sparse attention.
 // One warp per gathered row; byte-for-byte copy of every plane.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCodecThreads)

@@ -3,8 +3,8 @@
 //
 // colibri PR #399: the MLA latent c_t is both key and value, so per query and head
 //   s_t = tau (q_lat . c_t + q_rope . k_rope_t),  out = sum_t softmax(s)_t c_t;
-// long contexts are "split-T": each CTA reduces a chunk of rows to a partial softmax
-// state (m, l, o) and a combine merges the chunks; the "DSA-aware gather" restricts the
+// long contexts split T: each CTA reduces a chunk of rows to a partial softmax
+// state (m, l, o) and a combine merges the chunks; the sparse (DSA-style) gather restricts the
 // rows to a list of absolute indices; the native TQ4 consumer scores against
 // rot(q) and accumulates in the rotated domain, unrotating the output once.
 //

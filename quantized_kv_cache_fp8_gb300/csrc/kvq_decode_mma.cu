@@ -3,9 +3,9 @@
 // accumulation).
 //
 // colibri PR #399: per query and head s_t = tau (q_lat . c_t + q_rope . k_rope_t) and
-// out = sum_t softmax(s)_t c_t over the latent rows (Commit 2, "split-T kernels": each
+// out = sum_t softmax(s)_t c_t over the latent rows (Commit 2, the kernels that split T: each
 // CTA reduces a chunk of rows to (m, l, o), the log-sum-exp combine merges the chunks;
-// the "DSA-aware gather" restricts the rows to a list of indices; TQ4 rows are scored
+// the sparse (DSA-style) gather restricts the rows to a list of indices; TQ4 rows are scored
 // against rot(q) and accumulated in the rotated domain).  Same contract and the same
 // partials (m and l in the log2 domain, o unnormalised) as the other decode kernels;
 // mla_combine_kernel merges them.

@@ -146,6 +146,18 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 // Record a one-line reason for kvq_last_error() and return `status`.
 int set_last_error(int status, const char* fmt, ...);
 
+// The host-side checks of the decode entry points, shared by kvq_mla_decode and
+// kvq_mla_decode_noalloc so that each reports failures under its own name:
+// fault_injected: the status kvq_set_fault armed for `entry`, else 0;
+// validate_mla_decode_call: the problem and the out / lse pointers (no CUDA call);
+// mla_decode_checked: those checks, the workspace checks, then the launches.
+int fault_injected(const char* entry);
+int validate_mla_decode_call(const kvq_mla_problem* p, const float* out, const float* lse,
+                             const char* entry);
+int mla_decode_checked(const kvq_mla_problem* p, float* out, float* lse, void* workspace,
+                       size_t ws_bytes, uint32_t* dev_status, cudaStream_t stream,
+                       const char* entry);
+
 // ---- launchers (host), each enqueues on `s` and returns the launch error ----------
 cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx,
                               uint8_t* codes, int64_t ldc, float* scales, cudaStream_t s);

@@ -35,7 +35,12 @@ extern "C" int kvq_mla_decode_noalloc(const kvq_mla_problem* p, float* out, floa
                                       uint32_t* dev_status, kvq_stream_t stream)
 {
     const char* E = "kvq_mla_decode_noalloc";
-    const size_t need = kvq_mla_decode_workspace(p);          // 0 when p is invalid
+    // every host-side check comes first, under this entry's name, so that a refused or
+    // empty call touches no device (no symbol lookup, nothing enqueued)
+    if (int st = kvq::fault_injected(E)) return st;
+    if (int st = kvq::validate_mla_decode_call(p, out, lse, E)) return st;
+    if (p->n_seq == 0) return KVQ_OK;
+    const size_t need = kvq_mla_decode_workspace(p);
     if (need > kNoallocScratchBytes)
         return kvq::set_last_error(KVQ_EWORKSPACE,
                                    "%s: this problem needs %zu bytes of scratch but the fixed "
@@ -59,5 +64,6 @@ extern "C" int kvq_mla_decode_noalloc(const kvq_mla_problem* p, float* out, floa
         }
         scratch = g_scratch_ptr[device];
     }
-    return kvq_mla_decode(p, out, lse, scratch, kNoallocScratchBytes, dev_status, stream);
+    return kvq::mla_decode_checked(p, out, lse, scratch, kNoallocScratchBytes, dev_status,
+                                   (cudaStream_t)stream, E);
 }

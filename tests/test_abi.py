@@ -217,6 +217,34 @@ def test_fault_injection(kvq):
     assert L.kvq_encode_fp8(FAKE, 4, 0, 512, FAKE, 512, FAKE, None) == 1
 
 
+def test_noalloc_host_checks_come_first(kvq):
+    """kvq_mla_decode_noalloc checks everything on the host, under its own name, before it
+    looks up its device array: an injected fault, an invalid problem and an empty batch
+    return without any CUDA call (none is possible here, with no GPU)."""
+    L = kvq.lib()
+    na = lambda p, out=FAKE: L.kvq_mla_decode_noalloc(C.byref(p) if p is not None else None,
+                                                      out, None, None, None)
+    assert L.kvq_set_fault(b"kvq_mla_decode_noalloc:7") == 0
+    try:
+        assert na(_problem(kvq)) == 7
+        assert L.kvq_last_error() == b"kvq_mla_decode_noalloc: fault injected (KVQ_FAULT / kvq_set_fault)"
+    finally:
+        assert L.kvq_set_fault(None) == 0
+    # a fault armed for the workspace entry does not touch this one
+    assert L.kvq_set_fault(b"kvq_mla_decode:6") == 0
+    try:
+        assert na(_problem(kvq, d_lat=256)) == 1
+        assert L.kvq_last_error().startswith(b"kvq_mla_decode_noalloc: ")
+    finally:
+        assert L.kvq_set_fault(None) == 0
+    assert na(None) == 1
+    assert L.kvq_last_error() == b"kvq_mla_decode_noalloc: NULL problem"
+    assert na(_problem(kvq, fmt=7)) == 3
+    assert na(_problem(kvq), out=None) == 1
+    assert na(_problem(kvq), out=FAKE + 4) == 4
+    assert na(_problem(kvq, n_seq=0)) == 0                  # nothing to do, no device touched
+
+
 def test_struct_layouts_match_headers(kvq, tmp_path):
     """The ctypes mirrors have the sizes and field offsets the C headers give."""
     import subprocess

@@ -58,6 +58,30 @@ def test_fp8_encode_is_nearest_code(orc):
         assert codes[r, j] & 0x7F == 0x7E
 
 
+def test_fp8_divides_by_the_scale(orc):
+    """The codes come from x / scale (one IEEE division), not x * (1 / scale).
+
+    With amax = 448 * 41 the scale is exactly 41, and every x below is 41 times an
+    exact midpoint m between an odd e4m3 code and the even code above it, so x / 41 = m
+    exactly and round-to-nearest-even picks the even (upper) code.  fp32(1/41) is below
+    1/41 by about 2^-24.4 relative, so x * fp32(1/41) falls just under m and would pick
+    the odd (lower) code: the two readings disagree on every such element.
+      m = 1.6875 (between 1.625 = 0x3D and 1.75 = 0x3E)  -> 0x3E
+      m = 31     (between 30 = 0x5F and 32 = 0x60)        -> 0x60
+      m = 432    (between 416 = 0x7D and 448 = 0x7E)      -> 0x7E
+      m = 0.2109375 (between 0x25 and 0x26)               -> 0x26
+    """
+    amax = np.float32(448 * 41)
+    x = np.zeros((1, 16), np.float32)
+    x[0, :8] = [amax, 1.6875 * 41, 31 * 41, 432 * 41, -1.6875 * 41, 0.2109375 * 41, -31 * 41, 0]
+    codes, scales = orc.encode_fp8(x)
+    assert scales[0] == np.float32(41.0)
+    assert list(codes[0, :8]) == [0x7E, 0x3E, 0x60, 0x7E, 0xBE, 0x26, 0xE0, 0x00]
+    # the reading it rules out gives the odd neighbours
+    inv = np.float32(1.0) / np.float32(41.0)
+    assert np.float32(x[0, 1]) * inv < np.float32(1.6875)
+
+
 def test_fp8_zero_rows_and_scales(orc):
     rows = W.fp8_tiny_rows(T=1024, seed=0)
     codes, scales = orc.encode_fp8(rows.c)
@@ -190,6 +214,32 @@ def test_tq4_rotated_domain_identities(orc):
     assert np.allclose(w @ xhat, unrot, rtol=0, atol=1e-12)
 
 
+def test_rotated_tiers_exact_threshold_hit_goes_up(orc):
+    """code = #{k : u >= t_k}: a value exactly on a threshold takes the upper code.
+
+    The middle threshold of every symmetric codebook is exactly 0.  With all signs +1
+    and x = e_0 + e_1, the first FWHT stage gives (2, 0) and the later stages copy that
+    pattern, so y_i = 2c for even i and exactly 0 for odd i: every odd element sits on
+    the middle threshold and must take code L/2 (the reading u > t_k would give L/2 - 1).
+    For TQ4 the even elements have u = 2c / (32c * c) = sqrt(2), between t_11 = 1.0992
+    and t_12 = 1.4370, so code 12: every packed byte is 0x8C."""
+    x = np.zeros((1, 512), np.float32)
+    x[0, 0] = x[0, 1] = 1.0
+    signs = np.zeros(16, np.uint32)
+    lloyd, cb, thr, _ = orc.tq4_codebook()
+    assert thr[7] == 0.0 and thr[11] < math.sqrt(2) < thr[12]
+    packed, radius = orc.encode_tq4(x, signs)
+    assert np.all(packed[0] == 0x8C)
+    for bits in (3, 6):
+        L = 1 << bits
+        cbb, thb = orc.tq_codebook(bits)[1:3]
+        assert thb[L // 2 - 1] == 0.0
+        pk, _ = orc.encode_tq(x, signs, bits)
+        stream = np.unpackbits(pk[0], bitorder="little")
+        codes = stream.reshape(512, bits) @ (1 << np.arange(bits))
+        assert np.all(codes[1::2] == L // 2)
+
+
 def test_tq4_inert_rows_and_refusal(orc):
     x = np.zeros((3, 512), np.float32)
     x[1, 7] = 2.5
@@ -250,17 +300,77 @@ def test_q4_tie_rule(orc):
 
 
 def test_q4_dequant_error_bound(orc):
+    """Round-to-nearest codes: away from the clamp, |(q - 8) d_f16 - z| is at most half a
+    step |d| (the +8.5 offset rounds z/d + 8 half up), plus the binary16 rounding of d
+    (|q - 8| <= 8 steps of relative 2^-11) and the fp32 reciprocal (2^-20 of a step).  A
+    codeword without the half offset (floor) errs by up to a whole step and fails."""
     g = np.random.default_rng(8)
+    n_checked = 0
     for amp in (1e-3, 1.0, 40.0):
         for _ in range(40):
             z = (g.standard_normal(32) * amp).astype(np.float32)
             out = orc.q4_block(z)
-            d = float(np.frombuffer(bytes(out[:2]), np.float16)[0])
+            d16 = float(np.frombuffer(bytes(out[:2]), np.float16)[0])
             q = np.array([(out[2 + j] & 15) if j < 16 else (out[2 + j - 16] >> 4) for j in range(32)],
                          np.int32)
-            deq = (q - 8) * d
-            step = np.max(np.abs(z)) / 8               # the page: q4's code step is max|x|/8
-            assert np.max(np.abs(deq - z)) <= step * (1 + 2 ** -9) + 1e-30
+            mval = z[np.argmax(np.abs(z))]
+            d = abs(float(mval) / 8.0)
+            clamped = (q == 15) & (z.astype(np.float64) / -(float(mval) / 8.0) >= 7.5)
+            deq = (q - 8) * d16
+            err = np.abs(deq - z.astype(np.float64))[~clamped]
+            assert np.all(err <= d * (0.5 + 8 * 2.0 ** -11 + 2.0 ** -20)), (amp, err.max() / d)
+            # the code step is max|x|/8 (the page): even a clamped element is within a step
+            assert np.max(np.abs(deq - z)) <= np.max(np.abs(z)) / 8 * (1 + 2 ** -9) + 1e-30
+            n_checked += int((~clamped).sum())
+    assert n_checked > 3000
+
+
+def test_q4_codeword_rounds_half_up(orc):
+    """q = trunc(fma(z, id, 8.5)) on a block with d = 1 (mval = -8, id = 1): z + 8.5 is
+    exact, so each code is z + 8 rounded half up, clamped to [0, 15].  Codes written out:
+      j   z               z + 8.5       code      j   z        z + 8.5   code
+      0   -8 (mval)       0.5           0         16   2.5     11        11
+      1   0.5             9             9         17  -2.5     6         6
+      2   0.5 - 2^-20     9 - 2^-20     8         18   4.5     13        13
+      3   -0.5            8             8         19  -4.5     4         4
+      4   -0.5 - 2^-20    8 - 2^-20     7         20   0.75    9.25      9
+      5   1.5             10            10        21  -0.75    7.75      7
+      6   -1.5            7             7         22   5.5     14        14
+      7   6.5             15            15        23  -5.5     3         3
+      8   7               15.5          15        24   6       14.5      14
+      9   7.5             16 -> clamp   15        25  -6       2.5       2
+      10  -7.5            1             1         26   2       10.5      10
+      11  -7.5 - 2^-20    1 - 2^-20     0         27  -2       6.5       6
+      12  3.25            11.75         11        28   1       9.5       9
+      13  -3.25           5.25          5         29  -1       7.5       7
+      14  0               8.5           8         30   0.25    8.75      8
+      15  -0              8.5           8         31  -0.25    8.25      8
+    d = 1.0 is binary16 0x3C00 (bytes 00 3C); byte 2 + j = q_j | q_(j+16) << 4."""
+    e = 2.0 ** -20
+    z = np.array([-8, 0.5, 0.5 - e, -0.5, -0.5 - e, 1.5, -1.5, 6.5, 7, 7.5, -7.5, -7.5 - e, 3.25, -3.25,
+                  0.0, -0.0, 2.5, -2.5, 4.5, -4.5, 0.75, -0.75, 5.5, -5.5, 6, -6, 2, -2, 1, -1,
+                  0.25, -0.25], np.float32)
+    assert z[2] != 0.5 and z[4] != -0.5 and z[11] != -7.5
+    q = [0, 9, 8, 8, 7, 10, 7, 15, 15, 15, 1, 0, 11, 5, 8, 8,
+         11, 6, 13, 4, 9, 7, 14, 3, 14, 2, 10, 6, 9, 7, 8, 8]
+    expect = bytes([0x00, 0x3C] + [q[j] | (q[j + 16] << 4) for j in range(16)])
+    assert bytes(orc.q4_block(z)) == expect
+
+
+def test_q4_reciprocal_uses_the_fp32_scale(orc):
+    """id = 1/d from the fp32 d, before d is rounded to binary16 for storage.
+    mval = -(8 + 2^-9) gives d = 1 + 2^-12 (exact in fp32), stored as binary16 1.0
+    (0x3C00: 2^-12 is below half a binary16 ulp).  With the fp32 d, id = 1 - 2^-12 + ..., so
+      z = 0.5: 8.5 + 0.49988 = 8.99988 -> 8   (the binary16 d would give 9)
+      z = 4.5: 8.5 + 4.49890 = 12.9989 -> 12  (the binary16 d would give 13)
+      z = -0.5: 8.00012 -> 8;  z = mval: 0.5 -> 0;  z = 0: 8."""
+    z = np.zeros(32, np.float32)
+    z[0] = -(8.0 + 2.0 ** -9)
+    z[1], z[2], z[3] = 0.5, 4.5, -0.5
+    assert np.float32(z[0] / -8.0) == np.float32(1 + 2.0 ** -12)
+    q = [0, 8, 12, 8] + [8] * 28
+    expect = bytes([0x00, 0x3C] + [q[j] | (q[j + 16] << 4) for j in range(16)])
+    assert bytes(orc.q4_block(z)) == expect
 
 
 def test_fwht256_orthonormal(orc):

@@ -141,6 +141,33 @@ def test_tq4_encode_dims_and_edges(kvq, orc, dim):
     assert np.array_equal(p, op)
 
 
+def test_codecs_on_the_pinned_boundary_cases(kvq, orc):
+    """The hand-built inputs that fix the oracle's readings, through the CUDA encoders:
+    fp8 elements that are 41 x an exact e4m3 midpoint under a scale of exactly 41 (the
+    division x / scale decides them), and rotated rows (all signs +1, x = e_0 + e_1)
+    whose odd elements land exactly on the middle threshold 0 (an exact hit goes up)."""
+    x = np.zeros((2, 512), np.float32)
+    x[0, :8] = [448 * 41, 1.6875 * 41, 31 * 41, 432 * 41, -1.6875 * 41, 0.2109375 * 41, -31 * 41, 0]
+    x[1, 0] = x[1, 1] = 1.0
+    codes, scales = gpu_fp8(kvq, x)
+    oc, os_ = orc.encode_fp8(x)
+    assert np.array_equal(codes, oc) and np.array_equal(bits(scales), bits(os_))
+    assert list(codes[0, :8]) == [0x7E, 0x3E, 0x60, 0x7E, 0xBE, 0x26, 0xE0, 0x00]
+    signs = np.zeros(16, np.uint32)
+    p, r = gpu_tq4(kvq, x[1:], signs)
+    op, orad = orc.encode_tq4(x[1:], signs)
+    assert np.array_equal(p, op) and np.array_equal(bits(r), bits(orad))
+    assert np.all(p[0] == 0x8C)
+    for b in (3, 6):
+        packed = torch.full((1, 64 * b), 0xCD, dtype=torch.uint8, device="cuda")
+        rad = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+        kvq.kvq_encode_tq(dev(x[1:]), dev(signs), b, packed, rad)
+        torch.cuda.synchronize()
+        ref, ref_r = orc.encode_tq(x[1:], signs, b)
+        assert np.array_equal(packed.cpu().numpy(), ref)
+        assert np.array_equal(bits(rad.cpu().numpy()), bits(ref_r))
+
+
 def test_tq4_refuses_non_pow2(kvq):
     x = torch.zeros(4, 384, device="cuda")
     with pytest.raises(kvq.KvqError) as e:

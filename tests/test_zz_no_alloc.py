@@ -44,7 +44,7 @@ def problem(kvq, orc, fmt, T, H, n_q, seed):
                             causal=n_q > 1, **kw)
 
 
-def decode_both(kvq, p):
+def decode_both(kvq, p, with_lse=True):
     shape = (p.n_seq, p.n_q, p.n_heads)
     ws = torch.empty(kvq.kvq_mla_decode_workspace(p), dtype=torch.uint8, device="cuda")
     out_ref = torch.full(shape + (512,), np.nan, device="cuda")
@@ -53,22 +53,56 @@ def decode_both(kvq, p):
     out = torch.full(shape + (512,), np.nan, device="cuda")
     lse = torch.full(shape, np.nan, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kvq.kvq_mla_decode_noalloc(p, out, lse, st)
+    kvq.kvq_mla_decode_noalloc(p, out, lse if with_lse else None, st)
     torch.cuda.synchronize()
     return (out.cpu().numpy(), lse.cpu().numpy(), out_ref.cpu().numpy(), lse_ref.cpu().numpy(),
             int(st.item()))
 
 
 def test_noalloc_matches_workspace_decode_twice(kvq, orc):
-    # two calls in a row, different problems and scratch footprints
-    for fmt, T, H, n_q, seed in ((kvq.FMT_TQ4, 32768, 64, 1, 0), (kvq.FMT_FP8, 5000, 16, 3, 1)):
+    # calls in a row, different problems, kernels and scratch footprints: the tcgen05
+    # kernel (TQ4, 64 heads), the warp-level MMA kernel (fp8, 16 heads, 3 causal
+    # queries) and the CUDA-core kernel (TQ4 forced to impl 1, no lse output)
+    for fmt, T, H, n_q, seed, impl in ((kvq.FMT_TQ4, 32768, 64, 1, 0, 0), (kvq.FMT_FP8, 5000, 16, 3, 1, 0),
+                                       (kvq.FMT_TQ4, 3000, 8, 1, 2, 1)):
         p = problem(kvq, orc, fmt, T, H, n_q, seed)
-        out, lse, out_ref, lse_ref, st = decode_both(kvq, p)
+        p.impl = impl
+        with_lse = impl != 1
+        out, lse, out_ref, lse_ref, st = decode_both(kvq, p, with_lse)
         assert st == 0
-        assert not np.isnan(out).any() and not np.isnan(lse).any()
+        assert not np.isnan(out).any()
         err = np.abs(out - out_ref).max(axis=-1)
         assert np.all(err <= 1e-4 * np.abs(out_ref).max(axis=-1))
-        assert np.allclose(lse, lse_ref, rtol=2e-6, atol=1e-4)
+        if with_lse:
+            assert not np.isnan(lse).any()
+            assert np.allclose(lse, lse_ref, rtol=2e-6, atol=1e-4)
+        else:
+            assert np.isnan(lse).all()                  # lse=None: nothing written there
+
+
+def test_noalloc_against_the_oracle(kvq, orc):
+    """The allocation-free decode checked directly against the fp64 oracle at one size
+    (fp8, T = 777, 16 heads): within 1e-4 of max|out| per (query, head) row."""
+    T, H, seed = 777, 16, 5
+    rows = W.magnitude_rows(T, seed=seed, lo=1e-2, hi=10.0)
+    lat, ls = orc.encode_fp8(rows.c)
+    rope, rs = orc.encode_fp8(rows.k_rope)
+    q = W.queries(1, 1, H, seed=seed)
+    cache = {k: dev(v) for k, v in dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs).items()}
+    p = kvq.make_problem(seq_len=dev(np.array([T], np.int32)), q_lat=dev(q.q_lat),
+                         q_rope=dev(q.q_rope), sm_scale=W.SM_SCALE, max_seq_len=T,
+                         fmt=kvq.FMT_FP8, fp8=cache)
+    out = torch.full((1, 1, H, 512), np.nan, device="cuda")
+    lse = torch.full((1, 1, H), np.nan, device="cuda")
+    kvq.kvq_mla_decode_noalloc(p, out, lse)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = orc.mla_decode(seq_len=np.array([T], np.int32), seq_fmt=np.array([orc.FMT_FP8], np.int32),
+                                     q_lat=q.q_lat, q_rope=q.q_rope, sm_scale=W.SM_SCALE,
+                                     fp8=dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs))
+    o = out.cpu().numpy().reshape(H, 512)
+    r = ref.reshape(H, 512)
+    assert np.all(np.abs(o - r).max(axis=-1) <= 1e-4 * np.abs(r).max(axis=-1))
+    assert np.allclose(lse.cpu().numpy().ravel(), ref_lse.ravel(), rtol=2e-6, atol=1e-4)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(kvq):
