@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--T", type=int, default=32768)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="decode suite: skip the per-configuration records (hbm_points, configs)")
     ap.add_argument("--suite", default="decode", choices=["decode", "codecs", "decode-configs"],
                     help="decode: the decode step (one JSON line); codecs: one line per codec "
                          "kernel; decode-configs: one line per decode configuration")
@@ -123,10 +125,10 @@ def peaks():
         return 6800.0, 1700.0, "fallback"
 
 
-def profile_traffic(kernel_file: str):
+def profile_traffic(kernel_file: str, summary: str = "mla_decode_tq4_T32768_H64.txt"):
     """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
     the kernel source as it is now (its sha256 matches); else None."""
-    path = os.path.join(ROOT, "profiles", "mla_decode_tq4_T32768_H64.txt")
+    path = os.path.join(ROOT, "profiles", summary)
     src = os.path.join(ROOT, "quantized_kv_cache_fp8_gb300", "csrc", kernel_file)
     try:
         text = open(path).read()
@@ -156,10 +158,24 @@ def dist_setup(args):
 
 # --------------------------------------------------------------------------- oracle ----
 
-def oracle_sample(T_sample: int, H: int, seconds_target: float = 15.0):
-    """The oracle on a bounded sample of the workload: the new-row encode plus an fp64
-    decode over T_sample rows for all H heads; repeated until ~seconds_target.
-    Returns (rows/s scaled to the full step's unit, cores used, description)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), or the machine type when lscpu has none."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for l in out.splitlines():
+            if l.split(":")[0].strip() == "Model name":
+                return l.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+def _oracle_worker(job):
+    """One process of the oracle baseline: the fp64 decode of heads [h0, h1) of the
+    sample (plus, in the first process, the encode of the step's new row), repeated
+    until `seconds` have passed.  Returns (iterations, heads, elapsed seconds)."""
+    T_sample, H, h0, h1, seconds = job
     import oracle
     import workloads as W
     oracle.build()
@@ -172,32 +188,54 @@ def oracle_sample(T_sample: int, H: int, seconds_target: float = 15.0):
     new = W.unit_rows(1, seed=1)
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.encode_tq4(new.c, signs)
-        oracle.encode_fp8(new.k_rope)
+        if h0 == 0:
+            oracle.encode_tq4(new.c, signs)
+            oracle.encode_fp8(new.k_rope)
         oracle.mla_decode(seq_len=[T_sample], seq_fmt=[2], q_lat=q.q_lat, q_rope=q.q_rope,
-                          sm_scale=W.SM_SCALE, tq4=cache, signs=signs)
+                          sm_scale=W.SM_SCALE, tq4=cache, signs=signs, heads=(h0, h1))
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds_target:
-            break
-    rate = n * T_sample / el
-    desc = (f"oracle (plain C, fp64, 1 thread): {n} x [encode 1 new row + decode over "
-            f"T={T_sample} rows, H={H}] in {el:.1f} s")
-    return rate, 1, desc
+        if el >= seconds:
+            return n, h1 - h0, el
+
+
+def oracle_sample(T_sample: int, H: int, seconds_target: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the workload (the new-row encode
+    plus an fp64 decode over T_sample rows for all H heads), timed on one host core and
+    on every host core (one process per core, each decoding a share of the heads, started
+    with `spawn`).  Returns the all-core figure and the single-core one, each as rows/s of
+    the full step's unit."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    n1, _, el1 = _oracle_worker((T_sample, H, 0, H, seconds_target / 2))
+    single = n1 * T_sample / el1
+    cores = max(1, min(os.cpu_count() or 1, H))
+    bounds = [(H * k // cores, H * (k + 1) // cores) for k in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(T_sample, H, a, b, seconds_target / 2) for a, b in bounds])
+    # full-step iterations per second: each process covers its share of the heads
+    allcore = sum(n * h / el for n, h, el in res) / H * T_sample
+    model = cpu_model()
+    desc = (f"oracle (plain C, fp64) on {model}: encode 1 new row + decode over T={T_sample} "
+            f"rows, H={H}; {cores} processes of {H // cores}-{-(-H // cores)} heads each, "
+            f"{seconds_target / 2:.0f} s; one core alone: {single:.4g} rows/s")
+    return {"value": allcore, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+            "cpu_model": model, "single_core": {"value": single, "unit": UNIT, "cores": 1}}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    rate, cores, desc = oracle_sample(4096, args.H, seconds_target=max(5.0, 2.0 * args.steps))
+    base = oracle_sample(4096, args.H, seconds_target=max(8.0, min(40.0, 2.0 * args.steps)))
+    rate = base["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"tq4 MLA decode step, T={args.T}, H={args.H}, nq=1 (oracle "
                                f"sampled at T=4096)"},
-        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": base,
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -278,7 +316,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clk:
         # keep the GPU under the same load while the sampler starts, so that its
         # samples fall on loaded clocks; then time exactly K steps
-        t_end = time.perf_counter() + 0.3
+        t_end = time.perf_counter() + 1.5
         while time.perf_counter() < t_end:
             g_enc.replay(); g_dec.replay()
             torch.cuda.synchronize()
@@ -310,10 +348,15 @@ def run_ours(args, world, rank, local):
     hbm_peak, tc_peak, peak_kind = peaks()
     achieved_tf = alg_flops / dec_launch_s / 1e12
     achieved_gbs = alg_bytes / dec_launch_s / 1e9
+    kname, ksrc, ksum = {2: ("tcgen05", "kvq_decode_tc.cu", "mla_decode_tq4_T32768_H64.txt"),
+                         4: ("tcgen05x16", "kvq_decode_tc16.cu", "mla_decode_tc16_tq4_T32768_H64.txt"),
+                         3: ("warp-mma", "kvq_decode_mma.cu", "none"),
+                         1: ("cuda-cores", "kvq_decode.cu", "none")}[kvq.kvq_mla_decode_kernel(probs[0])]
     roofline = {"bound": "tensor", "achieved": round(achieved_tf, 2), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(achieved_tf / tc_peak, 4), "traffic": profile_traffic("kvq_decode_tc.cu"),
+                "frac": round(achieved_tf / tc_peak, 4), "traffic": profile_traffic(ksrc, ksum),
                 "peak_kind": f"{peak_kind} bf16 sustained (fp16 runs at the same rate)",
-                "kernel": f"kvq_mla_decode (TQ4, T={T}, H={H}): query image, decode, combine",
+                "kernel": f"kvq_mla_decode (TQ4, T={T}, H={H}) on the {kname} kernel: query image, "
+                          f"decode, combine",
                 "decode_us_per_layer": round(dec_launch_s * 1e6, 2),
                 "flops_per_launch": alg_flops, "tensor_flops_executed_per_launch": 2 * alg_flops,
                 "tensor_pipe_frac": round(2 * achieved_tf / tc_peak, 4),
@@ -353,9 +396,15 @@ def run_ours(args, world, rank, local):
         e2e = {"value": rows_per_step * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)}
 
+    # every other decode configuration (the HBM-bound 16-head points among them), each a
+    # CUDA graph over a stack of distinct caches, against both rooflines
+    records = decode_records(args, dev) if not args.no_configs else []
+    hbm_points = [r for r in records if r["config"].startswith("HBM point")]
+    configs = [r for r in records if not r["config"].startswith("HBM point")]
+
     if rank != 0:
         return
-    cpu_rate, cores, desc = oracle_sample(4096, H, seconds_target=12.0)
+    cpu = oracle_sample(4096, H, seconds_target=12.0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4),
@@ -369,11 +418,12 @@ def run_ours(args, world, rank, local):
                    "graph": "CUDA graphs (encode half, decode half)"},
         "effective_gbs": round(Lyr * T * ROW_BYTES_TQ4 / (ms_per_step / 1e3) / 1e9, 1),
         "roofline": roofline,
-        "cpu_baseline": {"value": cpu_rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
+        "hbm_points": hbm_points,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
@@ -546,28 +596,26 @@ def run_codecs(args, local):
     report("kvq_gather (fp8 rows by index)", f"top-k {k_sel} of T={T} rows", k_sel * (584 * 2 + 4), s, k_sel, "rows")
 
 
-def run_decode_configs(args, local):
-    """One JSON line per decode configuration: one kvq_mla_decode call (query image,
-    decode, combine), median of K calls, L2 flushed before each, against both rooflines:
-    the measured HBM copy rate for the cache bytes and the measured bf16 rate for the
-    algorithmic flops (2 H n_q (512 + 64 + 512) per admissible row)."""
+def decode_records(args, dev, wanted=lambda name: True):
+    """Every decode configuration, each timed as a CUDA graph of back-to-back calls over a
+    stack of distinct caches of about 512 MB (more than L2), so that rows come from HBM
+    as in a multi-layer decode.  Returns one record per configuration: the kernel that
+    ran, microseconds per call (query image + decode + combine), KV rows/s, and the call
+    against both rooflines with the binding one named by the arithmetic intensity."""
     import torch
-    import __graft_entry__
     import quantized_kv_cache_fp8_gb300 as kvq
     import workloads as W
 
-    __graft_entry__.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     hbm_peak, tc_peak, peak_kind = peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)      # executed FLOP per byte at the ridge
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    K = max(5, args.steps)
     signs = torch.from_numpy(W.sign_bits(0)).to(dev)
+    names = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma", 4: "tcgen05x16"}
+    target = 512 << 20
+    records = []
 
     def encode_pool(n_rows, fmt, mag=None):
-        """A pool of n_rows quantized rows (N(0,1), optionally times per-row magnitudes)."""
         c = torch.randn(n_rows, 512, generator=gen, device=dev)
         r = torch.randn(n_rows, 64, generator=gen, device=dev)
         if mag is not None:
@@ -587,56 +635,80 @@ def run_decode_configs(args, local):
         kvq.kvq_encode_fp8(r, rope, rs)
         return dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
 
-    def measure(name, p, out_shape, rows_read, row_bytes, flops):
-        ws = torch.empty(max(1, kvq.kvq_mla_decode_workspace(p)), dtype=torch.uint8, device=dev)
-        out = torch.empty(out_shape, device=dev)
-        lse = torch.empty(out_shape[:-1], device=dev)
-        for _ in range(3):
-            kvq.kvq_mla_decode(p, out, lse, ws)
-        ts = []
-        for _ in range(K):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            kvq.kvq_mla_decode(p, out, lse, ws)
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) / 1e3)
-        sec = statistics.median(ts)
+    def clone(pool):
+        return {k: v.clone() for k, v in pool.items()}
+
+    def measure(name, probs, out_shape, rows_read, row_bytes, flops, extra=None):
+        n = len(probs)
+        ws = torch.empty(max(1, max(kvq.kvq_mla_decode_workspace(p) for p in probs)),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty((n,) + out_shape, device=dev)
+        lse = torch.empty((n,) + out_shape[:-1], device=dev)
+
+        def calls():
+            for i, p in enumerate(probs):
+                kvq.kvq_mla_decode(p, out[i], lse[i], ws)
+        calls()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            calls()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(20, args.steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) / 1e3 / (reps * n)
         assert torch.isfinite(out).all()
         gbs = rows_read * row_bytes / sec / 1e9
         tf = flops / sec / 1e12
-        kernel = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma"}[kvq.kvq_mla_decode_kernel(p)]
-        print(json.dumps({"suite": "decode-configs", "config": name, "decode_impl": args.decode_impl,
-                          "kernel": kernel, "us": round(sec * 1e6, 2),
-                          "kv_rows_per_s": rows_read / sec,
-                          "hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm_peak,
-                                  "frac": round(gbs / hbm_peak, 4), "bytes": rows_read * row_bytes},
-                          "tensor": {"achieved_tflops": round(tf, 2), "peak": tc_peak,
-                                     "frac": round(tf / tc_peak, 4), "flops": flops},
-                          "peak_kind": peak_kind, "l2": "flushed before each call", "steps": K}),
-              flush=True)
-
-    def wanted(name):
-        return args.only in name
+        intensity = 2 * flops / (rows_read * row_bytes)   # executed (split fp16) per byte
+        rec = {"config": name, "kernel": names[kvq.kvq_mla_decode_kernel(probs[0])],
+               "us": round(sec * 1e6, 2), "kv_rows_per_s": rows_read / sec,
+               "bound": "hbm" if intensity < ridge else "tensor",
+               "hbm": {"achieved_gbs": round(gbs, 1), "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4),
+                       "bytes": int(rows_read * row_bytes)},
+               "tensor": {"achieved_tflops": round(tf, 2), "peak": tc_peak, "frac": round(tf / tc_peak, 4),
+                          "executed_frac": round(2 * tf / tc_peak, 4), "flops": int(flops)},
+               "stack": f"{n} distinct caches in one CUDA graph, {reps} replays"}
+        if extra:
+            rec.update(extra)
+        records.append(rec)
+        return rec
 
     def one_seq(name, fmt, T, H, idx_k=0, mag=None):
         if not wanted(name):
             return
-        cache = encode_pool(T, fmt, mag)
-        q = W.queries(1, 1, H, seed=0)
-        idx = None
-        if idx_k:
-            idx = torch.from_numpy(W.sparse_indices(T, idx_k, 1, seed=0)).to(dev).reshape(1, 1, idx_k)
-        kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
-        # 3- and 6-bit rows are read by the CUDA-core kernel only
-        impl = 1 if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and args.decode_impl >= 2 else args.decode_impl
-        p = kvq.make_problem(seq_len=torch.tensor([T], dtype=torch.int32, device=dev),
-                             q_lat=torch.from_numpy(q.q_lat).to(dev), q_rope=torch.from_numpy(q.q_rope).to(dev),
-                             sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx, impl=impl, **kw)
-        n = idx_k or T
         rb = {kvq.FMT_FP8: 584, kvq.FMT_TQ4: 328, kvq.FMT_TQ6: 456, kvq.FMT_TQ3: 264}[fmt]
-        measure(name, p, (1, 1, H, 512), n, rb, 2 * H * 1088 * n)
+        layers = max(2, min(256, -(-target // (T * rb))))
+        base = encode_pool(T, fmt, mag)
+        q = W.queries(1, 1, H, seed=0)
+        q_lat = torch.from_numpy(q.q_lat).to(dev)
+        q_rope = torch.from_numpy(q.q_rope).to(dev)
+        seq_len = torch.tensor([T], dtype=torch.int32, device=dev)
+        impl = args.decode_impl
+        if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and impl in (2, 3, 4):
+            impl = 1
+        probs, keep = [], []
+        for l in range(layers):
+            cache = base if l == 0 else clone(base)
+            idx = None
+            if idx_k:
+                idx = torch.from_numpy(W.sparse_indices(T, idx_k, 1, seed=l)).to(dev).reshape(1, 1, idx_k)
+            keep.append((cache, idx))
+            kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
+            probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat, q_rope=q_rope,
+                                          sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx,
+                                          impl=impl, **kw))
+        n = idx_k or T
+        measure(name, probs, (1, 1, H, 512), n, rb, 2 * H * 1088 * n)
+        del probs, keep, base
+        torch.cuda.empty_cache()
 
     F8, T4 = kvq.FMT_FP8, kvq.FMT_TQ4
     one_seq("fp8 tiny: T=1024, H=16, magnitudes log-uniform [1e-3, 40]", F8, 1024, 16, mag=(1e-3, 40.0))
@@ -646,30 +718,41 @@ def run_decode_configs(args, local):
     for fmt, tag in ((F8, "fp8"), (T4, "TQ4")):
         for T in (32768, 131072):
             one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
-    # the rotated tier at 6 and 3 bits (CUDA-core kernel, the one that reads them)
     for fmt, tag in ((kvq.FMT_TQ6, "TQ6"), (kvq.FMT_TQ3, "TQ3")):
-        one_seq(f"{tag}: T=32768, H=16 (CUDA-core kernel)", fmt, 32768, 16)
+        one_seq(f"{tag}: T=32768, H=16", fmt, 32768, 16)
 
     # ragged mixed-tier batch: 32 sequences, L ~ U[1024, 65536], 4 causal queries, H=64
-    if not wanted("ragged: 32 seqs"):
-        return
-    n_seq, n_q, H, ps = 32, 4, 64, 64
-    L, fmt, table, pool_pages = W.ragged_layout(n_seq, 1024, 65536, ps, seed=0)
-    pools = {f: encode_pool(pool_pages[f] * ps, f, mag=(1e-2, 10.0)) for f in (F8, T4)}
-    q = W.queries(n_seq, n_q, H, seed=0)
-    p = kvq.make_problem(seq_len=torch.from_numpy(L).to(dev), q_lat=torch.from_numpy(q.q_lat).to(dev),
-                         q_rope=torch.from_numpy(q.q_rope).to(dev), sm_scale=W.SM_SCALE,
-                         max_seq_len=int(L.max()), seq_fmt=torch.from_numpy(fmt).to(dev),
-                         block_table=torch.from_numpy(table).to(dev), page_size=ps, causal=True,
-                         fp8=pools[F8], tq4=pools[T4], signs=signs, impl=args.decode_impl)
-    rows_fp8 = int(L[fmt == 1].sum())
-    rows_tq4 = int(L[fmt == 2].sum())
-    # bytes: every sequence's rows are read once per head group and query by the kernel,
-    # but the algorithmic minimum is once per sequence
-    measure(f"ragged: 32 seqs, L ~ U[1024, 65536] ({rows_fp8 + rows_tq4} rows), 4 causal queries, "
-            f"H=64, fp8 + TQ4, pages of 64", p, (n_seq, n_q, H, 512), rows_fp8 + rows_tq4,
-            (rows_fp8 * 584 + rows_tq4 * 328) / (rows_fp8 + rows_tq4),
-            2 * H * n_q * 1088 * (rows_fp8 + rows_tq4))
+    name = "ragged: 32 seqs, L ~ U[1024, 65536], 4 causal queries, H=64, fp8 + TQ4, pages of 64"
+    if wanted(name):
+        n_seq, n_q, H, ps = 32, 4, 64, 64
+        L, fmt, table, pool_pages = W.ragged_layout(n_seq, 1024, 65536, ps, seed=0)
+        pools = {f: encode_pool(pool_pages[f] * ps, f, mag=(1e-2, 10.0)) for f in (F8, T4)}
+        q = W.queries(n_seq, n_q, H, seed=0)
+        p = kvq.make_problem(seq_len=torch.from_numpy(L).to(dev), q_lat=torch.from_numpy(q.q_lat).to(dev),
+                             q_rope=torch.from_numpy(q.q_rope).to(dev), sm_scale=W.SM_SCALE,
+                             max_seq_len=int(L.max()), seq_fmt=torch.from_numpy(fmt).to(dev),
+                             block_table=torch.from_numpy(table).to(dev), page_size=ps, causal=True,
+                             fp8=pools[F8], tq4=pools[T4], signs=signs, impl=args.decode_impl)
+        rows_fp8 = int(L[fmt == 1].sum())
+        rows_tq4 = int(L[fmt == 2].sum())
+        rows = rows_fp8 + rows_tq4
+        measure(name, [p], (n_seq, n_q, H, 512), rows, (rows_fp8 * 584 + rows_tq4 * 328) / rows,
+                2 * H * n_q * 1088 * rows, extra={"rows": rows})
+        del pools
+        torch.cuda.empty_cache()
+    return records
+
+
+def run_decode_configs(args, local):
+    """One JSON line per decode configuration (see decode_records)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    for rec in decode_records(args, dev, wanted=lambda name: args.only in name):
+        rec.update({"suite": "decode-configs", "decode_impl": args.decode_impl})
+        print(json.dumps(rec), flush=True)
 
 
 def main():

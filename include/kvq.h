@@ -89,6 +89,18 @@ const char* kvq_last_error(void);
 int kvq_set_fault(const char* spec);
 
 /*
+ * Test hook for the failure path of the tensor-core decode kernels (impl 2 and 4).  Every
+ * wait in their pipelines (for a copy, an MMA or another warp's hand-over) gives up after
+ * `ns` nanoseconds of %globaltimer time; ns = 0 restores the default of 2 s.  The limit
+ * is process-wide and read at each launch.  A CTA that gives up sets KVQ_DEV_TIMEOUT in
+ * *dev_status, stops its pipeline, waits (with the default limit) for every copy and MMA
+ * it already issued, frees its tensor memory and returns; its partial result is written
+ * as (m, l) = (+inf, +inf), which the combine turns into NaN for every output row it
+ * feeds, so an aborted row never reads as a result.  Returns KVQ_OK.
+ */
+int kvq_set_wait_limit_ns(uint64_t ns);
+
+/*
  * The TQ4 codebook in use: the 16 centroids (the Lloyd-Max fixed point of N(0,1) with
  * 16 levels, each rounded to the nearest binary16 value, ascending) and the 15
  * thresholds (midpoints of adjacent centroids).  Host arrays, written by the call.
@@ -240,8 +252,8 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  * log-sum-exp combine (Commit 2: the kernels that split T).  Rows are dequantised inside the
  * kernel: fp8 c_t = code * scale; the rotated tiers (TQ4, and TQ3 / TQ6 from
  * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
- * the combine unrotates the output).  The two tensor-core kernels read FP8 and TQ4 rows;
- * a uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2 or 3 with such a
+ * the combine unrotates the output).  The tensor-core kernels read FP8 and TQ4 rows;
+ * a uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2, 3 or 4 with such a
  * `fmt` is refused with KVQ_EFORMAT), and in a seq_fmt batch on a tensor-core kernel
  * their sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
  * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
@@ -273,7 +285,9 @@ typedef struct kvq_mla_problem {
     int32_t split_rows;             /* rows per split; 0: the library chooses            */
     int32_t impl;                   /* 0: library chooses; 1: CUDA-core kernel;
                                        2: tensor-core (tcgen05) kernel, 32 heads a CTA;
-                                       3: warp-level MMA kernel, 16 heads a CTA          */
+                                       3: warp-level MMA kernel, 16 heads a CTA;
+                                       4: tcgen05 kernel, 16 heads a CTA, each code
+                                          converted to binary16 once                     */
 } kvq_mla_problem;
 
 /* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */
@@ -281,9 +295,11 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
 
 /*
  * The decode kernel kvq_mla_decode runs for this problem: 1 the CUDA-core kernel, 2 the
- * tcgen05 kernel, 3 the warp-level MMA kernel; `impl` when it is non-zero, else the
- * library's choice (fp8 problems of at most 16 heads or with a top-k list: 3; other
- * problems of 8 or more heads: 2, except the 3- and 6-bit tiers; the rest: 1).  Host
+ * tcgen05 kernel with 32 heads a CTA, 3 the warp-level MMA kernel, 4 the tcgen05 kernel
+ * with 16 heads a CTA and each code converted once; `impl` when it is non-zero, else the
+ * library's choice (fp8 problems of at most 16 heads or with a top-k list: 3; TQ4
+ * problems of 8 to 16 heads: 4; other problems of 8 or more heads: 2, except the 3- and
+ * 6-bit tiers; the rest: 1).  Host
  * only, nothing enqueued.  An invalid problem returns the negated status
  * kvq_mla_decode would return (-KVQ_EINVAL, -KVQ_EFORMAT, -KVQ_EALIGN).
  */

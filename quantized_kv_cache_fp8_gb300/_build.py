@@ -23,6 +23,7 @@ UNITS = {
     "kvq_codec.cu": ["--fmad=false"],
     "kvq_decode.cu": [],
     "kvq_decode_tc.cu": [],
+    "kvq_decode_tc16.cu": [],
     "kvq_decode_mma.cu": [],
     "kvq_noalloc.cu": [],
     "kvq_q4_decode.cu": [],

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -14,6 +15,7 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+std::atomic<uint64_t> g_wait_limit_ns{kvq::kDefaultWaitNs};
 
 std::mutex g_fault_mu;
 std::string g_fault_entry;
@@ -70,6 +72,8 @@ int cuda_status(cudaError_t e, const char* entry)
 
 }  // namespace
 
+uint64_t kvq::wait_limit_ns() { return g_wait_limit_ns.load(); }
+
 int kvq::set_last_error(int status, const char* fmt, ...)
 {
     va_list ap;
@@ -106,6 +110,12 @@ int kvq_set_fault(const char* spec)
     g_fault_env_read = true;
     int st = parse_fault(spec);
     if (st != KVQ_OK) return fail(st, "kvq_set_fault: malformed spec (want \"entry:status\")");
+    return KVQ_OK;
+}
+
+int kvq_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_limit_ns.store(ns == 0 ? kvq::kDefaultWaitNs : ns);
     return KVQ_OK;
 }
 
@@ -240,7 +250,7 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if (p->n_q < 1 || p->n_heads < 1 || p->max_seq_len < 0 || p->split_rows < 0)
         return fail(KVQ_EINVAL, "%s: bad sizes", E);
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
-    if (p->impl < 0 || p->impl > 3) return fail(KVQ_EINVAL, "%s: impl must be 0..3", E);
+    if (p->impl < 0 || p->impl > 4) return fail(KVQ_EINVAL, "%s: impl must be 0..4", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
         return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);
@@ -283,7 +293,7 @@ int kvq_mla_decode_kernel(const kvq_mla_problem* p)
     if (int st = validate_decode(p, "kvq_mla_decode_kernel")) return -st;
     kvq::DecodePlan plan;
     kvq::plan_decode(*p, plan);
-    return plan.mma ? 3 : plan.tc ? 2 : 1;
+    return plan.tc16 ? 4 : plan.mma ? 3 : plan.tc ? 2 : 1;
 }
 
 }  // extern "C"

@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 // batches; then the grid has four quarters per row, and a row not in a rotated tier is
 // split into four CTAs of 128 dims whose 16 split groups keep up to 192 splits' partials
 // in flight at once.  A row of a rotated tier needs all 512 dims for the unrotation:
-// quarter 0 does the whole row.
+// quarter 0 does the whole row.  A split of a tensor-core kernel that gave up on a wait
+// marks its partial m = +inf; a row with such a split is written as NaN (lse too).
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, int quarter, int ns)
 {
@@ -341,14 +342,16 @@ __device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, 
         v[i] = S < ns ? po[(int64_t)S * (kDLat / 4)] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     float M = -INFINITY;
+    bool abort_mark = false;                      // a split that gave up (m = +inf)
     for (int S = tid; S < ns; S += 512) {
         const float2 x = reinterpret_cast<const float2*>(ml)[S];
+        abort_mark |= x.x == INFINITY;
         if (x.y > 0.0f) M = fmaxf(M, x.x);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     if (lane == 0) s_red[0][warp] = M;
-    __syncthreads();
+    const bool aborted = __syncthreads_or(abort_mark) != 0;
     M = s_red[0][0];
 #pragma unroll
     for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
@@ -404,8 +407,9 @@ __device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, 
     }
     res = empty ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
                 : make_float4(res.x / Lt, res.y / Lt, res.z / Lt, res.w / Lt);
+    if (aborted) res = make_float4(NAN, NAN, NAN, NAN);
     reinterpret_cast<float4*>(a.out + r * kDLat + quarter * 128)[j] = res;
-    if (quarter == 0 && tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+    if (quarter == 0 && tid == 0 && a.lse) a.lse[r] = aborted ? NAN : empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
 }
 
 __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
@@ -442,15 +446,17 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     }
     float M = -INFINITY;
     float2 mine = make_float2(-INFINITY, 0.0f);   // (m, l) of split tid
+    bool abort_mark = false;                      // a split that gave up (m = +inf)
     for (int S = tid; S < ns; S += 512) {
         const float2 x = reinterpret_cast<const float2*>(ml)[S];
         if (S == tid) mine = x;
+        abort_mark |= x.x == INFINITY;
         if (x.y > 0.0f) M = fmaxf(M, x.x);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     if (lane == 0) s_red[0][warp] = M;
-    __syncthreads();
+    const bool aborted = __syncthreads_or(abort_mark) != 0;
     M = s_red[0][0];
 #pragma unroll
     for (int w = 1; w < 16; ++w) M = fmaxf(M, s_red[0][w]);
@@ -516,8 +522,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
         const bool ng = (p.tq4_signs[tid >> 5] >> (tid & 31)) & 1u;
         res = res * tq4_inv_sqrt(kDLat) * (ng ? -1.0f : 1.0f);
     }
-    a.out[r * kDLat + tid] = res;
-    if (tid == 0 && a.lse) a.lse[r] = empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
+    a.out[r * kDLat + tid] = aborted ? NAN : res;
+    if (tid == 0 && a.lse) a.lse[r] = aborted ? NAN : empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -529,45 +535,84 @@ dim3 combine_grid(int64_t rows, const DecodePlan& plan)
 
 }  // namespace
 
+int sm_count()
+{
+    static std::atomic<int> cache[64];            // per device; 0 = not queried yet
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return kDefaultSMs;
+    }
+    int n = cache[dev].load();
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = kDefaultSMs;
+        }
+        cache[dev].store(n);
+    }
+    return n;
+}
+
+namespace {
+
+// rows per split for the tensor-core kernels (whole 128-row tiles): one CTA per SM over
+// all (sequence, query, head group) units, or about four waves when the units alone
+// fill the SMs
+int64_t plan_tc_split_rows(int64_t units, int64_t n_cand, int64_t n_sm)
+{
+    constexpr int kTile = 128;
+    const int64_t tiles = std::max<int64_t>(1, (n_cand + kTile - 1) / kTile);
+    int64_t split_tiles;
+    if (units >= n_sm) {
+        split_tiles = std::max<int64_t>(1, (units * tiles + 4 * n_sm - 1) / (4 * n_sm));
+    } else {
+        const int64_t splits = std::max<int64_t>(1, std::min<int64_t>(tiles, n_sm / units));
+        split_tiles = (tiles + splits - 1) / splits;
+    }
+    return split_tiles * kTile;
+}
+
+}  // namespace
+
 bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
 {
     plan = DecodePlan();
+    const int64_t n_sm = sm_count();
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
     // The library's choice (impl 0), by measurement on GB300: fp8 problems of at most 16
     // heads, or with a top-k index list, run on the warp-level MMA kernel (16 heads a CTA,
-    // each code converted once); other problems of 8 or more heads on the tcgen05 kernel
-    // (32 heads a CTA), below that the CUDA-core kernel; uniform 3- and 6-bit problems on
+    // each code converted once); TQ4 problems of 8 to 16 heads on the 16-head tcgen05
+    // kernel (each code converted once); other problems of 8 or more heads on the 32-head
+    // tcgen05 kernel, below that the CUDA-core kernel; uniform 3- and 6-bit problems on
     // the CUDA-core kernel, the only one that reads them.
     const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
+    const bool uniform_tq4 = !p.seq_fmt && p.fmt == KVQ_FMT_TQ4;
+    plan.tc16 = p.impl == 4 || (p.impl == 0 && uniform_tq4 && p.n_heads >= 8 && p.n_heads <= 16);
     plan.mma = p.impl == 3 || (p.impl == 0 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
-    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.mma && p.n_heads >= 8 &&
+    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
                               !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
     int64_t split_rows = p.split_rows;
-    if (plan.mma) {
+    if (plan.tc16) {
+        constexpr int kHeads = 16;
+        plan.head_block = kHeads;
+        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeads - 1) / kHeads));
+        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm);
+    } else if (plan.mma) {
         plan.head_block = mma_head_block();
         if (split_rows <= 0) plan_mma_splits(p, n_cand, split_rows);
     } else if (plan.tc) {
-        constexpr int kTile = 128, kHeadsTc = 32;
-        plan.head_block = kHeadsTc;
-        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeadsTc - 1) / kHeadsTc));
-        if (split_rows <= 0) {
-            const int64_t tiles = std::max<int64_t>(1, (n_cand + kTile - 1) / kTile);
-            int64_t split_tiles;
-            if (units >= kNumSMs) {
-                split_tiles = std::max<int64_t>(1, (units * tiles + 4 * kNumSMs - 1) / (4 * kNumSMs));
-            } else {
-                const int64_t splits = std::min<int64_t>(tiles, kNumSMs / units);
-                split_tiles = (tiles + splits - 1) / splits;
-            }
-            split_rows = split_tiles * kTile;
-        }
+        constexpr int kHeads = 32;
+        plan.head_block = kHeads;
+        const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeads - 1) / kHeads));
+        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm);
     } else {
         plan.head_block = kGH;
         const int64_t n_hblk = (p.n_heads + kGH - 1) / kGH;
         if (split_rows <= 0) {
             const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * n_hblk);
-            int64_t splits = (2 * kNumSMs + units - 1) / units;
+            int64_t splits = (2 * n_sm + units - 1) / units;
             const int64_t max_splits = std::max<int64_t>(1, (n_cand + 63) / 64);
             splits = std::min(std::max<int64_t>(splits, 1), max_splits);
             split_rows = (n_cand + splits - 1) / splits;
@@ -582,7 +627,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.off_qrot = off;
     off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
     plan.off_qimg = off;
-    off += plan.tc ? tc_q_image_bytes(p) : 0;
+    off += plan.tc ? tc_q_image_bytes(p) : plan.tc16 ? tc16_q_image_bytes(p) : 0;
     plan.off_ml = off;
     off += align256(rows * plan.n_splits * 2 * sizeof(float));
     plan.off_o = off;
@@ -610,8 +655,14 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
     if (any_tq4 && !plan.tc && !plan.mma) {
-        int64_t g = std::min<int64_t>((rows + 7) / 8, kNumSMs * 8);
+        int64_t g = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
+    }
+    if (plan.tc16) {
+        cudaError_t e = launch_mla_decode_tc16(p, plan, base + plan.off_qimg, a.part_ml, a.part_o,
+                                               dev_status, s);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }
     if (plan.mma) {
         cudaError_t e = launch_mla_decode_mma(p, plan, a.part_ml, a.part_o, dev_status, s);

@@ -778,10 +778,11 @@ void plan_mma_splits(const kvq_mla_problem& p, int64_t n_cand, int64_t& split_ro
     constexpr int kPair = 2 * kT;
     const int64_t tiles = std::max<int64_t>(1, (n_cand + kPair - 1) / kPair);
     int64_t split_tiles;
-    if (units >= kNumSMs) {
-        split_tiles = std::max<int64_t>(1, (units * tiles + 4 * kNumSMs - 1) / (4 * kNumSMs));
+    const int64_t n_sm = sm_count();
+    if (units >= n_sm) {
+        split_tiles = std::max<int64_t>(1, (units * tiles + 4 * n_sm - 1) / (4 * n_sm));
     } else {
-        const int64_t splits = std::min<int64_t>(tiles, kNumSMs / units);
+        const int64_t splits = std::min<int64_t>(tiles, n_sm / units);
         split_tiles = (tiles + splits - 1) / splits;
     }
     split_rows = split_tiles * kPair;

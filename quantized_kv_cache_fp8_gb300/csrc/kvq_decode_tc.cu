@@ -28,6 +28,7 @@
 
 #include "kvq_internal.cuh"
 #include "kvq_sm100.cuh"
+#include "kvq_tc_common.cuh"
 
 namespace kvq {
 
@@ -35,7 +36,8 @@ using namespace sm100;
 
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
+using namespace tc;
+
 constexpr int kRT = 128;                 // rows per tile (MMA M)
 constexpr int kGQ = 32;                  // query-heads per CTA
 constexpr int kN = 2 * kGQ;              // MMA N: hi | lo stacked
@@ -45,7 +47,7 @@ constexpr int kQBytes = 9 * kQSlabBytes; // 72 KB
 constexpr int kPBytes = kRT * 128;       // [128 rows x 64 fp16] MN-major
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;            // rescale only when the max grows by > 2^8
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = kDefaultWaitNs;   // drains
 
 // TMEM columns
 constexpr uint32_t kColO = 256;      // O^T M-tile m at 256 + 64m
@@ -61,138 +63,15 @@ struct TcArgs {
     float* part_ml;
     float* part_o;
     uint32_t* status;
+    uint64_t wait_ns;                    // limit of the pipeline waits
 };
 
-__device__ __forceinline__ int seq_fmt_of(const kvq_mla_problem& p, int s)
-{
-    return p.seq_fmt ? p.seq_fmt[s] : p.fmt;
-}
-
-__device__ __forceinline__ int64_t pool_row_of(const kvq_mla_problem& p, int s, int64_t t)
-{
-    if (!p.block_table) return (int64_t)s * p.seq_stride_rows + t;
-    const int64_t page = t / p.page_size;
-    if (page >= p.max_pages) return -1;
-    const int64_t pid = p.block_table[(int64_t)s * p.max_pages + page];
-    if (pid < 0) return -1;
-    return pid * p.page_size + t % p.page_size;
-}
-
-// byte offset of 16-byte chunk c (0..7) of row r in a 128B-swizzled [rows x 64] slab
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
-
-// four e4m3 codes (one 32-bit word) -> two half2 words (exact); the pattern S.1111.111,
-// which the encoder never writes, reads as 0
-__device__ __forceinline__ void e4m3x4_to_half(uint32_t w, uint32_t& lo, uint32_t& hi)
-{
-    // (b & 0x7F) + 1 has bit 7 set exactly when the low seven bits of b are all set;
-    // prmt's sign mode (selector 8 + i) spreads that bit over byte i, which then clears it
-    const uint32_t t = (w & 0x7F7F7F7Fu) + 0x01010101u;
-    uint32_t m;
-    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(t));
-    w &= ~m;
-    // low byte -> low half, as the two halves of one register
-    asm("{.reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h;}"
-        : "=r"(lo), "=r"(hi) : "r"(w));
-}
-
-// ------------------------------------------------------------------------------------
-// Q image: per (seq, query, head group) the 9 swizzled K-major slabs [64 x 64] fp16 the
-// score MMA reads as B: rows 0..31 the hi halves of the group's 32 heads, rows 32..63
-// the lo halves; k < 512 from q_lat (rotated for TQ4), k >= 512 from q_rope.
-// One warp per (row of 64, slab).
-// ------------------------------------------------------------------------------------
+// Q image of 32-head groups (see build_q_image): [9 slabs][64 rows][128 B], 72 KB.
 __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
 {
     grid_dependents_launch();                    // the decode may start loading codes
-    const kvq_mla_problem& p = a.p;
-    const int lane = threadIdx.x & 31;
-    const int64_t n_items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
-    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    uint32_t neg = 0;                                       // TQ4 signs of elements k*32+lane
-    if (p.tq4_signs) {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) neg |= ((p.tq4_signs[k] >> lane) & 1u) << k;
-    }
-    const float c512 = tq4_inv_sqrt(kDLat);
-    for (int64_t it = warp; it < n_items; it += n_warps) {
-        const int n = (int)(it % kGQ);                       // head within group
-        const int64_t grp = it / kGQ;                        // (s, q, hg)
-        const int hg = (int)(grp % a.n_hg);
-        const int64_t sq = grp / a.n_hg;                     // s * n_q + q
-        const int s = (int)(sq / p.n_q);
-        const int h = hg * kGQ + n;
-        const bool tq4 = seq_fmt_of(p, s) == KVQ_FMT_TQ4;
-        uint8_t* img = a.q_img + grp * (int64_t)kQBytes;
-        // latent: element k = j*32 + lane in register j; TQ4 rotates it, (1/sqrt 512)
-        // FWHT_512(s (.) q), in fp32 first
-        float y[16];
-        float r2[2] = {0.0f, 0.0f};
-        if (h < p.n_heads) {
-            const int64_t r = sq * p.n_heads + h;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = p.q_lat[r * kDLat + j * 32 + lane];
-            r2[0] = p.q_rope[r * kDRope + 2 * lane];
-            r2[1] = p.q_rope[r * kDRope + 2 * lane + 1];
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = 0.0f;
-        }
-        if (tq4) {                                           // warp-uniform
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = ((neg >> j) & 1u) ? -y[j] : y[j];
-            fwht_warp<16>(y, lane);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] *= c512;
-        }
-        // hi | lo halves into the swizzled K-major slabs [64 rows x 64 k]
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int k = j * 32 + lane, slab = k >> 6, kk = k & 63;
-            const __half hi = __float2half_rn(y[j]);
-            const __half lo = __float2half_rn(y[j] - __half2float(hi));
-            uint8_t* base = img + slab * kQSlabBytes + (kk & 7) * 2;
-            *reinterpret_cast<__half*>(base + sw128(n, kk >> 3)) = hi;
-            *reinterpret_cast<__half*>(base + sw128(n + kGQ, kk >> 3)) = lo;
-        }
-        {
-            const __half2 hi = __floats2half2_rn(r2[0], r2[1]);
-            const float2 hf = __half22float2(hi);
-            const __half2 lo = __floats2half2_rn(r2[0] - hf.x, r2[1] - hf.y);
-            const int c = lane >> 2, wd = lane & 3;          // k = 512 + 2*lane (+1)
-            uint8_t* slab_base = img + 8 * kQSlabBytes;
-            *reinterpret_cast<__half2*>(slab_base + sw128(n, c) + 4 * wd) = hi;
-            *reinterpret_cast<__half2*>(slab_base + sw128(n + kGQ, c) + 4 * wd) = lo;
-        }
-    }
+    build_q_image<kGQ>(a.p, a.n_hg, a.q_img);
 }
-
-// Row bookkeeping shared by producer and softmax threads: the pool row of candidate j
-// of this CTA's (sequence, query), or -1 when not admissible (flags bad data).
-struct RowCtx {
-    const kvq_mla_problem* p;
-    int s, q, L;
-    int64_t r1, lim;
-    const kvq_mla_cache* C;
-    uint32_t* status;
-    __device__ int64_t row(int64_t j, bool flag) const
-    {
-        if (j >= r1) return -1;
-        const int64_t tl = p->idx ? (int64_t)p->idx[((int64_t)s * p->n_q + q) * p->top_k + j] : j;
-        if (tl < 0 || tl >= L) {
-            if (flag && status) atomicOr(status, (unsigned)KVQ_DEV_BAD_INDEX);
-            return -1;
-        }
-        if (tl > lim) return -1;
-        const int64_t r = pool_row_of(*p, s, tl);
-        if (r < 0 || r >= C->n_rows) {
-            if (flag && status) atomicOr(status, (unsigned)KVQ_DEV_BAD_PAGE);
-            return -1;
-        }
-        return r;
-    }
-};
 
 // ====================================================================================
 // The decode kernel.
@@ -272,13 +151,17 @@ struct Shared {
 };
 
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
-                                          uint32_t* status)
+                                          uint32_t* status, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    // try_wait may sleep inside the instruction until the phase completes, which hides a
+    // deadline shorter than its sleep; a short limit (set only to exercise this path)
+    // therefore polls with the non-blocking test and reads the timer on every pass
+    const bool poll = limit_ns < 100000;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!(poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
         if (*sh.abort_flag()) return false;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *sh.abort_flag() = 1;
             if (status) atomicOr(status, (unsigned)KVQ_DEV_TIMEOUT);
             return false;
@@ -288,88 +171,6 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32
 }
 
 __device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// true in exactly one lane of the (converged) warp
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t pred;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
-// 16 bytes global -> shared without registers (zero-filled when `bytes` is 0); L2
-// fetches the aligned 256 bytes around them (the rest of the row's codes follow soon);
-// completion is tracked per thread in commit groups
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 2-D tiled TMA load of the box at (x, y) of `map` into shared memory; its bytes count
-// against the transaction count of `bar`
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
-{
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// The codebook is symmetric (code 15 - k is code k with the sign flipped) and its upper
-// half is positive; the byte tables below rely on both.
-constexpr bool tq4_codebook_symmetric()
-{
-    for (int k = 0; k < 8; ++k) {
-        if (kTq4CentroidBits[15 - k] != (kTq4CentroidBits[k] ^ 0x8000u)) return false;
-        if (kTq4CentroidBits[8 + k] & 0x8000u) return false;
-    }
-    return true;
-}
-static_assert(tq4_codebook_symmetric(), "TQ4 codebook must be symmetric");
-
-// byte `hi` (0: low byte, 1: high byte) of the binary16 magnitudes m[4*part .. 4*part+3]
-constexpr uint32_t tq4_mag_bytes(int hi, int part)
-{
-    uint32_t r = 0;
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t h = kTq4CentroidBits[8 + 4 * part + b];
-        r |= (hi ? (h >> 8) : (h & 0xFFu)) << (8 * b);
-    }
-    return r;
-}
-
-// eight TQ4 codes (code i in nibble i of w) -> four half2 words of centroids
-__device__ __forceinline__ void tq4x8_to_half(uint32_t w, uint32_t* h)
-{
-    constexpr uint32_t kL0 = tq4_mag_bytes(0, 0), kL1 = tq4_mag_bytes(0, 1);
-    constexpr uint32_t kH0 = tq4_mag_bytes(1, 0), kH1 = tq4_mag_bytes(1, 1);
-    const uint32_t pos = (w >> 3) & 0x11111111u;                        // 1: code >= 8
-    const uint32_t j = (w & 0x77777777u) ^ ((pos ^ 0x11111111u) * 7u);  // magnitude index
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const uint32_t js = j >> (16 * q), ps = pos >> (16 * q);
-        const uint32_t lo = prmt(kL0, kL1, js);
-        const uint32_t hi = prmt(kH0, kH1, js) | prmt(0x80u, 0u, ps);   // sign bit 0x80
-        h[2 * q] = prmt(lo, hi, 0x5140u);
-        h[2 * q + 1] = prmt(lo, hi, 0x7362u);
-    }
-}
 
 // Item j of a producer set that converts the chunks of parity `par` (NS = its score
 // chunks per tile: 5 for parity 0 of ch = 0..8, 4 for parity 1).  The common order is,
@@ -415,46 +216,6 @@ __device__ __forceinline__ OwnItem own_item(int j, int par, int NT)
         o.tile = i - 1; o.ch = 2 * (i < NT ? r - NS : r) + par; o.score = false;
     }
     return o;
-}
-
-// codes -> 32 fp16 values (half hq of a 64-code chunk): fp8 chunks hold 64 bytes in
-// raw[0..3], TQ4 chunks 32 bytes in raw[0..1]
-__device__ __forceinline__ void codes_to_half(const uint4 (&raw)[4], int hq, bool fp8, uint32_t (&h)[16])
-{
-    if (fp8) {
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const uint4 w = raw[2 * hq + v];
-            e4m3x4_to_half(w.x, h[8 * v + 0], h[8 * v + 1]);
-            e4m3x4_to_half(w.y, h[8 * v + 2], h[8 * v + 3]);
-            e4m3x4_to_half(w.z, h[8 * v + 4], h[8 * v + 5]);
-            e4m3x4_to_half(w.w, h[8 * v + 6], h[8 * v + 7]);
-        }
-    } else {
-        const uint4 w = raw[hq];
-        tq4x8_to_half(w.x, h + 0);
-        tq4x8_to_half(w.y, h + 4);
-        tq4x8_to_half(w.z, h + 8);
-        tq4x8_to_half(w.w, h + 12);
-    }
-}
-
-// max (or sum) over the warp's 32 lanes of each of 32 values, transposed: on return
-// v[0] of lane l holds the result for value index l.
-template <bool kMax>
-__device__ __forceinline__ void warp_reduce_transpose(float (&v)[32], int lane)
-{
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
-#pragma unroll
-        for (int j = 0; j < w; ++j) {
-            const float send = up ? v[j] : v[j + w];
-            const float keep = up ? v[j + w] : v[j];
-            const float got = __shfl_xor_sync(kFull, send, w);
-            v[j] = kMax ? fmaxf(keep, got) : keep + got;
-        }
-    }
 }
 
 // 15 warps: warp w runs on sub-partition w % 4, so sub-partitions 0-2 hold four warps
@@ -583,7 +344,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 // pieces swizzled (64-byte rows: piece i at i ^ ((t >> 1) & 3); 32-byte rows:
                 // i ^ ((t >> 2) & 1)) so that the rows a quarter-warp reads share no bank
                 const int d = j % kStages;
-                ok = __all_sync(kFull, wait_bar(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.raw_full(set, d), (uint32_t)(j / kStages) & 1u, a.status, a.wait_ns));
                 if (!ok) break;
                 const uint8_t* st = sh.stage(set, d) + t * (fp8 ? 64 : 32);
                 if (fp8) {
@@ -616,7 +377,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             }
             if (it.score) {
                 const int slot = set + 2 * (a_ord & 1);
-                ok = wait_bar(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = wait_bar(sh, sh.empty_a(slot), ((uint32_t)(a_ord >> 1) & 1u) ^ 1u, a.status, a.wait_ns);
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -628,7 +389,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 ++a_ord;
             } else {
                 const int slot = 2 * (c_ord & 1) + set;
-                ok = wait_bar(sh, sh.empty_c(slot), ((uint32_t)(c_ord >> 1) & 1u) ^ 1u, a.status);
+                ok = wait_bar(sh, sh.empty_c(slot), ((uint32_t)(c_ord >> 1) & 1u) ^ 1u, a.status, a.wait_ns);
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 uint8_t* dst = sh.slot(slot);
@@ -664,7 +425,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
                 sc_rope = C.rope_scale[row];
             }
-            if (ok) ok = wait_bar(sh, sh.s_full(), (uint32_t)i & 1u, a.status);
+            if (ok) ok = wait_bar(sh, sh.s_full(), (uint32_t)i & 1u, a.status, a.wait_ns);
             ok = __all_sync(kFull, ok);
             float sv[kGQ];
 #pragma unroll
@@ -716,7 +477,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             // so that this wait and the epilogue's never trail the barrier by more than
             // one phase (a parity wait cannot tell phase k from phase k+2); it also
             // makes O safe to rescale.
-            if (i > 0 && ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status);
+            if (i > 0 && ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(i - 1) & 1u, a.status, a.wait_ns);
             ok = __all_sync(kFull, ok);
             if (need_rescale) {
                 l_lane *= alpha_s[lane];
@@ -782,11 +543,19 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             l_lane += sv[0];
         }
         // ---- epilogue: l over the 128 rows, O^T -> partials ------------------------------
-        if (ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status);
+        if (ok) ok = wait_bar(sh, sh.o_done(), (uint32_t)(NT - 1) & 1u, a.status, a.wait_ns);
         ok = __all_sync(kFull, ok);
         red[wq * 32 + lane] = l_lane;
         named_bar_softmax();
-        if (ok) {
+        // every wait that can give up lies before o_done(NT - 1): a CTA whose pipeline
+        // completed has no abort flag, and one that gave up (anywhere) poisons its partial
+        if (*sh.abort_flag()) {
+            if (t < nh) {
+                const int64_t sl = (qrow + h0 + t) * a.n_splits + split;
+                a.part_ml[sl * 2] = INFINITY;
+                a.part_ml[sl * 2 + 1] = INFINITY;
+            }
+        } else if (ok) {
             tc_fence_after();
             if (t < nh) {
                 const float lt = red[t] + red[32 + t] + red[64 + t] + red[96 + t];
@@ -833,7 +602,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 if (set != my_set) continue;
                 const int j = set ? o1++ : o0++;
                 const int d = j % kStages;
-                ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status, a.wait_ns));
                 if (!ok) break;
                 if (leader) {
                     const bool rope = it.ch == 8;
@@ -875,18 +644,18 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                           kQBytes, sh.q_full());
         }
         __syncwarp();
-        bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status));
+        bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status, a.wait_ns));
         tc_fence_after();
         for (int i = 0; i <= NT && ok; ++i) {
             if (i < NT) {
-                if (i >= 1) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status));
+                if (i >= 1) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status, a.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 for (int ch = 0; ch < 9; ++ch) {
                     // chunk ch comes from producer set ch & 1: its ord-th score chunk
                     const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
                     const int slot = (ch & 1) + 2 * (ord & 1);
-                    ok = __all_sync(kFull, wait_bar(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    ok = __all_sync(kFull, wait_bar(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
@@ -907,7 +676,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             }
             if (i >= 1) {
                 const int tile = i - 1;
-                ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)tile & 1u, a.status));
+                ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)tile & 1u, a.status, a.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 for (int c = 0; c < 8; ++c) {
@@ -915,7 +684,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                     // 2 (ord % 2) + (c & 1), next to its M-tile partner
                     const int ord = 4 * tile + (c >> 1);
                     const int slot = 2 * (ord & 1) + (c & 1);
-                    ok = __all_sync(kFull, wait_bar(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status));
+                    ok = __all_sync(kFull, wait_bar(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
                     if (!ok) break;
                     tc_fence_after();
                     if (c & 1) {
@@ -971,36 +740,6 @@ size_t tc_q_image_bytes(const kvq_mla_problem& p)
 
 namespace {
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess || q != cudaDriverEntryPointSuccess)
-            ptr = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }();
-    return fn;
-}
-
-// [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes]; rows past n_rows read as 0
-bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes)
-{
-    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc || !plane || n_rows < 1 || n_rows > INT32_MAX) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)n_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kRT};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE,
-               box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
@@ -1029,8 +768,9 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
     a.part_ml = part_ml;
     a.part_o = part_o;
     a.status = dev_status;
+    a.wait_ns = wait_limit_ns();
     const int64_t items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
-    q_image_kernel<<<(int)std::min<int64_t>((items + 7) / 8, kNumSMs * 8), 256, 0, s>>>(a);
+    q_image_kernel<<<(int)std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, (int64_t)sm_count() * 8)), 256, 0, s>>>(a);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;

@@ -13,7 +13,19 @@ namespace kvq {
 
 constexpr int kDLat = 512;
 constexpr int kDRope = 64;
-constexpr int kNumSMs = 152;
+// SM count of a GB300, used only where no device can be queried (host-only size queries
+// on a machine without a GPU); every launch plans with sm_count().
+constexpr int kDefaultSMs = 152;
+
+// The number of SMs of the current device (cudaDevAttrMultiProcessorCount), queried once
+// per device and cached; kDefaultSMs when there is no device.
+int sm_count();
+
+// The limit, in ns, of the bounded device waits in the tensor-core decode kernels'
+// pipelines (kvq_set_wait_limit_ns; 2 s by default).  Their final drains always allow
+// the default, so that an aborted CTA still lands every copy and MMA it issued.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+uint64_t wait_limit_ns();
 
 // fp32(1/sqrt(n)) for the supported TQ4 widths, correctly rounded.
 __host__ __device__ inline float tq4_inv_sqrt(int n)
@@ -178,7 +190,8 @@ cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
 
 struct DecodePlan {
-    bool tc = false;        // tensor-core (tcgen05) kernel
+    bool tc16 = false;      // tensor-core (tcgen05) kernel, 16 heads a CTA, codes converted once
+    bool tc = false;        // tensor-core (tcgen05) kernel, 32 heads a CTA
     bool mma = false;       // warp-level MMA kernel (blocks of 16 heads)
     int split_rows = 0;     // candidate rows per split
     int n_splits = 0;       // splits per (seq, query) at most
@@ -190,6 +203,9 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan);
 cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, float* out,
                               float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
 size_t tc_q_image_bytes(const kvq_mla_problem& p);
+size_t tc16_q_image_bytes(const kvq_mla_problem& p);
+cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
+                                   float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
                                  uint32_t* dev_status, cudaStream_t s);

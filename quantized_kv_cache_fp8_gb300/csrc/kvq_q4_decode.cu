@@ -511,7 +511,7 @@ bool plan_q4_decode(const kvq_q4_problem& p, Q4Plan& plan)
         // resident warps, enough splits to hide the ragged end of each
         const int64_t hg = (p.n_kv > 0 && p.n_qh / p.n_kv == 8) ? 2 : 1;
         const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_kv * hg);
-        const int64_t target = (int64_t)kNumSMs * 12 * 2;
+        const int64_t target = (int64_t)sm_count() * 12 * 2;
         const int64_t splits = std::max<int64_t>(1, (target + units - 1) / units);
         split_rows = std::max<int64_t>(64, ((int64_t)p.max_seq_len + splits - 1) / splits);
         split_rows = (split_rows + 15) / 16 * 16;

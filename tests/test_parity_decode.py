@@ -12,7 +12,7 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-IMPLS = pytest.mark.parametrize("impl", [1, 2, 3], ids=["cudacore", "tcgen05", "mma"])
+IMPLS = pytest.mark.parametrize("impl", [1, 2, 3, 4], ids=["cudacore", "tcgen05", "mma", "tcgen05x16"])
 
 
 @pytest.fixture(scope="module")

@@ -137,7 +137,7 @@ def test_mixed_batch_tensor_core_flags_six_bit_sequences(kvq, orc):
     out, lse, st = run_gpu(kvq, impl=1, **kw)
     assert st == 0
     check(out, lse, ref, ref_lse)
-    for impl in (2, 3):
+    for impl in (2, 3, 4):
         out2, lse2, st2 = run_gpu(kvq, impl=impl, **kw)
         assert st2 & kvq.DEV_BAD_FORMAT
         check(out2[:1], lse2[:1], ref[:1], ref_lse[:1])
