@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--T", type=int, default=32768)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--preload-s", type=float, default=1.5,
+                    help="decode suite: seconds of untimed load before the timed steps, so that "
+                         "the clock sampler sees loaded clocks (0 for profiling runs)")
     ap.add_argument("--no-configs", action="store_true",
                     help="decode suite: skip the per-configuration records (hbm_points, configs)")
     ap.add_argument("--suite", default="decode", choices=["decode", "codecs", "decode-configs"],
@@ -316,7 +319,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clk:
         # keep the GPU under the same load while the sampler starts, so that its
         # samples fall on loaded clocks; then time exactly K steps
-        t_end = time.perf_counter() + 1.5
+        t_end = time.perf_counter() + args.preload_s
         while time.perf_counter() < t_end:
             g_enc.replay(); g_dec.replay()
             torch.cuda.synchronize()

@@ -252,10 +252,10 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  * log-sum-exp combine (Commit 2: the kernels that split T).  Rows are dequantised inside the
  * kernel: fp8 c_t = code * scale; the rotated tiers (TQ4, and TQ3 / TQ6 from
  * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
- * the combine unrotates the output).  The tensor-core kernels read FP8 and TQ4 rows;
- * a uniform TQ3 or TQ6 problem runs on the CUDA-core kernel (impl 2, 3 or 4 with such a
- * `fmt` is refused with KVQ_EFORMAT), and in a seq_fmt batch on a tensor-core kernel
- * their sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
+ * the combine unrotates the output).  The tensor-core kernels read FP8 and TQ4 rows, and
+ * impl 4 also a problem of one 3- or 6-bit format (impl 2 or 3 with such a `fmt` is
+ * refused with KVQ_EFORMAT); in a seq_fmt batch on a tensor-core kernel the 3- and 6-bit
+ * sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
  * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
  * t <= L - n_q + j (draft + verify); with idx, only t in idx[i][j][:] (an index
  * outside [0, L) sets KVQ_DEV_BAD_INDEX and is skipped).  A query with no admissible
@@ -298,8 +298,8 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
  * tcgen05 kernel with 32 heads a CTA, 3 the warp-level MMA kernel, 4 the tcgen05 kernel
  * with 16 heads a CTA and each code converted once; `impl` when it is non-zero, else the
  * library's choice (fp8 problems of at most 16 heads or with a top-k list: 3; TQ4
- * problems of 8 to 16 heads: 4; other problems of 8 or more heads: 2, except the 3- and
- * 6-bit tiers; the rest: 1).  Host
+ * problems of 8 to 16 heads and 3- or 6-bit problems of 8 or more heads: 4; other
+ * problems of 8 or more heads: 2; the rest: 1).  Host
  * only, nothing enqueued.  An invalid problem returns the negated status
  * kvq_mla_decode would return (-KVQ_EINVAL, -KVQ_EFORMAT, -KVQ_EALIGN).
  */

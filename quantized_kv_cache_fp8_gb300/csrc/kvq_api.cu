@@ -254,8 +254,8 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
         return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);
-    if (p->impl >= 2 && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
-        return fail(KVQ_EFORMAT, "%s: the tensor-core kernels read FP8 and TQ4 rows only", E);
+    if ((p->impl == 2 || p->impl == 3) && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
+        return fail(KVQ_EFORMAT, "%s: impl 2 and 3 read FP8 and TQ4 rows only", E);
     if (p->n_seq == 0) return KVQ_OK;
     if (!p->seq_len || !p->q_lat || !p->q_rope) return fail(KVQ_EINVAL, "%s: NULL pointer", E);
     const bool need_fp8 = p->seq_fmt || p->fmt == KVQ_FMT_FP8;

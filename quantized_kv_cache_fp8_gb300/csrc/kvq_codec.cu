@@ -198,6 +198,178 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
 }
 
 // ------------------------------------------------------------------------------------
+// TQ4 encode of 512-wide rows, the MLA latent, with fewer instructions a row (same bytes):
+//  * lane l loads elements 16 l .. 16 l + 15 with 16-byte loads; the FWHT stages h = 1..8
+//    run in its registers; one transpose through shared memory (element i at i + i/16,
+//    conflict-free both ways) gives lane (bit 8 of i, bits 0-3) registers over bits 4-7,
+//    so stages h = 16..128 run in registers too and only h = 256 is a shuffle.  The stage
+//    order and every rounding are those of the pinned transform.
+//  * the radius keeps the pinned order: partial l (i mod 32) sums i = l, l + 32, ...
+//    ascending; its first eight terms sit in lane (0, l mod 16), the last eight in lane
+//    (1, l mod 16), which continues the lower lane's sum; the xor butterfly follows.
+//  * the code counts the thresholds at or below u = y / sigma.  u' = y * rcp(sigma) (both
+//    correctly rounded) is within 4.1e-6 of u (|u| <= sqrt 512).  Buckets of width 1/7,
+//    b = rn(7 u' + 160), hold at most one threshold and every threshold lies at least
+//    0.0138 from a bucket edge, so the code is base[b] + (u' >= thr[b]) unless u' is
+//    within 1e-5 of thr[b]; then the IEEE division decides, in the same bucket.
+// ------------------------------------------------------------------------------------
+struct Tq4Bucket {
+    float thr;                 // the threshold inside the bucket, or +inf
+    int base;                  // thresholds below the bucket
+};
+constexpr int kTq4Buckets = 320;
+constexpr float kTq4BucketScale = 7.0f;
+constexpr float kTq4BucketOffset = 160.0f;
+constexpr float kTq4Near = 1e-5f;
+
+__global__ void __launch_bounds__(kCodecThreads)
+encode_tq4_512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                      const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
+                      int64_t ldp, float* __restrict__ radius, bool vec_store)
+{
+    __shared__ Tq4Bucket s_tab[kTq4Buckets];
+    __shared__ float s_t[kCodecWarps][544];
+    __shared__ __align__(16) uint8_t s_out[kCodecWarps][256];
+    for (int b = threadIdx.x; b < kTq4Buckets; b += blockDim.x) {
+        const float lo = ((float)b - kTq4BucketOffset - 0.5f) / kTq4BucketScale;
+        const float hi = ((float)b - kTq4BucketOffset + 0.5f) / kTq4BucketScale;
+        int base = 0;
+        float t = INFINITY;
+        for (int k = 0; k < 15; ++k) {
+            base += c_tq4_thr[k] < lo;
+            if (c_tq4_thr[k] >= lo && c_tq4_thr[k] < hi) t = c_tq4_thr[k];
+        }
+        s_tab[b] = Tq4Bucket{t, base};
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const uint32_t neg16 = (__ldg(sign_bits + (lane >> 1)) >> (16 * (lane & 1))) & 0xFFFFu;
+    const float c = tq4_inv_sqrt(512);
+    const float sgn256 = (lane & 16) ? -1.0f : 1.0f;      // upper half of the h = 256 stage
+    float* st = s_t[wib];
+
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    // each warp walks its rows with the next row's loads in flight during this row's work
+    float4 nx[4];
+    if (warp < rows) {
+        const float4* src = reinterpret_cast<const float4*>(x + warp * ldx) + 4 * lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) nx[q] = __ldcs(src + q);
+    }
+    for (int64_t r = warp; r < rows; r += n_warps) {
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[4 * q] = nx[q].x; v[4 * q + 1] = nx[q].y; v[4 * q + 2] = nx[q].z; v[4 * q + 3] = nx[q].w;
+        }
+        if (r + n_warps < rows) {
+            const float4* src = reinterpret_cast<const float4*>(x + (r + n_warps) * ldx) + 4 * lane;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) nx[q] = __ldcs(src + q);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)                       // s_i x_i: flip the sign bit
+            v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((neg16 >> j) & 1u) << 31));
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {                 // stages h = 1, 2, 4, 8
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if ((j & h) == 0) {
+                    const float a = v[j], b = v[j + h];
+                    v[j] = __fadd_rn(a, b);
+                    v[j + h] = __fsub_rn(a, b);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) st[17 * lane + j] = v[j];
+        __syncwarp();
+        // lane L: elements (L >> 4) * 256 + k * 16 + (L & 15), k = 0..15 (register k)
+        const int rb = (lane >> 4) * 272 + (lane & 15);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = st[rb + 17 * k];
+        __syncwarp();
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {                 // stages h = 16, 32, 64, 128
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if ((k & h) == 0) {
+                    const float a = v[k], b = v[k + h];
+                    v[k] = __fadd_rn(a, b);
+                    v[k + h] = __fsub_rn(a, b);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {                     // stage h = 256, then y = w * c
+            const float pv = __shfl_xor_sync(kFull, v[k], 16);
+            v[k] = __fmul_rn(__fmaf_rn(sgn256, v[k], pv), c);
+        }
+        // radius: partial l = ((k & 1) << 4) | (lane & 15); lane's own terms m = k >> 1
+        // (+ 8 in the upper half), ascending; the upper half continues the lower's sums
+        float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            a0 = __fmaf_rn(v[k], v[k], a0);
+            a1 = __fmaf_rn(v[k + 1], v[k + 1], a1);
+        }
+        float b0 = __shfl_up_sync(kFull, a0, 16), b1 = __shfl_up_sync(kFull, a1, 16);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            b0 = __fmaf_rn(v[k], v[k], b0);
+            b1 = __fmaf_rn(v[k + 1], v[k + 1], b1);
+        }
+        float acc = __fadd_rn(b0, b1);                     // o = 16
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, o));
+        const float rad = __fsqrt_rn(__shfl_sync(kFull, acc, 16));
+        const float sigma = __fmul_rn(rad, c);
+        const float inv = __frcp_rn(sigma);
+        const bool exact_row = !(sigma >= 0x1p-120f);      // tiny sigma: divide every element
+        int code[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float u1 = __fmul_rn(v[k], inv);
+            const float bf = __fmaf_rn(u1, kTq4BucketScale, 12582912.0f + kTq4BucketOffset);
+            const int b = min(max(__float_as_int(bf) - 0x4B400000, 0), kTq4Buckets - 1);
+            const Tq4Bucket e = s_tab[b];
+            const bool near = exact_row || fabsf(__fsub_rn(u1, e.thr)) <= kTq4Near;
+            code[k] = e.base + (u1 >= e.thr ? 1 : 0);
+            if (near) {
+                // within reach of the threshold: the IEEE quotient decides (same bucket)
+                const float u = __fdiv_rn(v[k], sigma);
+                int n = 0;
+#pragma unroll
+                for (int t = 0; t < 15; ++t) n += (u >= c_tq4_thr[t]) ? 1 : 0;
+                code[k] = n;
+            }
+            if (rad == 0.0f) code[k] = 0;
+        }
+        // pack: byte (lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1); odd lanes hold the
+        // high nibble
+        uint8_t* out = s_out[wib];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int hi = __shfl_down_sync(kFull, code[k], 1);
+            if ((lane & 1) == 0)
+                out[(lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1)] = (uint8_t)(code[k] | (hi << 4));
+        }
+        __syncwarp();
+        uint8_t* pr = packed + r * ldp;
+        if (vec_store) {
+            if (lane < 16) reinterpret_cast<uint4*>(pr)[lane] = reinterpret_cast<const uint4*>(out)[lane];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pr[q * 32 + lane] = out[q * 32 + lane];
+        }
+        __syncwarp();
+        if (lane == 0) radius[r] = rad;
+    }
+}
+
+// ------------------------------------------------------------------------------------
 // The rotated tiers at 3 and 6 bits (colibri PR #399: KV_TQ=6, and 3 bits): the same row
 // transform and radius as TQ4, a 2^b-level codebook, and codes packed as a little-endian
 // bit stream (code i at bits b*i .. b*i + b - 1 of the row).  24 / b consecutive codes fill
@@ -624,7 +796,16 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
         case 64:   encode_tq4_kernel<2><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         case 128:  encode_tq4_kernel<4><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         case 256:  encode_tq4_kernel<8><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
-        case 512:  encode_tq4_kernel<16><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
+        case 512:
+            if ((uintptr_t)x % 16 == 0 && ldx % 4 == 0) {
+                // one wave (four CTAs of eight warps per SM), each warp many rows
+                const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kCodecWarps - 1) / kCodecWarps,
+                                                                           (int64_t)sm_count() * 4));
+                encode_tq4_512_kernel<<<g1, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, vec);
+            }
+            else
+                encode_tq4_kernel<16><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec);
+            break;
         case 1024: encode_tq4_kernel<32><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         default: return cudaErrorInvalidValue;
     }

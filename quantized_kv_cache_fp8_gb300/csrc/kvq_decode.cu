@@ -583,13 +583,15 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.n_cand_max = (int)n_cand;
     // The library's choice (impl 0), by measurement on GB300: fp8 problems of at most 16
     // heads, or with a top-k index list, run on the warp-level MMA kernel (16 heads a CTA,
-    // each code converted once); TQ4 problems of 8 to 16 heads on the 16-head tcgen05
-    // kernel (each code converted once); other problems of 8 or more heads on the 32-head
-    // tcgen05 kernel, below that the CUDA-core kernel; uniform 3- and 6-bit problems on
-    // the CUDA-core kernel, the only one that reads them.
+    // each code converted once); TQ4 problems of 8 to 16 heads, and 3- and 6-bit problems
+    // of 8 or more heads, on the 16-head tcgen05 kernel (each code converted once); other
+    // problems of 8 or more heads on the 32-head tcgen05 kernel; below 8 heads the
+    // CUDA-core kernel.
     const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
     const bool uniform_tq4 = !p.seq_fmt && p.fmt == KVQ_FMT_TQ4;
-    plan.tc16 = p.impl == 4 || (p.impl == 0 && uniform_tq4 && p.n_heads >= 8 && p.n_heads <= 16);
+    const bool uniform_tqb = !p.seq_fmt && (p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6);
+    plan.tc16 = p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
+                                ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb));
     plan.mma = p.impl == 3 || (p.impl == 0 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
     plan.tc = p.impl == 2 || (p.impl == 0 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
                               !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));

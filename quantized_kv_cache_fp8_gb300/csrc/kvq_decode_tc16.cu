@@ -83,7 +83,8 @@ constexpr int kOffM = kOffRed + 4 * 16 * 4;               // [16] running maxima
 constexpr int kOffAlpha = kOffM + 16 * 4;                 // [16] rescale factors
 constexpr int kOffFlag = kOffAlpha + 16 * 4;              // some head rescales O
 constexpr int kOffVote = kOffFlag + 16;                   // [2][4] "a row exceeds the max"
-constexpr int kOffBar = kOffVote + 32;
+constexpr int kOffTab = kOffVote + 32;                    // [64] binary16 centroids (3/6 bits)
+constexpr int kOffBar = kOffTab + 128;
 // full_a[3][2], empty_a[3][2], full_v[8], empty_v[8], s_full, s_empty[2], p_full, o_done,
 // drain, q_full, raw_full[3][kStages], raw_empty[3][kStages]
 constexpr int kNumBars = 2 * kSets * kRingA + 16 + 7 + 2 * kSets * kStages;
@@ -102,6 +103,7 @@ struct Tc16Args {
     float* part_o;
     uint32_t* status;
     uint64_t wait_ns;                    // limit of the pipeline waits
+    uint16_t cb_tab[64];                 // binary16 centroids of a 3- or 6-bit problem
 };
 
 __global__ void __launch_bounds__(256) q_image16_kernel(Tc16Args a)
@@ -122,6 +124,7 @@ struct Shared {
     __device__ float* alpha() const { return reinterpret_cast<float*>(base + kOffAlpha); }
     __device__ volatile int* flag() const { return reinterpret_cast<volatile int*>(base + kOffFlag); }
     __device__ volatile int* vote(int par) const { return reinterpret_cast<volatile int*>(base + kOffVote) + 4 * par; }
+    __device__ uint16_t* tab() const { return reinterpret_cast<uint16_t*>(base + kOffTab); }
     __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
     __device__ uint64_t* full_a(int s, int j) const { return bar(s * kRingA + j); }
     __device__ uint64_t* empty_a(int s, int j) const { return bar(kSets * kRingA + s * kRingA + j); }
@@ -186,6 +189,9 @@ static_assert(kSets * kPer == 9, "nine chunks a tile");
 //  * Warps 17-19: TMA loaders of the three sets (contiguous caches); paged and sparse
 //    caches are copied by the producers themselves with cp.async.
 // ====================================================================================
+// kB = 0: fp8 and TQ4 rows (per sequence, mixed batches included); kB = 6 or 3: the
+// rotated tier at 6 or 3 bits in a problem of that one format.
+template <int kB>
 __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ Tc16Args a)
 {
     extern __shared__ uint8_t dsm[];
@@ -202,7 +208,10 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
     const int64_t r0 = (int64_t)split * a.split_rows;
     const int64_t r1 = min(r0 + (int64_t)a.split_rows, n_cand);
     const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
-    const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
+    // the 3- and 6-bit rotated tiers are read in problems of one format (the rotated
+    // planes of a seq_fmt batch hold 4-bit rows)
+    const bool bad_fmt = kB == 0 ? !(fmt == KVQ_FMT_FP8 || fmt == KVQ_FMT_TQ4)
+                                 : (p.seq_fmt != nullptr || fmt != (kB == 6 ? KVQ_FMT_TQ6 : KVQ_FMT_TQ3));
     grid_dependents_launch();                    // the combine may start launching
 
     if (r0 >= n_cand || bad_fmt) {
@@ -214,8 +223,10 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         }
         return;
     }
-    const bool tq4 = fmt == KVQ_FMT_TQ4;
-    const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
+    const bool rot = fmt != KVQ_FMT_FP8;               // a rotated tier: 3, 4 or 6 bits
+    const int bits = kB != 0 ? kB : rot ? 4 : 8;
+    const int lat_cb = 8 * bits;                        // bytes of a latent chunk of a row
+    const kvq_mla_cache& C = rot ? p.tq4 : p.fp8;
     const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
     const RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
 
@@ -250,6 +261,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         tmem_relinquish();
     }
     if (tid < kGQ) sh.m_run()[tid] = -INFINITY;
+    if (tid < 64) sh.tab()[tid] = a.cb_tab[tid];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -273,18 +285,20 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                 }
                 const int64_t row = row_c;
                 const bool rope = ch == 0;
-                const bool fp8 = rope || !tq4;
+                const int cb = rope ? 64 : lat_cb;
                 const uint8_t* src = row < 0 ? C.rope
                                    : rope ? C.rope + row * kDRope
-                                   : tq4 ? C.lat + row * (kDLat / 2) + (ch - 1) * 32
-                                         : C.lat + row * kDLat + (ch - 1) * 64;
-                const uint32_t nb = row < 0 ? 0u : 16u;      // invalid rows read as zeros
-                uint8_t* st = sh.stage(set, o % kStages) + t * 16;
-                cp_async16(st, src, nb);
-                cp_async16(st + kRT * 16, src + 16, nb);
-                if (fp8) {
-                    cp_async16(st + 2 * kRT * 16, src + 32, nb);
-                    cp_async16(st + 3 * kRT * 16, src + 48, nb);
+                                          : C.lat + row * (kDLat * bits / 8) + (ch - 1) * lat_cb;
+                uint8_t* st = sh.stage(set, o % kStages);
+                const uint32_t nb = row < 0 ? 0u : 16u;       // invalid rows read as zeros
+                if (cb == 24) {
+                    // a 3-bit chunk starts 0 or 8 bytes past a 16-byte boundary (24 j):
+                    // copy the two aligned 16-byte pieces that hold its 24 bytes
+                    const uint8_t* s16 = row < 0 ? src : src - ((ch - 1) & 1) * 8;
+                    cp_async16(st + t * 16, s16, nb);
+                    cp_async16(st + (kRT + t) * 16, s16 + 16, nb);
+                } else {
+                    for (int pc = 0; pc < cb / 16; ++pc) cp_async16(st + (pc * kRT + t) * 16, src + 16 * pc, nb);
                 }
             }
             cp_async_commit();                            // one group per item, maybe empty
@@ -293,33 +307,44 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         // the raw codes of chunk o into registers (TMA: after its box landed)
         auto fetch = [&](int o, uint4 (&raw)[4]) -> bool {
             const int tile = o / kPer, ch = kSets * (o - tile * kPer) + set;
-            const bool fp8 = ch == 0 || !tq4;
+            const int cb = ch == 0 ? 64 : lat_cb;
+            raw[1] = raw[2] = raw[3] = make_uint4(0u, 0u, 0u, 0u);
             if (tma) {
-                // the loader's box: row t at t * (bytes per row of the chunk), its 16-byte
-                // pieces swizzled by the TMA (64-byte rows: piece i at i ^ ((t >> 1) & 3);
-                // 32-byte rows: i ^ ((t >> 2) & 1))
+                // the loader's box: row t at t * cb; its 16-byte pieces swizzled by the TMA
+                // (64-byte rows: piece i at i ^ ((t >> 1) & 3); 32-byte rows: i ^ ((t >> 2)
+                // & 1); 48-byte rows unswizzled, conflict-free as they are)
                 const int d = o % kStages;
                 if (!__all_sync(kFull, wait_bar(sh, sh.raw_full(set, d), (uint32_t)(o / kStages) & 1u, a.status, a.wait_ns)))
                     return false;
-                const uint8_t* st = sh.stage(set, d) + t * (fp8 ? 64 : 32);
-                if (fp8) {
+                const uint8_t* st = sh.stage(set, d) + t * cb;
+                if (cb == 64) {
                     const int x = (t >> 1) & 3;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) raw[i] = *reinterpret_cast<const uint4*>(st + 16 * (i ^ x));
-                } else {
+                } else if (cb == 32) {
                     const int x = (t >> 2) & 1;
                     raw[0] = *reinterpret_cast<const uint4*>(st + 16 * x);
                     raw[1] = *reinterpret_cast<const uint4*>(st + 16 * (1 ^ x));
-                    raw[2] = make_uint4(0u, 0u, 0u, 0u);
-                    raw[3] = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) raw[i] = *reinterpret_cast<const uint4*>(st + 16 * i);
                 }
             } else {
                 cp_async_wait<kStages - 1>();             // item o's group has landed
-                const uint8_t* st = sh.stage(set, o % kStages) + t * 16;
-                raw[0] = *reinterpret_cast<const uint4*>(st);
-                raw[1] = *reinterpret_cast<const uint4*>(st + kRT * 16);
-                raw[2] = fp8 ? *reinterpret_cast<const uint4*>(st + 2 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
-                raw[3] = fp8 ? *reinterpret_cast<const uint4*>(st + 3 * kRT * 16) : make_uint4(0u, 0u, 0u, 0u);
+                const uint8_t* st = sh.stage(set, o % kStages);
+                if (cb == 24) {
+                    const uint4 a0 = *reinterpret_cast<const uint4*>(st + t * 16);
+                    const uint4 a1 = *reinterpret_cast<const uint4*>(st + (kRT + t) * 16);
+                    if (((ch - 1) & 1) == 0) {            // the chunk's 24 bytes start at byte 0
+                        raw[0] = a0;
+                        raw[1] = make_uint4(a1.x, a1.y, 0u, 0u);
+                    } else {                              // ... at byte 8
+                        raw[0] = make_uint4(a0.z, a0.w, a1.x, a1.y);
+                        raw[1] = make_uint4(a1.z, a1.w, 0u, 0u);
+                    }
+                } else {
+                    for (int i = 0; i < cb / 16; ++i) raw[i] = *reinterpret_cast<const uint4*>(st + (i * kRT + t) * 16);
+                }
             }
             return true;
         };
@@ -332,10 +357,14 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         for (int o = 0; o < n_own && ok; ++o) {
             const int tile = o / kPer, k = o - tile * kPer, ch = kSets * k + set;
             const bool rope = ch == 0;
-            const bool fp8 = rope || !tq4;
             uint32_t h[32];
-            codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
-            codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+            if (kB == 0 || rope) {
+                const bool fp8 = rope || bits == 8;
+                codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
+                codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+            } else {
+                tqb_codes_to_half<kB == 0 ? 6 : kB>(raw, sh.tab(), h);
+            }
             // the stage is free once every lane's reads of it are consumed
             if (tma) {
                 __syncwarp();
@@ -414,7 +443,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
             const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
             float sc_lat = 0.0f, sc_rope = 0.0f;
             if (row >= 0) {
-                sc_lat = tq4 ? C.lat_scale[row] * c512 : C.lat_scale[row];
+                sc_lat = rot ? C.lat_scale[row] * c512 : C.lat_scale[row];
                 sc_rope = C.rope_scale[row];
             }
             if (ok) ok = wait_bar(sh, sh.s_full(), (uint32_t)i & 1u, a.status, a.wait_ns);
@@ -582,8 +611,8 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         const int set = warp - kWarpLoad;
         if (a.use_tma) {
             const bool leader = elect_one();
-            const CUtensorMap* m_lat = &a.tm_lat[tq4 ? 1 : 0];
-            const CUtensorMap* m_rope = &a.tm_rope[tq4 ? 1 : 0];
+            const CUtensorMap* m_lat = &a.tm_lat[rot ? 1 : 0];
+            const CUtensorMap* m_rope = &a.tm_rope[rot ? 1 : 0];
             const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;   // pool row of candidate r0
             const int n_own = kPer * NT;
             bool ok = true;
@@ -595,7 +624,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                 if (!ok) break;
                 if (leader) {
                     const bool rope = ch == 0;
-                    const int inner = (rope || !tq4) ? 64 : 32;
+                    const int inner = rope ? 64 : lat_cb;
                     mbar_arrive_expect_tx(sh.raw_full(set, d), (uint32_t)(inner * kRT));
                     tma_load_2d(sh.stage(set, d), rope ? m_rope : m_lat, rope ? 0 : (ch - 1) * inner,
                                 (int)(row0 + (int64_t)tile * kRT), sh.raw_full(set, d));
@@ -729,13 +758,17 @@ cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& p
 {
     Tc16Args a;
     memset(&a, 0, sizeof(a));
-    if (!p.block_table && !p.idx) {
+    // TMA boxes of one 64-dim chunk: 64 B (fp8), 32 B (4 bits), 48 B (6 bits); 3-bit
+    // chunks (24 B) are no multiple of 16 bytes and go by cp.async
+    const int rot_bits = p.seq_fmt ? 4 : rotated_bits(p.fmt);
+    if (!p.block_table && !p.idx && !(!p.seq_fmt && p.fmt == KVQ_FMT_TQ3)) {
         bool ok = true;
         for (int k = 0; k < 2 && ok; ++k) {
-            const bool used = p.seq_fmt || p.fmt == (k ? KVQ_FMT_TQ4 : KVQ_FMT_FP8);
+            const bool used = p.seq_fmt || (k ? rotated_format(p.fmt) : p.fmt == KVQ_FMT_FP8);
             if (!used) continue;
             const kvq_mla_cache& c = k ? p.tq4 : p.fp8;
-            ok = make_code_map(&a.tm_lat[k], c.lat, c.n_rows, k ? kDLat / 2 : kDLat, k ? 32 : 64) &&
+            ok = make_code_map(&a.tm_lat[k], c.lat, c.n_rows, k ? kDLat * rot_bits / 8 : kDLat,
+                               k ? 8 * rot_bits : 64) &&
                  make_code_map(&a.tm_rope[k], c.rope, c.n_rows, kDRope, 64);
         }
         a.use_tma = ok ? 1 : 0;
@@ -749,6 +782,8 @@ cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& p
     a.part_o = part_o;
     a.status = dev_status;
     a.wait_ns = wait_limit_ns();
+    for (int k = 0; k < 64; ++k)
+        a.cb_tab[k] = p.fmt == KVQ_FMT_TQ6 ? kTq6CentroidBits[k] : p.fmt == KVQ_FMT_TQ3 ? kTq3CentroidBits[k & 7] : 0;
     const int64_t items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
     const int n_sm = sm_count();
     q_image16_kernel<<<(int)std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, (int64_t)n_sm * 8)), 256, 0, s>>>(a);
@@ -758,12 +793,16 @@ cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& p
     static std::atomic<uint64_t> attr_set{0};
     const uint64_t bit = 1ull << (device & 63);
     if (!(attr_set.load() & bit)) {
-        e = cudaFuncSetAttribute(mla_decode_tc16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
+        for (auto* k : {mla_decode_tc16_kernel<0>, mla_decode_tc16_kernel<6>, mla_decode_tc16_kernel<3>}) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         attr_set.fetch_or(bit);
     }
     dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    return launch_dependent(mla_decode_tc16_kernel, grid, dim3(kThreads), kSmemBytes, s, a);
+    auto* kern = (!p.seq_fmt && p.fmt == KVQ_FMT_TQ6) ? mla_decode_tc16_kernel<6>
+               : (!p.seq_fmt && p.fmt == KVQ_FMT_TQ3) ? mla_decode_tc16_kernel<3> : mla_decode_tc16_kernel<0>;
+    return launch_dependent(kern, grid, dim3(kThreads), kSmemBytes, s, a);
 }
 
 }  // namespace kvq

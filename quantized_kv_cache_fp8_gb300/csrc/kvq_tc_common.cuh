@@ -185,6 +185,31 @@ __device__ __forceinline__ void codes_to_half(const uint4 (&raw)[4], int hq, boo
     }
 }
 
+// 64 codes of b = 3 or 6 bits (a little-endian bit stream: code i at bits b i .. b i +
+// b - 1 of the chunk's 24 or 48 bytes, in the words raw[0].x, .y, ...) -> 32 half2 words
+// of centroids, looked up in a shared-memory table of 2^b binary16 values.  A table of at
+// most 64 binary16 values fills at most one 32-bit word per bank, so lanes that hit the
+// same bank read the same word: the lookups are free of bank conflicts for any codes.
+template <int B>
+__device__ __forceinline__ void tqb_codes_to_half(const uint4 (&raw)[4], const uint16_t* tab,
+                                                  uint32_t (&h)[32])
+{
+    const uint32_t w[12] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y,
+                            raw[1].z, raw[1].w, raw[2].x, raw[2].y, raw[2].z, raw[2].w};
+    constexpr uint32_t kMask = (1u << B) - 1u;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        uint32_t v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int bit = B * (2 * c + e), wi = bit >> 5, sh = bit & 31;
+            const uint32_t code = (sh + B <= 32 ? (w[wi] >> sh) : __funnelshift_r(w[wi], w[wi + 1], sh)) & kMask;
+            v[e] = tab[code];
+        }
+        h[c] = v[0] | (v[1] << 16);
+    }
+}
+
 // max (or sum) over the warp's 32 lanes of each of NV values (NV = 16 or 32), transposed:
 // on return v[0] of lane l holds the result for value index l % NV.  The stages that
 // halve the value count exchange halves between lane pairs (NV - 1 shuffles in all);
@@ -226,7 +251,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes] (64-byte boxes 64B-swizzled,
-// 32-byte boxes 32B-swizzled); rows past n_rows read as 0
+// 32-byte boxes 32B-swizzled, 48-byte boxes unswizzled); rows past n_rows read as 0
 inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes)
 {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -237,7 +262,8 @@ inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, 
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE,
-               box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+               box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+               : box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -89,9 +89,9 @@ def _problem(kvq, **kw):
 
 def test_decode_kernel_choice(kvq):
     """Which kernel kvq_mla_decode runs (host only): fp8 with at most 16 heads or a top-k
-    list on the warp-level MMA kernel, TQ4 with 8 to 16 heads on the 16-head tcgen05
-    kernel, other problems of 8+ heads on the 32-head tcgen05 kernel, the rest (and the
-    3- and 6-bit tiers) on CUDA cores; an explicit impl wins."""
+    list on the warp-level MMA kernel, TQ4 with 8 to 16 heads and the 3- and 6-bit tiers
+    with 8+ heads on the 16-head tcgen05 kernel, other problems of 8+ heads on the
+    32-head tcgen05 kernel, the rest on CUDA cores; an explicit impl wins."""
     fp8 = dict(fmt=kvq.FMT_FP8, fp8=kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768))
     k = lambda **kw: kvq.kvq_mla_decode_kernel(_problem(kvq, **kw))
     assert k(n_heads=16, **fp8) == kvq.IMPL_MMA
@@ -103,8 +103,9 @@ def test_decode_kernel_choice(kvq):
     assert k(n_heads=8) == kvq.IMPL_TC16
     assert k(n_heads=17) == kvq.IMPL_TC
     assert k(n_heads=4) == kvq.IMPL_SIMT
-    assert k(n_heads=16, fmt=kvq.FMT_TQ6) == kvq.IMPL_SIMT
-    assert k(n_heads=16, fmt=kvq.FMT_TQ3) == kvq.IMPL_SIMT
+    assert k(n_heads=16, fmt=kvq.FMT_TQ6) == kvq.IMPL_TC16
+    assert k(n_heads=64, fmt=kvq.FMT_TQ3) == kvq.IMPL_TC16
+    assert k(n_heads=4, fmt=kvq.FMT_TQ6) == kvq.IMPL_SIMT
     for impl in (1, 2, 3, 4):
         assert k(n_heads=16, impl=impl) == impl
     with pytest.raises(kvq.KvqError) as e:
@@ -123,7 +124,7 @@ def test_decode_argument_errors(kvq):
         assert dec(_problem(kvq, fmt=fmt)) == 5                                  # workspace next
         assert dec(_problem(kvq, fmt=fmt, impl=2)) == 3
         assert dec(_problem(kvq, fmt=fmt, impl=3)) == 3
-        assert dec(_problem(kvq, fmt=fmt, impl=4)) == 3
+        assert dec(_problem(kvq, fmt=fmt, impl=4)) == 5                          # read by impl 4
     assert dec(_problem(kvq, tq4_signs=None)) == 1
     assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
     assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1

@@ -1,7 +1,8 @@
 """GPU parity of the rotated tiers at 3 and 6 bits (colibri PR #399: KV_TQ=6 and a
 3-bit setting beside the 4-bit tier): every encoded byte and radius bit equal to the
-oracle's (kvq_encode_tq), the decode over 3- and 6-bit rows (the CUDA-core kernel)
-within 1e-4 * max|out| of the fp64 oracle, and the row gather byte for byte."""
+oracle's (kvq_encode_tq), the decode over 3- and 6-bit rows (the CUDA-core kernel and
+the 16-head tcgen05 kernel) within 1e-4 * max|out| of the fp64 oracle, and the row
+gather byte for byte."""
 import numpy as np
 import pytest
 import torch
@@ -86,23 +87,25 @@ def encode_cache(orc, rows, signs, bits):
     return dict(lat=lat, lat_scale=rad, rope=rope, rope_scale=rs)
 
 
+@pytest.mark.parametrize("impl", [1, 4], ids=["cudacore", "tcgen05x16"])
 @pytest.mark.parametrize("bits", [3, 6])
-@pytest.mark.parametrize("T,split", [(1, 0), (17, 0), (65, 32), (1000, 96), (4096, 0)])
-def test_decode_over_tq_rows(kvq, orc, bits, T, split):
+@pytest.mark.parametrize("T,split", [(1, 0), (17, 0), (65, 32), (1000, 96), (4096, 0), (20000, 0)])
+def test_decode_over_tq_rows(kvq, orc, bits, T, split, impl):
     rows = W.magnitude_rows(T, seed=T + bits, lo=1e-2, hi=10.0)
     signs = W.sign_bits(T + bits)
     cache = encode_cache(orc, rows, signs, bits)
     q = W.queries(1, 1, 16, seed=T)
     out, lse, st = run_gpu(kvq, cache_fmt=FMT[bits], caches={2: cache}, seq_len=[T], q=q,
-                           signs=signs, split_rows=split)
+                           signs=signs, split_rows=split, impl=impl)
     ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[FMT[bits]], q_lat=q.q_lat,
                                      q_rope=q.q_rope, sm_scale=W.SM_SCALE, tq4=cache, signs=signs)
     assert st == 0
     check(out, lse, ref, ref_lse)
 
 
+@pytest.mark.parametrize("impl", [1, 4], ids=["cudacore", "tcgen05x16"])
 @pytest.mark.parametrize("bits", [3, 6])
-def test_decode_paged_causal_multi_query(kvq, orc, bits):
+def test_decode_paged_causal_multi_query(kvq, orc, bits, impl):
     """Two sequences through a permuted block table (pages of 16), 3 causal queries."""
     lengths = [150, 47]
     rows = W.unit_rows(320, seed=60 + bits)
@@ -111,7 +114,7 @@ def test_decode_paged_causal_multi_query(kvq, orc, bits):
     table = np.random.default_rng(60).permutation(20).astype(np.int32).reshape(2, 10)
     q = W.queries(2, 3, 8, seed=60)
     kw = dict(seq_len=lengths, q=q, signs=signs, block_table=table, page_size=16, causal=True)
-    out, lse, st = run_gpu(kvq, cache_fmt=FMT[bits], caches={2: cache}, **kw)
+    out, lse, st = run_gpu(kvq, cache_fmt=FMT[bits], caches={2: cache}, impl=impl, **kw)
     ref, ref_lse, _ = orc.mla_decode(seq_len=lengths, seq_fmt=[FMT[bits]] * 2, q_lat=q.q_lat,
                                      q_rope=q.q_rope, sm_scale=W.SM_SCALE, causal=True,
                                      block_table=table, page_size=16, tq4=cache, signs=signs)
