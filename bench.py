@@ -58,8 +58,8 @@ def parse():
     ap.add_argument("--only", default="",
                     help="decode-configs: run only the configurations whose name contains this text")
     ap.add_argument("--decode-impl", type=int, default=0,
-                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tensor cores "
-                         "(tcgen05), 3 tensor cores (warp-level MMA)")
+                    help="decode kernel: 0 library's choice, 1 CUDA cores, 2 tcgen05 (32 heads), "
+                         "3 warp-level MMA, 4 tcgen05 (16 heads), 5 tcgen05 on e4m3 codes (fp8 tier)")
     return ap.parse_args()
 
 
@@ -287,7 +287,8 @@ def run_ours(args, world, rank, local):
         planes = dict(lat=lat[l], lat_scale=rad[l], rope=rope[l], rope_scale=rsc[l])
         probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat[l:l + 1], q_rope=q_rope[l:l + 1],
                                       sm_scale=W.SM_SCALE, max_seq_len=T, fmt=kvq.FMT_TQ4,
-                                      tq4=planes, signs=signs, impl=args.decode_impl))
+                                      tq4=planes, signs=signs,
+                                      impl=0 if args.decode_impl == 5 else args.decode_impl))
     ws = torch.empty(kvq.kvq_mla_decode_workspace(probs[0]), dtype=torch.uint8, device=dev)
 
     def encode_step():
@@ -614,7 +615,7 @@ def decode_records(args, dev, wanted=lambda name: True):
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     signs = torch.from_numpy(W.sign_bits(0)).to(dev)
-    names = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma", 4: "tcgen05x16"}
+    names = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma", 4: "tcgen05x16", 5: "tcgen05-e4m3"}
     target = 512 << 20
     records = []
 
@@ -695,8 +696,10 @@ def decode_records(args, dev, wanted=lambda name: True):
         q_rope = torch.from_numpy(q.q_rope).to(dev)
         seq_len = torch.tensor([T], dtype=torch.int32, device=dev)
         impl = args.decode_impl
-        if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and impl in (2, 3, 4):
-            impl = 1
+        if fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6) and impl in (2, 3):
+            impl = 4
+        if fmt != kvq.FMT_FP8 and impl == 5:
+            impl = 0
         probs, keep = [], []
         for l in range(layers):
             cache = base if l == 0 else clone(base)
@@ -735,7 +738,8 @@ def decode_records(args, dev, wanted=lambda name: True):
                              q_rope=torch.from_numpy(q.q_rope).to(dev), sm_scale=W.SM_SCALE,
                              max_seq_len=int(L.max()), seq_fmt=torch.from_numpy(fmt).to(dev),
                              block_table=torch.from_numpy(table).to(dev), page_size=ps, causal=True,
-                             fp8=pools[F8], tq4=pools[T4], signs=signs, impl=args.decode_impl)
+                             fp8=pools[F8], tq4=pools[T4], signs=signs,
+                             impl=0 if args.decode_impl == 5 else args.decode_impl)
         rows_fp8 = int(L[fmt == 1].sum())
         rows_tq4 = int(L[fmt == 2].sum())
         rows = rows_fp8 + rows_tq4

@@ -89,7 +89,7 @@ const char* kvq_last_error(void);
 int kvq_set_fault(const char* spec);
 
 /*
- * Test hook for the failure path of the tensor-core decode kernels (impl 2 and 4).  Every
+ * Test hook for the failure path of the tensor-core decode kernels (impl 2, 4 and 5).  Every
  * wait in their pipelines (for a copy, an MMA or another warp's hand-over) gives up after
  * `ns` nanoseconds of %globaltimer time; ns = 0 restores the default of 2 s.  The limit
  * is process-wide and read at each launch.  A CTA that gives up sets KVQ_DEV_TIMEOUT in
@@ -254,7 +254,10 @@ int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream);
  * kvq_encode_tq) in the rotated domain (the page's identity q . xhat = rot(q) . yhat;
  * the combine unrotates the output).  The tensor-core kernels read FP8 and TQ4 rows, and
  * impl 4 also a problem of one 3- or 6-bit format (impl 2 or 3 with such a `fmt` is
- * refused with KVQ_EFORMAT); in a seq_fmt batch on a tensor-core kernel the 3- and 6-bit
+ * refused with KVQ_EFORMAT); impl 5 reads problems of FP8 rows only (any other `fmt`, or
+ * a seq_fmt batch, is refused with KVQ_EFORMAT) and keeps the codes in e4m3 inside the
+ * tensor core, carrying q and the softmax weights as sums of 5 and 4 e4m3 values of
+ * decreasing power-of-two weight; in a seq_fmt batch on a tensor-core kernel the 3- and 6-bit
  * sequences set KVQ_DEV_BAD_FORMAT (use impl 1 for such batches).  Admissible rows of
  * query j of sequence i (holding L = seq_len[i] rows): t < L; with `causal`,
  * t <= L - n_q + j (draft + verify); with idx, only t in idx[i][j][:] (an index
@@ -287,7 +290,10 @@ typedef struct kvq_mla_problem {
                                        2: tensor-core (tcgen05) kernel, 32 heads a CTA;
                                        3: warp-level MMA kernel, 16 heads a CTA;
                                        4: tcgen05 kernel, 16 heads a CTA, each code
-                                          converted to binary16 once                     */
+                                          converted to binary16 once;
+                                       5: tcgen05 kernel of the fp8 tier, 16 heads a
+                                          CTA, e4m3 codes read by the tensor core as
+                                          they are (kind::f8f6f4)                        */
 } kvq_mla_problem;
 
 /* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */
@@ -296,8 +302,10 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
 /*
  * The decode kernel kvq_mla_decode runs for this problem: 1 the CUDA-core kernel, 2 the
  * tcgen05 kernel with 32 heads a CTA, 3 the warp-level MMA kernel, 4 the tcgen05 kernel
- * with 16 heads a CTA and each code converted once; `impl` when it is non-zero, else the
- * library's choice (fp8 problems of at most 16 heads or with a top-k list: 3; TQ4
+ * with 16 heads a CTA and each code converted once, 5 the e4m3 tcgen05 kernel of the fp8
+ * tier; `impl` when it is non-zero, else the library's choice (fp8 problems of 8 to 16
+ * heads without a top-k list: 5; other fp8 problems of at most 16 heads or with a top-k
+ * list: 3; TQ4
  * problems of 8 to 16 heads and 3- or 6-bit problems of 8 or more heads: 4; other
  * problems of 8 or more heads: 2; the rest: 1).  Host
  * only, nothing enqueued.  An invalid problem returns the negated status

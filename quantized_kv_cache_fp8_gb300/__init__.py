@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 
 FMT_FP8, FMT_TQ4, FMT_Q4_0, FMT_TQ6, FMT_TQ3 = 1, 2, 3, 4, 5
 TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code width
-IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16 = 0, 1, 2, 3, 4
+IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16, IMPL_TCF8 = 0, 1, 2, 3, 4, 5
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
           5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED", 8: "KVQ_EMISMATCH",
@@ -300,7 +300,7 @@ def kvq_mla_decode_workspace(p: MlaProblem) -> int:
 
 
 def kvq_mla_decode_kernel(p: MlaProblem) -> int:
-    """The kernel kvq_mla_decode runs for p: IMPL_SIMT, IMPL_TC, IMPL_MMA or IMPL_TC16."""
+    """The kernel kvq_mla_decode runs for p: IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16 or IMPL_TCF8."""
     r = lib().kvq_mla_decode_kernel(C.byref(p))
     if r < 0:
         _check(-r)

@@ -24,6 +24,7 @@ UNITS = {
     "kvq_decode.cu": [],
     "kvq_decode_tc.cu": [],
     "kvq_decode_tc16.cu": [],
+    "kvq_decode_tcf8.cu": [],
     "kvq_decode_mma.cu": [],
     "kvq_noalloc.cu": [],
     "kvq_q4_decode.cu": [],

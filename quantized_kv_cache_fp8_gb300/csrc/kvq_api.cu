@@ -250,12 +250,14 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
     if (p->n_q < 1 || p->n_heads < 1 || p->max_seq_len < 0 || p->split_rows < 0)
         return fail(KVQ_EINVAL, "%s: bad sizes", E);
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
-    if (p->impl < 0 || p->impl > 4) return fail(KVQ_EINVAL, "%s: impl must be 0..4", E);
+    if (p->impl < 0 || p->impl > 5) return fail(KVQ_EINVAL, "%s: impl must be 0..5", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
         return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);
     if ((p->impl == 2 || p->impl == 3) && !p->seq_fmt && (p->fmt == KVQ_FMT_TQ3 || p->fmt == KVQ_FMT_TQ6))
         return fail(KVQ_EFORMAT, "%s: impl 2 and 3 read FP8 and TQ4 rows only", E);
+    if (p->impl == 5 && (p->seq_fmt || p->fmt != KVQ_FMT_FP8))
+        return fail(KVQ_EFORMAT, "%s: impl 5 reads FP8 rows only (one format, no seq_fmt)", E);
     if (p->n_seq == 0) return KVQ_OK;
     if (!p->seq_len || !p->q_lat || !p->q_rope) return fail(KVQ_EINVAL, "%s: NULL pointer", E);
     const bool need_fp8 = p->seq_fmt || p->fmt == KVQ_FMT_FP8;
@@ -293,7 +295,7 @@ int kvq_mla_decode_kernel(const kvq_mla_problem* p)
     if (int st = validate_decode(p, "kvq_mla_decode_kernel")) return -st;
     kvq::DecodePlan plan;
     kvq::plan_decode(*p, plan);
-    return plan.tc16 ? 4 : plan.mma ? 3 : plan.tc ? 2 : 1;
+    return plan.tcf8 ? 5 : plan.tc16 ? 4 : plan.mma ? 3 : plan.tc ? 2 : 1;
 }
 
 }  // extern "C"

@@ -581,22 +581,24 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const int64_t n_sm = sm_count();
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
-    // The library's choice (impl 0), by measurement on GB300: fp8 problems of at most 16
-    // heads, or with a top-k index list, run on the warp-level MMA kernel (16 heads a CTA,
-    // each code converted once); TQ4 problems of 8 to 16 heads, and 3- and 6-bit problems
+    // The library's choice (impl 0), by measurement on GB300: fp8 problems of 8 to 16 heads
+    // without a top-k list run on the e4m3 tcgen05 kernel (codes read as they are); other
+    // fp8 problems of at most 16 heads, or with a top-k index list, on the warp-level MMA
+    // kernel (16 heads a CTA, each code converted once); TQ4 problems of 8 to 16 heads, and 3- and 6-bit problems
     // of 8 or more heads, on the 16-head tcgen05 kernel (each code converted once); other
     // problems of 8 or more heads on the 32-head tcgen05 kernel; below 8 heads the
     // CUDA-core kernel.
     const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
     const bool uniform_tq4 = !p.seq_fmt && p.fmt == KVQ_FMT_TQ4;
     const bool uniform_tqb = !p.seq_fmt && (p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6);
-    plan.tc16 = p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
-                                ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb));
-    plan.mma = p.impl == 3 || (p.impl == 0 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
-    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
+    plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && p.n_heads <= 16 && !p.idx);
+    plan.tc16 = !plan.tcf8 && (p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
+                                ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb)));
+    plan.mma = p.impl == 3 || (p.impl == 0 && !plan.tcf8 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
+    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.tcf8 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
                               !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
     int64_t split_rows = p.split_rows;
-    if (plan.tc16) {
+    if (plan.tc16 || plan.tcf8) {
         constexpr int kHeads = 16;
         plan.head_block = kHeads;
         const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeads - 1) / kHeads));
@@ -629,7 +631,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.off_qrot = off;
     off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
     plan.off_qimg = off;
-    off += plan.tc ? tc_q_image_bytes(p) : plan.tc16 ? tc16_q_image_bytes(p) : 0;
+    off += plan.tc ? tc_q_image_bytes(p) : plan.tc16 ? tc16_q_image_bytes(p) : plan.tcf8 ? tcf8_q_image_bytes(p) : 0;
     plan.off_ml = off;
     off += align256(rows * plan.n_splits * 2 * sizeof(float));
     plan.off_o = off;
@@ -656,9 +658,15 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.status = dev_status;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
-    if (any_tq4 && !plan.tc && !plan.mma) {
+    if (any_tq4 && !plan.tc && !plan.mma && !plan.tcf8) {
         int64_t g = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
+    }
+    if (plan.tcf8) {
+        cudaError_t e = launch_mla_decode_tcf8(p, plan, base + plan.off_qimg, a.part_ml, a.part_o,
+                                               dev_status, s);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }
     if (plan.tc16) {
         cudaError_t e = launch_mla_decode_tc16(p, plan, base + plan.off_qimg, a.part_ml, a.part_o,

@@ -190,6 +190,7 @@ cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
 
 struct DecodePlan {
+    bool tcf8 = false;      // tensor-core (tcgen05 kind::f8f6f4) kernel of the fp8 tier, 16 heads a CTA
     bool tc16 = false;      // tensor-core (tcgen05) kernel, 16 heads a CTA, codes converted once
     bool tc = false;        // tensor-core (tcgen05) kernel, 32 heads a CTA
     bool mma = false;       // warp-level MMA kernel (blocks of 16 heads)
@@ -204,6 +205,9 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
                               float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
 size_t tc_q_image_bytes(const kvq_mla_problem& p);
 size_t tc16_q_image_bytes(const kvq_mla_problem& p);
+size_t tcf8_q_image_bytes(const kvq_mla_problem& p);
+cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
+                                   float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
                                    float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,

@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// L2 prefetch of the box at (x, y) of `map` (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
     uint32_t d;
@@ -210,14 +219,14 @@ __device__ __forceinline__ void tqb_codes_to_half(const uint4 (&raw)[4], const u
     }
 }
 
-// max (or sum) over the warp's 32 lanes of each of NV values (NV = 16 or 32), transposed:
+// max (or sum) over the warp's 32 lanes of each of NV values (NV = 4, 8, 16 or 32), transposed:
 // on return v[0] of lane l holds the result for value index l % NV.  The stages that
 // halve the value count exchange halves between lane pairs (NV - 1 shuffles in all);
 // with NV < 32 the remaining lane bits are folded with plain xor shuffles of v[0].
 template <bool kMax, int NV>
 __device__ __forceinline__ void warp_reduce_transpose(float (&v)[NV], int lane)
 {
-    static_assert(NV == 16 || NV == 32, "16 or 32 values");
+    static_assert(NV == 4 || NV == 8 || NV == 16 || NV == 32, "4, 8, 16 or 32 values");
 #pragma unroll
     for (int w = NV / 2; w >= 1; w >>= 1) {
         const bool up = (lane & w) != 0;
@@ -250,8 +259,9 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes] (64-byte boxes 64B-swizzled,
-// 32-byte boxes 32B-swizzled, 48-byte boxes unswizzled); rows past n_rows read as 0
+// [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes] (128-byte boxes
+// 128B-swizzled, 64-byte boxes 64B-swizzled, 32-byte boxes 32B-swizzled, 48-byte boxes
+// unswizzled); rows past n_rows read as 0
 inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes)
 {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -262,7 +272,8 @@ inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, 
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE,
-               box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+               box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+               : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                : box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -88,13 +88,15 @@ def _problem(kvq, **kw):
 
 
 def test_decode_kernel_choice(kvq):
-    """Which kernel kvq_mla_decode runs (host only): fp8 with at most 16 heads or a top-k
+    """Which kernel kvq_mla_decode runs (host only): fp8 with 8 to 16 heads and no top-k
+    list on the e4m3 tcgen05 kernel, other fp8 problems of at most 16 heads or with a top-k
     list on the warp-level MMA kernel, TQ4 with 8 to 16 heads and the 3- and 6-bit tiers
     with 8+ heads on the 16-head tcgen05 kernel, other problems of 8+ heads on the
     32-head tcgen05 kernel, the rest on CUDA cores; an explicit impl wins."""
     fp8 = dict(fmt=kvq.FMT_FP8, fp8=kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768))
     k = lambda **kw: kvq.kvq_mla_decode_kernel(_problem(kvq, **kw))
-    assert k(n_heads=16, **fp8) == kvq.IMPL_MMA
+    assert k(n_heads=16, **fp8) == kvq.IMPL_TCF8
+    assert k(n_heads=8, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=4, **fp8) == kvq.IMPL_MMA
     assert k(n_heads=64, **fp8) == kvq.IMPL_TC
     assert k(n_heads=128, idx=FAKE, top_k=2048, **fp8) == kvq.IMPL_MMA
@@ -108,8 +110,13 @@ def test_decode_kernel_choice(kvq):
     assert k(n_heads=4, fmt=kvq.FMT_TQ6) == kvq.IMPL_SIMT
     for impl in (1, 2, 3, 4):
         assert k(n_heads=16, impl=impl) == impl
+    for impl in (1, 2, 3, 4, 5):
+        assert k(n_heads=16, impl=impl, **fp8) == impl
     with pytest.raises(kvq.KvqError) as e:
         k(fmt=kvq.FMT_TQ6, impl=3)
+    assert e.value.status == 3
+    with pytest.raises(kvq.KvqError) as e:                                # TQ4 rows
+        k(n_heads=16, impl=5)
     assert e.value.status == 3
     assert kvq.lib().kvq_mla_decode_kernel(C.byref(_problem(kvq, d_lat=256))) == -1
 
@@ -128,7 +135,10 @@ def test_decode_argument_errors(kvq):
     assert dec(_problem(kvq, tq4_signs=None)) == 1
     assert dec(_problem(kvq, q_lat=FAKE + 4)) == 4
     assert dec(_problem(kvq, n_seq=2, seq_stride_rows=100)) == 1
-    assert dec(_problem(kvq, impl=5)) == 1                                       # 0 .. 4 only
+    assert dec(_problem(kvq, impl=6)) == 1                                       # 0 .. 5 only
+    assert dec(_problem(kvq, impl=5)) == 3                                       # fp8 rows only
+    for fmt in (kvq.FMT_TQ3, kvq.FMT_TQ6):
+        assert dec(_problem(kvq, fmt=fmt, impl=5)) == 3
     assert dec(_problem(kvq, impl=-1)) == 1
     p = _problem(kvq)
     need = L.kvq_mla_decode_workspace(C.byref(p))

@@ -12,7 +12,8 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-IMPLS = pytest.mark.parametrize("impl", [1, 2, 3, 4], ids=["cudacore", "tcgen05", "mma", "tcgen05x16"])
+IMPLS = pytest.mark.parametrize("impl", [1, 2, 3, 4, 5],
+                                ids=["cudacore", "tcgen05", "mma", "tcgen05x16", "tcgen05f8"])
 
 
 @pytest.fixture(scope="module")
@@ -39,6 +40,8 @@ def encode(orc, rows, fmt, signs=None):
 def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=None,
             seq_fmt=None, idx=None, causal=False, block_table=None, page_size=0,
             seq_stride_rows=0, split_rows=0, max_seq_len=None, impl=0):
+    if impl == 5 and (cache_fmt != 1 or seq_fmt is not None):
+        pytest.skip("impl 5 reads problems of fp8 rows only")
     dcaches = {f: {k: dev(v) for k, v in c.items()} for f, c in caches.items()}
     n_seq, n_q, H, _ = q.q_lat.shape
     p = kvq.make_problem(
