@@ -581,7 +581,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const int64_t n_sm = sm_count();
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
-    // The library's choice (impl 0), by measurement on GB300: fp8 problems of 8 to 16 heads
+    // The library's choice (impl 0), by measurement on GB300: fp8 problems of 8 or more heads
     // without a top-k list run on the e4m3 tcgen05 kernel (codes read as they are); other
     // fp8 problems of at most 16 heads, or with a top-k index list, on the warp-level MMA
     // kernel (16 heads a CTA, each code converted once); TQ4 problems of 8 to 16 heads, and 3- and 6-bit problems
@@ -591,7 +591,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
     const bool uniform_tq4 = !p.seq_fmt && p.fmt == KVQ_FMT_TQ4;
     const bool uniform_tqb = !p.seq_fmt && (p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6);
-    plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && p.n_heads <= 16 && !p.idx);
+    plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && !p.idx);
     plan.tc16 = !plan.tcf8 && (p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
                                 ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb)));
     plan.mma = p.impl == 3 || (p.impl == 0 && !plan.tcf8 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));

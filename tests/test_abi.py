@@ -88,7 +88,7 @@ def _problem(kvq, **kw):
 
 
 def test_decode_kernel_choice(kvq):
-    """Which kernel kvq_mla_decode runs (host only): fp8 with 8 to 16 heads and no top-k
+    """Which kernel kvq_mla_decode runs (host only): fp8 with 8 or more heads and no top-k
     list on the e4m3 tcgen05 kernel, other fp8 problems of at most 16 heads or with a top-k
     list on the warp-level MMA kernel, TQ4 with 8 to 16 heads and the 3- and 6-bit tiers
     with 8+ heads on the 16-head tcgen05 kernel, other problems of 8+ heads on the
@@ -98,7 +98,7 @@ def test_decode_kernel_choice(kvq):
     assert k(n_heads=16, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=8, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=4, **fp8) == kvq.IMPL_MMA
-    assert k(n_heads=64, **fp8) == kvq.IMPL_TC
+    assert k(n_heads=64, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=128, idx=FAKE, top_k=2048, **fp8) == kvq.IMPL_MMA
     assert k(n_heads=64) == kvq.IMPL_TC                                   # TQ4
     assert k(n_heads=16) == kvq.IMPL_TC16

@@ -181,6 +181,50 @@ def test_decode_ragged_mixed_small(kvq, orc, impl):
     check(out, lse, ref, ref_lse)
 
 
+@IMPLS
+def test_decode_fp8_paged_causal_batch(kvq, orc, impl):
+    """fp8 rows only, paged (page size 64, seeded permuted table), 4 causal queries per
+    sequence, 20 heads (a full and a partial group of 16); lengths 0, 1, 3, 650, 1300."""
+    L = np.array([0, 1, 3, 650, 1300], np.int32)
+    ps, n_q, H = 64, 4, 20
+    pages = (L + ps - 1) // ps
+    total = int(pages.sum())
+    perm = np.random.default_rng(41).permutation(total).astype(np.int32)
+    table = np.full((len(L), int(pages.max())), -1, np.int32)
+    o = 0
+    for i, n in enumerate(pages):
+        table[i, :n] = perm[o:o + n]
+        o += n
+    rows = W.magnitude_rows(total * ps, seed=41, lo=1e-2, hi=10.0)
+    cache = encode(orc, rows, 1)
+    q = W.queries(len(L), n_q, H, seed=41)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=L, q=q, causal=True,
+                           block_table=table, page_size=ps)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=L, seq_fmt=np.ones(len(L), np.int32), q_lat=q.q_lat,
+                                     q_rope=q.q_rope, sm_scale=W.SM_SCALE, causal=True, block_table=table,
+                                     page_size=ps, fp8=cache)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@IMPLS
+def test_decode_fp8_strided_sequences(kvq, orc, impl):
+    """fp8 rows only, three sequences in one pool at a stride of 2048 rows (contiguous:
+    the TMA path), lengths 2048, 1500 and 777, 2 causal queries, 16 heads."""
+    L = np.array([2048, 1500, 777], np.int32)
+    stride, n_q, H = 2048, 2, 16
+    rows = W.magnitude_rows(stride * len(L), seed=43, lo=1e-3, hi=40.0)
+    cache = encode(orc, rows, 1)
+    q = W.queries(len(L), n_q, H, seed=43)
+    out, lse, st = run_gpu(kvq, impl=impl, cache_fmt=1, caches={1: cache}, seq_len=L, q=q, causal=True,
+                           seq_stride_rows=stride)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=L, seq_fmt=np.ones(len(L), np.int32), q_lat=q.q_lat,
+                                     q_rope=q.q_rope, sm_scale=W.SM_SCALE, causal=True, seq_stride_rows=stride,
+                                     fp8=cache)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
 @pytest.mark.slow
 @IMPLS
 def test_decode_ragged_workload(kvq, orc, impl):
