@@ -658,7 +658,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.status = dev_status;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
-    if (any_tq4 && !plan.tc && !plan.mma && !plan.tcf8) {
+    if (any_tq4 && !plan.tc && !plan.mma && !plan.tcf8 && !plan.tc16) {   // read by the CUDA-core kernel only
         int64_t g = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
     }
