@@ -304,8 +304,8 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
  * tcgen05 kernel with 32 heads a CTA, 3 the warp-level MMA kernel, 4 the tcgen05 kernel
  * with 16 heads a CTA and each code converted once, 5 the e4m3 tcgen05 kernel of the fp8
  * tier; `impl` when it is non-zero, else the library's choice (fp8 problems of 8 or more
- * heads without a top-k list: 5; other fp8 problems of at most 16 heads or with a top-k
- * list: 3; TQ4
+ * heads without a top-k list and with n_seq * n_q * ceil(H / 16) * ceil(rows / 128) >= 64:
+ * 5; other fp8 problems of at most 16 heads or with a top-k list: 3; TQ4
  * problems of 8 to 16 heads and 3- or 6-bit problems of 8 or more heads: 4; other
  * problems of 8 or more heads: 2; the rest: 1).  Host
  * only, nothing enqueued.  An invalid problem returns the negated status

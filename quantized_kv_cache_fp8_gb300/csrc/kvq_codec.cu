@@ -9,6 +9,8 @@
 // input, shuffles for the Walsh-Hadamard butterflies and the row reductions, and
 // 16-byte stores of the packed output staged through shared memory.
 #include <cuda_fp16.h>
+
+#include <atomic>
 #include <cuda_fp8.h>
 
 #include "kvq_internal.cuh"
@@ -798,9 +800,20 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
         case 256:  encode_tq4_kernel<8><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         case 512:
             if ((uintptr_t)x % 16 == 0 && ldx % 4 == 0) {
-                // one wave (four CTAs of eight warps per SM), each warp many rows
+                // one wave (as many CTAs of eight warps as fit on every SM at once), each
+                // warp many rows: a second, partial wave would double the time of its CTAs
+                static std::atomic<int> per_sm{0};
+                int n = per_sm.load();
+                if (n <= 0) {
+                    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_tq4_512_kernel, kCodecThreads, 0) !=
+                            cudaSuccess || n <= 0) {
+                        (void)cudaGetLastError();
+                        n = 1;
+                    }
+                    per_sm.store(n);
+                }
                 const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kCodecWarps - 1) / kCodecWarps,
-                                                                           (int64_t)sm_count() * 4));
+                                                                           (int64_t)sm_count() * n));
                 encode_tq4_512_kernel<<<g1, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, vec);
             }
             else

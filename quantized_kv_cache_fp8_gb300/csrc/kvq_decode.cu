@@ -582,7 +582,8 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)p.max_seq_len;
     plan.n_cand_max = (int)n_cand;
     // The library's choice (impl 0), by measurement on GB300: fp8 problems of 8 or more heads
-    // without a top-k list run on the e4m3 tcgen05 kernel (codes read as they are); other
+    // without a top-k list and with at least 64 tile-units of work run on the e4m3 tcgen05
+    // kernel (codes read as they are); other
     // fp8 problems of at most 16 heads, or with a top-k index list, on the warp-level MMA
     // kernel (16 heads a CTA, each code converted once); TQ4 problems of 8 to 16 heads, and 3- and 6-bit problems
     // of 8 or more heads, on the 16-head tcgen05 kernel (each code converted once); other
@@ -591,7 +592,11 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     const bool uniform_fp8 = !p.seq_fmt && p.fmt == KVQ_FMT_FP8;
     const bool uniform_tq4 = !p.seq_fmt && p.fmt == KVQ_FMT_TQ4;
     const bool uniform_tqb = !p.seq_fmt && (p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6);
-    plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && !p.idx);
+    // the e4m3 kernel's start-up (one CTA per SM, a 72 KB tile in flight before the first
+    // score) pays off from 64 tile-units of work (T = 1024, 16 heads: 8 units, the
+    // warp-level MMA kernel is faster; T = 32768: 256 units, the e4m3 kernel is)
+    const int64_t tcf8_units = (int64_t)p.n_seq * p.n_q * ((p.n_heads + 15) / 16) * ((n_cand + 127) / 128);
+    plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && !p.idx && tcf8_units >= 64);
     plan.tc16 = !plan.tcf8 && (p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
                                 ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb)));
     plan.mma = p.impl == 3 || (p.impl == 0 && !plan.tcf8 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));

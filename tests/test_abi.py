@@ -88,8 +88,9 @@ def _problem(kvq, **kw):
 
 
 def test_decode_kernel_choice(kvq):
-    """Which kernel kvq_mla_decode runs (host only): fp8 with 8 or more heads and no top-k
-    list on the e4m3 tcgen05 kernel, other fp8 problems of at most 16 heads or with a top-k
+    """Which kernel kvq_mla_decode runs (host only): fp8 with 8 or more heads, no top-k
+    list and at least 64 tile-units of work on the e4m3 tcgen05 kernel, other fp8 problems
+    of at most 16 heads or with a top-k
     list on the warp-level MMA kernel, TQ4 with 8 to 16 heads and the 3- and 6-bit tiers
     with 8+ heads on the 16-head tcgen05 kernel, other problems of 8+ heads on the
     32-head tcgen05 kernel, the rest on CUDA cores; an explicit impl wins."""
@@ -97,6 +98,9 @@ def test_decode_kernel_choice(kvq):
     k = lambda **kw: kvq.kvq_mla_decode_kernel(_problem(kvq, **kw))
     assert k(n_heads=16, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=8, **fp8) == kvq.IMPL_TCF8
+    assert k(n_heads=16, max_seq_len=1024, **fp8) == kvq.IMPL_MMA           # 8 tile-units
+    assert k(n_heads=16, max_seq_len=8192, **fp8) == kvq.IMPL_TCF8          # 64
+    assert k(n_heads=16, max_seq_len=1024, n_seq=8, seq_stride_rows=1024, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=4, **fp8) == kvq.IMPL_MMA
     assert k(n_heads=64, **fp8) == kvq.IMPL_TCF8
     assert k(n_heads=128, idx=FAKE, top_k=2048, **fp8) == kvq.IMPL_MMA
