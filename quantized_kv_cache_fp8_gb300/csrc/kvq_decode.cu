@@ -636,7 +636,7 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     plan.off_qrot = off;
     off += any_tq4 ? align256(rows * kDLat * sizeof(float)) : 0;
     plan.off_qimg = off;
-    off += plan.tc ? tc_q_image_bytes(p) : plan.tc16 ? tc16_q_image_bytes(p) : plan.tcf8 ? tcf8_q_image_bytes(p) : 0;
+    off += plan.tc ? tc_q_image_bytes(p) : plan.tc16 ? tc16_q_image_bytes(p) : 0;
     plan.off_ml = off;
     off += align256(rows * plan.n_splits * 2 * sizeof(float));
     plan.off_o = off;
@@ -668,8 +668,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
     }
     if (plan.tcf8) {
-        cudaError_t e = launch_mla_decode_tcf8(p, plan, base + plan.off_qimg, a.part_ml, a.part_o,
-                                               dev_status, s);
+        cudaError_t e = launch_mla_decode_tcf8(p, plan, a.part_ml, a.part_o, dev_status, s);
         if (e != cudaSuccess) return e;
         return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }

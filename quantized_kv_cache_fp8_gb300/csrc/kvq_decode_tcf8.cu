@@ -119,7 +119,6 @@ struct F8Args {
     int use_tma;                         // contiguous rows: tiles arrive by TMA
     kvq_mla_problem p;
     int split_rows, n_splits, n_hg;      // n_hg: head groups of 16
-    uint8_t* q_img;                      // [n_seq][n_q][n_hg][kQBytes]
     float* part_ml;
     float* part_o;
     uint32_t* status;
@@ -128,69 +127,59 @@ struct F8Args {
 
 
 // ------------------------------------------------------------------------------------
-// Q digit image per (sequence, query, head group): the B operand of the score MMA,
+// Q digit image of the CTA's 16 heads in shared memory: the B operand of the score MMA,
 // K-major, rows n = 16 j + head (digit j).  Latent k in four 128B-swizzled blocks
 // [80 x 128 B], rope k in one 64B-swizzled block [80 x 64 B], then 2^-sigma_h per head.
 // sigma_h puts max|q_h| in [128, 256): Qd_0 = RN(q 2^sigma), Qd_{j+1} = RN(16 (x_j - Qd_j))
-// with x_j the scaled residual (all exact in fp32).  One warp per head; heads past
-// n_heads are zero rows.  The decode kernel, launched as its dependent, loads its first
-// tiles meanwhile.
+// with x_j the scaled residual (all exact in fp32).  One softmax warp per head: its 18
+// values a lane are loaded first thing in the CTA (ahead of the tile loads, which would
+// otherwise queue in front of them), the digits written once the tiles are on their way.
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) q_digits_kernel(F8Args a)
+__device__ __forceinline__ void load_q_head(const kvq_mla_problem& p, int64_t qrow, int h, int lane, float (&y)[18])
 {
-    grid_dependents_launch();                    // the decode may start loading codes
-    const kvq_mla_problem& p = a.p;
-    const int lane = threadIdx.x & 31;
-    const int64_t n_items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t it = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; it < n_items; it += n_warps) {
-        const int n = (int)(it % kGQ);
-        const int64_t grp = it / kGQ;
-        const int hg = (int)(grp % a.n_hg);
-        const int64_t sq = grp / a.n_hg;
-        const int h = hg * kGQ + n;
-        float y[18];
-        if (h < p.n_heads) {
-            const int64_t r = sq * p.n_heads + h;
+    if (h < p.n_heads) {
+        const int64_t r = qrow + h;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) y[j] = p.q_lat[r * kDLat + j * 32 + lane];
-            y[16] = p.q_rope[r * kDRope + lane];
-            y[17] = p.q_rope[r * kDRope + 32 + lane];
-        } else {
+        for (int j = 0; j < 16; ++j) y[j] = p.q_lat[r * kDLat + j * 32 + lane];
+        y[16] = p.q_rope[r * kDRope + lane];
+        y[17] = p.q_rope[r * kDRope + 32 + lane];
+    } else {
 #pragma unroll
-            for (int j = 0; j < 18; ++j) y[j] = 0.0f;
-        }
-        float mx = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 18; ++j) mx = fmaxf(mx, fabsf(y[j]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-        int e = 0;
-        (void)frexpf(mx, &e);                    // mx < 2^e
-        const int sigma = mx > 0.0f ? std::min(100, std::max(-100, 8 - e)) : 0;
-        const float scale = ldexpf(1.0f, sigma);
-        uint8_t* img = a.q_img + grp * (int64_t)kQBytes;
-#pragma unroll
-        for (int j = 0; j < 18; ++j) {
-            float x = y[j] * scale;
-            const int k = (j & 15) * 32 + lane;  // latent dim (j < 16) or rope dim (j >= 16)
-#pragma unroll
-            for (int d = 0; d < kDQ; ++d) {
-                const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-                const int row = 16 * d + n;
-                uint8_t* dst;
-                if (j < 16) {
-                    const int kk = k & 127;
-                    dst = img + (k >> 7) * kQBlk + row * 128 + (((kk >> 4) ^ (row & 7)) << 4) + (kk & 15);
-                } else {
-                    dst = img + kQRope + row * 64 + (((k >> 4) ^ ((row >> 1) & 3)) << 4) + (k & 15);
-                }
-                *dst = c;
-                x = (x - __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)))) * 16.0f;
-            }
-        }
-        if (lane == 0) reinterpret_cast<float*>(img + kQScale)[n] = ldexpf(1.0f, -sigma);
+        for (int j = 0; j < 18; ++j) y[j] = 0.0f;
     }
+}
+
+__device__ __forceinline__ void write_q_digits(const float (&y)[18], int n, int lane, uint8_t* img)
+{
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 18; ++j) mx = fmaxf(mx, fabsf(y[j]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    int e = 0;
+    (void)frexpf(mx, &e);                        // mx < 2^e
+    const int sigma = mx > 0.0f ? std::min(100, std::max(-100, 8 - e)) : 0;
+    const float scale = ldexpf(1.0f, sigma);
+#pragma unroll
+    for (int j = 0; j < 18; ++j) {
+        float x = y[j] * scale;
+        const int k = (j & 15) * 32 + lane;      // latent dim (j < 16) or rope dim (j >= 16)
+#pragma unroll
+        for (int d = 0; d < kDQ; ++d) {
+            const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+            const int row = 16 * d + n;
+            uint8_t* dst;
+            if (j < 16) {
+                const int kk = k & 127;
+                dst = img + (k >> 7) * kQBlk + row * 128 + (((kk >> 4) ^ (row & 7)) << 4) + (kk & 15);
+            } else {
+                dst = img + kQRope + row * 64 + (((k >> 4) ^ ((row >> 1) & 3)) << 4) + (k & 15);
+            }
+            *dst = c;
+            x = (x - __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)))) * 16.0f;
+        }
+    }
+    if (lane == 0) reinterpret_cast<float*>(img + kQScale)[n] = ldexpf(1.0f, -sigma);
 }
 
 struct Shared {
@@ -378,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
             mbar_init(sh.o_done(), 1);
             mbar_init(sh.drain_s(), 1);
             mbar_init(sh.drain_c(), 1);
-            mbar_init(sh.q_full(), 1);
+            mbar_init(sh.q_full(), kSmx);            // one arrival per softmax warp (= head)
             *sh.abort_flag() = 0;
             fence_mbar_init();
         }
@@ -390,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
         sh.m_s()[tid] = -INFINITY;
         sh.m_u()[tid] = -INFINITY;
     }
+    static_assert(kSmx == kGQ, "one softmax warp per head builds the query digits");
+    float qv[18];
+    if (warp < kSmx) load_q_head(p, qrow, h0 + warp, lane, qv);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -418,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
         const int wx = (t >> 1) & 3;
         float l_lane = 0.0f;                          // sum of p over this warp's rows, head hb + gl
         float G[kGH];                                 // tau2 2^-sigma_h
+        write_q_digits(qv, warp, lane, sh.q());
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sh.q_full());
         bool ok = wait_bar<kSmxSpin>(sh, sh.q_full(), 0u, a.status, a.wait_ns);
         ok = __all_sync(kFull, ok);
         {
@@ -763,13 +759,6 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
         const bool leader = elect_one();
         constexpr uint32_t idesc_s = idesc_e4m3_f32(kRT, kNS, false, false);   // C . Qd^T
         const uint32_t q_addr = smem_u32(sh.q());
-        grid_dependency_wait();                 // the Q image comes from the kernel before
-        if (leader) {
-            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
-            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
-                          kQBytes, sh.q_full());
-        }
-        __syncwarp();
         bool ok = __all_sync(kFull, wait_bar<kRoleSpin>(sh, sh.q_full(), 0u, a.status, a.wait_ns));
         for (int i = 0; i < NT && ok; ++i) {
             const int st = i % kStages;
@@ -804,13 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
                 __syncwarp();
             }
         }
-        // drain: every MMA issued here completes before tensor memory is freed, and the Q
-        // copy has landed before the CTA's shared memory is released
+        // drain: every MMA issued here completes before tensor memory is freed
         if (leader) {
             mma_commit(sh.drain_s());
             if (!mbar_wait(sh.drain_s(), 0, kTimeoutNs) && a.status)
-                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
-            if (!mbar_wait(sh.q_full(), 0, kTimeoutNs) && a.status)
                 atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
         }
         __syncwarp();
@@ -860,14 +846,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
 
 }  // namespace
 
-size_t tcf8_q_image_bytes(const kvq_mla_problem& p)
-{
-    const size_t n_hg = (size_t)(p.n_heads + kGQ - 1) / kGQ;
-    return ((size_t)p.n_seq * p.n_q * n_hg * kQBytes + 255) & ~size_t(255);
-}
-
-cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
-                                   float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s)
+cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, float* part_ml,
+                                   float* part_o, uint32_t* dev_status, cudaStream_t s)
 {
     F8Args a;
     memset(&a, 0, sizeof(a));
@@ -878,14 +858,10 @@ cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& p
     a.split_rows = plan.split_rows;
     a.n_splits = plan.n_splits;
     a.n_hg = (p.n_heads + kGQ - 1) / kGQ;
-    a.q_img = static_cast<uint8_t*>(q_img);
     a.part_ml = part_ml;
     a.part_o = part_o;
     a.status = dev_status;
     a.wait_ns = wait_limit_ns();
-    const int64_t items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;
-    const int n_sm = sm_count();
-    q_digits_kernel<<<(int)std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, (int64_t)n_sm * 8)), 256, 0, s>>>(a);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
@@ -896,8 +872,14 @@ cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& p
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
-    dim3 grid(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
-    return launch_dependent(mla_decode_tcf8_kernel, grid, dim3(kThreads), kSmemBytes, s, a);
+    // an ordinary launch: the first kernel of the call reads the cache and the queries
+    // only after every kernel before it in the stream (an append, say) has completed
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, mla_decode_tcf8_kernel, a);
 }
 
 }  // namespace kvq

@@ -205,9 +205,8 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
                               float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
 size_t tc_q_image_bytes(const kvq_mla_problem& p);
 size_t tc16_q_image_bytes(const kvq_mla_problem& p);
-size_t tcf8_q_image_bytes(const kvq_mla_problem& p);
-cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
-                                   float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
+cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, float* part_ml,
+                                   float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
                                    float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,

@@ -2,8 +2,9 @@
 (an allocator or memory pool that owns the device, a loop that must not enter the
 allocator, an embedding handed only pre-placed buffers).  Its scratch is a fixed device
 array inside the library, so it takes no workspace.  Checked through the C ABI against
-kvq_mla_decode with a caller workspace, on two different problems called one after the
-other (the second call reuses the array the first one left behind).
+kvq_mla_decode with a caller workspace, on different problems called one after the other
+(each call reuses the array the one before left behind), and directly against the oracle
+on one of them.
 
 This file is named to be collected last; it must pass on its own in a fresh process as
 well as after every other test."""
@@ -39,9 +40,14 @@ def problem(kvq, orc, fmt, T, H, n_q, seed):
     cache = {k: dev(v) for k, v in dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs).items()}
     q = W.queries(1, n_q, H, seed=seed)
     kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=dev(signs))
-    return kvq.make_problem(seq_len=dev(np.array([T], np.int32)), q_lat=dev(q.q_lat),
-                            q_rope=dev(q.q_rope), sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt,
-                            causal=n_q > 1, **kw)
+    p = kvq.make_problem(seq_len=dev(np.array([T], np.int32)), q_lat=dev(q.q_lat),
+                         q_rope=dev(q.q_rope), sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt,
+                         causal=n_q > 1, **kw)
+    host = dict(lat=lat, lat_scale=ls, rope=rope, rope_scale=rs)
+    ref = lambda: orc.mla_decode(seq_len=np.array([T], np.int32), seq_fmt=np.array([fmt], np.int32),
+                                 q_lat=q.q_lat, q_rope=q.q_rope, sm_scale=W.SM_SCALE, causal=n_q > 1,
+                                 **(dict(fp8=host) if fmt == kvq.FMT_FP8 else dict(tq4=host, signs=signs)))
+    return p, ref
 
 
 def decode_both(kvq, p, with_lse=True):
@@ -60,12 +66,13 @@ def decode_both(kvq, p, with_lse=True):
 
 
 def test_noalloc_matches_workspace_decode_twice(kvq, orc):
-    # calls in a row, different problems, kernels and scratch footprints: the tcgen05
-    # kernel (TQ4, 64 heads), the warp-level MMA kernel (fp8, 16 heads, 3 causal
-    # queries) and the CUDA-core kernel (TQ4 forced to impl 1, no lse output)
+    # calls in a row, different problems, kernels and scratch footprints: the 32-head
+    # tcgen05 kernel (TQ4, 64 heads), the e4m3 kernel (fp8, 16 heads, 3 causal queries,
+    # also checked against the oracle), the warp-level MMA kernel (fp8, forced) and the
+    # CUDA-core kernel (TQ4 forced to impl 1, no lse output)
     for fmt, T, H, n_q, seed, impl in ((kvq.FMT_TQ4, 32768, 64, 1, 0, 0), (kvq.FMT_FP8, 5000, 16, 3, 1, 0),
-                                       (kvq.FMT_TQ4, 3000, 8, 1, 2, 1)):
-        p = problem(kvq, orc, fmt, T, H, n_q, seed)
+                                       (kvq.FMT_FP8, 3000, 16, 1, 3, 3), (kvq.FMT_TQ4, 3000, 8, 1, 2, 1)):
+        p, ref = problem(kvq, orc, fmt, T, H, n_q, seed)
         p.impl = impl
         with_lse = impl != 1
         out, lse, out_ref, lse_ref, st = decode_both(kvq, p, with_lse)
@@ -78,6 +85,12 @@ def test_noalloc_matches_workspace_decode_twice(kvq, orc):
             assert np.allclose(lse, lse_ref, rtol=2e-6, atol=1e-4)
         else:
             assert np.isnan(lse).all()                  # lse=None: nothing written there
+        if fmt == kvq.FMT_FP8 and n_q == 3:
+            # the fixed-array call on its own against the fp64 oracle
+            o_ref, l_ref, _ = ref()
+            o_ref = o_ref.reshape(out.shape)
+            assert np.all(np.abs(out - o_ref).max(axis=-1) <= 1e-4 * np.abs(o_ref).max(axis=-1))
+            assert np.allclose(lse, l_ref.reshape(lse.shape), rtol=2e-6, atol=1e-4)
 
 
 def test_noalloc_against_the_oracle(kvq, orc):
