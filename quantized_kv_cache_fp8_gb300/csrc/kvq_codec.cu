@@ -200,7 +200,65 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
 }
 
 // ------------------------------------------------------------------------------------
-// TQ4 encode of 512-wide rows, the MLA latent, with fewer instructions a row (same bytes):
+// The rotated tiers at 3 and 6 bits (colibri PR #399: KV_TQ=6, and 3 bits): the same row
+// transform and radius as TQ4, a 2^b-level codebook, and codes packed as a little-endian
+// bit stream (code i at bits b*i .. b*i + b - 1 of the row).  24 / b consecutive codes fill
+// 3 bytes: lanes combine them with a shuffle tree and the first lane of each group writes
+// the 3 bytes into shared memory, which the warp copies out with 16-byte stores.
+// ------------------------------------------------------------------------------------
+
+__constant__ TqCodebook<8> c_tq3 = kTq3;
+__constant__ TqCodebook<64> c_tq6 = kTq6;
+
+// 64 levels: instead of a six-step bisection, u is placed in one of 257 buckets
+// b = round-to-even(32 u + 128) (one fma against 1.5 * 2^23, exact), clamped to [0, 256];
+// kTq6Base[b] counts the thresholds below the bucket's lowest possible u (32 u + 128 =
+// b - 1/2), and no bucket, edges included, holds more than one threshold (checked below),
+// so the code is kTq6Base[b] + (u >= thr[kTq6Base[b]]).  thr[63] is +inf padding.
+struct Tq6Buckets {
+    uint8_t base[257];
+};
+
+constexpr Tq6Buckets tq6_buckets()
+{
+    Tq6Buckets r{};
+    for (int b = 0; b <= 256; ++b) {
+        int n = 0;
+        for (int k = 0; k < 63; ++k)
+            if (kTq6.thr[k] * 32.0f + 128.0f < (float)b - 0.5f) ++n;
+        r.base[b] = (uint8_t)n;
+    }
+    return r;
+}
+
+constexpr bool tq6_buckets_hold_one_threshold()
+{
+    for (int b = 0; b <= 256; ++b) {
+        int n = 0;
+        for (int k = 0; k < 63; ++k) {
+            const float v = kTq6.thr[k] * 32.0f + 128.0f;
+            if (v >= (float)b - 0.5f && v <= (float)b + 0.5f) ++n;
+        }
+        if (n > 1) return false;
+    }
+    // the clamped end buckets hold no threshold beyond their range
+    return kTq6.thr[0] * 32.0f + 128.0f > 0.5f && kTq6.thr[62] * 32.0f + 128.0f < 255.5f;
+}
+static_assert(tq6_buckets_hold_one_threshold(), "6-bit bucket table needs a finer grid");
+
+constexpr Tq6Buckets kTq6Buckets = tq6_buckets();
+__constant__ Tq6Buckets c_tq6_buckets = kTq6Buckets;
+
+template <int BITS>
+__device__ __forceinline__ const float* tq_thresholds()
+{
+    if constexpr (BITS == 3) return c_tq3.thr;
+    else return c_tq6.thr;
+}
+
+// ------------------------------------------------------------------------------------
+// Rotated-tier encode of 512-wide rows, the MLA latent, at 3, 4 or 6 bits, with fewer
+// instructions a row than the general kernels (same bytes):
 //  * lane l loads elements 16 l .. 16 l + 15 with 16-byte loads; the FWHT stages h = 1..8
 //    run in its registers; one transpose through shared memory (element i at i + i/16,
 //    conflict-free both ways) gives lane (bit 8 of i, bits 0-3) registers over bits 4-7,
@@ -210,38 +268,78 @@ encode_tq4_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
 //    ascending; its first eight terms sit in lane (0, l mod 16), the last eight in lane
 //    (1, l mod 16), which continues the lower lane's sum; the xor butterfly follows.
 //  * the code counts the thresholds at or below u = y / sigma.  u' = y * rcp(sigma) (both
-//    correctly rounded) is within 4.1e-6 of u (|u| <= sqrt 512).  Buckets of width 1/7,
-//    b = rn(7 u' + 160), hold at most one threshold and every threshold lies at least
-//    0.0138 from a bucket edge, so the code is base[b] + (u' >= thr[b]) unless u' is
-//    within 1e-5 of thr[b]; then the IEEE division decides, in the same bucket.
+//    correctly rounded) is within 4.1e-6 of u (|u| <= sqrt 512).  Buckets of width 1/S,
+//    b = rn(S u' + B), hold at most one threshold and every threshold lies at least 1e-3
+//    from a bucket edge (checked at compile time below), so u and u' share a bucket and
+//    the code is base[b] + (u' >= thr[b]) unless u' is within 1e-5 of thr[b]; then the
+//    IEEE quotient decides against the same threshold.
+//  * 4 bits: two codes a byte; 3 and 6 bits: 24 / b consecutive codes (consecutive lanes)
+//    combine into 3 bytes with a shuffle tree, code i at bits b i of the row's stream.
 // ------------------------------------------------------------------------------------
-struct Tq4Bucket {
+struct TqBucket {
     float thr;                 // the threshold inside the bucket, or +inf
     int base;                  // thresholds below the bucket
 };
-constexpr int kTq4Buckets = 320;
-constexpr float kTq4BucketScale = 7.0f;
-constexpr float kTq4BucketOffset = 160.0f;
-constexpr float kTq4Near = 1e-5f;
+constexpr float kTqNear = 1e-5f;
 
-__global__ void __launch_bounds__(kCodecThreads)
-encode_tq4_512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
-                      const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
-                      int64_t ldp, float* __restrict__ radius, bool vec_store)
+template <int BITS> struct Tq512Grid;
+template <> struct Tq512Grid<3> { static constexpr int n = 17;  static constexpr float scale = 4.0f;  static constexpr float off = 8.0f; };
+template <> struct Tq512Grid<4> { static constexpr int n = 320; static constexpr float scale = 7.0f;  static constexpr float off = 160.0f; };
+template <> struct Tq512Grid<6> { static constexpr int n = 129; static constexpr float scale = 16.0f; static constexpr float off = 64.0f; };
+
+// every threshold strictly inside the unclamped buckets, at least `margin` (in u) from a
+// bucket edge, and no two thresholds in one bucket
+template <int N>
+constexpr bool tq512_grid_ok(const float (&thr)[N], float scale, float off, int nb, double margin)
 {
-    __shared__ Tq4Bucket s_tab[kTq4Buckets];
+    long long prev = -1;
+    for (int k = 0; k < N; ++k) {
+        const double v = (double)thr[k] * scale + off;
+        if (v <= 0.5 + margin * scale || v >= nb - 1.5 - margin * scale) return false;
+        const double f = v - (double)(long long)v;
+        const double d = f > 0.5 ? f - 0.5 : 0.5 - f;
+        if (d < margin * scale) return false;
+        const long long bucket = (long long)(v + 0.5);
+        if (bucket == prev) return false;
+        prev = bucket;
+    }
+    return true;
+}
+static_assert(tq512_grid_ok(kTq3.thr, Tq512Grid<3>::scale, Tq512Grid<3>::off, Tq512Grid<3>::n, 1e-3), "3-bit grid");
+static_assert(tq512_grid_ok(kTq4Thresholds, Tq512Grid<4>::scale, Tq512Grid<4>::off, Tq512Grid<4>::n, 1e-3), "4-bit grid");
+static_assert(tq512_grid_ok(kTq6.thr, Tq512Grid<6>::scale, Tq512Grid<6>::off, Tq512Grid<6>::n, 1e-3), "6-bit grid");
+
+template <int BITS>
+__device__ __forceinline__ const float* tq512_thresholds()
+{
+    if constexpr (BITS == 3) return c_tq3.thr;
+    else if constexpr (BITS == 4) return c_tq4_thr;
+    else return c_tq6.thr;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kCodecThreads)
+encode_tq512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                    const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
+                    int64_t ldp, float* __restrict__ radius, bool vec_store)
+{
+    using G = Tq512Grid<BITS>;
+    constexpr int kNThr = (1 << BITS) - 1;
+    constexpr int kRowBytes = 64 * BITS;         // 512 codes of BITS bits
+    __shared__ TqBucket s_tab[G::n];
     __shared__ float s_t[kCodecWarps][544];
-    __shared__ __align__(16) uint8_t s_out[kCodecWarps][256];
-    for (int b = threadIdx.x; b < kTq4Buckets; b += blockDim.x) {
-        const float lo = ((float)b - kTq4BucketOffset - 0.5f) / kTq4BucketScale;
-        const float hi = ((float)b - kTq4BucketOffset + 0.5f) / kTq4BucketScale;
+    __shared__ __align__(16) uint8_t s_out[kCodecWarps][kRowBytes];
+    const float* thr_c = tq512_thresholds<BITS>();
+    for (int b = threadIdx.x; b < G::n; b += blockDim.x) {
+        const float lo = ((float)b - G::off - 0.5f) / G::scale;
+        const float hi = ((float)b - G::off + 0.5f) / G::scale;
         int base = 0;
         float t = INFINITY;
-        for (int k = 0; k < 15; ++k) {
-            base += c_tq4_thr[k] < lo;
-            if (c_tq4_thr[k] >= lo && c_tq4_thr[k] < hi) t = c_tq4_thr[k];
+        for (int k = 0; k < kNThr; ++k) {
+            base += thr_c[k] < lo;
+            if (thr_c[k] >= lo && thr_c[k] < hi) t = thr_c[k];
         }
-        s_tab[b] = Tq4Bucket{t, base};
+        s_tab[b] = TqBucket{t, base};
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -334,98 +432,61 @@ encode_tq4_512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const float u1 = __fmul_rn(v[k], inv);
-            const float bf = __fmaf_rn(u1, kTq4BucketScale, 12582912.0f + kTq4BucketOffset);
-            const int b = min(max(__float_as_int(bf) - 0x4B400000, 0), kTq4Buckets - 1);
-            const Tq4Bucket e = s_tab[b];
-            const bool near = exact_row || fabsf(__fsub_rn(u1, e.thr)) <= kTq4Near;
+            const float bf = __fmaf_rn(u1, G::scale, 12582912.0f + G::off);
+            const int b = min(max(__float_as_int(bf) - 0x4B400000, 0), G::n - 1);
+            const TqBucket e = s_tab[b];
             code[k] = e.base + (u1 >= e.thr ? 1 : 0);
-            if (near) {
-                // within reach of the threshold: the IEEE quotient decides (same bucket)
+            if (exact_row || fabsf(__fsub_rn(u1, e.thr)) <= kTqNear) {
+                // within reach of the threshold: the IEEE quotient decides.  u and u' share
+                // the bucket (its threshold is 1e-3 from the edges), except in a row of
+                // tiny sigma, where u' is not used at all
                 const float u = __fdiv_rn(v[k], sigma);
-                int n = 0;
-#pragma unroll
-                for (int t = 0; t < 15; ++t) n += (u >= c_tq4_thr[t]) ? 1 : 0;
-                code[k] = n;
+                if (exact_row) {
+                    int n = 0;
+                    for (int t = 0; t < kNThr; ++t) n += (u >= thr_c[t]) ? 1 : 0;
+                    code[k] = n;
+                } else {
+                    code[k] = e.base + (u >= e.thr ? 1 : 0);
+                }
             }
             if (rad == 0.0f) code[k] = 0;
         }
-        // pack: byte (lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1); odd lanes hold the
-        // high nibble
+        // lane L holds codes of elements (L >> 4) * 256 + k * 16 + (L & 15)
         uint8_t* out = s_out[wib];
+        if constexpr (BITS == 4) {
+            // byte (lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1); odd lanes the high nibble
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int hi = __shfl_down_sync(kFull, code[k], 1);
-            if ((lane & 1) == 0)
-                out[(lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1)] = (uint8_t)(code[k] | (hi << 4));
+            for (int k = 0; k < 16; ++k) {
+                const int hi = __shfl_down_sync(kFull, code[k], 1);
+                if ((lane & 1) == 0)
+                    out[(lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1)] = (uint8_t)(code[k] | (hi << 4));
+            }
+        } else {
+            constexpr int kG = 24 / BITS;        // consecutive codes (lanes) a 3-byte group
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                uint32_t w = (uint32_t)code[k];
+#pragma unroll
+                for (int d = 1; d < kG; d <<= 1) w |= __shfl_down_sync(kFull, w, d) << (BITS * d);
+                if ((lane & (kG - 1)) == 0) {
+                    const int e = (lane >> 4) * 256 + k * 16 + (lane & 15);
+                    uint8_t* dst = out + e * BITS / 8;
+                    dst[0] = (uint8_t)w;
+                    dst[1] = (uint8_t)(w >> 8);
+                    dst[2] = (uint8_t)(w >> 16);
+                }
+            }
         }
         __syncwarp();
         uint8_t* pr = packed + r * ldp;
         if (vec_store) {
-            if (lane < 16) reinterpret_cast<uint4*>(pr)[lane] = reinterpret_cast<const uint4*>(out)[lane];
+            if (lane < kRowBytes / 16) reinterpret_cast<uint4*>(pr)[lane] = reinterpret_cast<const uint4*>(out)[lane];
         } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pr[q * 32 + lane] = out[q * 32 + lane];
+            for (int q = lane; q < kRowBytes; q += 32) pr[q] = out[q];
         }
         __syncwarp();
         if (lane == 0) radius[r] = rad;
     }
-}
-
-// ------------------------------------------------------------------------------------
-// The rotated tiers at 3 and 6 bits (colibri PR #399: KV_TQ=6, and 3 bits): the same row
-// transform and radius as TQ4, a 2^b-level codebook, and codes packed as a little-endian
-// bit stream (code i at bits b*i .. b*i + b - 1 of the row).  24 / b consecutive codes fill
-// 3 bytes: lanes combine them with a shuffle tree and the first lane of each group writes
-// the 3 bytes into shared memory, which the warp copies out with 16-byte stores.
-// ------------------------------------------------------------------------------------
-
-__constant__ TqCodebook<8> c_tq3 = kTq3;
-__constant__ TqCodebook<64> c_tq6 = kTq6;
-
-// 64 levels: instead of a six-step bisection, u is placed in one of 257 buckets
-// b = round-to-even(32 u + 128) (one fma against 1.5 * 2^23, exact), clamped to [0, 256];
-// kTq6Base[b] counts the thresholds below the bucket's lowest possible u (32 u + 128 =
-// b - 1/2), and no bucket, edges included, holds more than one threshold (checked below),
-// so the code is kTq6Base[b] + (u >= thr[kTq6Base[b]]).  thr[63] is +inf padding.
-struct Tq6Buckets {
-    uint8_t base[257];
-};
-
-constexpr Tq6Buckets tq6_buckets()
-{
-    Tq6Buckets r{};
-    for (int b = 0; b <= 256; ++b) {
-        int n = 0;
-        for (int k = 0; k < 63; ++k)
-            if (kTq6.thr[k] * 32.0f + 128.0f < (float)b - 0.5f) ++n;
-        r.base[b] = (uint8_t)n;
-    }
-    return r;
-}
-
-constexpr bool tq6_buckets_hold_one_threshold()
-{
-    for (int b = 0; b <= 256; ++b) {
-        int n = 0;
-        for (int k = 0; k < 63; ++k) {
-            const float v = kTq6.thr[k] * 32.0f + 128.0f;
-            if (v >= (float)b - 0.5f && v <= (float)b + 0.5f) ++n;
-        }
-        if (n > 1) return false;
-    }
-    // the clamped end buckets hold no threshold beyond their range
-    return kTq6.thr[0] * 32.0f + 128.0f > 0.5f && kTq6.thr[62] * 32.0f + 128.0f < 255.5f;
-}
-static_assert(tq6_buckets_hold_one_threshold(), "6-bit bucket table needs a finer grid");
-
-constexpr Tq6Buckets kTq6Buckets = tq6_buckets();
-__constant__ Tq6Buckets c_tq6_buckets = kTq6Buckets;
-
-template <int BITS>
-__device__ __forceinline__ const float* tq_thresholds()
-{
-    if constexpr (BITS == 3) return c_tq3.thr;
-    else return c_tq6.thr;
 }
 
 template <int VPL, int BITS>   // dim = 32 * VPL
@@ -786,6 +847,29 @@ cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx
     return cudaGetLastError();
 }
 
+// one wave of the 512-wide rotated-tier encoder: as many CTAs of eight warps as fit on
+// every SM at once, each warp many rows (a second, partial wave would double the time of
+// its CTAs)
+template <int BITS>
+cudaError_t launch_tq512(const float* x, int64_t rows, int64_t ldx, const uint32_t* sign_bits,
+                         uint8_t* packed, int64_t ldp, float* radius, bool vec, cudaStream_t s)
+{
+    static std::atomic<int> per_sm{0};
+    int n = per_sm.load();
+    if (n <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_tq512_kernel<BITS>, kCodecThreads, 0) !=
+                cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = 1;
+        }
+        per_sm.store(n);
+    }
+    const int g = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kCodecWarps - 1) / kCodecWarps,
+                                                              (int64_t)sm_count() * n));
+    encode_tq512_kernel<BITS><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, vec);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx,
                               const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
                               float* radius, cudaStream_t s)
@@ -799,23 +883,8 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
         case 128:  encode_tq4_kernel<4><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         case 256:  encode_tq4_kernel<8><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec); break;
         case 512:
-            if ((uintptr_t)x % 16 == 0 && ldx % 4 == 0) {
-                // one wave (as many CTAs of eight warps as fit on every SM at once), each
-                // warp many rows: a second, partial wave would double the time of its CTAs
-                static std::atomic<int> per_sm{0};
-                int n = per_sm.load();
-                if (n <= 0) {
-                    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_tq4_512_kernel, kCodecThreads, 0) !=
-                            cudaSuccess || n <= 0) {
-                        (void)cudaGetLastError();
-                        n = 1;
-                    }
-                    per_sm.store(n);
-                }
-                const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>((rows + kCodecWarps - 1) / kCodecWarps,
-                                                                           (int64_t)sm_count() * n));
-                encode_tq4_512_kernel<<<g1, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, vec);
-            }
+            if ((uintptr_t)x % 16 == 0 && ldx % 4 == 0)
+                return launch_tq512<4>(x, rows, ldx, sign_bits, packed, ldp, radius, vec, s);
             else
                 encode_tq4_kernel<16><<<g, kCodecThreads, 0, s>>>(x, rows, ldx, sign_bits, packed, ldp, radius, c, vec);
             break;
@@ -853,6 +922,10 @@ cudaError_t launch_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx,
         case 512:  KVQ_TQB(16, B); break;                 \
         case 1024: KVQ_TQB(32, B); break;                 \
         default: return cudaErrorInvalidValue;            \
+    }
+    if (dim == 512 && (uintptr_t)x % 16 == 0 && ldx % 4 == 0) {
+        if (bits == 3) return launch_tq512<3>(x, rows, ldx, sign_bits, packed, ldp, radius, vec, s);
+        if (bits == 6) return launch_tq512<6>(x, rows, ldx, sign_bits, packed, ldp, radius, vec, s);
     }
     if (bits == 3) {
         KVQ_TQB_DIMS(3)
