@@ -9,8 +9,8 @@
 //   S^T[rows x 32] = C_tile[rows x 576] . Q^T        rows on M = 128, N = 16 heads hi | lo
 //   O^T[dims x 32] += V_tile^T[dims x rows] . W^T    dims on M (4 M-tiles), same N
 //
-// A producer thread (one row) converts a 64-code chunk once and stores it twice: into a
-// tensor-memory slot that the score MMA reads as A (lane = row), and, for latent chunks,
+// A producer thread (one row) converts a 64-code chunk once into a tensor-memory slot
+// that the score MMA reads as A (lane = row); latent chunks are later copied from there
 // into a 128B-swizzled shared-memory slot that the context MMA reads as the MN-major A
 // operand V^T once the softmax of the tile has produced W.  Three producer sets take
 // every third chunk, so three chains of conversion and hand-over latency overlap.  The codes are exact in fp16
@@ -57,21 +57,22 @@ constexpr int kWBytes = 2 * kWSlab;       // rows 0..63 and 64..127
 constexpr int kVSlot = kRT * 128;         // [128 rows x 64 dims] fp16, 128B-swizzled
 constexpr int kSets = 3;                  // producer sets; set s converts chunks ch = s mod 3
 constexpr int kPer = 3;                   // chunks per set and tile (9 = rope + 8 latent)
-constexpr int kRingA = 2;                 // score-A slots per set
 constexpr int kStages = 2;                // raw-code stages per producer set
 constexpr int kStageBytes = kRT * 64;     // one chunk of raw codes
 constexpr int kWarpSmx = 4 * kSets;       // first softmax warp
-constexpr int kWarpMma = kWarpSmx + 4;
-constexpr int kWarpLoad = kWarpMma + 1;   // loader of set s: kWarpLoad + s
-constexpr int kThreads = 32 * (kWarpLoad + kSets);   // 12 producer, 4 softmax, 1 MMA, 3 loader warps
+constexpr int kWarpMma = kWarpSmx + 4;   // score MMA issuer; allocates tensor memory
+constexpr int kWarpCtx = kWarpMma + 1;   // context MMA issuer
+constexpr int kWarpLoad = kWarpCtx + 1;  // TMA loader of the three sets
+constexpr int kThreads = 32 * (kWarpLoad + 1);   // 12 producer, 4 softmax, 2 MMA, 1 loader warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.0f;             // rescale only when the max grows by > 2^8
 constexpr uint64_t kTimeoutNs = kDefaultWaitNs;   // drains
 
-// tensor memory columns
-constexpr uint32_t kColO = 128;           // O^T M-tile m at 128 + 32 m
-constexpr uint32_t kColA = 256;           // score-A slot j of set s at 256 + 32 (2 s + j)
-// (S buffer b: latent scores at 64 b, rope scores at 64 b + 32)
+// tensor memory columns: S (latent scores at 0, rope scores at 32), O^T, and one score-A
+// slot per chunk of a tile (slot k of set s holds the set's k-th chunk)
+constexpr uint32_t kColO = 64;            // O^T M-tile m at 64 + 32 m
+constexpr uint32_t kColA = 192;           // score-A slot k of set s at 192 + 32 (3 s + k)
+static_assert(kColA + 32 * kSets * kPer <= 512, "tensor memory columns");
 
 // shared memory
 constexpr int kOffQ = 0;
@@ -85,9 +86,10 @@ constexpr int kOffFlag = kOffAlpha + 16 * 4;              // some head rescales 
 constexpr int kOffVote = kOffFlag + 16;                   // [2][4] "a row exceeds the max"
 constexpr int kOffTab = kOffVote + 32;                    // [64] binary16 centroids (3/6 bits)
 constexpr int kOffBar = kOffTab + 128;
-// full_a[3][2], empty_a[3][2], full_v[8], empty_v[8], s_full, s_empty[2], p_full, o_done,
-// drain, q_full, raw_full[3][kStages], raw_empty[3][kStages]
-constexpr int kNumBars = 2 * kSets * kRingA + 16 + 7 + 2 * kSets * kStages;
+// full_a[3][3], empty_a[3][3], full_v[8], empty_v[8], s_full, s_empty, p_full, o_done,
+// drain[2] (one per MMA issuer), q_full, raw_full[3][kStages], raw_empty[3][kStages]
+constexpr int kNumA = kSets * kPer;
+constexpr int kNumBars = 2 * kNumA + 16 + 7 + 2 * kSets * kStages;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -126,18 +128,18 @@ struct Shared {
     __device__ volatile int* vote(int par) const { return reinterpret_cast<volatile int*>(base + kOffVote) + 4 * par; }
     __device__ uint16_t* tab() const { return reinterpret_cast<uint16_t*>(base + kOffTab); }
     __device__ uint64_t* bar(int i) const { return reinterpret_cast<uint64_t*>(base + kOffBar) + i; }
-    __device__ uint64_t* full_a(int s, int j) const { return bar(s * kRingA + j); }
-    __device__ uint64_t* empty_a(int s, int j) const { return bar(kSets * kRingA + s * kRingA + j); }
-    __device__ uint64_t* full_v(int j) const { return bar(2 * kSets * kRingA + j); }
-    __device__ uint64_t* empty_v(int j) const { return bar(2 * kSets * kRingA + 8 + j); }
-    __device__ uint64_t* s_full() const { return bar(2 * kSets * kRingA + 16); }
-    __device__ uint64_t* s_empty(int b) const { return bar(2 * kSets * kRingA + 17 + b); }
-    __device__ uint64_t* p_full() const { return bar(2 * kSets * kRingA + 19); }
-    __device__ uint64_t* o_done() const { return bar(2 * kSets * kRingA + 20); }
-    __device__ uint64_t* drain() const { return bar(2 * kSets * kRingA + 21); }
-    __device__ uint64_t* q_full() const { return bar(2 * kSets * kRingA + 22); }
-    __device__ uint64_t* raw_full(int s, int d) const { return bar(2 * kSets * kRingA + 23 + s * kStages + d); }
-    __device__ uint64_t* raw_empty(int s, int d) const { return bar(2 * kSets * kRingA + 23 + kSets * kStages + s * kStages + d); }
+    __device__ uint64_t* full_a(int s, int k) const { return bar(s * kPer + k); }
+    __device__ uint64_t* empty_a(int s, int k) const { return bar(kNumA + s * kPer + k); }
+    __device__ uint64_t* full_v(int j) const { return bar(2 * kNumA + j); }
+    __device__ uint64_t* empty_v(int j) const { return bar(2 * kNumA + 8 + j); }
+    __device__ uint64_t* s_full() const { return bar(2 * kNumA + 16); }
+    __device__ uint64_t* s_empty() const { return bar(2 * kNumA + 17); }
+    __device__ uint64_t* p_full() const { return bar(2 * kNumA + 18); }
+    __device__ uint64_t* o_done() const { return bar(2 * kNumA + 19); }
+    __device__ uint64_t* drain(int w) const { return bar(2 * kNumA + 20 + w); }
+    __device__ uint64_t* q_full() const { return bar(2 * kNumA + 22); }
+    __device__ uint64_t* raw_full(int s, int d) const { return bar(2 * kNumA + 23 + s * kStages + d); }
+    __device__ uint64_t* raw_empty(int s, int d) const { return bar(2 * kNumA + 23 + kSets * kStages + s * kStages + d); }
     __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + kOffMisc); }
     __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kOffMisc + 4); }
 };
@@ -172,22 +174,22 @@ static_assert(kSets * kPer == 9, "nine chunks a tile");
 // ====================================================================================
 // The decode kernel.
 //  * Warps 0-11: three producer sets of four warps (thread = row of the tile).  Per chunk:
-//    raw codes from the set's stage ring -> binary16 -> score-A slot in tensor memory
-//    (tcgen05.st) -> for latent chunks the V slot in shared memory.  The A slot is handed
-//    over before the V slot is waited for, so the score MMAs never wait on the context
-//    of the tile before; when the V slot is already free both stores go out together.
-//    The next chunk's raw codes are read before this chunk's stores.
+//    raw codes from the set's stage ring -> binary16 -> the set's score-A slot of the
+//    chunk in tensor memory (tcgen05.st; one slot per chunk of a tile, so converting a
+//    tile waits only on the score MMAs of the tile before).  Once the set's three chunks
+//    of tile i are converted, it copies its latent chunks from their A slots (tcgen05.ld)
+//    into the V slots in shared memory, each as the context of tile i-1 frees it.  So
+//    the conversion of tile i+1 runs during the softmax and context of tile i.
 //  * Warps 12-15: softmax (thread = row): S from tensor memory, per-head tile maxima,
 //    lazy O rescale, W = p * scale as fp16 hi | lo into the K-major W image; epilogue
 //    (thread = output dim) writes the split's (m, l, o) partials.
-//  * Warp 16: allocates tensor memory and issues every MMA from one elected lane.  Order
-//    per tile i: the score chunks of tile i+1 that need no V slot of tile i (ch 0..3:
-//    each set's first chunk, and set 0's second, which follows the rope), then the
-//    context of tile i (after its softmax), then the rest of tile i+1's score.  The first
-//    group fills the tensor pipe during the softmax of tile i; nothing issued before the
-//    context of tile i waits on it, so the order cannot deadlock.
-//  * Warps 17-19: TMA loaders of the three sets (contiguous caches); paged and sparse
-//    caches are copied by the producers themselves with cp.async.
+//  * Warp 16: allocates tensor memory; issues the score MMAs chunk by chunk as the A
+//    slots fill (the first chunk of tile i after the softmax has read S of tile i-1).
+//  * Warp 17: issues the context MMAs of tile i after its softmax, M-tile by M-tile as
+//    the V copies land.  Two issuing warps, on two schedulers, keep the chain of waits
+//    and MMA issues off the critical path; each waits only on other roles.
+//  * Warp 18: the TMA loader of the three sets (contiguous caches), polling their stages;
+//    paged and sparse caches are copied by the producers themselves with cp.async.
 // ====================================================================================
 // kB = 0: fp8 and TQ4 rows (per sequence, mixed batches included); kB = 6 or 3: the
 // rotated tier at 6 or 3 bits in a problem of that one format.
@@ -233,9 +235,9 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
     if (warp == kWarpMma) {
         if (lane == 0) {
             for (int st = 0; st < kSets; ++st) {
-                for (int j = 0; j < kRingA; ++j) {
-                    mbar_init(sh.full_a(st, j), 4);      // one arrival per warp of the set
-                    mbar_init(sh.empty_a(st, j), 1);     // MMA commit
+                for (int k = 0; k < kPer; ++k) {
+                    mbar_init(sh.full_a(st, k), 4);      // one arrival per warp of the set
+                    mbar_init(sh.empty_a(st, k), 1);     // MMA commit
                 }
                 for (int d = 0; d < kStages; ++d) {
                     mbar_init(sh.raw_full(st, d), 1);
@@ -247,11 +249,11 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                 mbar_init(sh.empty_v(j), 1);
             }
             mbar_init(sh.s_full(), 1);
-            mbar_init(sh.s_empty(0), 4);                 // one arrival per softmax warp
-            mbar_init(sh.s_empty(1), 4);
+            mbar_init(sh.s_empty(), 4);                  // one arrival per softmax warp
             mbar_init(sh.p_full(), 4);
             mbar_init(sh.o_done(), 1);
-            mbar_init(sh.drain(), 1);
+            mbar_init(sh.drain(0), 1);
+            mbar_init(sh.drain(1), 1);
             mbar_init(sh.q_full(), 1);
             *sh.abort_flag() = 0;
             fence_mbar_init();
@@ -355,69 +357,64 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         uint4 raw[4];
         bool ok = n_own > 0 && fetch(0, raw);
         for (int o = 0; o < n_own && ok; ++o) {
-            const int tile = o / kPer, k = o - tile * kPer, ch = kSets * k + set;
-            const bool rope = ch == 0;
-            uint32_t h[32];
-            if (kB == 0 || rope) {
-                const bool fp8 = rope || bits == 8;
-                codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
-                codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
-            } else {
-                tqb_codes_to_half<kB == 0 ? 6 : kB>(raw, sh.tab(), h);
-            }
-            // the stage is free once every lane's reads of it are consumed
-            if (tma) {
+            const int tile = o / kPer, k = o - tile * kPer;
+            const bool rope = kSets * k + set == 0;
+            {
+                uint32_t h[32];
+                if (kB == 0 || rope) {
+                    const bool fp8 = rope || bits == 8;
+                    codes_to_half(raw, 0, fp8, *reinterpret_cast<uint32_t(*)[16]>(h));
+                    codes_to_half(raw, 1, fp8, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+                } else {
+                    tqb_codes_to_half<kB == 0 ? 6 : kB>(raw, sh.tab(), h);
+                }
+                // the stage is free once every lane's reads of it are consumed
+                if (tma) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sh.raw_empty(set, o % kStages));
+                } else {
+                    issue(o + kStages);                   // refills the stage just read
+                }
+                // score operand: the chunk's 64 binary16 values as TMEM lane t, 32 columns,
+                // in slot k of the set (free once the score of the tile before read it)
+                ok = __all_sync(kFull, wait_bar(sh, sh.empty_a(set, k), ((uint32_t)tile & 1u) ^ 1u, a.status, a.wait_ns));
+                if (!ok) break;
+                tc_fence_after();
+                tmem_st_x32(tmem + lane_base + kColA + 32 * (kPer * set + k), h);
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sh.raw_empty(set, o % kStages));
-            } else {
-                issue(o + kStages);                       // refills the stage just read
+                if (lane == 0) mbar_arrive(sh.full_a(set, k));
             }
-            // score operand: the chunk's 64 binary16 values as TMEM lane t, 32 columns
-            const int j = o & (kRingA - 1);
-            ok = __all_sync(kFull, wait_bar(sh, sh.empty_a(set, j), ((uint32_t)(o / kRingA) & 1u) ^ 1u, a.status, a.wait_ns));
-            if (!ok) break;
-            tc_fence_after();
-            tmem_st_x32(tmem + lane_base + kColA + 32 * (kRingA * set + j), h);
-            // context operand: row t of latent chunk ch - 1's V slot, now if the slot is free
-            const int vj = ch - 1;
+            // the next chunk's raw codes (for the last chunk of the tile, read before the
+            // copies below)
+            if (o + 1 < n_own) {
+                ok = fetch(o + 1, raw);
+                if (!ok) break;
+            }
+            if (k + 1 < kPer) continue;
+            // The set's chunks of this tile are converted: copy its latent chunks from their
+            // A slots into the V slots as the context of the tile before frees them.
             const uint32_t vpar = ((uint32_t)tile & 1u) ^ 1u;
-            bool v_done = rope;
-            if (!rope && __all_sync(kFull, mbar_test_wait(sh.empty_v(vj), vpar))) {
-                uint8_t* dst = sh.v(vj);
+            for (int kk = 0; kk < kPer && ok; ++kk) {
+                const int ch = kSets * kk + set;
+                if (ch == 0) continue;                    // the rope key has no V
+                ok = __all_sync(kFull, wait_bar(sh, sh.empty_v(ch - 1), vpar, a.status, a.wait_ns));
+                if (!ok) break;
+                uint32_t h[32];
+                const uint32_t src = tmem + lane_base + kColA + 32 * (kPer * set + kk);
+                tmem_ld_x16(src, *reinterpret_cast<uint32_t(*)[16]>(h));
+                tmem_ld_x16(src + 16, *reinterpret_cast<uint32_t(*)[16]>(h + 16));
+                tmem_ld_wait();
+                uint8_t* dst = sh.v(ch - 1);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<uint4*>(dst + sw128(t, c)) =
                         make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                v_done = true;
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sh.full_a(set, j));
-            // the next chunk's raw codes, read while this chunk's stores complete
-            uint4 nxt[4];
-            const bool more = o + 1 < n_own;
-            if (more) {
-                ok = fetch(o + 1, nxt);
-                if (!ok) break;
-            }
-            if (!rope) {
-                if (!v_done) {
-                    ok = __all_sync(kFull, wait_bar(sh, sh.empty_v(vj), vpar, a.status, a.wait_ns));
-                    if (!ok) break;
-                    uint8_t* dst = sh.v(vj);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(dst + sw128(t, c)) =
-                            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                }
                 fence_proxy_async_smem();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sh.full_v(vj));
-            }
-            if (more) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) raw[i] = nxt[i];
+                if (lane == 0) mbar_arrive(sh.full_v(ch - 1));
             }
         }
         cp_async_wait_all();                              // nothing lands after the CTA ends
@@ -439,7 +436,6 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
         float l_lane = 0.0f;                          // sum of p over this warp's rows, head g16
         bool ok = true;
         for (int i = 0; i < NT; ++i) {
-            const int b = i & 1;
             const int64_t row = rc.row(r0 + (int64_t)i * kRT + t, true);
             float sc_lat = 0.0f, sc_rope = 0.0f;
             if (row >= 0) {
@@ -454,7 +450,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
             if (ok) {
                 tc_fence_after();
                 uint32_t xh[16], xl[16], yh[16], yl[16];
-                const uint32_t cs = tmem + lane_base + 64u * b;
+                const uint32_t cs = tmem + lane_base;
                 tmem_ld_x16(cs, xh);
                 tmem_ld_x16(cs + 16, xl);
                 tmem_ld_x16(cs + 32, yh);
@@ -462,7 +458,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sh.s_empty(b));
+                if (lane == 0) mbar_arrive(sh.s_empty());   // S may take the next tile's scores
 #pragma unroll
                 for (int g = 0; g < kGQ; ++g)
                     sv[g] = fmaf(sc_lat, __uint_as_float(xh[g]) + __uint_as_float(xl[g]),
@@ -604,94 +600,85 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                             __uint_as_float(x[g]) + __uint_as_float(y[g]);
             }
         }
-    } else if (warp >= kWarpLoad) {
-        // ================================ loaders ========================================
-        // Contiguous rows: one TMA box per chunk ([128 rows x 32 or 64 bytes]) into the
-        // next stage of its producer set, in the set's order.
-        const int set = warp - kWarpLoad;
+    } else if (warp == kWarpLoad) {
+        // ================================ loader =========================================
+        // Contiguous rows: one TMA box per chunk ([128 rows x 32, 48 or 64 bytes]) into the
+        // next stage of the chunk's producer set.  One warp serves the three sets, polling
+        // their stages, so a lagging set does not hold back the refills of the others.
         if (a.use_tma) {
             const bool leader = elect_one();
             const CUtensorMap* m_lat = &a.tm_lat[rot ? 1 : 0];
             const CUtensorMap* m_rope = &a.tm_rope[rot ? 1 : 0];
             const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;   // pool row of candidate r0
             const int n_own = kPer * NT;
+            int nxt[kSets];                               // next item of each set
+#pragma unroll
+            for (int set = 0; set < kSets; ++set) nxt[set] = 0;
             bool ok = true;
-            int o = 0;
-            for (; o < n_own && ok; ++o) {
-                const int tile = o / kPer, ch = kSets * (o - tile * kPer) + set;
-                const int d = o % kStages;
-                ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(o / kStages) & 1u) ^ 1u, a.status, a.wait_ns));
-                if (!ok) break;
-                if (leader) {
-                    const bool rope = ch == 0;
-                    const int inner = rope ? 64 : lat_cb;
-                    mbar_arrive_expect_tx(sh.raw_full(set, d), (uint32_t)(inner * kRT));
-                    tma_load_2d(sh.stage(set, d), rope ? m_rope : m_lat, rope ? 0 : (ch - 1) * inner,
-                                (int)(row0 + (int64_t)tile * kRT), sh.raw_full(set, d));
+            uint64_t idle_since = 0;
+            while (ok && (nxt[0] < n_own || nxt[1] < n_own || nxt[2] < n_own)) {
+                bool progress = false;
+#pragma unroll
+                for (int set = 0; set < kSets; ++set) {
+                    const int o = nxt[set];
+                    if (o >= n_own) continue;
+                    const int d = o % kStages;
+                    int r = 0;
+                    if (lane == 0) r = mbar_test_wait(sh.raw_empty(set, d), ((uint32_t)(o / kStages) & 1u) ^ 1u) ? 1 : 0;
+                    if (!__shfl_sync(kFull, r, 0)) continue;
+                    if (leader) {
+                        const int tile = o / kPer, ch = kSets * (o - tile * kPer) + set;
+                        const bool rope = ch == 0;
+                        const int inner = rope ? 64 : lat_cb;
+                        mbar_arrive_expect_tx(sh.raw_full(set, d), (uint32_t)(inner * kRT));
+                        tma_load_2d(sh.stage(set, d), rope ? m_rope : m_lat, rope ? 0 : (ch - 1) * inner,
+                                    (int)(row0 + (int64_t)tile * kRT), sh.raw_full(set, d));
+                    }
+                    __syncwarp();
+                    nxt[set] = o + 1;
+                    progress = true;
                 }
-                __syncwarp();
+                if (progress) {
+                    idle_since = 0;
+                } else if (*sh.abort_flag()) {
+                    ok = false;
+                } else {
+                    const uint64_t now = globaltimer_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > a.wait_ns) {
+                        if (lane == 0) {
+                            *sh.abort_flag() = 1;
+                            if (a.status) atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+                        }
+                        ok = false;
+                    }
+                }
+                ok = __all_sync(kFull, ok);
             }
             // every box issued has landed before the CTA's shared memory is released
             if (leader) {
-                for (int d = 0; d < kStages && d < o; ++d) {
-                    const int jl = d + kStages * ((o - 1 - d) / kStages);
-                    if (!mbar_wait(sh.raw_full(set, d), (uint32_t)(jl / kStages) & 1u, kTimeoutNs) && a.status)
-                        atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+#pragma unroll
+                for (int set = 0; set < kSets; ++set) {
+                    for (int d = 0; d < kStages && d < nxt[set]; ++d) {
+                        const int jl = d + kStages * ((nxt[set] - 1 - d) / kStages);
+                        if (!mbar_wait(sh.raw_full(set, d), (uint32_t)(jl / kStages) & 1u, kTimeoutNs) && a.status)
+                            atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+                    }
                 }
             }
             __syncwarp();
         }
-    } else {
-        // ================================ MMA issuer =====================================
+    } else if (warp == kWarpCtx) {
+        // ============================ context MMA issuer =================================
+        // O^T += V^T . W^T per tile, after the tile's softmax, M-tile by M-tile as the V
+        // copies land
         const bool leader = elect_one();
-        const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
         const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, false);    // V^T (MN-major) . W^T
-        const uint64_t q_desc = desc_sw128(smem_u32(sh.q()), 1024);
         const uint32_t w_addr = smem_u32(sh.w());
-        grid_dependency_wait();                 // the Q image comes from the kernel before
-        if (leader) {
-            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
-            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
-                          kQBytes, sh.q_full());
-        }
-        __syncwarp();
-        bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status, a.wait_ns));
-        tc_fence_after();
-        // the score MMAs of chunk ch of tile i
-        auto score = [&](int i, int ch) -> bool {
-            const int set = ch % kSets, k = ch / kSets;
-            const int o = kPer * i + k, j = o & (kRingA - 1);
-            if (!__all_sync(kFull, wait_bar(sh, sh.full_a(set, j), (uint32_t)(o / kRingA) & 1u, a.status, a.wait_ns)))
-                return false;
-            tc_fence_after();
-            const uint32_t d = tmem + 64u * (uint32_t)(i & 1) + (ch == 0 ? 32u : 0u);
-            const uint32_t a_tm = tmem + kColA + 32 * (kRingA * set + j);
-            const uint64_t b_desc = q_desc + (uint64_t)(((ch == 0 ? 8 : ch - 1) * kQSlab) >> 4);
-            const bool first = ch <= 1;                 // first chunk of its accumulator
-            if (leader) {
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16_ts(d, a_tm + 8 * ks, b_desc + 2 * ks, idesc_s, first ? (ks > 0) : 1u);
-                mma_commit(sh.empty_a(set, j));
-            }
-            __syncwarp();
-            return true;
-        };
-        constexpr int kEarly = 4;                       // chunks of tile i+1 issued before C(i)
-        for (int ch = 0; ch < 9 && ok; ++ch) ok = score(0, ch);
-        if (ok && leader) mma_commit(sh.s_full());
-        __syncwarp();
+        bool ok = true;
         for (int i = 0; i < NT && ok; ++i) {
-            if (i + 1 < NT) {
-                // the S buffer of tile i+1 held tile i-1's scores: the softmax released it
-                if (i >= 1)
-                    ok = __all_sync(kFull, wait_bar(sh, sh.s_empty((i + 1) & 1), (uint32_t)((i - 1) >> 1) & 1u, a.status, a.wait_ns));
-                for (int ch = 0; ch < kEarly && ok; ++ch) ok = score(i + 1, ch);
-                if (!ok) break;
-            }
             ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)i & 1u, a.status, a.wait_ns));
-            if (!ok) break;
-            tc_fence_after();
             for (int m = 0; m < 4 && ok; ++m) {
                 ok = __all_sync(kFull, wait_bar(sh, sh.full_v(2 * m), (uint32_t)i & 1u, a.status, a.wait_ns));
                 if (ok) ok = __all_sync(kFull, wait_bar(sh, sh.full_v(2 * m + 1), (uint32_t)i & 1u, a.status, a.wait_ns));
@@ -710,24 +697,60 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                     }
                     mma_commit(sh.empty_v(2 * m));
                     mma_commit(sh.empty_v(2 * m + 1));
+                    if (m == 3) mma_commit(sh.o_done());
                 }
                 __syncwarp();
             }
-            if (!ok) break;
-            if (leader) mma_commit(sh.o_done());
-            __syncwarp();
-            if (i + 1 < NT) {
-                for (int ch = kEarly; ch < 9 && ok; ++ch) ok = score(i + 1, ch);
+        }
+        // drain: this warp's MMAs complete before tensor memory is freed
+        if (leader) {
+            mma_commit(sh.drain(1));
+            if (!mbar_wait(sh.drain(1), 0, kTimeoutNs) && a.status)
+                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ============================= score MMA issuer ==================================
+        // S^T = C . Q^T per tile, chunk by chunk as the producers fill the A slots; the
+        // first chunk waits until the softmax has read S of the tile before
+        const bool leader = elect_one();
+        const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
+        const uint64_t q_desc = desc_sw128(smem_u32(sh.q()), 1024);
+        grid_dependency_wait();                 // the Q image comes from the kernel before
+        if (leader) {
+            mbar_arrive_expect_tx(sh.q_full(), kQBytes);
+            bulk_copy_g2s(sh.q(), a.q_img + (((int64_t)s * p.n_q + q) * a.n_hg + hg) * (int64_t)kQBytes,
+                          kQBytes, sh.q_full());
+        }
+        __syncwarp();
+        bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status, a.wait_ns));
+        tc_fence_after();
+        for (int i = 0; i < NT && ok; ++i) {
+            if (i > 0) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status, a.wait_ns));
+            for (int ch = 0; ch < 9 && ok; ++ch) {
+                const int set = ch % kSets, k = ch / kSets;
+                ok = __all_sync(kFull, wait_bar(sh, sh.full_a(set, k), (uint32_t)i & 1u, a.status, a.wait_ns));
                 if (!ok) break;
-                if (leader) mma_commit(sh.s_full());
+                tc_fence_after();
+                const uint32_t d = tmem + (ch == 0 ? 32u : 0u);
+                const uint32_t a_tm = tmem + kColA + 32 * (kPer * set + k);
+                const uint64_t b_desc = q_desc + (uint64_t)(((ch == 0 ? 8 : ch - 1) * kQSlab) >> 4);
+                const bool first = ch <= 1;             // first chunk of its accumulator
+                if (leader) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts(d, a_tm + 8 * ks, b_desc + 2 * ks, idesc_s, first ? (ks > 0) : 1u);
+                    mma_commit(sh.empty_a(set, k));
+                    if (ch == 8) mma_commit(sh.s_full());
+                }
                 __syncwarp();
             }
         }
-        // drain: every MMA issued so far completes before tensor memory is freed, and
-        // the Q copy has landed before the CTA's shared memory is released
+        // drain: this warp's MMAs complete before tensor memory is freed, and the Q copy
+        // has landed before the CTA's shared memory is released
         if (leader) {
-            mma_commit(sh.drain());
-            if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
+            mma_commit(sh.drain(0));
+            if (!mbar_wait(sh.drain(0), 0, kTimeoutNs) && a.status)
                 atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
             if (!mbar_wait(sh.q_full(), 0, kTimeoutNs) && a.status)
                 atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
