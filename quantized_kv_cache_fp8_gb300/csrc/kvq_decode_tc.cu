@@ -75,14 +75,15 @@ __global__ void __launch_bounds__(256) q_image_kernel(TcArgs a)
 
 // ====================================================================================
 // The decode kernel.
-//  * Roles (480 threads): warps 0-7 are two producer sets of four warps (thread = row)
+//  * Roles (512 threads): warps 0-7 are two producer sets of four warps (thread = row)
 //    that convert alternate chunks of codes to fp16, so two chains of ring waits,
 //    stores and arrivals run at once and every warp scheduler holds one warp of each
 //    set; warps 8-11 run the softmax (thread = row) and the epilogue (thread = output
-//    dim); warp 12 allocates tensor memory and issues every MMA from one elected lane;
-//    warps 13 and 14 load code chunks by TMA for producer sets 0 and 1 (contiguous
-//    caches).
-//  * Order of work, common to producers, loader and MMA issuer: per step i, the 9
+//    dim); warp 12 allocates tensor memory and issues the score MMAs, warp 15 the
+//    context MMAs, each from one elected lane (two issuing warps on two schedulers, so
+//    neither chain of waits and issues queues behind the other); warps 13 and 14 load
+//    code chunks by TMA for producer sets 0 and 1 (contiguous caches).
+//  * Order of work, common to producers, loaders and MMA issuers: per step i, the 9
 //    score chunks of tile i (8 latent, 1 rope) if i < NT, then the 8 latent context
 //    chunks of tile i-1.  Score chunks go to tensor memory (thread = row = TMEM lane)
 //    and are read from there by the MMA; context chunks go to a shared-memory ring,
@@ -106,7 +107,7 @@ constexpr int kRingC = 4;                // shared-memory context slots (pairs a
 constexpr int kStages = 4;               // raw-code stages in flight per producer set
 constexpr int kStageBytes = kRT * 64;    // one chunk of raw codes, [4 pieces][128 rows][16 B]
 constexpr uint32_t kColA = 128;
-constexpr int kThreads = 480;           // 8 producer, 4 softmax, 1 MMA and 2 loader warps
+constexpr int kThreads = 512;           // 8 producer, 4 softmax, 2 MMA and 2 loader warps
 constexpr int kOffQ = 0;
 constexpr int kOffRing = kOffQ + kQBytes;
 constexpr int kOffP = kOffRing + kRingC * kChunkBytes;
@@ -117,8 +118,8 @@ constexpr int kOffAlpha = kOffM + 32 * 4;               // [32] rescale factors
 constexpr int kOffFlag = kOffAlpha + 32 * 4;            // some head rescales O
 constexpr int kOffBar = kOffFlag + 16;
 // full_a[4], empty_a[4], full_c[4], empty_c[4], s_full, s_empty, p_full, o_done, drain,
-// q_full, raw_full[2][kStages], raw_empty[2][kStages]
-constexpr int kNumBars = 2 * kRingA + 2 * kRingC + 6 + 4 * kStages;
+// q_full, raw_full[2][kStages], raw_empty[2][kStages], drain_c
+constexpr int kNumBars = 2 * kRingA + 2 * kRingC + 6 + 4 * kStages + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -146,6 +147,7 @@ struct Shared {
     __device__ uint64_t* q_full() const { return bar(2 * kRingA + 2 * kRingC + 5); }
     __device__ uint64_t* raw_full(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + set * kStages + d); }
     __device__ uint64_t* raw_empty(int set, int d) const { return bar(2 * kRingA + 2 * kRingC + 6 + 2 * kStages + set * kStages + d); }
+    __device__ uint64_t* drain_c() const { return bar(2 * kRingA + 2 * kRingC + 6 + 4 * kStages); }
     __device__ uint32_t* tmem_base() const { return reinterpret_cast<uint32_t*>(base + kOffMisc); }
     __device__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kOffMisc + 4); }
 };
@@ -268,6 +270,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             mbar_init(sh.p_full(), 4);
             mbar_init(sh.o_done(), 1);
             mbar_init(sh.drain(), 1);
+            mbar_init(sh.drain_c(), 1);
             mbar_init(sh.q_full(), 1);
             for (int i = 0; i < 2 * kStages; ++i) {
                 mbar_init(sh.raw_full(i / kStages, i % kStages), 1);
@@ -582,7 +585,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 }
             }
         }
-    } else if (warp >= 13) {
+    } else if (warp == 13 || warp == 14) {
         // ================================ loaders ========================================
         // Contiguous rows: one TMA box per chunk ([128 rows x 32 or 64 bytes]) into the
         // owning producer set's next stage, in the common order.  Warp 13 loads set 0's
@@ -626,16 +629,62 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             }
             __syncwarp();
         }
+    } else if (warp == 15) {
+        // ============================ context MMA issuer =================================
+        // The context of tile i after its softmax, chunk pair by chunk pair as the
+        // producers fill the ring.  A second issuing warp, on another scheduler, so that
+        // the score of the next tile is not queued behind this chain of waits and issues.
+        const bool leader = elect_one();
+        const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
+        const uint64_t p_desc = desc_sw128(smem_u32(sh.pbuf()), 1024);
+        const uint64_t v_desc = desc_sw128_lbo(smem_u32(sh.slot(0)), kChunkBytes, 1024);
+        bool ok = true;
+        for (int tile = 0; tile < NT && ok; ++tile) {
+            ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)tile & 1u, a.status, a.wait_ns));
+            if (!ok) break;
+            tc_fence_after();
+            for (int c = 0; c < 8; ++c) {
+                // chunk c comes from set c & 1: its ord-th context chunk, in slot
+                // 2 (ord % 2) + (c & 1), next to its M-tile partner
+                const int ord = 4 * tile + (c >> 1);
+                const int slot = 2 * (ord & 1) + (c & 1);
+                ok = __all_sync(kFull, wait_bar(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
+                if (!ok) break;
+                tc_fence_after();
+                if (c & 1) {
+                    // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
+                    const int m = c >> 1;
+                    const uint64_t a_desc = v_desc + (uint64_t)(((slot - 1) * kChunkBytes) >> 4);
+                    const uint32_t d = tmem + kColO + 64 * m;
+                    if (leader) {
+#pragma unroll
+                        for (int ks = 0; ks < kRT / 16; ++ks)
+                            mma_f16_ss(d, a_desc + (uint64_t)((2048 * ks) >> 4), p_desc + (uint64_t)((2048 * ks) >> 4),
+                                       idesc_c, (tile == 0 && ks == 0) ? 0u : 1u);
+                        mma_commit(sh.empty_c(slot - 1));
+                        mma_commit(sh.empty_c(slot));
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok) break;
+            if (leader) mma_commit(sh.o_done());
+            __syncwarp();
+        }
+        // drain: this warp's MMAs complete before tensor memory is freed
+        if (leader) {
+            mma_commit(sh.drain_c());
+            if (!mbar_wait(sh.drain_c(), 0, kTimeoutNs) && a.status)
+                atomicOr(a.status, (unsigned)KVQ_DEV_TIMEOUT);
+        }
+        __syncwarp();
     } else {
-        // ================================ MMA issuer =====================================
+        // ============================= score MMA issuer ==================================
         // The whole warp runs the loop (operands are computed warp-uniformly); one elected
         // lane issues the MMAs and commits.
         const bool leader = elect_one();
         const uint32_t idesc_s = idesc_f16_f32(kRT, kN, false, false);   // C . Q^T
-        const uint32_t idesc_c = idesc_f16_f32(kRT, kN, true, true);     // V^T . W^T
         const uint64_t q_desc = desc_sw128(smem_u32(sh.q()), 1024);
-        const uint64_t p_desc = desc_sw128(smem_u32(sh.pbuf()), 1024);
-        const uint64_t v_desc = desc_sw128_lbo(smem_u32(sh.slot(0)), kChunkBytes, 1024);
         // the Q image is written by the kernel launched just before this one
         grid_dependency_wait();
         if (leader) {
@@ -646,70 +695,35 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
         __syncwarp();
         bool ok = __all_sync(kFull, wait_bar(sh, sh.q_full(), 0u, a.status, a.wait_ns));
         tc_fence_after();
-        for (int i = 0; i <= NT && ok; ++i) {
-            if (i < NT) {
-                if (i >= 1) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status, a.wait_ns));
+        for (int i = 0; i < NT && ok; ++i) {
+            if (i >= 1) ok = __all_sync(kFull, wait_bar(sh, sh.s_empty(), (uint32_t)(i - 1) & 1u, a.status, a.wait_ns));
+            if (!ok) break;
+            tc_fence_after();
+            for (int ch = 0; ch < 9; ++ch) {
+                // chunk ch comes from producer set ch & 1: its ord-th score chunk
+                const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
+                const int slot = (ch & 1) + 2 * (ord & 1);
+                ok = __all_sync(kFull, wait_bar(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
                 if (!ok) break;
                 tc_fence_after();
-                for (int ch = 0; ch < 9; ++ch) {
-                    // chunk ch comes from producer set ch & 1: its ord-th score chunk
-                    const int ord = i * ((ch & 1) ? 4 : 5) + (ch >> 1);
-                    const int slot = (ch & 1) + 2 * (ord & 1);
-                    ok = __all_sync(kFull, wait_bar(sh, sh.full_a(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
-                    const uint32_t a_tm = tmem + kColA + 32 * slot;
-                    const uint64_t b_desc = q_desc + (uint64_t)((ch * kQSlabBytes) >> 4);
-                    if (leader) {
+                const uint32_t d = tmem + (ch == 8 ? 64u : 0u);
+                const uint32_t a_tm = tmem + kColA + 32 * slot;
+                const uint64_t b_desc = q_desc + (uint64_t)((ch * kQSlabBytes) >> 4);
+                if (leader) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            mma_f16_ts(d, a_tm + 8 * ks, b_desc + 2 * ks, idesc_s,
-                                       (ch == 0 || ch == 8) ? (ks > 0) : 1u);
-                        mma_commit(sh.empty_a(slot));
-                    }
-                    __syncwarp();
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16_ts(d, a_tm + 8 * ks, b_desc + 2 * ks, idesc_s,
+                                   (ch == 0 || ch == 8) ? (ks > 0) : 1u);
+                    mma_commit(sh.empty_a(slot));
                 }
-                if (!ok) break;
-                if (leader) mma_commit(sh.s_full());
                 __syncwarp();
             }
-            if (i >= 1) {
-                const int tile = i - 1;
-                ok = __all_sync(kFull, wait_bar(sh, sh.p_full(), (uint32_t)tile & 1u, a.status, a.wait_ns));
-                if (!ok) break;
-                tc_fence_after();
-                for (int c = 0; c < 8; ++c) {
-                    // chunk c comes from set c & 1: its ord-th context chunk, in slot
-                    // 2 (ord % 2) + (c & 1), next to its M-tile partner
-                    const int ord = 4 * tile + (c >> 1);
-                    const int slot = 2 * (ord & 1) + (c & 1);
-                    ok = __all_sync(kFull, wait_bar(sh, sh.full_c(slot), (uint32_t)(ord >> 1) & 1u, a.status, a.wait_ns));
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (c & 1) {
-                        // M-tile m = c/2 spans the slots of chunks c-1 (this - 1) and c
-                        const int m = c >> 1;
-                        const uint64_t a_desc = v_desc + (uint64_t)(((slot - 1) * kChunkBytes) >> 4);
-                        const uint32_t d = tmem + kColO + 64 * m;
-                        if (leader) {
-#pragma unroll
-                            for (int ks = 0; ks < kRT / 16; ++ks)
-                                mma_f16_ss(d, a_desc + (uint64_t)((2048 * ks) >> 4), p_desc + (uint64_t)((2048 * ks) >> 4),
-                                           idesc_c, (tile == 0 && ks == 0) ? 0u : 1u);
-                            mma_commit(sh.empty_c(slot - 1));
-                            mma_commit(sh.empty_c(slot));
-                        }
-                        __syncwarp();
-                    }
-                }
-                if (!ok) break;
-                if (leader) mma_commit(sh.o_done());
-                __syncwarp();
-            }
+            if (!ok) break;
+            if (leader) mma_commit(sh.s_full());
+            __syncwarp();
         }
-        // drain: every MMA issued so far completes before tensor memory is freed, and
-        // the Q copy has landed before the CTA's shared memory is released
+        // drain: this warp's MMAs complete before tensor memory is freed, and the Q copy
+        // has landed before the CTA's shared memory is released
         if (leader) {
             mma_commit(sh.drain());
             if (!mbar_wait(sh.drain(), 0, kTimeoutNs) && a.status)
