@@ -615,7 +615,8 @@ def decode_records(args, dev, wanted=lambda name: True):
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     signs = torch.from_numpy(W.sign_bits(0)).to(dev)
-    names = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma", 4: "tcgen05x16", 5: "tcgen05-e4m3"}
+    names = {1: "cuda-cores", 2: "tcgen05", 3: "warp-mma", 4: "tcgen05x16", 5: "tcgen05-e4m3",
+             6: "tcgen05-e4m3 (fp8 seqs) + tcgen05 (TQ4 seqs)"}
     target = 512 << 20
     records = []
 

@@ -303,11 +303,13 @@ size_t kvq_mla_decode_workspace(const kvq_mla_problem* p);
  * The decode kernel kvq_mla_decode runs for this problem: 1 the CUDA-core kernel, 2 the
  * tcgen05 kernel with 32 heads a CTA, 3 the warp-level MMA kernel, 4 the tcgen05 kernel
  * with 16 heads a CTA and each code converted once, 5 the e4m3 tcgen05 kernel of the fp8
- * tier; `impl` when it is non-zero, else the library's choice (fp8 problems of 8 or more
- * heads without a top-k list and with n_seq * n_q * ceil(H / 16) * ceil(rows / 128) >= 64:
- * 5; other fp8 problems of at most 16 heads or with a top-k list: 3; TQ4
- * problems of 8 to 16 heads and 3- or 6-bit problems of 8 or more heads: 4; other
- * problems of 8 or more heads: 2; the rest: 1).  Host
+ * tier, 6 both 5 (for the batch's fp8 sequences) and 2 (for its TQ4 sequences) in one
+ * call; `impl` when it is non-zero, else the library's choice.  With W =
+ * n_seq * n_q * ceil(H / 16) * ceil(rows / 128) tile-units of work: fp8 problems of 8 or
+ * more heads without a top-k list and W >= 64: 5; batches of per-sequence formats
+ * (seq_fmt) of 8 or more heads without a top-k list and W >= 64: 6; other fp8 problems of
+ * at most 16 heads or with a top-k list: 3; TQ4 problems of 8 to 16 heads and 3- or 6-bit
+ * problems of 8 or more heads: 4; other problems of 8 or more heads: 2; the rest: 1.  Host
  * only, nothing enqueued.  An invalid problem returns the negated status
  * kvq_mla_decode would return (-KVQ_EINVAL, -KVQ_EFORMAT, -KVQ_EALIGN).
  */

@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 FMT_FP8, FMT_TQ4, FMT_Q4_0, FMT_TQ6, FMT_TQ3 = 1, 2, 3, 4, 5
 TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code width
 IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16, IMPL_TCF8 = 0, 1, 2, 3, 4, 5
+IMPL_BY_FMT = 6   # kvq_mla_decode_kernel only: fp8 sequences on IMPL_TCF8, TQ4 ones on IMPL_TC
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_FORMAT = 1, 2, 4, 8
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: "KVQ_EALIGN",
           5: "KVQ_EWORKSPACE", 6: "KVQ_ECUDA", 7: "KVQ_EFAULT_INJECTED", 8: "KVQ_EMISMATCH",
@@ -300,7 +301,8 @@ def kvq_mla_decode_workspace(p: MlaProblem) -> int:
 
 
 def kvq_mla_decode_kernel(p: MlaProblem) -> int:
-    """The kernel kvq_mla_decode runs for p: IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16 or IMPL_TCF8."""
+    """The kernel kvq_mla_decode runs for p: IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16, IMPL_TCF8
+    or IMPL_BY_FMT (a batch of per-sequence formats split by tier)."""
     r = lib().kvq_mla_decode_kernel(C.byref(p))
     if r < 0:
         _check(-r)

@@ -295,7 +295,7 @@ int kvq_mla_decode_kernel(const kvq_mla_problem* p)
     if (int st = validate_decode(p, "kvq_mla_decode_kernel")) return -st;
     kvq::DecodePlan plan;
     kvq::plan_decode(*p, plan);
-    return plan.tcf8 ? 5 : plan.tc16 ? 4 : plan.mma ? 3 : plan.tc ? 2 : 1;
+    return plan.by_fmt ? 6 : plan.tcf8 ? 5 : plan.tc16 ? 4 : plan.mma ? 3 : plan.tc ? 2 : 1;
 }
 
 }  // extern "C"

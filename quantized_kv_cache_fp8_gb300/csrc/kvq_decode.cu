@@ -557,15 +557,15 @@ int sm_count()
 namespace {
 
 // rows per split for the tensor-core kernels (whole 128-row tiles): one CTA per SM over
-// all (sequence, query, head group) units, or about four waves when the units alone
+// all (sequence, query, head group) units, or about `waves` waves when the units alone
 // fill the SMs
-int64_t plan_tc_split_rows(int64_t units, int64_t n_cand, int64_t n_sm)
+int64_t plan_tc_split_rows(int64_t units, int64_t n_cand, int64_t n_sm, int64_t waves)
 {
     constexpr int kTile = 128;
     const int64_t tiles = std::max<int64_t>(1, (n_cand + kTile - 1) / kTile);
     int64_t split_tiles;
     if (units >= n_sm) {
-        split_tiles = std::max<int64_t>(1, (units * tiles + 4 * n_sm - 1) / (4 * n_sm));
+        split_tiles = std::max<int64_t>(1, (units * tiles + waves * n_sm - 1) / (waves * n_sm));
     } else {
         const int64_t splits = std::max<int64_t>(1, std::min<int64_t>(tiles, n_sm / units));
         split_tiles = (tiles + splits - 1) / splits;
@@ -597,25 +597,35 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
     // warp-level MMA kernel is faster; T = 32768: 256 units, the e4m3 kernel is)
     const int64_t tcf8_units = (int64_t)p.n_seq * p.n_q * ((p.n_heads + 15) / 16) * ((n_cand + 127) / 128);
     plan.tcf8 = p.impl == 5 || (p.impl == 0 && uniform_fp8 && p.n_heads >= 8 && !p.idx && tcf8_units >= 64);
+    // a batch of per-sequence formats (fp8 and TQ4) of as much work: its fp8 sequences on
+    // the e4m3 kernel and its TQ4 sequences on the 32-head kernel, into one set of partials
+    plan.by_fmt = p.impl == 0 && p.seq_fmt != nullptr && p.n_heads >= 8 && !p.idx && tcf8_units >= 64;
     plan.tc16 = !plan.tcf8 && (p.impl == 4 || (p.impl == 0 && p.n_heads >= 8 &&
                                 ((uniform_tq4 && p.n_heads <= 16) || uniform_tqb)));
     plan.mma = p.impl == 3 || (p.impl == 0 && !plan.tcf8 && uniform_fp8 && (p.n_heads <= 16 || p.idx != nullptr));
-    plan.tc = p.impl == 2 || (p.impl == 0 && !plan.tcf8 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
-                              !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
+    plan.tc = p.impl == 2 || plan.by_fmt ||
+              (p.impl == 0 && !plan.tcf8 && !plan.mma && !plan.tc16 && p.n_heads >= 8 &&
+               !(p.fmt == KVQ_FMT_TQ3 || p.fmt == KVQ_FMT_TQ6));
     int64_t split_rows = p.split_rows;
+    // A batch of several sequences is split into about 16 waves of CTAs rather than 4: its
+    // sequences may have many lengths (the plan sees only the longest), so shorter splits
+    // even out the last wave (ragged batch of 32 sequences on the 32-head kernel: 4855 us
+    // in 4 waves, 4107 us in 16).
+    const int64_t waves = p.n_seq > 1 ? 16 : 4;
     if (plan.tc16 || plan.tcf8) {
         constexpr int kHeads = 16;
         plan.head_block = kHeads;
         const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeads - 1) / kHeads));
-        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm);
+        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm, waves);
     } else if (plan.mma) {
         plan.head_block = mma_head_block();
         if (split_rows <= 0) plan_mma_splits(p, n_cand, split_rows);
     } else if (plan.tc) {
+        // (a batch split by tier takes these splits for both of its kernels)
         constexpr int kHeads = 32;
         plan.head_block = kHeads;
         const int64_t units = std::max<int64_t>(1, (int64_t)p.n_seq * p.n_q * ((p.n_heads + kHeads - 1) / kHeads));
-        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm);
+        if (split_rows <= 0) split_rows = plan_tc_split_rows(units, n_cand, n_sm, waves);
     } else {
         plan.head_block = kGH;
         const int64_t n_hblk = (p.n_heads + kGH - 1) / kGH;
@@ -667,8 +677,19 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
         int64_t g = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
         rotate_queries_kernel<<<(int)std::max<int64_t>(g, 1), kThreads, 0, s>>>(a);
     }
+    if (plan.by_fmt) {
+        // the fp8 sequences on the e4m3 kernel, then the TQ4 ones on the 32-head kernel
+        // (an ordinary launch of its query image after the e4m3 kernel, so the combine,
+        // dependent on the 32-head kernel, reads the partials of both)
+        cudaError_t e = launch_mla_decode_tcf8(p, plan, a.part_ml, a.part_o, dev_status, s, true);
+        if (e != cudaSuccess) return e;
+        e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml, a.part_o,
+                                 dev_status, s, true);
+        if (e != cudaSuccess) return e;
+        return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
+    }
     if (plan.tcf8) {
-        cudaError_t e = launch_mla_decode_tcf8(p, plan, a.part_ml, a.part_o, dev_status, s);
+        cudaError_t e = launch_mla_decode_tcf8(p, plan, a.part_ml, a.part_o, dev_status, s, false);
         if (e != cudaSuccess) return e;
         return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }
@@ -685,7 +706,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     }
     if (plan.tc) {
         cudaError_t e = launch_mla_decode_tc(p, plan, a.q_rot, base + plan.off_qimg, a.part_ml,
-                                             a.part_o, dev_status, s);
+                                             a.part_o, dev_status, s, false);
         if (e != cudaSuccess) return e;
         return launch_dependent(mla_combine_kernel, combine_grid(rows, plan), dim3(512), 0, s, a);
     }

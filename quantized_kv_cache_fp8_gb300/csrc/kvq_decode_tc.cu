@@ -58,6 +58,7 @@ struct TcArgs {
     int use_tma;                         // contiguous rows: chunks arrive by TMA
     kvq_mla_problem p;
     int split_rows, n_splits, n_hg;      // n_hg: head groups of 32
+    int fmt_split;                       // skip fp8 sequences (the e4m3 kernel reads them)
     const float* q_rot;                  // [n_seq][n_q][H][512] (TQ4 sequences)
     uint8_t* q_img;                      // [n_seq][n_q][n_hg][kQBytes]
     float* part_ml;
@@ -240,6 +241,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
     const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
     const bool bad_fmt = fmt != KVQ_FMT_FP8 && fmt != KVQ_FMT_TQ4;
     grid_dependents_launch();                    // the combine may start launching
+    if (fmt == KVQ_FMT_FP8 && a.fmt_split) return;   // the e4m3 kernel writes these partials
 
     if (r0 >= n_cand || bad_fmt) {
         if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
@@ -758,7 +760,7 @@ namespace {
 
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
-                                 uint32_t* dev_status, cudaStream_t s)
+                                 uint32_t* dev_status, cudaStream_t s, bool fmt_split)
 {
     TcArgs a;
     memset(&a, 0, sizeof(a));
@@ -777,6 +779,7 @@ cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& pla
     a.split_rows = plan.split_rows;
     a.n_splits = plan.n_splits;
     a.n_hg = (p.n_heads + kGQ - 1) / kGQ;
+    a.fmt_split = fmt_split ? 1 : 0;
     a.q_rot = q_rot;
     a.q_img = static_cast<uint8_t*>(q_img);
     a.part_ml = part_ml;

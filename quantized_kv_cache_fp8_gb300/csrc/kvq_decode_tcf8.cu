@@ -116,9 +116,11 @@ static_assert(kStageBytes % 1024 == 0 && kOffQ % 1024 == 0 && kQRope % 512 == 0 
 
 struct F8Args {
     CUtensorMap tm_lat, tm_rope;         // fp8 code planes ([128 x 128 B] and [128 x 64 B] boxes)
-    int use_tma;                         // contiguous rows: tiles arrive by TMA
+    int use_tma;                         // tiles arrive by TMA (contiguous rows, or pages)
+    int paged;                           // by TMA from pages: two boxes of 64 rows a tile
     kvq_mla_problem p;
     int split_rows, n_splits, n_hg;      // n_hg: head groups of 16
+    int fmt_split;                       // skip non-fp8 sequences (another kernel reads them)
     float* part_ml;
     float* part_o;
     uint32_t* status;
@@ -338,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
     const int64_t qrow = ((int64_t)s * p.n_q + q) * p.n_heads;
     const bool bad_fmt = seq_fmt_of(p, s) != KVQ_FMT_FP8;
     grid_dependents_launch();                    // the combine may start launching
+    if (bad_fmt && a.fmt_split) return;          // the other tier's kernel writes these partials
 
     if (r0 >= n_cand || bad_fmt) {
         if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
@@ -672,8 +675,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
             // stage refill from DRAM would sit on the critical path; tiles are prefetched
             // into L2 kPrefetch tiles ahead of their load instead.
             constexpr uint32_t kBoxBytes[kBoxes] = {kBox, kBox, kBox, kBox, kRopeBox};
+            // paged: the pool row of the 64-row half h of tile j, or -1 when the half holds
+            // no admissible row or its page is not in the table (the softmax clears the
+            // rows of the stage that are not admissible, whatever they hold)
+            auto half_row = [&](int j, int h) -> int {
+                const int64_t sr = r0 + (int64_t)j * kRT + 64 * h;
+                if (sr >= r1 || sr >= L) return -1;
+                const int64_t pr = pool_row_of(p, s, sr);
+                return (pr < 0 || pr > (int64_t)INT32_MAX - 64) ? -1 : (int)pr;
+            };
             auto prefetch = [&](int j) {
-                if (leader && j < NT) {
+                if (leader && j < NT && !a.paged) {
                     const int y = (int)(row0 + (int64_t)j * kRT);
 #pragma unroll
                     for (int b = 0; b < 4; ++b) tma_prefetch_2d(&a.tm_lat, 128 * b, y);
@@ -684,17 +696,37 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
             bool ok = true;
             int i = 0;
             int nb = 0;                               // boxes issued
+            int hy0 = 0, hy1 = 0;                     // paged: pool rows of tile i's halves
+            if (a.paged) {
+                hy0 = half_row(0, 0);
+                hy1 = half_row(0, 1);
+            }
             for (; i < NT && ok; ++i) {
                 const int st = i % kStages;
                 const int y = (int)(row0 + (int64_t)i * kRT);
+                const int y0 = hy0, y1 = hy1;
+                if (a.paged && i + 1 < NT) {          // the next tile's page lookups, in flight
+                    hy0 = half_row(i + 1, 0);         // while this tile's boxes wait
+                    hy1 = half_row(i + 1, 1);
+                }
                 // box b of tile i, as soon as the MMAs of tile i-2 are done with box b
                 for (int b = 0; b < kBoxes && ok; ++b) {
                     ok = __all_sync(kFull, wait_bar<kRoleSpin>(sh, sh.empty(st, b), ((uint32_t)(i / kStages) & 1u) ^ 1u, a.status, a.wait_ns));
                     if (!ok) break;
                     if (leader) {
-                        mbar_arrive_expect_tx(sh.full(st, b), kBoxBytes[b]);
-                        if (b < 4) tma_load_2d(sh.stage(st) + b * kBox, &a.tm_lat, 128 * b, y, sh.full(st, b));
-                        else tma_load_2d(sh.stage(st) + 4 * kBox, &a.tm_rope, 0, y, sh.full(st, b));
+                        const CUtensorMap* map = b < 4 ? &a.tm_lat : &a.tm_rope;
+                        uint8_t* dst = sh.stage(st) + b * kBox;
+                        const int x = b < 4 ? 128 * b : 0;
+                        if (!a.paged) {
+                            mbar_arrive_expect_tx(sh.full(st, b), kBoxBytes[b]);
+                            tma_load_2d(dst, map, x, y, sh.full(st, b));
+                        } else {
+                            // two boxes of 64 rows; their swizzle is that of one 128-row box
+                            const uint32_t half = kBoxBytes[b] / 2;
+                            mbar_arrive_expect_tx(sh.full(st, b), (y0 >= 0 ? half : 0u) + (y1 >= 0 ? half : 0u));
+                            if (y0 >= 0) tma_load_2d(dst, map, x, y0, sh.full(st, b));
+                            if (y1 >= 0) tma_load_2d(dst + half, map, x, y1, sh.full(st, b));
+                        }
                     }
                     ++nb;
                 }
@@ -847,17 +879,25 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
 }  // namespace
 
 cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, float* part_ml,
-                                   float* part_o, uint32_t* dev_status, cudaStream_t s)
+                                   float* part_o, uint32_t* dev_status, cudaStream_t s, bool fmt_split)
 {
     F8Args a;
     memset(&a, 0, sizeof(a));
-    if (!p.block_table && !p.idx)
+    if (!p.block_table && !p.idx) {
         a.use_tma = make_code_map(&a.tm_lat, p.fp8.lat, p.fp8.n_rows, kDLat, 128) &&
                     make_code_map(&a.tm_rope, p.fp8.rope, p.fp8.n_rows, kDRope, 64) ? 1 : 0;
+    } else if (p.block_table && !p.idx && p.page_size % 64 == 0 && plan.split_rows % 64 == 0) {
+        // pages of a multiple of 64 rows and splits on 64-row boundaries: each 64-row half
+        // of a tile lies in one page
+        a.use_tma = make_code_map(&a.tm_lat, p.fp8.lat, p.fp8.n_rows, kDLat, 128, 64) &&
+                    make_code_map(&a.tm_rope, p.fp8.rope, p.fp8.n_rows, kDRope, 64, 64) ? 1 : 0;
+        a.paged = a.use_tma;
+    }
     a.p = p;
     a.split_rows = plan.split_rows;
     a.n_splits = plan.n_splits;
     a.n_hg = (p.n_heads + kGQ - 1) / kGQ;
+    a.fmt_split = fmt_split ? 1 : 0;
     a.part_ml = part_ml;
     a.part_o = part_o;
     a.status = dev_status;

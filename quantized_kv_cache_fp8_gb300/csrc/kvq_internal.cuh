@@ -194,6 +194,8 @@ struct DecodePlan {
     bool tc16 = false;      // tensor-core (tcgen05) kernel, 16 heads a CTA, codes converted once
     bool tc = false;        // tensor-core (tcgen05) kernel, 32 heads a CTA
     bool mma = false;       // warp-level MMA kernel (blocks of 16 heads)
+    bool by_fmt = false;    // a batch of fp8 and TQ4 sequences: the fp8 ones on the e4m3
+                            // kernel, the TQ4 ones on the 32-head kernel (tc is set too)
     int split_rows = 0;     // candidate rows per split
     int n_splits = 0;       // splits per (seq, query) at most
     int n_cand_max = 0;     // candidate rows of the longest (seq, query)
@@ -205,13 +207,16 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
                               float* lse, void* ws, uint32_t* dev_status, cudaStream_t s);
 size_t tc_q_image_bytes(const kvq_mla_problem& p);
 size_t tc16_q_image_bytes(const kvq_mla_problem& p);
+// fmt_split: the kernel reads the sequences of its own tier only and leaves the others'
+// partials to the kernel of the other tier (the e4m3 kernel skips non-fp8 sequences, the
+// 32-head kernel fp8 ones)
 cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& plan, float* part_ml,
-                                   float* part_o, uint32_t* dev_status, cudaStream_t s);
+                                   float* part_o, uint32_t* dev_status, cudaStream_t s, bool fmt_split);
 cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& plan, void* q_img,
                                    float* part_ml, float* part_o, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_mla_decode_tc(const kvq_mla_problem& p, const DecodePlan& plan,
                                  const float* q_rot, void* q_img, float* part_ml, float* part_o,
-                                 uint32_t* dev_status, cudaStream_t s);
+                                 uint32_t* dev_status, cudaStream_t s, bool fmt_split);
 
 // the warp-level MMA decode (kvq_decode_mma.cu)
 int mma_head_block();

@@ -259,16 +259,17 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// [n_rows x row_bytes] bytes, boxes of [128 rows x box_bytes] (128-byte boxes
+// [n_rows x row_bytes] bytes, boxes of [box_rows x box_bytes] (128-byte boxes
 // 128B-swizzled, 64-byte boxes 64B-swizzled, 32-byte boxes 32B-swizzled, 48-byte boxes
 // unswizzled); rows past n_rows read as 0
-inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes)
+inline bool make_code_map(CUtensorMap* m, const uint8_t* plane, int64_t n_rows, int row_bytes, int box_bytes,
+                          int box_rows = 128)
 {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc || !plane || n_rows < 1 || n_rows > INT32_MAX) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)n_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)128};
+    const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(plane), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -112,6 +112,15 @@ def test_decode_kernel_choice(kvq):
     assert k(n_heads=16, fmt=kvq.FMT_TQ6) == kvq.IMPL_TC16
     assert k(n_heads=64, fmt=kvq.FMT_TQ3) == kvq.IMPL_TC16
     assert k(n_heads=4, fmt=kvq.FMT_TQ6) == kvq.IMPL_SIMT
+    # per-sequence formats: split by tier once there are 64 tile-units of work
+    mixed = dict(seq_fmt=FAKE, fp8=kvq.MlaCache(FAKE, FAKE, FAKE, FAKE, 32768))
+    assert k(n_heads=64, **mixed) == kvq.IMPL_BY_FMT
+    assert k(n_heads=16, **mixed) == kvq.IMPL_BY_FMT
+    assert k(n_heads=16, max_seq_len=1024, **mixed) == kvq.IMPL_TC        # 8 tile-units
+    assert k(n_heads=64, idx=FAKE, top_k=2048, **mixed) == kvq.IMPL_TC
+    assert k(n_heads=4, **mixed) == kvq.IMPL_SIMT
+    for impl in (1, 2, 3, 4):
+        assert k(n_heads=64, impl=impl, **mixed) == impl
     for impl in (1, 2, 3, 4):
         assert k(n_heads=16, impl=impl) == impl
     for impl in (1, 2, 3, 4, 5):

@@ -39,7 +39,7 @@ def encode(orc, rows, fmt, signs=None):
 
 def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=None,
             seq_fmt=None, idx=None, causal=False, block_table=None, page_size=0,
-            seq_stride_rows=0, split_rows=0, max_seq_len=None, impl=0):
+            seq_stride_rows=0, split_rows=0, max_seq_len=None, impl=0, kernel=None):
     if impl == 5 and (cache_fmt != 1 or seq_fmt is not None):
         pytest.skip("impl 5 reads problems of fp8 rows only")
     dcaches = {f: {k: dev(v) for k, v in c.items()} for f, c in caches.items()}
@@ -53,6 +53,8 @@ def run_gpu(kvq, *, cache_fmt, caches, seq_len, q, sm_scale=W.SM_SCALE, signs=No
         tq4=dcaches.get(2), signs=None if signs is None else dev(signs),
         idx=None if idx is None else dev(idx), split_rows=split_rows, impl=impl)
     keep = (dcaches, p)
+    if kernel is not None:
+        assert kvq.kvq_mla_decode_kernel(p) == kernel
     ws = torch.empty(max(1, kvq.kvq_mla_decode_workspace(p)), dtype=torch.uint8, device="cuda")
     out = torch.full((n_seq, n_q, H, 512), np.nan, dtype=torch.float32, device="cuda")
     lse = torch.full((n_seq, n_q, H), np.nan, dtype=torch.float32, device="cuda")
@@ -320,6 +322,61 @@ def test_decode_mixed_tiers_many_splits(kvq, orc, impl):
                                      tq4=caches[2], signs=signs)
     assert st == 0
     check(out, lse, ref, ref_lse)
+
+
+@pytest.mark.gpu
+def test_decode_mixed_batch_split_by_tier(kvq, orc):
+    """The library's choice for a seq_fmt batch with enough work: its fp8 sequences on the
+    e4m3 kernel and its TQ4 sequences on the 32-head kernel, into one set of partials.
+    A paged causal ragged batch (lengths 0, 1, 3 and U{500..3000}, 4 queries, 16 heads)
+    and an fp8 + TQ4 pair in splits of 32 rows (157 splits)."""
+    wl = W.ragged(n_seq=8, n_q=4, H=16, len_lo=500, len_hi=3000, page_size=64, seed=5)
+    wl.seq_len[0] = 0
+    wl.seq_len[1] = 1
+    wl.seq_len[5] = 3
+    caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
+    kw = dict(cache_fmt=1, caches=caches, seq_len=wl.seq_len, q=wl.queries, signs=wl.signs,
+              seq_fmt=wl.seq_fmt, causal=True, block_table=wl.block_table, page_size=wl.page_size)
+    out, lse, st = run_gpu(kvq, impl=0, kernel=kvq.IMPL_BY_FMT, **kw)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=wl.seq_len, seq_fmt=wl.seq_fmt, q_lat=wl.queries.q_lat,
+                                     q_rope=wl.queries.q_rope, sm_scale=W.SM_SCALE, causal=True,
+                                     block_table=wl.block_table, page_size=wl.page_size,
+                                     fp8=caches[1], tq4=caches[2], signs=wl.signs)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+    T = 5000
+    rows = W.magnitude_rows(2 * T, seed=49, lo=1e-2, hi=10.0)
+    signs = W.sign_bits(49)
+    caches = {1: encode(orc, rows, 1), 2: encode(orc, rows, 2, signs)}
+    q = W.queries(2, 1, 16, seed=49)
+    kw = dict(seq_len=[T, T], q=q, signs=signs, seq_fmt=[2, 1], seq_stride_rows=T, split_rows=32)
+    out, lse, st = run_gpu(kvq, impl=0, kernel=kvq.IMPL_BY_FMT, cache_fmt=1, caches=caches, **kw)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=[T, T], seq_fmt=[2, 1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                     sm_scale=W.SM_SCALE, seq_stride_rows=T, fp8=caches[1],
+                                     tq4=caches[2], signs=signs)
+    assert st == 0
+    check(out, lse, ref, ref_lse)
+
+
+@pytest.mark.gpu
+@pytest.mark.slow
+def test_decode_ragged_workload_split_by_tier(kvq, orc):
+    """The full ragged batch under the library's choice (fp8 sequences on the e4m3
+    kernel, TQ4 ones on the 32-head kernel); the oracle checks 8 heads of 4 sequences."""
+    wl = W.ragged(seed=0)
+    caches = {f: encode(orc, wl.rows[f], f, wl.signs) for f in (1, 2)}
+    out, lse, st = run_gpu(kvq, impl=0, kernel=kvq.IMPL_BY_FMT, cache_fmt=1, caches=caches,
+                           seq_len=wl.seq_len, q=wl.queries, signs=wl.signs, seq_fmt=wl.seq_fmt,
+                           causal=True, block_table=wl.block_table, page_size=wl.page_size)
+    sel = np.array([0, 7, 16, 31], np.int32)
+    ref, ref_lse, _ = orc.mla_decode(seq_len=wl.seq_len, seq_fmt=wl.seq_fmt, q_lat=wl.queries.q_lat,
+                                     q_rope=wl.queries.q_rope, sm_scale=W.SM_SCALE, causal=True,
+                                     block_table=wl.block_table, page_size=wl.page_size,
+                                     fp8=caches[1], tq4=caches[2], signs=wl.signs, seq_sel=sel,
+                                     heads=(0, 8))
+    assert st == 0
+    check(out[sel][:, :, :8], lse[sel][:, :, :8], ref[sel][:, :, :8], ref_lse[sel][:, :, :8])
 
 
 @pytest.mark.parametrize("fmt", [1, 2])
