@@ -4,8 +4,9 @@ Workload (the 4-bit rotated-int4 tier): a decode step of a 32-layer MLA stack, e
 layer with its own cache of T = 32768 rows (512-wide latent as TQ4 codes + radius,
 64-wide rope key as fp8 + scale, 328 B/row; 343 MB in all, larger than L2), H = 64
 heads, one query.  Per layer and step: quantize-on-append of the new token's row
-(kvq_encode_tq4 + kvq_encode_fp8 into row T-1), then kvq_mla_decode over the T rows
-(query rotation, split-T partials, log-sum-exp combine + unrotation).
+(kvq_encode_mla: its TQ4 latent and fp8 rope key into row T-1, one launch), then
+kvq_mla_decode over the T rows (query image, split-T partials, log-sum-exp combine +
+unrotation).
 
 metric  KV rows/s = layers x T / step time (higher is better); effective GB/s in the
         roofline object.
@@ -293,8 +294,8 @@ def run_ours(args, world, rank, local):
 
     def encode_step():
         for l in range(Lyr):
-            kvq.kvq_encode_tq4(new_c[l:l + 1], signs, lat[l, T - 1:T], rad[l, T - 1:T])
-            kvq.kvq_encode_fp8(new_r[l:l + 1], rope[l, T - 1:T], rsc[l, T - 1:T])
+            kvq.kvq_encode_mla(new_c[l:l + 1], new_r[l:l + 1], kvq.FMT_TQ4, signs, lat[l, T - 1:T],
+                               rad[l, T - 1:T], rope[l, T - 1:T], rsc[l, T - 1:T])
 
     def decode_step():
         for l in range(Lyr):
@@ -307,7 +308,7 @@ def run_ours(args, world, rank, local):
         encode_step()
     with torch.cuda.graph(g_dec):
         decode_step()
-    launches_per_step = Lyr * 2 + Lyr * 3          # encodes + (rotate, decode, combine)
+    launches_per_step = Lyr * 1 + Lyr * 3          # append + (query image, decode, combine)
 
     for _ in range(max(3, args.warmup)):
         g_enc.replay(); g_dec.replay()
@@ -500,7 +501,17 @@ def run_codecs(args, local):
         report(f"kvq_encode_tq ({bits} bits)", f"T={T} rows of 512",
                T * (512 * 4 + 512 * bits // 8 + 4) + 64, s, T, "rows")
         del pk
-    del x, packed, rad
+    # append-time form: a row's TQ4 latent and fp8 rope key in one launch, in bulk and
+    # for a single row (the per-token append of one layer)
+    xr = torch.randn(T, 64, generator=gen, device=dev)
+    rc = torch.empty(T, 64, dtype=torch.uint8, device=dev)
+    rs = torch.empty(T, device=dev)
+    s = timed(lambda: kvq.kvq_encode_mla(x, xr, kvq.FMT_TQ4, signs, packed, rad, rc, rs))
+    report("kvq_encode_mla (TQ4 + fp8 rope)", f"T={T} rows of 512 + 64 (one launch)",
+           T * (576 * 4 + 256 + 4 + 64 + 4) + 64, s, T, "rows")
+    s = timed(lambda: kvq.kvq_encode_mla(x[:1], xr[:1], kvq.FMT_TQ4, signs, packed[:1], rad[:1], rc[:1], rs[:1]))
+    report("kvq_encode_mla (TQ4 + fp8 rope)", "1 row (a per-token append)", 576 * 4 + 256 + 4 + 64 + 4, s, 1, "rows")
+    del x, xr, packed, rad, rc, rs
 
     # a3 / a4: q4_0 paged append and gather, 16 sequences x 8192 tokens x 8 heads x 256
     n_seq, n_tok, n_heads, ps = 16, 8192, 8, 64

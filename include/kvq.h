@@ -170,6 +170,32 @@ int kvq_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
                   kvq_stream_t stream);
 
 /*
+ * Quantize-on-append of MLA rows, both planes in one call — colibri PR #399, Commit 1
+ * (the fp8 tier) and Commit 2 (the rotated tier): the latent of a row goes to the
+ * cache's tier, its rope key to fp8.  Row r's latent c_lat[r] (512 dims) is encoded as
+ * kvq_encode_fp8 (fmt KVQ_FMT_FP8) or kvq_encode_tq (KVQ_FMT_TQ3 / TQ4 / TQ6, rotation
+ * signs `sign_bits`) would encode it, into lat + r * ldl and lat_scale[r]; its rope key
+ * k_rope[r] (64 dims) as kvq_encode_fp8 would, into rope + r * ldc and rope_scale[r].
+ * The bytes equal those of the separate calls.  With 16-byte aligned input rows and
+ * 4-byte aligned fp8 code rows the two encoders run as one kernel launch (the latent and
+ * rope CTAs side by side), so a per-token append costs one launch; otherwise they run as
+ * the two separate kernels.
+ *   c_lat      device fp32 [rows] x ldx  (ldx >= 512)
+ *   k_rope     device fp32 [rows] x ldr  (ldr >= 64)
+ *   lat        device u8   [rows] x ldl  (ldl >= 512 * bits / 8; 8 bits for fp8)
+ *   lat_scale  device fp32 [rows]         (fp8: amax/448; rotated: the row radius)
+ *   rope       device u8   [rows] x ldc  (ldc >= 64)
+ *   rope_scale device fp32 [rows]
+ * Errors: KVQ_EFORMAT for another fmt; KVQ_EINVAL for rows < 0, a stride too small or
+ * a NULL pointer (sign_bits only for the rotated tiers); KVQ_EALIGN for a float pointer
+ * that is not 4-byte aligned.  rows == 0 is a no-op.
+ */
+int kvq_encode_mla(const float* c_lat, int64_t ldx, const float* k_rope, int64_t ldr,
+                   int64_t rows, int fmt, const uint32_t* sign_bits, uint8_t* lat,
+                   int64_t ldl, float* lat_scale, uint8_t* rope, int64_t ldc,
+                   float* rope_scale, kvq_stream_t stream);
+
+/*
  * q4_0 paged append — Strata PR #2533, kv_q4.metal port commit (fwht256, q4_group /
  * q4_store, the tie rule, the fp16 scale) and the page-table commit.  Token t of
  * sequence s sits at position pos = pos0[s] + t and cell

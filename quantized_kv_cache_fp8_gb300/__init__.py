@@ -19,7 +19,7 @@ __all__ = [
     "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "kvq_mla_decode_kernel",
     "MlaCache",
     "MlaProblem", "Q4Problem", "make_q4_problem", "kvq_q4_decode", "kvq_q4_decode_workspace",
-    "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "FMT_TQ6", "FMT_TQ3", "TQ_FMT", "kvq_encode_tq",
+    "FMT_FP8", "FMT_TQ4", "FMT_Q4_0", "FMT_TQ6", "FMT_TQ3", "TQ_FMT", "kvq_encode_tq", "kvq_encode_mla",
     "kvq_tq_codebook", "DEV_BAD_INDEX", "DEV_BAD_PAGE", "DEV_TIMEOUT",
     "DEV_BAD_FORMAT",
 ]
@@ -40,7 +40,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_set_wait_limit_ns",
            "kvq_tq4_codebook", "kvq_tq_codebook", "kvq_encode_fp8", "kvq_encode_tq4",
-           "kvq_encode_tq", "kvq_append_q4",
+           "kvq_encode_tq", "kvq_encode_mla", "kvq_append_q4",
            "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode_kernel", "kvq_mla_decode",
            "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode",
            "kvq_cache_probe", "kvq_cache_save", "kvq_cache_save_f32", "kvq_cache_append",
@@ -130,6 +130,8 @@ def _declare(L):
     L.kvq_tq_codebook.argtypes = [C.c_int, _p, _p]
     L.kvq_encode_tq.restype = C.c_int
     L.kvq_encode_tq.argtypes = [_p, _i64, C.c_int, _i64, C.c_int, _p, _p, _i64, _p, _p]
+    L.kvq_encode_mla.restype = C.c_int
+    L.kvq_encode_mla.argtypes = [_p, _i64, _p, _i64, _i64, C.c_int, _p, _p, _i64, _p, _p, _i64, _p, _p]
     L.kvq_encode_tq4.restype = C.c_int
     L.kvq_encode_tq4.argtypes = [_p, _i64, C.c_int, _i64, _p, _p, _i64, _p, _p]
     L.kvq_append_q4.restype = C.c_int
@@ -226,6 +228,16 @@ def kvq_encode_tq(x, sign_bits, bits, packed, radius, stream=None) -> None:
     rows, dim = x.shape
     _check(lib().kvq_encode_tq(_ptr(x), rows, dim, x.stride(0), int(bits), _ptr(sign_bits),
                                _ptr(packed), packed.stride(0), _ptr(radius), _stream(stream)))
+
+
+def kvq_encode_mla(c_lat, k_rope, fmt, sign_bits, lat, lat_scale, rope, rope_scale, stream=None) -> None:
+    """Append-time encode of MLA rows: latent c_lat fp32 [rows][512] into the tier `fmt`
+    (lat u8 [rows][>= 512 * bits / 8], lat_scale fp32 [rows]) and rope key k_rope fp32
+    [rows][64] into fp8 (rope u8 [rows][>= 64], rope_scale fp32 [rows]), in one call."""
+    rows = c_lat.shape[0]
+    _check(lib().kvq_encode_mla(_ptr(c_lat), c_lat.stride(0), _ptr(k_rope), k_rope.stride(0), rows,
+                                int(fmt), _ptr(sign_bits), _ptr(lat), lat.stride(0), _ptr(lat_scale),
+                                _ptr(rope), rope.stride(0), _ptr(rope_scale), _stream(stream)))
 
 
 def kvq_append_q4(k, v, pos0, page_table, page_size, n_cells, k_pool, v_pool,

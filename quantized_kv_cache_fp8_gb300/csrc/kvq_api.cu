@@ -187,6 +187,28 @@ int kvq_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
                                              (cudaStream_t)stream), E);
 }
 
+int kvq_encode_mla(const float* c_lat, int64_t ldx, const float* k_rope, int64_t ldr,
+                   int64_t rows, int fmt, const uint32_t* sign_bits, uint8_t* lat,
+                   int64_t ldl, float* lat_scale, uint8_t* rope, int64_t ldc,
+                   float* rope_scale, kvq_stream_t stream)
+{
+    const char* E = "kvq_encode_mla";
+    if (int st = injected(E)) return st;
+    if (fmt != KVQ_FMT_FP8 && !kvq::rotated_format(fmt)) return fail(KVQ_EFORMAT, "%s: fmt %d", E, fmt);
+    const int bits = fmt == KVQ_FMT_FP8 ? 8 : kvq::rotated_bits(fmt);
+    if (rows < 0) return fail(KVQ_EINVAL, "%s: rows < 0", E);
+    if (ldx < kvq::kDLat || ldr < kvq::kDRope || ldl < (int64_t)kvq::kDLat * bits / 8 || ldc < kvq::kDRope)
+        return fail(KVQ_EINVAL, "%s: a row stride is smaller than its row", E);
+    if (rows == 0) return KVQ_OK;
+    if (!c_lat || !k_rope || !lat || !lat_scale || !rope || !rope_scale || (bits != 8 && !sign_bits))
+        return fail(KVQ_EINVAL, "%s: NULL pointer", E);
+    if (!aligned(c_lat, 4) || !aligned(k_rope, 4) || !aligned(lat_scale, 4) || !aligned(rope_scale, 4) ||
+        (bits != 8 && !aligned(sign_bits, 4)))
+        return fail(KVQ_EALIGN, "%s: a float or sign pointer is not 4-byte aligned", E);
+    return cuda_status(kvq::launch_encode_mla(c_lat, ldx, k_rope, ldr, rows, fmt, sign_bits, lat, ldl,
+                                              lat_scale, rope, ldc, rope_scale, (cudaStream_t)stream), E);
+}
+
 int kvq_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0, int n_tok,
                   int n_heads, int head_dim, const int32_t* page_table, int max_pages,
                   int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,

@@ -47,17 +47,16 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
 
 // LANES lanes per row (1 <= LANES <= 32, power of two), VPL float4 per lane:
 // dim = 4 * VPL * LANES.  Requires 16-byte aligned x rows and 4-byte aligned code rows.
+// Warp `warp` of `n_warps` takes every n_warps-th group of 32 / LANES rows.
 template <int LANES, int VPL>
-__global__ void __launch_bounds__(kCodecThreads)
-encode_fp8_vec_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
-                      uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales)
+__device__ __forceinline__ void encode_fp8_vec_rows(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                                                    uint8_t* __restrict__ codes, int64_t ldc,
+                                                    float* __restrict__ scales, int64_t warp, int64_t n_warps)
 {
     constexpr int kRowsPerWarp = 32 / LANES;
     const int lane = threadIdx.x & 31;
     const int sub = lane / LANES;
     const int l = lane % LANES;
-    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t r0 = warp * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
         const int64_t r = r0 + sub;
         const bool valid = r < rows;
@@ -88,6 +87,16 @@ encode_fp8_vec_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
         }
         if (l == 0) scales[r] = s;
     }
+}
+
+template <int LANES, int VPL>
+__global__ void __launch_bounds__(kCodecThreads)
+encode_fp8_vec_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                      uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales)
+{
+    encode_fp8_vec_rows<LANES, VPL>(x, rows, ldx, codes, ldc, scales,
+                                    (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5,
+                                    ((int64_t)gridDim.x * blockDim.x) >> 5);
 }
 
 // Any dim / alignment: one warp per row, two passes over the row.
@@ -317,11 +326,14 @@ __device__ __forceinline__ const float* tq512_thresholds()
     else return c_tq6.thr;
 }
 
+// Rows warp, warp + n_warps, ... of the grid's warps; every thread of the CTA calls it
+// (the bucket table is built by the CTA)
 template <int BITS>
-__global__ void __launch_bounds__(kCodecThreads)
-encode_tq512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
-                    const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
-                    int64_t ldp, float* __restrict__ radius, bool vec_store)
+__device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                                                  const uint32_t* __restrict__ sign_bits,
+                                                  uint8_t* __restrict__ packed, int64_t ldp,
+                                                  float* __restrict__ radius, bool vec_store,
+                                                  int64_t warp, int64_t n_warps)
 {
     using G = Tq512Grid<BITS>;
     constexpr int kNThr = (1 << BITS) - 1;
@@ -349,8 +361,6 @@ encode_tq512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
     const float sgn256 = (lane & 16) ? -1.0f : 1.0f;      // upper half of the h = 256 stage
     float* st = s_t[wib];
 
-    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     // each warp walks its rows with the next row's loads in flight during this row's work
     float4 nx[4];
     if (warp < rows) {
@@ -486,6 +496,42 @@ encode_tq512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
         }
         __syncwarp();
         if (lane == 0) radius[r] = rad;
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kCodecThreads)
+encode_tq512_kernel(const float* __restrict__ x, int64_t rows, int64_t ldx,
+                    const uint32_t* __restrict__ sign_bits, uint8_t* __restrict__ packed,
+                    int64_t ldp, float* __restrict__ radius, bool vec_store)
+{
+    encode_tq512_rows<BITS>(x, rows, ldx, sign_bits, packed, ldp, radius, vec_store,
+                            (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5,
+                            ((int64_t)gridDim.x * blockDim.x) >> 5);
+}
+
+// ------------------------------------------------------------------------------------
+// Quantize-on-append of MLA rows in one launch: blockIdx.y = 0 encodes the latent rows
+// (512 dims; BITS = 8: fp8, else the rotated tier at BITS bits), blockIdx.y = 1 the rope
+// keys (64 dims, fp8), with the device code of the separate encoders (the same bytes).
+// Both sets of CTAs run at once; a per-token append is one launch instead of two.
+// ------------------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(kCodecThreads)
+encode_mla_kernel(const float* __restrict__ c_lat, int64_t ldx, const float* __restrict__ k_rope,
+                  int64_t ldr, int64_t rows, const uint32_t* __restrict__ sign_bits,
+                  uint8_t* __restrict__ lat, int64_t ldl, float* __restrict__ lat_scale,
+                  uint8_t* __restrict__ rope, int64_t ldc, float* __restrict__ rope_scale, bool vec_store)
+{
+    const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    if (blockIdx.y == 1) {
+        encode_fp8_vec_rows<16, 1>(k_rope, rows, ldr, rope, ldc, rope_scale, warp, n_warps);
+    } else {
+        if constexpr (BITS == 8)
+            encode_fp8_vec_rows<32, 4>(c_lat, rows, ldx, lat, ldl, lat_scale, warp, n_warps);
+        else
+            encode_tq512_rows<BITS>(c_lat, rows, ldx, sign_bits, lat, ldl, lat_scale, vec_store, warp, n_warps);
     }
 }
 
@@ -892,6 +938,63 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_encode_mla_fused(const float* c_lat, int64_t ldx, const float* k_rope, int64_t ldr,
+                                    int64_t rows, const uint32_t* sign_bits, uint8_t* lat, int64_t ldl,
+                                    float* lat_scale, uint8_t* rope, int64_t ldc, float* rope_scale,
+                                    bool vec, cudaStream_t s)
+{
+    // the latent CTAs sized as the separate encoder would be (one wave of the rotated
+    // encoder, by this kernel's occupancy); the rope CTAs share the count and stride
+    int64_t g;
+    if constexpr (BITS == 8) {
+        g = grid_for(rows, kCodecWarps);
+    } else {
+        static std::atomic<int> per_sm{0};
+        int n = per_sm.load();
+        if (n <= 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, encode_mla_kernel<BITS>, kCodecThreads, 0) !=
+                    cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();
+                n = 1;
+            }
+            per_sm.store(n);
+        }
+        g = std::max<int64_t>(1, std::min<int64_t>((rows + kCodecWarps - 1) / kCodecWarps, (int64_t)sm_count() * n));
+    }
+    encode_mla_kernel<BITS><<<dim3((unsigned)g, 2), kCodecThreads, 0, s>>>(
+        c_lat, ldx, k_rope, ldr, rows, sign_bits, lat, ldl, lat_scale, rope, ldc, rope_scale, vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_mla(const float* c_lat, int64_t ldx, const float* k_rope, int64_t ldr,
+                              int64_t rows, int fmt, const uint32_t* sign_bits, uint8_t* lat,
+                              int64_t ldl, float* lat_scale, uint8_t* rope, int64_t ldc,
+                              float* rope_scale, cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    const int bits = fmt == KVQ_FMT_FP8 ? 8 : rotated_bits(fmt);
+    // the one-launch form needs what the separate encoders' fast paths need: 16-byte
+    // aligned input rows, 4-byte aligned fp8 code rows; otherwise the two encoders run
+    const bool x16 = (uintptr_t)c_lat % 16 == 0 && ldx % 4 == 0 && (uintptr_t)k_rope % 16 == 0 && ldr % 4 == 0;
+    const bool c4 = (uintptr_t)rope % 4 == 0 && ldc % 4 == 0 &&
+                    (bits != 8 || ((uintptr_t)lat % 4 == 0 && ldl % 4 == 0));
+    if (!x16 || !c4) {
+        cudaError_t e = bits == 8 ? launch_encode_fp8(c_lat, rows, kDLat, ldx, lat, ldl, lat_scale, s)
+                                  : launch_encode_tq(c_lat, rows, kDLat, ldx, bits, sign_bits, lat, ldl, lat_scale, s);
+        if (e != cudaSuccess) return e;
+        return launch_encode_fp8(k_rope, rows, kDRope, ldr, rope, ldc, rope_scale, s);
+    }
+    const bool vec = ((uintptr_t)lat % 16 == 0) && (ldl % 16 == 0);
+    switch (bits) {
+        case 8: return launch_encode_mla_fused<8>(c_lat, ldx, k_rope, ldr, rows, sign_bits, lat, ldl, lat_scale, rope, ldc, rope_scale, vec, s);
+        case 4: return launch_encode_mla_fused<4>(c_lat, ldx, k_rope, ldr, rows, sign_bits, lat, ldl, lat_scale, rope, ldc, rope_scale, vec, s);
+        case 3: return launch_encode_mla_fused<3>(c_lat, ldx, k_rope, ldr, rows, sign_bits, lat, ldl, lat_scale, rope, ldc, rope_scale, vec, s);
+        case 6: return launch_encode_mla_fused<6>(c_lat, ldx, k_rope, ldr, rows, sign_bits, lat, ldl, lat_scale, rope, ldc, rope_scale, vec, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 void tq_codebook_values(int bits, float* centroids, float* thresholds)

@@ -180,6 +180,11 @@ cudaError_t launch_encode_tq4(const float* x, int64_t rows, int dim, int64_t ldx
 cudaError_t launch_encode_tq(const float* x, int64_t rows, int dim, int64_t ldx, int bits,
                              const uint32_t* sign_bits, uint8_t* packed, int64_t ldp,
                              float* radius, cudaStream_t s);
+// a row's latent (fp8 or rotated, by fmt) and rope key (fp8), one launch when aligned
+cudaError_t launch_encode_mla(const float* c_lat, int64_t ldx, const float* k_rope, int64_t ldr,
+                              int64_t rows, int fmt, const uint32_t* sign_bits, uint8_t* lat,
+                              int64_t ldl, float* lat_scale, uint8_t* rope, int64_t ldc,
+                              float* rope_scale, cudaStream_t s);
 // the stored codebook of width b (2^b centroids, 2^b - 1 thresholds), host side
 void tq_codebook_values(int bits, float* centroids, float* thresholds);
 cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0,

@@ -57,6 +57,25 @@ def test_encode_argument_errors(kvq):
     assert b"ldx" in L.kvq_last_error() or b"dim" in L.kvq_last_error() or True
 
 
+def test_encode_mla_argument_errors(kvq):
+    L = kvq.lib()
+    def call(fmt=kvq.FMT_TQ4, rows=1, ldx=512, ldr=64, ldl=256, ldc=64, c=FAKE, signs=FAKE, ls=FAKE):
+        return L.kvq_encode_mla(c, ldx, FAKE, ldr, rows, fmt, signs, FAKE, ldl, ls, FAKE, ldc, FAKE, None)
+    assert call(fmt=kvq.FMT_Q4_0) == 3                                    # not an MLA tier
+    assert call(rows=-1) == 1
+    assert call(ldx=511) == 1
+    assert call(ldr=63) == 1
+    assert call(ldl=255) == 1                                             # 4 bits: 256 bytes
+    assert call(fmt=kvq.FMT_TQ6, ldl=383) == 1                            # 6 bits: 384 bytes
+    assert call(fmt=kvq.FMT_FP8, ldl=511) == 1
+    assert call(ldc=63) == 1
+    assert call(c=None) == 1
+    assert call(signs=None) == 1                                          # rotated tier needs signs
+    assert call(c=FAKE + 2) == 4
+    assert call(ls=FAKE + 1) == 4
+    assert call(rows=0, c=None) == 0                                      # no-op
+
+
 def test_append_and_gather_argument_errors(kvq):
     L = kvq.lib()
     assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 250, FAKE, 1, 64, 64, FAKE, FAKE, None, None) == 2

@@ -279,3 +279,61 @@ def test_gather_rows_byte_exact(kvq, orc, fmt):
         got = dst[k].cpu().numpy()
         assert np.array_equal(got[good], host[idx[good]])
         assert not got[3].any()
+
+
+# ------------------------------------------------------- append-time MLA row encode ------
+
+@pytest.mark.parametrize("fmt,b", [(1, 8), (5, 3), (2, 4), (4, 6)], ids=["fp8", "tq3", "tq4", "tq6"])
+@pytest.mark.parametrize("T", [1, 7, 1000])
+def test_encode_mla_rows_match_oracle(kvq, orc, fmt, b, T):
+    """kvq_encode_mla (latent in the tier, rope key in fp8, one launch) against the
+    oracle's encoders: every code byte and scale bit pattern; magnitudes log-uniform
+    1e-3..40 with a zero row."""
+    rows = W.magnitude_rows(T, seed=90 + T, lo=1e-3, hi=40.0)
+    rows.c[0] = 0.0
+    signs = W.sign_bits(90)
+    lw = 512 * b // 8
+    lat = torch.full((T, lw), 0xAB, dtype=torch.uint8, device="cuda")
+    ls = torch.full((T,), -1.0, dtype=torch.float32, device="cuda")
+    rope = torch.full((T, 64), 0xAB, dtype=torch.uint8, device="cuda")
+    rs = torch.full((T,), -1.0, dtype=torch.float32, device="cuda")
+    kvq.kvq_encode_mla(dev(rows.c), dev(rows.k_rope), fmt, dev(signs), lat, ls, rope, rs)
+    torch.cuda.synchronize()
+    ref_lat, ref_ls = orc.encode_fp8(rows.c) if b == 8 else orc.encode_tq(rows.c, signs, b)
+    ref_rope, ref_rs = orc.encode_fp8(rows.k_rope)
+    assert np.array_equal(lat.cpu().numpy(), ref_lat)
+    assert np.array_equal(bits(ls.cpu().numpy()), bits(ref_ls))
+    assert np.array_equal(rope.cpu().numpy(), ref_rope)
+    assert np.array_equal(bits(rs.cpu().numpy()), bits(ref_rs))
+
+
+@pytest.mark.parametrize("fmt,b", [(1, 8), (2, 4)], ids=["fp8", "tq4"])
+def test_encode_mla_strided_and_unaligned(kvq, orc, fmt, b):
+    """Row strides wider than the rows (the one-launch form), and inputs 4 bytes off a
+    16-byte boundary (the two-kernel fallback), into rows of wider code planes; the
+    bytes past each row stay untouched."""
+    T = 33
+    rows = W.magnitude_rows(T, seed=97, lo=1e-2, hi=10.0)
+    signs = W.sign_bits(97)
+    lw = 512 * b // 8
+    ref_lat, ref_ls = orc.encode_fp8(rows.c) if b == 8 else orc.encode_tq(rows.c, signs, b)
+    ref_rope, ref_rs = orc.encode_fp8(rows.k_rope)
+    for off in (0, 1):                                   # floats of offset
+        cbuf = torch.zeros(T, 520 + off, dtype=torch.float32, device="cuda")
+        cbuf[:, off:off + 512] = dev(rows.c)
+        rbuf = torch.zeros(T, 72 + off, dtype=torch.float32, device="cuda")
+        rbuf[:, off:off + 64] = dev(rows.k_rope)
+        lat = torch.full((T, lw + 16), 0xAB, dtype=torch.uint8, device="cuda")
+        ls = torch.full((T,), -1.0, dtype=torch.float32, device="cuda")
+        rope = torch.full((T, 80), 0xAB, dtype=torch.uint8, device="cuda")
+        rs = torch.full((T,), -1.0, dtype=torch.float32, device="cuda")
+        kvq.kvq_encode_mla(cbuf[:, off:off + 512], rbuf[:, off:off + 64], fmt, dev(signs),
+                           lat[:, :lw], ls, rope[:, :64], rs)
+        torch.cuda.synchronize()
+        got_lat, got_rope = lat.cpu().numpy(), rope.cpu().numpy()
+        assert np.array_equal(got_lat[:, :lw], ref_lat)
+        assert np.all(got_lat[:, lw:] == 0xAB)
+        assert np.array_equal(bits(ls.cpu().numpy()), bits(ref_ls))
+        assert np.array_equal(got_rope[:, :64], ref_rope)
+        assert np.all(got_rope[:, 64:] == 0xAB)
+        assert np.array_equal(bits(rs.cpu().numpy()), bits(ref_rs))
