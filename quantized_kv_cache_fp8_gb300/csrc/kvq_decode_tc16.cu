@@ -231,6 +231,31 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
     const kvq_mla_cache& C = rot ? p.tq4 : p.fp8;
     const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
     const RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
+    // Contiguous rows: the loader sets up the stage barriers itself and requests each set's
+    // first kStages chunks at once, before the CTA-wide setup below (tensor memory, the
+    // other barriers), which would otherwise delay the first loads by ~1 us.
+    const bool pre = a.use_tma != 0;
+    if (warp == kWarpLoad && pre && lane == 0) {
+        for (int st = 0; st < kSets; ++st) {
+            for (int d = 0; d < kStages; ++d) {
+                mbar_init(sh.raw_full(st, d), 1);
+                mbar_init(sh.raw_empty(st, d), 4);       // one per warp of the set
+            }
+        }
+        fence_mbar_init();
+        const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;
+        static_assert(kStages <= kPer, "the first kStages chunks of a set are in tile 0");
+        for (int st = 0; st < kSets; ++st) {
+            for (int d = 0; d < kStages; ++d) {
+                const int ch = kSets * d + st;
+                const bool rope = ch == 0;
+                const int inner = rope ? 64 : lat_cb;
+                mbar_arrive_expect_tx(sh.raw_full(st, d), (uint32_t)(inner * kRT));
+                tma_load_2d(sh.stage(st, d), rope ? &a.tm_rope[rot ? 1 : 0] : &a.tm_lat[rot ? 1 : 0],
+                            rope ? 0 : (ch - 1) * inner, (int)row0, sh.raw_full(st, d));
+            }
+        }
+    }
 
     if (warp == kWarpMma) {
         if (lane == 0) {
@@ -239,7 +264,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                     mbar_init(sh.full_a(st, k), 4);      // one arrival per warp of the set
                     mbar_init(sh.empty_a(st, k), 1);     // MMA commit
                 }
-                for (int d = 0; d < kStages; ++d) {
+                for (int d = 0; d < kStages && !pre; ++d) {
                     mbar_init(sh.raw_full(st, d), 1);
                     mbar_init(sh.raw_empty(st, d), 4);   // one per warp of the set
                 }
@@ -613,7 +638,7 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
             const int n_own = kPer * NT;
             int nxt[kSets];                               // next item of each set
 #pragma unroll
-            for (int set = 0; set < kSets; ++set) nxt[set] = 0;
+            for (int set = 0; set < kSets; ++set) nxt[set] = kStages;   // the first went out at the start
             bool ok = true;
             uint64_t idle_since = 0;
             while (ok && (nxt[0] < n_own || nxt[1] < n_own || nxt[2] < n_own)) {

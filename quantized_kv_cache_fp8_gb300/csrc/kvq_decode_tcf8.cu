@@ -355,10 +355,32 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
     const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
     const RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
     const bool tma = a.use_tma != 0;
+    // Contiguous rows: the loader sets up the stage barriers itself and requests the first
+    // kStages tiles at once, before the CTA-wide setup below (tensor memory, the other
+    // barriers, the query loads), which would otherwise delay the first loads by ~1 us.
+    const int pre = (tma && !a.paged) ? min(NT, kStages) : 0;
+    if (warp == kWarpLoad && pre > 0 && lane == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            for (int b = 0; b < kBoxes; ++b) {
+                mbar_init(sh.full(st, b), 1);
+                mbar_init(sh.empty(st, b), 1);
+            }
+        }
+        fence_mbar_init();
+        const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;
+        for (int i = 0; i < pre; ++i) {
+            const int y = (int)(row0 + (int64_t)i * kRT);
+            for (int b = 0; b < kBoxes; ++b) {
+                mbar_arrive_expect_tx(sh.full(i, b), b < 4 ? kBox : kRopeBox);
+                tma_load_2d(sh.stage(i) + b * kBox, b < 4 ? &a.tm_lat : &a.tm_rope, b < 4 ? 128 * b : 0, y,
+                            sh.full(i, b));
+            }
+        }
+    }
 
     if (warp == kWarpS) {
         if (lane == 0) {
-            for (int st = 0; st < kStages; ++st) {
+            for (int st = 0; st < kStages && pre == 0; ++st) {
                 for (int b = 0; b < kBoxes; ++b) {
                     mbar_init(sh.full(st, b), tma ? 1 : kGatherThreads);   // TMA: the loader; else every gather thread
                     mbar_init(sh.empty(st, b), 1);
@@ -693,9 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
                 }
             };
             for (int j = kStages; j < kPrefetch; ++j) prefetch(j);
+            for (int j = 0; j < pre; ++j) prefetch(j + kPrefetch);
             bool ok = true;
-            int i = 0;
-            int nb = 0;                               // boxes issued
+            int i = pre;                              // the first `pre` tiles went out at the start
+            int nb = pre * kBoxes;                    // boxes issued
             int hy0 = 0, hy1 = 0;                     // paged: pool rows of tile i's halves
             if (a.paged) {
                 hy0 = half_row(0, 0);
