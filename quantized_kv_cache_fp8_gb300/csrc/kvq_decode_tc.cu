@@ -256,6 +256,30 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
     const kvq_mla_cache& C = tq4 ? p.tq4 : p.fp8;
     const int NT = (int)((r1 - r0 + kRT - 1) / kRT);
     const RowCtx rc{&p, s, q, L, r1, p.causal ? (int64_t)L - p.n_q + q : (int64_t)L - 1, &C, a.status};
+    // Contiguous rows: each loader sets up its set's stage barriers and requests the set's
+    // first kStages chunks before the CTA-wide setup below (tensor memory, the other
+    // barriers), which would otherwise delay the first loads.
+    const bool pre = a.use_tma != 0;
+    if ((warp == 13 || warp == 14) && pre && lane == 0) {
+        const int set = warp - 13;
+        for (int d = 0; d < kStages; ++d) {
+            mbar_init(sh.raw_full(set, d), 1);
+            mbar_init(sh.raw_empty(set, d), 4);       // one per warp of the set
+        }
+        fence_mbar_init();
+        const int64_t row0 = (int64_t)s * p.seq_stride_rows + r0;
+        int j = 0;
+        for (int n = 0; n < 17 * NT && j < kStages; ++n) {
+            const OwnItem it = common_item(n, NT);
+            if ((it.ch & 1) != set) continue;
+            const bool rope = it.ch == 8;
+            const int inner = (rope || !tq4) ? 64 : 32;
+            mbar_arrive_expect_tx(sh.raw_full(set, j), (uint32_t)(inner * kRT));
+            tma_load_2d(sh.stage(set, j), rope ? &a.tm_rope[tq4 ? 1 : 0] : &a.tm_lat[tq4 ? 1 : 0],
+                        rope ? 0 : it.ch * inner, (int)(row0 + (int64_t)it.tile * kRT), sh.raw_full(set, j));
+            ++j;
+        }
+    }
 
     if (warp == 12) {
         if (lane == 0) {
@@ -274,7 +298,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
             mbar_init(sh.drain(), 1);
             mbar_init(sh.drain_c(), 1);
             mbar_init(sh.q_full(), 1);
-            for (int i = 0; i < 2 * kStages; ++i) {
+            for (int i = 0; i < 2 * kStages && !pre; ++i) {
                 mbar_init(sh.raw_full(i / kStages, i % kStages), 1);
                 mbar_init(sh.raw_empty(i / kStages, i % kStages), 4);   // one per warp of the set
             }
@@ -606,6 +630,7 @@ __global__ void __maxnreg__(128) mla_decode_tc_kernel(const __grid_constant__ Tc
                 const int set = it.ch & 1;
                 if (set != my_set) continue;
                 const int j = set ? o1++ : o0++;
+                if (j < kStages) continue;            // requested at the start
                 const int d = j % kStages;
                 ok = __all_sync(kFull, wait_bar(sh, sh.raw_empty(set, d), ((uint32_t)(j / kStages) & 1u) ^ 1u, a.status, a.wait_ns));
                 if (!ok) break;
