@@ -373,9 +373,9 @@ int kvq_mla_decode_noalloc(const kvq_mla_problem* p, float* out, float* lse,
  * q4_0 paged decode attention, grouped-query, head_dim 256 — Strata PR #2533, the qsa
  * decode commit: the query rows pass through the orthonormal 256-point FWHT (the
  * rotation the K and V rows received when kvq_append_q4 stored them), attention reads
- * the q4_0 pools with every block dequantised as (nibble - 8) * f32(d), and the merged
- * output row is rotated back (the orthonormal FWHT is its own inverse) BEFORE the
- * optional sigmoid(gate) multiply.  For sequence s and query head h, with KV head
+ * the q4_0 pools, each 4-bit code of a block standing for its value less 8 times the
+ * block's binary16 scale, and the merged output row is rotated back (the orthonormal
+ * FWHT is its own inverse) before the optional multiply by sigmoid(gate).  For sequence s and query head h, with KV head
  * g = h / (n_qh / n_kv) and the tokens at positions 0 .. seq_len[s] - 1:
  *   q_rot = FWHT256(q[s][h]) / 16,  score_t = sm_scale * q_rot . k_t,
  *   out[s][h] = FWHT256(sum_t softmax(score)_t v_t) / 16  [* sigmoid(gate[s][h])],
