@@ -49,6 +49,7 @@ struct DecodeArgs {
     float* out;
     float* lse;
     uint32_t* status;
+    int premix;        // rotated rows' partials carry the unrotation's stages h = 128, 256
 };
 
 __device__ __forceinline__ int seq_format(const kvq_mla_problem& p, int s)
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) mla_decode_simt_kernel(DecodeArgs a)
 // quarter 0 does the whole row.  A split of a tensor-core kernel that gave up on a wait
 // marks its partial m = +inf; a row with such a split is written as NaN (lse too).
 // ------------------------------------------------------------------------------------
-__device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, int quarter, int ns)
+__device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, int quarter, int ns, bool rot)
 {
     constexpr int kGroups = 16, kPer = 12, kBatch = kGroups * kPer;
     __shared__ float s_w[kBatch];
@@ -407,6 +408,36 @@ __device__ __forceinline__ void combine_quarter(const DecodeArgs& a, int64_t r, 
     }
     res = empty ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
                 : make_float4(res.x / Lt, res.y / Lt, res.z / Lt, res.w / Lt);
+    if (rot) {
+        // the rest of the unrotation, (1/sqrt 512) s (.) FWHT_512(out): the decode kernel
+        // applied the stages h = 128 and 256 (across the quarters) to each split's
+        // partial; stages h = 1, 2 within the float4, h = 4 .. 64 across the lanes
+        float e[4] = {res.x, res.y, res.z, res.w};
+#pragma unroll
+        for (int h = 1; h < 4; h <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if ((c & h) == 0) {
+                    const float x = e[c], y = e[c + h];
+                    e[c] = x + y;
+                    e[c + h] = x - y;
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float o = __shfl_xor_sync(kFull, e[c], h);
+                e[c] = (j & h) ? o - e[c] : e[c] + o;
+            }
+        }
+        const int d0 = quarter * 128 + 4 * j;
+        const uint32_t sw = a.p.tq4_signs[d0 >> 5] >> (d0 & 31);
+        const float c = tq4_inv_sqrt(kDLat);
+        res = make_float4(e[0] * c * ((sw & 1u) ? -1.0f : 1.0f), e[1] * c * ((sw & 2u) ? -1.0f : 1.0f),
+                          e[2] * c * ((sw & 4u) ? -1.0f : 1.0f), e[3] * c * ((sw & 8u) ? -1.0f : 1.0f));
+    }
     if (aborted) res = make_float4(NAN, NAN, NAN, NAN);
     reinterpret_cast<float4*>(a.out + r * kDLat + quarter * 128)[j] = res;
     if (quarter == 0 && tid == 0 && a.lse) a.lse[r] = aborted ? NAN : empty ? -INFINITY : (M + log2f(Lt)) * kLn2;
@@ -427,8 +458,8 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     const int fmt = seq_format(p, s);
     const int64_t n_cand = p.idx ? (int64_t)p.top_k : (int64_t)L;
     const int ns = (int)min((int64_t)a.n_splits, (n_cand + a.split_rows - 1) / a.split_rows);
-    if (gridDim.y == 4 && !rotated_format(fmt)) {
-        combine_quarter(a, r, blockIdx.y, ns);
+    if (gridDim.y == 4 && (!rotated_format(fmt) || a.premix)) {
+        combine_quarter(a, r, blockIdx.y, ns, rotated_format(fmt));
         return;
     }
     if (blockIdx.y != 0) return;                  // a rotated row: quarter 0 does it all
@@ -528,9 +559,10 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// four quarters a row for many splits, or for rotated rows whose partials were premixed
 dim3 combine_grid(int64_t rows, const DecodePlan& plan)
 {
-    return dim3((unsigned)rows, plan.n_splits > 80 ? 4 : 1);
+    return dim3((unsigned)rows, (plan.n_splits > 80 || plan.premix) ? 4 : 1);
 }
 
 }  // namespace
@@ -639,6 +671,14 @@ bool plan_decode(const kvq_mla_problem& p, DecodePlan& plan)
         }
     }
     plan.split_rows = (int)split_rows;
+    // Few rows (say 16 heads of one query): the combine of a rotated row, which needs all
+    // 512 dims for the unrotation, would run on as many CTAs as there are rows.  Then tc /
+    // tc16 apply the unrotation's stages that mix the 128-dim quarters to each partial and
+    // the combine takes four quarters a row (TQ4, T = 131072, 16 heads: 46.6 -> 44.4 us).
+    // With more rows the one-CTA-a-row combine is already spread over the SMs, and the
+    // extra epilogue work costs more than it saves (64 heads: 43.8 against 45.1 us).
+    plan.premix = (plan.tc || plan.tc16) && (p.seq_fmt != nullptr || rotated_format(p.fmt)) &&
+                  (int64_t)p.n_seq * p.n_q * p.n_heads <= 32;
     plan.n_splits = (int)std::max<int64_t>(1, (n_cand + split_rows - 1) / split_rows);
     const size_t rows = (size_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
@@ -671,6 +711,7 @@ cudaError_t launch_mla_decode(const kvq_mla_problem& p, const DecodePlan& plan, 
     a.out = out;
     a.lse = lse;
     a.status = dev_status;
+    a.premix = plan.premix ? 1 : 0;
     const int64_t rows = (int64_t)p.n_seq * p.n_q * p.n_heads;
     const bool any_tq4 = p.seq_fmt != nullptr || rotated_format(p.fmt);
     if (any_tq4 && !plan.tc && !plan.mma && !plan.tcf8 && !plan.tc16) {   // read by the CUDA-core kernel only

@@ -105,6 +105,7 @@ struct Tc16Args {
     float* part_o;
     uint32_t* status;
     uint64_t wait_ns;                    // limit of the pipeline waits
+    int premix;                          // rotated rows: partials carry stages h = 128, 256
     uint16_t cb_tab[64];                 // binary16 centroids of a 3- or 6-bit problem
 };
 
@@ -611,8 +612,45 @@ __global__ void __maxnreg__(96) mla_decode_tc16_kernel(const __grid_constant__ T
                 a.part_ml[sl * 2] = m_s[t];
                 a.part_ml[sl * 2 + 1] = lt;
             }
+            // Premixed rotated rows: eight heads at a time, all four M-tiles (dims 128 m +
+            // 32 wq + lane) of each, with the unrotation's stages h = 128 and 256, which mix
+            // the M-tiles; the combine does the rest.  Otherwise M-tile by M-tile.
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
+            for (int hb = 0; hb < kGQ && a.premix && rot; hb += 8) {
+                uint32_t x[4][8], y[4][8];           // every load issued, then one wait
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    tmem_ld_x8(tmem + lane_base + kColO + 32 * m + hb, x[m]);
+                    tmem_ld_x8(tmem + lane_base + kColO + 32 * m + 16 + hb, y[m]);
+                }
+                tmem_ld_wait();
+                float v[4][8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) v[m][g] = __uint_as_float(x[m][g]) + __uint_as_float(y[m][g]);
+                {
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const float a0 = v[0][g] + v[1][g], a1 = v[0][g] - v[1][g];    // h = 128
+                        const float a2 = v[2][g] + v[3][g], a3 = v[2][g] - v[3][g];
+                        v[0][g] = a0 + a2;                                             // h = 256
+                        v[2][g] = a0 - a2;
+                        v[1][g] = a1 + a3;
+                        v[3][g] = a1 - a3;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int d = 128 * m + 32 * wq + lane;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        if (hb + g < nh)
+                            a.part_o[((qrow + h0 + hb + g) * a.n_splits + split) * kDLat + d] = v[m][g];
+                }
+            }
+#pragma unroll 1
+            for (int m = 0; m < 4 && !(a.premix && rot); ++m) {
                 const int d = 128 * m + 32 * wq + lane;
                 uint32_t x[16], y[16];
                 tmem_ld_x16(tmem + lane_base + kColO + 32 * m, x);
@@ -830,6 +868,7 @@ cudaError_t launch_mla_decode_tc16(const kvq_mla_problem& p, const DecodePlan& p
     a.part_o = part_o;
     a.status = dev_status;
     a.wait_ns = wait_limit_ns();
+    a.premix = plan.premix ? 1 : 0;
     for (int k = 0; k < 64; ++k)
         a.cb_tab[k] = p.fmt == KVQ_FMT_TQ6 ? kTq6CentroidBits[k] : p.fmt == KVQ_FMT_TQ3 ? kTq3CentroidBits[k & 7] : 0;
     const int64_t items = (int64_t)p.n_seq * p.n_q * a.n_hg * kGQ;

@@ -199,6 +199,8 @@ struct DecodePlan {
     bool tc16 = false;      // tensor-core (tcgen05) kernel, 16 heads a CTA, codes converted once
     bool tc = false;        // tensor-core (tcgen05) kernel, 32 heads a CTA
     bool mma = false;       // warp-level MMA kernel (blocks of 16 heads)
+    bool premix = false;    // tc / tc16 put the unrotation's stages h = 128, 256 into the
+                            // rotated rows' partials; the combine takes four quarters a row
     bool by_fmt = false;    // a batch of fp8 and TQ4 sequences: the fp8 ones on the e4m3
                             // kernel, the TQ4 ones on the 32-head kernel (tc is set too)
     int split_rows = 0;     // candidate rows per split
