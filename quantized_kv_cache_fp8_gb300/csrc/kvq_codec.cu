@@ -620,6 +620,16 @@ __device__ __forceinline__ bool q4_prefer(float a, float b)
     return !signbit(a) && signbit(b);
 }
 
+// q4_prefer as an integer order: key(a) > key(b) exactly when a is preferred over b, for
+// every a, b that are not NaN: |a| in the upper 31 bits, "not negative" in bit 0 (a
+// larger |.| first; among equal |.| the positive one, or +0 over -0).  A NaN's key lies
+// above that of +inf (0xFF000001).
+__device__ __forceinline__ uint32_t q4_key(float a)
+{
+    const uint32_t u = __float_as_uint(a);
+    return ((u & 0x7FFFFFFFu) << 1) | (~u >> 31);
+}
+
 // cell of (sequence s, position pos), or -1 (and the status bit) when outside
 __device__ __forceinline__ int64_t q4_cell(const int32_t* __restrict__ page_table, int max_pages,
                                            int page_size, int64_t n_cells, int s, int pos)
@@ -711,15 +721,26 @@ append_q4_kernel(const float* __restrict__ k, const float* __restrict__ v, int n
             fwht256_lane8(z, lane);
 #pragma unroll
             for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
-            // the block's preferred element (a total order: every lane of the block agrees)
-            float mval = z[0];
+            // the block's preferred element: the largest key over the block's 4 lanes (every
+            // lane of the block gets the same); a block holding a NaN takes the scan of
+            // q4_prefer instead, which decides NaN by position like the reference order
+            uint32_t key = q4_key(z[0]);
 #pragma unroll
-            for (int j = 1; j < 8; ++j)
-                if (q4_prefer(z[j], mval)) mval = z[j];
+            for (int j = 1; j < 8; ++j) key = max(key, q4_key(z[j]));
 #pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) {
-                const float other = __shfl_xor_sync(kFull, mval, o);
-                if (q4_prefer(other, mval)) mval = other;
+            for (int o = 1; o <= 2; o <<= 1) key = max(key, __shfl_xor_sync(kFull, key, o));
+            float mval = __uint_as_float(key >> 1);
+            if (!(key & 1u)) mval = -mval;
+            if (__any_sync(kFull, key > 0xFF000001u)) {
+                mval = z[0];
+#pragma unroll
+                for (int j = 1; j < 8; ++j)
+                    if (q4_prefer(z[j], mval)) mval = z[j];
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float other = __shfl_xor_sync(kFull, mval, o);
+                    if (q4_prefer(other, mval)) mval = other;
+                }
             }
             const float d = __fmul_rn(mval, -0.125f);          // mval / -8, exact
             const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
