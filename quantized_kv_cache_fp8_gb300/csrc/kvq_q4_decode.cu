@@ -7,7 +7,9 @@
 // One warp per (split, sequence, KV head) [and half of the 8 query heads when a KV head
 // serves 8]; four such warps per CTA, each with its own 3-stage cp.async ring of 16-row
 // tiles (the K and V rows of 16 positions, 4.5 KB); three CTAs per SM.  A warp computes
-// tile i + 1's scores and tile i's context in one straight-line body.
+// tile i + 1's scores and tile i's context in one straight-line body.  Each landed row is
+// rewritten in place as its 8 blocks' code bytes (16-byte aligned) and then its 8 scales,
+// so the operands come from ldmatrix and 16-byte loads instead of 2-byte ones.
 // Both contractions of a tile run on the tensor cores with register operands
 // (mma.sync m16n8k16, fp16 in, fp32 out; the operands are built in registers, so
 // there is no shared-memory or tensor-memory operand image to stage):
@@ -84,8 +86,6 @@ __device__ __forceinline__ float exp2i(int k)             // 2^k, k in [-126, 12
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
-__device__ __forceinline__ uint16_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
-
 // {lo, hi} -> f16x2 (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
@@ -145,13 +145,59 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Code bytes 4t .. 4t + 3 of a block (they start 2 bytes into the block, so the word is
-// 4-byte aligned in odd blocks only).
-template <bool kOdd>
-__device__ __forceinline__ uint32_t code_word(const uint8_t* p)
+// Four 8 x 8 matrices of 16-bit elements (a code byte pair each) from shared memory; lanes
+// 8m .. 8m + 7 give the 16-byte rows of matrix m.  Lane (g, t) receives elements 2t, 2t + 1
+// of row g (plain) or elements g of rows 2t, 2t + 1 (transposed): the A fragments of
+// m16n8k16 for rows on M (score) and for V^T (context).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
-    if constexpr (kOdd) return *reinterpret_cast<const uint32_t*>(p);
-    else return __byte_perm(lds16(p), lds16(p + 2), 0x5410);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+// A staged row of 8 blocks [scale (2 B) | 16 code bytes] rewritten in place as the 8
+// blocks' code bytes (block b at 16 b, 16-byte aligned for ldmatrix) followed by the 8
+// binary16 scales (block b at 128 + 2 b).  Block 2e starts at word 9e, so its scale is
+// the low half of that word and its codes straddle words; block 2e + 1's scale is the
+// high half of word 9e + 4 and its codes are words 9e + 5 .. 9e + 8.  Returns the row's
+// largest |scale| as binary16 bits.
+__device__ __forceinline__ uint32_t repack_row(uint8_t* row)
+{
+    uint4* r4 = reinterpret_cast<uint4*>(row);
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = r4[i];
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    uint32_t c[32], s[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            c[8 * e + k] = __byte_perm(w[9 * e + k], w[9 * e + k + 1], 0x5432);
+            c[8 * e + 4 + k] = w[9 * e + 5 + k];
+        }
+        s[e] = __byte_perm(w[9 * e], w[9 * e + 4], 0x7610);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r4[i] = make_uint4(c[4 * i], c[4 * i + 1], c[4 * i + 2], c[4 * i + 3]);
+    r4[8] = make_uint4(s[0], s[1], s[2], s[3]);
+    const uint32_t m2 = __vmaxu2(__vmaxu2(s[0] & 0x7FFF7FFFu, s[1] & 0x7FFF7FFFu),
+                                 __vmaxu2(s[2] & 0x7FFF7FFFu, s[3] & 0x7FFF7FFFu));
+    return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// binary16 scale of block b from a row's four scale words
+__device__ __forceinline__ float scale_of(const uint4& s, int b)
+{
+    const uint32_t w = (b >> 1) == 0 ? s.x : (b >> 1) == 1 ? s.y : (b >> 1) == 2 ? s.z : s.w;
+    return h2f((uint16_t)((b & 1) ? (w >> 16) : (w & 0xFFFFu)));
 }
 
 constexpr int kTileRows = 16;
@@ -289,35 +335,37 @@ __global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_
     int tau = 40;                                    // P carries 2^tau
     const bool head_ok = t < GH;
 
-    // scores of rows g and g + 8 of a staged tile for head t (unscaled)
-    auto scores = [&](const uint8_t* sK, float& sg, float& sg8) {
+    // scores of rows g and g + 8 of a repacked tile for head t (unscaled); aK is the
+    // tile's shared-memory address
+    auto scores = [&](uint32_t aK, const uint8_t* sK, float& sg, float& sg8) {
         sg = 0.0f;
         sg8 = 0.0f;
+        const uint4 dg = *reinterpret_cast<const uint4*>(sK + g * kRowBytes + 128);
+        const uint4 dg8 = *reinterpret_cast<const uint4*>(sK + (g + 8) * kRowBytes + 128);
+        // lanes 0..15 give rows 0..15 of block 2bp, lanes 16..31 those of block 2bp + 1
+        const uint32_t arow = aK + (lane & 15) * kRowBytes + 16 * (lane >> 4);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const uint8_t* rg = sK + g * kRowBytes + 18 * b;
-            const uint8_t* rg8 = rg + 8 * kRowBytes;
-            uint32_t xg, xg8;
-            if (b & 1) {
-                xg = code_word<true>(rg + 2 + 4 * t);
-                xg8 = code_word<true>(rg8 + 2 + 4 * t);
-            } else {
-                xg = code_word<false>(rg + 2 + 4 * t);
-                xg8 = code_word<false>(rg8 + 2 + 4 * t);
+        for (int bp = 0; bp < 4; ++bp) {
+            uint32_t x[4];                           // code bytes 4t..4t+3 of rows g, g + 8
+            ldsm_x4(arow + 32 * bp, x);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int b = 2 * bp + h;
+                const uint32_t xg = x[2 * h], xg8 = x[2 * h + 1];
+                const uint4 bq = frag[b * 32 + lane];
+                float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma16816(c, nib_lo(xg), nib_lo(xg8), nib_lo(xg >> 8), nib_lo(xg8 >> 8), bq.x, bq.y);
+                mma16816(c, nib_hi(xg), nib_hi(xg8), nib_hi(xg >> 8), nib_hi(xg8 >> 8), bq.z, bq.w);
+                sg = fmaf(scale_of(dg, b), c[0] + c[1], sg);
+                sg8 = fmaf(scale_of(dg8, b), c[2] + c[3], sg8);
             }
-            const uint4 bq = frag[b * 32 + lane];
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma16816(c, nib_lo(xg), nib_lo(xg8), nib_lo(xg >> 8), nib_lo(xg8 >> 8), bq.x, bq.y);
-            mma16816(c, nib_hi(xg), nib_hi(xg8), nib_hi(xg >> 8), nib_hi(xg8 >> 8), bq.z, bq.w);
-            sg = fmaf(h2f(lds16(rg)), c[0] + c[1], sg);
-            sg8 = fmaf(h2f(lds16(rg8)), c[2] + c[3], sg8);
         }
     };
     // online softmax of head t over a tile's 16 rows (lanes of equal t); returns the
     // factor the running output takes before this tile's context, and this tile's
     // weights of head g >> 1 for rows 2t, 2t+1, 2t+8, 2t+9 times 2^tau
     float f = 1.0f, pa = 0.0f, pb = 0.0f, pc = 0.0f, pd = 0.0f;
-    auto softmax = [&](float sg, float sg8, unsigned valid, const uint8_t* sV) {
+    auto softmax = [&](float sg, float sg8, unsigned valid, uint32_t dm) {
         const bool vg = head_ok && ((valid >> g) & 1u), vg8 = head_ok && ((valid >> (g + 8)) & 1u);
         const float s0 = vg ? sg * sinv : -INFINITY;
         const float s1 = vg8 ? sg8 * sinv : -INFINITY;
@@ -335,10 +383,8 @@ __global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_
         ps += __shfl_xor_sync(kFull, ps, 16);
         l_run = l_run * alpha + ps;
         m_run = m_new;
-        // the tile's largest V block scale bounds P = p * d (p <= 1): P * 2^tau < 2^15
-        const uint8_t* rv = sV + (lane & 15) * kRowBytes + 72 * (lane >> 4);
-        uint32_t dm = max(max(lds16(rv) & 0x7FFFu, lds16(rv + 18) & 0x7FFFu),
-                          max(lds16(rv + 36) & 0x7FFFu, lds16(rv + 54) & 0x7FFFu));
+        // the tile's largest V block scale bounds P = p * d (p <= 1): P * 2^tau < 2^15;
+        // dm is a V row's largest |scale| (lanes 16..31) or 0 (lanes 0..15)
 #pragma unroll
         for (int w = 16; w >= 1; w >>= 1) dm = max(dm, __shfl_xor_sync(kFull, dm, w));
         int tau_new = tau;
@@ -354,8 +400,8 @@ __global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_
         pc = __shfl_sync(kFull, p1, src) * pscale;
         pd = __shfl_sync(kFull, p1, src + 4) * pscale;
     };
-    // context of a staged tile with the current weights
-    auto context = [&](const uint8_t* sV) {
+    // context of a repacked tile's V rows (shared-memory address aV) with the current weights
+    auto context = [&](uint32_t aV, const uint8_t* sV) {
         if (__any_sync(kFull, f != 1.0f)) {
 #pragma unroll
             for (int b = 0; b < 8; ++b)
@@ -365,32 +411,43 @@ __global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_
                     o[b][1][k] *= f;
                 }
         }
+        const uint8_t* v0 = sV + 2 * t * kRowBytes + 128;     // scales of rows 2t, 2t+1, 2t+8, 2t+9
+        const uint4 d0 = *reinterpret_cast<const uint4*>(v0);
+        const uint4 d1 = *reinterpret_cast<const uint4*>(v0 + kRowBytes);
+        const uint4 d2 = *reinterpret_cast<const uint4*>(v0 + 8 * kRowBytes);
+        const uint4 d3 = *reinterpret_cast<const uint4*>(v0 + 9 * kRowBytes);
+        const uint32_t arow = aV + (lane & 15) * kRowBytes + 16 * (lane >> 4);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const uint8_t* v0 = sV + 2 * t * kRowBytes + 18 * b;
-            const uint8_t* v1 = v0 + kRowBytes;
-            const uint8_t* v2 = v0 + 8 * kRowBytes;
-            const uint8_t* v3 = v2 + kRowBytes;
-            const uint32_t b0 = split_pair(pa * h2f(lds16(v0)), pb * h2f(lds16(v1)), part);
-            const uint32_t b1 = split_pair(pc * h2f(lds16(v2)), pd * h2f(lds16(v3)), part);
-            // A = V^T: m = g is code byte 2g, m = g + 8 byte 2g + 1; k = rows
-            const uint32_t X = __byte_perm(lds16(v0 + 2 + 2 * g), lds16(v1 + 2 + 2 * g), 0x5410);
-            const uint32_t Y = __byte_perm(lds16(v2 + 2 + 2 * g), lds16(v3 + 2 + 2 * g), 0x5410);
-            mma16816(o[b][0], nib_lo(X), nib_lo(X >> 8), nib_lo(Y), nib_lo(Y >> 8), b0, b1);
-            mma16816(o[b][1], nib_hi(X), nib_hi(X >> 8), nib_hi(Y), nib_hi(Y >> 8), b0, b1);
+        for (int bp = 0; bp < 4; ++bp) {
+            // A = V^T: m = g is code byte 2g, m = g + 8 byte 2g + 1; k = rows.  X holds the
+            // byte pair g of rows 2t, 2t+1, Y that of rows 2t+8, 2t+9.
+            uint32_t x[4];
+            ldsm_x4_trans(arow + 32 * bp, x);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int b = 2 * bp + h;
+                const uint32_t X = x[2 * h], Y = x[2 * h + 1];
+                const uint32_t b0 = split_pair(pa * scale_of(d0, b), pb * scale_of(d1, b), part);
+                const uint32_t b1 = split_pair(pc * scale_of(d2, b), pd * scale_of(d3, b), part);
+                mma16816(o[b][0], nib_lo(X), nib_lo(X >> 8), nib_lo(Y), nib_lo(Y >> 8), b0, b1);
+                mma16816(o[b][1], nib_hi(X), nib_hi(X >> 8), nib_hi(Y), nib_hi(Y >> 8), b0, b1);
+            }
         }
     };
 
     // Software pipeline: iteration i computes the scores of tile i + 1 and the context of
     // tile i in one straight-line body (two independent chains for the scheduler), then
-    // the softmax of tile i + 1.  The last iteration's scores read a stale stage and are
-    // discarded.
+    // the softmax of tile i + 1.  Each lane repacks the row it copied once its copies
+    // have landed; the warp then reads the tile through ldmatrix.  The last iteration's
+    // scores read a stale stage and are discarded.
+    const uint32_t tiles_sa = (uint32_t)__cvta_generic_to_shared(tiles[0]);
     cp_async_wait<kStages - 2>();                    // tile 0 has landed
-    __syncwarp();
     {
+        const uint32_t dm0 = repack_row(tiles[0] + lane * kRowBytes);
+        __syncwarp();
         float sg, sg8;
-        scores(tiles[0], sg, sg8);
-        softmax(sg, sg8, valid_of[0], tiles[0] + kTileRows * kRowBytes);
+        scores(tiles_sa, tiles[0], sg, sg8);
+        softmax(sg, sg8, valid_of[0], lane >= 16 ? dm0 : 0u);
     }
     for (int i = 0; i < n_tiles; ++i) {
         const int ti = i + kStages - 1;
@@ -400,13 +457,15 @@ __global__ void __launch_bounds__(32 * kWarps, 3) q4_decode_kernel(const __grid_
         }
         cp_async_commit();
         cp_async_wait<kStages - 2>();                // tile i + 1 has landed
+        const int sn = (i + 1) % kStages, sc = i % kStages;
+        uint32_t dmn = 0;
+        if (i + 1 < n_tiles) dmn = repack_row(tiles[sn] + lane * kRowBytes);
         __syncwarp();
-        const int sn = (i + 1) % kStages;
         float sg, sg8;
-        scores(tiles[sn], sg, sg8);
-        context(tiles[i % kStages] + kTileRows * kRowBytes);
+        scores(tiles_sa + sn * kStageBytes, tiles[sn], sg, sg8);
+        context(tiles_sa + sc * kStageBytes + kTileRows * kRowBytes, tiles[sc] + kTileRows * kRowBytes);
         __syncwarp();                                // tile i's stage is refilled next iteration
-        if (i + 1 < n_tiles) softmax(sg, sg8, valid_of[sn], tiles[sn] + kTileRows * kRowBytes);
+        if (i + 1 < n_tiles) softmax(sg, sg8, valid_of[sn], lane >= 16 ? dmn : 0u);
     }
     // ---- partials: (m, l) of head t from lane t, o of head t: dims 32b + 16mt + 2g (+1)
     if (t < GH) {
