@@ -465,14 +465,16 @@ def run_codecs(args, local):
             ts.append(e0.elapsed_time(e1) / 1e3)
         return statistics.median(ts)
 
-    def report(kernel, workload, alg_bytes, seconds, units, unit_name):
+    def report(kernel, workload, alg_bytes, seconds, units, unit_name, extra=None):
         gbs = alg_bytes / seconds / 1e9
-        print(json.dumps({"suite": "codecs", "kernel": kernel, "workload": workload,
-                          "us": round(seconds * 1e6, 2), f"{unit_name}_per_s": units / seconds,
-                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                                       "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
-                                       "bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
-                          "l2": "flushed before each timed launch", "steps": K}), flush=True)
+        line = {"suite": "codecs", "kernel": kernel, "workload": workload,
+                "us": round(seconds * 1e6, 2), f"{unit_name}_per_s": units / seconds,
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                             "bytes_per_launch": alg_bytes, "peak_kind": peak_kind},
+                "l2": "flushed before each timed launch", "steps": K}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
 
     # a1: fp8 encode of the latent and rope planes, T = 131072 rows (the long-context cache)
     T = 131072
@@ -537,6 +539,29 @@ def run_codecs(args, local):
     report("kvq_gather (q4_0)", f"one pool: {n_seq} seqs x {n_tok} tokens x {n_heads} heads -> fp16",
            toks * n_heads * (144 + 256 * 2) + table.size * 4, s, toks, "tokens")
     del out
+
+    # the producer with its K/V projection fused (one new token per sequence, as in a
+    # decode step): hidden rows of 4096, bfloat16 weights [4096][8 heads x 256] for K and V
+    d_model = 4096
+    hp = torch.randn(n_seq, 1, d_model, generator=gen, device=dev)
+    wk = (torch.randn(d_model, n_heads * 256, generator=gen, device=dev) / 64).to(torch.bfloat16)
+    wv = (torch.randn(d_model, n_heads * 256, generator=gen, device=dev) / 64).to(torch.bfloat16)
+    pos0p = torch.full((n_seq,), n_tok - 1, dtype=torch.int32, device=dev)
+    for n_new in (n_seq, 1):                         # a 16-sequence step, then one token
+        s = timed(lambda: kvq.kvq_project_append_q4(hp[:n_new], wk, wv, pos0p[:n_new], table_d, ps,
+                                                    n_cells, k_pool, v_pool))
+        # the fixed-order fp32 sum runs on the CUDA cores: n_new * d_model * 2 * n_heads * 256
+        # fmas against 152 SMs x 128 fp32 lanes x 2.07 GHz (the fp32 fma peak)
+        fmas = n_new * d_model * 2 * n_heads * 256
+        alu_peak = 152 * 128 * 2.07e9
+        report("kvq_project_append_q4", f"{n_new} seqs x 1 token, d_model {d_model}, K,V x {n_heads} "
+               f"heads x 256, bf16 weights",
+               2 * d_model * n_heads * 256 * 2 + n_new * d_model * 4 + 2 * n_new * n_heads * 144, s,
+               n_new, "tokens",
+               {"alu": {"fmas_per_launch": fmas, "achieved_tfma_s": round(fmas / s / 1e12, 2),
+                        "peak_tfma_s": round(alu_peak / 1e12, 2), "frac": round(fmas / s / alu_peak, 4),
+                        "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2.07 GHz"}})
+    del hp, wk, wv
 
     # q4_0 decode attention over the same pools' layout: 16 sequences x 8192 positions
     # (appended from position 0), 8 KV heads, 16 query heads (two per KV head), gated

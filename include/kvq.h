@@ -71,6 +71,13 @@ typedef enum kvq_format {
     KVQ_FMT_TQ3 = 5          /* rotated tier, 3-bit codes (8 levels) + fp32 radius      */
 } kvq_format;
 
+/* element type of a projection weight matrix */
+typedef enum kvq_weight_type {
+    KVQ_WEIGHT_F32 = 0,      /* fp32                                                   */
+    KVQ_WEIGHT_BF16 = 1      /* bfloat16 (the upper half of an fp32 pattern; widened
+                                exactly)                                               */
+} kvq_weight_type;
+
 /* Library version (major*10000 + minor*100 + patch). */
 int kvq_version(void);
 
@@ -218,6 +225,35 @@ int kvq_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0
                   int max_pages, int page_size, int64_t n_cells,
                   uint8_t* k_pool, uint8_t* v_pool, uint32_t* dev_status,
                   kvq_stream_t stream);
+
+/*
+ * q4_0 append with the K/V projection fused into its producer — Strata PR #2533, the qsa
+ * decode commit (fwht_row256 applied inside qsa_prep, the kernel that produces the rows,
+ * so no unrotated fp32 row makes a round trip through memory) with the q4_0 layout of
+ * the kv_q4.metal port commit.  Token t of sequence s has the hidden row
+ * h[s][t][0 .. d_model - 1]; its K row of head g is
+ *     k[c] = sum_k h[k] * w_k[k][256 g + c],   c < 256   (V alike with w_v),
+ * summed in this fixed fp32 order: the k range is cut into 64 chunks of
+ * L = 4 * ceil(d_model / 256) consecutive terms (the last chunks short or empty); each
+ * chunk is the chain acc = fmaf(h[k], w[k][col], acc) from acc = 0 in ascending k; the
+ * 64 chunk sums are added pairwise ((0 + 1), (2 + 3), ..., then the 32, 16, 8, 4 and 2
+ * results the same way).
+ * The rows are then rotated, quantized and stored exactly as kvq_append_q4 stores its k
+ * and v rows (same pool layout, page rule and status), in the same launch: the bytes
+ * equal kvq_append_q4 applied to those fp32 rows.
+ *   h          device fp32 [n_seq][n_tok][d_model], 16-byte aligned; d_model % 4 == 0
+ *   w_k, w_v   device [d_model][n_heads * 256], row-major, of `w_type`, 16-byte aligned
+ *   pos0, page_table, pools, dev_status: as kvq_append_q4 (head_dim 256)
+ * The projection reads every weight once per group of 16 tokens: it is built for the
+ * few new tokens of a decode step, not for a prefill.  Errors: KVQ_EINVAL for bad sizes
+ * (d_model < 4 or not a multiple of 4, more than 1048560 tokens), a NULL pointer or another
+ * w_type; KVQ_EALIGN as above.  n_seq * n_tok == 0 is a no-op.
+ */
+int kvq_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok,
+                          int d_model, const void* w_k, const void* w_v, int w_type,
+                          int n_heads, int head_dim, const int32_t* page_table,
+                          int max_pages, int page_size, int64_t n_cells, uint8_t* k_pool,
+                          uint8_t* v_pool, uint32_t* dev_status, kvq_stream_t stream);
 
 /* Planes of one MLA cache tier (device pointers, pool-row indexed). */
 typedef struct kvq_mla_cache {

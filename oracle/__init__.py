@@ -113,6 +113,10 @@ def _declare(L: C.CDLL) -> None:
     L.orc_gather_q4.argtypes = [_p, C.c_int, _p, C.c_int, C.c_int, C.c_int, _p, C.c_int,
                                 C.c_int, _i64, _p]
     L.orc_mla_decode.restype = C.c_int
+    L.orc_project_rows.argtypes = [_p, _i64, C.c_int, _p, C.c_int, _i64, _p]
+    L.orc_project_rows.restype = None
+    L.orc_project_append_q4.argtypes = [_p, C.c_int, _p, C.c_int, C.c_int, _p, _p, C.c_int,
+                                        C.c_int, _p, C.c_int, C.c_int, _i64, _p, _p]
     L.orc_mla_decode.argtypes = [C.POINTER(OrcMla), _p, _p, _p]
     L.orc_q4_decode.argtypes = [C.c_int, C.c_int, C.c_int, _p, _p, C.c_int, C.c_int, _i64, _p, _p,
                                 _p, _p, C.c_double, _p, C.c_int, _p, _p, _p]
@@ -293,6 +297,39 @@ def append_q4(k, v, pos0, page_table, page_size, n_cells, k_pool, v_pool):
                              pt.shape[1], page_size, n_cells, _ptr(k_pool), _ptr(v_pool))
     if rc != 0:
         raise ValueError(f"oracle q4 append refused (rc={rc})")
+
+
+def project_rows(h: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """h [rows][d_model] fp32; w [d_model][n_out] fp32, or uint16 bfloat16 patterns ->
+    y [rows][n_out] fp32 in the library's fixed summation order."""
+    h = _c(h, np.float32)
+    bf16 = w.dtype == np.uint16
+    w = _c(w, np.uint16 if bf16 else np.float32)
+    rows, d_model = h.shape
+    n_out = w.shape[1]
+    assert w.shape[0] == d_model
+    y = np.empty((rows, n_out), np.float32)
+    lib().orc_project_rows(_ptr(h), rows, d_model, _ptr(w), int(bf16), n_out, _ptr(y))
+    return y
+
+
+def project_append_q4(h, w_k, w_v, pos0, page_table, page_size, n_cells, k_pool, v_pool):
+    """h [n_seq][n_tok][d_model] fp32; w_k, w_v [d_model][n_heads * 256] fp32 or uint16
+    bfloat16 patterns; pools [n_cells][n_heads][144] u8 (in place)."""
+    h = _c(h, np.float32)
+    bf16 = w_k.dtype == np.uint16
+    w_k = _c(w_k, np.uint16 if bf16 else np.float32)
+    w_v = _c(w_v, np.uint16 if bf16 else np.float32)
+    pos0 = _c(pos0, np.int32)
+    pt = _c(page_table, np.int32)
+    n_seq, n_tok, d_model = h.shape
+    n_heads = w_k.shape[1] // 256
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    rc = lib().orc_project_append_q4(_ptr(h), n_seq, _ptr(pos0), n_tok, d_model, _ptr(w_k),
+                                     _ptr(w_v), int(bf16), n_heads, _ptr(pt), pt.shape[1],
+                                     page_size, n_cells, _ptr(k_pool), _ptr(v_pool))
+    if rc != 0:
+        raise ValueError(f"oracle projected q4 append refused (rc={rc})")
 
 
 def gather_q4(pool, pos0, n_tok, page_table, page_size, n_cells, n_heads) -> np.ndarray:

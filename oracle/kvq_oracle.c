@@ -18,6 +18,11 @@
  *                                    radius invariance, rotated-domain identities
  *   orc_q4_block / append / gather  all-zero group bits, tie blocks, dequant bound,
  *                                    brute-force page placement
+ *   orc_project_rows / _append_q4   exact integer products (numpy int64 matmul), the
+ *                                    identity and permutation weights (rows reproduced
+ *                                    bit for bit, so the append equals orc_append_q4 of
+ *                                    h), the fp32 error bound against an fp64 matmul,
+ *                                    bfloat16 widening
  *   orc_mla_decode                  hand-expanded softmax, one-hot and uniform cases,
  *                                    split invariance, a numpy float128-free re-derivation
  */
@@ -531,6 +536,68 @@ int orc_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0
             }
         }
     return 0;
+}
+
+/* ===================================================================================
+ * The q4_0 append with its K/V projection (the producer that computes the rows rotates
+ * and quantizes them: Strata PR #2533, the qsa decode commit, fwht_row256 in qsa_prep).
+ * The pages leave the projection's arithmetic to the model; this library fixes it as
+ * below, and the oracle follows the same steps so that the codes can be compared.
+ * =================================================================================== */
+
+/* element i of a weight matrix: fp32, or bfloat16 widened (its bits are the upper half
+ * of an fp32 pattern) */
+static float weight_at(const void* w, int w_bf16, int64_t i)
+{
+    if (!w_bf16) return ((const float*)w)[i];
+    uint32_t bits = (uint32_t)((const uint16_t*)w)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* y[r][c] = sum_k h[r][k] * w[k][c] (h [rows][d_model], w [d_model][n_out]): the k range
+ * in 64 chunks of L = 4 * ceil(d_model / 256) consecutive terms (the last ones short or
+ * empty); a chunk's sum is the chain acc = fmaf(h, w, acc) from 0 in ascending k; the 64
+ * chunk sums are added in pairs (0+1, 2+3, ...), then the 32 results in pairs, and so on. */
+void orc_project_rows(const float* h, int64_t rows, int d_model, const void* w, int w_bf16,
+                      int64_t n_out, float* y)
+{
+    const int L = 4 * ((d_model + 255) / 256);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < n_out; ++c) {
+            float part[64];
+            for (int j = 0; j < 64; ++j) {
+                float acc = 0.0f;
+                int k_end = (j + 1) * L < d_model ? (j + 1) * L : d_model;
+                for (int k = j * L; k < k_end; ++k)
+                    acc = fmaf(h[r * d_model + k], weight_at(w, w_bf16, (int64_t)k * n_out + c), acc);
+                part[j] = acc;
+            }
+            for (int n = 64; n > 1; n /= 2)
+                for (int i = 0; i < n / 2; ++i) part[i] = part[2 * i] + part[2 * i + 1];
+            y[r * n_out + c] = part[0];
+        }
+}
+
+/* The projected rows of every new token (K with w_k, V with w_v; [n_seq][n_tok][n_heads
+ * * 256]) appended as orc_append_q4 appends them. */
+int orc_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok,
+                          int d_model, const void* w_k, const void* w_v, int w_bf16,
+                          int n_heads, const int32_t* page_table, int max_pages,
+                          int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool)
+{
+    const int64_t rows = (int64_t)n_seq * n_tok, n_out = (int64_t)n_heads * 256;
+    float* k = (float*)malloc((size_t)(rows * n_out > 0 ? rows * n_out : 1) * sizeof(float));
+    float* v = (float*)malloc((size_t)(rows * n_out > 0 ? rows * n_out : 1) * sizeof(float));
+    if (!k || !v) { free(k); free(v); return -3; }
+    orc_project_rows(h, rows, d_model, w_k, w_bf16, n_out, k);
+    orc_project_rows(h, rows, d_model, w_v, w_bf16, n_out, v);
+    int rc = orc_append_q4(k, v, n_seq, pos0, n_tok, n_heads, 256, page_table, max_pages,
+                           page_size, n_cells, k_pool, v_pool);
+    free(k);
+    free(v);
+    return rc;
 }
 
 /* Gather back to binary16 in the rotated domain: out = f16_rne((q - 8) * f32(d)),

@@ -68,6 +68,13 @@ int  orc_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos
 int  orc_gather_q4(const uint8_t* pool, int n_seq, const int32_t* pos0, int n_tok,
                    int n_heads, int head_dim, const int32_t* page_table,
                    int max_pages, int page_size, int64_t n_cells, uint16_t* out);
+/* projection producer of the q4_0 append: y = h . w in the library's fixed fp32 order */
+void orc_project_rows(const float* h, int64_t rows, int d_model, const void* w, int w_bf16,
+                      int64_t n_out, float* y);
+int  orc_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok,
+                           int d_model, const void* w_k, const void* w_v, int w_bf16,
+                           int n_heads, const int32_t* page_table, int max_pages,
+                           int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool);
 
 /* ---- absorbed-MLA decode attention, fp64 ---------------------------------------- */
 typedef struct orc_mla {

@@ -15,7 +15,8 @@ import threading
 
 __all__ = [
     "KvqError", "lib", "kvq_version", "kvq_tq4_codebook", "kvq_set_fault",
-    "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_gather_q4", "kvq_gather_rows",
+    "kvq_encode_fp8", "kvq_encode_tq4", "kvq_append_q4", "kvq_project_append_q4",
+    "kvq_gather_q4", "kvq_gather_rows", "WEIGHT_F32", "WEIGHT_BF16",
     "kvq_mla_decode", "kvq_mla_decode_workspace", "kvq_mla_decode_noalloc", "kvq_mla_decode_kernel",
     "MlaCache",
     "MlaProblem", "Q4Problem", "make_q4_problem", "kvq_q4_decode", "kvq_q4_decode_workspace",
@@ -28,6 +29,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libkvq.so")
 
 FMT_FP8, FMT_TQ4, FMT_Q4_0, FMT_TQ6, FMT_TQ3 = 1, 2, 3, 4, 5
+WEIGHT_F32, WEIGHT_BF16 = 0, 1
 TQ_FMT = {3: FMT_TQ3, 4: FMT_TQ4, 6: FMT_TQ6}     # rotated tier of each code width
 IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_MMA, IMPL_TC16, IMPL_TCF8 = 0, 1, 2, 3, 4, 5
 IMPL_BY_FMT = 6   # kvq_mla_decode_kernel only: fp8 sequences on IMPL_TCF8, TQ4 ones on IMPL_TC
@@ -40,7 +42,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOTPOW2", 3: "KVQ_EFORMAT", 4: 
 EXPORTS = ["kvq_version", "kvq_status_string", "kvq_last_error", "kvq_set_fault",
            "kvq_set_wait_limit_ns",
            "kvq_tq4_codebook", "kvq_tq_codebook", "kvq_encode_fp8", "kvq_encode_tq4",
-           "kvq_encode_tq", "kvq_encode_mla", "kvq_append_q4",
+           "kvq_encode_tq", "kvq_encode_mla", "kvq_append_q4", "kvq_project_append_q4",
            "kvq_gather", "kvq_mla_decode_workspace", "kvq_mla_decode_kernel", "kvq_mla_decode",
            "kvq_mla_decode_noalloc", "kvq_q4_decode_workspace", "kvq_q4_decode",
            "kvq_cache_probe", "kvq_cache_save", "kvq_cache_save_f32", "kvq_cache_append",
@@ -137,6 +139,10 @@ def _declare(L):
     L.kvq_append_q4.restype = C.c_int
     L.kvq_append_q4.argtypes = [_p, _p, C.c_int, _p, C.c_int, C.c_int, C.c_int, _p, C.c_int,
                                 C.c_int, _i64, _p, _p, _p, _p]
+    L.kvq_project_append_q4.restype = C.c_int
+    L.kvq_project_append_q4.argtypes = [_p, C.c_int, _p, C.c_int, C.c_int, _p, _p, C.c_int,
+                                        C.c_int, C.c_int, _p, C.c_int, C.c_int, _i64, _p, _p,
+                                        _p, _p]
     L.kvq_gather.restype = C.c_int
     L.kvq_gather.argtypes = [C.POINTER(GatherDesc), _p]
     L.kvq_mla_decode_workspace.restype = C.c_size_t
@@ -246,6 +252,22 @@ def kvq_append_q4(k, v, pos0, page_table, page_size, n_cells, k_pool, v_pool,
     _check(lib().kvq_append_q4(_ptr(k), _ptr(v), n_seq, _ptr(pos0), n_tok, n_heads, hd,
                                _ptr(page_table), page_table.shape[1], page_size, n_cells,
                                _ptr(k_pool), _ptr(v_pool), _ptr(dev_status), _stream(stream)))
+
+
+def kvq_project_append_q4(h, w_k, w_v, pos0, page_table, page_size, n_cells, k_pool, v_pool,
+                          dev_status=None, stream=None) -> None:
+    """h fp32 [n_seq][n_tok][d_model]; w_k, w_v [d_model][n_heads * 256] float32 or
+    bfloat16 tensors; the projected rows are appended as kvq_append_q4 appends k, v."""
+    n_seq, n_tok, d_model = h.shape
+    w_type = WEIGHT_BF16 if str(w_k.dtype).endswith("bfloat16") else WEIGHT_F32
+    n_heads = w_k.shape[1] // 256
+    if tuple(w_k.shape) != (d_model, n_heads * 256) or tuple(w_v.shape) != tuple(w_k.shape) \
+            or w_v.dtype != w_k.dtype:
+        raise ValueError("w_k, w_v must both be [d_model][n_heads * 256] of one dtype")
+    _check(lib().kvq_project_append_q4(_ptr(h), n_seq, _ptr(pos0), n_tok, d_model, _ptr(w_k),
+                                       _ptr(w_v), w_type, n_heads, 256, _ptr(page_table),
+                                       page_table.shape[1], page_size, n_cells, _ptr(k_pool),
+                                       _ptr(v_pool), _ptr(dev_status), _stream(stream)))
 
 
 def kvq_gather_q4(pool, pos0, n_tok, page_table, page_size, n_cells, out, dev_status=None,

@@ -230,6 +230,34 @@ int kvq_append_q4(const float* k, const float* v, int n_seq, const int32_t* pos0
                                              dev_status, (cudaStream_t)stream), E);
 }
 
+int kvq_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok, int d_model,
+                          const void* w_k, const void* w_v, int w_type, int n_heads, int head_dim,
+                          const int32_t* page_table, int max_pages, int page_size, int64_t n_cells,
+                          uint8_t* k_pool, uint8_t* v_pool, uint32_t* dev_status, kvq_stream_t stream)
+{
+    const char* E = "kvq_project_append_q4";
+    if (int st = injected(E)) return st;
+    if (!is_pow2(head_dim)) return fail(KVQ_ENOTPOW2, "%s: head_dim %d is not a power of two", E, head_dim);
+    if (head_dim != 256) return fail(KVQ_EINVAL, "%s: head_dim must be 256", E);
+    if (n_seq < 0 || n_tok < 0 || n_heads < 1 || max_pages < 1 || page_size < 1 || n_cells < 0)
+        return fail(KVQ_EINVAL, "%s: bad sizes", E);
+    if (d_model < 4 || d_model % 4 != 0) return fail(KVQ_EINVAL, "%s: d_model %d is not a positive multiple of 4", E, d_model);
+    if (w_type != KVQ_WEIGHT_F32 && w_type != KVQ_WEIGHT_BF16) return fail(KVQ_EINVAL, "%s: w_type %d", E, w_type);
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
+    if (n_tokens == 0) return KVQ_OK;
+    if (n_tokens > (int64_t)65535 * 16) return fail(KVQ_EINVAL, "%s: more than 1048560 tokens", E);
+    if ((int64_t)n_heads * 16 > INT32_MAX) return fail(KVQ_EINVAL, "%s: bad sizes", E);
+    if (!h || !w_k || !w_v || !pos0 || !page_table || !k_pool || !v_pool)
+        return fail(KVQ_EINVAL, "%s: NULL pointer", E);
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16)) return fail(KVQ_EALIGN, "%s: pools not 16-byte aligned", E);
+    if (!aligned(h, 16)) return fail(KVQ_EALIGN, "%s: h not 16-byte aligned", E);
+    if (!aligned(w_k, 16) || !aligned(w_v, 16)) return fail(KVQ_EALIGN, "%s: weights not 16-byte aligned", E);
+    return cuda_status(kvq::launch_project_append_q4(h, n_seq, pos0, n_tok, d_model, w_k, w_v,
+                                                     w_type == KVQ_WEIGHT_BF16, n_heads, page_table,
+                                                     max_pages, page_size, n_cells, k_pool, v_pool,
+                                                     dev_status, (cudaStream_t)stream), E);
+}
+
 int kvq_gather(const kvq_gather_desc* d, kvq_stream_t stream)
 {
     const char* E = "kvq_gather";

@@ -9,9 +9,10 @@
 // input, shuffles for the Walsh-Hadamard butterflies and the row reductions, and
 // 16-byte stores of the packed output staged through shared memory.
 #include <cuda_fp16.h>
-
-#include <atomic>
 #include <cuda_fp8.h>
+
+#include <algorithm>
+#include <atomic>
 
 #include "kvq_internal.cuh"
 
@@ -674,6 +675,61 @@ __device__ __forceinline__ void fwht256_lane8(float (&z)[8], int lane)
 // One warp per (sequence, token, K/V, head) row of 256, 8 elements per lane; block b of
 // 32 elements is lanes 4b .. 4b + 3.  The next row's loads are issued before this row's
 // arithmetic (16-byte loads when k and v allow them).
+// One row of 256 values, 8 consecutive ones a lane (element 8 * lane + k), rotated
+// (z = FWHT_256(x) / 16, stages h = 1..128) and stored as 8 q4_0 blocks of 18 bytes at
+// dst (16-byte aligned), staged through the warp's 144-byte s_row.
+__device__ __forceinline__ void q4_store_row(float (&z)[8], int lane, uint8_t* s_row, uint8_t* dst)
+{
+    fwht256_lane8(z, lane);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
+    // the block's preferred element: the largest key over the block's 4 lanes (every
+    // lane of the block gets the same); a block holding a NaN takes the scan of
+    // q4_prefer instead, which decides NaN by position like the reference order
+    uint32_t key = q4_key(z[0]);
+#pragma unroll
+    for (int j = 1; j < 8; ++j) key = max(key, q4_key(z[j]));
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) key = max(key, __shfl_xor_sync(kFull, key, o));
+    float mval = __uint_as_float(key >> 1);
+    if (!(key & 1u)) mval = -mval;
+    if (__any_sync(kFull, key > 0xFF000001u)) {
+        mval = z[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            if (q4_prefer(z[j], mval)) mval = z[j];
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            const float other = __shfl_xor_sync(kFull, mval, o);
+            if (q4_prefer(other, mval)) mval = other;
+        }
+    }
+    const float d = __fmul_rn(mval, -0.125f);          // mval / -8, exact
+    const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    uint32_t q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        q[j] = (uint32_t)min(max(__float2int_rz(__fmaf_rn(z[j], idv, 8.5f)), 0), 15);
+    // lanes 4b + p (p = 0, 1) hold codes j = 8p .. 8p + 7 of block b, lanes
+    // 4b + p + 2 the codes j + 16 that share their bytes (high nibble)
+    uint32_t w0 = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+    uint32_t w1 = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+    const uint32_t u0 = __shfl_down_sync(kFull, w0, 2), u1 = __shfl_down_sync(kFull, w1, 2);
+    const int b = lane >> 2, p = lane & 3;
+    if (p < 2) {
+        w0 |= u0 << 4;
+        w1 |= u1 << 4;
+        uint8_t* blk = s_row + b * 18;
+        uint16_t* hw = reinterpret_cast<uint16_t*>(blk + 2 + 8 * p);   // bytes 2 + 8p ..
+        hw[0] = (uint16_t)w0; hw[1] = (uint16_t)(w0 >> 16);
+        hw[2] = (uint16_t)w1; hw[3] = (uint16_t)(w1 >> 16);
+        if (p == 0) *reinterpret_cast<uint16_t*>(blk) = __half_as_ushort(__float2half_rn(d));
+    }
+    __syncwarp();
+    if (lane < 9) reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(s_row)[lane];
+    __syncwarp();
+}
+
 template <bool kVec>
 __device__ __forceinline__ void load8(const float* p, float4& a, float4& b)
 {
@@ -718,59 +774,258 @@ append_q4_kernel(const float* __restrict__ k, const float* __restrict__ v, int n
             if (r + 1 < rows) load8<kVec>(src_of(tok, r + 1), nx0, nx1);
             else if (tok + n_warps < n_tokens) load8<kVec>(src_of(tok + n_warps, 0), nx0, nx1);
             if (cell < 0) continue;
-            fwht256_lane8(z, lane);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) z[j] = __fmul_rn(z[j], 0.0625f);
-            // the block's preferred element: the largest key over the block's 4 lanes (every
-            // lane of the block gets the same); a block holding a NaN takes the scan of
-            // q4_prefer instead, which decides NaN by position like the reference order
-            uint32_t key = q4_key(z[0]);
-#pragma unroll
-            for (int j = 1; j < 8; ++j) key = max(key, q4_key(z[j]));
-#pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) key = max(key, __shfl_xor_sync(kFull, key, o));
-            float mval = __uint_as_float(key >> 1);
-            if (!(key & 1u)) mval = -mval;
-            if (__any_sync(kFull, key > 0xFF000001u)) {
-                mval = z[0];
-#pragma unroll
-                for (int j = 1; j < 8; ++j)
-                    if (q4_prefer(z[j], mval)) mval = z[j];
-#pragma unroll
-                for (int o = 1; o <= 2; o <<= 1) {
-                    const float other = __shfl_xor_sync(kFull, mval, o);
-                    if (q4_prefer(other, mval)) mval = other;
-                }
-            }
-            const float d = __fmul_rn(mval, -0.125f);          // mval / -8, exact
-            const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-            uint32_t q[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                q[j] = (uint32_t)min(max(__float2int_rz(__fmaf_rn(z[j], idv, 8.5f)), 0), 15);
-            // lanes 4b + p (p = 0, 1) hold codes j = 8p .. 8p + 7 of block b, lanes
-            // 4b + p + 2 the codes j + 16 that share their bytes (high nibble)
-            uint32_t w0 = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-            uint32_t w1 = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
-            const uint32_t u0 = __shfl_down_sync(kFull, w0, 2), u1 = __shfl_down_sync(kFull, w1, 2);
-            const int b = lane >> 2, p = lane & 3;
-            if (p < 2) {
-                w0 |= u0 << 4;
-                w1 |= u1 << 4;
-                uint8_t* blk = s_row[wib] + b * 18;
-                uint16_t* dst = reinterpret_cast<uint16_t*>(blk + 2 + 8 * p);   // bytes 2 + 8p ..
-                dst[0] = (uint16_t)w0; dst[1] = (uint16_t)(w0 >> 16);
-                dst[2] = (uint16_t)w1; dst[3] = (uint16_t)(w1 >> 16);
-                if (p == 0) *reinterpret_cast<uint16_t*>(blk) = __half_as_ushort(__float2half_rn(d));
-            }
-            __syncwarp();
             const int kv = r >= n_heads;
-            uint8_t* dst = (kv ? v_pool : k_pool) + (cell * n_heads + (r - kv * n_heads)) * 144;
-            if (lane < 9)
-                reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(s_row[wib])[lane];
-            __syncwarp();
+            q4_store_row(z, lane, s_row[wib],
+                         (kv ? v_pool : k_pool) + (cell * n_heads + (r - kv * n_heads)) * 144);
         }
     }
+}
+
+// ------------------------------------------------------------------------------------
+// Project-and-append producer of the q4_0 pools: a new token's K and V rows are
+// y = h . W (W [d_model][n_heads * 256], fp32 or bfloat16, row-major), rotated and stored
+// as kvq_append_q4 stores a row, in one launch: no fp32 row is written to memory.
+// The sum has a fixed fp32 order: k runs in 64 chunks of L = 4 ceil(d_model / 256)
+// consecutive terms (the last ones short or empty); each chunk is one chain
+// acc = fmaf(h[k], w[k][c], acc) from acc = 0 in ascending k, and the 64 chunk sums are
+// added pairwise, (0 + 1), (2 + 3), ..., then the 32, 16, 8, 4 and 2 results the same way.
+// A cluster of 4 CTAs owns one head row (K head or V head) of a group of 8 tokens.  CTA
+// rank r takes chunks 16r .. 16r + 15, one a warp, for all 256 columns (lane = 8
+// consecutive columns, so a warp reads whole 512- or 1024-byte weight rows) and the 8
+// tokens (NP pairs of them: a group of fewer than 8 tokens runs no chains on empty
+// ones); the warp stages its weight rows in shared memory by cp.async (two 4 KB batches
+// in flight) and the tokens' h values per 64-term window, and runs its fma chains two at
+// a time (fma.rn.f32x2, one rounding per lane).  The CTA adds its 16 chunks (the
+// first four pairwise levels); rank r then finishes the last two levels over the 4
+// ranks' sums for tokens 2r and 2r + 1, read from the cluster's shared memory, and
+// rotates and stores those rows.
+// ------------------------------------------------------------------------------------
+constexpr int kProjTok = 8;                           // tokens per cluster
+constexpr int kProjRanks = 4;                         // CTAs per cluster (chunk groups)
+constexpr int kProjLocal = 16;                        // chunks per CTA (64 in all), a warp each
+constexpr int kProjWarps = kProjLocal;
+constexpr int kProjThreads = 32 * kProjWarps;
+constexpr int kProjWin = 64;                          // h terms staged per window
+constexpr int kProjBatch = 4096;                      // weight bytes a warp stages per batch
+constexpr int kProjStages = 2;                        // batches a warp has in its ring
+constexpr size_t kProjWBytes = (size_t)kProjWarps * kProjStages * kProjBatch;       // 128 KB
+constexpr size_t kProjPBytes = (size_t)kProjLocal * kProjTok * 256 * 4;             // 128 KB
+constexpr size_t kProjHBytes = (size_t)kProjWarps * kProjWin * kProjTok * 4;        // 32 KB
+constexpr size_t kProjRBytes = (size_t)kProjTok * 256 * 4;                          // 8 KB
+static_assert(kProjWBytes >= kProjPBytes, "the weight stages become the chunk sums");
+static_assert(kProjRanks * kProjLocal == 64 && 2 * kProjRanks == kProjTok, "64 chunks, 2 tokens a rank");
+constexpr size_t kProjSmem = kProjWBytes + kProjHBytes + kProjRBytes + 2 * 144;
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+    return v;
+}
+
+// d.x = fma(a.x, b.x, d.x), d.y = fma(a.y, b.y, d.y): two fp32 fmas, each rounded once
+__device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t dup2(float x)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+template <bool kBf16, int NP>
+__global__ void __cluster_dims__(kProjRanks, 1, 1) __launch_bounds__(kProjThreads, 1)
+project_append_q4_kernel(const float* __restrict__ h, int n_seq, const int32_t* __restrict__ pos0,
+                         int n_tok, int d_model, const void* __restrict__ w_k,
+                         const void* __restrict__ w_v, int n_heads,
+                         const int32_t* __restrict__ page_table, int max_pages, int page_size,
+                         int64_t n_cells, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
+                         uint32_t* __restrict__ dev_status)
+{
+    extern __shared__ __align__(16) float proj_smem[];
+    float* s_p = proj_smem;                            // [16 chunks][8 tokens][256 columns],
+                                                       // the weight stages until then
+    float* s_h = proj_smem + kProjWBytes / 4;          // [warp][64 terms][8 tokens]
+    float* s_r = s_h + kProjHBytes / 4;                // [8 tokens][256 columns]
+    uint8_t* s_row = reinterpret_cast<uint8_t*>(s_r + kProjTok * 256);   // [2][144]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t rank = cluster_rank();
+    const int unit = blockIdx.x / kProjRanks;          // K heads 0 .. n_heads - 1, then V heads
+    const int kv = unit >= n_heads, head = unit - kv * n_heads;
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
+    const int64_t tok0 = (int64_t)blockIdx.y * kProjTok;
+    const int nt = (int)min((int64_t)kProjTok, n_tokens - tok0);
+    const int64_t n_out = (int64_t)n_heads * 256;
+    const int L = 4 * ((d_model + 255) / 256);
+    const int chunk = kProjLocal * rank + warp;
+    const int k0 = min(chunk * L, d_model), k1 = min(k0 + L, d_model);
+
+    // this warp's weight rows: columns head * 256 .. + 255 of rows k0 .. k1 - 1
+    constexpr int kElt = kBf16 ? 2 : 4;
+    constexpr int kSlab = 256 * kElt;                  // bytes of a row
+    constexpr int kRows = kProjBatch / kSlab;          // rows a batch (8 or 4)
+    constexpr int kPerRow = kSlab / 16;                // 16-byte pieces a row
+    const uint8_t* wsrc = static_cast<const uint8_t*>(kv ? w_v : w_k) + (int64_t)head * 256 * kElt;
+    const int64_t row_bytes = n_out * kElt;
+    uint8_t* wst = reinterpret_cast<uint8_t*>(s_p) + (size_t)warp * kProjStages * kProjBatch;
+    const uint32_t wst_sa = (uint32_t)__cvta_generic_to_shared(wst);
+    // rows k .. k + n - 1 into stage st: lane copies the 16-byte pieces lane, lane + 32, ...
+    auto issue = [&](int k, int n, int st) {
+        const uint32_t dst = wst_sa + st * kProjBatch + 16 * lane;
+#pragma unroll
+        for (int j = 0; j < kProjBatch / 512; ++j) {
+            const int q = 32 * j + lane, row = q / kPerRow;
+            if (row < n)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 512 * j),
+                             "l"(wsrc + (int64_t)(k + row) * row_bytes + 16 * (q - row * kPerRow))
+                             : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    // acc[p][j]: tokens 2p (low half) and 2p + 1 (high half) of column 8 lane + j
+    uint64_t acc[NP][8];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[p][j] = 0ull;
+    float* hw = s_h + warp * (kProjWin * kProjTok);
+    for (int kw = k0; kw < k1; kw += kProjWin) {
+        const int kn = min(kProjWin, k1 - kw);         // a multiple of 4
+        const int nb = (kn + kRows - 1) / kRows;
+        issue(kw, min(kRows, kn), 0);
+        // stage h[tok0 + t][kw .. kw + kn) as hw[k][t]: lane = (token t, 16-term quarter)
+        {
+            const int t = lane & 7, kq = 16 * (lane >> 3);
+            const float* src = h + (tok0 + min(t, nt - 1)) * d_model + kw + kq;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (t < nt && kq + i < kn) x = __ldg(reinterpret_cast<const float4*>(src + i));
+                hw[(kq + i) * kProjTok + t] = x.x;
+                hw[(kq + i + 1) * kProjTok + t] = x.y;
+                hw[(kq + i + 2) * kProjTok + t] = x.z;
+                hw[(kq + i + 3) * kProjTok + t] = x.w;
+            }
+        }
+        for (int b = 0; b < nb; ++b) {
+            const int kb = b * kRows, nr = min(kRows, kn - kb);
+            if (b + 1 < nb) {                          // batch b + 1 stays in flight
+                issue(kw + kb + kRows, min(kRows, kn - kb - kRows), (b + 1) % kProjStages);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncwarp();                              // batch b (and the h window) visible
+            const uint8_t* ws = wst + (b % kProjStages) * kProjBatch + (8 * kElt) * lane;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                if (r < nr) {
+                    float wv[8];
+                    if constexpr (kBf16) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(ws + r * kSlab);
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            wv[2 * j] = __uint_as_float(uw[j] << 16);
+                            wv[2 * j + 1] = __uint_as_float(uw[j] & 0xFFFF0000u);
+                        }
+                    } else {
+                        const float4 a = *reinterpret_cast<const float4*>(ws + r * kSlab);
+                        const float4 c = *reinterpret_cast<const float4*>(ws + r * kSlab + 16);
+                        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+                        wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+                    }
+                    // the 8 tokens' h of this row as 4 pairs (token 2p low, 2p + 1 high)
+                    const ulonglong2* hp = reinterpret_cast<const ulonglong2*>(hw + (kb + r) * kProjTok);
+                    uint64_t hv[4];
+                    const ulonglong2 h0 = hp[0];
+                    hv[0] = h0.x; hv[1] = h0.y;
+                    if constexpr (NP > 2) {
+                        const ulonglong2 h1 = hp[1];
+                        hv[2] = h1.x; hv[3] = h1.y;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint64_t wd = dup2(wv[j]);
+#pragma unroll
+                        for (int p = 0; p < NP; ++p) fma2(acc[p][j], hv[p], wd);
+                    }
+                }
+            }
+            __syncwarp();                              // stage b % 2 is refilled next
+        }
+    }
+    __syncthreads();                                   // the weight stages become s_p
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {                     // rows of tokens past 2 NP are not read
+        float* d0 = s_p + (warp * kProjTok + 2 * p) * 256 + 8 * lane;
+        float* d1 = d0 + 256;
+        *reinterpret_cast<float4*>(d0) = make_float4(lo_of(acc[p][0]), lo_of(acc[p][1]), lo_of(acc[p][2]), lo_of(acc[p][3]));
+        *reinterpret_cast<float4*>(d0 + 4) = make_float4(lo_of(acc[p][4]), lo_of(acc[p][5]), lo_of(acc[p][6]), lo_of(acc[p][7]));
+        *reinterpret_cast<float4*>(d1) = make_float4(hi_of(acc[p][0]), hi_of(acc[p][1]), hi_of(acc[p][2]), hi_of(acc[p][3]));
+        *reinterpret_cast<float4*>(d1 + 4) = make_float4(hi_of(acc[p][4]), hi_of(acc[p][5]), hi_of(acc[p][6]), hi_of(acc[p][7]));
+    }
+    __syncthreads();
+    // the first four pairwise levels over this CTA's 16 chunks, per (token, column)
+    for (int i = threadIdx.x; i < kProjTok * 256; i += kProjThreads) {
+        float p[kProjLocal];
+#pragma unroll
+        for (int q = 0; q < kProjLocal; ++q) p[q] = s_p[q * kProjTok * 256 + i];
+#pragma unroll
+        for (int n = kProjLocal; n > 1; n >>= 1)
+#pragma unroll
+            for (int j = 0; j < n / 2; ++j) p[j] = __fadd_rn(p[2 * j], p[2 * j + 1]);
+        s_r[i] = p[0];
+    }
+    cluster_sync_all();                                // every rank's sums are in place
+
+    // tokens 2r, 2r + 1: the last two levels over the 4 ranks (lane = columns 8 lane ..
+    // 8 lane + 7), then the rotation, the q4_0 blocks and the pool row
+    if (warp < 2) {
+        const int tl = 2 * (int)rank + warp;
+        const int64_t tok = tok0 + tl;
+        if (tl < nt) {
+            const int s = (int)(tok / n_tok), t = (int)(tok - (int64_t)s * n_tok);
+            const int64_t cell = q4_cell(page_table, max_pages, page_size, n_cells, s, pos0[s] + t);
+            if (cell < 0) {
+                if (lane == 0 && dev_status) atomicOr(dev_status, (unsigned)KVQ_DEV_BAD_PAGE);
+            } else {
+                const uint32_t la = (uint32_t)__cvta_generic_to_shared(s_r + tl * 256 + 8 * lane);
+                float v[kProjRanks][8];
+#pragma unroll
+                for (int q = 0; q < kProjRanks; ++q) {
+                    const float4 a = ld_cluster_f4(la, q), b = ld_cluster_f4(la + 16, q);
+                    v[q][0] = a.x; v[q][1] = a.y; v[q][2] = a.z; v[q][3] = a.w;
+                    v[q][4] = b.x; v[q][5] = b.y; v[q][6] = b.z; v[q][7] = b.w;
+                }
+                float z[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    z[j] = __fadd_rn(__fadd_rn(v[0][j], v[1][j]), __fadd_rn(v[2][j], v[3][j]));
+                q4_store_row(z, lane, s_row + 144 * warp,
+                             (kv ? v_pool : k_pool) + (cell * n_heads + head) * 144);
+            }
+        }
+    }
+    cluster_sync_all();                                // the peers' reads of s_r are done
 }
 
 // gather: rows (s, t, h) -> binary16 [256], (q - 8) * d rounded to nearest even
@@ -1079,6 +1334,42 @@ cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const in
         append_q4_kernel<false><<<grid_for(n_tokens, kCodecWarps), kCodecThreads, 0, s>>>(
             k, v, n_seq, pos0, n_tok, n_heads, page_table, max_pages, page_size, n_cells,
             k_pool, v_pool, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok,
+                                     int d_model, const void* w_k, const void* w_v, bool w_bf16,
+                                     int n_heads, const int32_t* page_table, int max_pages,
+                                     int page_size, int64_t n_cells, uint8_t* k_pool,
+                                     uint8_t* v_pool, uint32_t* dev_status, cudaStream_t s)
+{
+    const int64_t n_tokens = (int64_t)n_seq * n_tok;
+    if (n_tokens == 0 || n_heads == 0) return cudaSuccess;
+    using Kern = void (*)(const float*, int, const int32_t*, int, int, const void*, const void*, int,
+                          const int32_t*, int, int, int64_t, uint8_t*, uint8_t*, uint32_t*);
+    // token pairs a group computes: 4, or fewer when all tokens fit in one short group
+    const int np = (int)std::min<int64_t>(kProjTok / 2, (n_tokens + 1) / 2);
+    static const Kern kKern[2][4] = {
+        {project_append_q4_kernel<false, 1>, project_append_q4_kernel<false, 2>,
+         project_append_q4_kernel<false, 3>, project_append_q4_kernel<false, 4>},
+        {project_append_q4_kernel<true, 1>, project_append_q4_kernel<true, 2>,
+         project_append_q4_kernel<true, 3>, project_append_q4_kernel<true, 4>}};
+    const Kern kern = kKern[w_bf16 ? 1 : 0][np - 1];
+    // the shared-memory opt-in, once per (device, kernel)
+    static std::atomic<uint32_t> opted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint32_t bit = 1u << ((w_bf16 ? 4 : 0) + np - 1);
+    if (dev >= 64 || !(opted[dev].load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) opted[dev].fetch_or(bit, std::memory_order_release);
+    }
+    const dim3 grid((unsigned)(kProjRanks * 2 * n_heads), (unsigned)((n_tokens + kProjTok - 1) / kProjTok));
+    kern<<<grid, kProjThreads, kProjSmem, s>>>(h, n_seq, pos0, n_tok, d_model, w_k, w_v, n_heads,
+                                              page_table, max_pages, page_size, n_cells, k_pool,
+                                              v_pool, dev_status);
     return cudaGetLastError();
 }
 

@@ -191,6 +191,11 @@ cudaError_t launch_append_q4(const float* k, const float* v, int n_seq, const in
                              int n_tok, int n_heads, const int32_t* page_table, int max_pages,
                              int page_size, int64_t n_cells, uint8_t* k_pool, uint8_t* v_pool,
                              uint32_t* dev_status, cudaStream_t s);
+cudaError_t launch_project_append_q4(const float* h, int n_seq, const int32_t* pos0, int n_tok,
+                                     int d_model, const void* w_k, const void* w_v, bool w_bf16,
+                                     int n_heads, const int32_t* page_table, int max_pages,
+                                     int page_size, int64_t n_cells, uint8_t* k_pool,
+                                     uint8_t* v_pool, uint32_t* dev_status, cudaStream_t s);
 cudaError_t launch_gather_q4(const kvq_gather_desc& d, cudaStream_t s);
 cudaError_t launch_gather_mla(const kvq_gather_desc& d, cudaStream_t s);
 

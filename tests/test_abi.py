@@ -76,6 +76,27 @@ def test_encode_mla_argument_errors(kvq):
     assert call(rows=0, c=None) == 0                                      # no-op
 
 
+def test_project_append_argument_errors(kvq):
+    L = kvq.lib()
+    def call(h=FAKE, d_model=1024, wk=FAKE, wv=FAKE, w_type=kvq.WEIGHT_F32, n_seq=1, n_tok=1,
+             head_dim=256, kp=FAKE, pt=FAKE):
+        return L.kvq_project_append_q4(h, n_seq, FAKE, n_tok, d_model, wk, wv, w_type, 8, head_dim,
+                                       pt, 1, 64, 64, kp, FAKE, None, None)
+    assert call(head_dim=250) == 2
+    assert call(head_dim=128) == 1
+    assert call(d_model=1022) == 1                                         # not a multiple of 4
+    assert call(d_model=0) == 1
+    assert call(w_type=2) == 1
+    assert call(n_seq=65536, n_tok=17) == 1                                # too many tokens
+    assert call(wv=None) == 1
+    assert call(pt=None) == 1
+    assert call(h=FAKE + 4) == 4                                           # h rows need 16 bytes
+    assert call(wk=FAKE + 8) == 4                                          # 16-byte rows
+    assert call(wv=FAKE + 8, w_type=kvq.WEIGHT_BF16) == 4                  # bf16 too
+    assert call(kp=FAKE + 8) == 4
+    assert call(n_tok=0, h=None) == 0                                      # no-op
+
+
 def test_append_and_gather_argument_errors(kvq):
     L = kvq.lib()
     assert L.kvq_append_q4(FAKE, FAKE, 1, FAKE, 1, 8, 250, FAKE, 1, 64, 64, FAKE, FAKE, None, None) == 2

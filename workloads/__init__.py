@@ -144,6 +144,25 @@ def q4_paged(n_seq: int = 16, n_tok: int = 8192, n_heads: int = 8, page_size: in
     return Q4Workload(k, v, np.full(n_seq, pos0, np.int32), table, page_size, n_pages * page_size)
 
 
+def projection_inputs(n_seq: int, n_tok: int, d_model: int, n_heads: int, seed: int,
+                      bf16: bool = False):
+    """Hidden rows h [n_seq][n_tok][d_model] (N(0,1) times a per-token amplitude drawn
+    from {1e-3, 1, 40}) and K/V projection weights [d_model][n_heads * 256], N(0, 1/d_model)
+    so that projected rows are of the order of h.  With bf16 the weights are bfloat16 bit
+    patterns (uint16): the upper halves of the fp32 draws."""
+    g = rng(seed + 13)
+    amp_choices = np.array([1e-3, 1.0, 40.0], np.float32)
+    h = normal(g, (n_seq, n_tok, d_model))
+    h *= amp_choices[g.integers(0, 3, (n_seq, n_tok))][..., None]
+    sd = np.float32(1.0 / np.sqrt(d_model))
+    w_k = normal(g, (d_model, n_heads * 256)) * sd
+    w_v = normal(g, (d_model, n_heads * 256)) * sd
+    if bf16:
+        w_k = (w_k.view(np.uint32) >> 16).astype(np.uint16)
+        w_v = (w_v.view(np.uint32) >> 16).astype(np.uint16)
+    return h, w_k, w_v
+
+
 def paged_table(n_seq: int, n_tok: int, page_size: int, pos0: int, seed: int):
     """(pos0 [n_seq], page table [n_seq][max_pages], n_cells) for appending n_tok tokens
     per sequence from position pos0: the table is a seeded permutation of all page ids."""
