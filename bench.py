@@ -753,6 +753,33 @@ def decode_records(args, dev, wanted=lambda name: True):
         del probs, keep, base
         torch.cuda.empty_cache()
 
+    def batch_seq(name, fmt, n_seq, T, H):
+        """n_seq sequences of T rows (contiguous, one query each) in one call: the per-call
+        fixed cost (start-up, last tile, combine) spread over n_seq x T rows."""
+        if not wanted(name):
+            return
+        rb = {kvq.FMT_FP8: 584, kvq.FMT_TQ4: 328}[fmt]
+        layers = max(2, min(64, -(-target // (n_seq * T * rb))))
+        base = encode_pool(n_seq * T, fmt)
+        q = W.queries(n_seq, 1, H, seed=0)
+        q_lat = torch.from_numpy(q.q_lat).to(dev)
+        q_rope = torch.from_numpy(q.q_rope).to(dev)
+        seq_len = torch.full((n_seq,), T, dtype=torch.int32, device=dev)
+        impl = args.decode_impl
+        if fmt != kvq.FMT_FP8 and impl == 5:
+            impl = 0
+        probs, keep = [], []
+        for l in range(layers):
+            cache = base if l == 0 else clone(base)
+            keep.append(cache)
+            kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
+            probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat, q_rope=q_rope,
+                                          sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt,
+                                          seq_stride_rows=T, impl=impl, **kw))
+        measure(name, probs, (n_seq, 1, H, 512), n_seq * T, rb, 2 * H * 1088 * n_seq * T)
+        del probs, keep, base
+        torch.cuda.empty_cache()
+
     F8, T4 = kvq.FMT_FP8, kvq.FMT_TQ4
     one_seq("fp8 tiny: T=1024, H=16, magnitudes log-uniform [1e-3, 40]", F8, 1024, 16, mag=(1e-3, 40.0))
     one_seq("TQ4: T=32768, H=64", T4, 32768, 64)
@@ -761,6 +788,7 @@ def decode_records(args, dev, wanted=lambda name: True):
     for fmt, tag in ((F8, "fp8"), (T4, "TQ4")):
         for T in (32768, 131072):
             one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
+        batch_seq(f"HBM point, batch: {tag}, 8 seqs x T=32768, H=16", fmt, 8, 32768, 16)
     for fmt, tag in ((kvq.FMT_TQ6, "TQ6"), (kvq.FMT_TQ3, "TQ3")):
         one_seq(f"{tag}: T=32768, H=16", fmt, 32768, 16)
 
