@@ -342,6 +342,7 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
     __shared__ TqBucket s_tab[G::n];
     __shared__ float s_t[kCodecWarps][544];
     __shared__ __align__(16) uint8_t s_out[kCodecWarps][kRowBytes];
+    __shared__ __align__(16) uint8_t s_code[kCodecWarps][512];
     const float* thr_c = tq512_thresholds<BITS>();
     for (int b = threadIdx.x; b < G::n; b += blockDim.x) {
         const float lo = ((float)b - G::off - 0.5f) / G::scale;
@@ -439,52 +440,74 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
         const float sigma = __fmul_rn(rad, c);
         const float inv = __frcp_rn(sigma);
         const bool exact_row = !(sigma >= 0x1p-120f);      // tiny sigma: divide every element
-        int code[16];
+        // the code from u' = y * rcp(sigma) and the bucket of u', one byte per element into
+        // s_code (element order); elements within reach of their bucket's threshold (bit k
+        // of `near`) are decided again by the IEEE quotient, which shares the bucket (its
+        // threshold is 1e-3 from the edges), except in a row of tiny sigma, where u' is not
+        // used at all.  y stays in the (now free) transpose buffer for those decisions.
+        uint8_t* cb = s_code[wib];
+        const int eb = (lane >> 4) * 256 + (lane & 15);    // element of register k: eb + 16 k
+        uint32_t near = 0;
+        auto bucket_of = [&](float u1) {
+            const float bf = __fmaf_rn(u1, G::scale, 12582912.0f + G::off);
+            return s_tab[min(max(__float_as_int(bf) - 0x4B400000, 0), G::n - 1)];
+        };
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
+            st[rb + 17 * k] = v[k];
             const float u1 = __fmul_rn(v[k], inv);
-            const float bf = __fmaf_rn(u1, G::scale, 12582912.0f + G::off);
-            const int b = min(max(__float_as_int(bf) - 0x4B400000, 0), G::n - 1);
-            const TqBucket e = s_tab[b];
-            code[k] = e.base + (u1 >= e.thr ? 1 : 0);
-            if (exact_row || fabsf(__fsub_rn(u1, e.thr)) <= kTqNear) {
-                // within reach of the threshold: the IEEE quotient decides.  u and u' share
-                // the bucket (its threshold is 1e-3 from the edges), except in a row of
-                // tiny sigma, where u' is not used at all
-                const float u = __fdiv_rn(v[k], sigma);
-                if (exact_row) {
-                    int n = 0;
-                    for (int t = 0; t < kNThr; ++t) n += (u >= thr_c[t]) ? 1 : 0;
-                    code[k] = n;
-                } else {
-                    code[k] = e.base + (u >= e.thr ? 1 : 0);
+            const TqBucket e = bucket_of(u1);
+            cb[eb + 16 * k] = (uint8_t)(rad == 0.0f ? 0 : e.base + (u1 >= e.thr ? 1 : 0));
+            near |= (fabsf(__fsub_rn(u1, e.thr)) <= kTqNear ? 1u : 0u) << k;
+        }
+        if (exact_row) near = 0xFFFFu;
+        if (rad == 0.0f) near = 0;                          // an all-zero row codes to 0
+        if (__any_sync(kFull, near != 0)) {
+#pragma unroll 1
+            for (int k = 0; k < 16; ++k) {
+                if ((near >> k) & 1u) {
+                    const float y = st[rb + 17 * k];
+                    const float u = __fdiv_rn(y, sigma);
+                    int c;
+                    if (exact_row) {
+                        c = 0;
+                        for (int t = 0; t < kNThr; ++t) c += (u >= thr_c[t]) ? 1 : 0;
+                    } else {
+                        const TqBucket e = bucket_of(__fmul_rn(y, inv));
+                        c = e.base + (u >= e.thr ? 1 : 0);
+                    }
+                    cb[eb + 16 * k] = (uint8_t)c;
                 }
             }
-            if (rad == 0.0f) code[k] = 0;
         }
-        // lane L holds codes of elements (L >> 4) * 256 + k * 16 + (L & 15)
+        __syncwarp();
+        // lane l packs elements 16l .. 16l + 15: code i at bits BITS i .. of the row
+        // (little-endian), i.e. BITS * 2 bytes at byte 2 BITS l
         uint8_t* out = s_out[wib];
-        if constexpr (BITS == 4) {
-            // byte (lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1); odd lanes the high nibble
+        {
+            const uint4 c16 = reinterpret_cast<const uint4*>(cb)[lane];
+            if constexpr (BITS == 4) {
+                const uint32_t t0 = c16.x | (c16.x >> 4), t1 = c16.y | (c16.y >> 4);
+                const uint32_t t2 = c16.z | (c16.z >> 4), t3 = c16.w | (c16.w >> 4);
+                reinterpret_cast<uint2*>(out)[lane] =
+                    make_uint2(__byte_perm(t0, t1, 0x6420), __byte_perm(t2, t3, 0x6420));
+            } else {
+                const uint32_t cw[4] = {c16.x, c16.y, c16.z, c16.w};
+                uint32_t g[4];                              // codes 4j .. 4j + 3 as 4 BITS bits
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int hi = __shfl_down_sync(kFull, code[k], 1);
-                if ((lane & 1) == 0)
-                    out[(lane >> 4) * 128 + k * 8 + ((lane & 15) >> 1)] = (uint8_t)(code[k] | (hi << 4));
-            }
-        } else {
-            constexpr int kG = 24 / BITS;        // consecutive codes (lanes) a 3-byte group
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                uint32_t w = (uint32_t)code[k];
-#pragma unroll
-                for (int d = 1; d < kG; d <<= 1) w |= __shfl_down_sync(kFull, w, d) << (BITS * d);
-                if ((lane & (kG - 1)) == 0) {
-                    const int e = (lane >> 4) * 256 + k * 16 + (lane & 15);
-                    uint8_t* dst = out + e * BITS / 8;
-                    dst[0] = (uint8_t)w;
-                    dst[1] = (uint8_t)(w >> 8);
-                    dst[2] = (uint8_t)(w >> 16);
+                for (int j = 0; j < 4; ++j)
+                    g[j] = (cw[j] & 0xFFu) | ((cw[j] >> 8) & 0xFFu) << BITS |
+                           ((cw[j] >> 16) & 0xFFu) << (2 * BITS) | (cw[j] >> 24) << (3 * BITS);
+                if constexpr (BITS == 6) {                  // four 24-bit groups: 12 bytes
+                    uint32_t* o = reinterpret_cast<uint32_t*>(out + 12 * lane);
+                    o[0] = g[0] | g[1] << 24;
+                    o[1] = g[1] >> 8 | g[2] << 16;
+                    o[2] = g[2] >> 16 | g[3] << 8;
+                } else {                                    // four 12-bit groups: 6 bytes
+                    uint16_t* o = reinterpret_cast<uint16_t*>(out + 6 * lane);
+                    o[0] = (uint16_t)(g[0] | g[1] << 12);
+                    o[1] = (uint16_t)(g[1] >> 4 | g[2] << 8);
+                    o[2] = (uint16_t)(g[2] >> 8 | g[3] << 4);
                 }
             }
         }
