@@ -722,7 +722,7 @@ def decode_records(args, dev, wanted=lambda name: True):
         records.append(rec)
         return rec
 
-    def one_seq(name, fmt, T, H, idx_k=0, mag=None):
+    def one_seq(name, fmt, T, H, idx_k=0, mag=None, overlap=0):
         if not wanted(name):
             return
         rb = {kvq.FMT_FP8: 584, kvq.FMT_TQ4: 328, kvq.FMT_TQ6: 456, kvq.FMT_TQ3: 264}[fmt]
@@ -747,13 +747,13 @@ def decode_records(args, dev, wanted=lambda name: True):
             kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
             probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat, q_rope=q_rope,
                                           sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt, idx=idx,
-                                          impl=impl, **kw))
+                                          impl=impl, overlap_prior=overlap, **kw))
         n = idx_k or T
         measure(name, probs, (1, 1, H, 512), n, rb, 2 * H * 1088 * n)
         del probs, keep, base
         torch.cuda.empty_cache()
 
-    def batch_seq(name, fmt, n_seq, T, H):
+    def batch_seq(name, fmt, n_seq, T, H, overlap=0):
         """n_seq sequences of T rows (contiguous, one query each) in one call: the per-call
         fixed cost (start-up, last tile, combine) spread over n_seq x T rows."""
         if not wanted(name):
@@ -775,7 +775,7 @@ def decode_records(args, dev, wanted=lambda name: True):
             kw = dict(fp8=cache) if fmt == kvq.FMT_FP8 else dict(tq4=cache, signs=signs)
             probs.append(kvq.make_problem(seq_len=seq_len, q_lat=q_lat, q_rope=q_rope,
                                           sm_scale=W.SM_SCALE, max_seq_len=T, fmt=fmt,
-                                          seq_stride_rows=T, impl=impl, **kw))
+                                          seq_stride_rows=T, impl=impl, overlap_prior=overlap, **kw))
         measure(name, probs, (n_seq, 1, H, 512), n_seq * T, rb, 2 * H * 1088 * n_seq * T)
         del probs, keep, base
         torch.cuda.empty_cache()
@@ -789,6 +789,11 @@ def decode_records(args, dev, wanted=lambda name: True):
         for T in (32768, 131072):
             one_seq(f"HBM point: {tag}, T={T}, H=16", fmt, T, 16)
         batch_seq(f"HBM point, batch: {tag}, 8 seqs x T=32768, H=16", fmt, 8, 32768, 16)
+    # the same fp8 calls with overlap_prior: each decode of the graph's back-to-back calls
+    # (distinct caches, nothing written between them) may start during the combine before it
+    for T in (32768, 131072):
+        one_seq(f"HBM point, calls overlapped: fp8, T={T}, H=16", F8, T, 16, overlap=1)
+    batch_seq("HBM point, batch, calls overlapped: fp8, 8 seqs x T=32768, H=16", F8, 8, 32768, 16, overlap=1)
     for fmt, tag in ((kvq.FMT_TQ6, "TQ6"), (kvq.FMT_TQ3, "TQ3")):
         one_seq(f"{tag}: T=32768, H=16", fmt, 32768, 16)
 

@@ -356,6 +356,18 @@ typedef struct kvq_mla_problem {
                                        5: tcgen05 kernel of the fp8 tier, 16 heads a
                                           CTA, e4m3 codes read by the tensor core as
                                           they are (kind::f8f6f4)                        */
+    int32_t overlap_prior;          /* 0: the call starts after everything before it on
+                                       the stream.  1 (used by kernel 5 alone; the others
+                                       ignore it): the decode may start while the kernel
+                                       just before it still runs, once that kernel lets
+                                       dependents launch (this library's combine does, so
+                                       back-to-back calls overlap a decode's start with the
+                                       previous call's combine).  It reads the queries and
+                                       writes the workspace and outputs only after that
+                                       kernel has completed, but reads the cache rows and
+                                       scales, seq_len, seq_fmt and block_table, and may set
+                                       dev_status bits, before: set 1 only when the kernel
+                                       just before the call writes none of those.  0 or 1. */
 } kvq_mla_problem;
 
 /* Bytes of workspace kvq_mla_decode needs for this problem (0 if invalid). */

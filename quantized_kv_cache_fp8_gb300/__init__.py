@@ -81,7 +81,8 @@ class MlaProblem(C.Structure):
                 ("max_pages", _i32), ("page_size", _i32), ("seq_stride_rows", _i64),
                 ("fp8", MlaCache), ("tq4", MlaCache), ("tq4_signs", _p),
                 ("q_lat", _p), ("q_rope", _p), ("idx", _p), ("top_k", _i32),
-                ("sm_scale", _f32), ("split_rows", _i32), ("impl", _i32)]
+                ("sm_scale", _f32), ("split_rows", _i32), ("impl", _i32),
+                ("overlap_prior", _i32)]
 
 
 class Q4Problem(C.Structure):
@@ -309,7 +310,8 @@ def _cache(planes):
 
 def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, seq_fmt=None,
                  causal=False, block_table=None, page_size=0, seq_stride_rows=0, fp8=None,
-                 tq4=None, signs=None, idx=None, split_rows=0, impl=0) -> MlaProblem:
+                 tq4=None, signs=None, idx=None, split_rows=0, impl=0,
+                 overlap_prior=0) -> MlaProblem:
     """Fill a kvq_mla_problem from torch tensors.  The returned object holds a reference
     to every tensor whose device pointer it carries, so the memory stays allocated (and
     is not handed to a later allocation) for as long as the problem is alive."""
@@ -326,6 +328,7 @@ def make_problem(*, seq_len, q_lat, q_rope, sm_scale, max_seq_len, fmt=FMT_FP8, 
     if idx is not None:
         p.idx, p.top_k = _ptr(idx), idx.shape[-1]
     p.sm_scale, p.split_rows, p.impl = float(sm_scale), int(split_rows), int(impl)
+    p.overlap_prior = int(overlap_prior)
     p._keep = [seq_len, seq_fmt, block_table, fp8, tq4, signs, q_lat, q_rope, idx]
     return p
 

@@ -301,6 +301,7 @@ static int validate_decode(const kvq_mla_problem* p, const char* E)
         return fail(KVQ_EINVAL, "%s: bad sizes", E);
     if ((int64_t)p->n_q * ((p->n_heads + 7) / 8) > 65535) return fail(KVQ_EINVAL, "%s: n_q * n_heads too large", E);
     if (p->impl < 0 || p->impl > 5) return fail(KVQ_EINVAL, "%s: impl must be 0..5", E);
+    if (p->overlap_prior != 0 && p->overlap_prior != 1) return fail(KVQ_EINVAL, "%s: overlap_prior must be 0 or 1", E);
     if (p->idx && p->top_k < 0) return fail(KVQ_EINVAL, "%s: top_k < 0", E);
     if (!p->seq_fmt && p->fmt != KVQ_FMT_FP8 && !kvq::rotated_format(p->fmt))
         return fail(KVQ_EFORMAT, "%s: fmt %d is not FP8, TQ3, TQ4 or TQ6", E, p->fmt);

@@ -449,6 +449,9 @@ __global__ void __launch_bounds__(512) mla_combine_kernel(DecodeArgs a)
     __shared__ float s_w[kBatch];
     __shared__ __align__(16) float s_part[4][kDLat];
     __shared__ float s_red[2][16];
+    // a decode of the next call launched with overlap_prior may start now: it reads its
+    // queries and writes the workspace only after this kernel has completed
+    grid_dependents_launch();
     const kvq_mla_problem& p = a.p;
     const int64_t r = blockIdx.x;                 // (s * n_q + q) * H + h
     const int s = (int)(r / ((int64_t)p.n_q * p.n_heads));

@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
     if (bad_fmt && a.fmt_split) return;          // the other tier's kernel writes these partials
 
     if (r0 >= n_cand || bad_fmt) {
+        grid_dependency_wait();                  // the workspace may still be read before us
         if (bad_fmt && tid == 0 && split == 0 && a.status) atomicOr(a.status, (unsigned)KVQ_DEV_BAD_FORMAT);
         if (tid < nh) {
             const int64_t sl = (qrow + h0 + tid) * a.n_splits + split;
@@ -406,7 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tcf8_kernel(const __gr
     }
     static_assert(kSmx == kGQ, "one softmax warp per head builds the query digits");
     float qv[18];
-    if (warp < kSmx) load_q_head(p, qrow, h0 + warp, lane, qv);
+    if (warp < kSmx) {
+        // with overlap_prior the kernel before this call may still run: the queries, and
+        // every write these warps make to the workspace, come after it has completed (an
+        // immediate return for an ordinary launch)
+        grid_dependency_wait();
+        load_q_head(p, qrow, h0 + warp, lane, qv);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -936,12 +943,21 @@ cudaError_t launch_mla_decode_tcf8(const kvq_mla_problem& p, const DecodePlan& p
         attr_set.fetch_or(bit);
     }
     // an ordinary launch: the first kernel of the call reads the cache and the queries
-    // only after every kernel before it in the stream (an append, say) has completed
+    // only after every kernel before it in the stream (an append, say) has completed;
+    // with overlap_prior (not in a batch split by tier) a programmatic one, which may start
+    // once the kernel before it lets dependents launch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.n_splits, p.n_seq, p.n_q * a.n_hg);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.overlap_prior && !fmt_split) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, mla_decode_tcf8_kernel, a);
 }
 

@@ -471,3 +471,57 @@ def test_decode_host_errors(kvq):
     kvq.kvq_mla_decode(p, out, None, ws)
     torch.cuda.synchronize()
     assert torch.all(out == 0.0)                     # equal (zero) scores: the mean of zeros
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rewrite_q", [False, True])
+def test_decode_overlap_prior_back_to_back(kvq, orc, rewrite_q):
+    """overlap_prior = 1 on the e4m3 kernel: three fp8 problems (distinct caches, one
+    workspace) decoded back to back, five times over, inside a CUDA graph, so that each
+    decode may start during the combine before it.  Every output equals the oracle.  With
+    rewrite_q a device copy writes each call's queries just before the call (a kernel that
+    does not let dependents launch early, so the decode still reads them after it)."""
+    T, H = 16384, 16
+    probs, refs, keep = [], [], []
+    for i in range(3):
+        rows = W.unit_rows(T, seed=70 + i)
+        cache = encode(orc, rows, 1)
+        q = W.queries(1, 1, H, seed=70 + i)
+        dc = {k: dev(v) for k, v in cache.items()}
+        ql, qr = dev(q.q_lat), dev(q.q_rope)
+        ql_dst, qr_dst = (torch.empty_like(ql), torch.empty_like(qr)) if rewrite_q else (ql, qr)
+        p = kvq.make_problem(seq_len=dev(np.array([T], np.int32)), q_lat=ql_dst, q_rope=qr_dst,
+                             sm_scale=W.SM_SCALE, max_seq_len=T, fmt=1, fp8=dc, impl=5,
+                             overlap_prior=1)
+        assert kvq.kvq_mla_decode_kernel(p) == kvq.IMPL_TCF8
+        ref, ref_lse, _ = orc.mla_decode(seq_len=[T], seq_fmt=[1], q_lat=q.q_lat, q_rope=q.q_rope,
+                                         sm_scale=W.SM_SCALE, fp8=cache)
+        probs.append(p)
+        refs.append((ref, ref_lse))
+        keep.append((dc, ql, qr, ql_dst, qr_dst))
+    ws = torch.empty(max(kvq.kvq_mla_decode_workspace(p) for p in probs), dtype=torch.uint8, device="cuda")
+    outs = [torch.full((1, 1, H, 512), np.nan, device="cuda") for _ in probs]
+    lses = [torch.full((1, 1, H), np.nan, device="cuda") for _ in probs]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def calls():
+        for (p, o, l, k) in zip(probs, outs, lses, keep):
+            if rewrite_q:
+                k[3].copy_(k[1])
+                k[4].copy_(k[2])
+            kvq.kvq_mla_decode(p, o, l, ws, st)
+
+    calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(5):
+            calls()
+    for o, l in zip(outs, lses):
+        o.fill_(np.nan)
+        l.fill_(np.nan)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for o, l, (ref, ref_lse) in zip(outs, lses, refs):
+        check(o.cpu().numpy(), l.cpu().numpy(), ref, ref_lse)
