@@ -127,6 +127,20 @@ def _problem(kvq, **kw):
     return p
 
 
+def test_overlap_prior_must_be_0_or_1(kvq):
+    """overlap_prior is a flag: any other value is an argument error of the kernel choice
+    and of the decode call, before anything launches."""
+    L = kvq.lib()
+    for bad in (2, -1):
+        p = _problem(kvq, overlap_prior=bad)
+        assert L.kvq_mla_decode_kernel(C.byref(p)) == -1
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.kvq_mla_decode_kernel(p)
+        assert e.value.status == 1
+        assert L.kvq_mla_decode(C.byref(p), FAKE, None, None, 0, None, None) == 1
+    assert kvq.kvq_mla_decode_kernel(_problem(kvq, overlap_prior=1)) == kvq.IMPL_TC
+
+
 def test_decode_kernel_choice(kvq):
     """Which kernel kvq_mla_decode runs (host only): fp8 with 8 or more heads, no top-k
     list and at least 64 tile-units of work on the e4m3 tcgen05 kernel, other fp8 problems
