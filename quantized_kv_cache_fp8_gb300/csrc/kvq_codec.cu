@@ -282,15 +282,35 @@ __device__ __forceinline__ const float* tq_thresholds()
 //    b = rn(S u' + B), hold at most one threshold and every threshold lies at least 1e-3
 //    from a bucket edge (checked at compile time below), so u and u' share a bucket and
 //    the code is base[b] + (u' >= thr[b]) unless u' is within 1e-5 of thr[b]; then the
-//    IEEE quotient decides against the same threshold.
+//    IEEE quotient decides against the same threshold.  A bucket is one 32-bit word: the
+//    thresholds are midpoints of binary16 values, so the low 6 bits of their fp32
+//    patterns are zero (checked at compile time) and hold base[b]; a bucket without a
+//    threshold holds the largest finite float with those bits cleared.
 //  * 4 bits: two codes a byte; 3 and 6 bits: 24 / b consecutive codes (consecutive lanes)
 //    combine into 3 bytes with a shuffle tree, code i at bits b i of the row's stream.
 // ------------------------------------------------------------------------------------
-struct TqBucket {
-    float thr;                 // the threshold inside the bucket, or +inf
-    int base;                  // thresholds below the bucket
-};
 constexpr float kTqNear = 1e-5f;
+constexpr uint32_t kTqBaseMask = 63u;          // bits of a bucket word that hold base[b]
+constexpr uint32_t kTqNoThreshold = 0x7F7FFFC0u;   // FLT_MAX with the base bits cleared
+
+// the low `nbits` bits of the fp32 pattern of t are zero (t normal or zero)
+constexpr bool tq_low_bits_zero(float t, int nbits)
+{
+    if (t == 0.0f) return true;
+    double v = t < 0.0f ? -(double)t : (double)t;
+    while (v >= 16777216.0) v *= 0.5;          // the significand as an integer in [2^23, 2^24)
+    while (v < 8388608.0) v *= 2.0;
+    return (long long)v % (1LL << nbits) == 0;
+}
+template <int N>
+constexpr bool tq_thresholds_packable(const float (&thr)[N])
+{
+    for (int k = 0; k < N; ++k)
+        if (!tq_low_bits_zero(thr[k], 6)) return false;
+    return N <= (int)kTqBaseMask;
+}
+static_assert(tq_thresholds_packable(kTq3.thr) && tq_thresholds_packable(kTq4Thresholds) &&
+              tq_thresholds_packable(kTq6.thr), "thresholds leave 6 low bits for the bucket base");
 
 template <int BITS> struct Tq512Grid;
 template <> struct Tq512Grid<3> { static constexpr int n = 17;  static constexpr float scale = 4.0f;  static constexpr float off = 8.0f; };
@@ -339,37 +359,36 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
     using G = Tq512Grid<BITS>;
     constexpr int kNThr = (1 << BITS) - 1;
     constexpr int kRowBytes = 64 * BITS;         // 512 codes of BITS bits
-    __shared__ TqBucket s_tab[G::n];
+    __shared__ uint32_t s_tab[G::n];
     __shared__ float s_t[kCodecWarps][544];
     __shared__ __align__(16) uint8_t s_out[kCodecWarps][kRowBytes];
     __shared__ __align__(16) uint8_t s_code[kCodecWarps][512];
     const float* thr_c = tq512_thresholds<BITS>();
-    for (int b = threadIdx.x; b < G::n; b += blockDim.x) {
-        const float lo = ((float)b - G::off - 0.5f) / G::scale;
-        const float hi = ((float)b - G::off + 0.5f) / G::scale;
-        int base = 0;
-        float t = INFINITY;
-        for (int k = 0; k < kNThr; ++k) {
-            base += thr_c[k] < lo;
-            if (thr_c[k] >= lo && thr_c[k] < hi) t = thr_c[k];
-        }
-        s_tab[b] = TqBucket{t, base};
-    }
-    __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    const uint32_t neg16 = (__ldg(sign_bits + (lane >> 1)) >> (16 * (lane & 1))) & 0xFFFFu;
-    const float c = tq4_inv_sqrt(512);
-    const float sgn256 = (lane & 16) ? -1.0f : 1.0f;      // upper half of the h = 256 stage
-    float* st = s_t[wib];
-
-    // each warp walks its rows with the next row's loads in flight during this row's work
+    // each warp walks its rows with the next row's loads in flight during this row's work;
+    // the first row's loads are issued before the bucket table is built
     float4 nx[4];
     if (warp < rows) {
         const float4* src = reinterpret_cast<const float4*>(x + warp * ldx) + 4 * lane;
 #pragma unroll
         for (int q = 0; q < 4; ++q) nx[q] = __ldcs(src + q);
     }
+    for (int b = threadIdx.x; b < G::n; b += blockDim.x) {
+        const float lo = ((float)b - G::off - 0.5f) / G::scale;
+        const float hi = ((float)b - G::off + 0.5f) / G::scale;
+        uint32_t base = 0, t = kTqNoThreshold;
+        for (int k = 0; k < kNThr; ++k) {
+            base += thr_c[k] < lo;
+            if (thr_c[k] >= lo && thr_c[k] < hi) t = __float_as_uint(thr_c[k]);
+        }
+        s_tab[b] = t | base;
+    }
+    __syncthreads();
+    const int wib = threadIdx.x >> 5;
+    const uint32_t neg16 = (__ldg(sign_bits + (lane >> 1)) >> (16 * (lane & 1))) & 0xFFFFu;
+    const float c = tq4_inv_sqrt(512);
+    const float sgn256 = (lane & 16) ? -1.0f : 1.0f;      // upper half of the h = 256 stage
+    float* st = s_t[wib];
     for (int64_t r = warp; r < rows; r += n_warps) {
         float v[16];
 #pragma unroll
@@ -444,7 +463,8 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
         // s_code (element order); elements within reach of their bucket's threshold (bit k
         // of `near`) are decided again by the IEEE quotient, which shares the bucket (its
         // threshold is 1e-3 from the edges), except in a row of tiny sigma, where u' is not
-        // used at all.  y stays in the (now free) transpose buffer for those decisions.
+        // used at all.  For those decisions a warp with such an element puts y in the (now
+        // free) transpose buffer.
         uint8_t* cb = s_code[wib];
         const int eb = (lane >> 4) * 256 + (lane & 15);    // element of register k: eb + 16 k
         uint32_t near = 0;
@@ -452,17 +472,22 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
             const float bf = __fmaf_rn(u1, G::scale, 12582912.0f + G::off);
             return s_tab[min(max(__float_as_int(bf) - 0x4B400000, 0), G::n - 1)];
         };
+        if (rad == 0.0f) {                                 // an all-zero row codes to 0
+            reinterpret_cast<uint4*>(cb)[lane] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            st[rb + 17 * k] = v[k];
-            const float u1 = __fmul_rn(v[k], inv);
-            const TqBucket e = bucket_of(u1);
-            cb[eb + 16 * k] = (uint8_t)(rad == 0.0f ? 0 : e.base + (u1 >= e.thr ? 1 : 0));
-            near |= (fabsf(__fsub_rn(u1, e.thr)) <= kTqNear ? 1u : 0u) << k;
+            for (int k = 0; k < 16; ++k) {
+                const float u1 = __fmul_rn(v[k], inv);
+                const uint32_t e = bucket_of(u1);
+                const float thr = __uint_as_float(e & ~kTqBaseMask);
+                cb[eb + 16 * k] = (uint8_t)((e & kTqBaseMask) + (u1 >= thr ? 1u : 0u));
+                near |= (fabsf(__fsub_rn(u1, thr)) <= kTqNear ? 1u : 0u) << k;
+            }
+            if (exact_row) near = 0xFFFFu;
         }
-        if (exact_row) near = 0xFFFFu;
-        if (rad == 0.0f) near = 0;                          // an all-zero row codes to 0
         if (__any_sync(kFull, near != 0)) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) st[rb + 17 * k] = v[k];
 #pragma unroll 1
             for (int k = 0; k < 16; ++k) {
                 if ((near >> k) & 1u) {
@@ -473,8 +498,8 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
                         c = 0;
                         for (int t = 0; t < kNThr; ++t) c += (u >= thr_c[t]) ? 1 : 0;
                     } else {
-                        const TqBucket e = bucket_of(__fmul_rn(y, inv));
-                        c = e.base + (u >= e.thr ? 1 : 0);
+                        const uint32_t e = bucket_of(__fmul_rn(y, inv));
+                        c = (int)(e & kTqBaseMask) + (u >= __uint_as_float(e & ~kTqBaseMask) ? 1 : 0);
                     }
                     cb[eb + 16 * k] = (uint8_t)c;
                 }
