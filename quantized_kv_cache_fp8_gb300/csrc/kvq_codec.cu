@@ -753,11 +753,12 @@ __device__ __forceinline__ void q4_store_row(float (&z)[8], int lane, uint8_t* s
         }
     }
     const float d = __fmul_rn(mval, -0.125f);          // mval / -8, exact
-    const float idv = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    // 1/d correctly rounded (the reciprocal and the quotient 1/d round the same value)
+    const float idv = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
     uint32_t q[8];
+    // truncation toward zero; the unsigned conversion takes negatives and NaN to 0
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        q[j] = (uint32_t)min(max(__float2int_rz(__fmaf_rn(z[j], idv, 8.5f)), 0), 15);
+    for (int j = 0; j < 8; ++j) q[j] = min(__float2uint_rz(__fmaf_rn(z[j], idv, 8.5f)), 15u);
     // lanes 4b + p (p = 0, 1) hold codes j = 8p .. 8p + 7 of block b, lanes
     // 4b + p + 2 the codes j + 16 that share their bytes (high nibble)
     uint32_t w0 = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
