@@ -362,7 +362,7 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
     __shared__ uint32_t s_tab[G::n];
     __shared__ float s_t[kCodecWarps][544];
     __shared__ __align__(16) uint8_t s_out[kCodecWarps][kRowBytes];
-    __shared__ __align__(16) uint8_t s_code[kCodecWarps][512];
+    __shared__ __align__(16) uint8_t s_code[kCodecWarps][528];
     const float* thr_c = tq512_thresholds<BITS>();
     const int lane = threadIdx.x & 31;
     // each warp walks its rows with the next row's loads in flight during this row's work;
@@ -460,20 +460,22 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
         const float inv = __frcp_rn(sigma);
         const bool exact_row = !(sigma >= 0x1p-120f);      // tiny sigma: divide every element
         // the code from u' = y * rcp(sigma) and the bucket of u', one byte per element into
-        // s_code (element order); elements within reach of their bucket's threshold (bit k
-        // of `near`) are decided again by the IEEE quotient, which shares the bucket (its
-        // threshold is 1e-3 from the edges), except in a row of tiny sigma, where u' is not
-        // used at all.  For those decisions a warp with such an element puts y in the (now
-        // free) transpose buffer.
+        // s_code (element order, elements 256.. 16 bytes further on, so that the two
+        // half-warps' byte stores of a register fall in different banks); elements within
+        // reach of their bucket's threshold (bit k of `near`) are decided again by the IEEE
+        // quotient, which shares the bucket (its threshold is 1e-3 from the edges), except
+        // in a row of tiny sigma, where u' is not used at all.  For those decisions a warp
+        // with such an element puts y in the (now free) transpose buffer.
         uint8_t* cb = s_code[wib];
-        const int eb = (lane >> 4) * 256 + (lane & 15);    // element of register k: eb + 16 k
+        const int eb = (lane >> 4) * 272 + (lane & 15);    // byte of register k: eb + 16 k
+        const int cq = lane + (lane >> 4);                 // 16-byte piece of elements 16 lane ..
         uint32_t near = 0;
         auto bucket_of = [&](float u1) {
             const float bf = __fmaf_rn(u1, G::scale, 12582912.0f + G::off);
             return s_tab[min(max(__float_as_int(bf) - 0x4B400000, 0), G::n - 1)];
         };
         if (rad == 0.0f) {                                 // an all-zero row codes to 0
-            reinterpret_cast<uint4*>(cb)[lane] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(cb)[cq] = make_uint4(0u, 0u, 0u, 0u);
         } else {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -510,7 +512,7 @@ __device__ __forceinline__ void encode_tq512_rows(const float* __restrict__ x, i
         // (little-endian), i.e. BITS * 2 bytes at byte 2 BITS l
         uint8_t* out = s_out[wib];
         {
-            const uint4 c16 = reinterpret_cast<const uint4*>(cb)[lane];
+            const uint4 c16 = reinterpret_cast<const uint4*>(cb)[cq];
             if constexpr (BITS == 4) {
                 const uint32_t t0 = c16.x | (c16.x >> 4), t1 = c16.y | (c16.y >> 4);
                 const uint32_t t2 = c16.z | (c16.z >> 4), t3 = c16.w | (c16.w >> 4);
