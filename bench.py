@@ -486,6 +486,10 @@ def run_codecs(args, local):
     rsc = torch.empty(T, device=dev)
     s = timed(lambda: (kvq.kvq_encode_fp8(x, codes, sc), kvq.kvq_encode_fp8(xr, rcodes, rsc)))
     report("kvq_encode_fp8", f"T={T} rows of 512 + 64 (two launches)", T * (576 * 4 + 576 + 8), s, T, "rows")
+    # the same rows as an MLA append: latent and rope key in one launch (kvq_encode_mla)
+    s = timed(lambda: kvq.kvq_encode_mla(x, xr, kvq.FMT_FP8, None, codes, sc, rcodes, rsc))
+    report("kvq_encode_mla (fp8 + fp8 rope)", f"T={T} rows of 512 + 64 (one launch)",
+           T * (576 * 4 + 576 + 8), s, T, "rows")
     del x, xr, codes, rcodes, sc, rsc
 
     # a2: TQ4 encode of the latent, T = 32768 rows (the 4-bit tier's cache)

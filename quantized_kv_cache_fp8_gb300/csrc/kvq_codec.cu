@@ -577,7 +577,7 @@ encode_mla_kernel(const float* __restrict__ c_lat, int64_t ldx, const float* __r
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     if (blockIdx.y == 1) {
-        encode_fp8_vec_rows<16, 1>(k_rope, rows, ldr, rope, ldc, rope_scale, warp, n_warps);
+        encode_fp8_vec_rows<4, 4>(k_rope, rows, ldr, rope, ldc, rope_scale, warp, n_warps);
     } else {
         if constexpr (BITS == 8)
             encode_fp8_vec_rows<32, 4>(c_lat, rows, ldx, lat, ldl, lat_scale, warp, n_warps);
@@ -1208,7 +1208,7 @@ cudaError_t launch_encode_fp8(const float* x, int64_t rows, int dim, int64_t ldx
                                             kCodecThreads, 0, s>>>(x, rows, ldx, codes, ldc, scales); \
         return cudaGetLastError();                                                         \
     }
-    KVQ_FP8_CASE(64, 16, 1)
+    KVQ_FP8_CASE(64, 4, 4)          // 8 rows a warp (with 2, too few loads were in flight)
     KVQ_FP8_CASE(128, 32, 1)
     KVQ_FP8_CASE(256, 32, 2)
     KVQ_FP8_CASE(512, 32, 4)
